@@ -1,0 +1,141 @@
+"""ctypes wrapper around the C oracle of matmul_backward.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it; the product library never imports it.
+``mmbwd_oracle.c`` states what is computed and which readings of the CPU
+reference it takes.
+
+Builds (gcc, -O2, -ffp-contract=off, no -ffast-math):
+  * ``st``  - single-threaded
+  * ``omp`` - the same source with -fopenmp
+  * ``mutant<k>`` - the same source with one planted mistake (tests only)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mmbwd_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict = {}
+
+F32, BF16, F64 = 0, 1, 2
+DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
+MUTANTS = tuple(range(1, 9))
+
+
+def lib_path(variant: str) -> str:
+    return os.path.join(_BUILD, f"liboracle_{variant}.so")
+
+
+def build(variant: str = "st", force: bool = False) -> str:
+    """Compile one variant of the oracle and return the path of its .so."""
+    out = lib_path(variant)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    flags = ["-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11"]
+    if variant == "omp":
+        flags.append("-fopenmp")
+    elif variant.startswith("mutant"):
+        flags.append(f"-DORACLE_MUTANT={int(variant[6:])}")
+    elif variant != "st":
+        raise ValueError(variant)
+    tmp = out + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", *flags, _SRC, "-o", tmp])
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """One loaded build of the oracle."""
+
+    def __init__(self, variant: str = "st"):
+        self.variant = variant
+        lib = ctypes.CDLL(build(variant))
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.oracle_dinp_rows.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
+        lib.oracle_dweight_rows.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
+        lib.oracle_matmul_backward.argtypes = [vp] * 8 + [i64] * 4 + [ci]
+        for f in (lib.oracle_dinp_rows, lib.oracle_dweight_rows, lib.oracle_matmul_backward,
+                  lib.oracle_threads, lib.oracle_mutant):
+            f.restype = ci
+        self._lib = lib
+
+    @property
+    def threads(self) -> int:
+        return int(self._lib.oracle_threads())
+
+    @staticmethod
+    def _ptr(a):
+        return None if a is None else a.ctypes.data
+
+    @staticmethod
+    def _check(a, dtype_code):
+        if a is None:
+            return
+        want = {F32: np.float32, BF16: np.uint16, F64: np.float64}[dtype_code]
+        assert a.dtype == want and a.flags.c_contiguous, (a.dtype, want)
+
+    def dinp_rows(self, dout, weight, dtype: str, rows=None, dinp_init=None):
+        """Rows ``rows`` (all rows if None) of dinp_init + dout @ weight, in float64."""
+        dt = DTYPES[dtype]
+        BT, OC = dout.shape
+        C = weight.shape[1]
+        for a in (dout, weight, dinp_init):
+            self._check(a, dt)
+        r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = BT if r is None else len(r)
+        out = np.empty((n, C), dtype=np.float64)
+        rc = self._lib.oracle_dinp_rows(out.ctypes.data, self._ptr(r), n, self._ptr(dinp_init),
+                                        dout.ctypes.data, weight.ctypes.data, BT, C, OC, dt)
+        assert rc == 0
+        return out
+
+    def dweight_rows(self, dout, inp, dtype: str, rows=None, dweight_init=None, bias=True):
+        """Rows ``rows`` (all if None) of dweight_init + dout^T @ inp and the matching dbias."""
+        dt = DTYPES[dtype]
+        BT, OC = dout.shape
+        C = inp.shape[1]
+        for a in (dout, inp, dweight_init):
+            self._check(a, dt)
+        r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = OC if r is None else len(r)
+        out = np.empty((n, C), dtype=np.float64)
+        db = np.empty(n, dtype=np.float64) if bias else None
+        rc = self._lib.oracle_dweight_rows(out.ctypes.data, self._ptr(db), self._ptr(r), n,
+                                           self._ptr(dweight_init), dout.ctypes.data,
+                                           inp.ctypes.data, BT, C, OC, dt)
+        assert rc == 0
+        return out, db
+
+    def matmul_backward(self, dout, inp, weight, dtype: str, dinp_init=None, dweight_init=None,
+                        bias=True):
+        """Full (dinp, dweight, dbias-or-None) in float64; shapes as 2-D (BT, .) arrays."""
+        dt = DTYPES[dtype]
+        BT, OC = dout.shape
+        C = inp.shape[1]
+        for a in (dout, inp, weight, dinp_init, dweight_init):
+            self._check(a, dt)
+        dinp = np.empty((BT, C), dtype=np.float64)
+        dweight = np.empty((OC, C), dtype=np.float64)
+        dbias = np.empty(OC, dtype=np.float64) if bias else None
+        rc = self._lib.oracle_matmul_backward(
+            dinp.ctypes.data, dweight.ctypes.data, self._ptr(dbias), dout.ctypes.data,
+            inp.ctypes.data, weight.ctypes.data, self._ptr(dinp_init), self._ptr(dweight_init),
+            1, BT, C, OC, dt)
+        assert rc == 0
+        return dinp, dweight, dbias
+
+
+def get(variant: str = "st") -> Oracle:
+    with _lock:
+        if variant not in _libs:
+            _libs[variant] = Oracle(variant)
+        return _libs[variant]
