@@ -1,0 +1,146 @@
+/*
+ * mmbwd.h -- C ABI of the GB300 (sm_103a) linear-layer backward library.
+ *
+ * The operation is the backward pass of a GPT-2 linear layer, as computed by
+ * `matmul_backward_cpu` and launched by `matmul_backward1` in llm.c's
+ * dev/cuda/matmul_backward.cu. With BT = B*T and every tensor row-major and
+ * contiguous,
+ *
+ *     dout (B,T,OC)   inp (B,T,C)   weight (OC,C)
+ *     dinp    (B,T,C) += dout . weight          (the "backward into inp" loop;
+ *                                                 cuBLAS beta = 1 there: "gradients add")
+ *     dweight (OC,C)  += dout^T . inp           (the "backward into weight" loop,
+ *                                                 contracting over BT)
+ *     dbias   (OC)     = sum over (b,t) of dout (the bias sum: `dbias[o] = sum`,
+ *                                                 an overwrite, skipped when dbias is NULL)
+ *
+ * Element types (one type for all six tensors, like the pages' floatX switch):
+ *   MMBWD_BF16: bf16 storage, products accumulated in fp32, each output element
+ *               rounded once to bf16 (round-to-nearest-even) after the old value
+ *               (converted to fp32) and the fp32 sum are added.
+ *   MMBWD_F32:  fp32 storage, fp32 fused multiply-add accumulation.
+ *
+ * Every entry point is plain C: device pointers, sizes, a CUDA stream.
+ * Nothing here takes or returns a framework type.
+ */
+#ifndef MMBWD_H
+#define MMBWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+#define MMBWD_F32 0
+#define MMBWD_BF16 1
+
+/* Status codes. MMBWD_OK is 0; every error is negative. */
+#define MMBWD_OK 0
+#define MMBWD_ERR_NULL (-1)           /* a required pointer is NULL */
+#define MMBWD_ERR_DTYPE (-2)          /* dtype is neither MMBWD_F32 nor MMBWD_BF16 */
+#define MMBWD_ERR_SHAPE (-3)          /* a size is negative, or a product overflows */
+#define MMBWD_ERR_ALIGN (-4)          /* a pointer is not 16-byte aligned, or C or OC
+                                         times the element size is not a multiple of 16 */
+#define MMBWD_ERR_ALIAS (-5)          /* an output overlaps an input or another output */
+#define MMBWD_ERR_ALLOC (-6)          /* the library could not allocate its workspace */
+#define MMBWD_ERR_CUDA (-7)           /* a CUDA runtime call or a launch failed */
+#define MMBWD_ERR_DEVICE_TIMEOUT (-8) /* a kernel gave up a bounded wait (device status) */
+#define MMBWD_ERR_ARCH (-9)           /* the current device is not sm_103 */
+#define MMBWD_ERR_CAPTURE (-10)       /* the workspace would have to grow while the
+                                         stream is being captured into a CUDA graph */
+
+/*
+ * mmbwd_run -- enqueue the whole backward pass of one linear layer on `stream`.
+ *
+ *   dinp           device, (B*T, C), read and written (+=)
+ *   dweight        device, (OC, C),  read and written (+=)
+ *   dbias_or_null  device, (OC),     written (=); NULL skips the bias sum and
+ *                  nothing else changes
+ *   dout           device, (B*T, OC), read only
+ *   inp            device, (B*T, C),  read only
+ *   weight         device, (OC, C),   read only
+ *   B, T, C, OC    sizes, each >= 0
+ *   dtype          MMBWD_F32 or MMBWD_BF16 (the type of all six tensors)
+ *   stream         the CUDA stream to enqueue on (0 = legacy default stream)
+ *
+ * Argument order follows matmul_backward_cpu (dinp, dweight, dbias, dout, inp,
+ * weight, B, T, C, OC); the all-ones vector that matmul_backward1 takes is not
+ * needed. Layout: row-major, contiguous, no strides.
+ *
+ * Ownership: the caller owns every buffer; the library never frees them.
+ * Outputs must not overlap inputs or each other (MMBWD_ERR_ALIAS); inputs may
+ * overlap each other. Pointers must be 16-byte aligned, and C and OC times the
+ * element size must be multiples of 16 bytes (MMBWD_ERR_ALIGN). A pointer may
+ * be NULL only when its tensor has no elements.
+ *
+ * Workspace: the bf16 path may need a library-owned fp32 workspace for its
+ * split reduction (mmbwd_workspace_bytes). It is allocated per device on
+ * first need and reused; growing it synchronises the device, so the first
+ * call of a new, larger shape should not be made during stream capture
+ * (MMBWD_ERR_CAPTURE). Calls that share a device share this workspace:
+ * calls on different streams of one device must not overlap in time.
+ *
+ * Synchronisation: asynchronous. The call validates, enqueues and returns; the
+ * caller synchronises the stream before reading results. Invalid arguments
+ * enqueue nothing and return a negative code. A kernel that gives up a bounded
+ * wait records MMBWD_ERR_DEVICE_TIMEOUT in the device status word, read by
+ * mmbwd_device_status(); nothing in the library calls exit() or traps.
+ *
+ * Degenerate sizes: B*T == 0 sets dbias to 0 (the empty sum) and leaves dinp
+ * and dweight untouched; OC == 0 changes nothing; C == 0 still computes dbias.
+ *
+ * Determinism: for a given shape the work split is a pure function of the
+ * shape, every reduction runs in a fixed order and no float atomics are used,
+ * so repeated calls on identical inputs give bitwise identical results.
+ */
+int mmbwd_run(void* dinp, void* dweight, void* dbias_or_null, const void* dout, const void* inp,
+              const void* weight, int64_t B, int64_t T, int64_t C, int64_t OC, int dtype,
+              cudaStream_t stream);
+
+/* Bytes of workspace mmbwd_run needs for this shape on the current device
+ * (0 when it needs none, and for invalid arguments). The work split depends
+ * on the device's SM count, which this queries (152, a full GB300, when no
+ * usable device is present). Enqueues nothing. */
+size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype);
+
+/* Free the current device's workspace (synchronises the device). Returns a status. */
+int mmbwd_release(void);
+
+/* Static description of a status code. Never NULL. */
+const char* mmbwd_strerror(int code);
+
+/* Read the current device's status word, written by kernels that gave up a
+ * bounded wait: MMBWD_OK or MMBWD_ERR_DEVICE_TIMEOUT. Synchronises the device.
+ * reset != 0 clears the word after reading. `info` (may be NULL) receives 3
+ * integers: the block, the wait site and the work item of the first failure. */
+int mmbwd_device_status(int reset, int* info);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int mmbwd_version(void);
+
+/* Describe the work split mmbwd_run would use (a pure function of the shape
+ * and the SM count). out[0..n) receives, in order: path (0 = fp32 SIMT,
+ * 1 = bf16 tensor-core), grid size, work items, dweight splits, k-blocks per
+ * split, dinp tiles, dweight tiles, schedule order, tile M, tile N, tile K,
+ * pipeline stages. Returns the number of values written, or a negative status. */
+int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms,
+                    int* out, int n);
+
+/* Self-test of the bounded-wait machinery: launches one tiny kernel whose
+ * thread waits on a barrier that nothing completes, giving up after
+ * `timeout_ns`. Synchronises, reads and clears the status word, and returns
+ * what the kernel recorded (MMBWD_ERR_DEVICE_TIMEOUT when the mechanism works). */
+int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
+
+/* Test hook: make the next `n` workspace allocations fail (MMBWD_ERR_ALLOC). */
+void mmbwd_debug_fail_next_alloc(int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMBWD_H */

@@ -1,0 +1,162 @@
+"""GB300 (sm_103a) backward pass of a GPT-2 linear layer.
+
+Thin Python binding of the C-ABI library ``libmmbwd.so`` (declared in
+``include/mmbwd.h``): the same entry points, arguments marshalled through
+ctypes, nothing computed here. Every step of the backward pass runs in the
+library's CUDA kernels; if the library is not built this module raises on
+first use instead of falling back to anything else.
+
+    dinp    (B,T,C)  += dout . weight
+    dweight (OC,C)   += dout^T . inp
+    dbias   (OC)      = sum over (b,t) of dout        (NULL / None skips it)
+
+Pointers may be given as integers or as objects with ``data_ptr()`` (for
+example torch tensors on the current CUDA device); ``stream`` is a raw
+``cudaStream_t`` integer, or None for the current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F32 = 0
+BF16 = 1
+
+OK = 0
+ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_ALIAS = -1, -2, -3, -4, -5
+ERR_ALLOC, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_ARCH, ERR_CAPTURE = -6, -7, -8, -9, -10
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmmbwd.so")
+
+# Names and C signatures of every entry point declared in include/mmbwd.h.
+_vp, _i64, _ci, _u64, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                             ctypes.c_size_t)
+SIGNATURES = {
+    "mmbwd_run": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
+    "mmbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
+    "mmbwd_release": ([], _ci),
+    "mmbwd_strerror": ([_ci], ctypes.c_char_p),
+    "mmbwd_device_status": ([_ci, ctypes.POINTER(_ci)], _ci),
+    "mmbwd_version": ([], _ci),
+    "mmbwd_plan_info": ([_i64] * 4 + [_ci, _ci, ctypes.POINTER(_ci), _ci], _ci),
+    "mmbwd_selftest_wait_timeout": ([_u64], _ci),
+    "mmbwd_debug_fail_next_alloc": ([_ci], None),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MmbwdError(RuntimeError):
+    def __init__(self, code: int, what: str = "mmbwd"):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+def load(path: str | None = None):
+    """Load libmmbwd.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libmmbwd.so is not built ({p}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is not None:
+        return int(stream)
+    import torch  # only for the current stream handle
+
+    return torch.cuda.current_stream().cuda_stream
+
+
+def mmbwd_run(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, OC: int, dtype: int,
+              stream=None) -> int:
+    """Enqueue one backward pass; returns the C status code (0 = OK)."""
+    return load().mmbwd_run(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp),
+                            _ptr(weight), B, T, C, OC, dtype, _stream(stream))
+
+
+def mmbwd_workspace_bytes(B: int, T: int, C: int, OC: int, dtype: int) -> int:
+    return int(load().mmbwd_workspace_bytes(B, T, C, OC, dtype))
+
+
+def mmbwd_release() -> int:
+    return load().mmbwd_release()
+
+
+def strerror(code: int) -> str:
+    return load().mmbwd_strerror(code).decode()
+
+
+def mmbwd_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def mmbwd_device_status(reset: bool = True):
+    """(status, [block, wait site, item]) of the device status word."""
+    info = (ctypes.c_int * 3)()
+    code = load().mmbwd_device_status(1 if reset else 0, info)
+    return code, list(info)
+
+
+def mmbwd_version() -> int:
+    return load().mmbwd_version()
+
+
+PLAN_FIELDS = ("path", "grid", "items", "splits", "kb_per_split", "dinp_tiles", "dweight_tiles",
+               "order", "tile_m", "tile_n", "tile_k", "stages")
+
+
+def mmbwd_plan_info(B: int, T: int, C: int, OC: int, dtype: int, num_sms: int = 0) -> dict:
+    out = (ctypes.c_int * len(PLAN_FIELDS))()
+    n = load().mmbwd_plan_info(B, T, C, OC, dtype, num_sms, out, len(PLAN_FIELDS))
+    if n < 0:
+        raise MmbwdError(n, "mmbwd_plan_info")
+    return dict(zip(PLAN_FIELDS, list(out)[:n]))
+
+
+def mmbwd_selftest_wait_timeout(timeout_ns: int) -> int:
+    return load().mmbwd_selftest_wait_timeout(timeout_ns)
+
+
+def mmbwd_debug_fail_next_alloc(n: int) -> None:
+    load().mmbwd_debug_fail_next_alloc(n)
+
+
+def matmul_backward(dinp, dweight, dbias, dout, inp, weight, stream=None) -> None:
+    """Convenience wrapper for torch tensors: shapes from the tensors, dtype
+    from their element type (float32 or bfloat16); raises MmbwdError on a
+    non-zero status."""
+    import torch
+
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(dout.dtype)
+    if dt is None:
+        raise MmbwdError(ERR_DTYPE, "matmul_backward")
+    if dout.dim() == 3:
+        B, T, OC = dout.shape
+    else:
+        (BT, OC), B = dout.shape, 1
+        T = BT
+    C = inp.shape[-1]
+    rc = mmbwd_run(dinp, dweight, dbias, dout, inp, weight, B, T, C, OC, dt, stream)
+    if rc != OK:
+        raise MmbwdError(rc, "mmbwd_run")

@@ -1,0 +1,298 @@
+// C ABI of the matmul_backward library: argument checks, the shape-only plan,
+// the per-device workspace and the launches. See include/mmbwd.h for the
+// contract of every entry point.
+#include "../../include/mmbwd.h"
+#include "internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+namespace mmbwd {
+
+EncodeTiledFn get_encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    int arch_checked = 0;  // 0 unknown, 1 ok, -1 not sm_103
+    int num_sms = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_fail_allocs{0};
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// a * b without overflow beyond 2^62; returns false on overflow.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > (int64_t(1) << 62) / a) return false;
+    *out = a * b;
+    return true;
+}
+
+struct Shape {
+    int64_t BT = 0, n_dinp = 0, n_dw = 0, n_dout = 0;
+    size_t es = 0;
+};
+
+int check_shape(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, Shape* s) {
+    if (dtype != MMBWD_F32 && dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    if (B < 0 || T < 0 || C < 0 || OC < 0) return MMBWD_ERR_SHAPE;
+    if (!mul_ok(B, T, &s->BT) || !mul_ok(s->BT, C, &s->n_dinp) || !mul_ok(OC, C, &s->n_dw) ||
+        !mul_ok(s->BT, OC, &s->n_dout))
+        return MMBWD_ERR_SHAPE;
+    s->es = dtype == MMBWD_F32 ? 4 : 2;
+    // Limits of the launch geometry and the tensor maps (dims < 2^31, tile counts in int).
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (s->BT > lim || C > lim || OC > lim) return MMBWD_ERR_SHAPE;
+    if ((s->BT + 127) / 128 * ((C + 255) / 256) > lim / 32) return MMBWD_ERR_SHAPE;
+    if ((OC + 127) / 128 * ((C + 255) / 256) > lim / 32) return MMBWD_ERR_SHAPE;
+    if ((C + 127) / 128 > 65535) return MMBWD_ERR_SHAPE;  // fp32 path grid.y
+    int64_t bytes = 0;
+    if (!mul_ok(s->n_dout, static_cast<int64_t>(s->es), &bytes) ||
+        !mul_ok(s->n_dinp, static_cast<int64_t>(s->es), &bytes) ||
+        !mul_ok(s->n_dw, static_cast<int64_t>(s->es), &bytes))
+        return MMBWD_ERR_SHAPE;
+    return MMBWD_OK;
+}
+
+int device_state(DeviceState** out, int* dev_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MMBWD_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    if (d.arch_checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MMBWD_ERR_CUDA;
+        d.arch_checked = (major == 10 && minor == 3) ? 1 : -1;
+        d.num_sms = sms;
+    }
+    if (d.arch_checked != 1) return MMBWD_ERR_ARCH;
+    *out = &d;
+    *dev_out = dev;
+    return MMBWD_OK;
+}
+
+// Grow the device's workspace to `need` bytes (counters start at zero).
+int ensure_workspace(DeviceState& d, size_t need, cudaStream_t stream) {
+    if (need <= d.ws_bytes) return MMBWD_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MMBWD_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return MMBWD_ERR_CAPTURE;
+    if (g_fail_allocs.load() > 0) {
+        g_fail_allocs.fetch_sub(1);
+        return MMBWD_ERR_ALLOC;
+    }
+    if (d.ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return MMBWD_ERR_CUDA;
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+        cudaGetLastError();
+        return MMBWD_ERR_ALLOC;
+    }
+    if (cudaMemset(p, 0, need) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(p);
+        return MMBWD_ERR_CUDA;
+    }
+    d.ws = p;
+    d.ws_bytes = need;
+    return MMBWD_OK;
+}
+
+}  // namespace
+}  // namespace mmbwd
+
+using namespace mmbwd;
+
+extern "C" {
+
+int mmbwd_version(void) { return 10000; }
+
+const char* mmbwd_strerror(int code) {
+    switch (code) {
+        case MMBWD_OK: return "ok";
+        case MMBWD_ERR_NULL: return "a required pointer is NULL";
+        case MMBWD_ERR_DTYPE: return "dtype must be MMBWD_F32 or MMBWD_BF16";
+        case MMBWD_ERR_SHAPE: return "a size is negative, too large, or a product overflows";
+        case MMBWD_ERR_ALIGN: return "pointers must be 16-byte aligned and C, OC times the element size multiples of 16 bytes";
+        case MMBWD_ERR_ALIAS: return "an output overlaps an input or another output";
+        case MMBWD_ERR_ALLOC: return "workspace allocation failed";
+        case MMBWD_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case MMBWD_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+        case MMBWD_ERR_ARCH: return "the current device is not sm_103 (GB300)";
+        case MMBWD_ERR_CAPTURE: return "the workspace must grow but the stream is being captured";
+        default: return "unknown status code";
+    }
+}
+
+size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype) {
+    Shape s;
+    if (check_shape(B, T, C, OC, dtype, &s) != MMBWD_OK) return 0;
+    if (dtype != MMBWD_BF16 || s.BT == 0 || C == 0 || OC == 0) return 0;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> g(g_mutex);
+        DeviceState* d = nullptr;
+        int dev = 0;
+        if (device_state(&d, &dev) == MMBWD_OK) sms = d->num_sms;
+    }
+    if (sms <= 0) sms = 152;  // no usable device: size for a full GB300
+    return tc_make_plan(s.BT, C, OC, sms).ws_bytes();
+}
+
+int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms, int* out, int n) {
+    Shape s;
+    const int rc = check_shape(B, T, C, OC, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+    if (!out || n < 0) return MMBWD_ERR_NULL;
+    int v[12] = {0};
+    if (dtype == MMBWD_BF16) {
+        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms > 0 ? num_sms : 152);
+        const int vals[12] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
+                              pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.dw_first * 2 + pl.snake,
+                              TC_BM, TC_BN, TC_BK, TC_STAGES};
+        for (int i = 0; i < 12; ++i) v[i] = vals[i];
+    } else {
+        const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
+        const int go = static_cast<int>((OC + SIMT_BM - 1) / SIMT_BM);
+        const int vals[12] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BK, 2};
+        for (int i = 0; i < 12; ++i) v[i] = vals[i];
+    }
+    const int m = n < 12 ? n : 12;
+    for (int i = 0; i < m; ++i) out[i] = v[i];
+    return m;
+}
+
+int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+              int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream) {
+    Shape s;
+    int rc = check_shape(B, T, C, OC, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = s.es;
+    const size_t b_dinp = static_cast<size_t>(s.n_dinp) * es, b_dw = static_cast<size_t>(s.n_dw) * es,
+                 b_db = static_cast<size_t>(OC) * es, b_dout = static_cast<size_t>(s.n_dout) * es,
+                 b_inp = static_cast<size_t>(s.n_dinp) * es, b_w = static_cast<size_t>(s.n_dw) * es;
+
+    // NULL only where the tensor is empty (dbias NULL means "skip the bias").
+    if ((b_dinp && !dinp) || (b_dw && !dweight) || (b_dout && !dout) || (b_inp && !inp) || (b_w && !weight))
+        return MMBWD_ERR_NULL;
+    const void* ptrs[6] = {dinp, dweight, dbias, dout, inp, weight};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0 || (static_cast<size_t>(OC) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+
+    // Outputs overlap neither inputs nor each other.
+    const void* outs[3] = {dinp, dweight, dbias};
+    const size_t nouts[3] = {b_dinp, b_dw, b_db};
+    const void* ins[3] = {dout, inp, weight};
+    const size_t nins[3] = {b_dout, b_inp, b_w};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return MMBWD_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return MMBWD_ERR_ALIAS;
+    }
+
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+
+    cudaError_t e = cudaSuccess;
+    if (OC == 0) return MMBWD_OK;  // empty sums everywhere; dbias has no elements
+    if (s.BT == 0) {
+        if (dbias) e = cudaMemsetAsync(dbias, 0, b_db, stream);  // the empty sum
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    if (C == 0) {
+        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+
+    if (dtype == MMBWD_F32) {
+        e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                        static_cast<const float*>(dout), static_cast<const float*>(inp),
+                        static_cast<const float*>(weight), s.BT, C, OC, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+
+    const TcPlan plan = tc_make_plan(s.BT, C, OC, d->num_sms);
+    rc = ensure_workspace(*d, plan.ws_bytes(), stream);
+    if (rc != MMBWD_OK) return rc;
+    e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+int mmbwd_release(void) {
+    std::lock_guard<std::mutex> g(g_mutex);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MMBWD_ERR_CUDA;
+    DeviceState& d = g_dev[dev];
+    if (d.ws) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return MMBWD_ERR_CUDA;
+        if (cudaFree(d.ws) != cudaSuccess) return MMBWD_ERR_CUDA;
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+    }
+    return MMBWD_OK;
+}
+
+int mmbwd_device_status(int reset, int* info) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MMBWD_ERR_CUDA;
+    int code = MMBWD_OK;
+    if (tc_read_status(&code, info, reset != 0) != cudaSuccess) return MMBWD_ERR_CUDA;
+    return code;
+}
+
+int mmbwd_selftest_wait_timeout(uint64_t timeout_ns) {
+    {
+        std::lock_guard<std::mutex> g(g_mutex);
+        DeviceState* d = nullptr;
+        int dev = 0;
+        const int rc = device_state(&d, &dev);
+        if (rc != MMBWD_OK) return rc;
+    }
+    if (tc_selftest_wait(timeout_ns) != cudaSuccess) return MMBWD_ERR_CUDA;
+    int code = MMBWD_OK;
+    if (tc_read_status(&code, nullptr, true) != cudaSuccess) return MMBWD_ERR_CUDA;
+    return code;
+}
+
+void mmbwd_debug_fail_next_alloc(int n) { g_fail_allocs.store(n < 0 ? 0 : n); }
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// Internal declarations shared by the C-ABI layer and the kernel translation
+// units. Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mmbwd {
+
+// ------------------------------------------------------------ bf16 tensor-core path
+// Tile shape of the persistent tcgen05 kernel: one CTA computes a 128 x 256
+// fp32 accumulator in tensor memory, 64 elements of K per pipeline stage.
+constexpr int TC_BM = 128;
+constexpr int TC_BN = 256;
+constexpr int TC_BK = 64;
+constexpr int TC_STAGES = 4;
+constexpr int TC_THREADS = 256;
+
+// Wait sites reported in the device status word.
+enum WaitSite : int {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_TMEM_EMPTY = 2,
+    SITE_MMA_FULL = 3,
+    SITE_EPI_TMEM_FULL = 4,
+    SITE_EPI_BIAS_FULL = 5,
+    SITE_BIAS_TMEM_EMPTY = 6,
+    SITE_BIAS_FULL = 7,
+    SITE_TEARDOWN = 8,
+    SITE_SELFTEST = 9,
+};
+
+// Work list of one call: the dweight (TN) items -- dweight tiles times the
+// K splits -- and the dinp (NN) tiles. `dw_first` says which group comes
+// first in the item order; `snake` reverses the CTA order on odd rounds.
+struct TcPlan {
+    int tiles_n;       // ceil(C / BN), shared by both products (N = C for both)
+    int dinp_tiles_m;  // ceil(BT / BM)
+    int dw_tiles_m;    // ceil(OC / BM)
+    int dinp_kb;       // ceil(OC / BK)
+    int dw_kb;         // ceil(BT / BK)
+    int splits;        // K splits of the dweight product
+    int kb_per_split;  // k-blocks per split (the last may have fewer)
+    int n_dw_items;    // dw_tiles_m * tiles_n * splits
+    int n_dinp_items;  // dinp_tiles_m * tiles_n
+    int n_items;
+    int dw_first;
+    int snake;
+    int grid;
+    size_t ws_partials_bytes;  // fp32 partial tiles (splits > 1 only)
+    size_t ws_bias_bytes;      // fp32 partial bias sums
+    size_t ws_counter_bytes;   // arrival counters, one per dweight tile
+    size_t ws_bytes() const { return ws_partials_bytes + ws_bias_bytes + ws_counter_bytes; }
+};
+
+struct TcParams {
+    int64_t BT, C, OC;
+    __nv_bfloat16* dinp;
+    __nv_bfloat16* dweight;
+    __nv_bfloat16* dbias;  // may be null
+    int tiles_n, dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
+    int n_dw_items, n_dinp_items, n_items, dw_first, snake;
+    float* partials;       // [dw tile][split][BN/4][BM][4]
+    float* bias_partials;  // [dw_tiles_m][split][BM]
+    int* counters;         // [dw tile]
+    unsigned long long timeout_ns;
+};
+
+// Plans (pure functions of the shape and SM count). Overrides for tuning and
+// tests come from the environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs).
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms);
+
+// Launch the tensor-core kernel. `ws` must hold plan.ws_bytes() bytes whose
+// counter region is zero. Returns a cudaError_t.
+cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
+                      const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC,
+                      void* ws, cudaStream_t stream);
+
+size_t tc_smem_bytes();
+
+// Device status word of the tensor-core translation unit.
+cudaError_t tc_read_status(int* code, int* info3, bool reset);
+cudaError_t tc_selftest_wait(unsigned long long timeout_ns);
+
+// ------------------------------------------------------------ fp32 SIMT path
+constexpr int SIMT_BM = 128;
+constexpr int SIMT_BN = 128;
+constexpr int SIMT_BK = 8;
+constexpr int SIMT_THREADS = 256;
+
+cudaError_t simt_launch(float* dinp, float* dweight, float* dbias, const float* dout,
+                        const float* inp, const float* weight, int64_t BT, int64_t C, int64_t OC,
+                        cudaStream_t stream);
+
+// dbias = column sums of dout (used when C == 0, where no GEMM tile exists).
+cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype,
+                          cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding (resolved through the runtime).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace mmbwd

@@ -1,0 +1,133 @@
+"""The C-ABI library on the host: it loads, exports every entry point the
+header declares, and rejects bad arguments before any CUDA call."""
+import os
+import re
+
+import pytest
+
+import linear_layer_gemms_gb300 as mm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from linear_layer_gemms_gb300 import _build
+
+    _build.build()
+    mm.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mmbwd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mmbwd_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    names = declared_functions()
+    assert "mmbwd_run" in names and len(names) >= 9
+    lib = mm.load()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in mm.SIGNATURES, n
+    assert set(mm.SIGNATURES) == set(names)
+
+
+def test_version_and_strerror():
+    assert mm.mmbwd_version() >= 10000
+    msgs = {c: mm.strerror(c) for c in range(-10, 1)}
+    assert len(set(msgs.values())) == len(msgs)
+    assert "unknown" in mm.strerror(-99)
+
+
+A = 1 << 20  # fake, 16-byte aligned addresses: validation fails before any use
+
+
+def run(**kw):
+    args = dict(dinp=A, dweight=2 * A, dbias=3 * A, dout=4 * A, inp=5 * A, weight=6 * A,
+                B=2, T=8, C=64, OC=32, dtype=mm.BF16, stream=0)
+    args.update(kw)
+    return mm.mmbwd_run(**args)
+
+
+def test_rejects_bad_dtype_and_shapes():
+    assert run(dtype=7) == mm.ERR_DTYPE
+    assert run(B=-1) == mm.ERR_SHAPE
+    assert run(OC=-8) == mm.ERR_SHAPE
+    assert run(B=1 << 40, T=1 << 40) == mm.ERR_SHAPE
+    assert run(T=1 << 31) == mm.ERR_SHAPE
+
+
+def test_rejects_null_misaligned_and_aliased():
+    assert run(dout=None) == mm.ERR_NULL
+    assert run(dinp=None) == mm.ERR_NULL
+    assert run(weight=None) == mm.ERR_NULL
+    assert run(inp=A * 5 + 8) == mm.ERR_ALIGN
+    assert run(dbias=A * 3 + 2) == mm.ERR_ALIGN
+    assert run(C=60) == mm.ERR_ALIGN          # 60 bf16 = 120 bytes, not a multiple of 16
+    assert run(OC=36, dtype=mm.BF16) == mm.ERR_ALIGN
+    assert run(dinp=4 * A + 64) == mm.ERR_ALIAS    # dinp inside dout
+    assert run(dbias=2 * A + 16) == mm.ERR_ALIAS   # dbias inside dweight
+    assert run(dweight=A + 32) == mm.ERR_ALIAS     # dweight overlaps dinp
+
+
+def test_empty_tensors_may_be_null():
+    # With B*T == 0 the activations are empty and may be NULL; with no dbias
+    # either, the call does no device work at all (safe with fake addresses).
+    rc = run(B=0, dinp=None, dout=None, inp=None, dbias=None)
+    assert rc in (mm.OK, mm.ERR_CUDA, mm.ERR_ARCH)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_arguments_without_a_gpu_fail_cleanly():
+    assert run() in (mm.ERR_CUDA, mm.ERR_ARCH)
+    assert mm.mmbwd_device_status()[0] == mm.ERR_CUDA
+
+
+def test_plan_is_a_pure_function_of_shape():
+    for (B, T, C, OC) in [(8, 1024, 768, 3072), (8, 1024, 3072, 768), (8, 1024, 768, 768),
+                          (8, 1024, 768, 50304), (4, 1024, 1600, 6400), (1, 5, 8, 16)]:
+        a = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        b = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        assert a == b
+        BT = B * T
+        tiles_n = -(-C // 256)
+        assert a["path"] == 1 and 1 <= a["grid"] <= 152
+        assert a["dinp_tiles"] == -(-BT // 128) * tiles_n
+        assert a["dweight_tiles"] == -(-OC // 128) * tiles_n
+        assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"] * a["splits"]
+        kb = -(-BT // 64)
+        # every split is non-empty and together they cover the reduction
+        assert (a["splits"] - 1) * a["kb_per_split"] < kb <= a["splits"] * a["kb_per_split"]
+        ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
+        assert (ws > 0) == (a["splits"] > 1)
+    f = mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32, 152)
+    assert f["path"] == 0
+
+
+def test_split_override_from_environment(monkeypatch):
+    monkeypatch.setenv("MMBWD_SPLITK", "3")
+    monkeypatch.setenv("MMBWD_GRID", "5")
+    a = mm.mmbwd_plan_info(1, 1000, 264, 392, mm.BF16, 152)
+    assert a["splits"] == 3 and a["grid"] == 5
+    monkeypatch.delenv("MMBWD_SPLITK")
+    monkeypatch.delenv("MMBWD_GRID")
+
+
+def test_workspace_size_formula():
+    import os as _os
+    _os.environ["MMBWD_SPLITK"] = "2"
+    try:
+        B, T, C, OC = 1, 1000, 264, 392
+        info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
+        tiles = info["dweight_tiles"]
+        align = lambda x: (x + 255) // 256 * 256  # noqa: E731
+        want = (align(tiles * 2 * 128 * 256 * 4) + align(-(-OC // 128) * 2 * 128 * 4) +
+                align(tiles * 4))
+        assert ws == want
+    finally:
+        del _os.environ["MMBWD_SPLITK"]
+    assert mm.mmbwd_workspace_bytes(1, 8, 64, 64, mm.F32) == 0
+    assert mm.mmbwd_workspace_bytes(-1, 8, 64, 64, mm.BF16) == 0
