@@ -1,0 +1,481 @@
+"""Benchmark of the GPT-2 small MLP backward (fc then fc_proj) on GB300.
+
+One step = the backward pass of both MLP linear layers of one GPT-2 small
+block, B=8, T=1024, bf16 storage, fp32 accumulation, with bias:
+    fc      C=768  -> OC=3072
+    fc_proj C=3072 -> OC=768
+each one call of mmbwd_run (dinp += dout.W, dweight += dout^T.inp, dbias).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0). The metric is TFLOP/s with
+FLOPs = 4*B*T*C*OC + B*T*OC (the bias sum) per layer.
+
+* value: device-resident inputs, CUDA events on the launching stream around
+  exactly K steps (barrier + synchronize on both sides), three rotating input
+  sets (~620 MB) so no step starts with its inputs in the 129 MB L2.
+* e2e: the same steps through the same C-ABI call, with pinned HOST inputs:
+  every step copies dout, inp, weight host->device and reads dinp, dweight,
+  dbias back, copies inside the timed region.
+* roofline: the tensor-core kernel's FLOPs per launch / its mean launch time
+  (events around each launch), against the measured bf16 peak.
+* cpu_baseline / --impl reference: the C oracle (OpenMP build, all host
+  cores) on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "mlp"
+METRIC = "matmul_backward TFLOP/s at GPT-2 shapes; % of GB300 dense bf16 peak"
+UNIT = "TFLOP/s"
+N_SETS = 3
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+def config_dict():
+    wl = synth.WORKLOADS[WORKLOAD]
+    l0 = wl.layers[0]
+    set_bytes = sum(layer_bytes(l) for l in wl.layers)
+    return {
+        "workload": "gpt2_small_mlp_backward",
+        "B": l0.B, "T": l0.T,
+        "layers": [{"name": l.name, "C": l.C, "OC": l.OC, "bias": l.bias} for l in wl.layers],
+        "dtype_storage": "bf16", "accumulate": "fp32",
+        "flops_per_step": wl.flops(),
+        "l2": f"{N_SETS} rotating input sets of {set_bytes / 1e6:.0f} MB each (> 129 MB L2)",
+        "parallelism": "replicas",
+    }
+
+
+def layer_bytes(l):
+    es = l.elem_bytes()
+    return es * (l.BT * l.OC + 2 * l.BT * l.C + 2 * l.OC * l.C + l.OC)
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(units: float, seconds: float, group=None):
+    """Whole-job throughput over replicas: units summed over ranks, divided by
+    the slowest rank's time. Works for any torch.distributed backend."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized():
+        return units, seconds
+    t = torch.tensor([units, seconds], dtype=torch.float64)
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = t.to(dev)
+    u = t[0:1].clone()
+    s = t[1:2].clone()
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(u.item()), float(s.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        load = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(load),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        u = torch.cuda.get_device_properties(dev_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+# ----------------------------------------------------------------------------- peaks / profile
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha1()
+    for f in ("tc_gemm.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "linear_layer_gemms_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the tensor-core kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "tc_mmbwd_kernel_mlp.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.lstrip().startswith("- "):
+            k, v = line.lstrip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(seconds: float, inputs=None, seed=0):
+    """Time the C oracle (OpenMP build, all host cores) on a bounded row sample
+    of the workload: first dinp rows and dweight rows (with the bias) of each
+    layer, as many as fill about `seconds`. Returns (TFLOP/s, seconds, desc, threads)."""
+    import oracle
+
+    orc = oracle.get("omp")
+    wl = synth.WORKLOADS[WORKLOAD]
+    if inputs is None:
+        inputs = [synth.make_inputs(l, seed) for l in wl.layers]
+    # calibrate on a few rows, then size the sample
+    rows0 = max(1, orc.threads)
+    t0 = time.perf_counter()
+    flops0 = _oracle_rows(orc, wl, inputs, rows0)
+    cal = time.perf_counter() - t0
+    rate = flops0 / max(cal, 1e-6)
+    budget = max(seconds - cal, 0.5)
+    rows = max(rows0, int(rows0 * budget * rate / max(flops0, 1)))
+    t0 = time.perf_counter()
+    flops = _oracle_rows(orc, wl, inputs, rows)
+    dt = time.perf_counter() - t0
+    desc = (f"{rows} dinp rows and {rows} dweight rows (+dbias) of each MLP layer "
+            f"({flops / 1e9:.1f} GFLOP of the {wl.flops() / 1e9:.1f} GFLOP step)")
+    return flops / dt / 1e12, dt, desc, orc.threads, flops
+
+
+def _oracle_rows(orc, wl, inputs, rows):
+    flops = 0
+    for l, x in zip(wl.layers, inputs):
+        r_bt = np.arange(min(rows, l.BT))
+        r_o = np.arange(min(rows, l.OC))
+        orc.dinp_rows(x["dout"], x["weight"], l.dtype, r_bt, x["dinp"])
+        orc.dweight_rows(x["dout"], x["inp"], l.dtype, r_o, x["dweight"], bias=l.bias)
+        flops += 2 * len(r_bt) * l.C * l.OC + 2 * len(r_o) * l.BT * l.C + (len(r_o) * l.BT if l.bias else 0)
+    return flops
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = synth.WORKLOADS[WORKLOAD]
+    inputs = [synth.make_inputs(l, 0) for l in wl.layers]
+    import oracle
+
+    orc = oracle.get("omp")
+    total_steps = args.steps + args.warmup
+    # rows per step so that the whole run stays within ~90 s
+    rows0 = max(1, orc.threads)
+    t0 = time.perf_counter()
+    f0 = _oracle_rows(orc, wl, inputs, rows0)
+    rate = f0 / max(time.perf_counter() - t0, 1e-6)
+    per_step_flops = max(f0 / rows0, rate * 90.0 / max(total_steps, 1))
+    rows = max(1, int(per_step_flops / (f0 / rows0)))
+    for _ in range(args.warmup):
+        _oracle_rows(orc, wl, inputs, rows)
+    t0 = time.perf_counter()
+    flops = 0
+    for _ in range(args.steps):
+        flops += _oracle_rows(orc, wl, inputs, rows)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"each step: {rows} dinp rows and {rows} dweight rows (+dbias) of each MLP layer "
+              f"({flops / args.steps / 1e9:.2f} GFLOP of the {wl.flops() / 1e9:.1f} GFLOP step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def to_device_tensor(torch, a, dev):
+    t = torch.from_numpy(a)
+    if a.dtype == np.uint16:
+        t = t.view(torch.bfloat16)
+    return t.to(dev)
+
+
+def run_gpu(args):
+    import torch
+
+    import linear_layer_gemms_gb300 as mm
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    mm.load()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    host = [synth.make_inputs(l, seed=0) for l in wl.layers]
+    sets = []
+    for s in range(N_SETS):
+        sets.append([{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for x in host])
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def call(layer, t):
+        rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
+                          t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
+                          t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T, layer.C,
+                          layer.OC, mm.BF16, sh)
+        if rc != mm.OK:
+            raise RuntimeError(f"mmbwd_run: {mm.strerror(rc)}")
+
+    # warm-up (also grows the workspace outside the timed region)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            for layer, t in zip(wl.layers, sets[k % N_SETS]):
+                call(layer, t)
+    torch.cuda.synchronize()
+    status, info = mm.mmbwd_device_status(reset=True)
+    if status != mm.OK:
+        raise RuntimeError(f"device status after warm-up: {mm.strerror(status)} {info}")
+
+    K = args.steps
+    L = len(wl.layers)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(L)] for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for k in range(K):
+            tset = sets[k % N_SETS]
+            for li, layer in enumerate(wl.layers):
+                ev[k][li][0].record(stream)
+                call(layer, tset[li])
+                ev[k][li][1].record(stream)
+        e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_s = e_start.elapsed_time(e_end) / 1e3
+    status, info = mm.mmbwd_device_status(reset=True)
+    if status != mm.OK:
+        raise RuntimeError(f"device status after timed region: {mm.strerror(status)} {info}")
+
+    launch_ms = [[ev[k][li][0].elapsed_time(ev[k][li][1]) for k in range(K)] for li in range(L)]
+    flops_step = wl.flops()
+    units, max_s = aggregate(flops_step * K, elapsed_s)
+    value = units / max_s / 1e12
+
+    # roofline of the tensor-core kernel (the only kernel these launches run)
+    peaks, peak_src = measured_peaks()
+    kernel_flops = sum(l.flops() for l in wl.layers) * K
+    kernel_s = sum(sum(x) for x in launch_ms) / 1e3
+    achieved = kernel_flops / kernel_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = profiled_traffic()
+
+    # end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, mm, wl, host, dev, stream, args.e2e_steps, barrier)
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and ws >= 1:
+        v, dt, desc, cores, _ = oracle_sample(args.cpu_seconds, inputs=host)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+
+    per_layer = {l.name: {"mean_us": 1e3 * statistics.mean(launch_ms[i]),
+                          "tflops": l.flops() / (statistics.mean(launch_ms[i]) / 1e3) / 1e12}
+                 for i, l in enumerate(wl.layers)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_s / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, GPT-2 small MLP shapes)",
+        "config": config_dict(),
+        "frac_of_bf16_peak": value / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "tc_mmbwd_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "per_layer": per_layer},
+        "gpu_launches": K * L,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(torch, mm, wl, host, dev, stream, steps, barrier):
+    """Same steps through mmbwd_run with pinned host inputs: H2D of dout, inp,
+    weight and D2H of dinp, dweight, dbias every step, inside the timed region."""
+    pin_in = [{k: torch.from_numpy(x[k]).pin_memory() for k in ("dout", "inp", "weight")} for x in host]
+    pin_out = [{k: torch.from_numpy(x[k].copy()).pin_memory() for k in ("dinp", "dweight", "dbias")} for x in host]
+    d = [{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for x in host]
+    h2d = sum(v.numel() * v.element_size() for x in pin_in for v in x.values())
+    d2h = sum(v.numel() * v.element_size() for x in pin_out for v in x.values())
+    sh = stream.cuda_stream
+
+    def step():
+        for layer, pi, po, t in zip(wl.layers, pin_in, pin_out, d):
+            for k in ("dout", "inp", "weight"):
+                t[k].view(torch.int16).copy_(pi[k].view(torch.int16), non_blocking=True)
+            rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
+                              t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
+                              t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T, layer.C,
+                              layer.OC, mm.BF16, sh)
+            if rc != mm.OK:
+                raise RuntimeError(mm.strerror(rc))
+            for k in ("dinp", "dweight", "dbias"):
+                po[k].view(torch.int16).copy_(t[k].view(torch.int16), non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    s = a.elapsed_time(b) / 1e3
+    units, max_s = aggregate(wl.flops() * steps, s)
+    return {"value": units / max_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": max_s / steps * 1e3}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 namespace mmbwd {
@@ -41,6 +42,39 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_fail_allocs{0};
+
+// Plans depend only on (BT, C, OC, SM count) and the tuning overrides; the
+// schedule search is cached so that a call costs a table lookup.
+struct PlanKey {
+    int64_t BT, C, OC;
+    int sms;
+    long splitk, grid;
+    bool operator==(const PlanKey& o) const {
+        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && splitk == o.splitk && grid == o.grid;
+    }
+};
+constexpr int kPlanCache = 32;
+PlanKey g_plan_keys[kPlanCache];
+TcPlan g_plans[kPlanCache];
+int g_plan_count = 0, g_plan_next = 0;
+
+long env_long(const char* name) {
+    const char* s = std::getenv(name);
+    return (s && *s) ? std::strtol(s, nullptr, 10) : 0;
+}
+
+// Caller holds g_mutex.
+const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms) {
+    const PlanKey k{BT, C, OC, sms, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID")};
+    for (int i = 0; i < g_plan_count; ++i)
+        if (g_plan_keys[i] == k) return g_plans[i];
+    const int slot = g_plan_next;
+    g_plan_next = (g_plan_next + 1) % kPlanCache;
+    if (g_plan_count < kPlanCache) ++g_plan_count;
+    g_plan_keys[slot] = k;
+    g_plans[slot] = tc_make_plan(BT, C, OC, sms);
+    return g_plans[slot];
+}
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     if (!a || !b || na == 0 || nb == 0) return false;
@@ -251,7 +285,7 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
 
-    const TcPlan plan = tc_make_plan(s.BT, C, OC, d->num_sms);
+    const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms);
     rc = ensure_workspace(*d, plan.ws_bytes(), stream);
     if (rc != MMBWD_OK) return rc;
     e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream);
