@@ -412,7 +412,9 @@ def run_gpu(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "tc_mmbwd_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "per_layer": per_layer},
-        "gpu_launches": K * L,
+        "gpu_launches": K * sum(mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0)["launches"]
+                                for l in wl.layers),
+        "plans": {l.name: mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0) for l in wl.layers},
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -123,10 +123,12 @@ int mmbwd_device_status(int reset, int* info);
 int mmbwd_version(void);
 
 /* Describe the work split mmbwd_run would use (a pure function of the shape
- * and the SM count). out[0..n) receives, in order: path (0 = fp32 SIMT,
- * 1 = bf16 tensor-core), grid size, work items, dweight splits, k-blocks per
- * split, dinp tiles, dweight tiles, schedule order, tile M, tile N, tile K,
- * pipeline stages. Returns the number of values written, or a negative status. */
+ * and the number of co-resident CTAs; num_sms <= 0 takes the current device's
+ * value, or 152 without a usable device). out[0..n) receives, in order: path (0 = fp32 SIMT,
+ * 1 = bf16 tensor-core), grid size (CTAs), work items, dweight splits, k-blocks
+ * per split, dinp tiles, dweight tiles, schedule order, tile M, tile N, tile K,
+ * pipeline stages, kernel launches per call. Returns the number of values
+ * written (at most 13), or a negative status. */
 int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms,
                     int* out, int n);
 

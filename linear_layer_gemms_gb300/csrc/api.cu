@@ -130,6 +130,11 @@ int device_state(DeviceState** out, int* dev_out) {
             return MMBWD_ERR_CUDA;
         d.arch_checked = (major == 10 && minor == 3) ? 1 : -1;
         d.num_sms = sms;
+        if (d.arch_checked == 1) {
+            // CTAs the persistent kernel can keep resident: whole pairs only.
+            const int pairs = tc_max_active_pairs();
+            if (pairs > 0 && 2 * pairs < sms) d.num_sms = 2 * pairs;
+        }
     }
     if (d.arch_checked != 1) return MMBWD_ERR_ARCH;
     *out = &d;
@@ -137,7 +142,7 @@ int device_state(DeviceState** out, int* dev_out) {
     return MMBWD_OK;
 }
 
-// Grow the device's workspace to `need` bytes (counters start at zero).
+// Grow the device's workspace to `need` bytes (its contents need no initial value).
 int ensure_workspace(DeviceState& d, size_t need, cudaStream_t stream) {
     if (need <= d.ws_bytes) return MMBWD_OK;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -158,7 +163,7 @@ int ensure_workspace(DeviceState& d, size_t need, cudaStream_t stream) {
         cudaGetLastError();
         return MMBWD_ERR_ALLOC;
     }
-    if (cudaMemset(p, 0, need) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
         cudaFree(p);
         return MMBWD_ERR_CUDA;
     }
@@ -213,20 +218,26 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     const int rc = check_shape(B, T, C, OC, dtype, &s);
     if (rc != MMBWD_OK) return rc;
     if (!out || n < 0) return MMBWD_ERR_NULL;
-    int v[12] = {0};
+    int v[13] = {0};
+    if (num_sms <= 0) {  // the current device's resident CTAs (a full GB300 without a device)
+        std::lock_guard<std::mutex> g(g_mutex);
+        DeviceState* d = nullptr;
+        int dev = 0;
+        num_sms = device_state(&d, &dev) == MMBWD_OK ? d->num_sms : 152;
+    }
     if (dtype == MMBWD_BF16) {
-        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms > 0 ? num_sms : 152);
-        const int vals[12] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
-                              pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.dw_first * 2 + pl.snake,
-                              TC_BM, TC_BN, TC_BK, TC_STAGES};
-        for (int i = 0; i < 12; ++i) v[i] = vals[i];
+        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms);
+        const int vals[13] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
+                              pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.table,
+                              TC_PAIR_BM, TC_BN, TC_BK, TC_STAGES, pl.launches()};
+        for (int i = 0; i < 13; ++i) v[i] = vals[i];
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
         const int go = static_cast<int>((OC + SIMT_BM - 1) / SIMT_BM);
-        const int vals[12] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BK, 2};
-        for (int i = 0; i < 12; ++i) v[i] = vals[i];
+        const int vals[13] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BK, 2, 2};
+        for (int i = 0; i < 13; ++i) v[i] = vals[i];
     }
-    const int m = n < 12 ? n : 12;
+    const int m = n < 13 ? n : 13;
     for (int i = 0; i < m; ++i) out[i] = v[i];
     return m;
 }

@@ -12,12 +12,15 @@
 namespace mmbwd {
 
 // ------------------------------------------------------------ bf16 tensor-core path
-// Tile shape of the persistent tcgen05 kernel: one CTA computes a 128 x 256
-// fp32 accumulator in tensor memory, 64 elements of K per pipeline stage.
-constexpr int TC_BM = 128;
-constexpr int TC_BN = 256;
+// Tile shape of the persistent tcgen05 kernel: a pair of CTAs (a cluster of 2
+// on neighbouring SMs) computes a 256 x 256 tile with pair MMAs; each CTA holds
+// 128 rows of the fp32 accumulator in its tensor memory and stages its 128
+// rows of A and 128 columns of B, 64 elements of K per pipeline stage.
+constexpr int TC_BM = 128;       // rows per CTA
+constexpr int TC_PAIR_BM = 256;  // rows per CTA pair
+constexpr int TC_BN = 256;       // columns per tile (128 staged by each CTA)
 constexpr int TC_BK = 64;
-constexpr int TC_STAGES = 4;
+constexpr int TC_STAGES = 6;
 constexpr int TC_THREADS = 256;
 
 // Wait sites reported in the device status word.
@@ -31,15 +34,28 @@ enum WaitSite : int {
     SITE_BIAS_FULL = 7,
     SITE_TEARDOWN = 8,
     SITE_SELFTEST = 9,
+    SITE_FORWARD_FULL = 10,
+};
+
+// Schedule of a launch: which work items each CTA pair processes, in order
+// (items of pair c: items[start[c] .. start[c+1])). It travels in the kernel
+// parameters, so a launch needs no device memory for it.
+constexpr int TC_MAX_PAIRS = 128;
+constexpr int TC_MAX_SCHED_ITEMS = 3072;
+struct TcSchedule {
+    uint16_t start[TC_MAX_PAIRS + 1];
+    uint16_t items[TC_MAX_SCHED_ITEMS];
 };
 
 // Work list of one call: the dweight (TN) items -- dweight tiles times the
-// K splits -- and the dinp (NN) tiles. `dw_first` says which group comes
-// first in the item order; `snake` reverses the CTA order on odd rounds.
+// K splits -- and the dinp (NN) tiles, item w < n_dw_items being a dweight
+// item. Items are assigned to CTA pairs longest first, each to the pair with
+// the least work so far (`table` = 1); when a list is too long for the
+// parameter table, pairs take items round-robin instead (`table` = 0).
 struct TcPlan {
     int tiles_n;       // ceil(C / BN), shared by both products (N = C for both)
-    int dinp_tiles_m;  // ceil(BT / BM)
-    int dw_tiles_m;    // ceil(OC / BM)
+    int dinp_tiles_m;  // ceil(BT / PAIR_BM): row tiles of dinp, one per CTA pair
+    int dw_tiles_m;    // ceil(OC / PAIR_BM): row tiles of dweight, one per CTA pair
     int dinp_kb;       // ceil(OC / BK)
     int dw_kb;         // ceil(BT / BK)
     int splits;        // K splits of the dweight product
@@ -47,13 +63,15 @@ struct TcPlan {
     int n_dw_items;    // dw_tiles_m * tiles_n * splits
     int n_dinp_items;  // dinp_tiles_m * tiles_n
     int n_items;
-    int dw_first;
-    int snake;
-    int grid;
+    int table;         // 1: per-pair item lists in `sched`; 0: round-robin
+    int grid;          // CTAs (twice the number of CTA pairs)
+    double est_us;     // the planner's time estimate
+    int fixup_grid;    // CTAs of the split-reduction pass (0 when splits == 1)
     size_t ws_partials_bytes;  // fp32 partial tiles (splits > 1 only)
-    size_t ws_bias_bytes;      // fp32 partial bias sums
-    size_t ws_counter_bytes;   // arrival counters, one per dweight tile
-    size_t ws_bytes() const { return ws_partials_bytes + ws_bias_bytes + ws_counter_bytes; }
+    size_t ws_bias_bytes;      // fp32 partial bias sums (splits > 1 only)
+    size_t ws_bytes() const { return ws_partials_bytes + ws_bias_bytes; }
+    int launches() const { return splits > 1 ? 2 : 1; }
+    TcSchedule sched;
 };
 
 struct TcParams {
@@ -62,24 +80,29 @@ struct TcParams {
     __nv_bfloat16* dweight;
     __nv_bfloat16* dbias;  // may be null
     int tiles_n, dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
-    int n_dw_items, n_dinp_items, n_items, dw_first, snake;
-    float* partials;       // [dw tile][split][BN/4][BM][4]
-    float* bias_partials;  // [dw_tiles_m][split][BM]
-    int* counters;         // [dw tile]
+    int n_dw_items, n_dinp_items, n_items, table;
+    float* partials;       // [dw half tile][split][BM][BN]; half tile = 128-row tile x column tile
+    float* bias_partials;  // [dw 128-row tile][split][BM]
     unsigned long long timeout_ns;
 };
 
-// Plans (pure functions of the shape and SM count). Overrides for tuning and
-// tests come from the environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs).
+// Plans (pure functions of the shape and the number of co-resident CTAs,
+// twice the resident CTA pairs). Overrides for tuning and tests come from the
+// environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs).
 TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms);
 
-// Launch the tensor-core kernel. `ws` must hold plan.ws_bytes() bytes whose
-// counter region is zero. Returns a cudaError_t.
+// Launch the tensor-core kernel (and, with split dweight, the fixed-order
+// split reduction after it on the same stream). `ws` must hold plan.ws_bytes()
+// bytes. Returns a cudaError_t.
 cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC,
                       void* ws, cudaStream_t stream);
 
 size_t tc_smem_bytes();
+
+// How many CTA pairs of the tensor-core kernel can be resident at once on the
+// current device (0 if the query fails).
+int tc_max_active_pairs();
 
 // Device status word of the tensor-core translation unit.
 cudaError_t tc_read_status(int* code, int* info3, bool reset);

@@ -7,37 +7,51 @@
 //   dweight (OC x C) += dout^T (OC x BT) . inp (BT x C)      "TN": A MN-major, B MN-major
 //   dbias   (OC)      = column sums of dout                  fused into the dweight pass
 //
-// Work list: every 128 x 256 output tile of dinp is one item; every 128 x 256
-// tile of dweight is cut into `splits` items along its long BT reduction.
-// Each CTA (one per SM) walks a static, shape-determined sequence of items.
+// CTA pairs. The grid is made of clusters of two CTAs on neighbouring SMs.
+// A pair computes one 256 x 256 output tile with pair MMAs (tcgen05.mma
+// cta_group::2, M = 256, N = 256, K = 16): CTA r of the pair stages rows
+// [128 r, 128 r + 128) of A and columns [128 r, 128 r + 128) of B, and its
+// tensor memory receives rows [128 r, 128 r + 128) of the accumulator. Each SM
+// thus moves 32 KB per 64-deep K step instead of 48 KB for a single-CTA
+// 128 x 256 tile, which is what lets the load pipeline keep the tensor core fed.
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer: fills a 4-stage ring of (A 16 KB, B 32 KB) tiles
-//               in 128-byte-swizzled shared memory.
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma (M128 N256 K16) per
-//               stage into one of two 128 x 256 fp32 accumulators in tensor
-//               memory (512 columns), so the epilogue of tile i overlaps the
-//               main loop of tile i+1.
-//   warps 2-3   bias: on dweight items of the first column tile, sum the dout
-//               tile of every stage over its BT rows (the A operand already in
-//               shared memory), reduce across lanes with shuffles.
-//   warps 4-7   epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes
-//               32*(w%4)..+31, i.e. tile rows), then either
+// Work list: every 256 x 256 tile of dinp is one item; every 256 x 256 tile of
+// dweight is cut into `splits` items along its long BT reduction. Each pair
+// walks a static, shape-determined sequence of items.
+//
+// Warp roles (256 threads per CTA):
+//   warp 0      TMA producer (both CTAs): a 6-stage ring of (A 16 KB, B 16 KB)
+//               tiles in 128-byte-swizzled shared memory; completion lands on
+//               the CTA's own "full" barrier.
+//   warp 1      even CTA: MMA issuer (one thread) into one of two 128 x 256 fp32
+//               accumulators per CTA (512 tensor-memory columns), so the epilogue
+//               of one item overlaps the main loop of the next; commits are
+//               multicast to both CTAs' barriers.
+//               odd CTA: forwards each stage's "full" to the even CTA's barrier.
+//   warps 2-3   bias: on dweight items of the first column tile, sum the CTA's
+//               dout tile of every stage over its BT rows (the A operand already
+//               in shared memory) and reduce across lanes with shuffles.
+//   warps 4-7   epilogue (both CTAs): tcgen05.ld the accumulator (warp w reads
+//               tensor-memory lanes 32*(w%4)..+31, i.e. tile rows), transpose each
+//               32-column chunk through shared memory so that global accesses are
+//               row-contiguous, then either
 //                 - read-modify-write the bf16 output: old + acc, one rounding
-//                   (dinp, and dweight when it is not split), or
-//                 - store an fp32 partial tile, count arrivals, and let the last
-//                   arriving split sum all partials in split order 0..S-1 and
-//                   do the read-modify-write (deterministic: the order of the
-//                   sum never depends on which split finished last).
+//                   (dinp, and dweight when it is not split), old values
+//                   prefetched four chunks ahead, or
+//                 - store the fp32 partial tile of this split (dweight split
+//                   along BT); a second kernel then sums the partials of every
+//                   tile in split order 0..S-1 and does the read-modify-write, so
+//                   the sum never depends on which split finished first.
 //
 // Every wait is bounded (global timer); a wait that gives up records the
 // failure in the device status word, raises a CTA abort flag, and all roles
-// unwind; in-flight copies and MMAs are waited for before the tensor memory
-// is released.
+// unwind; copies and MMAs in flight are waited for before tensor memory is
+// released.
 #include "../../include/mmbwd.h"
 #include "internal.h"
 #include "ptx.cuh"
 
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -49,36 +63,41 @@ __device__ unsigned int g_status[4];
 
 namespace {
 
-constexpr int A_BYTES = TC_BM * TC_BK * 2;      // 16 KB
-constexpr int B_BYTES = TC_BN * TC_BK * 2;      // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
-constexpr int BOX_BYTES = 64 * TC_BK * 2;       // 8 KB: 64 (MN) x 64 (K) bf16, MN-major
-constexpr int ROW_BYTES = 128;                  // one swizzled 128-byte row
+constexpr int A_BYTES = TC_BM * TC_BK * 2;            // 16 KB: this CTA's 128 rows of A
+constexpr int B_BYTES = (TC_BN / 2) * TC_BK * 2;      // 16 KB: this CTA's 128 columns of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // 32 KB
+constexpr int BOX_BYTES = 64 * TC_BK * 2;             // 8 KB: 64 (MN) x 64 (K) bf16, MN-major
+constexpr int ROW_BYTES = 128;                        // one swizzled 128-byte row
 constexpr int NUM_BIAS_WARPS = 2;
 constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_BIAS = 2;
 constexpr int WARP_EPI = 4;
-constexpr int NUM_EPI_THREADS = 128;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_EPI_THREADS = 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * TC_BN;
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int OFF_BARS = TC_STAGES * STAGE_BYTES;
-constexpr int BAR_FULL = 0;
-constexpr int BAR_EMPTY = TC_STAGES;
-constexpr int BAR_TFULL = 2 * TC_STAGES;
-constexpr int BAR_TEMPTY = 2 * TC_STAGES + 2;
-constexpr int BAR_BIAS = 2 * TC_STAGES + 4;
-constexpr int BAR_TEARDOWN = 2 * TC_STAGES + 6;
-constexpr int N_BARS = 2 * TC_STAGES + 7;
+constexpr int BAR_FULL = 0;                    // [stages] TMA landed (even CTA: and the peer's too)
+constexpr int BAR_EMPTY = TC_STAGES;           // [stages] stage may be refilled
+constexpr int BAR_TFULL = 2 * TC_STAGES;       // [2] accumulator ready
+constexpr int BAR_TEMPTY = 2 * TC_STAGES + 2;  // [2] accumulator drained by both CTAs (even CTA)
+constexpr int BAR_EPIDONE = 2 * TC_STAGES + 4; // [2] this CTA's epilogue finished an item
+constexpr int BAR_BIAS = 2 * TC_STAGES + 6;    // [2] bias sums ready
+constexpr int BAR_TEARDOWN = 2 * TC_STAGES + 8;
+constexpr int N_BARS = 2 * TC_STAGES + 9;
 constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag, [2] broadcast
 constexpr int OFF_BIAS = (OFF_MISC + 16 + 127) & ~127;
-constexpr int SMEM_USED = OFF_BIAS + 2 * TC_BM * 4;
+constexpr int STG_STRIDE = 36;  // floats per staged row: 16-byte aligned, conflict-free
+constexpr int STG_WARP_BYTES = 32 * STG_STRIDE * 4;
+constexpr int OFF_STAGE = OFF_BIAS + 2 * TC_BM * 4;
+constexpr int SMEM_USED = OFF_STAGE + NUM_EPI_WARPS * STG_WARP_BYTES;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t IDESC_DINP = ptx::idesc_bf16_f32(TC_BM, TC_BN, /*A MN*/ 0, /*B MN*/ 1);
-constexpr uint32_t IDESC_DW = ptx::idesc_bf16_f32(TC_BM, TC_BN, /*A MN*/ 1, /*B MN*/ 1);
+constexpr uint32_t IDESC_DINP = ptx::idesc_bf16_f32(TC_PAIR_BM, TC_BN, /*A MN*/ 0, /*B MN*/ 1);
+constexpr uint32_t IDESC_DW = ptx::idesc_bf16_f32(TC_PAIR_BM, TC_BN, /*A MN*/ 1, /*B MN*/ 1);
 
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per wait
 
@@ -136,42 +155,40 @@ struct Waiter {
 
 struct Item {
     int is_dw;
-    int m_tile, n_tile;
+    int pm;      // row tile of the pair (256 rows)
+    int n_tile;  // column tile (256 columns)
     int split;
     int kb0, kb1;  // k-block range [kb0, kb1)
-    int tile;      // dweight tile index (m_tile * tiles_n + n_tile)
 };
 
 __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
     Item it;
-    const int first_n = p.dw_first ? p.n_dw_items : p.n_dinp_items;
-    const bool in_first = w < first_n;
-    const int local = in_first ? w : w - first_n;
-    it.is_dw = (in_first == (p.dw_first != 0)) ? 1 : 0;
+    it.is_dw = w < p.n_dw_items ? 1 : 0;
+    const int local = it.is_dw ? w : w - p.n_dw_items;
     it.n_tile = local % p.tiles_n;
     const int rest = local / p.tiles_n;
     if (it.is_dw) {
-        it.m_tile = rest % p.dw_tiles_m;
+        it.pm = rest % p.dw_tiles_m;
         it.split = rest / p.dw_tiles_m;
         it.kb0 = it.split * p.kb_per_split;
         it.kb1 = min(it.kb0 + p.kb_per_split, p.dw_kb);
-        it.tile = it.m_tile * p.tiles_n + it.n_tile;
     } else {
-        it.m_tile = rest;
+        it.pm = rest;
         it.split = 0;
         it.kb0 = 0;
         it.kb1 = p.dinp_kb;
-        it.tile = 0;
     }
     return it;
 }
 
-// Item processed by this CTA in round `round` (>= n_items: none).
-__device__ __forceinline__ int item_at(const TcParams& p, int round) {
-    const int G = static_cast<int>(gridDim.x);
-    const int b = (p.snake && (round & 1)) ? (G - 1 - static_cast<int>(blockIdx.x))
-                                           : static_cast<int>(blockIdx.x);
-    return round * G + b;
+// Item processed by this CTA pair in round `round` (>= n_items: none).
+__device__ __forceinline__ int item_at(const TcParams& p, const TcSchedule& sch, int round) {
+    const int c = static_cast<int>(blockIdx.x >> 1);
+    if (p.table) {
+        const int idx = sch.start[c] + round;
+        return idx < sch.start[c + 1] ? static_cast<int>(sch.items[idx]) : p.n_items;
+    }
+    return round * static_cast<int>(gridDim.x >> 1) + c;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -192,23 +209,12 @@ __device__ __forceinline__ uint4 add_round8(uint4 old, const float (&s)[8]) {
     return r;
 }
 
-// Old values of one tile row: 32 vectors of 8 bf16 (256 columns). Vectors
-// outside the tensor are not read.
-__device__ __forceinline__ void load_row(uint4 (&old)[TC_BN / 8], const __nv_bfloat16* drow,
-                                         bool row_ok, int ncols) {
-#pragma unroll
-    for (int v = 0; v < TC_BN / 8; ++v) {
-        old[v] = (row_ok && v * 8 < ncols) ? *reinterpret_cast<const uint4*>(drow + v * 8)
-                                           : make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_mmbwd_kernel(const __grid_constant__ CUtensorMap tm_dout_k,   // dout, A of dinp (K-major)
                     const __grid_constant__ CUtensorMap tm_weight,   // weight, B of dinp (MN-major)
                     const __grid_constant__ CUtensorMap tm_dout_mn,  // dout, A of dweight (MN-major)
                     const __grid_constant__ CUtensorMap tm_inp,      // inp, B of dweight (MN-major)
-                    const TcParams p) {
+                    const TcParams p, const __grid_constant__ TcSchedule sch) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -219,16 +225,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
+    const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the pair MMAs
+    const bool leader = rank == 0;
     const bool bias_on = p.dbias != nullptr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
-            ptx::mbar_init(bars + 8u * (BAR_FULL + s), 1);
+            ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
             ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on ? NUM_BIAS_WARPS : 0));
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
-            ptx::mbar_init(bars + 8u * (BAR_TEMPTY + a), NUM_EPI_THREADS / 32);
+            ptx::mbar_init(bars + 8u * (BAR_TEMPTY + a), 2 * NUM_EPI_WARPS);
+            ptx::mbar_init(bars + 8u * (BAR_EPIDONE + a), NUM_EPI_WARPS);
             ptx::mbar_init(bars + 8u * (BAR_BIAS + a), NUM_BIAS_WARPS);
         }
         ptx::mbar_init(bars + 8u * BAR_TEARDOWN, 1);
@@ -236,11 +245,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         ptx::fence_mbar_init();
     }
     if (warp == WARP_MMA) {
-        ptx::tmem_alloc(base + OFF_MISC, TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_pair(base + OFF_MISC, TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = misc[0];
     const Waiter wt{misc + 1, p.timeout_ns};
@@ -255,17 +265,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
-                const int w = item_at(p, r);
+                const int w = item_at(p, sch, r);
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
-                // Boxes that start inside the tensor; boxes wholly outside would
-                // only feed accumulator rows/columns that are never stored.
-                int nb = 0;
-                for (int j = 0; j < TC_BN / 64; ++j) nb += (it.n_tile * TC_BN + j * 64 < p.C) ? 1 : 0;
-                int na = 1;
-                if (it.is_dw) na = (it.m_tile * TC_BM + 64 < p.OC) ? 2 : 1;
+                // This CTA's rows of A and columns of B. Boxes wholly outside the
+                // tensor are skipped: they would only feed accumulator rows or
+                // columns that are never stored.
+                const int row0 = it.pm * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
+                const int col0 = it.n_tile * TC_BN + static_cast<int>(rank) * (TC_BN / 2);
+                const int nb = (col0 < p.C ? 1 : 0) + (col0 + 64 < p.C ? 1 : 0);
+                int na;
+                if (it.is_dw) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
+                else na = row0 < p.BT ? 1 : 0;
                 const uint32_t bytes =
-                    static_cast<uint32_t>((it.is_dw ? na * BOX_BYTES : A_BYTES) + nb * BOX_BYTES);
+                    static_cast<uint32_t>((it.is_dw ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES);
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wt.wait(bars + 8u * (BAR_EMPTY + stage), phase ^ 1u, SITE_PRODUCER_EMPTY, w)) {
                         ok = false;
@@ -277,16 +290,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(fb, bytes);
                     if (it.is_dw) {
                         for (int j = 0; j < na; ++j)
-                            ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb,
-                                             it.m_tile * TC_BM + j * 64, kb * TC_BK);
+                            ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * TC_BK);
                         for (int j = 0; j < nb; ++j)
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_inp, fb,
-                                             it.n_tile * TC_BN + j * 64, kb * TC_BK);
+                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_inp, fb, col0 + j * 64, kb * TC_BK);
                     } else {
-                        ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, it.m_tile * TC_BM);
+                        if (na) ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, row0);
                         for (int j = 0; j < nb; ++j)
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_weight, fb,
-                                             it.n_tile * TC_BN + j * 64, kb * TC_BK);
+                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_weight, fb, col0 + j * 64, kb * TC_BK);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -296,61 +306,91 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
             }
-            // Copies still in flight must land before shared memory goes away.
+            // This CTA's copies still in flight land before shared memory goes
+            // away (its own full barrier counts its own bytes; in a normal run
+            // every phase has already been consumed and these return at once).
             for (int s = 0; s < TC_STAGES; ++s)
                 if ((issued >> s) & 1u) wt.wait_teardown(bars + 8u * (BAR_FULL + s), (last_parity >> s) & 1u);
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            for (int r = 0; ok; ++r) {
-                const int w = item_at(p, r);
-                if (w >= p.n_items) break;
-                const Item it = decode_item(p, w);
-                if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * TC_BN;
-                const uint32_t idesc = it.is_dw ? IDESC_DW : IDESC_DINP;
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (!wt.wait(bars + 8u * (BAR_FULL + stage), phase, SITE_MMA_FULL, w)) {
-                        ok = false;
-                        break;
-                    }
+        if (leader) {
+            // -------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+                bool ok = true;
+                for (int r = 0; ok; ++r) {
+                    const int w = item_at(p, sch, r);
+                    if (w >= p.n_items) break;
+                    const Item it = decode_item(p, w);
+                    if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
                     ptx::tc_fence_after();
-                    const uint32_t sA = base + stage * STAGE_BYTES;
-                    const uint32_t sB = sA + A_BYTES;
+                    const uint32_t d_tmem = tmem_base + acc * TC_BN;
+                    const uint32_t idesc = it.is_dw ? IDESC_DW : IDESC_DINP;
+                    for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                        // Both CTAs' copies of this stage have landed (own bytes +
+                        // the odd CTA's forwarded arrival).
+                        if (!wt.wait(bars + 8u * (BAR_FULL + stage), phase, SITE_MMA_FULL, w)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sA = base + stage * STAGE_BYTES;
+                        const uint32_t sB = sA + A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < TC_BK / 16; ++k) {
-                        // K-major A: the 16-element K slice starts 32 bytes further
-                        // into each swizzled 128-byte row; rows in 8-row groups of
-                        // 1024 bytes. MN-major operands: 16 K rows of 128 bytes per
-                        // slice (2048 bytes); 64-wide MN boxes 8 KB apart (leading
-                        // offset), 8-row K groups 1024 bytes apart (stride offset).
-                        const uint64_t adesc =
-                            it.is_dw ? ptx::smem_desc_sw128(sA + k * 2048, BOX_BYTES, 1024)
-                                     : ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
-                        const uint64_t bdesc = ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
-                        ptx::mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < TC_BK / 16; ++k) {
+                            // K-major A: the 16-element K slice starts 32 bytes further
+                            // into each swizzled 128-byte row; rows in 8-row groups of
+                            // 1024 bytes. MN-major operands: 16 K rows of 128 bytes per
+                            // slice (2048 bytes); 64-wide MN boxes 8 KB apart (leading
+                            // offset), 8-row K groups 1024 bytes apart (stride offset).
+                            const uint64_t adesc =
+                                it.is_dw ? ptx::smem_desc_sw128(sA + k * 2048, BOX_BYTES, 1024)
+                                         : ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
+                            const uint64_t bdesc = ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
+                            ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
+                        }
+                        ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), 0x3);
+                        if (++stage == TC_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    ptx::mma_commit(bars + 8u * (BAR_EMPTY + stage));
-                    if (++stage == TC_STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (!ok) break;
+                    ptx::mma_commit_pair_multicast(bars + 8u * (BAR_TFULL + acc), 0x3);
+                    if (++acc == 2) {
+                        acc = 0;
+                        acc_phase ^= 1u;
                     }
                 }
-                if (!ok) break;
-                ptx::mma_commit(bars + 8u * (BAR_TFULL + acc));
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
+                // Every MMA this thread issued completes (and with it every copy
+                // they read) before shared and tensor memory are released.
+                ptx::mma_commit_pair(bars + 8u * BAR_TEARDOWN);
+                wt.wait_teardown(bars + 8u * BAR_TEARDOWN, 0);
+            }
+        } else {
+            // ---------------------------------------------- forwarder (odd CTA)
+            if (lane == 0) {
+                const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, 0);
+                uint32_t stage = 0, phase = 0;
+                bool ok = true;
+                for (int r = 0; ok; ++r) {
+                    const int w = item_at(p, sch, r);
+                    if (w >= p.n_items) break;
+                    const Item it = decode_item(p, w);
+                    for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                        if (!wt.wait(bars + 8u * (BAR_FULL + stage), phase, SITE_FORWARD_FULL, w)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_cluster_relaxed(leader_full + 8u * stage);
+                        if (++stage == TC_STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
                 }
             }
-            // Every MMA this thread issued completes before tensor memory is freed.
-            ptx::mma_commit(bars + 8u * BAR_TEARDOWN);
-            wt.wait_teardown(bars + 8u * BAR_TEARDOWN, 0);
         }
         __syncwarp();
     } else if (warp < WARP_EPI) {
@@ -359,13 +399,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             for (int r = 0;; ++r) {
-                const int w = item_at(p, r);
+                const int w = item_at(p, sch, r);
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
                 const bool has_bias = it.is_dw && it.n_tile == 0;
-                // Lockstep with the MMA issuer: the epilogue has finished with this
-                // accumulator slot (and its bias slot) from two items ago.
-                if (!wt.wait_warp(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_BIAS_TMEM_EMPTY, w))
+                // The epilogue of this CTA has finished with this accumulator
+                // slot (and its bias slot) from two items ago.
+                if (!wt.wait_warp(bars + 8u * (BAR_EPIDONE + acc), acc_phase ^ 1u, SITE_BIAS_TMEM_EMPTY, w))
                     break;
                 float s[8];
 #pragma unroll
@@ -425,26 +465,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;         // TMEM lane quadrant this warp may read
-        const int rit = q * 32 + lane;  // tile row owned by this thread
+        const int q = warp & 3;         // tensor-memory lane quadrant: tile rows 32q..32q+31
+        const int rit = q * 32 + lane;  // tile row this thread reads from tensor memory
+        const int r8 = lane >> 2;       // coalesced phase: rows 8i + r8 of the quadrant,
+        const int cg = (lane & 3) * 8;  //   columns cg..cg+7 of each 32-column chunk
+        const uint32_t stg = base + OFF_STAGE + q * STG_WARP_BYTES;
+        const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, 0);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t bias_parity[2] = {0u, 0u};
         for (int r = 0;; ++r) {
-            const int w = item_at(p, r);
+            const int w = item_at(p, sch, r);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
+            const int m_tile = it.pm * 2 + static_cast<int>(rank);  // this CTA's 128-row tile
             const bool has_bias = bias_on && it.is_dw && it.n_tile == 0;
             const bool split_mode = it.is_dw && p.splits > 1;
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
-            const int64_t row = static_cast<int64_t>(it.m_tile) * TC_BM + rit;
-            const bool row_ok = row < rows_total;
+            const int64_t qrow0 = static_cast<int64_t>(m_tile) * TC_BM + q * 32;  // first row of the quadrant
             const int col0 = it.n_tile * TC_BN;
             const int ncols = static_cast<int>(min(static_cast<int64_t>(TC_BN), p.C - col0));
             __nv_bfloat16* D = it.is_dw ? p.dweight : p.dinp;
-            __nv_bfloat16* drow = D + (row_ok ? row : 0) * p.C + col0;
-
-            uint4 old[TC_BN / 8];
-            if (!split_mode) load_row(old, drow, row_ok, ncols);  // in flight during the main loop
+            bool rok[4];
+            __nv_bfloat16* drow[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t row = qrow0 + 8 * i + r8;
+                rok[i] = row < rows_total;
+                drow[i] = D + (rok[i] ? row : 0) * p.C + col0 + cg;
+            }
+            // Old output values, four 32-column chunks ahead of their use.
+            uint4 oldw[4][4];
+            auto prefetch = [&](int c) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    oldw[c & 3][i] = (rok[i] && c * 32 + cg < ncols)
+                                         ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+            };
+            if (!split_mode) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) prefetch(c);
+            }
 
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
@@ -457,106 +518,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 bias_val = bias_smem[acc * TC_BM + rit];
             }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
-
-            if (!split_mode) {
+            // Partial tile of this split: [128 rows][256 columns] fp32, row-major.
+            float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.tiles_n + it.n_tile) * p.splits +
+                                                     it.split) * (TC_BM * TC_BN)
+                                     : nullptr;
 #pragma unroll
-                for (int c = 0; c < TC_BN / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tbase + c * 32, v);
+            for (int c = 0; c < TC_BN / 32; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tbase + c * 32, v);
+                // Row `lane` of the quadrant into the staging buffer ...
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int vi = c * 4 + j;
-                        if (row_ok && vi * 8 < ncols) {
-                            float s[8];
+                for (int k = 0; k < 8; ++k)
+                    ptx::sts128(stg + (lane * STG_STRIDE + 4 * k) * 4, __uint_as_float(v[4 * k]),
+                                __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
+                                __uint_as_float(v[4 * k + 3]));
+                __syncwarp();
+                // ... and back out as 8 rows x 32 columns per instruction.
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) s[e] = __uint_as_float(v[j * 8 + e]);
-                            *reinterpret_cast<uint4*>(drow + vi * 8) = add_round8(old[vi], s);
-                        }
+                for (int i = 0; i < 4; ++i) {
+                    const int lr = 8 * i + r8;
+                    const float4 a4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg) * 4);
+                    const float4 b4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg + 4) * 4);
+                    if (split_mode) {
+                        float* pp = part + static_cast<size_t>(q * 32 + lr) * TC_BN + c * 32 + cg;
+                        __stcg(reinterpret_cast<float4*>(pp), a4);
+                        __stcg(reinterpret_cast<float4*>(pp + 4), b4);
+                    } else if (rok[i] && c * 32 + cg < ncols) {
+                        const float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(oldw[c & 3][i], s8);
                     }
                 }
-                if (has_bias && row_ok) p.dbias[row] = __float2bfloat16_rn(bias_val);
-            } else {
-                // Partial tile, laid out [column quad][row][4] so that a warp's
-                // 16-byte stores are contiguous.
-                float* part = p.partials +
-                              (static_cast<size_t>(it.tile) * p.splits + it.split) * (TC_BM * TC_BN);
-#pragma unroll
-                for (int c = 0; c < TC_BN / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tbase + c * 32, v);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int qd = c * 8 + j;
-                        *reinterpret_cast<float4*>(part + (static_cast<size_t>(qd) * TC_BM + rit) * 4) =
-                            make_float4(__uint_as_float(v[j * 4 + 0]), __uint_as_float(v[j * 4 + 1]),
-                                        __uint_as_float(v[j * 4 + 2]), __uint_as_float(v[j * 4 + 3]));
-                    }
-                }
-                if (has_bias)
-                    p.bias_partials[(static_cast<size_t>(it.m_tile) * p.splits + it.split) * TC_BM + rit] =
-                        bias_val;
-                __threadfence();
-                ptx::named_bar_sync(1, NUM_EPI_THREADS);
-                if (threadIdx.x == WARP_EPI * 32) misc[2] = static_cast<uint32_t>(atomicAdd(&p.counters[it.tile], 1));
-                ptx::named_bar_sync(1, NUM_EPI_THREADS);
-                const bool last = misc[2] == static_cast<uint32_t>(p.splits - 1);
-                if (last) {
-                    __threadfence();
-#pragma unroll 1
-                    for (int c = 0; c < TC_BN / 32; ++c) {
-                        uint4 oldc[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int vi = c * 4 + j;
-                            oldc[j] = (row_ok && vi * 8 < ncols) ? *reinterpret_cast<const uint4*>(drow + vi * 8)
-                                                                 : make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        uint32_t v[32];
-                        ptx::tmem_ld32(tbase + c * 32, v);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int vi = c * 4 + j;
-                            float s[8];
-                            for (int sp = 0; sp < p.splits; ++sp) {
-                                float f[8];
-                                if (sp == it.split) {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[j * 8 + e]);
-                                } else {
-                                    const float* ps = p.partials +
-                                                      (static_cast<size_t>(it.tile) * p.splits + sp) * (TC_BM * TC_BN);
-                                    const float4 a = __ldcg(reinterpret_cast<const float4*>(
-                                        ps + (static_cast<size_t>(2 * vi) * TC_BM + rit) * 4));
-                                    const float4 b = __ldcg(reinterpret_cast<const float4*>(
-                                        ps + (static_cast<size_t>(2 * vi + 1) * TC_BM + rit) * 4));
-                                    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-                                    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-                                }
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) s[e] = (sp == 0) ? f[e] : s[e] + f[e];
-                            }
-                            if (row_ok && vi * 8 < ncols)
-                                *reinterpret_cast<uint4*>(drow + vi * 8) = add_round8(oldc[j], s);
-                        }
-                    }
-                    if (has_bias) {
-                        float b = 0.f;
-                        for (int sp = 0; sp < p.splits; ++sp) {
-                            const float f = (sp == it.split)
-                                                ? bias_val
-                                                : __ldcg(p.bias_partials +
-                                                         (static_cast<size_t>(it.m_tile) * p.splits + sp) * TC_BM + rit);
-                            b = (sp == 0) ? f : b + f;
-                        }
-                        if (row_ok) p.dbias[row] = __float2bfloat16_rn(b);
-                    }
-                    // Every split has arrived: reset the counter for the next call.
-                    if (threadIdx.x == WARP_EPI * 32) p.counters[it.tile] = 0;
-                }
+                __syncwarp();
+                if (!split_mode && c + 4 < TC_BN / 32) prefetch(c + 4);
+            }
+            if (has_bias) {
+                const int64_t brow = static_cast<int64_t>(m_tile) * TC_BM + rit;
+                if (split_mode)
+                    p.bias_partials[(static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + rit] = bias_val;
+                else if (brow < p.OC)
+                    p.dbias[brow] = __float2bfloat16_rn(bias_val);
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_TEMPTY + acc));
+            if (lane == 0) {
+                ptx::mbar_arrive(bars + 8u * (BAR_EPIDONE + acc));
+                ptx::mbar_arrive_cluster_relaxed(leader_tempty + 8u * acc);
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -566,9 +573,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // The even CTA's MMAs (which write this CTA's tensor memory and read its
+    // shared memory) have completed before either CTA releases anything.
+    ptx::cluster_sync();
     if (warp == WARP_MMA) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// Split reduction: dweight = dweight + (partial_0 + partial_1 + ... + partial_{S-1})
+// with the partials summed in split order and one rounding to bf16, and
+// dbias = bias_partial_0 + ... + bias_partial_{S-1} in the same order. One
+// thread per 8-column vector of dweight; all loads are independent, so the
+// pass runs at memory speed with the partials still in L2.
+__global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) {
+    const int64_t vec_per_row = p.C / 8;
+    const int64_t nvec = p.OC * vec_per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const size_t tile_elems = static_cast<size_t>(TC_BM) * TC_BN;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        const int64_t row = v / vec_per_row;
+        const int64_t col = (v - row * vec_per_row) * 8;
+        const int m_tile = static_cast<int>(row / TC_BM), rl = static_cast<int>(row % TC_BM);
+        const int n_tile = static_cast<int>(col / TC_BN), cl = static_cast<int>(col % TC_BN);
+        const float* pp = p.partials + static_cast<size_t>(m_tile * p.tiles_n + n_tile) * p.splits * tile_elems +
+                          static_cast<size_t>(rl) * TC_BN + cl;
+        float s8[8];
+#pragma unroll 4
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(pp + sp * tile_elems));
+            const float4 b = __ldcg(reinterpret_cast<const float4*>(pp + sp * tile_elems + 4));
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s8[e] = (sp == 0) ? f[e] : s8[e] + f[e];
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.dweight + row * p.C + col);
+        *dst = add_round8(*dst, s8);
+    }
+    if (p.dbias) {
+        for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < p.OC; o += stride) {
+            const int m_tile = static_cast<int>(o / TC_BM), rl = static_cast<int>(o % TC_BM);
+            float b = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp) {
+                const float f = __ldcg(p.bias_partials + (static_cast<size_t>(m_tile) * p.splits + sp) * TC_BM + rl);
+                b = (sp == 0) ? f : b + f;
+            }
+            p.dbias[o] = __float2bfloat16_rn(b);
+        }
     }
 }
 
@@ -598,38 +650,83 @@ long env_long(const char* name, long dflt) {
     return (end && *end == '\0') ? v : dflt;
 }
 
-// Makespan of the static schedule, in units of one k-block of MMA work.
-double schedule_cost(const TcPlan& pl, int grid) {
-    const double item_overhead = 2.0;   // prologue/epilogue not hidden by the pipeline
-    const double split_overhead = 2.0;  // partial-tile store and the fixed-order sum
-    static thread_local double load[4096];
-    for (int b = 0; b < grid; ++b) load[b] = 0.0;
-    for (int r = 0;; ++r) {
-        bool any = false;
-        for (int b = 0; b < grid; ++b) {
-            const int bb = (pl.snake && (r & 1)) ? grid - 1 - b : b;
-            const int w = r * grid + bb;
-            if (w >= pl.n_items) continue;
-            any = true;
-            const int first_n = pl.dw_first ? pl.n_dw_items : pl.n_dinp_items;
-            const bool in_first = w < first_n;
-            const bool is_dw = in_first == (pl.dw_first != 0);
-            double c;
-            if (is_dw) {
-                const int local = in_first ? w : w - first_n;
-                const int split = local / pl.tiles_n / pl.dw_tiles_m;
-                const int kb0 = split * pl.kb_per_split;
-                const int kb1 = std::min(kb0 + pl.kb_per_split, pl.dw_kb);
-                c = (kb1 - kb0) + item_overhead + (pl.splits > 1 ? split_overhead : 0.0);
-            } else {
-                c = pl.dinp_kb + item_overhead;
-            }
-            load[b] += c;
-        }
-        if (!any) break;
+// Planner cost model (µs). An item costs its main loop (one 64-deep k-block of
+// a 256 x 256 pair tile is 512 tensor-core cycles, ~0.27 µs) or its epilogue,
+// whichever is longer, since the two overlap across the two accumulators; the
+// last item's epilogue is not overlapped. Split dweight adds the fixup pass.
+constexpr double T_KB = 0.27;       // one k-block of pair MMAs
+constexpr double T_RMW = 2.6;       // bf16 read-modify-write epilogue of a 128 x 256 half tile
+constexpr double T_PARTIAL = 1.8;   // fp32 partial store of a 128 x 256 half tile
+constexpr double T_ITEM = 0.3;      // per-item handoff
+
+struct ItemCost {
+    double run, epi;
+};
+
+ItemCost item_cost(const TcPlan& pl, int w) {
+    if (w < pl.n_dw_items) {
+        const int split = w / pl.tiles_n / pl.dw_tiles_m;
+        const int kb0 = split * pl.kb_per_split;
+        const int kb = std::min(kb0 + pl.kb_per_split, pl.dw_kb) - kb0;
+        const double epi = pl.splits > 1 ? T_PARTIAL : T_RMW;
+        return {std::max(kb * T_KB, epi) + T_ITEM, epi};
     }
+    return {std::max(pl.dinp_kb * T_KB, T_RMW) + T_ITEM, T_RMW};
+}
+
+double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
+    if (pl.splits == 1) return 0.0;
+    // a launch gap plus S fp32 partials read and dweight read and written
+    const double bytes = static_cast<double>(OC) * C * (4.0 * pl.splits + 4.0);
+    return 3.0 + bytes / 5.0e6;  // ~5 TB/s effective, in bytes per µs
+}
+
+// Longest-first greedy assignment of items to pairs; fills pl.sched and
+// returns the estimated makespan (µs). Ties go to the lower pair index and to
+// the earlier item, so the schedule is a pure function of the shape.
+double assign_lpt(TcPlan& pl, int pairs) {
+    static thread_local double load[TC_MAX_PAIRS], last_epi[TC_MAX_PAIRS];
+    static thread_local int cnt[TC_MAX_PAIRS];
+    static thread_local uint16_t owner[TC_MAX_SCHED_ITEMS];
+    static thread_local int order[TC_MAX_SCHED_ITEMS];
+    const int n = pl.n_items;
+    for (int w = 0; w < n; ++w) order[w] = w;
+    std::stable_sort(order, order + n, [&](int a, int b) { return item_cost(pl, a).run > item_cost(pl, b).run; });
+    for (int c = 0; c < pairs; ++c) load[c] = last_epi[c] = 0.0, cnt[c] = 0;
+    for (int k = 0; k < n; ++k) {
+        const int w = order[k];
+        int best = 0;
+        for (int c = 1; c < pairs; ++c)
+            if (load[c] < load[best] - 1e-9) best = c;
+        const ItemCost ic = item_cost(pl, w);
+        load[best] += ic.run;
+        last_epi[best] = ic.epi;
+        owner[k] = static_cast<uint16_t>(best);
+        ++cnt[best];
+    }
+    pl.sched.start[0] = 0;
+    for (int c = 0; c < pairs; ++c) pl.sched.start[c + 1] = static_cast<uint16_t>(pl.sched.start[c] + cnt[c]);
+    for (int c = pairs; c < TC_MAX_PAIRS; ++c) pl.sched.start[c + 1] = pl.sched.start[pairs];
+    int fill[TC_MAX_PAIRS];
+    for (int c = 0; c < pairs; ++c) fill[c] = pl.sched.start[c];
+    for (int k = 0; k < n; ++k) pl.sched.items[fill[owner[k]]++] = static_cast<uint16_t>(order[k]);
     double m = 0.0;
-    for (int b = 0; b < grid; ++b) m = std::max(m, load[b]);
+    for (int c = 0; c < pairs; ++c) m = std::max(m, load[c] + last_epi[c]);
+    return m;
+}
+
+// Makespan (µs) of round-robin assignment (lists too long for the table).
+double roundrobin_cost(const TcPlan& pl, int pairs) {
+    double m = 0.0;
+    for (int c = 0; c < pairs; ++c) {
+        double l = 0.0, e = 0.0;
+        for (int w = c; w < pl.n_items; w += pairs) {
+            const ItemCost ic = item_cost(pl, w);
+            l += ic.run;
+            e = ic.epi;
+        }
+        m = std::max(m, l + e);
+    }
     return m;
 }
 
@@ -642,50 +739,82 @@ bool g_attr_set[64];
 
 size_t tc_smem_bytes() { return SMEM_TOTAL; }
 
+int tc_max_active_pairs() {
+    if (cudaFuncSetAttribute(tc_mmbwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_TOTAL;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_mmbwd_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     TcPlan pl{};
     pl.tiles_n = ceil_div_i(C, TC_BN);
-    pl.dinp_tiles_m = ceil_div_i(BT, TC_BM);
-    pl.dw_tiles_m = ceil_div_i(OC, TC_BM);
+    pl.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
+    pl.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
     pl.dinp_kb = ceil_div_i(OC, TC_BK);
     pl.dw_kb = ceil_div_i(BT, TC_BK);
     pl.n_dinp_items = pl.dinp_tiles_m * pl.tiles_n;
     const int dw_tiles = pl.dw_tiles_m * pl.tiles_n;
-    num_sms = std::max(1, std::min(num_sms, 4096));
+    const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
 
+    // A forced split count that would leave an empty split is lowered to the
+    // nearest count that does not; a forced grid is rounded down to whole pairs.
     const long force_splits = env_long("MMBWD_SPLITK", 0);
-    const long force_grid = env_long("MMBWD_GRID", 0);
+    const long force_pairs = env_long("MMBWD_GRID", 0) / 2;
     const int max_splits = std::max(1, std::min(pl.dw_kb, 16));
     double best = 1e300;
-    TcPlan best_pl = pl;
-    for (int S = 1; S <= max_splits; ++S) {
-        if (force_splits > 0 && S != std::min<long>(force_splits, max_splits)) continue;
-        const int kps = ceil_div_i(pl.dw_kb, S);
-        if (ceil_div_i(pl.dw_kb, kps) != S) continue;  // would leave an empty split
-        for (int dw_first = 1; dw_first >= 0; --dw_first) {
-            for (int snake = 0; snake <= 1; ++snake) {
-                TcPlan c = pl;
-                c.splits = S;
-                c.kb_per_split = kps;
-                c.n_dw_items = dw_tiles * S;
-                c.n_items = c.n_dw_items + c.n_dinp_items;
-                c.dw_first = dw_first;
-                c.snake = snake;
-                c.grid = std::max(1, std::min(c.n_items, num_sms));
-                if (force_grid > 0) c.grid = static_cast<int>(std::min<long>(force_grid, c.grid));
-                const double cost = schedule_cost(c, c.grid) * (1.0 + 0.01 * (S - 1));
-                if (cost < best - 1e-9) {
-                    best = cost;
-                    best_pl = c;
-                }
-            }
+    static thread_local TcPlan best_pl, c;
+    int prev_S = 0;
+    for (int s_try = 1; s_try <= max_splits; ++s_try) {
+        const int kps = ceil_div_i(pl.dw_kb, s_try);
+        const int S = ceil_div_i(pl.dw_kb, kps);  // every split non-empty
+        if (S == prev_S) continue;
+        prev_S = S;
+        if (force_splits > 0 &&
+            S != ceil_div_i(pl.dw_kb, ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
+            continue;
+        c = pl;
+        c.splits = S;
+        c.kb_per_split = kps;
+        c.n_dw_items = dw_tiles * S;
+        c.n_items = c.n_dw_items + c.n_dinp_items;
+        int pairs = std::max(1, std::min(c.n_items, max_pairs));
+        if (force_pairs > 0) pairs = static_cast<int>(std::min<long>(force_pairs, pairs));
+        c.grid = 2 * pairs;
+        c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
+        const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
+        c.est_us = cost;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_pl = c;
         }
     }
     pl = best_pl;
+    pl.fixup_grid = 0;
     if (pl.splits > 1) {
-        pl.ws_partials_bytes = align256(static_cast<size_t>(dw_tiles) * pl.splits * TC_BM * TC_BN * 4);
-        pl.ws_bias_bytes = align256(static_cast<size_t>(pl.dw_tiles_m) * pl.splits * TC_BM * 4);
-        pl.ws_counter_bytes = align256(static_cast<size_t>(dw_tiles) * 4);
+        const int64_t nvec = OC * (C / 8);
+        pl.fixup_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, 8 * std::max(2, num_sms))));
+    }
+    if (pl.splits > 1) {
+        const size_t half_tiles = static_cast<size_t>(2 * pl.dw_tiles_m) * pl.tiles_n;
+        pl.ws_partials_bytes = align256(half_tiles * pl.splits * TC_BM * TC_BN * 4);
+        pl.ws_bias_bytes = align256(static_cast<size_t>(2 * pl.dw_tiles_m) * pl.splits * TC_BM * 4);
     }
     return pl;
 }
@@ -747,15 +876,27 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     p.n_dw_items = plan.n_dw_items;
     p.n_dinp_items = plan.n_dinp_items;
     p.n_items = plan.n_items;
-    p.dw_first = plan.dw_first;
-    p.snake = plan.snake;
+    p.table = plan.table;
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
     p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
-    p.counters = plan.splits > 1 ? reinterpret_cast<int*>(w + plan.ws_partials_bytes + plan.ws_bias_bytes) : nullptr;
     p.timeout_ns = static_cast<unsigned long long>(env_long("MMBWD_WAIT_TIMEOUT_NS", static_cast<long>(DEFAULT_TIMEOUT_NS)));
 
-    tc_mmbwd_kernel<<<plan.grid, TC_THREADS, SMEM_TOTAL, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_TOTAL;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel, maps[0], maps[1], maps[2], maps[3], p, plan.sched);
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    tc_splitk_fixup_kernel<<<plan.fixup_grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

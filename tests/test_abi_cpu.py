@@ -93,9 +93,11 @@ def test_plan_is_a_pure_function_of_shape():
         assert a == b
         BT = B * T
         tiles_n = -(-C // 256)
-        assert a["path"] == 1 and 1 <= a["grid"] <= 152
-        assert a["dinp_tiles"] == -(-BT // 128) * tiles_n
-        assert a["dweight_tiles"] == -(-OC // 128) * tiles_n
+        # CTA pairs: 256 x 256 tiles, an even grid
+        assert a["path"] == 1 and 2 <= a["grid"] <= 152 and a["grid"] % 2 == 0
+        assert a["dinp_tiles"] == -(-BT // 256) * tiles_n
+        assert a["dweight_tiles"] == -(-OC // 256) * tiles_n
+        assert a["grid"] // 2 <= a["items"]
         assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"] * a["splits"]
         kb = -(-BT // 64)
         # every split is non-empty and together they cover the reduction
@@ -110,7 +112,12 @@ def test_split_override_from_environment(monkeypatch):
     monkeypatch.setenv("MMBWD_SPLITK", "3")
     monkeypatch.setenv("MMBWD_GRID", "5")
     a = mm.mmbwd_plan_info(1, 1000, 264, 392, mm.BF16, 152)
-    assert a["splits"] == 3 and a["grid"] == 5
+    assert a["splits"] == 3 and a["grid"] == 4  # rounded down to whole CTA pairs
+    # a forced count that would leave an empty split is lowered, never dropped:
+    # 16 k-blocks in 5 splits of 4 would leave the fifth empty, so 4 splits
+    monkeypatch.setenv("MMBWD_SPLITK", "5")
+    a = mm.mmbwd_plan_info(1, 1024, 264, 392, mm.BF16, 152)
+    assert a["splits"] == 4 and a["kb_per_split"] == 4 and a["items"] > 0
     monkeypatch.delenv("MMBWD_SPLITK")
     monkeypatch.delenv("MMBWD_GRID")
 
@@ -122,10 +129,10 @@ def test_workspace_size_formula():
         B, T, C, OC = 1, 1000, 264, 392
         info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
         ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
-        tiles = info["dweight_tiles"]
+        half_tiles = 2 * info["dweight_tiles"]  # per-CTA 128-row halves of the pair tiles
         align = lambda x: (x + 255) // 256 * 256  # noqa: E731
-        want = (align(tiles * 2 * 128 * 256 * 4) + align(-(-OC // 128) * 2 * 128 * 4) +
-                align(tiles * 4))
+        want = align(half_tiles * 2 * 128 * 256 * 4) + align(2 * -(-OC // 256) * 2 * 128 * 4)
+        assert info["launches"] == 2  # the split reduction is a second kernel
         assert ws == want
     finally:
         del _os.environ["MMBWD_SPLITK"]

@@ -104,14 +104,17 @@ def test_split_reduction_and_schedule(monkeypatch, splits):
     B, T, C, OC = 1, 1000, 264, 392
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-2)
     monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+    kb = -(-B * T // 64)
+    want_splits = -(-kb // -(-kb // splits))  # lowered so that no split is empty
     outs = []
-    for grid in (0, 1, 3, 7):
+    for grid in (0, 2, 6, 14):
         if grid:
             monkeypatch.setenv("MMBWD_GRID", str(grid))
         else:
             monkeypatch.delenv("MMBWD_GRID", raising=False)
         info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
-        assert info["splits"] == splits
+        assert info["splits"] == want_splits
+        assert grid == 0 or info["grid"] == grid
         g, _ = check_full(x, B, T, C, OC, "bf16")
         outs.append({k: to_host(g[k], "bf16") for k in ("dinp", "dweight", "dbias")})
     for o in outs[1:]:
