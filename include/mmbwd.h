@@ -141,6 +141,42 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
 /* Test hook: make the next `n` workspace allocations fail (MMBWD_ERR_ALLOC). */
 void mmbwd_debug_fail_next_alloc(int n);
 
+/* Size of the library's fixed scratch buffer used by mmbwd_run_static_scratch. */
+#define MMBWD_STATIC_SCRATCH_BYTES (32u << 20)
+#define MMBWD_ERR_SCRATCH (-11) /* the problem needs more scratch than that buffer holds */
+
+/*
+ * mmbwd_run_static_scratch -- the same operation, arguments, layout, errors and
+ * results as mmbwd_run, for callers that must not allocate device memory.
+ * The paper has no counterpart: this entry point exists only for such callers.
+ *
+ * Who needs it: code that runs where device allocation is unavailable or not
+ * allowed -- inside a custom allocator or memory-pool callback (allocating
+ * there re-enters the allocator), under a hard device-memory budget that was
+ * fixed up front, or in a runtime that forbids cudaMalloc after start-up
+ * because it synchronises the device. mmbwd_run may grow a workspace with
+ * cudaMalloc; this entry point never calls cudaMalloc, cudaFree or any other
+ * allocating routine.
+ *
+ * Instead, the split reduction of the bf16 path uses one fixed buffer of
+ * MMBWD_STATIC_SCRATCH_BYTES compiled into the library (a file-scope device
+ * array, so every GPU that loads the library holds it until the process
+ * exits). A problem whose work split needs more than that returns
+ * MMBWD_ERR_SCRATCH and enqueues nothing; mmbwd_workspace_bytes() tells the
+ * need in advance. Nothing in the buffer has to start at zero: every value a
+ * call reads there is written earlier by the same call.
+ *
+ * All calls on a device share the one buffer, which keeps whatever the last
+ * call left in it: calls that overlap on the GPU (for example on two streams
+ * with nothing ordering them) race on it and give wrong results.
+ *
+ * The first call on each device looks up the buffer's device address (with
+ * that device current); make that first call before any stream capture.
+ */
+int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias_or_null, const void* dout,
+                             const void* inp, const void* weight, int64_t B, int64_t T, int64_t C,
+                             int64_t OC, int dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

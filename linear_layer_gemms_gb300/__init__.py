@@ -26,6 +26,8 @@ BF16 = 1
 OK = 0
 ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_ALIAS = -1, -2, -3, -4, -5
 ERR_ALLOC, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_ARCH, ERR_CAPTURE = -6, -7, -8, -9, -10
+ERR_SCRATCH = -11
+STATIC_SCRATCH_BYTES = 32 << 20  # MMBWD_STATIC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmmbwd.so")
@@ -43,6 +45,7 @@ SIGNATURES = {
     "mmbwd_plan_info": ([_i64] * 4 + [_ci, _ci, ctypes.POINTER(_ci), _ci], _ci),
     "mmbwd_selftest_wait_timeout": ([_u64], _ci),
     "mmbwd_debug_fail_next_alloc": ([_ci], None),
+    "mmbwd_run_static_scratch": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
 }
 
 _lock = threading.Lock()
@@ -93,6 +96,18 @@ def mmbwd_run(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, O
     """Enqueue one backward pass; returns the C status code (0 = OK)."""
     return load().mmbwd_run(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp),
                             _ptr(weight), B, T, C, OC, dtype, _stream(stream))
+
+
+def mmbwd_run_static_scratch(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, OC: int,
+                             dtype: int, stream=None) -> int:
+    """Like mmbwd_run, but never allocates device memory: for callers that
+    cannot (inside an allocator callback, under a fixed memory budget, or in a
+    runtime that forbids cudaMalloc once running). Its split reduction uses the
+    library's fixed STATIC_SCRATCH_BYTES buffer, shared by every call on the
+    device, so overlapping calls race; larger needs return ERR_SCRATCH."""
+    return load().mmbwd_run_static_scratch(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout),
+                                           _ptr(inp), _ptr(weight), B, T, C, OC, dtype,
+                                           _stream(stream))
 
 
 def mmbwd_workspace_bytes(B: int, T: int, C: int, OC: int, dtype: int) -> int:

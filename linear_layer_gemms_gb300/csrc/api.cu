@@ -194,6 +194,7 @@ const char* mmbwd_strerror(int code) {
         case MMBWD_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
         case MMBWD_ERR_ARCH: return "the current device is not sm_103 (GB300)";
         case MMBWD_ERR_CAPTURE: return "the workspace must grow but the stream is being captured";
+        case MMBWD_ERR_SCRATCH: return "the problem needs more scratch than the library's fixed buffer holds";
         default: return "unknown status code";
     }
 }
@@ -341,3 +342,88 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns) {
 void mmbwd_debug_fail_next_alloc(int n) { g_fail_allocs.store(n < 0 ? 0 : n); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// mmbwd_run_static_scratch: the backward pass without any device allocation.
+// The split partials of the bf16 path live in a fixed file-scope device array
+// instead of the grown workspace. In host code `g_static_scratch` only names
+// a host-side stand-in, so its device address is looked up once per device
+// with cudaGetSymbolAddress and that address is what the kernels receive.
+namespace mmbwd {
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[MMBWD_STATIC_SCRATCH_BYTES];
+void* g_static_scratch_addr[kMaxDevices];  // device address per device, set on first use
+
+// The argument checks of mmbwd_run, for this entry point.
+int check_run_args(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+                   int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, Shape* s) {
+    const int rc = check_shape(B, T, C, OC, dtype, s);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = s->es;
+    const size_t b_dinp = static_cast<size_t>(s->n_dinp) * es, b_dw = static_cast<size_t>(s->n_dw) * es,
+                 b_db = static_cast<size_t>(OC) * es, b_dout = static_cast<size_t>(s->n_dout) * es;
+    if ((b_dinp && !dinp) || (b_dw && !dweight) || (b_dout && !dout) || (b_dinp && !inp) || (b_dw && !weight))
+        return MMBWD_ERR_NULL;
+    const void* ptrs[6] = {dinp, dweight, dbias, dout, inp, weight};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0 || (static_cast<size_t>(OC) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+    const void* outs[3] = {dinp, dweight, dbias};
+    const size_t nouts[3] = {b_dinp, b_dw, b_db};
+    const void* ins[3] = {dout, inp, weight};
+    const size_t nins[3] = {b_dout, b_dinp, b_dw};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return MMBWD_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return MMBWD_ERR_ALIAS;
+    }
+    return MMBWD_OK;
+}
+
+}  // namespace
+}  // namespace mmbwd
+
+extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp,
+                                        const void* weight, int64_t B, int64_t T, int64_t C, int64_t OC, int dtype,
+                                        cudaStream_t stream) {
+    Shape s;
+    int rc = check_run_args(dinp, dweight, dbias, dout, inp, weight, B, T, C, OC, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    if (!g_static_scratch_addr[dev]) {  // first call on this device: it is the current device
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) {
+            cudaGetLastError();
+            return MMBWD_ERR_CUDA;
+        }
+        g_static_scratch_addr[dev] = addr;
+    }
+
+    cudaError_t e = cudaSuccess;
+    if (OC == 0) return MMBWD_OK;
+    if (s.BT == 0) {
+        if (dbias) e = cudaMemsetAsync(dbias, 0, static_cast<size_t>(OC) * s.es, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    if (C == 0) {
+        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    if (dtype == MMBWD_F32) {  // the fp32 path uses no scratch at all
+        e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                        static_cast<const float*>(dout), static_cast<const float*>(inp),
+                        static_cast<const float*>(weight), s.BT, C, OC, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms);
+    if (plan.ws_bytes() > MMBWD_STATIC_SCRATCH_BYTES) return MMBWD_ERR_SCRATCH;
+    e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, g_static_scratch_addr[dev], stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}

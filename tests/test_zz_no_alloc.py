@@ -1,0 +1,96 @@
+"""mmbwd_run_static_scratch -- the entry point that allocates nothing.
+
+Some callers cannot allocate device memory: code running inside an allocator
+or memory-pool callback (allocating there would re-enter the allocator),
+programs held to a device-memory budget fixed at start-up, or runtimes that
+forbid cudaMalloc once running because it synchronises the device. For them
+this entry point takes the split partials of the bf16 path from a fixed
+buffer compiled into the library instead of growing a workspace.
+
+Each test runs both entry points from identical buffers, twice in a row, and
+compares the outputs after each call. The file is named so that pytest
+collects it last.
+"""
+import numpy as np
+import pytest
+
+import linear_layer_gemms_gb300 as mm
+import synth
+from gpu_helpers import TOL, scaled_error, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    mm.load()
+    yield
+
+
+# (B, T, C, OC, forced splits): a forced 3-way split with ragged tiles, the
+# attention-projection shape whose own plan splits dweight, and a small shape
+# whose plan needs no scratch at all.
+CASES = [(1, 1000, 264, 392, "3"), (8, 1024, 768, 768, ""), (2, 100, 136, 264, "1")]
+
+
+def _call(fn, t, layer):
+    return fn(t["dinp"], t["dweight"], t["dbias"], t["dout"], t["inp"], t["weight"], layer.B, layer.T,
+              layer.C, layer.OC, mm.BF16)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:4])) + (f"-s{c[4]}" if c[4] else ""))
+def test_matches_mmbwd_run_on_two_calls_in_a_row(monkeypatch, case):
+    import torch
+
+    B, T, C, OC, splits = case
+    if splits:
+        monkeypatch.setenv("MMBWD_SPLITK", splits)
+    else:
+        monkeypatch.delenv("MMBWD_SPLITK", raising=False)
+    monkeypatch.delenv("MMBWD_GRID", raising=False)
+    layer = synth.Layer("no_alloc", B, T, C, OC, "bf16", True, init_std=0.01, dout_std=1e-2, layer=3)
+    x = synth.make_inputs(layer, seed=11)
+    info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 0)
+    needs_scratch = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16) > 0
+    assert needs_scratch == (info["splits"] > 1)
+    assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16) <= mm.STATIC_SCRATCH_BYTES
+    ref = {k: to_dev(v, "bf16") for k, v in x.items()}
+    got = {k: to_dev(v, "bf16") for k, v in x.items()}
+    for call in range(2):
+        assert _call(mm.mmbwd_run, ref, layer) == mm.OK
+        assert _call(mm.mmbwd_run_static_scratch, got, layer) == mm.OK
+        torch.cuda.synchronize()
+        assert mm.mmbwd_device_status()[0] == mm.OK
+        for name in ("dinp", "dweight", "dbias"):
+            a, b = to_host(ref[name], "bf16"), to_host(got[name], "bf16")
+            err = scaled_error(b, a)
+            assert err <= TOL["bf16"], (call, name, err)
+            # same plan and same kernels: the results are in fact identical
+            assert np.array_equal(a, b), (call, name)
+
+
+def test_rejects_a_split_that_does_not_fit_and_enqueues_nothing(monkeypatch):
+    import torch
+
+    B, T, C, OC = 1, 1024, 4096, 4096
+    monkeypatch.setenv("MMBWD_SPLITK", "4")
+    monkeypatch.delenv("MMBWD_GRID", raising=False)
+    assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16) > mm.STATIC_SCRATCH_BYTES
+    dev = torch.device("cuda:0")
+    t = {"dinp": torch.zeros(B * T, C, dtype=torch.bfloat16, device=dev),
+         "dweight": torch.zeros(OC, C, dtype=torch.bfloat16, device=dev),
+         "dbias": torch.full((OC,), 3.0, dtype=torch.bfloat16, device=dev),
+         "dout": torch.ones(B * T, OC, dtype=torch.bfloat16, device=dev),
+         "inp": torch.ones(B * T, C, dtype=torch.bfloat16, device=dev),
+         "weight": torch.ones(OC, C, dtype=torch.bfloat16, device=dev)}
+    layer = synth.Layer("too_big", B, T, C, OC, "bf16", True)
+    assert _call(mm.mmbwd_run_static_scratch, t, layer) == mm.ERR_SCRATCH
+    torch.cuda.synchronize()
+    assert bool((t["dinp"] == 0).all()) and bool((t["dweight"] == 0).all())
+    assert bool((t["dbias"] == 3.0).all())
+    assert "scratch" in mm.strerror(mm.ERR_SCRATCH)
