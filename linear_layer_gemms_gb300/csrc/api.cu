@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 
@@ -48,9 +49,10 @@ std::atomic<int> g_fail_allocs{0};
 struct PlanKey {
     int64_t BT, C, OC;
     int sms;
-    long splitk, grid;
+    long splitk, grid, tile_n;
     bool operator==(const PlanKey& o) const {
-        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && splitk == o.splitk && grid == o.grid;
+        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && splitk == o.splitk && grid == o.grid &&
+               tile_n == o.tile_n;
     }
 };
 constexpr int kPlanCache = 32;
@@ -63,9 +65,16 @@ long env_long(const char* name) {
     return (s && *s) ? std::strtol(s, nullptr, 10) : 0;
 }
 
+// "<dinp>,<dweight>" tile-width override as one number for the cache key.
+long env_tile_n() {
+    const char* s = std::getenv("MMBWD_TILE_N");
+    int a = 0, b = 0;
+    return (s && std::sscanf(s, "%d,%d", &a, &b) == 2) ? 1000L * a + b : 0;
+}
+
 // Caller holds g_mutex.
 const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms) {
-    const PlanKey k{BT, C, OC, sms, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID")};
+    const PlanKey k{BT, C, OC, sms, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n()};
     for (int i = 0; i < g_plan_count; ++i)
         if (g_plan_keys[i] == k) return g_plans[i];
     const int slot = g_plan_next;
@@ -219,7 +228,7 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     const int rc = check_shape(B, T, C, OC, dtype, &s);
     if (rc != MMBWD_OK) return rc;
     if (!out || n < 0) return MMBWD_ERR_NULL;
-    int v[13] = {0};
+    int v[14] = {0};
     if (num_sms <= 0) {  // the current device's resident CTAs (a full GB300 without a device)
         std::lock_guard<std::mutex> g(g_mutex);
         DeviceState* d = nullptr;
@@ -228,17 +237,17 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     }
     if (dtype == MMBWD_BF16) {
         const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms);
-        const int vals[13] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
+        const int vals[14] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
                               pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.table,
-                              TC_PAIR_BM, TC_BN, TC_BK, TC_STAGES, pl.launches()};
-        for (int i = 0; i < 13; ++i) v[i] = vals[i];
+                              TC_PAIR_BM, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches()};
+        for (int i = 0; i < 14; ++i) v[i] = vals[i];
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
         const int go = static_cast<int>((OC + SIMT_BM - 1) / SIMT_BM);
-        const int vals[13] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BK, 2, 2};
-        for (int i = 0; i < 13; ++i) v[i] = vals[i];
+        const int vals[14] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BN, SIMT_BK, 2, 2};
+        for (int i = 0; i < 14; ++i) v[i] = vals[i];
     }
-    const int m = n < 13 ? n : 13;
+    const int m = n < 14 ? n : 14;
     for (int i = 0; i < m; ++i) out[i] = v[i];
     return m;
 }

@@ -18,7 +18,7 @@ namespace mmbwd {
 // rows of A and 128 columns of B, 64 elements of K per pipeline stage.
 constexpr int TC_BM = 128;       // rows per CTA
 constexpr int TC_PAIR_BM = 256;  // rows per CTA pair
-constexpr int TC_BN = 256;       // columns per tile (128 staged by each CTA)
+constexpr int TC_BN = 256;       // widest tile (N of one MMA); each CTA stages half of the columns
 constexpr int TC_BK = 64;
 constexpr int TC_STAGES = 6;
 constexpr int TC_THREADS = 256;
@@ -53,15 +53,18 @@ struct TcSchedule {
 // the least work so far (`table` = 1); when a list is too long for the
 // parameter table, pairs take items round-robin instead (`table` = 0).
 struct TcPlan {
-    int tiles_n;       // ceil(C / BN), shared by both products (N = C for both)
+    int dinp_bn;       // tile width of the dinp product (128 or 256 columns of C)
+    int dw_bn;         // tile width of the dweight product
+    int dinp_tiles_n;  // ceil(C / dinp_bn)
+    int dw_tiles_n;    // ceil(C / dw_bn)
     int dinp_tiles_m;  // ceil(BT / PAIR_BM): row tiles of dinp, one per CTA pair
     int dw_tiles_m;    // ceil(OC / PAIR_BM): row tiles of dweight, one per CTA pair
     int dinp_kb;       // ceil(OC / BK)
     int dw_kb;         // ceil(BT / BK)
     int splits;        // K splits of the dweight product
     int kb_per_split;  // k-blocks per split (the last may have fewer)
-    int n_dw_items;    // dw_tiles_m * tiles_n * splits
-    int n_dinp_items;  // dinp_tiles_m * tiles_n
+    int n_dw_items;    // dw_tiles_m * dw_tiles_n * splits
+    int n_dinp_items;  // dinp_tiles_m * dinp_tiles_n
     int n_items;
     int table;         // 1: per-pair item lists in `sched`; 0: round-robin
     int grid;          // CTAs (twice the number of CTA pairs)
@@ -79,9 +82,10 @@ struct TcParams {
     __nv_bfloat16* dinp;
     __nv_bfloat16* dweight;
     __nv_bfloat16* dbias;  // may be null
-    int tiles_n, dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
+    int dinp_bn, dw_bn, dinp_tiles_n, dw_tiles_n;
+    int dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
     int n_dw_items, n_dinp_items, n_items, table;
-    float* partials;       // [dw half tile][split][BM][BN]; half tile = 128-row tile x column tile
+    float* partials;       // [dw half tile][split][BM][dw_bn]; half tile = 128-row tile x column tile
     float* bias_partials;  // [dw 128-row tile][split][BM]
     unsigned long long timeout_ns;
 };

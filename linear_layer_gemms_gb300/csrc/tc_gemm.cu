@@ -64,7 +64,7 @@ __device__ unsigned int g_status[4];
 namespace {
 
 constexpr int A_BYTES = TC_BM * TC_BK * 2;            // 16 KB: this CTA's 128 rows of A
-constexpr int B_BYTES = (TC_BN / 2) * TC_BK * 2;      // 16 KB: this CTA's 128 columns of B
+constexpr int B_BYTES = (TC_BN / 2) * TC_BK * 2;      // 16 KB: room for this CTA's (up to) 128 columns of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // 32 KB
 constexpr int BOX_BYTES = 64 * TC_BK * 2;             // 8 KB: 64 (MN) x 64 (K) bf16, MN-major
 constexpr int ROW_BYTES = 128;                        // one swizzled 128-byte row
@@ -96,8 +96,6 @@ constexpr int SMEM_USED = OFF_STAGE + NUM_EPI_WARPS * STG_WARP_BYTES;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t IDESC_DINP = ptx::idesc_bf16_f32(TC_PAIR_BM, TC_BN, /*A MN*/ 0, /*B MN*/ 1);
-constexpr uint32_t IDESC_DW = ptx::idesc_bf16_f32(TC_PAIR_BM, TC_BN, /*A MN*/ 1, /*B MN*/ 1);
 
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per wait
 
@@ -156,7 +154,8 @@ struct Waiter {
 struct Item {
     int is_dw;
     int pm;      // row tile of the pair (256 rows)
-    int n_tile;  // column tile (256 columns)
+    int n_tile;  // column tile (bn columns)
+    int bn;      // tile width: 128 or 256
     int split;
     int kb0, kb1;  // k-block range [kb0, kb1)
 };
@@ -165,8 +164,10 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
     Item it;
     it.is_dw = w < p.n_dw_items ? 1 : 0;
     const int local = it.is_dw ? w : w - p.n_dw_items;
-    it.n_tile = local % p.tiles_n;
-    const int rest = local / p.tiles_n;
+    const int tiles_n = it.is_dw ? p.dw_tiles_n : p.dinp_tiles_n;
+    it.bn = it.is_dw ? p.dw_bn : p.dinp_bn;
+    it.n_tile = local % tiles_n;
+    const int rest = local / tiles_n;
     if (it.is_dw) {
         it.pm = rest % p.dw_tiles_m;
         it.split = rest / p.dw_tiles_m;
@@ -214,6 +215,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_weight,   // weight, B of dinp (MN-major)
                     const __grid_constant__ CUtensorMap tm_dout_mn,  // dout, A of dweight (MN-major)
                     const __grid_constant__ CUtensorMap tm_inp,      // inp, B of dweight (MN-major)
+                    const __grid_constant__ CUtensorMap tm_dinp_out, // dinp, for L2 prefetch of old values
+                    const __grid_constant__ CUtensorMap tm_dw_out,   // dweight, likewise
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -262,6 +265,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ptx::prefetch_tmap(&tm_weight);
             ptx::prefetch_tmap(&tm_dout_mn);
             ptx::prefetch_tmap(&tm_inp);
+            ptx::prefetch_tmap(&tm_dinp_out);
+            ptx::prefetch_tmap(&tm_dw_out);
             uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
             bool ok = true;
             for (int r = 0; ok; ++r) {
@@ -272,8 +277,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // tensor are skipped: they would only feed accumulator rows or
                 // columns that are never stored.
                 const int row0 = it.pm * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
-                const int col0 = it.n_tile * TC_BN + static_cast<int>(rank) * (TC_BN / 2);
-                const int nb = (col0 < p.C ? 1 : 0) + (col0 + 64 < p.C ? 1 : 0);
+                const int half = it.bn / 2;  // columns of B staged by this CTA
+                const int col0 = it.n_tile * it.bn + static_cast<int>(rank) * half;
+                int nb = 0;
+                for (int j = 0; j < half / 64; ++j) nb += (col0 + j * 64 < p.C) ? 1 : 0;
+                // Output tile of this CTA, prefetched into L2 a few k-blocks before the
+                // main loop ends so that the epilogue's read of the old values hits L2.
+                const bool direct = !(it.is_dw && p.splits > 1);
+                const int64_t out_rows = it.is_dw ? p.OC : p.BT;
+                const int pf_kb = max(it.kb0, it.kb1 - 8);
                 int na;
                 if (it.is_dw) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
                 else na = row0 < p.BT ? 1 : 0;
@@ -288,6 +300,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t sB = sA + A_BYTES;
                     const uint32_t fb = bars + 8u * (BAR_FULL + stage);
                     ptx::mbar_arrive_expect_tx(fb, bytes);
+                    if (direct && kb == pf_kb && row0 < out_rows) {
+                        for (int j = 0; j < it.bn / 128; ++j)
+                            if (it.n_tile * it.bn + j * 128 < p.C)
+                                ptx::tma_prefetch_l2_2d(it.is_dw ? &tm_dw_out : &tm_dinp_out,
+                                                        it.n_tile * it.bn + j * 128, row0);
+                    }
                     if (it.is_dw) {
                         for (int j = 0; j < na; ++j)
                             ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * TC_BK);
@@ -326,7 +344,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * TC_BN;
-                    const uint32_t idesc = it.is_dw ? IDESC_DW : IDESC_DINP;
+                    const uint32_t idesc = ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw, /*B MN*/ 1);
                     for (int kb = it.kb0; kb < it.kb1; ++kb) {
                         // Both CTAs' copies of this stage have landed (own bytes +
                         // the odd CTA's forwarded arrival).
@@ -482,8 +500,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const bool split_mode = it.is_dw && p.splits > 1;
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
             const int64_t qrow0 = static_cast<int64_t>(m_tile) * TC_BM + q * 32;  // first row of the quadrant
-            const int col0 = it.n_tile * TC_BN;
-            const int ncols = static_cast<int>(min(static_cast<int64_t>(TC_BN), p.C - col0));
+            const int col0 = it.n_tile * it.bn;
+            const int ncols = static_cast<int>(min(static_cast<int64_t>(it.bn), p.C - col0));
+            const int nchunks = it.bn / 32;
             __nv_bfloat16* D = it.is_dw ? p.dweight : p.dinp;
             bool rok[4];
             __nv_bfloat16* drow[4];
@@ -493,19 +512,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 rok[i] = row < rows_total;
                 drow[i] = D + (rok[i] ? row : 0) * p.C + col0 + cg;
             }
-            // Old output values, four 32-column chunks ahead of their use.
-            uint4 oldw[4][4];
-            auto prefetch = [&](int c) {
+            // All old output values of this tile, loaded before waiting for the
+            // accumulator (the producer has prefetched them into L2).
+            uint4 oldw[TC_BN / 32][4];
+#pragma unroll
+            for (int c = 0; c < TC_BN / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    oldw[c & 3][i] = (rok[i] && c * 32 + cg < ncols)
-                                         ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-            };
-            if (!split_mode) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) prefetch(c);
-            }
+                    oldw[c][i] = (!split_mode && c < nchunks && rok[i] && c * 32 + cg < ncols)
+                                     ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
+                                     : make_uint4(0u, 0u, 0u, 0u);
 
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
@@ -518,12 +534,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 bias_val = bias_smem[acc * TC_BM + rit];
             }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
-            // Partial tile of this split: [128 rows][256 columns] fp32, row-major.
-            float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.tiles_n + it.n_tile) * p.splits +
-                                                     it.split) * (TC_BM * TC_BN)
+            // Partial tile of this split: [128 rows][dw_bn columns] fp32, row-major.
+            float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.dw_tiles_n + it.n_tile) * p.splits +
+                                                     it.split) * (TC_BM * p.dw_bn)
                                      : nullptr;
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c) {
+                if (c >= nchunks) break;
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
                 // Row `lane` of the quadrant into the staging buffer ...
@@ -540,16 +557,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const float4 a4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg) * 4);
                     const float4 b4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg + 4) * 4);
                     if (split_mode) {
-                        float* pp = part + static_cast<size_t>(q * 32 + lr) * TC_BN + c * 32 + cg;
+                        float* pp = part + static_cast<size_t>(q * 32 + lr) * p.dw_bn + c * 32 + cg;
                         __stcg(reinterpret_cast<float4*>(pp), a4);
                         __stcg(reinterpret_cast<float4*>(pp + 4), b4);
                     } else if (rok[i] && c * 32 + cg < ncols) {
                         const float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(oldw[c & 3][i], s8);
+                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(oldw[c][i], s8);
                     }
                 }
                 __syncwarp();
-                if (!split_mode && c + 4 < TC_BN / 32) prefetch(c + 4);
             }
             if (has_bias) {
                 const int64_t brow = static_cast<int64_t>(m_tile) * TC_BM + rit;
@@ -591,14 +607,14 @@ __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) 
     const int64_t vec_per_row = p.C / 8;
     const int64_t nvec = p.OC * vec_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const size_t tile_elems = static_cast<size_t>(TC_BM) * TC_BN;
+    const size_t tile_elems = static_cast<size_t>(TC_BM) * p.dw_bn;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
         const int64_t row = v / vec_per_row;
         const int64_t col = (v - row * vec_per_row) * 8;
         const int m_tile = static_cast<int>(row / TC_BM), rl = static_cast<int>(row % TC_BM);
-        const int n_tile = static_cast<int>(col / TC_BN), cl = static_cast<int>(col % TC_BN);
-        const float* pp = p.partials + static_cast<size_t>(m_tile * p.tiles_n + n_tile) * p.splits * tile_elems +
-                          static_cast<size_t>(rl) * TC_BN + cl;
+        const int n_tile = static_cast<int>(col / p.dw_bn), cl = static_cast<int>(col % p.dw_bn);
+        const float* pp = p.partials + static_cast<size_t>(m_tile * p.dw_tiles_n + n_tile) * p.splits * tile_elems +
+                          static_cast<size_t>(rl) * p.dw_bn + cl;
         float s8[8];
 #pragma unroll 4
         for (int sp = 0; sp < p.splits; ++sp) {
@@ -650,14 +666,15 @@ long env_long(const char* name, long dflt) {
     return (end && *end == '\0') ? v : dflt;
 }
 
-// Planner cost model (µs). An item costs its main loop (one 64-deep k-block of
-// a 256 x 256 pair tile is 512 tensor-core cycles, ~0.27 µs) or its epilogue,
-// whichever is longer, since the two overlap across the two accumulators; the
-// last item's epilogue is not overlapped. Split dweight adds the fixup pass.
-constexpr double T_KB = 0.27;       // one k-block of pair MMAs
-constexpr double T_RMW = 2.6;       // bf16 read-modify-write epilogue of a 128 x 256 half tile
-constexpr double T_PARTIAL = 1.8;   // fp32 partial store of a 128 x 256 half tile
-constexpr double T_ITEM = 0.3;      // per-item handoff
+// Planner cost model (µs), from per-item timelines on GB300 under load. An item
+// costs its main loop (a 64-deep k-block of a 256 x bn pair tile) or its
+// epilogue, whichever is longer, since the two overlap across the two
+// accumulators; the last item's epilogue is not overlapped. Split dweight adds
+// the fixup pass.
+double t_kb(int bn) { return bn == 256 ? 0.37 : 0.33; }  // a 128-wide tile is load-bound
+double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
+double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
+constexpr double T_ITEM = 0.3;                                 // per-item handoff
 
 struct ItemCost {
     double run, epi;
@@ -665,20 +682,22 @@ struct ItemCost {
 
 ItemCost item_cost(const TcPlan& pl, int w) {
     if (w < pl.n_dw_items) {
-        const int split = w / pl.tiles_n / pl.dw_tiles_m;
+        const int split = w / pl.dw_tiles_n / pl.dw_tiles_m;
         const int kb0 = split * pl.kb_per_split;
         const int kb = std::min(kb0 + pl.kb_per_split, pl.dw_kb) - kb0;
-        const double epi = pl.splits > 1 ? T_PARTIAL : T_RMW;
-        return {std::max(kb * T_KB, epi) + T_ITEM, epi};
+        const double epi = pl.splits > 1 ? t_partial(pl.dw_bn) : t_rmw(pl.dw_bn);
+        return {std::max(kb * t_kb(pl.dw_bn), epi) + T_ITEM, epi};
     }
-    return {std::max(pl.dinp_kb * T_KB, T_RMW) + T_ITEM, T_RMW};
+    const double epi = t_rmw(pl.dinp_bn);
+    return {std::max(pl.dinp_kb * t_kb(pl.dinp_bn), epi) + T_ITEM, epi};
 }
 
 double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
     if (pl.splits == 1) return 0.0;
-    // a launch gap plus S fp32 partials read and dweight read and written
+    // a launch gap plus S fp32 partials read and dweight read and written, and
+    // the partial stores; measured, the pass costs about twice the traffic time
     const double bytes = static_cast<double>(OC) * C * (4.0 * pl.splits + 4.0);
-    return 3.0 + bytes / 5.0e6;  // ~5 TB/s effective, in bytes per µs
+    return 6.0 + bytes / 2.5e6;
 }
 
 // Longest-first greedy assignment of items to pairs; fills pl.sched and
@@ -764,45 +783,63 @@ int tc_max_active_pairs() {
 
 TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     TcPlan pl{};
-    pl.tiles_n = ceil_div_i(C, TC_BN);
     pl.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
     pl.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
     pl.dinp_kb = ceil_div_i(OC, TC_BK);
     pl.dw_kb = ceil_div_i(BT, TC_BK);
-    pl.n_dinp_items = pl.dinp_tiles_m * pl.tiles_n;
-    const int dw_tiles = pl.dw_tiles_m * pl.tiles_n;
     const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
 
-    // A forced split count that would leave an empty split is lowered to the
-    // nearest count that does not; a forced grid is rounded down to whole pairs.
+    // Overrides (tuning, tests): a forced split count that would leave an
+    // empty split is lowered to the nearest count that does not; a forced grid
+    // is rounded down to whole pairs; MMBWD_TILE_N = "<dinp>,<dweight>" widths.
     const long force_splits = env_long("MMBWD_SPLITK", 0);
     const long force_pairs = env_long("MMBWD_GRID", 0) / 2;
+    int force_dinp_bn = 0, force_dw_bn = 0;
+    if (const char* t = std::getenv("MMBWD_TILE_N")) {
+        int a = 0, b = 0;
+        if (std::sscanf(t, "%d,%d", &a, &b) == 2 && (a == 128 || a == 256) && (b == 128 || b == 256)) {
+            force_dinp_bn = a;
+            force_dw_bn = b;
+        }
+    }
     const int max_splits = std::max(1, std::min(pl.dw_kb, 16));
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
-    int prev_S = 0;
-    for (int s_try = 1; s_try <= max_splits; ++s_try) {
-        const int kps = ceil_div_i(pl.dw_kb, s_try);
-        const int S = ceil_div_i(pl.dw_kb, kps);  // every split non-empty
-        if (S == prev_S) continue;
-        prev_S = S;
-        if (force_splits > 0 &&
-            S != ceil_div_i(pl.dw_kb, ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
-            continue;
-        c = pl;
-        c.splits = S;
-        c.kb_per_split = kps;
-        c.n_dw_items = dw_tiles * S;
-        c.n_items = c.n_dw_items + c.n_dinp_items;
-        int pairs = std::max(1, std::min(c.n_items, max_pairs));
-        if (force_pairs > 0) pairs = static_cast<int>(std::min<long>(force_pairs, pairs));
-        c.grid = 2 * pairs;
-        c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
-        const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
-        c.est_us = cost;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_pl = c;
+    for (int dinp_bn = 256; dinp_bn >= 128; dinp_bn -= 128) {
+        if (force_dinp_bn && dinp_bn != force_dinp_bn) continue;
+        for (int dw_bn = 256; dw_bn >= 128; dw_bn -= 128) {
+            if (force_dw_bn && dw_bn != force_dw_bn) continue;
+            int prev_S = 0;
+            for (int s_try = 1; s_try <= max_splits; ++s_try) {
+                const int kps = ceil_div_i(pl.dw_kb, s_try);
+                const int S = ceil_div_i(pl.dw_kb, kps);  // every split non-empty
+                if (S == prev_S) continue;
+                prev_S = S;
+                if (force_splits > 0 &&
+                    S != ceil_div_i(pl.dw_kb,
+                                    ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
+                    continue;
+                c = pl;
+                c.dinp_bn = dinp_bn;
+                c.dw_bn = dw_bn;
+                c.dinp_tiles_n = ceil_div_i(C, dinp_bn);
+                c.dw_tiles_n = ceil_div_i(C, dw_bn);
+                c.n_dinp_items = c.dinp_tiles_m * c.dinp_tiles_n;
+                c.splits = S;
+                c.kb_per_split = kps;
+                c.n_dw_items = c.dw_tiles_m * c.dw_tiles_n * S;
+                c.n_items = c.n_dw_items + c.n_dinp_items;
+                int pairs = std::max(1, std::min(c.n_items, max_pairs));
+                if (force_pairs > 0) pairs = static_cast<int>(std::min<long>(force_pairs, pairs));
+                c.grid = 2 * pairs;
+                c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
+                const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
+                c.est_us = cost;
+                if (cost < best - 1e-9) {
+                    best = cost;
+                    best_pl = c;
+                }
+            }
         }
     }
     pl = best_pl;
@@ -810,10 +847,8 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     if (pl.splits > 1) {
         const int64_t nvec = OC * (C / 8);
         pl.fixup_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, 8 * std::max(2, num_sms))));
-    }
-    if (pl.splits > 1) {
-        const size_t half_tiles = static_cast<size_t>(2 * pl.dw_tiles_m) * pl.tiles_n;
-        pl.ws_partials_bytes = align256(half_tiles * pl.splits * TC_BM * TC_BN * 4);
+        const size_t half_tiles = static_cast<size_t>(2 * pl.dw_tiles_m) * pl.dw_tiles_n;
+        pl.ws_partials_bytes = align256(half_tiles * pl.splits * TC_BM * pl.dw_bn * 4);
         pl.ws_bias_bytes = align256(static_cast<size_t>(2 * pl.dw_tiles_m) * pl.splits * TC_BM * 4);
     }
     return pl;
@@ -836,25 +871,28 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     EncodeTiledFn encode = get_encode_tiled();
     if (!encode) return cudaErrorNotSupported;
 
-    CUtensorMap maps[4];
+    CUtensorMap maps[6];
     struct MapSpec {
         const void* base;
         uint64_t inner, outer;
         uint32_t box_inner, box_outer;
-    } specs[4] = {
-        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), TC_BK, TC_BM},  // dout, K-major A
-        {weight, static_cast<uint64_t>(C), static_cast<uint64_t>(OC), 64, TC_BK},    // weight, MN-major B
-        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), 64, TC_BK},     // dout, MN-major A
-        {inp, static_cast<uint64_t>(C), static_cast<uint64_t>(BT), 64, TC_BK},       // inp, MN-major B
+        CUtensorMapSwizzle swz;
+    } specs[6] = {
+        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},  // dout, K-major A
+        {weight, static_cast<uint64_t>(C), static_cast<uint64_t>(OC), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},    // weight, MN-major B
+        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},     // dout, MN-major A
+        {inp, static_cast<uint64_t>(C), static_cast<uint64_t>(BT), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},       // inp, MN-major B
+        {dinp, static_cast<uint64_t>(C), static_cast<uint64_t>(BT), 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},     // dinp, L2 prefetch
+        {dweight, static_cast<uint64_t>(C), static_cast<uint64_t>(OC), 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},  // dweight, L2 prefetch
     };
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
         const cuuint64_t strides[1] = {specs[i].inner * 2};
         const cuuint32_t box[2] = {specs[i].box_inner, specs[i].box_outer};
         const cuuint32_t estr[2] = {1, 1};
         const CUresult r = encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(specs[i].base),
                                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  specs[i].swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
@@ -866,7 +904,10 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     p.dinp = static_cast<__nv_bfloat16*>(dinp);
     p.dweight = static_cast<__nv_bfloat16*>(dweight);
     p.dbias = static_cast<__nv_bfloat16*>(dbias);
-    p.tiles_n = plan.tiles_n;
+    p.dinp_bn = plan.dinp_bn;
+    p.dw_bn = plan.dw_bn;
+    p.dinp_tiles_n = plan.dinp_tiles_n;
+    p.dw_tiles_n = plan.dw_tiles_n;
     p.dinp_tiles_m = plan.dinp_tiles_m;
     p.dw_tiles_m = plan.dw_tiles_m;
     p.dinp_kb = plan.dinp_kb;
@@ -894,7 +935,8 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel, maps[0], maps[1], maps[2], maps[3], p, plan.sched);
+    e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                           plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     tc_splitk_fixup_kernel<<<plan.fixup_grid, 256, 0, stream>>>(p);
     return cudaGetLastError();

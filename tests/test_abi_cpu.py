@@ -92,11 +92,11 @@ def test_plan_is_a_pure_function_of_shape():
         b = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
         assert a == b
         BT = B * T
-        tiles_n = -(-C // 256)
-        # CTA pairs: 256 x 256 tiles, an even grid
+        # CTA pairs: 256-row tiles, 128 or 256 columns per product, an even grid
         assert a["path"] == 1 and 2 <= a["grid"] <= 152 and a["grid"] % 2 == 0
-        assert a["dinp_tiles"] == -(-BT // 256) * tiles_n
-        assert a["dweight_tiles"] == -(-OC // 256) * tiles_n
+        assert a["tile_n_dinp"] in (128, 256) and a["tile_n_dweight"] in (128, 256)
+        assert a["dinp_tiles"] == -(-BT // 256) * -(-C // a["tile_n_dinp"])
+        assert a["dweight_tiles"] == -(-OC // 256) * -(-C // a["tile_n_dweight"])
         assert a["grid"] // 2 <= a["items"]
         assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"] * a["splits"]
         kb = -(-BT // 64)
@@ -122,6 +122,15 @@ def test_split_override_from_environment(monkeypatch):
     monkeypatch.delenv("MMBWD_GRID")
 
 
+def test_tile_width_override(monkeypatch):
+    monkeypatch.setenv("MMBWD_TILE_N", "128,256")
+    a = mm.mmbwd_plan_info(8, 1024, 768, 3072, mm.BF16, 152)
+    assert (a["tile_n_dinp"], a["tile_n_dweight"]) == (128, 256)
+    monkeypatch.setenv("MMBWD_TILE_N", "256,128")
+    a = mm.mmbwd_plan_info(8, 1024, 768, 3072, mm.BF16, 152)
+    assert (a["tile_n_dinp"], a["tile_n_dweight"]) == (256, 128)
+
+
 def test_workspace_size_formula():
     import os as _os
     _os.environ["MMBWD_SPLITK"] = "2"
@@ -131,7 +140,8 @@ def test_workspace_size_formula():
         ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
         half_tiles = 2 * info["dweight_tiles"]  # per-CTA 128-row halves of the pair tiles
         align = lambda x: (x + 255) // 256 * 256  # noqa: E731
-        want = align(half_tiles * 2 * 128 * 256 * 4) + align(2 * -(-OC // 256) * 2 * 128 * 4)
+        want = (align(half_tiles * 2 * 128 * info["tile_n_dweight"] * 4) +
+                align(2 * -(-OC // 256) * 2 * 128 * 4))
         assert info["launches"] == 2  # the split reduction is a second kernel
         assert ws == want
     finally:

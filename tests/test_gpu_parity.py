@@ -204,3 +204,17 @@ def test_workspace_growth_refused_during_capture(monkeypatch):
         rc = mm.mmbwd_run(g["dinp"], g["dweight"], g["dbias"], g["dout"], g["inp"], g["weight"], B, T,
                           C, OC, mm.BF16, s.cuda_stream)
     assert rc == mm.ERR_CAPTURE
+
+
+@pytest.mark.parametrize("tile_n", ["128,128", "128,256", "256,128", "256,256"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_tile_widths(monkeypatch, tile_n, splits):
+    """Every tile width of each product, with and without a split dweight
+    reduction, on a shape with ragged rows and columns."""
+    B, T, C, OC = 2, 300, 392, 520
+    monkeypatch.setenv("MMBWD_TILE_N", tile_n)
+    monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+    info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+    assert f"{info['tile_n_dinp']},{info['tile_n_dweight']}" == tile_n
+    _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
+    check_full(x, B, T, C, OC, "bf16")
