@@ -58,6 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-other", action="store_true", help="skip the other configurations")
     return ap.parse_args(argv)
 
 
@@ -226,11 +227,11 @@ def oracle_sample(seconds: float, inputs=None, seed=0):
     # calibrate on a few rows, then size the sample
     rows0 = max(1, orc.threads)
     t0 = time.perf_counter()
-    flops0 = _oracle_rows(orc, wl, inputs, rows0)
+    _oracle_rows(orc, wl, inputs, rows0)
     cal = time.perf_counter() - t0
-    rate = flops0 / max(cal, 1e-6)
     budget = max(seconds - cal, 0.5)
-    rows = max(rows0, int(rows0 * budget * rate / max(flops0, 1)))
+    rows = max(rows0, int(rows0 * budget / max(cal, 1e-6)))
+    rows = min(rows, max(l.BT for l in wl.layers))
     t0 = time.perf_counter()
     flops = _oracle_rows(orc, wl, inputs, rows)
     dt = time.perf_counter() - t0
@@ -391,6 +392,10 @@ def run_gpu(args):
     if not args.no_e2e:
         e2e = run_e2e(torch, mm, wl, host, dev, stream, args.e2e_steps, barrier)
 
+    other = None
+    if not args.no_other and rank == 0:
+        other = measure_other_configs(torch, mm, dev, stream)
+
     if rank != 0:
         return 0
     cpu = None
@@ -418,6 +423,7 @@ def run_gpu(args):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "other_configs": other,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -425,6 +431,63 @@ def run_gpu(args):
 
         dist.destroy_process_group()
     return 0
+
+
+OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
+
+
+def measure_other_configs(torch, mm, dev, stream, reps=10):
+    """The remaining configurations of the workload set, each one mmbwd_run
+    call on device-resident inputs, timed with CUDA events (median of `reps`
+    launches after warm-up), reported with their plan and the fraction of the
+    peak that bounds them (bf16 tensor peak; the fp32 path against the FP32
+    ALU peak of 152 SMs x 128 lanes x 2 FLOP at the maximum SM clock)."""
+    peaks, _ = measured_peaks()
+    fp32_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    out = {}
+    for name in OTHER_CONFIGS:
+        layer = synth.WORKLOADS[name].layers[0]
+        x = synth.make_inputs(layer, seed=0)
+        t = {k: to_device_tensor(torch, v, dev) for k, v in x.items()}
+        dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
+
+        def call():
+            rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
+                              t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
+                              t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T, layer.C,
+                              layer.OC, dt, stream.cuda_stream)
+            if rc != mm.OK:
+                raise RuntimeError(mm.strerror(rc))
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                call()
+                b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+        sec = statistics.median(times)
+        tf = layer.flops() / sec / 1e12
+        peak = float(peaks["bf16_tflops"]) if layer.dtype == "bf16" else fp32_peak
+        info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
+        out[name] = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
+                     "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2),
+                     "frac_of_peak": round(tf / peak, 4),
+                     "peak": "bf16 tensor (measured)" if layer.dtype == "bf16" else
+                             f"fp32 ALU {fp32_peak:.1f} TFLOP/s (152 SMs x 128 lanes x 2 x max clock)",
+                     "plan": {k: info[k] for k in ("path", "grid", "items", "splits", "launches")}}
+        del t
+        torch.cuda.empty_cache()
+    status, info = mm.mmbwd_device_status(reset=True)
+    if status != mm.OK:
+        raise RuntimeError(f"device status after other configs: {mm.strerror(status)} {info}")
+    return out
 
 
 def run_e2e(torch, mm, wl, host, dev, stream, steps, barrier):
