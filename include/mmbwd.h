@@ -126,9 +126,11 @@ int mmbwd_version(void);
  * and the number of co-resident CTAs; num_sms <= 0 takes the current device's
  * value, or 152 without a usable device). out[0..n) receives, in order: path (0 = fp32 SIMT,
  * 1 = bf16 tensor-core), grid size (CTAs), work items, dweight splits, k-blocks
- * per split, dinp tiles, dweight tiles, schedule kind (1 = per-pair tables),
- * tile M, tile N of dinp, tile N of dweight, tile K, pipeline stages, kernel
- * launches per call. Returns the number of values written (at most 14), or a
+ * per split, dinp tiles, dweight tiles, schedule kind (1 = per-cluster tables),
+ * tile M (rows per cluster), tile N of dinp, tile N of dweight, tile K,
+ * pipeline stages, kernel launches per call, CTA pairs per cluster. num_sms
+ * stands for the resident CTAs; a quarter of it is taken as the resident
+ * 4-CTA clusters. Returns the number of values written (at most 15), or a
  * negative status. */
 int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms,
                     int* out, int n);

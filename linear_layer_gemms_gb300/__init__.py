@@ -138,7 +138,8 @@ def mmbwd_version() -> int:
 
 
 PLAN_FIELDS = ("path", "grid", "items", "splits", "kb_per_split", "dinp_tiles", "dweight_tiles",
-               "table", "tile_m", "tile_n_dinp", "tile_n_dweight", "tile_k", "stages", "launches")
+               "table", "tile_m", "tile_n_dinp", "tile_n_dweight", "tile_k", "stages", "launches",
+               "pairs_per_cluster")
 
 
 def mmbwd_plan_info(B: int, T: int, C: int, OC: int, dtype: int, num_sms: int = 0) -> dict:

@@ -36,6 +36,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     int arch_checked = 0;  // 0 unknown, 1 ok, -1 not sm_103
     int num_sms = 0;
+    int num_quads = 0;  // resident 4-CTA clusters (two CTA pairs each)
     void* ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -48,11 +49,11 @@ std::atomic<int> g_fail_allocs{0};
 // schedule search is cached so that a call costs a table lookup.
 struct PlanKey {
     int64_t BT, C, OC;
-    int sms;
-    long splitk, grid, tile_n;
+    int sms, quads;
+    long splitk, grid, tile_n, ppc;
     bool operator==(const PlanKey& o) const {
-        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && splitk == o.splitk && grid == o.grid &&
-               tile_n == o.tile_n;
+        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && quads == o.quads && splitk == o.splitk &&
+               grid == o.grid && tile_n == o.tile_n && ppc == o.ppc;
     }
 };
 constexpr int kPlanCache = 32;
@@ -73,15 +74,16 @@ long env_tile_n() {
 }
 
 // Caller holds g_mutex.
-const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms) {
-    const PlanKey k{BT, C, OC, sms, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n()};
+const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int quads) {
+    const PlanKey k{BT, C, OC, sms, quads, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n(),
+                    env_long("MMBWD_PPC")};
     for (int i = 0; i < g_plan_count; ++i)
         if (g_plan_keys[i] == k) return g_plans[i];
     const int slot = g_plan_next;
     g_plan_next = (g_plan_next + 1) % kPlanCache;
     if (g_plan_count < kPlanCache) ++g_plan_count;
     g_plan_keys[slot] = k;
-    g_plans[slot] = tc_make_plan(BT, C, OC, sms);
+    g_plans[slot] = tc_make_plan(BT, C, OC, sms, quads);
     return g_plans[slot];
 }
 
@@ -141,8 +143,9 @@ int device_state(DeviceState** out, int* dev_out) {
         d.num_sms = sms;
         if (d.arch_checked == 1) {
             // CTAs the persistent kernel can keep resident: whole pairs only.
-            const int pairs = tc_max_active_pairs();
+            const int pairs = tc_max_active_clusters(2);
             if (pairs > 0 && 2 * pairs < sms) d.num_sms = 2 * pairs;
+            d.num_quads = tc_max_active_clusters(4);
         }
     }
     if (d.arch_checked != 1) return MMBWD_ERR_ARCH;
@@ -212,15 +215,15 @@ size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dt
     Shape s;
     if (check_shape(B, T, C, OC, dtype, &s) != MMBWD_OK) return 0;
     if (dtype != MMBWD_BF16 || s.BT == 0 || C == 0 || OC == 0) return 0;
-    int sms = 0;
+    int sms = 0, quads = 0;
     {
         std::lock_guard<std::mutex> g(g_mutex);
         DeviceState* d = nullptr;
         int dev = 0;
-        if (device_state(&d, &dev) == MMBWD_OK) sms = d->num_sms;
+        if (device_state(&d, &dev) == MMBWD_OK) sms = d->num_sms, quads = d->num_quads;
     }
-    if (sms <= 0) sms = 152;  // no usable device: size for a full GB300
-    return tc_make_plan(s.BT, C, OC, sms).ws_bytes();
+    if (sms <= 0) sms = 152, quads = 38;  // no usable device: size for a full GB300
+    return tc_make_plan(s.BT, C, OC, sms, quads).ws_bytes();
 }
 
 int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms, int* out, int n) {
@@ -228,26 +231,29 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     const int rc = check_shape(B, T, C, OC, dtype, &s);
     if (rc != MMBWD_OK) return rc;
     if (!out || n < 0) return MMBWD_ERR_NULL;
-    int v[14] = {0};
+    int v[15] = {0};
+    int num_quads = num_sms / 4;
     if (num_sms <= 0) {  // the current device's resident CTAs (a full GB300 without a device)
         std::lock_guard<std::mutex> g(g_mutex);
         DeviceState* d = nullptr;
         int dev = 0;
-        num_sms = device_state(&d, &dev) == MMBWD_OK ? d->num_sms : 152;
+        const bool have = device_state(&d, &dev) == MMBWD_OK;
+        num_sms = have ? d->num_sms : 152;
+        num_quads = have ? d->num_quads : 38;
     }
     if (dtype == MMBWD_BF16) {
-        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms);
-        const int vals[14] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
+        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms, num_quads);
+        const int vals[15] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
                               pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.table,
-                              TC_PAIR_BM, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches()};
-        for (int i = 0; i < 14; ++i) v[i] = vals[i];
+                              TC_PAIR_BM * pl.ppc, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), pl.ppc};
+        for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
         const int go = static_cast<int>((OC + SIMT_BM - 1) / SIMT_BM);
-        const int vals[14] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BN, SIMT_BK, 2, 2};
-        for (int i = 0; i < 14; ++i) v[i] = vals[i];
+        const int vals[15] = {0, gm * gn + go * gn, gm * gn + go * gn, 1, 0, gm * gn, go * gn, 0, SIMT_BM, SIMT_BN, SIMT_BN, SIMT_BK, 2, 2, 0};
+        for (int i = 0; i < 15; ++i) v[i] = vals[i];
     }
-    const int m = n < 14 ? n : 14;
+    const int m = n < 15 ? n : 15;
     for (int i = 0; i < m; ++i) out[i] = v[i];
     return m;
 }
@@ -306,7 +312,7 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
 
-    const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms);
+    const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads);
     rc = ensure_workspace(*d, plan.ws_bytes(), stream);
     if (rc != MMBWD_OK) return rc;
     e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream);
@@ -431,7 +437,7 @@ extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, 
                         static_cast<const float*>(weight), s.BT, C, OC, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
-    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms);
+    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads);
     if (plan.ws_bytes() > MMBWD_STATIC_SCRATCH_BYTES) return MMBWD_ERR_SCRATCH;
     e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, g_static_scratch_addr[dev], stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;

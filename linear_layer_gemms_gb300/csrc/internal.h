@@ -37,8 +37,8 @@ enum WaitSite : int {
     SITE_FORWARD_FULL = 10,
 };
 
-// Schedule of a launch: which work items each CTA pair processes, in order
-// (items of pair c: items[start[c] .. start[c+1])). It travels in the kernel
+// Schedule of a launch: which work items each cluster (one or two CTA pairs)
+// processes, in order (items of cluster c: items[start[c] .. start[c+1])). It travels in the kernel
 // parameters, so a launch needs no device memory for it.
 constexpr int TC_MAX_PAIRS = 128;
 constexpr int TC_MAX_SCHED_ITEMS = 3072;
@@ -66,7 +66,8 @@ struct TcPlan {
     int n_dw_items;    // dw_tiles_m * dw_tiles_n * splits
     int n_dinp_items;  // dinp_tiles_m * dinp_tiles_n
     int n_items;
-    int table;         // 1: per-pair item lists in `sched`; 0: round-robin
+    int table;         // 1: per-cluster item lists in `sched`; 0: round-robin
+    int ppc;           // CTA pairs per cluster: 1, or 2 sharing the B tile through multicast
     int grid;          // CTAs (twice the number of CTA pairs)
     double est_us;     // the planner's time estimate
     int fixup_grid;    // CTAs of the split-reduction pass (0 when splits == 1)
@@ -84,7 +85,7 @@ struct TcParams {
     __nv_bfloat16* dbias;  // may be null
     int dinp_bn, dw_bn, dinp_tiles_n, dw_tiles_n;
     int dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
-    int n_dw_items, n_dinp_items, n_items, table;
+    int n_dw_items, n_dinp_items, n_items, table, ppc;
     float* partials;       // [dw half tile][split][BM][dw_bn]; half tile = 128-row tile x column tile
     float* bias_partials;  // [dw 128-row tile][split][BM]
     unsigned long long timeout_ns;
@@ -93,7 +94,7 @@ struct TcParams {
 // Plans (pure functions of the shape and the number of co-resident CTAs,
 // twice the resident CTA pairs). Overrides for tuning and tests come from the
 // environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs).
-TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms);
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
 
 // Launch the tensor-core kernel (and, with split dweight, the fixed-order
 // split reduction after it on the same stream). `ws` must hold plan.ws_bytes()
@@ -104,9 +105,9 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
 
 size_t tc_smem_bytes();
 
-// How many CTA pairs of the tensor-core kernel can be resident at once on the
-// current device (0 if the query fails).
-int tc_max_active_pairs();
+// How many clusters of `cluster_size` CTAs of the tensor-core kernel can be
+// resident at once on the current device (0 if the query fails).
+int tc_max_active_clusters(int cluster_size);
 
 // Device status word of the tensor-core translation unit.
 cudaError_t tc_read_status(int* code, int* info3, bool reset);

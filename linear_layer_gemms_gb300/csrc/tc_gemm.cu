@@ -184,12 +184,13 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
 
 // Item processed by this CTA pair in round `round` (>= n_items: none).
 __device__ __forceinline__ int item_at(const TcParams& p, const TcSchedule& sch, int round) {
-    const int c = static_cast<int>(blockIdx.x >> 1);
+    const int csize = 2 * p.ppc;
+    const int c = static_cast<int>(blockIdx.x) / csize;
     if (p.table) {
         const int idx = sch.start[c] + round;
         return idx < sch.start[c + 1] ? static_cast<int>(sch.items[idx]) : p.n_items;
     }
-    return round * static_cast<int>(gridDim.x >> 1) + c;
+    return round * (static_cast<int>(gridDim.x) / csize) + c;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -228,14 +229,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
-    const uint32_t rank = ptx::cluster_ctarank();  // 0: issues the pair MMAs
+    const uint32_t crank = ptx::cluster_ctarank();  // 0 .. 2*ppc-1
+    const uint32_t rank = crank & 1u;               // within the CTA pair: 0 issues the pair MMAs
+    const uint32_t pp = crank >> 1;                 // which pair of the cluster
+    const uint32_t pair_leader = crank & ~1u;       // cluster rank of this pair's MMA issuer
+    const uint32_t twin = crank ^ 2u;               // same position in the other pair (ppc == 2)
     const bool leader = rank == 0;
     const bool bias_on = p.dbias != nullptr;
+    const int ppc = p.ppc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
-            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on ? NUM_BIAS_WARPS : 0));
+            // refilled once every pair MMA reading it has completed (one commit
+            // per pair of the cluster) and every bias warp reading it is done
+            // (this CTA's and, with two pairs, the twin CTA's: the twin's loads
+            // multicast into this stage)
+            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s),
+                           static_cast<uint32_t>(ppc) * (1u + (bias_on ? NUM_BIAS_WARPS : 0)));
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive
+    ptx::cluster_sync();  // every CTA's barriers exist before any remote arrive or multicast
     ptx::tc_fence_after();
     const uint32_t tmem_base = misc[0];
     const Waiter wt{misc + 1, p.timeout_ns};
@@ -276,11 +287,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // This CTA's rows of A and columns of B. Boxes wholly outside the
                 // tensor are skipped: they would only feed accumulator rows or
                 // columns that are never stored.
-                const int row0 = it.pm * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
+                const int prow = it.pm * ppc + static_cast<int>(pp);  // this pair's 256-row tile
+                const int row0 = prow * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
                 const int half = it.bn / 2;  // columns of B staged by this CTA
                 const int col0 = it.n_tile * it.bn + static_cast<int>(rank) * half;
                 int nb = 0;
                 for (int j = 0; j < half / 64; ++j) nb += (col0 + j * 64 < p.C) ? 1 : 0;
+                // With two pairs, the twin CTA needs the same B boxes: box j is loaded
+                // by the CTA of pair j and multicast to both.
+                const uint16_t bmask = static_cast<uint16_t>((1u << crank) | (1u << twin));
                 // Output tile of this CTA, prefetched into L2 a few k-blocks before the
                 // main loop ends so that the epilogue's read of the old values hits L2.
                 const bool direct = !(it.is_dw && p.splits > 1);
@@ -309,12 +324,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (it.is_dw) {
                         for (int j = 0; j < na; ++j)
                             ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * TC_BK);
-                        for (int j = 0; j < nb; ++j)
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_inp, fb, col0 + j * 64, kb * TC_BK);
-                    } else {
-                        if (na) ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, row0);
-                        for (int j = 0; j < nb; ++j)
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_weight, fb, col0 + j * 64, kb * TC_BK);
+                    } else if (na) {
+                        ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, row0);
+                    }
+                    const void* tmB = it.is_dw ? static_cast<const void*>(&tm_inp) : static_cast<const void*>(&tm_weight);
+                    if (ppc == 1) {
+                        for (int j = 0; j < nb; ++j) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * TC_BK);
+                    } else if (static_cast<int>(pp) < nb) {
+                        ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, col0 + static_cast<int>(pp) * 64,
+                                                   kb * TC_BK, bmask);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -335,6 +353,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (leader) {
             // -------------------------------------------------------- MMA issuer
             if (lane == 0) {
+                const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2u * pp));
+                const uint16_t empty_mask = static_cast<uint16_t>(ppc == 2 ? 0xFu : pair_mask);
                 uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
                 bool ok = true;
                 for (int r = 0; ok; ++r) {
@@ -368,14 +388,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             const uint64_t bdesc = ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
                             ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
                         }
-                        ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), 0x3);
+                        ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), empty_mask);
                         if (++stage == TC_STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    ptx::mma_commit_pair_multicast(bars + 8u * (BAR_TFULL + acc), 0x3);
+                    ptx::mma_commit_pair_multicast(bars + 8u * (BAR_TFULL + acc), pair_mask);
                     if (++acc == 2) {
                         acc = 0;
                         acc_phase ^= 1u;
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         } else {
             // ---------------------------------------------- forwarder (odd CTA)
             if (lane == 0) {
-                const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, 0);
+                const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, pair_leader);
                 uint32_t stage = 0, phase = 0;
                 bool ok = true;
                 for (int r = 0; ok; ++r) {
@@ -415,6 +435,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ------------------------------------------------------------ bias warps
         if (bias_on) {
             const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
+            const uint32_t twin_empty = ptx::mapa(bars + 8u * BAR_EMPTY, twin);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             for (int r = 0;; ++r) {
                 const int w = item_at(p, sch, r);
@@ -455,7 +476,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
+                        if (ppc == 2) ptx::mbar_arrive_cluster_relaxed(twin_empty + 8u * stage);
+                    }
                     if (++stage == TC_STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -488,14 +512,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int r8 = lane >> 2;       // coalesced phase: rows 8i + r8 of the quadrant,
         const int cg = (lane & 3) * 8;  //   columns cg..cg+7 of each 32-column chunk
         const uint32_t stg = base + OFF_STAGE + q * STG_WARP_BYTES;
-        const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, 0);
+        const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, pair_leader);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t bias_parity[2] = {0u, 0u};
         for (int r = 0;; ++r) {
             const int w = item_at(p, sch, r);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
-            const int m_tile = it.pm * 2 + static_cast<int>(rank);  // this CTA's 128-row tile
+            const int m_tile = (it.pm * ppc + static_cast<int>(pp)) * 2 + static_cast<int>(rank);  // 128-row tile
             const bool has_bias = bias_on && it.is_dw && it.n_tile == 0;
             const bool split_mode = it.is_dw && p.splits > 1;
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
@@ -671,7 +695,12 @@ long env_long(const char* name, long dflt) {
 // epilogue, whichever is longer, since the two overlap across the two
 // accumulators; the last item's epilogue is not overlapped. Split dweight adds
 // the fixup pass.
-double t_kb(int bn) { return bn == 256 ? 0.37 : 0.33; }  // a 128-wide tile is load-bound
+// One k-block of a cluster item (ppc pairs, 256 * ppc rows): load-bound, and two
+// pairs that share B through multicast read a quarter less from L2 per pair.
+double t_kb(int bn, int ppc) {
+    if (ppc == 2) return bn == 256 ? 0.31 : 0.29;
+    return bn == 256 ? 0.37 : 0.33;
+}
 double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
 double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
 constexpr double T_ITEM = 0.3;                                 // per-item handoff
@@ -686,10 +715,10 @@ ItemCost item_cost(const TcPlan& pl, int w) {
         const int kb0 = split * pl.kb_per_split;
         const int kb = std::min(kb0 + pl.kb_per_split, pl.dw_kb) - kb0;
         const double epi = pl.splits > 1 ? t_partial(pl.dw_bn) : t_rmw(pl.dw_bn);
-        return {std::max(kb * t_kb(pl.dw_bn), epi) + T_ITEM, epi};
+        return {std::max(kb * t_kb(pl.dw_bn, pl.ppc), epi) + T_ITEM, epi};
     }
     const double epi = t_rmw(pl.dinp_bn);
-    return {std::max(pl.dinp_kb * t_kb(pl.dinp_bn), epi) + T_ITEM, epi};
+    return {std::max(pl.dinp_kb * t_kb(pl.dinp_bn, pl.ppc), epi) + T_ITEM, epi};
 }
 
 double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
@@ -758,17 +787,17 @@ bool g_attr_set[64];
 
 size_t tc_smem_bytes() { return SMEM_TOTAL; }
 
-int tc_max_active_pairs() {
+int tc_max_active_clusters(int cluster_size) {
     if (cudaFuncSetAttribute(tc_mmbwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster_size), 1, 1);
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_TOTAL;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -781,19 +810,17 @@ int tc_max_active_pairs() {
     return n;
 }
 
-TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
     TcPlan pl{};
-    pl.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
-    pl.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
     pl.dinp_kb = ceil_div_i(OC, TC_BK);
     pl.dw_kb = ceil_div_i(BT, TC_BK);
-    const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
 
     // Overrides (tuning, tests): a forced split count that would leave an
     // empty split is lowered to the nearest count that does not; a forced grid
     // is rounded down to whole pairs; MMBWD_TILE_N = "<dinp>,<dweight>" widths.
     const long force_splits = env_long("MMBWD_SPLITK", 0);
-    const long force_pairs = env_long("MMBWD_GRID", 0) / 2;
+    const long force_grid = env_long("MMBWD_GRID", 0);
+    const long force_ppc = env_long("MMBWD_PPC", 0);
     int force_dinp_bn = 0, force_dw_bn = 0;
     if (const char* t = std::getenv("MMBWD_TILE_N")) {
         int a = 0, b = 0;
@@ -805,6 +832,11 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     const int max_splits = std::max(1, std::min(pl.dw_kb, 16));
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
+    for (int ppc = 1; ppc <= 2; ++ppc) {
+    if (force_ppc && ppc != force_ppc) continue;
+    const int max_clusters =
+        std::max(1, std::min(ppc == 1 ? num_sms / 2 : num_quads, TC_MAX_PAIRS));
+    if (ppc == 2 && num_quads <= 0) continue;
     for (int dinp_bn = 256; dinp_bn >= 128; dinp_bn -= 128) {
         if (force_dinp_bn && dinp_bn != force_dinp_bn) continue;
         for (int dw_bn = 256; dw_bn >= 128; dw_bn -= 128) {
@@ -820,6 +852,9 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
                                     ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
                     continue;
                 c = pl;
+                c.ppc = ppc;
+                c.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM * ppc);
+                c.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM * ppc);
                 c.dinp_bn = dinp_bn;
                 c.dw_bn = dw_bn;
                 c.dinp_tiles_n = ceil_div_i(C, dinp_bn);
@@ -829,9 +864,9 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
                 c.kb_per_split = kps;
                 c.n_dw_items = c.dw_tiles_m * c.dw_tiles_n * S;
                 c.n_items = c.n_dw_items + c.n_dinp_items;
-                int pairs = std::max(1, std::min(c.n_items, max_pairs));
-                if (force_pairs > 0) pairs = static_cast<int>(std::min<long>(force_pairs, pairs));
-                c.grid = 2 * pairs;
+                int pairs = std::max(1, std::min(c.n_items, max_clusters));  // clusters
+                if (force_grid > 0) pairs = static_cast<int>(std::max<long>(1, std::min<long>(force_grid / (2 * ppc), pairs)));
+                c.grid = 2 * ppc * pairs;
                 c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
                 const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
                 c.est_us = cost;
@@ -842,14 +877,16 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
             }
         }
     }
+    }
     pl = best_pl;
     pl.fixup_grid = 0;
     if (pl.splits > 1) {
         const int64_t nvec = OC * (C / 8);
         pl.fixup_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, 8 * std::max(2, num_sms))));
-        const size_t half_tiles = static_cast<size_t>(2 * pl.dw_tiles_m) * pl.dw_tiles_n;
+        const size_t row_tiles = static_cast<size_t>(2 * pl.ppc * pl.dw_tiles_m);  // 128-row tiles
+        const size_t half_tiles = row_tiles * pl.dw_tiles_n;
         pl.ws_partials_bytes = align256(half_tiles * pl.splits * TC_BM * pl.dw_bn * 4);
-        pl.ws_bias_bytes = align256(static_cast<size_t>(2 * pl.dw_tiles_m) * pl.splits * TC_BM * 4);
+        pl.ws_bias_bytes = align256(row_tiles * pl.splits * TC_BM * 4);
     }
     return pl;
 }
@@ -918,6 +955,7 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     p.n_dinp_items = plan.n_dinp_items;
     p.n_items = plan.n_items;
     p.table = plan.table;
+    p.ppc = plan.ppc;
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
     p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
@@ -930,7 +968,7 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(2 * plan.ppc);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

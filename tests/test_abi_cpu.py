@@ -95,9 +95,11 @@ def test_plan_is_a_pure_function_of_shape():
         # CTA pairs: 256-row tiles, 128 or 256 columns per product, an even grid
         assert a["path"] == 1 and 2 <= a["grid"] <= 152 and a["grid"] % 2 == 0
         assert a["tile_n_dinp"] in (128, 256) and a["tile_n_dweight"] in (128, 256)
-        assert a["dinp_tiles"] == -(-BT // 256) * -(-C // a["tile_n_dinp"])
-        assert a["dweight_tiles"] == -(-OC // 256) * -(-C // a["tile_n_dweight"])
-        assert a["grid"] // 2 <= a["items"]
+        assert a["pairs_per_cluster"] in (1, 2) and a["tile_m"] == 256 * a["pairs_per_cluster"]
+        assert a["grid"] % (2 * a["pairs_per_cluster"]) == 0
+        assert a["dinp_tiles"] == -(-BT // a["tile_m"]) * -(-C // a["tile_n_dinp"])
+        assert a["dweight_tiles"] == -(-OC // a["tile_m"]) * -(-C // a["tile_n_dweight"])
+        assert a["grid"] // (2 * a["pairs_per_cluster"]) <= a["items"]
         assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"] * a["splits"]
         kb = -(-BT // 64)
         # every split is non-empty and together they cover the reduction
@@ -122,6 +124,13 @@ def test_split_override_from_environment(monkeypatch):
     monkeypatch.delenv("MMBWD_GRID")
 
 
+def test_pairs_per_cluster_override(monkeypatch):
+    for ppc in (1, 2):
+        monkeypatch.setenv("MMBWD_PPC", str(ppc))
+        a = mm.mmbwd_plan_info(8, 1024, 768, 3072, mm.BF16, 152)
+        assert a["pairs_per_cluster"] == ppc and a["tile_m"] == 256 * ppc
+
+
 def test_tile_width_override(monkeypatch):
     monkeypatch.setenv("MMBWD_TILE_N", "128,256")
     a = mm.mmbwd_plan_info(8, 1024, 768, 3072, mm.BF16, 152)
@@ -138,10 +147,11 @@ def test_workspace_size_formula():
         B, T, C, OC = 1, 1000, 264, 392
         info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
         ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
-        half_tiles = 2 * info["dweight_tiles"]  # per-CTA 128-row halves of the pair tiles
+        ppc = info["pairs_per_cluster"]
+        half_tiles = 2 * ppc * info["dweight_tiles"]  # per-CTA 128-row parts of the cluster tiles
         align = lambda x: (x + 255) // 256 * 256  # noqa: E731
         want = (align(half_tiles * 2 * 128 * info["tile_n_dweight"] * 4) +
-                align(2 * -(-OC // 256) * 2 * 128 * 4))
+                align(2 * ppc * -(-OC // info["tile_m"]) * 2 * 128 * 4))
         assert info["launches"] == 2  # the split reduction is a second kernel
         assert ws == want
     finally:

@@ -104,6 +104,7 @@ def test_split_reduction_and_schedule(monkeypatch, splits):
     B, T, C, OC = 1, 1000, 264, 392
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-2)
     monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+    monkeypatch.setenv("MMBWD_PPC", "1")  # one CTA pair per cluster: grids of any even size
     kb = -(-B * T // 64)
     want_splits = -(-kb // -(-kb // splits))  # lowered so that no split is empty
     outs = []
@@ -218,3 +219,24 @@ def test_tile_widths(monkeypatch, tile_n, splits):
     assert f"{info['tile_n_dinp']},{info['tile_n_dweight']}" == tile_n
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
     check_full(x, B, T, C, OC, "bf16")
+
+
+@pytest.mark.parametrize("ppc", [1, 2])
+@pytest.mark.parametrize("tile_n", ["256,256", "128,128"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_pairs_per_cluster(monkeypatch, ppc, tile_n, splits):
+    """One CTA pair per cluster, or two pairs sharing the B tile through TMA
+    multicast, with both tile widths and with or without a split dweight
+    reduction, on a ragged shape; and the 4-CTA mode on a grid of one cluster."""
+    B, T, C, OC = 3, 300, 392, 1032
+    monkeypatch.setenv("MMBWD_PPC", str(ppc))
+    monkeypatch.setenv("MMBWD_TILE_N", tile_n)
+    monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+    info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+    assert info["pairs_per_cluster"] == ppc
+    _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
+    g0, _ = check_full(x, B, T, C, OC, "bf16")
+    monkeypatch.setenv("MMBWD_GRID", str(2 * ppc))  # every item on one cluster
+    g1, _ = check_full(x, B, T, C, OC, "bf16")
+    for k in ("dinp", "dweight", "dbias"):
+        assert np.array_equal(to_host(g0[k], "bf16"), to_host(g1[k], "bf16")), k
