@@ -1,4 +1,4 @@
-"""ctypes wrapper around the C oracle of matmul_backward.
+"""ctypes wrapper around the C oracle of matmul_backward (and of the layer's forward).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product library never imports it.
@@ -27,7 +27,7 @@ _libs: dict = {}
 
 F32, BF16, F64 = 0, 1, 2
 DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
-MUTANTS = tuple(range(1, 9))
+MUTANTS = tuple(range(1, 11))
 
 
 def lib_path(variant: str) -> str:
@@ -63,8 +63,9 @@ class Oracle:
         lib.oracle_dinp_rows.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
         lib.oracle_dweight_rows.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
         lib.oracle_matmul_backward.argtypes = [vp] * 8 + [i64] * 4 + [ci]
+        lib.oracle_forward_rows.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
         for f in (lib.oracle_dinp_rows, lib.oracle_dweight_rows, lib.oracle_matmul_backward,
-                  lib.oracle_threads, lib.oracle_mutant):
+                  lib.oracle_forward_rows, lib.oracle_threads, lib.oracle_mutant):
             f.restype = ci
         self._lib = lib
 
@@ -114,6 +115,21 @@ class Oracle:
                                            inp.ctypes.data, BT, C, OC, dt)
         assert rc == 0
         return out, db
+
+    def forward_rows(self, inp, weight, dtype: str, rows=None, bias=None):
+        """Rows ``rows`` (all if None) of inp @ weight^T + bias, in float64."""
+        dt = DTYPES[dtype]
+        BT, C = inp.shape
+        OC = weight.shape[0]
+        for a in (inp, weight, bias):
+            self._check(a, dt)
+        r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = BT if r is None else len(r)
+        out = np.empty((n, OC), dtype=np.float64)
+        rc = self._lib.oracle_forward_rows(out.ctypes.data, self._ptr(r), n, inp.ctypes.data,
+                                           weight.ctypes.data, self._ptr(bias), BT, C, OC, dt)
+        assert rc == 0
+        return out
 
     def matmul_backward(self, dout, inp, weight, dtype: str, dinp_init=None, dweight_init=None,
                         bias=True):

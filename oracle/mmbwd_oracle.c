@@ -35,6 +35,8 @@
  * L = sum(dout * (inp weight^T + bias)), and special cases (identity weight,
  * one-hot dout, zero dout).
  *
+ * The file also states the forward of the layer (oracle_forward_rows).
+ *
  * ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake so that
  * the tests can show that their pins catch it; it is never set in a real build.
  */
@@ -169,6 +171,44 @@ int oracle_matmul_backward(double* dinp, double* dweight, double* dbias, const v
     int64_t BT = B * T;
     if (oracle_dinp_rows(dinp, NULL, BT, dinp_init, dout, weight, BT, C, OC, dtype)) return -1;
     return oracle_dweight_rows(dweight, dbias, NULL, OC, dweight_init, dout, inp, BT, C, OC, dtype);
+}
+
+/*
+ * Forward of the same linear layer, the product `matmul_backward1`'s comment
+ * recalls ("the forward pass was calculated with alpha = 1.0f, beta = 0.0f":
+ * out = inp . weight^T, overwritten), with the optional bias of a GPT-2 linear
+ * layer added. For r in [0, nrows): bt = rows ? rows[r] : r,
+ *   out[r*OC + o] = bias[o] + sum_{i=0..C-1} inp[bt,i] * weight[o,i]
+ * summed in double over i ascending; bias may be NULL (no bias term).
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_forward_rows(double* out, const int64_t* rows, int64_t nrows, const void* inp,
+                        const void* weight, const void* bias, int64_t BT, int64_t C, int64_t OC,
+                        int dtype) {
+    if (bad_args(BT, C, OC, dtype) || nrows < 0 || (!rows && nrows != BT)) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows && (rows[r] < 0 || rows[r] >= BT)) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t bt = rows ? rows[r] : r;
+        for (int64_t o = 0; o < OC; ++o) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < C; ++i) {
+#if ORACLE_MUTANT == 10 /* transposed operand: weight indexed by (i, o) on the square case */
+                acc += load(inp, dtype, bt * C + i) * load(weight, dtype, (C == OC ? i * C + o : o * C + i));
+#else
+                acc += load(inp, dtype, bt * C + i) * load(weight, dtype, o * C + i);
+#endif
+            }
+#if ORACLE_MUTANT == 9 /* dropped term: the bias is not added */
+            (void)bias;
+#else
+            if (bias) acc += load(bias, dtype, o);
+#endif
+            out[r * OC + o] = acc;
+        }
+    }
+    return 0;
 }
 
 /* Number of threads a parallel region of this build uses (1 when built without OpenMP). */

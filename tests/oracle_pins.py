@@ -268,7 +268,41 @@ def pin_empty_dims(orc):
     assert np.array_equal(dbias, dout.sum(axis=0))
 
 
+def pin_forward_exact_integers(orc):
+    """The forward on small integer inputs against exact Python integer sums,
+    with and without the bias, on shapes that include a square weight."""
+    rng = np.random.default_rng(31)
+    for (BT, C, OC) in [(3, 4, 5), (4, 4, 4), (2, 7, 3)]:
+        inp = rng.integers(-3, 4, size=(BT, C)).astype(np.float64)
+        w = rng.integers(-3, 4, size=(OC, C)).astype(np.float64)
+        b = rng.integers(-3, 4, size=OC).astype(np.float64)
+        got_b = orc.forward_rows(inp, w, "f64", bias=b)
+        got_n = orc.forward_rows(inp, w, "f64")
+        for bt in range(BT):
+            for o in range(OC):
+                exact = sum(int(inp[bt, i]) * int(w[o, i]) for i in range(C))
+                assert got_n[bt, o] == exact
+                assert got_b[bt, o] == exact + int(b[o])
+
+
+def pin_forward_library_and_adjoint(orc):
+    """The forward equals numpy's float64 inp @ W^T + b, and is the adjoint of
+    the (separately pinned) backward into inp: <dout, inp W^T> = <dout W, inp>."""
+    rng = np.random.default_rng(32)
+    BT, C, OC = 40, 24, 56
+    inp, w = rng.standard_normal((BT, C)), rng.standard_normal((OC, C))
+    b, dout = rng.standard_normal(OC), rng.standard_normal((BT, OC))
+    out = orc.forward_rows(inp, w, "f64", bias=b)
+    want = inp @ w.T + b
+    assert np.max(np.abs(out - want) / (np.abs(want) + 1)) < 1e-12
+    dinp = orc.dinp_rows(dout, w, "f64")
+    lhs, rhs = np.sum(dout * (out - b)), np.sum(dinp * inp)
+    assert abs(lhs - rhs) <= 1e-10 * (abs(rhs) + 1)
+    rows = np.array([0, 5, 39])
+    assert np.array_equal(orc.forward_rows(inp, w, "f64", rows, b), out[rows])
+
+
 ALL_PINS = [pin_exact_unit_differences, pin_central_differences, pin_library_matmul,
             pin_colsum_invariant, pin_adjoint_identities, pin_special_cases,
             pin_double_accumulation, pin_storage_types, pin_subset_rows, pin_null_bias,
-            pin_empty_dims]
+            pin_empty_dims, pin_forward_exact_integers, pin_forward_library_and_adjoint]
