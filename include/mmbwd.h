@@ -141,6 +141,29 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
  * what the kernel recorded (MMBWD_ERR_DEVICE_TIMEOUT when the mechanism works). */
 int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
 
+/*
+ * mmbwd_forward -- the forward of the same linear layer, enqueued on `stream`:
+ *
+ *     out (B,T,OC) = inp (B,T,C) . weight^T + bias          (overwritten)
+ *
+ * the product that matmul_backward1's comment recalls ("the forward pass was
+ * calculated with alpha = 1.0f, beta = 0.0f": cuBLAS SGEMM of weight^T and
+ * inp into out), plus the optional bias of a GPT-2 linear layer.
+ *
+ *   out            device, (B*T, OC), written
+ *   inp            device, (B*T, C),  read only
+ *   weight         device, (OC, C),   read only
+ *   bias_or_null   device, (OC),      read only; NULL: no bias term
+ *   dtype          MMBWD_F32 or MMBWD_BF16 (all four tensors)
+ *
+ * bf16: fp32 accumulation on the tensor cores, out rounded once (RNE) after
+ * adding the bias in fp32. fp32: FFMA accumulation. Same alignment, aliasing
+ * (out must not overlap an input), status codes, asynchrony and determinism
+ * as mmbwd_run; no workspace. C == 0 gives out = bias (or 0).
+ */
+int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bias_or_null, int64_t B,
+                  int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream);
+
 /* Test hook: make the next `n` workspace allocations fail (MMBWD_ERR_ALLOC). */
 void mmbwd_debug_fail_next_alloc(int n);
 

@@ -10,6 +10,8 @@ first use instead of falling back to anything else.
     dweight (OC,C)   += dout^T . inp
     dbias   (OC)      = sum over (b,t) of dout        (NULL / None skips it)
 
+and the layer's forward, out = inp . weight^T + bias (mmbwd_forward).
+
 Pointers may be given as integers or as objects with ``data_ptr()`` (for
 example torch tensors on the current CUDA device); ``stream`` is a raw
 ``cudaStream_t`` integer, or None for the current torch stream.
@@ -46,6 +48,7 @@ SIGNATURES = {
     "mmbwd_selftest_wait_timeout": ([_u64], _ci),
     "mmbwd_debug_fail_next_alloc": ([_ci], None),
     "mmbwd_run_static_scratch": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
+    "mmbwd_forward": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
 }
 
 _lock = threading.Lock()
@@ -108,6 +111,13 @@ def mmbwd_run_static_scratch(dinp, dweight, dbias, dout, inp, weight, B: int, T:
     return load().mmbwd_run_static_scratch(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout),
                                            _ptr(inp), _ptr(weight), B, T, C, OC, dtype,
                                            _stream(stream))
+
+
+def mmbwd_forward(out, inp, weight, bias, B: int, T: int, C: int, OC: int, dtype: int,
+                  stream=None) -> int:
+    """Enqueue out = inp . weight^T + bias (bias may be None); returns the status."""
+    return load().mmbwd_forward(_ptr(out), _ptr(inp), _ptr(weight), _ptr(bias), B, T, C, OC, dtype,
+                                _stream(stream))
 
 
 def mmbwd_workspace_bytes(B: int, T: int, C: int, OC: int, dtype: int) -> int:

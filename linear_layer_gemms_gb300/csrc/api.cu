@@ -49,11 +49,11 @@ std::atomic<int> g_fail_allocs{0};
 // schedule search is cached so that a call costs a table lookup.
 struct PlanKey {
     int64_t BT, C, OC;
-    int sms, quads;
+    int sms, quads, fwd;
     long splitk, grid, tile_n, ppc;
     bool operator==(const PlanKey& o) const {
-        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && quads == o.quads && splitk == o.splitk &&
-               grid == o.grid && tile_n == o.tile_n && ppc == o.ppc;
+        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && quads == o.quads && fwd == o.fwd &&
+               splitk == o.splitk && grid == o.grid && tile_n == o.tile_n && ppc == o.ppc;
     }
 };
 constexpr int kPlanCache = 32;
@@ -74,8 +74,8 @@ long env_tile_n() {
 }
 
 // Caller holds g_mutex.
-const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int quads) {
-    const PlanKey k{BT, C, OC, sms, quads, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n(),
+const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int quads, int fwd = 0) {
+    const PlanKey k{BT, C, OC, sms, quads, fwd, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n(),
                     env_long("MMBWD_PPC")};
     for (int i = 0; i < g_plan_count; ++i)
         if (g_plan_keys[i] == k) return g_plans[i];
@@ -83,7 +83,7 @@ const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int quads)
     g_plan_next = (g_plan_next + 1) % kPlanCache;
     if (g_plan_count < kPlanCache) ++g_plan_count;
     g_plan_keys[slot] = k;
-    g_plans[slot] = tc_make_plan(BT, C, OC, sms, quads);
+    g_plans[slot] = fwd ? tc_make_plan_forward(BT, C, OC, sms, quads) : tc_make_plan(BT, C, OC, sms, quads);
     return g_plans[slot];
 }
 
@@ -355,6 +355,43 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns) {
 }
 
 void mmbwd_debug_fail_next_alloc(int n) { g_fail_allocs.store(n < 0 ? 0 : n); }
+
+int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bias, int64_t B, int64_t T,
+                  int64_t C, int64_t OC, int dtype, cudaStream_t stream) {
+    Shape s;
+    int rc = check_shape(B, T, C, OC, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = s.es;
+    const size_t b_out = static_cast<size_t>(s.n_dout) * es, b_inp = static_cast<size_t>(s.n_dinp) * es,
+                 b_w = static_cast<size_t>(s.n_dw) * es, b_b = static_cast<size_t>(OC) * es;
+    if ((b_out && !out) || (b_inp && !inp) || (b_w && !weight)) return MMBWD_ERR_NULL;
+    const void* ptrs[4] = {out, inp, weight, bias};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0 || (static_cast<size_t>(OC) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+    if (overlaps(out, b_out, inp, b_inp) || overlaps(out, b_out, weight, b_w) || overlaps(out, b_out, bias, b_b))
+        return MMBWD_ERR_ALIAS;
+
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    cudaError_t e = cudaSuccess;
+    if (s.BT == 0 || OC == 0) return MMBWD_OK;  // no output element
+    if (C == 0) {                                // the empty product: out = bias (or 0)
+        e = fill_rows_launch(out, bias, s.BT, OC, dtype, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    if (dtype == MMBWD_F32) {
+        e = simt_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
+                                static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC, stream);
+        return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+    }
+    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads, 1);
+    e = tc_launch_forward(plan, out, inp, weight, bias, s.BT, C, OC, stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
 
 }  // extern "C"
 

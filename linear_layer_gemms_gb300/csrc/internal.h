@@ -80,6 +80,13 @@ struct TcPlan {
 
 struct TcParams {
     int64_t BT, C, OC;
+    // Forward launches (the kernel's forward instantiation) run only "dinp-type"
+    // items -- K-major A, rows over BT -- with a K-major B (weight rows) and an
+    // overwrite epilogue: out = acc + bias. n_dinp is the N extent and row
+    // stride of that product's output: C for the backward (dinp), OC for the
+    // forward (out, passed in `dinp`).
+    int64_t n_dinp;
+    const __nv_bfloat16* fwd_bias;  // may be null
     __nv_bfloat16* dinp;
     __nv_bfloat16* dweight;
     __nv_bfloat16* dbias;  // may be null
@@ -95,6 +102,13 @@ struct TcParams {
 // twice the resident CTA pairs). Overrides for tuning and tests come from the
 // environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs).
 TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
+
+// Plan of the forward out (BT x OC) = inp (BT x C) . weight^T (+ bias): only
+// dinp-type items, K = C, N = OC.
+TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
+
+cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight,
+                              const void* bias, int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
 
 // Launch the tensor-core kernel (and, with split dweight, the fixed-order
 // split reduction after it on the same stream). `ws` must hold plan.ws_bytes()
@@ -122,6 +136,14 @@ constexpr int SIMT_THREADS = 256;
 cudaError_t simt_launch(float* dinp, float* dweight, float* dbias, const float* dout,
                         const float* inp, const float* weight, int64_t BT, int64_t C, int64_t OC,
                         cudaStream_t stream);
+
+// out (BT x OC) = inp (BT x C) . weight^T + bias (bias may be null), fp32 FFMA.
+cudaError_t simt_forward_launch(float* out, const float* inp, const float* weight, const float* bias,
+                                int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
+
+// out[r, o] = bias[o], or 0 without a bias (the forward when C == 0).
+cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t cols, int dtype,
+                             cudaStream_t stream);
 
 // dbias = column sums of dout (used when C == 0, where no GEMM tile exists).
 cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype,

@@ -1,5 +1,5 @@
-// fp32 linear-layer backward on the CUDA cores (FFMA), and the stand-alone
-// column sum used when C == 0.
+// fp32 linear-layer backward and forward on the CUDA cores (FFMA), and the
+// stand-alone column sum used when C == 0.
 //
 // fp32 storage needs fp32-accurate products: the page's harness turns TF32
 // off ("use fp32 to get accurate results for checking w.r.t. CPU", llm.c
@@ -17,6 +17,8 @@
 #include "../../include/mmbwd.h"
 #include "internal.h"
 
+#include <algorithm>
+
 namespace mmbwd {
 namespace {
 
@@ -24,11 +26,14 @@ constexpr int BM = SIMT_BM, BN = SIMT_BN, BK = SIMT_BK;
 constexpr int PAD = 4;  // keeps 16-byte alignment of smem rows
 
 // D (M x N, row-major) += A . B, with A either (M x K) row-major (A_KM = false)
-// or stored as (K x M) row-major (A_KM = true); B is (K x N) row-major.
-template <bool A_KM>
+// or stored as (K x M) row-major (A_KM = true); B is (K x N) row-major, or
+// stored as (N x K) row-major (B_NK = true). With OVERWRITE, D = A . B + bias
+// (bias per column, may be null) instead of the accumulation.
+template <bool A_KM, bool B_NK = false, bool OVERWRITE = false>
 __global__ void __launch_bounds__(SIMT_THREADS, 2)
     simt_gemm_acc(float* __restrict__ D, const float* __restrict__ A, const float* __restrict__ Bm,
-                  int64_t M, int64_t N, int64_t K, float* __restrict__ dbias) {
+                  int64_t M, int64_t N, int64_t K, float* __restrict__ dbias,
+                  const float* __restrict__ col_bias = nullptr) {
     __shared__ __align__(16) float As[2][BK][BM + PAD];
     __shared__ __align__(16) float Bs[2][BK][BN + PAD];
 
@@ -55,10 +60,17 @@ __global__ void __launch_bounds__(SIMT_THREADS, 2)
             ra = (k < K && m < M) ? *reinterpret_cast<const float4*>(A + k * M + m)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int64_t k = k0 + tid / 32;
-        const int64_t n = n0 + (tid % 32) * 4;
-        rb = (k < K && n < N) ? *reinterpret_cast<const float4*>(Bm + k * N + n)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!B_NK) {
+            const int64_t k = k0 + tid / 32;
+            const int64_t n = n0 + (tid % 32) * 4;
+            rb = (k < K && n < N) ? *reinterpret_cast<const float4*>(Bm + k * N + n)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            const int64_t n = n0 + tid / 2;
+            const int64_t k = k0 + (tid % 2) * 4;
+            rb = (n < N && k < K) ? *reinterpret_cast<const float4*>(Bm + n * K + k)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     };
     auto store_tile = [&](int buf) {
         if (!A_KM) {
@@ -70,7 +82,15 @@ __global__ void __launch_bounds__(SIMT_THREADS, 2)
         } else {
             *reinterpret_cast<float4*>(&As[buf][tid / 32][(tid % 32) * 4]) = ra;
         }
-        *reinterpret_cast<float4*>(&Bs[buf][tid / 32][(tid % 32) * 4]) = rb;
+        if (!B_NK) {
+            *reinterpret_cast<float4*>(&Bs[buf][tid / 32][(tid % 32) * 4]) = rb;
+        } else {
+            const int n = tid / 2, k = (tid % 2) * 4;
+            Bs[buf][k + 0][n] = rb.x;
+            Bs[buf][k + 1][n] = rb.y;
+            Bs[buf][k + 2][n] = rb.z;
+            Bs[buf][k + 3][n] = rb.w;
+        }
     };
 
     float acc[8][8];
@@ -119,7 +139,12 @@ __global__ void __launch_bounds__(SIMT_THREADS, 2)
             const int64_t n = n0 + tx * 4 + h * 64;
             if (n >= N) continue;  // N is a multiple of 4: a float4 is all in or all out
             float4* p = reinterpret_cast<float4*>(D + m * N + n);
-            float4 o = *p;
+            float4 o;
+            if (OVERWRITE) {
+                o = col_bias ? *reinterpret_cast<const float4*>(col_bias + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                o = *p;
+            }
             o.x += acc[i][h * 4 + 0];
             o.y += acc[i][h * 4 + 1];
             o.z += acc[i][h * 4 + 2];
@@ -154,6 +179,38 @@ cudaError_t simt_launch(float* dinp, float* dweight, float* dbias, const float* 
         dim3 grid(static_cast<unsigned>((OC + BM - 1) / BM), static_cast<unsigned>((C + BN - 1) / BN));
         if (grid.x && grid.y) simt_gemm_acc<true><<<grid, SIMT_THREADS, 0, stream>>>(dweight, dout, inp, OC, C, BT, dbias);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t simt_forward_launch(float* out, const float* inp, const float* weight, const float* bias,
+                                int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    // out: M = BT, N = OC, K = C; A = inp (BT x C), B = weight stored (OC x C)
+    dim3 grid(static_cast<unsigned>((BT + BM - 1) / BM), static_cast<unsigned>((OC + BN - 1) / BN));
+    if (grid.x && grid.y)
+        simt_gemm_acc<false, true, true><<<grid, SIMT_THREADS, 0, stream>>>(out, inp, weight, BT, OC, C, nullptr, bias);
+    return cudaGetLastError();
+}
+
+// out[r, o] = bias[o] (or 0 without a bias): the forward when C == 0.
+template <typename T>
+__global__ void fill_rows_kernel(T* __restrict__ out, const T* __restrict__ bias, int64_t rows, int64_t cols) {
+    const int64_t n = rows * cols;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = bias ? bias[i % cols] : static_cast<T>(0.f);
+}
+
+cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t cols, int dtype,
+                             cudaStream_t stream) {
+    const int64_t n = rows * cols;
+    if (n == 0) return cudaSuccess;
+    const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4096));
+    if (dtype == MMBWD_F32)
+        fill_rows_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<float*>(out), static_cast<const float*>(bias),
+                                                            rows, cols);
+    else
+        fill_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+            static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(bias), rows, cols);
     return cudaGetLastError();
 }
 

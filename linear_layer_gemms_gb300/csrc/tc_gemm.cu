@@ -211,6 +211,10 @@ __device__ __forceinline__ uint4 add_round8(uint4 old, const float (&s)[8]) {
     return r;
 }
 
+// FWD = false: the backward (dinp and dweight items); FWD = true: the forward
+// (dinp-type items with a K-major B and an overwrite epilogue). Two
+// instantiations, so that neither pays for the other's branches.
+template <bool FWD>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_mmbwd_kernel(const __grid_constant__ CUtensorMap tm_dout_k,   // dout, A of dinp (K-major)
                     const __grid_constant__ CUtensorMap tm_weight,   // weight, B of dinp (MN-major)
@@ -291,14 +295,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int row0 = prow * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
                 const int half = it.bn / 2;  // columns of B staged by this CTA
                 const int col0 = it.n_tile * it.bn + static_cast<int>(rank) * half;
+                const int64_t n_extent = FWD ? p.n_dinp : p.C;  // N of this item's product
                 int nb = 0;
-                for (int j = 0; j < half / 64; ++j) nb += (col0 + j * 64 < p.C) ? 1 : 0;
+                for (int j = 0; j < half / 64; ++j) nb += (col0 + j * 64 < n_extent) ? 1 : 0;
                 // With two pairs, the twin CTA needs the same B boxes: box j is loaded
                 // by the CTA of pair j and multicast to both.
                 const uint16_t bmask = static_cast<uint16_t>((1u << crank) | (1u << twin));
                 // Output tile of this CTA, prefetched into L2 a few k-blocks before the
                 // main loop ends so that the epilogue's read of the old values hits L2.
-                const bool direct = !(it.is_dw && p.splits > 1);
+                const bool direct = !(it.is_dw && p.splits > 1) && !FWD;  // forward: nothing to read back
                 const int64_t out_rows = it.is_dw ? p.OC : p.BT;
                 const int pf_kb = max(it.kb0, it.kb1 - 8);
                 int na;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(fb, bytes);
                     if (direct && kb == pf_kb && row0 < out_rows) {
                         for (int j = 0; j < it.bn / 128; ++j)
-                            if (it.n_tile * it.bn + j * 128 < p.C)
+                            if (it.n_tile * it.bn + j * 128 < n_extent)
                                 ptx::tma_prefetch_l2_2d(it.is_dw ? &tm_dw_out : &tm_dinp_out,
                                                         it.n_tile * it.bn + j * 128, row0);
                     }
@@ -328,11 +333,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, row0);
                     }
                     const void* tmB = it.is_dw ? static_cast<const void*>(&tm_inp) : static_cast<const void*>(&tm_weight);
+                    // B boxes: 64 columns x 64 k, MN-major (backward) or K-major (forward)
                     if (ppc == 1) {
-                        for (int j = 0; j < nb; ++j) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * TC_BK);
+                        for (int j = 0; j < nb; ++j) {
+                            if (FWD) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, kb * TC_BK, col0 + j * 64);
+                            else ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * TC_BK);
+                        }
                     } else if (static_cast<int>(pp) < nb) {
-                        ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, col0 + static_cast<int>(pp) * 64,
-                                                   kb * TC_BK, bmask);
+                        const int cj = col0 + static_cast<int>(pp) * 64;
+                        if (FWD) ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, kb * TC_BK, cj, bmask);
+                        else ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, cj, kb * TC_BK, bmask);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -364,7 +374,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * TC_BN;
-                    const uint32_t idesc = ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw, /*B MN*/ 1);
+                    const uint32_t idesc =
+                        ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw, /*B MN*/ FWD ? 0 : 1);
                     for (int kb = it.kb0; kb < it.kb1; ++kb) {
                         // Both CTAs' copies of this stage have landed (own bytes +
                         // the odd CTA's forwarded arrival).
@@ -385,7 +396,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             const uint64_t adesc =
                                 it.is_dw ? ptx::smem_desc_sw128(sA + k * 2048, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
-                            const uint64_t bdesc = ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
+                            // Forward: B is K-major like A (weight rows of 128 bytes of K).
+                            const uint64_t bdesc = FWD ? ptx::smem_desc_sw128(sB + k * 32, 16, 1024)
+                                                         : ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
                             ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
                         }
                         ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), empty_mask);
@@ -525,7 +538,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
             const int64_t qrow0 = static_cast<int64_t>(m_tile) * TC_BM + q * 32;  // first row of the quadrant
             const int col0 = it.n_tile * it.bn;
-            const int ncols = static_cast<int>(min(static_cast<int64_t>(it.bn), p.C - col0));
+            const int64_t n_extent = FWD ? p.n_dinp : p.C;  // columns and row stride of D
+            const int ncols = static_cast<int>(min(static_cast<int64_t>(it.bn), n_extent - col0));
             const int nchunks = it.bn / 32;
             __nv_bfloat16* D = it.is_dw ? p.dweight : p.dinp;
             bool rok[4];
@@ -534,7 +548,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int i = 0; i < 4; ++i) {
                 const int64_t row = qrow0 + 8 * i + r8;
                 rok[i] = row < rows_total;
-                drow[i] = D + (rok[i] ? row : 0) * p.C + col0 + cg;
+                drow[i] = D + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
             // All old output values of this tile, loaded before waiting for the
             // accumulator (the producer has prefetched them into L2).
@@ -543,7 +557,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int c = 0; c < TC_BN / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    oldw[c][i] = (!split_mode && c < nchunks && rok[i] && c * 32 + cg < ncols)
+                    oldw[c][i] = (!split_mode && !FWD && c < nchunks && rok[i] && c * 32 + cg < ncols)
                                      ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
                                      : make_uint4(0u, 0u, 0u, 0u);
 
@@ -585,8 +599,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         __stcg(reinterpret_cast<float4*>(pp), a4);
                         __stcg(reinterpret_cast<float4*>(pp + 4), b4);
                     } else if (rok[i] && c * 32 + cg < ncols) {
-                        const float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(oldw[c][i], s8);
+                        float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+                        uint4 base8 = oldw[c][i];  // zero for the forward: out = acc (+ bias)
+                        if (FWD && p.fwd_bias)
+                            base8 = *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg);
+                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(base8, s8);
                     }
                 }
                 __syncwarp();
@@ -788,8 +805,10 @@ bool g_attr_set[64];
 size_t tc_smem_bytes() { return SMEM_TOTAL; }
 
 int tc_max_active_clusters(int cluster_size) {
-    if (cudaFuncSetAttribute(tc_mmbwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(tc_mmbwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc_mmbwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+            cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster_size), 1, 1);
@@ -803,14 +822,16 @@ int tc_max_active_clusters(int cluster_size) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_mmbwd_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_mmbwd_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
+// The planner for a launch whose dinp-type product is (BT x N) += (BT x K) . (K x N)
+// with N = C and K = OC, plus, when `with_dw`, the dweight product.
+static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads, bool with_dw) {
     TcPlan pl{};
     pl.dinp_kb = ceil_div_i(OC, TC_BK);
     pl.dw_kb = ceil_div_i(BT, TC_BK);
@@ -829,7 +850,7 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quad
             force_dw_bn = b;
         }
     }
-    const int max_splits = std::max(1, std::min(pl.dw_kb, 16));
+    const int max_splits = with_dw ? std::max(1, std::min(pl.dw_kb, 16)) : 1;
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
     for (int ppc = 1; ppc <= 2; ++ppc) {
@@ -862,7 +883,7 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quad
                 c.n_dinp_items = c.dinp_tiles_m * c.dinp_tiles_n;
                 c.splits = S;
                 c.kb_per_split = kps;
-                c.n_dw_items = c.dw_tiles_m * c.dw_tiles_n * S;
+                c.n_dw_items = with_dw ? c.dw_tiles_m * c.dw_tiles_n * S : 0;
                 c.n_items = c.n_dw_items + c.n_dinp_items;
                 int pairs = std::max(1, std::min(c.n_items, max_clusters));  // clusters
                 if (force_grid > 0) pairs = static_cast<int>(std::max<long>(1, std::min<long>(force_grid / (2 * ppc), pairs)));
@@ -891,56 +912,53 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quad
     return pl;
 }
 
-cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
-                      const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC, void* ws,
-                      cudaStream_t stream) {
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
+    return make_plan_impl(BT, C, OC, num_sms, num_quads, true);
+}
+
+TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
+    // forward: N = OC, K = C, no dweight product
+    return make_plan_impl(BT, OC, C, num_sms, num_quads, false);
+}
+
+namespace {
+
+struct MapSpec {
+    const void* base;
+    uint64_t inner, outer;  // elements: contiguous dimension, rows
+    uint32_t box_inner, box_outer;
+    CUtensorMapSwizzle swz;
+};
+
+// Encodes the six tensor maps, completes the parameters from the plan, and
+// launches the kernel (and the split fixup when the plan splits dweight).
+cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParams& p, bool fwd, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     {
         std::lock_guard<std::mutex> g(g_attr_mutex);
         if (dev < 0 || dev >= 64 || !g_attr_set[dev]) {
-            e = cudaFuncSetAttribute(tc_mmbwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+            e = cudaFuncSetAttribute(tc_mmbwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(tc_mmbwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) g_attr_set[dev] = true;
         }
     }
     EncodeTiledFn encode = get_encode_tiled();
     if (!encode) return cudaErrorNotSupported;
-
     CUtensorMap maps[6];
-    struct MapSpec {
-        const void* base;
-        uint64_t inner, outer;
-        uint32_t box_inner, box_outer;
-        CUtensorMapSwizzle swz;
-    } specs[6] = {
-        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},  // dout, K-major A
-        {weight, static_cast<uint64_t>(C), static_cast<uint64_t>(OC), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},    // weight, MN-major B
-        {dout, static_cast<uint64_t>(OC), static_cast<uint64_t>(BT), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},     // dout, MN-major A
-        {inp, static_cast<uint64_t>(C), static_cast<uint64_t>(BT), 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},       // inp, MN-major B
-        {dinp, static_cast<uint64_t>(C), static_cast<uint64_t>(BT), 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},     // dinp, L2 prefetch
-        {dweight, static_cast<uint64_t>(C), static_cast<uint64_t>(OC), 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},  // dweight, L2 prefetch
-    };
     for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
         const cuuint64_t strides[1] = {specs[i].inner * 2};
         const cuuint32_t box[2] = {specs[i].box_inner, specs[i].box_outer};
         const cuuint32_t estr[2] = {1, 1};
         const CUresult r = encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(specs[i].base),
-                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                  specs[i].swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, specs[i].swz,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-
-    TcParams p{};
-    p.BT = BT;
-    p.C = C;
-    p.OC = OC;
-    p.dinp = static_cast<__nv_bfloat16*>(dinp);
-    p.dweight = static_cast<__nv_bfloat16*>(dweight);
-    p.dbias = static_cast<__nv_bfloat16*>(dbias);
     p.dinp_bn = plan.dinp_bn;
     p.dw_bn = plan.dw_bn;
     p.dinp_tiles_n = plan.dinp_tiles_n;
@@ -956,9 +974,6 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     p.n_items = plan.n_items;
     p.table = plan.table;
     p.ppc = plan.ppc;
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
-    p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
     p.timeout_ns = static_cast<unsigned long long>(env_long("MMBWD_WAIT_TIMEOUT_NS", static_cast<long>(DEFAULT_TIMEOUT_NS)));
 
     cudaLaunchConfig_t cfg{};
@@ -973,11 +988,64 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
-                           plan.sched);
+    if (fwd)
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<true>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                               plan.sched);
+    else
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<false>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                               plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     tc_splitk_fixup_kernel<<<plan.fixup_grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
+                      const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC, void* ws,
+                      cudaStream_t stream) {
+    const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
+    const MapSpec specs[6] = {
+        {dout, oc, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},        // dout, K-major A of dinp
+        {weight, c, oc, 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},          // weight, MN-major B of dinp
+        {dout, oc, bt, 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},           // dout, MN-major A of dweight
+        {inp, c, bt, 64, TC_BK, CU_TENSOR_MAP_SWIZZLE_128B},             // inp, MN-major B of dweight
+        {dinp, c, bt, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},           // dinp, L2 prefetch
+        {dweight, c, oc, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},        // dweight, L2 prefetch
+    };
+    TcParams p{};
+    p.BT = BT;
+    p.C = C;
+    p.OC = OC;
+    p.n_dinp = C;
+    p.dinp = static_cast<__nv_bfloat16*>(dinp);
+    p.dweight = static_cast<__nv_bfloat16*>(dweight);
+    p.dbias = static_cast<__nv_bfloat16*>(dbias);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
+    p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
+    return launch_common(plan, specs, p, false, stream);
+}
+
+cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight, const void* bias,
+                              int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
+    const MapSpec specs[6] = {
+        {inp, c, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},      // inp, K-major A
+        {weight, c, oc, TC_BK, 64, CU_TENSOR_MAP_SWIZZLE_128B},      // weight rows, K-major B (64 rows per box)
+        {inp, c, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},      // unused by forward items
+        {weight, c, oc, TC_BK, 64, CU_TENSOR_MAP_SWIZZLE_128B},      // unused
+        {out, oc, bt, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},       // unused (nothing read back)
+        {out, oc, bt, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE},       // unused
+    };
+    TcParams p{};
+    p.BT = BT;
+    p.C = C;
+    p.OC = OC;
+    p.n_dinp = OC;
+    p.fwd_bias = static_cast<const __nv_bfloat16*>(bias);
+    p.dinp = static_cast<__nv_bfloat16*>(out);
+    return launch_common(plan, specs, p, true, stream);
 }
 
 cudaError_t tc_read_status(int* code, int* info3, bool reset) {

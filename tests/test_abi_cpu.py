@@ -158,3 +158,15 @@ def test_workspace_size_formula():
         del _os.environ["MMBWD_SPLITK"]
     assert mm.mmbwd_workspace_bytes(1, 8, 64, 64, mm.F32) == 0
     assert mm.mmbwd_workspace_bytes(-1, 8, 64, 64, mm.BF16) == 0
+
+
+def test_forward_rejects_bad_arguments():
+    f = lambda **kw: mm.mmbwd_forward(**{**dict(out=A, inp=2 * A, weight=3 * A, bias=4 * A, B=2, T=8,  # noqa: E731
+                                                 C=64, OC=32, dtype=mm.BF16, stream=0), **kw})
+    assert f(dtype=3) == mm.ERR_DTYPE
+    assert f(T=-1) == mm.ERR_SHAPE
+    assert f(out=None) == mm.ERR_NULL
+    assert f(inp=2 * A + 4) == mm.ERR_ALIGN
+    assert f(C=12) == mm.ERR_ALIGN
+    assert f(out=2 * A + 32) == mm.ERR_ALIAS   # out overlaps inp
+    assert f(out=4 * A - 16) == mm.ERR_ALIAS   # out overlaps bias

@@ -1,0 +1,124 @@
+"""The forward out = inp . weight^T + bias through the C ABI against the
+oracle's forward, element by element."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import linear_layer_gemms_gb300 as mm
+import oracle
+import synth
+from gpu_helpers import TOL, assert_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    mm.load()
+    yield
+
+
+def run_fwd(x, BT, C, OC, dtype, bias=True):
+    import torch
+
+    g = {k: to_dev(v, dtype) for k, v in x.items()}
+    out = to_dev(synth.normal((BT, OC), dtype, 0, 99), dtype)  # garbage: must be overwritten
+    rc = mm.mmbwd_forward(out, g["inp"], g["weight"], g["bias"] if bias else None, 1, BT, C, OC,
+                          mm.BF16 if dtype == "bf16" else mm.F32)
+    assert rc == mm.OK, mm.strerror(rc)
+    torch.cuda.synchronize()
+    assert mm.mmbwd_device_status()[0] == mm.OK
+    return out
+
+
+def inputs(BT, C, OC, dtype, seed=0):
+    return {"inp": synth.normal((BT, C), dtype, seed, 61, 0.0, 1.0),
+            "weight": synth.normal((OC, C), dtype, seed, 62, 0.0, 0.02),
+            "bias": synth.normal((OC,), dtype, seed, 63, 0.0, 0.02)}
+
+
+SHAPES = [(1, 8, 8), (200, 136, 200), (300, 392, 1032), (129, 256, 136), (640, 1600, 264)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("bias", [True, False])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_forward_parity(shape, dtype, bias):
+    BT, C, OC = shape
+    x = inputs(BT, C, OC, dtype)
+    out = run_fwd(x, BT, C, OC, dtype, bias)
+    ref = oracle.get("omp").forward_rows(x["inp"], x["weight"], dtype, bias=x["bias"] if bias else None)
+    assert_close(to_host(out, dtype), ref, dtype, "out")
+
+
+@pytest.mark.parametrize("ppc", [1, 2])
+@pytest.mark.parametrize("tile_n", ["256,256", "128,128"])
+def test_forward_cluster_modes(monkeypatch, ppc, tile_n):
+    BT, C, OC = 600, 520, 776
+    monkeypatch.setenv("MMBWD_PPC", str(ppc))
+    monkeypatch.setenv("MMBWD_TILE_N", tile_n)
+    x = inputs(BT, C, OC, "bf16", seed=3)
+    out = run_fwd(x, BT, C, OC, "bf16")
+    ref = oracle.get("omp").forward_rows(x["inp"], x["weight"], "bf16", bias=x["bias"])
+    assert_close(to_host(out, "bf16"), ref, "bf16", "out")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_forward_integer_case_exact(dtype):
+    g = json.load(open(os.path.join(GOLDEN, "int_case.json")))
+    inp = np.array(g["inputs"]["inp"], dtype=np.float64)
+    w = np.array(g["inputs"]["weight"], dtype=np.float64)
+    b = np.arange(w.shape[0], dtype=np.float64) - 3
+    conv = (lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)) if dtype == "bf16" \
+        else (lambda a: a.astype(np.float32))
+    x = {"inp": conv(inp), "weight": conv(w), "bias": conv(b)}
+    out = run_fwd(x, inp.shape[0], inp.shape[1], w.shape[0], dtype)
+    assert np.array_equal(to_host(out, dtype), inp @ w.T + b)
+
+
+def test_forward_degenerate_and_deterministic():
+    import torch
+
+    # C == 0: out = bias
+    BT, OC = 33, 64
+    b = to_dev(synth.normal((OC,), "bf16", 0, 64), "bf16")
+    out = to_dev(synth.normal((BT, OC), "bf16", 0, 65), "bf16")
+    assert mm.mmbwd_forward(out, None, None, b, 1, BT, 0, OC, mm.BF16) == mm.OK
+    torch.cuda.synchronize()
+    assert torch.equal(out, b.expand(BT, OC))
+    # repeated runs are bitwise identical
+    BT, C, OC = 1024, 768, 3072
+    x = inputs(BT, C, OC, "bf16", seed=4)
+    first = run_fwd(x, BT, C, OC, "bf16").cpu()
+    for _ in range(5):
+        assert torch.equal(run_fwd(x, BT, C, OC, "bf16").cpu(), first)
+
+
+FULL = [("mlp_fc", 8192, 768, 3072, "bf16"), ("mlp_fc_proj", 8192, 3072, 768, "bf16"),
+        ("attn_proj", 8192, 768, 768, "bf16"), ("lm_head", 8192, 768, 50304, "bf16"),
+        ("xl_fc_f32", 4096, 1600, 6400, "f32")]
+
+
+@pytest.mark.parametrize("case", FULL, ids=lambda c: c[0])
+def test_forward_full_size_sampled(case, monkeypatch):
+    import torch
+
+    monkeypatch.delenv("MMBWD_PPC", raising=False)
+    monkeypatch.delenv("MMBWD_TILE_N", raising=False)
+    name, BT, C, OC, dt = case
+    x = inputs(BT, C, OC, dt, seed=5)
+    out = run_fwd(x, BT, C, OC, dt, bias=name != "lm_head")
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, BT - 1], rng.integers(0, BT, 24)]))
+    ref = oracle.get("omp").forward_rows(x["inp"], x["weight"], dt, rows,
+                                         bias=x["bias"] if name != "lm_head" else None)
+    got = to_host(out[torch.from_numpy(rows).to(out.device)], dt)
+    assert_close(got, ref, dt, name)
