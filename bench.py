@@ -484,6 +484,45 @@ def measure_other_configs(torch, mm, dev, stream, reps=10):
                      "plan": {k: info[k] for k in ("path", "grid", "items", "splits", "launches")}}
         del t
         torch.cuda.empty_cache()
+    # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
+    for name, lname in (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
+                        ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32")):
+        wl, _, i = lname.partition(":")
+        layer = synth.WORKLOADS[wl].layers[int(i or 0)]
+        x = synth.make_inputs(layer, seed=0)
+        t = {k: to_device_tensor(torch, x[k], dev) for k in ("inp", "weight", "dbias")}
+        o = torch.empty((layer.BT, layer.OC), dtype=t["inp"].dtype, device=dev)
+        dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
+
+        def fcall():
+            rc = mm.mmbwd_forward(o.data_ptr(), t["inp"].data_ptr(), t["weight"].data_ptr(),
+                                  t["dbias"].data_ptr() if layer.bias else None, layer.B, layer.T,
+                                  layer.C, layer.OC, dt, stream.cuda_stream)
+            if rc != mm.OK:
+                raise RuntimeError(mm.strerror(rc))
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fcall()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                fcall()
+                b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+        sec = statistics.median(times)
+        flops = 2 * layer.BT * layer.C * layer.OC + (layer.BT * layer.OC if layer.bias else 0)
+        tf = flops / sec / 1e12
+        peak = float(peaks["bf16_tflops"]) if layer.dtype == "bf16" else fp32_peak
+        out[name] = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
+                     "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2),
+                     "frac_of_peak": round(tf / peak, 4)}
+        del t, o
+        torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
         raise RuntimeError(f"device status after other configs: {mm.strerror(status)} {info}")
