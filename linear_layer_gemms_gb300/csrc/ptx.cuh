@@ -270,6 +270,17 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
                  : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this launch depends on have completed and their
+// memory is visible (returns at once when launched without such a dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next launch on the stream start its prologue on SMs this grid frees.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- misc
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

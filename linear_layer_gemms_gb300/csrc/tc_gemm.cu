@@ -270,6 +270,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     ptx::cluster_sync();  // every CTA's barriers exist before any remote arrive or multicast
     ptx::tc_fence_after();
+    // Everything above overlaps the previous launch on the stream; global memory
+    // is touched only after it has completed.
+    ptx::grid_dependency_wait();
     const uint32_t tmem_base = misc[0];
     const Waiter wt{misc + 1, p.timeout_ns};
 
@@ -628,6 +631,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
 
+    // Each thread is done with its role: the next launch on the stream may start
+    // its prologue on SMs this grid frees (every thread signals; measured faster
+    // than a single signalling thread).
+    ptx::grid_launch_dependents();
     ptx::tc_fence_before();
     __syncthreads();
     // The even CTA's MMAs (which write this CTA's tensor memory and read its
@@ -645,6 +652,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // thread per 8-column vector of dweight; all loads are independent, so the
 // pass runs at memory speed with the partials still in L2.
 __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) {
+    ptx::grid_dependency_wait();  // the partials of the GEMM launch before this one
     const int64_t vec_per_row = p.C / 8;
     const int64_t nvec = p.OC * vec_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -981,13 +989,17 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_TOTAL;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(2 * plan.ppc);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the prologue may start while the previous
+    // kernel on the stream finishes; the kernel waits for it before any load.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (fwd)
         e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<true>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
@@ -995,8 +1007,13 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
         e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<false>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
-    tc_splitk_fixup_kernel<<<plan.fixup_grid, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t fcfg{};
+    fcfg.gridDim = dim3(static_cast<unsigned>(plan.fixup_grid), 1, 1);
+    fcfg.blockDim = dim3(256, 1, 1);
+    fcfg.stream = stream;
+    fcfg.attrs = attr + 1;
+    fcfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&fcfg, tc_splitk_fixup_kernel, p);
 }
 
 }  // namespace
