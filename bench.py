@@ -443,53 +443,86 @@ def run_gpu(args):
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 
 
-def measure_other_configs(torch, mm, dev, stream, reps=10):
-    """The remaining configurations of the workload set, each one mmbwd_run
-    call on device-resident inputs, timed with CUDA events (median of `reps`
-    launches after warm-up), reported with their plan and the fraction of the
-    peak that bounds them (bf16 tensor peak; the fp32 path against the FP32
-    ALU peak of 152 SMs x 128 lanes x 2 FLOP at the maximum SM clock)."""
+L2_BYTES = 129 * 1024 * 1024
+
+
+def time_back_to_back(torch, stream, calls, per_batch, batches=5):
+    """Median over `batches` of (time of `per_batch` back-to-back calls) /
+    per_batch, CUDA events on `stream`; the calls cycle through `calls` (one
+    per resident input set) so that consecutive calls touch different memory."""
+    with torch.cuda.stream(stream):
+        for c in calls * 2:
+            c()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(batches):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for k in range(per_batch):
+                calls[k % len(calls)]()
+            b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) / 1e3 / per_batch)
+    return statistics.median(times)
+
+
+def input_sets(nbytes_one, cap=8):
+    """How many copies of a configuration's tensors to rotate through so that
+    they span more than the L2 (capped; tiny problems stay L2-resident)."""
+    return max(1, min(cap, -(-2 * L2_BYTES // max(nbytes_one, 1))))
+
+
+def measure_other_configs(torch, mm, dev, stream):
+    """The remaining configurations of the workload set and the forward of the
+    GPT-2 layers: back-to-back calls on device-resident inputs rotated over
+    enough copies to exceed the L2 (see `input_sets`), timed with CUDA events,
+    reported with their plan and the fraction of the peak that bounds them
+    (bf16 tensor peak; the fp32 path against the FP32 ALU peak of 152 SMs x 128
+    lanes x 2 FLOP at the maximum SM clock)."""
     peaks, _ = measured_peaks()
     fp32_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    sh = stream.cuda_stream
     out = {}
-    for name in OTHER_CONFIGS:
-        layer = synth.WORKLOADS[name].layers[0]
-        x = synth.make_inputs(layer, seed=0)
-        t = {k: to_device_tensor(torch, v, dev) for k, v in x.items()}
-        dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
 
-        def call():
-            rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
-                              t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
-                              t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T, layer.C,
-                              layer.OC, dt, stream.cuda_stream)
-            if rc != mm.OK:
-                raise RuntimeError(mm.strerror(rc))
-
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                call()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                call()
-                b.record(stream)
-            b.synchronize()
-            times.append(a.elapsed_time(b) / 1e3)
-        sec = statistics.median(times)
-        tf = layer.flops() / sec / 1e12
+    def finish(name, layer, flops, sec, n_sets, set_bytes, plan=None):
+        tf = flops / sec / 1e12
         peak = float(peaks["bf16_tflops"]) if layer.dtype == "bf16" else fp32_peak
-        info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
         out[name] = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
                      "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2),
                      "frac_of_peak": round(tf / peak, 4),
                      "peak": "bf16 tensor (measured)" if layer.dtype == "bf16" else
                              f"fp32 ALU {fp32_peak:.1f} TFLOP/s (152 SMs x 128 lanes x 2 x max clock)",
-                     "plan": {k: info[k] for k in ("path", "grid", "items", "splits", "launches")}}
-        del t
+                     "input_sets": n_sets,
+                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
+        if plan is not None:
+            out[name]["plan"] = plan
+
+    for name in OTHER_CONFIGS:
+        layer = synth.WORKLOADS[name].layers[0]
+        x = synth.make_inputs(layer, seed=0)
+        set_bytes = sum(v.nbytes for v in x.values())
+        n_sets = input_sets(set_bytes)
+        sets = [{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for _ in range(n_sets)]
+        dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
+
+        def make_call(t, layer=layer, dt=dt):
+            def call():
+                rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
+                                  t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
+                                  t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T,
+                                  layer.C, layer.OC, dt, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return call
+
+        calls = [make_call(t) for t in sets]
+        per_batch = max(len(calls), 20 if layer.flops() < 5e11 else 8)
+        sec = time_back_to_back(torch, stream, calls, per_batch)
+        info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
+        finish(name, layer, layer.flops(), sec, n_sets, set_bytes,
+               {k: info[k] for k in ("path", "grid", "items", "splits", "launches")})
+        del sets, calls
         torch.cuda.empty_cache()
     # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
     for name, lname in (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
@@ -497,38 +530,30 @@ def measure_other_configs(torch, mm, dev, stream, reps=10):
         wl, _, i = lname.partition(":")
         layer = synth.WORKLOADS[wl].layers[int(i or 0)]
         x = synth.make_inputs(layer, seed=0)
-        t = {k: to_device_tensor(torch, x[k], dev) for k in ("inp", "weight", "dbias")}
-        o = torch.empty((layer.BT, layer.OC), dtype=t["inp"].dtype, device=dev)
+        set_bytes = x["inp"].nbytes + x["weight"].nbytes + x["dbias"].nbytes + layer.BT * layer.OC * x["inp"].itemsize
+        n_sets = input_sets(set_bytes)
+        sets = []
+        for _ in range(n_sets):
+            t = {k: to_device_tensor(torch, x[k], dev) for k in ("inp", "weight", "dbias")}
+            t["out"] = torch.empty((layer.BT, layer.OC), dtype=t["inp"].dtype, device=dev)
+            sets.append(t)
         dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
 
-        def fcall():
-            rc = mm.mmbwd_forward(o.data_ptr(), t["inp"].data_ptr(), t["weight"].data_ptr(),
-                                  t["dbias"].data_ptr() if layer.bias else None, layer.B, layer.T,
-                                  layer.C, layer.OC, dt, stream.cuda_stream)
-            if rc != mm.OK:
-                raise RuntimeError(mm.strerror(rc))
+        def make_fcall(t, layer=layer, dt=dt):
+            def fcall():
+                rc = mm.mmbwd_forward(t["out"].data_ptr(), t["inp"].data_ptr(), t["weight"].data_ptr(),
+                                      t["dbias"].data_ptr() if layer.bias else None, layer.B, layer.T,
+                                      layer.C, layer.OC, dt, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return fcall
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                fcall()
-        torch.cuda.synchronize()
-        times = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                fcall()
-                b.record(stream)
-            b.synchronize()
-            times.append(a.elapsed_time(b) / 1e3)
-        sec = statistics.median(times)
+        calls = [make_fcall(t) for t in sets]
         flops = 2 * layer.BT * layer.C * layer.OC + (layer.BT * layer.OC if layer.bias else 0)
-        tf = flops / sec / 1e12
-        peak = float(peaks["bf16_tflops"]) if layer.dtype == "bf16" else fp32_peak
-        out[name] = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
-                     "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2),
-                     "frac_of_peak": round(tf / peak, 4)}
-        del t, o
+        per_batch = max(len(calls), 20 if flops < 2.5e11 else 8)
+        sec = time_back_to_back(torch, stream, calls, per_batch)
+        finish(name, layer, flops, sec, n_sets, set_bytes)
+        del sets, calls
         torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
