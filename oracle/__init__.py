@@ -2,8 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product library never imports it.
-``mmbwd_oracle.c`` states what is computed and which readings of the CPU
-reference it takes.
+``mmbwd_oracle.c`` (the linear layer) and ``layernorm_oracle.c`` (the
+LayerNorm backward) state what is computed and which readings of the CPU
+references they take.
 
 Builds (gcc, -O2, -ffp-contract=off, no -ffast-math):
   * ``st``  - single-threaded
@@ -20,14 +21,14 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "mmbwd_oracle.c")
+_SRCS = (os.path.join(_HERE, "mmbwd_oracle.c"), os.path.join(_HERE, "layernorm_oracle.c"))
 _BUILD = os.path.join(_HERE, "_build")
 _lock = threading.Lock()
 _libs: dict = {}
 
 F32, BF16, F64 = 0, 1, 2
 DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
-MUTANTS = tuple(range(1, 11))
+MUTANTS = tuple(range(1, 16))
 
 
 def lib_path(variant: str) -> str:
@@ -37,7 +38,7 @@ def lib_path(variant: str) -> str:
 def build(variant: str = "st", force: bool = False) -> str:
     """Compile one variant of the oracle and return the path of its .so."""
     out = lib_path(variant)
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= max(map(os.path.getmtime, _SRCS)):
         return out
     os.makedirs(_BUILD, exist_ok=True)
     flags = ["-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11"]
@@ -48,7 +49,7 @@ def build(variant: str = "st", force: bool = False) -> str:
     elif variant != "st":
         raise ValueError(variant)
     tmp = out + f".{os.getpid()}.tmp"
-    subprocess.check_call(["gcc", *flags, _SRC, "-o", tmp])
+    subprocess.check_call(["gcc", *flags, *_SRCS, "-o", tmp, "-lm"])
     os.replace(tmp, out)
     return out
 
@@ -64,8 +65,13 @@ class Oracle:
         lib.oracle_dweight_rows.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
         lib.oracle_matmul_backward.argtypes = [vp] * 8 + [i64] * 4 + [ci]
         lib.oracle_forward_rows.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, ci]
+        lib.oracle_layernorm_forward.argtypes = [vp] * 6 + [i64, i64, ci]
+        lib.oracle_layernorm_dinp_rows.argtypes = [vp, vp, i64] + [vp] * 6 + [ci, i64, i64, ci]
+        lib.oracle_layernorm_params.argtypes = [vp] * 8 + [ci, i64, i64, ci]
         for f in (lib.oracle_dinp_rows, lib.oracle_dweight_rows, lib.oracle_matmul_backward,
-                  lib.oracle_forward_rows, lib.oracle_threads, lib.oracle_mutant):
+                  lib.oracle_forward_rows, lib.oracle_threads, lib.oracle_mutant,
+                  lib.oracle_layernorm_forward, lib.oracle_layernorm_dinp_rows,
+                  lib.oracle_layernorm_params):
             f.restype = ci
         self._lib = lib
 
@@ -148,6 +154,63 @@ class Oracle:
             1, BT, C, OC, dt)
         assert rc == 0
         return dinp, dweight, dbias
+
+
+    # ------------------------------------------------------------------ LayerNorm backward
+
+    def layernorm_forward(self, inp, weight, bias, dtype: str, want_out=True):
+        """(out or None, mean, rstd) of the layer norm of each row of ``inp``, in float64."""
+        dt = DTYPES[dtype]
+        BT, C = inp.shape
+        for a in (inp, weight, bias):
+            self._check(a, dt)
+        out = np.empty((BT, C), dtype=np.float64) if want_out else None
+        mean = np.empty(BT, dtype=np.float64)
+        rstd = np.empty(BT, dtype=np.float64)
+        rc = self._lib.oracle_layernorm_forward(self._ptr(out), mean.ctypes.data, rstd.ctypes.data,
+                                                inp.ctypes.data, weight.ctypes.data, self._ptr(bias),
+                                                BT, C, dt)
+        assert rc == 0
+        return out, mean, rstd
+
+    @staticmethod
+    def _stat(a):
+        code = {np.dtype(np.float32): F32, np.dtype(np.float64): F64}[a.dtype]
+        assert a.flags.c_contiguous
+        return code
+
+    def layernorm_dinp_rows(self, dout, inp, weight, mean, rstd, dtype: str, rows=None, dinp_init=None):
+        """Rows ``rows`` (all if None) of dinp_init + the LayerNorm input gradient, in float64."""
+        dt = DTYPES[dtype]
+        BT, C = inp.shape
+        for a in (dout, inp, weight, dinp_init):
+            self._check(a, dt)
+        sd = self._stat(mean)
+        assert self._stat(rstd) == sd
+        r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = BT if r is None else len(r)
+        out = np.empty((n, C), dtype=np.float64)
+        rc = self._lib.oracle_layernorm_dinp_rows(out.ctypes.data, self._ptr(r), n, self._ptr(dinp_init),
+                                                  dout.ctypes.data, inp.ctypes.data, weight.ctypes.data,
+                                                  mean.ctypes.data, rstd.ctypes.data, sd, BT, C, dt)
+        assert rc == 0
+        return out
+
+    def layernorm_params(self, dout, inp, mean, rstd, dtype: str, dweight_init=None, dbias_init=None):
+        """(dweight, dbias) of the LayerNorm backward added to their initial values, in float64."""
+        dt = DTYPES[dtype]
+        BT, C = inp.shape
+        for a in (dout, inp, dweight_init, dbias_init):
+            self._check(a, dt)
+        sd = self._stat(mean)
+        assert self._stat(rstd) == sd
+        dw = np.empty(C, dtype=np.float64)
+        db = np.empty(C, dtype=np.float64)
+        rc = self._lib.oracle_layernorm_params(dw.ctypes.data, db.ctypes.data, self._ptr(dweight_init),
+                                               self._ptr(dbias_init), dout.ctypes.data, inp.ctypes.data,
+                                               mean.ctypes.data, rstd.ctypes.data, sd, BT, C, dt)
+        assert rc == 0
+        return dw, db
 
 
 def get(variant: str = "st") -> Oracle:

@@ -306,3 +306,8 @@ ALL_PINS = [pin_exact_unit_differences, pin_central_differences, pin_library_mat
             pin_colsum_invariant, pin_adjoint_identities, pin_special_cases,
             pin_double_accumulation, pin_storage_types, pin_subset_rows, pin_null_bias,
             pin_empty_dims, pin_forward_exact_integers, pin_forward_library_and_adjoint]
+
+# The LayerNorm backward's pins live beside these; the mutant test runs them all.
+from oracle_pins_ln import LN_PINS  # noqa: E402
+
+ALL_PINS = ALL_PINS + LN_PINS
