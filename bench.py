@@ -441,6 +441,7 @@ def run_gpu(args):
 
 
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
+LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32")
 
 
 L2_BYTES = 129 * 1024 * 1024
@@ -553,6 +554,44 @@ def measure_other_configs(torch, mm, dev, stream):
         per_batch = max(len(calls), 20 if flops < 2.5e11 else 8)
         sec = time_back_to_back(torch, stream, calls, per_batch)
         finish(name, layer, flops, sec, n_sets, set_bytes)
+        del sets, calls
+        torch.cuda.empty_cache()
+    # the LayerNorm backward (lnbwd_run): bound by HBM, reported in GB/s of
+    # algorithmic bytes against the measured copy bandwidth
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    for name in LN_CONFIGS:
+        p = synth.LN_WORKLOADS[name]
+        x = synth.make_ln_inputs(p, seed=0)
+        # row statistics as the forward caches them (fp32), computed on the host
+        xi = synth.to_f64(x["inp"], p.dtype)
+        mean = xi.mean(axis=1).astype(np.float32)
+        rstd = (1.0 / np.sqrt(xi.var(axis=1) + 1e-5)).astype(np.float32)
+        set_bytes = p.bytes()
+        n_sets = input_sets(set_bytes)
+        sets = []
+        for _ in range(n_sets):
+            t = {k: to_device_tensor(torch, v, dev) for k, v in x.items()}
+            t["mean"], t["rstd"] = torch.from_numpy(mean).to(dev), torch.from_numpy(rstd).to(dev)
+            sets.append(t)
+        dt = mm.BF16 if p.dtype == "bf16" else mm.F32
+
+        def make_lcall(t, p=p, dt=dt):
+            def lcall():
+                rc = mm.lnbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(), t["dbias"].data_ptr(),
+                                  t["dout"].data_ptr(), t["inp"].data_ptr(), t["weight"].data_ptr(),
+                                  t["mean"].data_ptr(), t["rstd"].data_ptr(), p.B, p.T, p.C, dt, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return lcall
+
+        calls = [make_lcall(t) for t in sets]
+        sec = time_back_to_back(torch, stream, calls, max(len(calls), 40))
+        gbs = p.bytes() / sec / 1e9
+        out[name] = {"B": p.B, "T": p.T, "C": p.C, "dtype": p.dtype, "us": round(sec * 1e6, 2),
+                     "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
+                     "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": p.bytes(),
+                     "input_sets": n_sets,
+                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
         del sets, calls
         torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)

@@ -10,7 +10,8 @@ first use instead of falling back to anything else.
     dweight (OC,C)   += dout^T . inp
     dbias   (OC)      = sum over (b,t) of dout        (NULL / None skips it)
 
-and the layer's forward, out = inp . weight^T + bias (mmbwd_forward).
+and the layer's forward, out = inp . weight^T + bias (mmbwd_forward); plus the
+LayerNorm backward of a GPT-2 block (lnbwd_run, include/layernorm_backward.h).
 
 Pointers may be given as integers or as objects with ``data_ptr()`` (for
 example torch tensors on the current CUDA device); ``stream`` is a raw
@@ -34,7 +35,8 @@ STATIC_SCRATCH_BYTES = 32 << 20  # MMBWD_STATIC_SCRATCH_BYTES
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmmbwd.so")
 
-# Names and C signatures of every entry point declared in include/mmbwd.h.
+# Names and C signatures of every entry point declared in include/mmbwd.h and
+# include/layernorm_backward.h.
 _vp, _i64, _ci, _u64, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
                              ctypes.c_size_t)
 SIGNATURES = {
@@ -49,7 +51,10 @@ SIGNATURES = {
     "mmbwd_debug_fail_next_alloc": ([_ci], None),
     "mmbwd_run_static_scratch": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
     "mmbwd_forward": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
+    "lnbwd_run": ([_vp] * 8 + [_i64] * 3 + [_ci, _vp], _ci),
+    "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
+LNBWD_MAX_C = {F32: 2048, BF16: 4096}  # LNBWD_MAX_C_F32, LNBWD_MAX_C_BF16
 
 _lock = threading.Lock()
 _lib = None
@@ -118,6 +123,18 @@ def mmbwd_forward(out, inp, weight, bias, B: int, T: int, C: int, OC: int, dtype
     """Enqueue out = inp . weight^T + bias (bias may be None); returns the status."""
     return load().mmbwd_forward(_ptr(out), _ptr(inp), _ptr(weight), _ptr(bias), B, T, C, OC, dtype,
                                 _stream(stream))
+
+
+def lnbwd_run(dinp, dweight, dbias, dout, inp, weight, mean, rstd, B: int, T: int, C: int, dtype: int,
+              stream=None) -> int:
+    """Enqueue the LayerNorm backward (dinp, dweight and dbias all +=); mean
+    and rstd are fp32 row statistics; returns the C status code."""
+    return load().lnbwd_run(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp), _ptr(weight),
+                            _ptr(mean), _ptr(rstd), B, T, C, dtype, _stream(stream))
+
+
+def lnbwd_workspace_bytes(B: int, T: int, C: int, dtype: int) -> int:
+    return int(load().lnbwd_workspace_bytes(B, T, C, dtype))
 
 
 def mmbwd_workspace_bytes(B: int, T: int, C: int, OC: int, dtype: int) -> int:

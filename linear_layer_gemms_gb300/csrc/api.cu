@@ -2,6 +2,7 @@
 // the per-device workspace and the launches. See include/mmbwd.h for the
 // contract of every entry point.
 #include "../../include/mmbwd.h"
+#include "../../include/layernorm_backward.h"
 #include "internal.h"
 
 #include <cuda.h>
@@ -390,6 +391,95 @@ int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bi
     }
     const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads, 1);
     e = tc_launch_forward(plan, out, inp, weight, bias, s.BT, C, OC, stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// LayerNorm backward (layernorm_backward.h)
+
+namespace {
+
+struct LnShape {
+    int64_t BT = 0, n = 0;
+    size_t es = 0;
+};
+
+int ln_check_shape(int64_t B, int64_t T, int64_t C, int dtype, LnShape* s) {
+    if (dtype != MMBWD_F32 && dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    if (B < 0 || T < 0 || C < 0) return MMBWD_ERR_SHAPE;
+    if (!mul_ok(B, T, &s->BT) || !mul_ok(s->BT, C, &s->n)) return MMBWD_ERR_SHAPE;
+    if (C > (dtype == MMBWD_F32 ? LNBWD_MAX_C_F32 : LNBWD_MAX_C_BF16)) return MMBWD_ERR_SHAPE;
+    s->es = dtype == MMBWD_F32 ? 4 : 2;
+    int64_t bytes = 0;
+    if (!mul_ok(s->n, static_cast<int64_t>(s->es), &bytes)) return MMBWD_ERR_SHAPE;
+    return MMBWD_OK;
+}
+
+int ln_num_sms(int* sms) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MMBWD_ERR_CUDA;
+    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? MMBWD_OK
+                                                                                          : MMBWD_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t lnbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int dtype) {
+    LnShape s;
+    if (ln_check_shape(B, T, C, dtype, &s) != MMBWD_OK || s.BT == 0 || C == 0) return 0;
+    if (C % ln_vec_elems(dtype) != 0) return 0;
+    int sms = 0;
+    if (ln_num_sms(&sms) != MMBWD_OK) return 0;
+    LnPlan plan;
+    if (ln_make_plan(s.BT, static_cast<int>(C), dtype, sms, &plan) != cudaSuccess) return 0;
+    return plan.ws_bytes;
+}
+
+int lnbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+              const float* mean, const float* rstd, int64_t B, int64_t T, int64_t C, int dtype,
+              cudaStream_t stream) {
+    LnShape s;
+    int rc = ln_check_shape(B, T, C, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = s.es;
+    const size_t b_rows = static_cast<size_t>(s.n) * es, b_col = static_cast<size_t>(C) * es,
+                 b_stat = static_cast<size_t>(s.BT) * 4;
+    // NULL only where the tensor is empty.
+    if ((b_rows && (!dinp || !dout || !inp)) || (b_col && (!dweight || !dbias || !weight)) ||
+        (b_stat && (!mean || !rstd)))
+        return MMBWD_ERR_NULL;
+    const void* vec_ptrs[6] = {dinp, dweight, dbias, dout, inp, weight};
+    for (const void* p : vec_ptrs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(mean) | reinterpret_cast<uintptr_t>(rstd)) & 3u) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+
+    const void* outs[3] = {dinp, dweight, dbias};
+    const size_t nouts[3] = {b_rows, b_col, b_col};
+    const void* ins[5] = {dout, inp, weight, mean, rstd};
+    const size_t nins[5] = {b_rows, b_rows, b_col, b_stat, b_stat};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return MMBWD_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return MMBWD_ERR_ALIAS;
+    }
+
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    if (s.BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
+    int sms = 0;
+    rc = ln_num_sms(&sms);
+    if (rc != MMBWD_OK) return rc;
+    LnPlan plan;
+    if (ln_make_plan(s.BT, static_cast<int>(C), dtype, sms, &plan) != cudaSuccess) return MMBWD_ERR_CUDA;
+    rc = ensure_workspace(*d, plan.ws_bytes, stream);
+    if (rc != MMBWD_OK) return rc;
+    const cudaError_t e = ln_launch(plan, dinp, dweight, dbias, dout, inp, weight, mean, rstd, s.BT,
+                                    static_cast<int>(C), dtype, d->ws, stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
 }
 

@@ -156,4 +156,21 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
+// ---------------------------------------------------------------- LayerNorm backward
+
+struct LnPlan {
+    int vpl = 0;             // 16-byte vectors per lane (row width covered: 32 * vpl vectors)
+    int warps = 0;           // warps per block, one row at a time each
+    int grid = 0;            // blocks, each a contiguous range of rows
+    int64_t rows_per_block = 0;
+    size_t smem = 0;         // weight (fp32) + per-warp dweight / dbias sums
+    size_t ws_bytes = 0;     // per-block partial sums, fp32 [grid][2][C]
+};
+
+int ln_vec_elems(int dtype);
+cudaError_t ln_make_plan(int64_t BT, int C, int dtype, int num_sms, LnPlan* plan);
+cudaError_t ln_launch(const LnPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
+                      const void* inp, const void* weight, const float* mean, const float* rstd, int64_t BT,
+                      int C, int dtype, void* ws, cudaStream_t stream);
+
 }  // namespace mmbwd

@@ -194,3 +194,81 @@ def make_inputs(layer: Layer, seed: int = 0) -> dict:
         out["dweight"] = np.zeros((OC, C), dtype=_NP[_DT[dt]])
     out["dbias"] = normal((OC,), dt, seed, s("dbias_init"), 0.0, 1.0)
     return out
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm backward workloads (llm.c dev/cuda/layernorm_backward.cu: B=8, T=1024,
+# C=1600 in its main; C=768 is GPT-2 small's width)
+# ---------------------------------------------------------------------------
+
+# Stream ids of the LayerNorm inputs (disjoint from the linear layers' ids).
+LN_STREAM = {"inp_z": 257, "inp_shift": 258, "inp_scale": 259, "weight": 260, "dout": 261,
+             "dinp_init": 262, "dweight_init": 263, "dbias_init": 264}
+
+
+@dataclass(frozen=True)
+class LNProblem:
+    """One LayerNorm backward problem: inp, dout, dinp (B,T,C); weight, dweight, dbias (C).
+
+    inp rows are shift + scale * N(0,1) with a per-row shift ~ N(0, 0.5) and a
+    per-row scale exp(N(0, 0.5)), so that the row statistics differ from row
+    to row; weight ~ N(1, 0.1) (GPT-2 initialises it to one); dout ~ N(0, 1e-2)
+    like the gradients the linear layers produce; dinp, dweight and dbias start
+    from N(0, init_std) noise so that accumulation is visible."""
+    name: str
+    B: int
+    T: int
+    C: int
+    dtype: str
+    dout_std: float = 1e-2
+    init_std: float = 1e-2
+
+    @property
+    def BT(self) -> int:
+        return self.B * self.T
+
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: dout and inp read, dinp read and written,
+        weight read, dweight and dbias read and written, mean and rstd read."""
+        s = self.elem_bytes()
+        return 4 * self.BT * self.C * s + 5 * self.C * s + 8 * self.BT
+
+
+LN_WORKLOADS = {
+    "ln_tiny": LNProblem("ln_tiny", 2, 48, 72, "f32", dout_std=1.0),
+    "ln_gpt2_small": LNProblem("ln_gpt2_small", 8, 1024, 768, "bf16"),
+    "ln_xl": LNProblem("ln_xl", 8, 1024, 1600, "bf16"),
+    "ln_xl_f32": LNProblem("ln_xl_f32", 8, 1024, 1600, "f32"),
+}
+
+
+def round_to(a64: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 -> float32 (RNE) -> bf16 bits (RNE) when dtype is bf16."""
+    if dtype == "f64":
+        return np.ascontiguousarray(a64, dtype=np.float64)
+    f = np.ascontiguousarray(a64, dtype=np.float64).astype(np.float32)
+    if dtype == "f32":
+        return f
+    bits = f.view(np.uint32).astype(np.uint64)
+    return ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def make_ln_inputs(p: LNProblem, seed: int = 0) -> dict:
+    """Host arrays (storage dtype) of one LayerNorm backward problem: inp,
+    weight, dout and the initial dinp, dweight, dbias. The row statistics
+    (mean, rstd) are not drawn here: they are what the forward caches, so the
+    caller derives them from ``inp``."""
+    dt, BT, C = p.dtype, p.BT, p.C
+    z = normal((BT, C), "f64", seed, LN_STREAM["inp_z"])
+    shift = normal((BT, 1), "f64", seed, LN_STREAM["inp_shift"], 0.0, 0.5)
+    scale = np.exp(normal((BT, 1), "f64", seed, LN_STREAM["inp_scale"], 0.0, 0.5))
+    out = {"inp": round_to(shift + scale * z, dt)}
+    out["weight"] = normal((C,), dt, seed, LN_STREAM["weight"], 1.0, 0.1)
+    out["dout"] = normal((BT, C), dt, seed, LN_STREAM["dout"], 0.0, p.dout_std)
+    out["dinp"] = normal((BT, C), dt, seed, LN_STREAM["dinp_init"], 0.0, p.init_std)
+    out["dweight"] = normal((C,), dt, seed, LN_STREAM["dweight_init"], 0.0, p.init_std)
+    out["dbias"] = normal((C,), dt, seed, LN_STREAM["dbias_init"], 0.0, p.init_std)
+    return out

@@ -19,14 +19,18 @@ def built():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "mmbwd.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mmbwd_\w+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b((?:mmbwd|lnbwd)_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported_and_bound():
     names = declared_functions()
-    assert "mmbwd_run" in names and len(names) >= 9
+    assert "mmbwd_run" in names and "lnbwd_run" in names and len(names) >= 11
     lib = mm.load()
     for n in names:
         assert hasattr(lib, n), n
@@ -170,3 +174,25 @@ def test_forward_rejects_bad_arguments():
     assert f(C=12) == mm.ERR_ALIGN
     assert f(out=2 * A + 32) == mm.ERR_ALIAS   # out overlaps inp
     assert f(out=4 * A - 16) == mm.ERR_ALIAS   # out overlaps bias
+
+
+def test_layernorm_rejects_bad_arguments():
+    f = lambda **kw: mm.lnbwd_run(**{**dict(dinp=A, dweight=2 * A, dbias=3 * A, dout=4 * A, inp=5 * A,  # noqa: E731
+                                             weight=6 * A, mean=7 * A, rstd=8 * A, B=2, T=8, C=64,
+                                             dtype=mm.BF16, stream=0), **kw})
+    assert f(dtype=2) == mm.ERR_DTYPE
+    assert f(T=-1) == mm.ERR_SHAPE
+    assert f(C=4104) == mm.ERR_SHAPE                  # above LNBWD_MAX_C_BF16
+    assert f(C=2052, dtype=mm.F32) == mm.ERR_SHAPE    # above LNBWD_MAX_C_F32
+    assert f(B=1 << 40, T=1 << 40) == mm.ERR_SHAPE
+    assert f(mean=None) == mm.ERR_NULL
+    assert f(weight=None) == mm.ERR_NULL
+    assert f(dout=None) == mm.ERR_NULL
+    assert f(inp=5 * A + 8) == mm.ERR_ALIGN
+    assert f(rstd=8 * A + 2) == mm.ERR_ALIGN          # statistics need 4-byte alignment
+    assert f(C=60) == mm.ERR_ALIGN                    # 120 bytes per row
+    assert f(dinp=4 * A + 64) == mm.ERR_ALIAS         # dinp inside dout
+    assert f(dbias=2 * A + 16) == mm.ERR_ALIAS        # dbias overlaps dweight
+    assert f(dweight=7 * A) == mm.ERR_ALIAS           # dweight on top of mean
+    assert mm.lnbwd_workspace_bytes(-1, 8, 64, mm.BF16) == 0
+    assert mm.LNBWD_MAX_C == {mm.F32: 2048, mm.BF16: 4096}

@@ -74,3 +74,22 @@ def test_workload_recipes_match_the_configs():
     tiny = synth.WORKLOADS["tiny"].layers[0]
     x = synth.make_inputs(tiny)
     assert x["dinp"].dtype == np.float32 and np.std(x["dinp"]) > 0.005
+
+
+def test_round_to_matches_the_generators_rounding():
+    """synth.round_to (used for the LayerNorm inputs) rounds like the C
+    generator: float64 -> f32 (RNE) -> bf16 (RNE)."""
+    for dt in ("f32", "bf16"):
+        a = synth.normal((4000,), dt, 7, 5, 0.3, 2.0)
+        b = synth.round_to(synth.normal((4000,), "f64", 7, 5, 0.3, 2.0), dt)
+        assert a.dtype == b.dtype and np.array_equal(a, b)
+
+
+def test_layernorm_inputs_are_seeded_and_shaped():
+    p = synth.LN_WORKLOADS["ln_tiny"]
+    a, b = synth.make_ln_inputs(p), synth.make_ln_inputs(p)
+    for k in a:
+        assert np.array_equal(a[k], b[k])
+    assert a["inp"].shape == (p.BT, p.C) and a["weight"].shape == (p.C,)
+    rows = a["inp"].astype(np.float64)
+    assert np.std(rows.mean(axis=1)) > 0.2 and np.std(np.log(rows.std(axis=1))) > 0.2
