@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-other", action="store_true", help="skip the other configurations")
+    ap.add_argument("--case", default=None,
+                    help="time only this one configuration of the other-configs list (for example "
+                         "ln_xl or attn_proj) with --steps batches, print its line and exit")
     return ap.parse_args(argv)
 
 
@@ -442,6 +445,8 @@ def run_gpu(args):
 
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32")
+FORWARD_CONFIGS = (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
+                   ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32"))
 
 
 L2_BYTES = 129 * 1024 * 1024
@@ -474,7 +479,7 @@ def input_sets(nbytes_one, cap=8):
     return max(1, min(cap, -(-2 * L2_BYTES // max(nbytes_one, 1))))
 
 
-def measure_other_configs(torch, mm, dev, stream):
+def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
     """The remaining configurations of the workload set and the forward of the
     GPT-2 layers: back-to-back calls on device-resident inputs rotated over
     enough copies to exceed the L2 (see `input_sets`), timed with CUDA events,
@@ -500,6 +505,8 @@ def measure_other_configs(torch, mm, dev, stream):
             out[name]["plan"] = plan
 
     for name in OTHER_CONFIGS:
+        if only is not None and name not in only:
+            continue
         layer = synth.WORKLOADS[name].layers[0]
         x = synth.make_inputs(layer, seed=0)
         set_bytes = sum(v.nbytes for v in x.values())
@@ -519,15 +526,16 @@ def measure_other_configs(torch, mm, dev, stream):
 
         calls = [make_call(t) for t in sets]
         per_batch = max(len(calls), 20 if layer.flops() < 5e11 else 8)
-        sec = time_back_to_back(torch, stream, calls, per_batch)
+        sec = time_back_to_back(torch, stream, calls, per_batch, batches)
         info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
         finish(name, layer, layer.flops(), sec, n_sets, set_bytes,
                {k: info[k] for k in ("path", "grid", "items", "splits", "launches")})
         del sets, calls
         torch.cuda.empty_cache()
     # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
-    for name, lname in (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
-                        ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32")):
+    for name, lname in FORWARD_CONFIGS:
+        if only is not None and name not in only:
+            continue
         wl, _, i = lname.partition(":")
         layer = synth.WORKLOADS[wl].layers[int(i or 0)]
         x = synth.make_inputs(layer, seed=0)
@@ -552,7 +560,7 @@ def measure_other_configs(torch, mm, dev, stream):
         calls = [make_fcall(t) for t in sets]
         flops = 2 * layer.BT * layer.C * layer.OC + (layer.BT * layer.OC if layer.bias else 0)
         per_batch = max(len(calls), 20 if flops < 2.5e11 else 8)
-        sec = time_back_to_back(torch, stream, calls, per_batch)
+        sec = time_back_to_back(torch, stream, calls, per_batch, batches)
         finish(name, layer, flops, sec, n_sets, set_bytes)
         del sets, calls
         torch.cuda.empty_cache()
@@ -560,6 +568,8 @@ def measure_other_configs(torch, mm, dev, stream):
     # algorithmic bytes against the measured copy bandwidth
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     for name in LN_CONFIGS:
+        if only is not None and name not in only:
+            continue
         p = synth.LN_WORKLOADS[name]
         x = synth.make_ln_inputs(p, seed=0)
         # row statistics as the forward caches them (fp32), computed on the host
@@ -585,7 +595,7 @@ def measure_other_configs(torch, mm, dev, stream):
             return lcall
 
         calls = [make_lcall(t) for t in sets]
-        sec = time_back_to_back(torch, stream, calls, max(len(calls), 40))
+        sec = time_back_to_back(torch, stream, calls, max(len(calls), 40), batches)
         gbs = p.bytes() / sec / 1e9
         out[name] = {"B": p.B, "T": p.T, "C": p.C, "dtype": p.dtype, "us": round(sec * 1e6, 2),
                      "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
@@ -643,12 +653,33 @@ def run_e2e(torch, mm, wl, host, dev, stream, steps, barrier):
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": max_s / steps * 1e3}
 
 
+def run_case(args):
+    """One configuration of the other-configs list on its own (used to profile
+    a single kernel): its usual timing with `--steps` batches, one JSON line."""
+    import torch
+
+    import linear_layer_gemms_gb300 as mm
+
+    names = set(OTHER_CONFIGS) | set(LN_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
+    if args.case not in names:
+        raise SystemExit(f"unknown case {args.case}; one of {sorted(names)}")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    mm.load()
+    stream = torch.cuda.Stream(device=dev)
+    out = measure_other_configs(torch, mm, dev, stream, only={args.case}, batches=max(1, args.steps))
+    print(json.dumps({"case": args.case, **out[args.case]}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     return run_gpu(args)
 
 

@@ -78,6 +78,8 @@ extern "C" {
  * Ownership and synchronisation as for mmbwd_run: the caller owns every buffer;
  * the call returns after enqueueing; the library's workspace is per device and
  * shared with mmbwd_run, so calls on one device must be ordered (one stream).
+ * Every wait inside the kernels is bounded; one that gives up is reported as
+ * MMBWD_ERR_DEVICE_TIMEOUT by mmbwd_device_status().
  */
 int lnbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
               const float* mean, const float* rstd, int64_t B, int64_t T, int64_t C, int dtype,

@@ -336,8 +336,14 @@ int mmbwd_release(void) {
 
 int mmbwd_device_status(int reset, int* info) {
     if (cudaDeviceSynchronize() != cudaSuccess) return MMBWD_ERR_CUDA;
-    int code = MMBWD_OK;
+    int code = MMBWD_OK, ln_code = MMBWD_OK, ln_info[3] = {0, 0, 0};
     if (tc_read_status(&code, info, reset != 0) != cudaSuccess) return MMBWD_ERR_CUDA;
+    if (ln_read_status(&ln_code, ln_info, reset != 0) != cudaSuccess) return MMBWD_ERR_CUDA;
+    if (code == MMBWD_OK && ln_code != MMBWD_OK) {
+        code = ln_code;
+        if (info)
+            for (int i = 0; i < 3; ++i) info[i] = ln_info[i];
+    }
     return code;
 }
 

@@ -159,11 +159,12 @@ EncodeTiledFn get_encode_tiled();
 // ---------------------------------------------------------------- LayerNorm backward
 
 struct LnPlan {
-    int vpl = 0;             // 16-byte vectors per lane (row width covered: 32 * vpl vectors)
-    int warps = 0;           // warps per block, one row at a time each
-    int grid = 0;            // blocks, each a contiguous range of rows
+    int vpl = 0;             // 16-byte column vectors per thread and row
+    int team_warps = 0;      // warps that share one row
+    int warps = 0;           // warps per block
+    int grid = 0;            // blocks (one per SM), each a contiguous range of rows
     int64_t rows_per_block = 0;
-    size_t smem = 0;         // weight (fp32) + per-warp dweight / dbias sums
+    size_t smem = 0;         // weight (fp32) + row-sum exchange + the teams' sums
     size_t ws_bytes = 0;     // per-block partial sums, fp32 [grid][2][C]
 };
 
@@ -172,5 +173,6 @@ cudaError_t ln_make_plan(int64_t BT, int C, int dtype, int num_sms, LnPlan* plan
 cudaError_t ln_launch(const LnPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, const float* mean, const float* rstd, int64_t BT,
                       int C, int dtype, void* ws, cudaStream_t stream);
+cudaError_t ln_read_status(int* code, int* info3, bool reset);
 
 }  // namespace mmbwd
