@@ -164,7 +164,8 @@ struct LnPlan {
     int warps = 0;           // warps per block
     int grid = 0;            // blocks (one per SM), each a contiguous range of rows
     int64_t rows_per_block = 0;
-    size_t smem = 0;         // weight (fp32) + row-sum exchange + the teams' sums
+    size_t off_ring = 0;     // start of the teams' row buffers in shared memory
+    size_t smem = 0;         // weight (fp32) + row-sum exchange + barriers + row buffers
     size_t ws_bytes = 0;     // per-block partial sums, fp32 [grid][2][C]
 };
 

@@ -48,18 +48,53 @@ constexpr int LN_WARPS = 16;
 constexpr int LN_THREADS = LN_WARPS * 32;
 constexpr int LN_MAX_VPT = 2;  // 16-byte vectors per thread and row
 constexpr int LN_PARAM_WARPS = 32;
+constexpr int LN_STAGES = 4;  // row buffers per team (three rows in flight)
+constexpr unsigned long long LN_TIMEOUT_NS = 2000000000ull;
+
+enum LnSite { LN_SITE_FULL = 2, LN_SITE_TEARDOWN = 4 };
 
 __device__ __forceinline__ void ln_grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void ln_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-// 16-byte asynchronous copy global -> shared (L2 only), and its group waits
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`
+// (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ void ln_record_failure(int site, int64_t row) {
+    if (atomicCAS(&g_ln_status[0], 0u, static_cast<unsigned>(-MMBWD_ERR_DEVICE_TIMEOUT)) == 0u) {
+        g_ln_status[1] = blockIdx.x;
+        g_ln_status[2] = static_cast<unsigned>(site);
+        g_ln_status[3] = static_cast<unsigned>(row);
+        __threadfence();
+    }
+}
+
+// Bounded wait on an mbarrier phase (2 s by the global timer); false on
+// timeout (recorded, abort raised) or, unless `ignore_abort`, once the block
+// has aborted.
+__device__ bool ln_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort, int site, int64_t row,
+                        bool ignore_abort = false) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (!ignore_abort && *abort) return false;
+            if (ptx::globaltimer() - t0 > LN_TIMEOUT_NS) {
+                *abort = 1u;
+                ln_record_failure(site, row);
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void team_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -119,6 +154,7 @@ struct LnParams {
     int C;
     int nvec;        // C / N
     int team_warps;  // P
+    uint32_t off_ring;  // bytes from the start of shared memory to the row buffers
 };
 
 template <typename T, int VPT, int P>
@@ -132,11 +168,18 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
     const int team = warp / P, pw = warp % P;
     const int tt = pw * 32 + lane;  // thread index in the team
     float* w_s = ln_smem;                                    // weight as fp32, C
-    float* red = ln_smem + C;                                // [teams][2][P][4] row sums
+    float* red = ln_smem + C;                                // [teams][2][P][2] row sums
+    uint64_t* bars = reinterpret_cast<uint64_t*>(red + teams * 2 * P * 2);  // [teams][LN_STAGES]
+    volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(bars + teams * LN_STAGES);
     // [teams][2C] team sums at the end; during the row loop the same region
-    // (sized for both) holds each team's two-stage row buffer
-    float* tsum = red + static_cast<size_t>(teams) * 2 * P * 4;
+    // (sized for both, 128-byte aligned) holds each team's ring of row buffers
+    float* tsum = reinterpret_cast<float*>(ln_smem + p.off_ring / 4);
 
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < teams * LN_STAGES; ++b) ptx::mbar_init(ptx::smem_u32(bars + b), 1);
+        *abort = 0u;
+        ptx::fence_mbar_init();
+    }
     ln_grid_wait();  // global memory only from here on
     for (int i = threadIdx.x; i < C; i += blockDim.x) w_s[i] = E::load1(p.weight, i);
     __syncthreads();
@@ -158,157 +201,113 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
 
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_block;
     const int64_t r1 = r0 + p.rows_per_block < p.BT ? r0 + p.rows_per_block : p.BT;
-    // Two-stage buffer of this team: [stage][row][dout | inp | dinp][C] in the
-    // storage type. A thread copies its own vectors with cp.async and reads
-    // back only those bytes, so its own wait_group is the only wait needed.
+    // This team's ring of LN_STAGES row buffers ([dout | inp | dinp] of one
+    // row each, storage type) and its "full" barriers. One thread of the team
+    // issues the bulk copies of the team's rows in order; the team consumes
+    // them in order, so each barrier is waited on phase by phase.
     const uint32_t row_bytes = static_cast<uint32_t>(C) * sizeof(T);
-    const uint32_t stage_bytes = 6 * row_bytes;
-    const uint32_t team_buf = ptx::smem_u32(tsum) + static_cast<uint32_t>(team) * 2 * stage_bytes;
-    auto issue = [&](int64_t k, int stage) {  // copies of rows k and k + teams (those < r1)
-        const uint32_t sb = team_buf + static_cast<uint32_t>(stage) * stage_bytes;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int64_t r = k + q * teams;
-            if (r < r1) {
-#pragma unroll
-                for (int t3 = 0; t3 < 3; ++t3) {
-                    const void* src = t3 == 0 ? p.dout : (t3 == 1 ? p.inp : static_cast<const void*>(p.dinp));
-                    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(src) + r * C);
-                    const uint32_t dst = sb + static_cast<uint32_t>(q * 3 + t3) * row_bytes;
-#pragma unroll
-                    for (int j = 0; j < VPT; ++j) {
-                        const int v = tt + 32 * P * j;
-                        if (v < p.nvec) cp_async16(dst + 16u * v, row + v);
-                    }
-                }
-            }
-        }
-        cp_async_commit();
+    const uint32_t stage_bytes = 3 * row_bytes;
+    const uint32_t team_buf = ptx::smem_u32(tsum) + static_cast<uint32_t>(team) * LN_STAGES * stage_bytes;
+    const uint32_t full0 = ptx::smem_u32(bars) + static_cast<uint32_t>(team) * LN_STAGES * 8u;
+    const bool issuer = pw == 0 && lane == 0;
+    const int64_t first = r0 + team;  // the team's rows: first + j * teams
+    const int nj = first < r1 ? static_cast<int>((r1 - first + teams - 1) / teams) : 0;
+    auto issue = [&](int j) {
+        const int64_t off = (first + static_cast<int64_t>(j) * teams) * C;
+        const uint32_t st = static_cast<uint32_t>(j % LN_STAGES);
+        const uint32_t bar = full0 + 8u * st, dst = team_buf + st * stage_bytes;
+        // the team's earlier reads of this buffer come before the copies' writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        ptx::mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(dst, static_cast<const T*>(p.dout) + off, row_bytes, bar);
+        bulk_load(dst + row_bytes, static_cast<const T*>(p.inp) + off, row_bytes, bar);
+        bulk_load(dst + 2 * row_bytes, static_cast<const T*>(p.dinp) + off, row_bytes, bar);
     };
+    if (issuer)
+        for (int j = 0; j < LN_STAGES - 1 && j < nj; ++j) issue(j);
 
-    // row statistics travel one iteration ahead in registers
-    float st[4] = {0.f, 0.f, 0.f, 0.f};  // mean, rstd of rows k and k + teams
-    auto stats = [&](int64_t k, float (&o)[4]) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int64_t r = k + q * teams < r1 ? k + q * teams : k;
-            o[2 * q] = __ldg(p.mean + r);
-            o[2 * q + 1] = __ldg(p.rstd + r);
-        }
-    };
-    int par = 0, stage = 0;
-    if (r0 + team < r1) {
-        issue(r0 + team, 0);
-        stats(r0 + team, st);
-    }
-    for (int64_t k = r0 + team; k < r1; k += 2 * teams, par ^= 1, stage ^= 1) {
-        const int64_t rows[2] = {k, k + teams};
-        const bool two = rows[1] < r1;
-        // the next iteration's rows are in flight while this one is computed
-        float st_next[4] = {0.f, 0.f, 0.f, 0.f};
-        if (k + 2 * teams < r1) {
-            issue(k + 2 * teams, stage ^ 1);
-            stats(k + 2 * teams, st_next);
-        } else {
-            cp_async_commit();  // an empty group keeps the count of groups in step
-        }
-        cp_async_wait_one();    // this iteration's group has landed (for this thread)
-        const uint32_t sb = team_buf + static_cast<uint32_t>(stage) * stage_bytes;
-        uint4 vd[2][VPT], vx[2][VPT], vo[2][VPT];
-        float m[2], sd[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            m[q] = st[2 * q];
-            sd[q] = st[2 * q + 1];
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tt + 32 * P * j;
-                if (v < p.nvec && (q == 0 || two)) {
-                    vd[q][j] = ptx::lds128(sb + static_cast<uint32_t>(q * 3 + 0) * row_bytes + 16u * v);
-                    vx[q][j] = ptx::lds128(sb + static_cast<uint32_t>(q * 3 + 1) * row_bytes + 16u * v);
-                    vo[q][j] = ptx::lds128(sb + static_cast<uint32_t>(q * 3 + 2) * row_bytes + 16u * v);
-                }
-            }
-        }
+    int par = 0;
+    for (int j = 0; j < nj; ++j, par ^= 1) {
+        const int64_t r = first + static_cast<int64_t>(j) * teams;
+        const float m = __ldg(p.mean + r), sd = __ldg(p.rstd + r);
+        // A wait that gives up is recorded (device status) and the row is
+        // processed anyway, so that every warp still reaches every barrier.
+        ln_wait(full0 + 8u * (j % LN_STAGES), static_cast<uint32_t>((j / LN_STAGES) & 1), abort, LN_SITE_FULL, r);
+        const uint32_t sb = team_buf + static_cast<uint32_t>(j % LN_STAGES) * stage_bytes;
 
-        // first pass: the two row sums of each row
-        float su[4] = {0.f, 0.f, 0.f, 0.f};  // sa0, sc0, sa1, sc1
+        // first pass: the two row sums
+        float sa = 0.f, sc = 0.f;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (q == 1 && !two) break;
+        for (int jj = 0; jj < VPT; ++jj) {
+            const int v = tt + 32 * P * jj;
+            if (v < p.nvec) {
+                float d[N], x[N], w[N];
+                E::unpack(ptx::lds128(sb + 16u * v), d);
+                E::unpack(ptx::lds128(sb + row_bytes + 16u * v), x);
+                weights(v, w);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tt + 32 * P * j;
-                if (v < p.nvec) {
-                    float d[N], x[N], w[N];
-                    E::unpack(vd[q][j], d);
-                    E::unpack(vx[q][j], x);
-                    weights(v, w);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) {
-                        const float g = w[e] * d[e];
-                        su[2 * q] += g;
-                        su[2 * q + 1] += g * ((x[e] - m[q]) * sd[q]);
-                    }
+                for (int e = 0; e < N; ++e) {
+                    const float g = w[e] * d[e];
+                    sa += g;
+                    sc += g * ((x[e] - m) * sd);
                 }
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) su[u] += __shfl_xor_sync(0xffffffffu, su[u], off);
+        for (int off = 16; off > 0; off >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, off);
+            sc += __shfl_xor_sync(0xffffffffu, sc, off);
+        }
         if (P > 1) {
-            // across the team's warps, in warp order (buffer `par`: the previous
-            // use of this buffer was read before every warp reached the last
-            // barrier of the team)
-            float* rb = red + (static_cast<size_t>(team) * 2 + par) * P * 4;
-            if (lane == 0)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) rb[pw * 4 + u] = su[u];
+            // across the team's warps, in warp order (buffer `par`: its previous
+            // use was read before every warp reached the team's last barrier)
+            float* rb = red + (static_cast<size_t>(team) * 2 + par) * P * 2;
+            if (lane == 0) rb[pw * 2] = sa, rb[pw * 2 + 1] = sc;
             team_sync(1 + team, 32 * P);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float t = rb[u];
-                for (int w = 1; w < P; ++w) t += rb[w * 4 + u];
-                su[u] = t;
-            }
+            sa = rb[0];
+            sc = rb[1];
+            for (int w = 1; w < P; ++w) sa += rb[2 * w], sc += rb[2 * w + 1];
+        } else {
+            __syncwarp();
         }
+        // Every warp of the team is past its second pass of row j - 1 (it came
+        // before the barrier above): that row's buffer takes row j + LN_STAGES - 1.
+        if (issuer && j + LN_STAGES - 1 < nj) issue(j + LN_STAGES - 1);
 
-        // second pass: dinp, and this thread's parameter sums (row k, then k + teams)
+        // second pass: dinp, and this thread's parameter sums
+        const float a = sa / static_cast<float>(C), c = sc / static_cast<float>(C);
+        const float sda = sd * a, sdc = sd * c;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.dinp) + r * C);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (q == 1 && !two) break;
-            const float a = su[2 * q] / static_cast<float>(C), c = su[2 * q + 1] / static_cast<float>(C);
-            const float sda = sd[q] * a, sdc = sd[q] * c;
-            uint4* orow = reinterpret_cast<uint4*>(static_cast<T*>(p.dinp) + rows[q] * C);
+        for (int jj = 0; jj < VPT; ++jj) {
+            const int v = tt + 32 * P * jj;
+            if (v < p.nvec) {
+                float d[N], x[N], o[N], w[N];
+                E::unpack(ptx::lds128(sb + 16u * v), d);
+                E::unpack(ptx::lds128(sb + row_bytes + 16u * v), x);
+                E::unpack(ptx::lds128(sb + 2 * row_bytes + 16u * v), o);
+                weights(v, w);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = tt + 32 * P * j;
-                if (v < p.nvec) {
-                    float d[N], x[N], o[N], w[N];
-                    E::unpack(vd[q][j], d);
-                    E::unpack(vx[q][j], x);
-                    E::unpack(vo[q][j], o);
-                    weights(v, w);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) {
-                        const float nrm = (x[e] - m[q]) * sd[q];
-                        // rstd * (g - a - n c), as sd*g - sd*a - (sd*c)*n
-                        o[e] += fmaf(sd[q], w[e] * d[e], -fmaf(sdc, nrm, sda));
-                        acc_w[j][e] = fmaf(nrm, d[e], acc_w[j][e]);
-                        acc_b[j][e] += d[e];
-                    }
-                    __stcg(orow + v, E::pack(o));
+                for (int e = 0; e < N; ++e) {
+                    const float nrm = (x[e] - m) * sd;
+                    // rstd * (g - a - n c), as sd*g - sd*a - (sd*c)*n
+                    o[e] += fmaf(sd, w[e] * d[e], -fmaf(sdc, nrm, sda));
+                    acc_w[jj][e] = fmaf(nrm, d[e], acc_w[jj][e]);
+                    acc_b[jj][e] += d[e];
                 }
+                __stcg(orow + v, E::pack(o));
             }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) st[u] = st_next[u];
     }
+    // copies in flight land before the buffers are reused (normally all have
+    // been waited for already)
+    if (issuer)
+        for (int j = nj - LN_STAGES > 0 ? nj - LN_STAGES : 0; j < nj; ++j)
+            ln_wait(full0 + 8u * (j % LN_STAGES), static_cast<uint32_t>((j / LN_STAGES) & 1), abort,
+                    LN_SITE_TEARDOWN, first + static_cast<int64_t>(j) * teams, true);
 
     // the teams' sums, added in team order (the row buffers are free once
     // every team has finished)
-    cp_async_wait_all();
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
@@ -416,9 +415,12 @@ cudaError_t ln_make_plan(int64_t BT, int C, int dtype, int num_sms, LnPlan* plan
     plan->team_warps = P;
     plan->warps = LN_WARPS;
     const size_t es = dtype == MMBWD_F32 ? 4 : 2;
-    const size_t rows_buf = static_cast<size_t>(teams) * 2 * 6 * C * es;  // two stages of two rows
-    plan->smem = 4 * (static_cast<size_t>(C) + static_cast<size_t>(teams) * 2 * P * 4) +
-                 std::max(rows_buf, static_cast<size_t>(teams) * 2 * C * 4);
+    const size_t rows_buf = static_cast<size_t>(teams) * LN_STAGES * 3 * C * es;  // each team's ring
+    const size_t head = 4 * (static_cast<size_t>(C) + static_cast<size_t>(teams) * 2 * P * 2) +
+                        8 * static_cast<size_t>(teams) * LN_STAGES + 8;  // weight, row sums, barriers, flag
+    plan->off_ring = (head + 127) / 128 * 128;
+    plan->smem = plan->off_ring + std::max(rows_buf, static_cast<size_t>(teams) * 2 * C * 4);
+    if (plan->smem > 227 * 1024) return cudaErrorInvalidValue;
     const void* k = dtype == MMBWD_F32 ? rows_kernel_for<float>(vpt, P) : rows_kernel_for<__nv_bfloat16>(vpt, P);
     cudaError_t e =
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan->smem));
@@ -449,6 +451,7 @@ cudaError_t ln_launch(const LnPlan& plan, void* dinp, void* dweight, void* dbias
     p.C = C;
     p.nvec = C / ln_vec_elems(dtype);
     p.team_warps = plan.team_warps;
+    p.off_ring = static_cast<uint32_t>(plan.off_ring);
     const void* k = dtype == MMBWD_F32 ? rows_kernel_for<float>(plan.vpl, plan.team_warps)
                                        : rows_kernel_for<__nv_bfloat16>(plan.vpl, plan.team_warps);
     void* args[] = {&p};
