@@ -8,20 +8,22 @@
 //
 // Rows kernel (one block of 16 warps per SM, a contiguous range of rows per
 // block). Warps form teams of P warps (P a compile-time parameter); a team
-// takes two rows at a time (rows k and k + teams, then k + 2 teams ...). A
-// thread owns the 16-byte column vectors t, t + 32P (at most two) of every
-// row of its team. It copies its share of dout, inp and the old dinp of the
-// next two rows into its team's two-stage shared-memory buffer with cp.async
-// while it computes the current two, and reads back only the bytes it copied
-// itself, so its own cp.async.wait_group is the only wait the data needs. Its
-// share of dweight and dbias stays in registers for the block's whole range
-// of rows. The two row sums are reduced in the warp with an xor butterfly
-// (the same bits in every lane) and across the team's warps through shared
-// memory in warp order behind a named barrier of the team. At the end the
-// teams' sums are added in team order and the block writes one fp32 partial
-// row pair to the workspace. There is no spin wait anywhere: the only waits
-// are cp.async group waits and hardware barriers that every warp of the
-// block or team reaches.
+// takes rows k, k + teams, k + 2 teams, ... One thread of the team streams its
+// rows (dout, inp and the old dinp of one row per buffer) into the team's
+// ring of four shared-memory buffers with 1-D TMA bulk copies completing on
+// the buffer's mbarrier, three rows ahead of the row being computed; the team
+// consumes its ring in order, so each barrier is waited on phase by phase.
+// A thread owns the 16-byte column vectors t, t + 32P (at most two) of every
+// row of its team; its share of dweight and dbias stays in registers for the
+// block's whole range of rows. The two row sums are reduced in the warp with
+// an xor butterfly (the same bits in every lane) and across the team's warps
+// through shared memory in warp order behind a named barrier of the team;
+// that barrier also tells the issuing thread that the team is done with the
+// buffer it refills next (with an async-proxy fence before the copies).
+// Every mbarrier wait is bounded (2 s): one that gives up records the failure
+// in the device status word and the row is processed anyway, so that every
+// warp still reaches every barrier. At the end the teams' sums are added in
+// team order and the block writes one fp32 partial row pair to the workspace.
 //
 // Params kernel: for each group of 32 columns, 32 warps each sum a fixed
 // contiguous range of the block partials in block order, then one warp adds
@@ -38,8 +40,8 @@
 
 namespace mmbwd {
 
-// Status word of the LayerNorm kernels (they have no bounded waits that could
-// give up; kept so that the device status covers every kernel of the library).
+// Status word of the LayerNorm kernels: [0] error code (positive), [1] block,
+// [2] wait site, [3] row.
 __device__ unsigned int g_ln_status[4];
 
 namespace {
