@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmmbwd.so")
-SOURCES = ["api.cu", "tc_gemm.cu", "simt_f32.cu", "layernorm_bwd.cu"]
+SOURCES = ["api.cu", "tc_gemm.cu", "simt_f32.cu", "layernorm_bwd.cu", "split_tf32.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

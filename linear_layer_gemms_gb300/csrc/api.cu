@@ -8,10 +8,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace mmbwd {
@@ -156,6 +158,18 @@ int device_state(DeviceState** out, int* dev_out) {
 }
 
 // Grow the device's workspace to `need` bytes (its contents need no initial value).
+// fp32 path: three tf32 products on the tensor cores for problems large enough
+// to fill the GPU (and shapes it supports), fp32 FMAs otherwise. MMBWD_F32_PATH
+// = "ffma" or "x3" forces one (the latter where the shape allows it).
+bool use_x3(int64_t BT, int64_t C, int64_t OC) {
+    if (!x3_shape_ok(BT, C, OC)) return false;
+    if (const char* f = std::getenv("MMBWD_F32_PATH")) {
+        if (std::strcmp(f, "ffma") == 0) return false;
+        if (std::strcmp(f, "x3") == 0) return true;
+    }
+    return BT >= 256 && C >= 256 && OC >= 256 && static_cast<double>(BT) * C * OC >= 6.7e7;
+}
+
 int ensure_workspace(DeviceState& d, size_t need, cudaStream_t stream) {
     if (need <= d.ws_bytes) return MMBWD_OK;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -215,7 +229,8 @@ const char* mmbwd_strerror(int code) {
 size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype) {
     Shape s;
     if (check_shape(B, T, C, OC, dtype, &s) != MMBWD_OK) return 0;
-    if (dtype != MMBWD_BF16 || s.BT == 0 || C == 0 || OC == 0) return 0;
+    if (s.BT == 0 || C == 0 || OC == 0) return 0;
+    if (dtype == MMBWD_F32) return use_x3(s.BT, C, OC) ? x3_workspace_bytes(s.BT, C, OC, true) : 0;
     int sms = 0, quads = 0;
     {
         std::lock_guard<std::mutex> g(g_mutex);
@@ -247,6 +262,11 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
         const int vals[15] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
                               pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.table,
                               TC_PAIR_BM * pl.ppc, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), pl.ppc};
+        for (int i = 0; i < 15; ++i) v[i] = vals[i];
+    } else if (use_x3(s.BT, C, OC)) {
+        const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
+        const int vals[15] = {2, std::max(p1.grid, p2.grid), p1.n_items + p2.n_items, 1, 0, p1.n_items, p2.n_items,
+                              0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES / 2, 6, 1};
         for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
@@ -307,9 +327,17 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
     }
 
     if (dtype == MMBWD_F32) {
-        e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
-                        static_cast<const float*>(dout), static_cast<const float*>(inp),
-                        static_cast<const float*>(weight), s.BT, C, OC, stream);
+        if (use_x3(s.BT, C, OC)) {
+            rc = ensure_workspace(*d, x3_workspace_bytes(s.BT, C, OC, dbias != nullptr), stream);
+            if (rc != MMBWD_OK) return rc;
+            e = x3_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                          static_cast<const float*>(dout), static_cast<const float*>(inp),
+                          static_cast<const float*>(weight), s.BT, C, OC, d->ws, d->num_sms, stream);
+        } else {
+            e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                            static_cast<const float*>(dout), static_cast<const float*>(inp),
+                            static_cast<const float*>(weight), s.BT, C, OC, stream);
+        }
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
 

@@ -107,6 +107,13 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quad
 // dinp-type items, K = C, N = OC.
 TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
 
+// One fp32 product D (M x N, row-major, leading dimension N) += A (M x K) .
+// B (N x K)^T from tf32 halves (hi: the tf32 value, lo: the exact remainder),
+// both K-major with leading dimensions lda, ldb (elements, multiples of 4).
+TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms);
+cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
+                         const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream);
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight,
                               const void* bias, int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
 
@@ -155,6 +162,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
+
+// ---------------------------------------------------------------- fp32 on the tensor cores (3xTF32)
+
+int64_t x3_ld(int64_t n);
+bool x3_shape_ok(int64_t BT, int64_t C, int64_t OC);
+size_t x3_workspace_bytes(int64_t BT, int64_t C, int64_t OC, bool bias);
+cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
+                      const float* weight, int64_t BT, int64_t C, int64_t OC, void* ws, int num_sms,
+                      cudaStream_t stream);
 
 // ---------------------------------------------------------------- LayerNorm backward
 

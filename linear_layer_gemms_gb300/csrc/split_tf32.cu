@@ -1,0 +1,166 @@
+// fp32 operands of the linear-layer backward split into tf32 halves, laid out
+// K-major for the three-product tensor-core path (MODE 2 of tc_mmbwd_kernel).
+//
+// The fp32 path needs fp32-accurate products (llm.c dev/cuda/matmul_backward.cu
+// turns TF32 off in its main for exactly that reason). A value x is split into
+//   hi = x with its 13 low mantissa bits cleared   (a tf32 value, exactly)
+//   lo = x - hi                                     (exact in fp32, |lo| < 2^-10 |x|)
+// and x*y is formed as hi_x*hi_y + hi_x*lo_y + lo_x*hi_y: the dropped lo_x*lo_y
+// and the tf32 reading of lo leave a relative error near 2^-20 per product,
+// below fp32 accumulation error over the long reductions.
+//
+// Layouts (every product becomes D += A . B^T with both operands K-major):
+//   dinp    (BT x C) += dout (BT x OC) . (weight^T) (C x OC)^T   A = dout,    B = weight^T
+//   dweight (OC x C) += (dout^T) (OC x BT) . (inp^T) (C x BT)^T  A = dout^T,  B = inp^T
+// so dout is split in place and transposed, weight and inp transposed. The
+// transposing pass over dout also sums each 32-row tile of every column, and
+// a second small kernel adds those tile sums in tile order: dbias.
+#include "../../include/mmbwd.h"
+#include "internal.h"
+
+namespace mmbwd {
+namespace {
+
+constexpr int TILE = 32;
+
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
+// src (R x Cc, row-major) in 32 x 32 tiles, 256 threads (32 x 8):
+//   COPY:   hi / lo with the layout of src
+//   TRANS:  thi / tlo = the transpose (Cc x R), row pitch ldT
+//   COLSUM: part[tile row][c] = sum of the tile's rows of column c, in row order
+template <bool COPY, bool TRANS, bool COLSUM>
+__global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ src, int64_t R, int64_t Cc,
+                                                    float* __restrict__ hi, float* __restrict__ lo,
+                                                    float* __restrict__ thi, float* __restrict__ tlo, int64_t ldT,
+                                                    float* __restrict__ part) {
+    __shared__ float t[TILE][TILE + 1];
+    const int tx = static_cast<int>(threadIdx.x & 31), ty = static_cast<int>(threadIdx.x >> 5);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * TILE, c0 = static_cast<int64_t>(blockIdx.x) * TILE;
+#pragma unroll
+    for (int i = 0; i < TILE / 8; ++i) {
+        const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
+        float x = 0.f;
+        if (r < R && c < Cc) {
+            x = __ldcs(src + r * Cc + c);
+            if (COPY) {
+                float h, l;
+                split_tf32(x, h, l);
+                hi[r * Cc + c] = h;
+                lo[r * Cc + c] = l;
+            }
+        }
+        t[ty + 8 * i][tx] = x;
+    }
+    if (!TRANS && !COLSUM) return;
+    __syncthreads();
+    if (TRANS) {
+#pragma unroll
+        for (int i = 0; i < TILE / 8; ++i) {
+            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;  // row c, column r of the transpose
+            if (c < Cc && r < R) {
+                float h, l;
+                split_tf32(t[tx][ty + 8 * i], h, l);
+                thi[c * ldT + r] = h;
+                tlo[c * ldT + r] = l;
+            }
+        }
+    }
+    if (COLSUM && ty == 0 && c0 + tx < Cc) {
+        float s = 0.f;
+        for (int i = 0; i < TILE; ++i) s += t[i][tx];  // rows past R hold 0
+        part[static_cast<int64_t>(blockIdx.y) * Cc + c0 + tx] = s;
+    }
+}
+
+// dbias[c] = sum over tile rows of part[.][c], in tile order (overwrite).
+__global__ void __launch_bounds__(256) tile_sum_kernel(float* __restrict__ dbias, const float* __restrict__ part,
+                                                       int64_t tiles, int64_t Cc) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= Cc) return;
+    float s = 0.f;
+    for (int64_t k = 0; k < tiles; ++k) s += part[k * Cc + c];
+    dbias[c] = s;
+}
+
+template <bool COPY, bool TRANS, bool COLSUM>
+cudaError_t launch_split(const float* src, int64_t R, int64_t Cc, float* hi, float* lo, float* thi, float* tlo,
+                         int64_t ldT, float* part, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((Cc + TILE - 1) / TILE), static_cast<unsigned>((R + TILE - 1) / TILE));
+    split_kernel<COPY, TRANS, COLSUM><<<grid, 256, 0, stream>>>(src, R, Cc, hi, lo, thi, tlo, ldT, part);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t x3_ld(int64_t n) { return (n + 3) / 4 * 4; }
+
+size_t x3_workspace_bytes(int64_t BT, int64_t C, int64_t OC, bool bias) {
+    auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t f = 4;
+    const size_t ldbt = static_cast<size_t>(x3_ld(BT));
+    size_t n = 0;
+    n += 2 * a(static_cast<size_t>(BT) * OC * f);  // dout hi, lo
+    n += 2 * a(static_cast<size_t>(OC) * ldbt * f);  // dout^T hi, lo
+    n += 2 * a(static_cast<size_t>(C) * OC * f);     // weight^T hi, lo
+    n += 2 * a(static_cast<size_t>(C) * ldbt * f);   // inp^T hi, lo
+    if (bias) n += a(static_cast<size_t>((BT + TILE - 1) / TILE) * OC * f);
+    return n;
+}
+
+bool x3_shape_ok(int64_t BT, int64_t C, int64_t OC) {
+    // K-major rows of 16-byte multiples, 8-column epilogue groups, tile grids
+    // within the launch limits
+    return BT > 0 && C > 0 && OC > 0 && C % 8 == 0 && OC % 4 == 0 && (BT + TILE - 1) / TILE <= 65535 &&
+           (OC + TILE - 1) / TILE <= 65535;
+}
+
+cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
+                      const float* weight, int64_t BT, int64_t C, int64_t OC, void* ws, int num_sms,
+                      cudaStream_t stream) {
+    auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const int64_t ldbt = x3_ld(BT);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    auto take = [&](size_t bytes) {
+        float* p = reinterpret_cast<float*>(w);
+        w += a(bytes);
+        return p;
+    };
+    float* dout_hi = take(static_cast<size_t>(BT) * OC * 4);
+    float* dout_lo = take(static_cast<size_t>(BT) * OC * 4);
+    float* doutT_hi = take(static_cast<size_t>(OC) * ldbt * 4);
+    float* doutT_lo = take(static_cast<size_t>(OC) * ldbt * 4);
+    float* wT_hi = take(static_cast<size_t>(C) * OC * 4);
+    float* wT_lo = take(static_cast<size_t>(C) * OC * 4);
+    float* inpT_hi = take(static_cast<size_t>(C) * ldbt * 4);
+    float* inpT_lo = take(static_cast<size_t>(C) * ldbt * 4);
+    float* part = dbias ? take(static_cast<size_t>((BT + TILE - 1) / TILE) * OC * 4) : nullptr;
+
+    cudaError_t e = dbias ? launch_split<true, true, true>(dout, BT, OC, dout_hi, dout_lo, doutT_hi, doutT_lo, ldbt,
+                                                           part, stream)
+                          : launch_split<true, true, false>(dout, BT, OC, dout_hi, dout_lo, doutT_hi, doutT_lo, ldbt,
+                                                            nullptr, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_split<false, true, false>(weight, OC, C, nullptr, nullptr, wT_hi, wT_lo, OC, nullptr, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_split<false, true, false>(inp, BT, C, nullptr, nullptr, inpT_hi, inpT_lo, ldbt, nullptr, stream);
+    if (e != cudaSuccess) return e;
+    if (dbias) {
+        tile_sum_kernel<<<static_cast<unsigned>((OC + 255) / 256), 256, 0, stream>>>(dbias, part,
+                                                                                       (BT + TILE - 1) / TILE, OC);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // dinp (BT x C) += dout . (weight^T)^T, K = OC
+    const TcPlan p1 = tc_make_plan_x3(BT, C, OC, num_sms);
+    e = tc_launch_x3(p1, dinp, dout_hi, dout_lo, OC, wT_hi, wT_lo, OC, BT, C, OC, stream);
+    if (e != cudaSuccess) return e;
+    // dweight (OC x C) += (dout^T) . (inp^T)^T, K = BT
+    const TcPlan p2 = tc_make_plan_x3(OC, C, BT, num_sms);
+    return tc_launch_x3(p2, dweight, doutT_hi, doutT_lo, ldbt, inpT_hi, inpT_lo, ldbt, OC, C, BT, stream);
+}
+
+}  // namespace mmbwd

@@ -211,10 +211,14 @@ __device__ __forceinline__ uint4 add_round8(uint4 old, const float (&s)[8]) {
     return r;
 }
 
-// FWD = false: the backward (dinp and dweight items); FWD = true: the forward
-// (dinp-type items with a K-major B and an overwrite epilogue). Two
-// instantiations, so that neither pays for the other's branches.
-template <bool FWD>
+// MODE 0: the backward (dinp and dweight items). MODE 1: the forward
+// (dinp-type items with a K-major B and an overwrite epilogue). MODE 2: one
+// fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves, both
+// operands K-major: each operand arrives as a high part (its tf32 value) and
+// a low part (the exact remainder), and each K step issues three tf32 MMAs,
+// hi.hi + hi.lo + lo.hi, into one fp32 accumulator; fp32 read-modify-write
+// epilogue. Three instantiations, so that none pays for the others' branches.
+template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_mmbwd_kernel(const __grid_constant__ CUtensorMap tm_dout_k,   // dout, A of dinp (K-major)
                     const __grid_constant__ CUtensorMap tm_weight,   // weight, B of dinp (MN-major)
@@ -223,6 +227,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_dinp_out, // dinp, for L2 prefetch of old values
                     const __grid_constant__ CUtensorMap tm_dw_out,   // dweight, likewise
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
+    constexpr bool FWD = MODE != 0;  // dinp-type items only, K-major B
+    constexpr bool X3 = MODE == 2;   // fp32 from three tf32 products
+    // MODE 2 stages hold A hi | A lo | B hi | B lo (twice the bytes, half the
+    // stages: the same shared memory) and 32 fp32 of K per k-block (128 bytes).
+    constexpr int STAGES = X3 ? TC_STAGES / 2 : TC_STAGES;
+    constexpr int STG_BYTES = X3 ? 2 * STAGE_BYTES : STAGE_BYTES;
+    constexpr int KBLK = X3 ? TC_BK / 2 : TC_BK;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -306,21 +317,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint16_t bmask = static_cast<uint16_t>((1u << crank) | (1u << twin));
                 // Output tile of this CTA, prefetched into L2 a few k-blocks before the
                 // main loop ends so that the epilogue's read of the old values hits L2.
-                const bool direct = !(it.is_dw && p.splits > 1) && !FWD;  // forward: nothing to read back
+                const bool direct = X3 || (!(it.is_dw && p.splits > 1) && !FWD);  // forward: nothing to read back
                 const int64_t out_rows = it.is_dw ? p.OC : p.BT;
                 const int pf_kb = max(it.kb0, it.kb1 - 8);
                 int na;
                 if (it.is_dw) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
                 else na = row0 < p.BT ? 1 : 0;
-                const uint32_t bytes =
-                    static_cast<uint32_t>((it.is_dw ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES);
+                const uint32_t bytes = static_cast<uint32_t>(
+                    ((it.is_dw ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES) * (X3 ? 2 : 1));
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wt.wait(bars + 8u * (BAR_EMPTY + stage), phase ^ 1u, SITE_PRODUCER_EMPTY, w)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sA = base + stage * STAGE_BYTES;
-                    const uint32_t sB = sA + A_BYTES;
+                    const uint32_t sA = base + stage * STG_BYTES;
+                    const uint32_t sB = sA + (X3 ? 2 : 1) * A_BYTES;
                     const uint32_t fb = bars + 8u * (BAR_FULL + stage);
                     ptx::mbar_arrive_expect_tx(fb, bytes);
                     if (direct && kb == pf_kb && row0 < out_rows) {
@@ -329,27 +340,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 ptx::tma_prefetch_l2_2d(it.is_dw ? &tm_dw_out : &tm_dinp_out,
                                                         it.n_tile * it.bn + j * 128, row0);
                     }
-                    if (it.is_dw) {
+                    if (X3) {
+                        // A hi, A lo (maps 0 and 2), then B hi, B lo (maps 1 and 3)
+                        if (na) {
+                            ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * KBLK, row0);
+                            ptx::tma_load_2d(sA + A_BYTES, &tm_dout_mn, fb, kb * KBLK, row0);
+                        }
+                        for (int j = 0; j < nb; ++j) {
+                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_weight, fb, kb * KBLK, col0 + j * 64);
+                            ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, &tm_inp, fb, kb * KBLK, col0 + j * 64);
+                        }
+                    } else if (it.is_dw) {
                         for (int j = 0; j < na; ++j)
-                            ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * TC_BK);
+                            ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * KBLK);
                     } else if (na) {
-                        ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * TC_BK, row0);
+                        ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * KBLK, row0);
                     }
                     const void* tmB = it.is_dw ? static_cast<const void*>(&tm_inp) : static_cast<const void*>(&tm_weight);
                     // B boxes: 64 columns x 64 k, MN-major (backward) or K-major (forward)
-                    if (ppc == 1) {
+                    if (X3) {
+                        // loaded above (one pair per cluster)
+                    } else if (ppc == 1) {
                         for (int j = 0; j < nb; ++j) {
-                            if (FWD) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, kb * TC_BK, col0 + j * 64);
-                            else ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * TC_BK);
+                            if (FWD) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, kb * KBLK, col0 + j * 64);
+                            else ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * KBLK);
                         }
                     } else if (static_cast<int>(pp) < nb) {
                         const int cj = col0 + static_cast<int>(pp) * 64;
-                        if (FWD) ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, kb * TC_BK, cj, bmask);
-                        else ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, cj, kb * TC_BK, bmask);
+                        if (FWD) ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, kb * KBLK, cj, bmask);
+                        else ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, cj, kb * KBLK, bmask);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == TC_STAGES) {
+                    if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -377,8 +400,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * TC_BN;
-                    const uint32_t idesc =
-                        ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw, /*B MN*/ FWD ? 0 : 1);
+                    const uint32_t idesc = X3 ? ptx::idesc_tf32_f32(TC_PAIR_BM, it.bn, 0, 0)
+                                              : ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw,
+                                                                    /*B MN*/ FWD ? 0 : 1);
                     for (int kb = it.kb0; kb < it.kb1; ++kb) {
                         // Both CTAs' copies of this stage have landed (own bytes +
                         // the odd CTA's forwarded arrival).
@@ -387,8 +411,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t sA = base + stage * STAGE_BYTES;
-                        const uint32_t sB = sA + A_BYTES;
+                        const uint32_t sA = base + stage * STG_BYTES;
+                        const uint32_t sB = sA + (X3 ? 2 : 1) * A_BYTES;
+                        if constexpr (X3) {
+                            // K-major tf32 slices of 8 elements: 32 bytes further into
+                            // each swizzled 128-byte row, as for the bf16 K-major case.
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t ah = ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
+                                const uint64_t al = ptx::smem_desc_sw128(sA + A_BYTES + k * 32, 16, 1024);
+                                const uint64_t bh = ptx::smem_desc_sw128(sB + k * 32, 16, 1024);
+                                const uint64_t bl = ptx::smem_desc_sw128(sB + B_BYTES + k * 32, 16, 1024);
+                                ptx::mma_tf32_pair(d_tmem, ah, bh, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
+                                ptx::mma_tf32_pair(d_tmem, ah, bl, idesc, 1u);
+                                ptx::mma_tf32_pair(d_tmem, al, bh, idesc, 1u);
+                            }
+                        } else {
 #pragma unroll
                         for (int k = 0; k < TC_BK / 16; ++k) {
                             // K-major A: the 16-element K slice starts 32 bytes further
@@ -404,8 +442,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                          : ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
                             ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
                         }
+                        }
                         ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), empty_mask);
-                        if (++stage == TC_STAGES) {
+                        if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -438,7 +477,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             break;
                         }
                         ptx::mbar_arrive_cluster_relaxed(leader_full + 8u * stage);
-                        if (++stage == TC_STAGES) {
+                        if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -474,7 +513,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (has_bias) {
                         // A tile of dweight: 64 BT rows x 64 OC columns per box, each
                         // row 128 bytes with its 16-byte chunks swizzled by (row & 7).
-                        const uint8_t* box = smem + stage * STAGE_BYTES + bw * BOX_BYTES;
+                        const uint8_t* box = smem + stage * STG_BYTES + bw * BOX_BYTES;
                         const int chunk = lane & 7;
 #pragma unroll
                         for (int j = 0; j < TC_BK / 4; ++j) {
@@ -496,7 +535,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
                         if (ppc == 2) ptx::mbar_arrive_cluster_relaxed(twin_empty + 8u * stage);
                     }
-                    if (++stage == TC_STAGES) {
+                    if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -545,13 +584,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int ncols = static_cast<int>(min(static_cast<int64_t>(it.bn), n_extent - col0));
             const int nchunks = it.bn / 32;
             __nv_bfloat16* D = it.is_dw ? p.dweight : p.dinp;
+            float* Df = reinterpret_cast<float*>(D);  // MODE 2: fp32 output
             bool rok[4];
             __nv_bfloat16* drow[4];
+            float* drowf[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int64_t row = qrow0 + 8 * i + r8;
                 rok[i] = row < rows_total;
                 drow[i] = D + (rok[i] ? row : 0) * n_extent + col0 + cg;
+                drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
             // All old output values of this tile, loaded before waiting for the
             // accumulator (the producer has prefetched them into L2).
@@ -560,7 +602,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int c = 0; c < TC_BN / 32; ++c)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    oldw[c][i] = (!split_mode && !FWD && c < nchunks && rok[i] && c * 32 + cg < ncols)
+                    oldw[c][i] = (!X3 && !split_mode && !FWD && c < nchunks && rok[i] && c * 32 + cg < ncols)
                                      ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
                                      : make_uint4(0u, 0u, 0u, 0u);
 
@@ -601,6 +643,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         float* pp = part + static_cast<size_t>(q * 32 + lr) * p.dw_bn + c * 32 + cg;
                         __stcg(reinterpret_cast<float4*>(pp), a4);
                         __stcg(reinterpret_cast<float4*>(pp + 4), b4);
+                    } else if (X3) {
+                        // fp32 read-modify-write (the old values were prefetched into L2)
+                        if (rok[i] && c * 32 + cg < ncols) {
+                            float4* dp = reinterpret_cast<float4*>(drowf[i] + c * 32);
+                            float4 o0 = dp[0], o1 = dp[1];
+                            o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
+                            o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
+                            dp[0] = o0;
+                            dp[1] = o1;
+                        }
                     } else if (rok[i] && c * 32 + cg < ncols) {
                         float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
                         uint4 base8 = oldw[c][i];  // zero for the forward: out = acc (+ bias)
@@ -813,9 +865,11 @@ bool g_attr_set[64];
 size_t tc_smem_bytes() { return SMEM_TOTAL; }
 
 int tc_max_active_clusters(int cluster_size) {
-    if (cudaFuncSetAttribute(tc_mmbwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+    if (cudaFuncSetAttribute(tc_mmbwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(tc_mmbwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+        cudaFuncSetAttribute(tc_mmbwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc_mmbwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
             cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
@@ -830,7 +884,7 @@ int tc_max_active_clusters(int cluster_size) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_mmbwd_kernel<false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_mmbwd_kernel<0>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -929,6 +983,45 @@ TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int 
     return make_plan_impl(BT, OC, C, num_sms, num_quads, false);
 }
 
+// One fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves: one
+// pair per cluster, k-blocks of 32, the tile width (128 or 256) that gives the
+// fewer column-weighted waves of 256-row tiles over the pairs; items are equal
+// in cost, so a round-robin assignment is balanced.
+TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
+    TcPlan pl{};
+    pl.ppc = 1;
+    pl.dinp_kb = ceil_div_i(K, TC_BK / 2);
+    pl.dw_kb = 0;
+    pl.dinp_tiles_m = ceil_div_i(M, TC_PAIR_BM);
+    const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
+    double best = 1e300;
+    const long force = env_long("MMBWD_TILE_N_X3", 0);
+    for (int bn = 256; bn >= 128; bn -= 128) {
+        if (force && bn != force) continue;
+        const int tiles = pl.dinp_tiles_m * ceil_div_i(N, bn);
+        const int pairs = std::max(1, std::min(tiles, max_pairs));
+        const double cost = std::ceil(static_cast<double>(tiles) / pairs) * (bn + 32);
+        if (cost < best) {
+            best = cost;
+            pl.dinp_bn = bn;
+        }
+    }
+    pl.dw_bn = pl.dinp_bn;
+    pl.dinp_tiles_n = ceil_div_i(N, pl.dinp_bn);
+    pl.dw_tiles_n = pl.dinp_tiles_n;
+    pl.n_dinp_items = pl.dinp_tiles_m * pl.dinp_tiles_n;
+    pl.n_dw_items = 0;
+    pl.n_items = pl.n_dinp_items;
+    pl.splits = 1;
+    pl.kb_per_split = pl.dinp_kb;
+    const int pairs = std::max(1, std::min(pl.n_items, max_pairs));
+    pl.grid = 2 * pairs;
+    pl.table = 0;  // round robin
+    pl.est_us = best;
+    pl.fixup_grid = 0;
+    return pl;
+}
+
 namespace {
 
 struct MapSpec {
@@ -936,20 +1029,23 @@ struct MapSpec {
     uint64_t inner, outer;  // elements: contiguous dimension, rows
     uint32_t box_inner, box_outer;
     CUtensorMapSwizzle swz;
+    uint64_t pitch = 0;     // bytes between rows (0: inner x element size)
 };
 
 // Encodes the six tensor maps, completes the parameters from the plan, and
 // launches the kernel (and the split fixup when the plan splits dweight).
-cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParams& p, bool fwd, cudaStream_t stream) {
+cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParams& p, int mode, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     {
         std::lock_guard<std::mutex> g(g_attr_mutex);
         if (dev < 0 || dev >= 64 || !g_attr_set[dev]) {
-            e = cudaFuncSetAttribute(tc_mmbwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+            e = cudaFuncSetAttribute(tc_mmbwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(tc_mmbwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+                e = cudaFuncSetAttribute(tc_mmbwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(tc_mmbwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) g_attr_set[dev] = true;
         }
@@ -959,10 +1055,12 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     CUtensorMap maps[6];
     for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
-        const cuuint64_t strides[1] = {specs[i].inner * 2};
+        const uint64_t es = mode == 2 ? 4 : 2;
+        const cuuint64_t strides[1] = {specs[i].pitch ? specs[i].pitch : specs[i].inner * es};
         const cuuint32_t box[2] = {specs[i].box_inner, specs[i].box_outer};
         const cuuint32_t estr[2] = {1, 1};
-        const CUresult r = encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(specs[i].base),
+        const CUresult r = encode(&maps[i], mode == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                  2, const_cast<void*>(specs[i].base),
                                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, specs[i].swz,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -1000,11 +1098,14 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (fwd)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<true>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+    if (mode == 2)
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                               plan.sched);
+    else if (mode == 1)
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
     else
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<false>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     cudaLaunchConfig_t fcfg{};
@@ -1041,7 +1142,7 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
     p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
-    return launch_common(plan, specs, p, false, stream);
+    return launch_common(plan, specs, p, 0, stream);
 }
 
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight, const void* bias,
@@ -1062,7 +1163,29 @@ cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, co
     p.n_dinp = OC;
     p.fwd_bias = static_cast<const __nv_bfloat16*>(bias);
     p.dinp = static_cast<__nv_bfloat16*>(out);
-    return launch_common(plan, specs, p, true, stream);
+    return launch_common(plan, specs, p, 1, stream);
+}
+
+cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
+                         const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream) {
+    const uint64_t m = static_cast<uint64_t>(M), n = static_cast<uint64_t>(N), k = static_cast<uint64_t>(K);
+    const uint64_t pa = static_cast<uint64_t>(lda) * 4, pb = static_cast<uint64_t>(ldb) * 4;
+    const MapSpec specs[6] = {
+        {a_hi, k, m, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa},  // A hi, K-major (128 rows per box)
+        {b_hi, k, n, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb},     // B hi, K-major (64 rows per box)
+        {a_lo, k, m, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa},  // A lo
+        {b_lo, k, n, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb},     // B lo
+        {D, n, m, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},            // D, L2 prefetch of old values
+        {D, n, m, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},            // (dweight slot, unused)
+    };
+    TcParams p{};
+    p.BT = M;
+    p.C = K;
+    p.OC = K;
+    p.n_dinp = N;
+    p.dinp = reinterpret_cast<__nv_bfloat16*>(D);
+    return launch_common(plan, specs, p, 2, stream);
 }
 
 cudaError_t tc_read_status(int* code, int* info3, bool reset) {

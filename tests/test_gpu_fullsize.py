@@ -13,7 +13,7 @@ from gpu_helpers import TOL, scaled_error, to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 CONFIGS = ["tiny", "attn_proj", "mlp:0", "mlp:1", "lm_head", "xl_fc_bf16", "xl_qkv_bf16",
-           "xl_fc_f32", "xl_qkv_f32"]
+           "xl_fc_f32", "xl_qkv_f32", "xl_fc_f32@ffma"]  # @ffma: the fp32 FMA kernel forced
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,6 +49,10 @@ def test_full_size_sampled_parity(name, monkeypatch):
 
     monkeypatch.delenv("MMBWD_SPLITK", raising=False)
     monkeypatch.delenv("MMBWD_GRID", raising=False)
+    monkeypatch.delenv("MMBWD_F32_PATH", raising=False)
+    if name.endswith("@ffma"):
+        name = name[: -len("@ffma")]
+        monkeypatch.setenv("MMBWD_F32_PATH", "ffma")
     layer = _layer(name)
     dt = layer.dtype
     x = synth.make_inputs(layer, seed=0)

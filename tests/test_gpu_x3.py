@@ -1,0 +1,78 @@
+"""The fp32 path on the tensor cores (three tf32 products per K step from
+split operands) through the C ABI against the oracle, element by element:
+ragged sizes (K not a multiple of the 32-deep k-block, rows not a multiple of
+the 256-row tile or of 4, one tile, many tiles), with and without dbias,
+run-to-run bitwise determinism, and the choice between it and the fp32 FMA
+kernel."""
+import numpy as np
+import pytest
+
+import linear_layer_gemms_gb300 as mm
+import oracle
+import synth
+from gpu_helpers import assert_close, run_gpu, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    mm.load()
+    yield
+
+
+def inputs(BT, C, OC, seed=0):
+    layer = synth.Layer("x3", 1, BT, C, OC, "f32", True, inp_std=1.0, w_std=0.02, dout_std=1.0,
+                        init_std=0.01)
+    return synth.make_inputs(layer, seed)
+
+
+# (BT, C, OC): K = OC or BT ragged against 32; BT not a multiple of 4 (the
+# transposed operands' rows are padded); one 256 x 128 tile; several tiles.
+SHAPES = [(64, 8, 4), (301, 264, 136), (513, 520, 1028), (256, 128, 256), (2048, 768, 768)]
+
+
+@pytest.mark.parametrize("bias", [True, False])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_x3_parity(shape, bias, monkeypatch):
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    BT, C, OC = shape
+    assert mm.mmbwd_plan_info(1, BT, C, OC, mm.F32)["path"] == 2
+    x = inputs(BT, C, OC)
+    g = run_gpu(x, 1, BT, C, OC, "f32", bias=bias)
+    ref = oracle.get("omp").matmul_backward(x["dout"], x["inp"], x["weight"], "f32", x["dinp"], x["dweight"],
+                                            bias=bias)
+    assert_close(to_host(g["dinp"], "f32"), ref[0], "f32", "dinp")
+    assert_close(to_host(g["dweight"], "f32"), ref[1], "f32", "dweight")
+    if bias:
+        assert_close(to_host(g["dbias"], "f32"), ref[2], "f32", "dbias")
+    else:
+        assert np.array_equal(to_host(g["dbias"], "f32"), x["dbias"].astype(np.float64))
+
+
+def test_x3_deterministic(monkeypatch):
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    BT, C, OC = 777, 392, 520
+    x = inputs(BT, C, OC, seed=5)
+    outs = []
+    for _ in range(3):
+        g = run_gpu(x, 1, BT, C, OC, "f32")
+        outs.append([g[k].cpu().numpy().tobytes() for k in ("dinp", "dweight", "dbias")])
+    assert outs[0] == outs[1] == outs[2]
+
+
+def test_path_choice(monkeypatch):
+    monkeypatch.delenv("MMBWD_F32_PATH", raising=False)
+    # the tiny check stays on the FMA kernel; the XL fp32 layers use the tensor cores
+    assert mm.mmbwd_plan_info(2, 64, 64, 192, mm.F32)["path"] == 0
+    assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 2
+    # shapes the split layout cannot take fall back: C not a multiple of 8
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    assert mm.mmbwd_plan_info(1, 512, 260, 512, mm.F32)["path"] == 0
+    monkeypatch.setenv("MMBWD_F32_PATH", "ffma")
+    assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 0
