@@ -483,24 +483,34 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
     """The remaining configurations of the workload set and the forward of the
     GPT-2 layers: back-to-back calls on device-resident inputs rotated over
     enough copies to exceed the L2 (see `input_sets`), timed with CUDA events,
-    reported with their plan and the fraction of the peak that bounds them
-    (bf16 tensor peak; the fp32 path against the FP32 ALU peak of 152 SMs x 128
-    lanes x 2 FLOP at the maximum SM clock)."""
+    reported with their plan and the fraction of the peak that bounds them:
+    the measured bf16 tensor peak for bf16; for fp32, the peak of the path the
+    plan chose -- the TF32 tensor peak (the measured bf16 peak x the nominal
+    tf32/bf16 ratio 1.1/2.25) for the three-product tensor-core path, whose own
+    ceiling is a third of it, or the FP32 ALU peak (152 SMs x 128 lanes x 2
+    FLOP at the maximum SM clock) for the FMA kernel."""
     peaks, _ = measured_peaks()
     fp32_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    tf32_peak = float(peaks["bf16_tflops"]) * 1.1 / 2.25
     sh = stream.cuda_stream
     out = {}
 
     def finish(name, layer, flops, sec, n_sets, set_bytes, plan=None):
         tf = flops / sec / 1e12
-        peak = float(peaks["bf16_tflops"]) if layer.dtype == "bf16" else fp32_peak
-        out[name] = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
-                     "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2),
-                     "frac_of_peak": round(tf / peak, 4),
-                     "peak": "bf16 tensor (measured)" if layer.dtype == "bf16" else
-                             f"fp32 ALU {fp32_peak:.1f} TFLOP/s (152 SMs x 128 lanes x 2 x max clock)",
-                     "input_sets": n_sets,
-                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
+        rec = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
+               "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2)}
+        if layer.dtype == "bf16":
+            rec.update(frac_of_peak=round(tf / float(peaks["bf16_tflops"]), 4), peak="bf16 tensor (measured)")
+        elif plan is not None and plan.get("path") == 2:
+            rec.update(frac_of_peak=round(tf / tf32_peak, 4),
+                       frac_of_3xtf32_ceiling=round(3 * tf / tf32_peak, 4),
+                       peak=f"tf32 tensor {tf32_peak:.0f} TFLOP/s (measured bf16 x 1.1/2.25); "
+                            "three tf32 products per fp32 product")
+        else:
+            rec.update(frac_of_peak=round(tf / fp32_peak, 4),
+                       peak=f"fp32 ALU {fp32_peak:.1f} TFLOP/s (152 SMs x 128 lanes x 2 x max clock)")
+        rec.update(input_sets=n_sets, l2="rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident")
+        out[name] = rec
         if plan is not None:
             out[name]["plan"] = plan
 
