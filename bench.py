@@ -571,7 +571,8 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         flops = 2 * layer.BT * layer.C * layer.OC + (layer.BT * layer.OC if layer.bias else 0)
         per_batch = max(len(calls), 20 if flops < 2.5e11 else 8)
         sec = time_back_to_back(torch, stream, calls, per_batch, batches)
-        finish(name, layer, flops, sec, n_sets, set_bytes)
+        finish(name, layer, flops, sec, n_sets, set_bytes,
+               {"path": mm.mmbwd_forward_path(layer.B, layer.T, layer.C, layer.OC, dt)})
         del sets, calls
         torch.cuda.empty_cache()
     # the LayerNorm backward (lnbwd_run): bound by HBM, reported in GB/s of

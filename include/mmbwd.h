@@ -18,7 +18,14 @@
  *   MMBWD_BF16: bf16 storage, products accumulated in fp32, each output element
  *               rounded once to bf16 (round-to-nearest-even) after the old value
  *               (converted to fp32) and the fp32 sum are added.
- *   MMBWD_F32:  fp32 storage, fp32 fused multiply-add accumulation.
+ *   MMBWD_F32:  fp32 storage and fp32-accurate products. Problems large enough
+ *               to fill the GPU (B*T, C, OC >= 256, C a multiple of 8) run on the
+ *               tensor cores: each operand is split into its tf32 value and the
+ *               exact fp32 remainder, and each product is formed from three tf32
+ *               products (hi.hi + hi.lo + lo.hi) accumulated in fp32 (relative
+ *               error near 2^-20 per product). Smaller or other shapes use fp32
+ *               fused multiply-adds on the CUDA cores. MMBWD_F32_PATH = "ffma" or
+ *               "x3" in the environment forces one where the shape allows it.
  *
  * Every entry point is plain C: device pointers, sizes, a CUDA stream.
  * Nothing here takes or returns a framework type.
@@ -78,7 +85,8 @@ extern "C" {
  * be NULL only when its tensor has no elements.
  *
  * Workspace: the bf16 path may need a library-owned fp32 workspace for its
- * split reduction (mmbwd_workspace_bytes). It is allocated per device on
+ * split reduction, and the fp32 tensor-core path one for the split operands
+ * (mmbwd_workspace_bytes). It is allocated per device on
  * first need and reused; growing it synchronises the device, so the first
  * call of a new, larger shape should not be made during stream capture
  * (MMBWD_ERR_CAPTURE). Calls that share a device share this workspace:
@@ -125,7 +133,7 @@ int mmbwd_version(void);
 /* Describe the work split mmbwd_run would use (a pure function of the shape
  * and the number of co-resident CTAs; num_sms <= 0 takes the current device's
  * value, or 152 without a usable device). out[0..n) receives, in order: path (0 = fp32 SIMT,
- * 1 = bf16 tensor-core), grid size (CTAs), work items, dweight splits, k-blocks
+ * 1 = bf16 tensor-core, 2 = fp32 from three tf32 products), grid size (CTAs), work items, dweight splits, k-blocks
  * per split, dinp tiles, dweight tiles, schedule kind (1 = per-cluster tables),
  * tile M (rows per cluster), tile N of dinp, tile N of dweight, tile K,
  * pipeline stages, kernel launches per call, CTA pairs per cluster. num_sms
@@ -157,12 +165,20 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
  *   dtype          MMBWD_F32 or MMBWD_BF16 (all four tensors)
  *
  * bf16: fp32 accumulation on the tensor cores, out rounded once (RNE) after
- * adding the bias in fp32. fp32: FFMA accumulation. Same alignment, aliasing
- * (out must not overlap an input), status codes, asynchrony and determinism
- * as mmbwd_run; no workspace. C == 0 gives out = bias (or 0).
+ * adding the bias in fp32. fp32: as for mmbwd_run, three tf32 products on the
+ * tensor cores for large layers (OC a multiple of 8; out is set to the bias,
+ * then the product is added), FFMA otherwise. Same alignment, aliasing (out
+ * must not overlap an input), status codes, asynchrony and determinism as
+ * mmbwd_run; the fp32 tensor-core path uses the library workspace. C == 0
+ * gives out = bias (or 0).
  */
 int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bias_or_null, int64_t B,
                   int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream);
+
+/* The path mmbwd_forward takes for this shape and type (0 = fp32 FMA kernel,
+ * 1 = bf16 tensor cores, 2 = fp32 from three tf32 products), or a negative
+ * status for invalid arguments. Reads MMBWD_F32_PATH like the call itself. */
+int mmbwd_forward_path(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype);
 
 /* Test hook: make the next `n` workspace allocations fail (MMBWD_ERR_ALLOC). */
 void mmbwd_debug_fail_next_alloc(int n);

@@ -51,6 +51,7 @@ SIGNATURES = {
     "mmbwd_debug_fail_next_alloc": ([_ci], None),
     "mmbwd_run_static_scratch": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
     "mmbwd_forward": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
+    "mmbwd_forward_path": ([_i64] * 4 + [_ci], _ci),
     "lnbwd_run": ([_vp] * 8 + [_i64] * 3 + [_ci, _vp], _ci),
     "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
@@ -135,6 +136,11 @@ def lnbwd_run(dinp, dweight, dbias, dout, inp, weight, mean, rstd, B: int, T: in
 
 def lnbwd_workspace_bytes(B: int, T: int, C: int, dtype: int) -> int:
     return int(load().lnbwd_workspace_bytes(B, T, C, dtype))
+
+
+def mmbwd_forward_path(B: int, T: int, C: int, OC: int, dtype: int) -> int:
+    """0 = fp32 FMA kernel, 1 = bf16 tensor cores, 2 = fp32 from three tf32 products."""
+    return int(load().mmbwd_forward_path(B, T, C, OC, dtype))
 
 
 def mmbwd_workspace_bytes(B: int, T: int, C: int, OC: int, dtype: int) -> int:

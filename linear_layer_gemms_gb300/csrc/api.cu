@@ -170,6 +170,15 @@ bool use_x3(int64_t BT, int64_t C, int64_t OC) {
     return BT >= 256 && C >= 256 && OC >= 256 && static_cast<double>(BT) * C * OC >= 6.7e7;
 }
 
+bool use_x3_forward(int64_t BT, int64_t C, int64_t OC) {
+    if (!x3_forward_shape_ok(BT, C, OC)) return false;
+    if (const char* f = std::getenv("MMBWD_F32_PATH")) {
+        if (std::strcmp(f, "ffma") == 0) return false;
+        if (std::strcmp(f, "x3") == 0) return true;
+    }
+    return BT >= 256 && C >= 256 && OC >= 256 && static_cast<double>(BT) * C * OC >= 6.7e7;
+}
+
 int ensure_workspace(DeviceState& d, size_t need, cudaStream_t stream) {
     if (need <= d.ws_bytes) return MMBWD_OK;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -419,13 +428,30 @@ int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bi
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     if (dtype == MMBWD_F32) {
-        e = simt_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
-                                static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC, stream);
+        if (use_x3_forward(s.BT, C, OC)) {
+            rc = ensure_workspace(*d, x3_forward_workspace_bytes(s.BT, C, OC), stream);
+            if (rc != MMBWD_OK) return rc;
+            e = x3_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
+                                  static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC,
+                                  d->ws, d->num_sms, stream);
+        } else {
+            e = simt_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
+                                    static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC,
+                                    stream);
+        }
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads, 1);
     e = tc_launch_forward(plan, out, inp, weight, bias, s.BT, C, OC, stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+int mmbwd_forward_path(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype) {
+    Shape s;
+    const int rc = check_shape(B, T, C, OC, dtype, &s);
+    if (rc != MMBWD_OK) return rc;
+    if (dtype == MMBWD_BF16) return 1;
+    return use_x3_forward(s.BT, C, OC) ? 2 : 0;
 }
 
 // ---------------------------------------------------------------------------

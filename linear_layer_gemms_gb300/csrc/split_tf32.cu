@@ -163,4 +163,35 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
     return tc_launch_x3(p2, dweight, doutT_hi, doutT_lo, ldbt, inpT_hi, inpT_lo, ldbt, OC, C, BT, stream);
 }
 
+// The forward out = inp . weight^T + bias on the same path: both operands are
+// already K-major, so they are only split; out is first set to the bias (or
+// zero) and the product is then added to it.
+bool x3_forward_shape_ok(int64_t BT, int64_t C, int64_t OC) {
+    return BT > 0 && C > 0 && OC > 0 && OC % 8 == 0 && C % 4 == 0 && (BT + TILE - 1) / TILE <= 65535 &&
+           (OC + TILE - 1) / TILE <= 65535;
+}
+
+size_t x3_forward_workspace_bytes(int64_t BT, int64_t C, int64_t OC) {
+    auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    return 2 * a(static_cast<size_t>(BT) * C * 4) + 2 * a(static_cast<size_t>(OC) * C * 4);
+}
+
+cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight, const float* bias, int64_t BT,
+                              int64_t C, int64_t OC, void* ws, int num_sms, cudaStream_t stream) {
+    auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* inp_hi = reinterpret_cast<float*>(w);
+    float* inp_lo = reinterpret_cast<float*>(w + a(static_cast<size_t>(BT) * C * 4));
+    float* w_hi = reinterpret_cast<float*>(w + 2 * a(static_cast<size_t>(BT) * C * 4));
+    float* w_lo = reinterpret_cast<float*>(w + 2 * a(static_cast<size_t>(BT) * C * 4) + a(static_cast<size_t>(OC) * C * 4));
+    cudaError_t e = fill_rows_launch(out, bias, BT, OC, MMBWD_F32, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_split<true, false, false>(inp, BT, C, inp_hi, inp_lo, nullptr, nullptr, 0, nullptr, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_split<true, false, false>(weight, OC, C, w_hi, w_lo, nullptr, nullptr, 0, nullptr, stream);
+    if (e != cudaSuccess) return e;
+    const TcPlan p = tc_make_plan_x3(BT, OC, C, num_sms);
+    return tc_launch_x3(p, out, inp_hi, inp_lo, C, w_hi, w_lo, C, BT, OC, C, stream);
+}
+
 }  // namespace mmbwd

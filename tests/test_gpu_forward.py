@@ -122,3 +122,17 @@ def test_forward_full_size_sampled(case, monkeypatch):
                                          bias=x["bias"] if name != "lm_head" else None)
     got = to_host(out[torch.from_numpy(rows).to(out.device)], dt)
     assert_close(got, ref, dt, name)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_forward_fp32_three_products(shape, monkeypatch):
+    """fp32 forward through the tensor-core path (operands split into tf32
+    high and exact low parts, three products per K step), forced on small and
+    ragged shapes; the default takes it for large layers."""
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    BT, C, OC = shape
+    for bias in (True, False):
+        x = inputs(BT, C, OC, "f32")
+        out = run_fwd(x, BT, C, OC, "f32", bias)
+        ref = oracle.get("omp").forward_rows(x["inp"], x["weight"], "f32", bias=x["bias"] if bias else None)
+        assert_close(to_host(out, "f32"), ref, "f32", "out")
