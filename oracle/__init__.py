@@ -2,9 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product library never imports it.
-``mmbwd_oracle.c`` (the linear layer) and ``layernorm_oracle.c`` (the
-LayerNorm backward) state what is computed and which readings of the CPU
-references they take.
+``mmbwd_oracle.c`` (the linear layer), ``layernorm_oracle.c`` (the LayerNorm
+backward) and ``encoder_oracle.c`` (the encoder backward) state what is
+computed and which readings of the pages they take.
 
 Builds (gcc, -O2, -ffp-contract=off, no -ffast-math):
   * ``st``  - single-threaded
@@ -21,14 +21,14 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = (os.path.join(_HERE, "mmbwd_oracle.c"), os.path.join(_HERE, "layernorm_oracle.c"))
+_SRCS = tuple(os.path.join(_HERE, f) for f in ("mmbwd_oracle.c", "layernorm_oracle.c", "encoder_oracle.c"))
 _BUILD = os.path.join(_HERE, "_build")
 _lock = threading.Lock()
 _libs: dict = {}
 
 F32, BF16, F64 = 0, 1, 2
 DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
-MUTANTS = tuple(range(1, 16))
+MUTANTS = tuple(range(1, 19))
 
 
 def lib_path(variant: str) -> str:
@@ -68,10 +68,11 @@ class Oracle:
         lib.oracle_layernorm_forward.argtypes = [vp] * 6 + [i64, i64, ci]
         lib.oracle_layernorm_dinp_rows.argtypes = [vp, vp, i64] + [vp] * 6 + [ci, i64, i64, ci]
         lib.oracle_layernorm_params.argtypes = [vp] * 8 + [ci, i64, i64, ci]
+        lib.oracle_encoder_backward.argtypes = [vp] * 6 + [i64] * 4 + [ci]
         for f in (lib.oracle_dinp_rows, lib.oracle_dweight_rows, lib.oracle_matmul_backward,
                   lib.oracle_forward_rows, lib.oracle_threads, lib.oracle_mutant,
                   lib.oracle_layernorm_forward, lib.oracle_layernorm_dinp_rows,
-                  lib.oracle_layernorm_params):
+                  lib.oracle_layernorm_params, lib.oracle_encoder_backward):
             f.restype = ci
         self._lib = lib
 
@@ -211,6 +212,26 @@ class Oracle:
                                                mean.ctypes.data, rstd.ctypes.data, sd, BT, C, dt)
         assert rc == 0
         return dw, db
+
+
+    # ------------------------------------------------------------------ encoder backward
+
+    def encoder_backward(self, dout, inp, B: int, T: int, V: int, dtype: str, dwte_init=None, dwpe_init=None):
+        """(dwte (V, C), dwpe (T, C)) in float64; dout is (B*T, C), inp (B*T,) int32."""
+        dt = DTYPES[dtype]
+        C = dout.shape[1]
+        for a in (dout, dwte_init, dwpe_init):
+            self._check(a, dt)
+        assert inp.dtype == np.int32 and inp.flags.c_contiguous and inp.size == B * T
+        dwte = np.empty((V, C), dtype=np.float64)
+        dwpe = np.empty((T, C), dtype=np.float64)
+        rc = self._lib.oracle_encoder_backward(dwte.ctypes.data, dwpe.ctypes.data, self._ptr(dwte_init),
+                                               self._ptr(dwpe_init), dout.ctypes.data, inp.ctypes.data,
+                                               B, T, C, V, dt)
+        if rc == -2:
+            raise ValueError("token id outside [0, V)")
+        assert rc == 0
+        return dwte, dwpe
 
 
 def get(variant: str = "st") -> Oracle:

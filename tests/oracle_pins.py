@@ -311,3 +311,6 @@ ALL_PINS = [pin_exact_unit_differences, pin_central_differences, pin_library_mat
 from oracle_pins_ln import LN_PINS  # noqa: E402
 
 ALL_PINS = ALL_PINS + LN_PINS
+from oracle_pins_enc import ENC_PINS  # noqa: E402
+
+ALL_PINS = ALL_PINS + ENC_PINS
