@@ -445,6 +445,7 @@ def run_gpu(args):
 
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32")
+ENC_CONFIGS = ("enc_gpt2_small", "enc_gpt2_small_f32")
 FORWARD_CONFIGS = (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
                    ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32"))
 
@@ -615,6 +616,39 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
                      "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
         del sets, calls
         torch.cuda.empty_cache()
+    # the encoder backward (encbwd_run): bound by HBM, GB/s of algorithmic bytes
+    for name in ENC_CONFIGS:
+        if only is not None and name not in only:
+            continue
+        p = synth.ENC_WORKLOADS[name]
+        x = synth.make_enc_inputs(p, seed=0)
+        set_bytes = p.bytes()
+        n_sets = input_sets(x["dout"].nbytes)
+        sets = []
+        for _ in range(n_sets):
+            t = {k: to_device_tensor(torch, x[k], dev) for k in ("dout", "dwte", "dwpe")}
+            t["inp"] = torch.from_numpy(x["inp"]).to(dev)
+            sets.append(t)
+        dt = mm.BF16 if p.dtype == "bf16" else mm.F32
+
+        def make_ecall(t, p=p, dt=dt):
+            def ecall():
+                rc = mm.encbwd_run(t["dwte"].data_ptr(), t["dwpe"].data_ptr(), t["dout"].data_ptr(),
+                                   t["inp"].data_ptr(), p.B, p.T, p.C, p.V, dt, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return ecall
+
+        calls = [make_ecall(t) for t in sets]
+        sec = time_back_to_back(torch, stream, calls, max(len(calls), 40), batches)
+        gbs = p.bytes() / sec / 1e9
+        out[name] = {"B": p.B, "T": p.T, "C": p.C, "V": p.V, "dtype": p.dtype, "us": round(sec * 1e6, 2),
+                     "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
+                     "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": p.bytes(),
+                     "tokens": "Zipf(s=1.1) over 50257 ids", "input_sets": n_sets,
+                     "l2": "rotating sets > L2" if n_sets * x["dout"].nbytes > L2_BYTES else "L2-resident"}
+        del sets, calls
+        torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
         raise RuntimeError(f"device status after other configs: {mm.strerror(status)} {info}")
@@ -671,7 +705,7 @@ def run_case(args):
 
     import linear_layer_gemms_gb300 as mm
 
-    names = set(OTHER_CONFIGS) | set(LN_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
+    names = set(OTHER_CONFIGS) | set(LN_CONFIGS) | set(ENC_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
     if args.case not in names:
         raise SystemExit(f"unknown case {args.case}; one of {sorted(names)}")
     dev = torch.device("cuda", 0)

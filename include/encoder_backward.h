@@ -1,0 +1,72 @@
+/*
+ * encoder_backward.h -- C ABI of the GPT-2 encoder backward in the same library
+ * (libmmbwd.so) as the linear-layer backward.
+ *
+ * The operation is the backward of the encoder of llm.c's llmc/encoder.cuh,
+ * whose forward adds token row inp[b,t] of wte and position row t of wpe:
+ *
+ *     dwte[ix, c] += sum over (b, t) with inp[b, t] == ix of dout[b, t, c]
+ *     dwpe[t, c]  += sum over b of dout[b, t, c]
+ *
+ * Deterministic: the positions of each token are gathered on the device (a
+ * stable sort of (token, position) keys), summed in position order in chunks
+ * of up to 32, and the chunks of a token added in order; dwpe is summed in
+ * batch order. No atomics on the data: repeated calls give bitwise identical
+ * results. Each output element is rounded
+ * once (round-to-nearest-even for bf16) after its old value is added.
+ *
+ * Element types: MMBWD_F32 or MMBWD_BF16 (mmbwd.h) for dwte, dwpe and dout;
+ * inp is int32.
+ */
+#ifndef ENCODER_BACKWARD_H
+#define ENCODER_BACKWARD_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#include "mmbwd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Limits of the single-block device sort (B*T positions, V token ids) and of
+ * the channel count C. */
+#define ENCBWD_MAX_POSITIONS 16384
+#define ENCBWD_MAX_VOCAB 131071
+#define ENCBWD_MAX_CHANNELS 65536
+
+/*
+ * encbwd_run -- enqueue the encoder backward on `stream`.
+ *
+ *   dwte   device, (V, C), read and written (+=)
+ *   dwpe   device, (T, C), read and written (+=)
+ *   dout   device, (B*T, C), read only
+ *   inp    device, (B*T) int32 token ids, read only
+ *   B, T, C, V   sizes >= 0; B*T <= ENCBWD_MAX_POSITIONS, V <= ENCBWD_MAX_VOCAB,
+ *                C <= ENCBWD_MAX_CHANNELS
+ *   dtype  MMBWD_F32 or MMBWD_BF16
+ *
+ * Argument order follows the page's encoder_backward (dwte, dwpe, dout, inp,
+ * B, T, C) with the vocabulary size added; no host copy of inp is needed.
+ *
+ * Returns MMBWD_OK or a negative MMBWD_ERR_* code (nothing enqueued on an
+ * error): ERR_NULL, ERR_DTYPE, ERR_SHAPE (a size out of range), ERR_ALIGN
+ * (dwte, dwpe, dout not 16-byte aligned or C times the element size not a
+ * multiple of 16 bytes; inp not 4-byte aligned), ERR_ALIAS, ERR_ALLOC /
+ * ERR_CAPTURE (the shared workspace). A token id outside [0, V) is skipped by
+ * the kernels and reported as MMBWD_ERR_SHAPE by mmbwd_device_status().
+ * B*T == 0, C == 0 enqueue nothing.
+ */
+int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+               int64_t V, int dtype, cudaStream_t stream);
+
+/* Workspace bytes encbwd_run needs for this problem (0 for invalid arguments). */
+size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENCODER_BACKWARD_H */

@@ -11,7 +11,8 @@ first use instead of falling back to anything else.
     dbias   (OC)      = sum over (b,t) of dout        (NULL / None skips it)
 
 and the layer's forward, out = inp . weight^T + bias (mmbwd_forward); plus the
-LayerNorm backward of a GPT-2 block (lnbwd_run, include/layernorm_backward.h).
+LayerNorm backward of a GPT-2 block (lnbwd_run, include/layernorm_backward.h)
+and the encoder backward (encbwd_run, include/encoder_backward.h).
 
 Pointers may be given as integers or as objects with ``data_ptr()`` (for
 example torch tensors on the current CUDA device); ``stream`` is a raw
@@ -35,8 +36,8 @@ STATIC_SCRATCH_BYTES = 32 << 20  # MMBWD_STATIC_SCRATCH_BYTES
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmmbwd.so")
 
-# Names and C signatures of every entry point declared in include/mmbwd.h and
-# include/layernorm_backward.h.
+# Names and C signatures of every entry point declared in include/mmbwd.h,
+# include/layernorm_backward.h and include/encoder_backward.h.
 _vp, _i64, _ci, _u64, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
                              ctypes.c_size_t)
 SIGNATURES = {
@@ -53,9 +54,12 @@ SIGNATURES = {
     "mmbwd_forward": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
     "mmbwd_forward_path": ([_i64] * 4 + [_ci], _ci),
     "lnbwd_run": ([_vp] * 8 + [_i64] * 3 + [_ci, _vp], _ci),
+    "encbwd_run": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
+    "encbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
     "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
 LNBWD_MAX_C = {F32: 2048, BF16: 4096}  # LNBWD_MAX_C_F32, LNBWD_MAX_C_BF16
+ENCBWD_MAX_POSITIONS, ENCBWD_MAX_VOCAB, ENCBWD_MAX_CHANNELS = 16384, 131071, 65536
 
 _lock = threading.Lock()
 _lib = None
@@ -132,6 +136,16 @@ def lnbwd_run(dinp, dweight, dbias, dout, inp, weight, mean, rstd, B: int, T: in
     and rstd are fp32 row statistics; returns the C status code."""
     return load().lnbwd_run(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp), _ptr(weight),
                             _ptr(mean), _ptr(rstd), B, T, C, dtype, _stream(stream))
+
+
+def encbwd_run(dwte, dwpe, dout, inp, B: int, T: int, C: int, V: int, dtype: int, stream=None) -> int:
+    """Enqueue the encoder backward (dwte and dwpe +=); inp holds int32 token
+    ids; returns the C status code."""
+    return load().encbwd_run(_ptr(dwte), _ptr(dwpe), _ptr(dout), _ptr(inp), B, T, C, V, dtype, _stream(stream))
+
+
+def encbwd_workspace_bytes(B: int, T: int, C: int, V: int, dtype: int) -> int:
+    return int(load().encbwd_workspace_bytes(B, T, C, V, dtype))
 
 
 def lnbwd_workspace_bytes(B: int, T: int, C: int, dtype: int) -> int:

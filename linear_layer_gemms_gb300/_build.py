@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmmbwd.so")
-SOURCES = ["api.cu", "tc_gemm.cu", "simt_f32.cu", "layernorm_bwd.cu", "split_tf32.cu"]
+SOURCES = ["api.cu", "tc_gemm.cu", "simt_f32.cu", "layernorm_bwd.cu", "split_tf32.cu", "encoder_bwd.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -36,7 +36,7 @@ def _cuda_lib_dir(nvcc: str) -> str:
 
 def _inputs():
     return ([os.path.join(CSRC, s) for s in SOURCES + HEADERS] +
-            [os.path.join(ROOT, "include", h) for h in ("mmbwd.h", "layernorm_backward.h")] +
+            [os.path.join(ROOT, "include", h) for h in ("mmbwd.h", "layernorm_backward.h", "encoder_backward.h")] +
             [os.path.abspath(__file__)])
 
 

@@ -3,6 +3,7 @@
 // contract of every entry point.
 #include "../../include/mmbwd.h"
 #include "../../include/layernorm_backward.h"
+#include "../../include/encoder_backward.h"
 #include "internal.h"
 
 #include <cuda.h>
@@ -381,6 +382,13 @@ int mmbwd_device_status(int reset, int* info) {
         if (info)
             for (int i = 0; i < 3; ++i) info[i] = ln_info[i];
     }
+    int enc_code = MMBWD_OK, enc_info[3] = {0, 0, 0};
+    if (enc_read_status(&enc_code, enc_info, reset != 0) != cudaSuccess) return MMBWD_ERR_CUDA;
+    if (code == MMBWD_OK && enc_code != MMBWD_OK) {
+        code = enc_code;
+        if (info)
+            for (int i = 0; i < 3; ++i) info[i] = enc_info[i];
+    }
     return code;
 }
 
@@ -452,6 +460,58 @@ int mmbwd_forward_path(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype) {
     if (rc != MMBWD_OK) return rc;
     if (dtype == MMBWD_BF16) return 1;
     return use_x3_forward(s.BT, C, OC) ? 2 : 0;
+}
+
+// ---------------------------------------------------------------------------
+// Encoder backward (encoder_backward.h)
+
+namespace {
+
+int enc_check(int64_t B, int64_t T, int64_t C, int64_t V, int dtype, int64_t* BT) {
+    if (dtype != MMBWD_F32 && dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    if (B < 0 || T < 0 || C < 0 || V < 0) return MMBWD_ERR_SHAPE;
+    if (!mul_ok(B, T, BT) || *BT > ENCBWD_MAX_POSITIONS || V > ENCBWD_MAX_VOCAB) return MMBWD_ERR_SHAPE;
+    int64_t x = 0;
+    if (!mul_ok(*BT, C, &x) || !mul_ok(V, C, &x) || C > ENCBWD_MAX_CHANNELS) return MMBWD_ERR_SHAPE;
+    return MMBWD_OK;
+}
+
+}  // namespace
+
+size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype) {
+    int64_t BT = 0;
+    if (enc_check(B, T, C, V, dtype, &BT) != MMBWD_OK || BT == 0 || C == 0) return 0;
+    return enc_workspace_bytes(BT, C);
+}
+
+int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+               int64_t V, int dtype, cudaStream_t stream) {
+    int64_t BT = 0;
+    int rc = enc_check(B, T, C, V, dtype, &BT);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = dtype == MMBWD_F32 ? 4 : 2;
+    const size_t b_out = static_cast<size_t>(BT) * C * es, b_wte = static_cast<size_t>(V) * C * es,
+                 b_wpe = static_cast<size_t>(T) * C * es, b_inp = static_cast<size_t>(BT) * 4;
+    if ((b_out && (!dout || !dwpe)) || (b_inp && !inp) || (b_wte && !dwte)) return MMBWD_ERR_NULL;
+    const void* vecs[3] = {dwte, dwpe, dout};
+    for (const void* p : vecs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(inp) & 3u) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+    if (overlaps(dwte, b_wte, dwpe, b_wpe) || overlaps(dwte, b_wte, dout, b_out) || overlaps(dwte, b_wte, inp, b_inp) ||
+        overlaps(dwpe, b_wpe, dout, b_out) || overlaps(dwpe, b_wpe, inp, b_inp))
+        return MMBWD_ERR_ALIAS;
+
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    if (BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
+    rc = ensure_workspace(*d, enc_workspace_bytes(BT, C), stream);
+    if (rc != MMBWD_OK) return rc;
+    const cudaError_t e = enc_launch(dwte, dwpe, dout, inp, B, T, C, V, dtype, d->ws, d->num_sms, stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

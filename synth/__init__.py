@@ -272,3 +272,69 @@ def make_ln_inputs(p: LNProblem, seed: int = 0) -> dict:
     out["dweight"] = normal((C,), dt, seed, LN_STREAM["dweight_init"], 0.0, p.init_std)
     out["dbias"] = normal((C,), dt, seed, LN_STREAM["dbias_init"], 0.0, p.init_std)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Encoder backward workloads (llm.c llmc/encoder.cuh; GPT-2 small: C=768, padded
+# vocabulary V=50304, B=8, T=1024)
+# ---------------------------------------------------------------------------
+
+ENC_STREAM = {"tokens": 300, "dout": 301, "dwte_init": 302, "dwpe_init": 303}
+
+
+@dataclass(frozen=True)
+class EncProblem:
+    """One encoder backward problem: dout (B,T,C), inp (B,T) token ids, dwte
+    (V,C), dwpe (T,C). Token ids follow a Zipf law over the first `V_used` ids
+    (p(k) ~ 1/(k+1)^s, the rank-frequency shape of text), so a few tokens
+    recur hundreds of times and most once or never, as with real batches."""
+    name: str
+    B: int
+    T: int
+    C: int
+    V: int
+    dtype: str
+    V_used: int = 50257
+    zipf_s: float = 1.1
+    dout_std: float = 1e-2
+    init_std: float = 1e-2
+
+    @property
+    def BT(self) -> int:
+        return self.B * self.T
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: dout read (for dwte and for dwpe), the touched
+        dwte rows read and written (bounded here by B*T rows), dwpe read and
+        written, token ids read."""
+        s = 4 if self.dtype == "f32" else 2
+        return 2 * self.BT * self.C * s + 2 * self.T * self.C * s + 4 * self.BT
+
+
+ENC_WORKLOADS = {
+    "enc_tiny": EncProblem("enc_tiny", 2, 64, 72, 97, "f32", V_used=90, dout_std=1.0),
+    "enc_gpt2_small": EncProblem("enc_gpt2_small", 8, 1024, 768, 50304, "bf16"),
+    "enc_gpt2_small_f32": EncProblem("enc_gpt2_small_f32", 8, 1024, 768, 50304, "f32"),
+}
+
+
+def zipf_tokens(n: int, v_used: int, s: float, seed: int, stream: int) -> np.ndarray:
+    """n token ids in [0, v_used) with p(k) proportional to 1/(k+1)^s, by the
+    inverse CDF of uniforms from the counter-based generator."""
+    w = 1.0 / np.power(np.arange(1, v_used + 1, dtype=np.float64), s)
+    cdf = np.cumsum(w)
+    cdf /= cdf[-1]
+    u = uniform(n, seed, stream)
+    return np.minimum(np.searchsorted(cdf, u, side="right"), v_used - 1).astype(np.int32)
+
+
+def make_enc_inputs(p: EncProblem, seed: int = 0) -> dict:
+    """Host arrays of one encoder backward problem: inp (int32), dout and the
+    initial dwte, dwpe (storage dtype)."""
+    dt = p.dtype
+    return {
+        "inp": zipf_tokens(p.BT, min(p.V_used, p.V), p.zipf_s, seed, ENC_STREAM["tokens"]),
+        "dout": normal((p.BT, p.C), dt, seed, ENC_STREAM["dout"], 0.0, p.dout_std),
+        "dwte": normal((p.V, p.C), dt, seed, ENC_STREAM["dwte_init"], 0.0, p.init_std),
+        "dwpe": normal((p.T, p.C), dt, seed, ENC_STREAM["dwpe_init"], 0.0, p.init_std),
+    }

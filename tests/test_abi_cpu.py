@@ -24,13 +24,13 @@ def declared_functions():
         if h.endswith(".h"):
             text = open(os.path.join(ROOT, "include", h)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b((?:mmbwd|lnbwd)_\w+)\s*\(", text))
+            names |= set(re.findall(r"\b((?:mmbwd|lnbwd|encbwd)_\w+)\s*\(", text))
     return sorted(names)
 
 
 def test_every_declared_symbol_is_exported_and_bound():
     names = declared_functions()
-    assert "mmbwd_run" in names and "lnbwd_run" in names and len(names) >= 11
+    assert "mmbwd_run" in names and "lnbwd_run" in names and "encbwd_run" in names and len(names) >= 14
     lib = mm.load()
     for n in names:
         assert hasattr(lib, n), n
@@ -202,3 +202,22 @@ def test_layernorm_rejects_bad_arguments():
     assert f(dweight=7 * A) == mm.ERR_ALIAS           # dweight on top of mean
     assert mm.lnbwd_workspace_bytes(-1, 8, 64, mm.BF16) == 0
     assert mm.LNBWD_MAX_C == {mm.F32: 2048, mm.BF16: 4096}
+
+
+def test_encoder_rejects_bad_arguments():
+    f = lambda **kw: mm.encbwd_run(**{**dict(dwte=A, dwpe=2 * A, dout=3 * A, inp=4 * A, B=2, T=8, C=64,  # noqa: E731
+                                             V=100, dtype=mm.BF16, stream=0), **kw})
+    assert f(dtype=5) == mm.ERR_DTYPE
+    assert f(T=-1) == mm.ERR_SHAPE
+    assert f(B=2, T=8193) == mm.ERR_SHAPE             # above ENCBWD_MAX_POSITIONS
+    assert f(V=131072) == mm.ERR_SHAPE                # above ENCBWD_MAX_VOCAB
+    assert f(C=65536 + 8) == mm.ERR_SHAPE             # above ENCBWD_MAX_CHANNELS
+    assert f(dout=None) == mm.ERR_NULL
+    assert f(inp=None) == mm.ERR_NULL
+    assert f(dwte=A + 8) == mm.ERR_ALIGN
+    assert f(inp=4 * A + 2) == mm.ERR_ALIGN
+    assert f(C=12) == mm.ERR_ALIGN                    # 24 bytes per row
+    assert f(dwpe=A + 64) == mm.ERR_ALIAS             # dwpe inside dwte
+    assert f(dwte=3 * A - 64) == mm.ERR_ALIAS         # dwte runs into dout
+    assert mm.encbwd_workspace_bytes(2, 8, 64, 100, mm.BF16) > 0
+    assert mm.encbwd_workspace_bytes(-1, 8, 64, 100, mm.BF16) == 0

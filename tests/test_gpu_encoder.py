@@ -1,0 +1,145 @@
+"""The encoder backward (encbwd_run) through the C ABI against the oracle,
+element by element on every dwte and dwpe element: ragged position counts
+(not powers of two), a token repeated far beyond one chunk, the largest sort
+(B*T = 16384), the GPT-2 small workload with Zipf-distributed tokens,
+run-to-run bitwise determinism, a token id out of range, empty problems."""
+import numpy as np
+import pytest
+
+import linear_layer_gemms_gb300 as mm
+import oracle
+import synth
+from gpu_helpers import assert_close, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    mm.load()
+    yield
+
+
+def run_enc(x, B, T, C, V, dtype):
+    import torch
+
+    g = {k: to_dev(x[k], dtype) for k in ("dout", "dwte", "dwpe")}
+    gi = torch.from_numpy(x["inp"]).to("cuda:0")
+    rc = mm.encbwd_run(g["dwte"], g["dwpe"], g["dout"], gi, B, T, C, V, mm.BF16 if dtype == "bf16" else mm.F32)
+    assert rc == mm.OK, mm.strerror(rc)
+    torch.cuda.synchronize()
+    return g
+
+
+def check(x, g, B, T, V, dtype):
+    ref_wte, ref_wpe = oracle.get("st").encoder_backward(x["dout"], x["inp"], B, T, V, dtype, x["dwte"], x["dwpe"])
+    assert_close(to_host(g["dwte"], dtype), ref_wte, dtype, "dwte")
+    assert_close(to_host(g["dwpe"], dtype), ref_wpe, dtype, "dwpe")
+
+
+def problem(B, T, C, V, dtype, v_used=None, seed=0):
+    p = synth.EncProblem("t", B, T, C, V, dtype, V_used=v_used or V, dout_std=1.0)
+    return synth.make_enc_inputs(p, seed)
+
+
+# (B, T, C, V, dtype): one position; a one-token vocabulary; a ragged count;
+# fp32; Zipf with long repeats; every position the same token (one segment of
+# many chunks); the largest sort with a narrow C; a vocabulary of 2^16 ids.
+CASES = [(1, 1, 8, 3, "bf16"), (1, 40, 16, 1, "f32"), (2, 37, 264, 50, "bf16"), (2, 64, 72, 97, "f32"),
+         (4, 300, 768, 1000, "bf16"), (3, 500, 128, 7, "f32"), (16, 1024, 16, 50304, "bf16"),
+         (2, 700, 32, 65536, "bf16")]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_encoder_parity(case):
+    B, T, C, V, dtype = case
+    x = problem(B, T, C, V, dtype)
+    g = run_enc(x, B, T, C, V, dtype)
+    check(x, g, B, T, V, dtype)
+    assert mm.mmbwd_device_status()[0] == mm.OK
+
+
+def test_encoder_single_token():
+    B, T, C, V, dtype = 4, 1000, 256, 10, "bf16"
+    x = problem(B, T, C, V, dtype)
+    x["inp"][:] = 3
+    g = run_enc(x, B, T, C, V, dtype)
+    check(x, g, B, T, V, dtype)
+
+
+@pytest.mark.parametrize("name", ["enc_tiny", "enc_gpt2_small", "enc_gpt2_small_f32"])
+def test_encoder_workloads(name):
+    p = synth.ENC_WORKLOADS[name]
+    x = synth.make_enc_inputs(p)
+    g = run_enc(x, p.B, p.T, p.C, p.V, p.dtype)
+    check(x, g, p.B, p.T, p.V, p.dtype)
+
+
+def test_encoder_deterministic():
+    import torch
+
+    p = synth.ENC_WORKLOADS["enc_gpt2_small"]
+    x = synth.make_enc_inputs(p, seed=2)
+    outs = []
+    for _ in range(3):
+        g = run_enc(x, p.B, p.T, p.C, p.V, p.dtype)
+        outs.append([bytes(g[k].cpu().view(-1).view(torch.uint8).numpy()) for k in ("dwte", "dwpe")])
+    assert outs[0] == outs[1] == outs[2]
+
+
+def test_encoder_bad_token_reported():
+    """A token id outside [0, V) is skipped and reported; with its dout row
+    zero, every output equals the oracle's with that id replaced."""
+    B, T, C, V, dtype = 1, 50, 64, 20, "f32"
+    x = problem(B, T, C, V, dtype)
+    x["inp"][17] = V + 5
+    x["dout"][17] = 0.0
+    mm.mmbwd_device_status(reset=True)
+    g = run_enc(x, B, T, C, V, dtype)
+    status, info = mm.mmbwd_device_status(reset=True)
+    assert status == mm.ERR_SHAPE and info[0] == 17 and info[1] == V + 5
+    fixed = dict(x)
+    fixed["inp"] = x["inp"].copy()
+    fixed["inp"][17] = 0
+    check(fixed, g, B, T, V, dtype)
+
+
+def test_encoder_empty_and_errors():
+    import torch
+
+    x = problem(1, 8, 16, 5, "bf16")
+    g = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+    gi = torch.from_numpy(x["inp"]).to("cuda:0")
+    before = {k: v.clone() for k, v in g.items()}
+    assert mm.encbwd_run(g["dwte"], g["dwpe"], g["dout"], gi, 0, 8, 16, 5, mm.BF16) == mm.OK
+    assert mm.encbwd_run(g["dwte"], g["dwpe"], g["dout"], gi, 1, 8, 0, 5, mm.BF16) == mm.OK
+    assert mm.encbwd_run(g["dwte"], g["dwte"], g["dout"], gi, 1, 8, 16, 5, mm.BF16) == mm.ERR_ALIAS
+    assert mm.encbwd_run(g["dwte"], g["dwpe"], g["dout"], gi.data_ptr() + 2, 1, 8, 16, 5, mm.BF16) == mm.ERR_ALIGN
+    torch.cuda.synchronize()
+    for k in g:
+        assert g[k].equal(before[k]), k
+
+
+def test_encoder_bad_tokens_among_last_id():
+    """Invalid ids interleaved with copies of the largest valid id of a
+    power-of-two vocabulary: the invalid positions are skipped (their dout
+    rows are zero here) and every valid one is summed."""
+    B, T, C, V, dtype = 2, 150, 64, 8, "bf16"
+    x = problem(B, T, C, V, dtype)
+    bad = np.arange(3, B * T, 7)
+    x["inp"][bad - 1] = V - 1
+    x["inp"][bad] = np.array([V, -1, 100, V + 1])[np.arange(bad.size) % 4]
+    x["dout"][bad] = 0
+    mm.mmbwd_device_status(reset=True)
+    g = run_enc(x, B, T, C, V, dtype)
+    status, info = mm.mmbwd_device_status(reset=True)
+    assert status == mm.ERR_SHAPE and info[0] in set(bad.tolist())
+    fixed = dict(x)
+    fixed["inp"] = x["inp"].copy()
+    fixed["inp"][bad] = 0
+    check(fixed, g, B, T, V, dtype)
