@@ -622,7 +622,8 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
             continue
         p = synth.ENC_WORKLOADS[name]
         x = synth.make_enc_inputs(p, seed=0)
-        set_bytes = p.bytes()
+        distinct = int(np.unique(x["inp"]).size)
+        set_bytes = p.bytes(distinct)
         n_sets = input_sets(x["dout"].nbytes)
         sets = []
         for _ in range(n_sets):
@@ -641,11 +642,11 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
 
         calls = [make_ecall(t) for t in sets]
         sec = time_back_to_back(torch, stream, calls, max(len(calls), 40), batches)
-        gbs = p.bytes() / sec / 1e9
+        gbs = set_bytes / sec / 1e9
         out[name] = {"B": p.B, "T": p.T, "C": p.C, "V": p.V, "dtype": p.dtype, "us": round(sec * 1e6, 2),
                      "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
-                     "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": p.bytes(),
-                     "tokens": "Zipf(s=1.1) over 50257 ids", "input_sets": n_sets,
+                     "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": set_bytes,
+                     "tokens": f"Zipf(s=1.1) over 50257 ids, {distinct} distinct", "input_sets": n_sets,
                      "l2": "rotating sets > L2" if n_sets * x["dout"].nbytes > L2_BYTES else "L2-resident"}
         del sets, calls
         torch.cuda.empty_cache()

@@ -8,24 +8,27 @@
 //   1. enc_sort_wpe_kernel. Block 0 (1024 threads) sorts the keys
 //      (token << 15) | position stably by token in shared memory (LSD radix
 //      passes of 4 bits over the token bits), so each token's positions end
-//      up contiguous and in increasing order; block scans then cut the sorted
-//      list into segments (one per token present) and chunks of at most 32
-//      positions (a long segment is several chunks), and write the tables.
+//      up contiguous and in increasing order, and writes the sorted keys and,
+//      per window of 32 sorted slots, where the run of the window's first slot
+//      begins and where the run of its last slot ends.
 //      Token ids outside [0, V) are left out and reported in the status word.
 //      The other blocks meanwhile form dwpe: one thread per (t, 16-byte
 //      vector) sums dout over b in order, adds the old value, rounds once.
-//   2. enc_chunk_kernel: one warp per (chunk, group of channels) sums its
-//      positions' dout rows in order. A segment of one chunk is finished at
-//      once (added to the old dwte row, rounded once). A longer segment's
-//      chunks write fp32 partials and count themselves on a per-(segment,
-//      channel group) counter; the last to arrive adds the partials in chunk
-//      order to the old row. Which warp is last varies, the order of the sum
-//      does not, so repeated calls give identical bits.
-// The second grid is sized from the upper bound B*T and loops over the chunk
-// count the sort wrote, so the host never waits for the device. Both launch
-// with programmatic stream serialization and wait for their predecessor
-// before touching global memory.
+//   2. enc_window_kernel: one warp per (window of 32 sorted slots, group of
+//      128 channels). The warp sums the window's dout rows in slot order, 16
+//      in flight for bf16 and 8 for fp32, cutting at token changes. A token run that lies inside the
+//      window is added to its old dwte row and rounded once. A run that
+//      crosses a window edge belongs to a token spanning windows wa..wb: each
+//      of those windows stores its fp32 partial and counts itself on the
+//      token's counter (kept at window wa); the last to arrive adds the
+//      partials in window order to the old row. Which warp is last varies,
+//      the order of the sum does not, so repeated calls give identical bits.
+// The second grid is sized from the upper bound B*T and its warps skip windows
+// past the valid count the sort wrote, so the host never waits for the
+// device. Both launch with programmatic stream serialization and wait for
+// their predecessor before touching global memory.
 #include <algorithm>
+#include <climits>
 
 #include "../../include/encoder_backward.h"
 #include "../../include/mmbwd.h"
@@ -40,7 +43,7 @@ __device__ unsigned int g_enc_status[4];
 namespace {
 
 constexpr int ENC_SORT_THREADS = 1024;
-constexpr int ENC_CHUNK = 32;  // positions per chunk
+constexpr int ENC_WIN = 32;  // sorted slots per window (one per lane)
 constexpr unsigned ENC_PAD = 0xFFFFFFFFu;
 constexpr int ENC_DIGIT_BITS = 4;  // radix digit width per pass
 constexpr int ENC_DIGITS = 1 << ENC_DIGIT_BITS;
@@ -53,6 +56,11 @@ constexpr int ENC_CNT_WORDS = ENC_CNT + ENC_CNT / 32;   // with one pad word per
 __device__ __forceinline__ int enc_cnt_at(int e) { return e + (e >> 5); }
 
 __device__ __forceinline__ void enc_grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream be scheduled now; it still waits (its
+// own griddepcontrol.wait) for this grid to finish before reading anything.
+__device__ __forceinline__ void enc_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <typename T>
 struct EncElem;
@@ -86,13 +94,42 @@ struct EncElem<__nv_bfloat16> {
     }
 };
 
+// Four channels per lane (8 bytes of bf16 or 16 of fp32), for the window kernel.
+template <typename T>
+struct EncVec4;
+template <>
+struct EncVec4<float> {
+    using V = uint4;
+    __device__ static V zero() { return make_uint4(0u, 0u, 0u, 0u); }
+    __device__ static V ld(const float* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+    __device__ static V ld_plain(const float* p) { return *reinterpret_cast<const uint4*>(p); }
+    __device__ static void st(float* p, V v) { *reinterpret_cast<uint4*>(p) = v; }
+    __device__ static void add(const V& v, float (&a)[4]) { EncElem<float>::add(v, a); }
+    __device__ static V add_round(const V& old, const float (&s)[4]) { return EncElem<float>::add_round(old, s); }
+};
+template <>
+struct EncVec4<__nv_bfloat16> {
+    using V = uint2;
+    using E = EncElem<__nv_bfloat16>;
+    __device__ static V zero() { return make_uint2(0u, 0u); }
+    __device__ static V ld(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+    __device__ static V ld_plain(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+    __device__ static void st(__nv_bfloat16* p, V v) { *reinterpret_cast<uint2*>(p) = v; }
+    __device__ static void add(const V& v, float (&a)[4]) {
+        a[0] += E::lo(v.x), a[1] += E::hi(v.x), a[2] += E::lo(v.y), a[3] += E::hi(v.y);
+    }
+    __device__ static V add_round(const V& old, const float (&s)[4]) {
+        return make_uint2(E::rp(old.x, s[0], s[1]), E::rp(old.y, s[2], s[3]));
+    }
+};
+
 struct EncTables {
-    int* meta;          // [0] valid positions, [1] chunks, [2] segments
-    int* rows;          // [B*T] positions in sorted order
-    int2* chunk;        // [B*T + 1] per chunk: first sorted index, segment (sentinel: valid positions, segments)
-    int2* seg;          // [B*T + 1] per segment: token id, first chunk (sentinel: 0, chunks)
-    unsigned* arrivals; // [B*T][G] chunks of a segment done, per channel group
-    float* partials;    // [B*T][C] fp32 chunk sums (segments of several chunks)
+    int* meta;           // [0] valid positions
+    unsigned* skeys;     // [B*T] sorted keys (token << 15 | position)
+    int* win_head;       // [windows] first slot of the run holding the window's first slot
+    int* win_tail;       // [windows] last slot of the run holding the window's last slot
+    unsigned* arrivals;  // [windows][G] windows done for the token whose run starts in the window
+    float* partials;     // [windows][2][C] fp32 sums of a window's first / last run
 };
 
 // Exclusive scan of one value per thread over the block (1024 threads, in
@@ -152,6 +189,44 @@ __device__ void enc_wpe_part(T* __restrict__ dwpe, const T* __restrict__ dout, i
     }
 }
 
+// Exclusive max-scan (over lower threads, -1 if none) and exclusive suffix
+// min-scan (over higher threads, INT_MAX if none) of one value per thread.
+__device__ void block_exclusive_max_and_suffix_min(int mx, int mn, int* warp_sums, int* warp_sums2, int* max_before,
+                                                   int* min_after) {
+    const int lane = static_cast<int>(threadIdx.x & 31), warp = static_cast<int>(threadIdx.x >> 5);
+    int x = mx, y = mn;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, x, off);
+        const int b = __shfl_down_sync(0xffffffffu, y, off);
+        if (lane >= off) x = max(x, a);
+        if (lane + off < 32) y = min(y, b);
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    if (lane == 0) warp_sums2[warp] = y;
+    __syncthreads();
+    if (warp == 0) {
+        int a = warp_sums[lane], b = warp_sums2[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, a, off);
+            const int v = __shfl_down_sync(0xffffffffu, b, off);
+            if (lane >= off) a = max(a, u);
+            if (lane + off < 32) b = min(b, v);
+        }
+        warp_sums[lane] = a;   // max over warps 0..lane
+        warp_sums2[lane] = b;  // min over warps lane..31
+    }
+    __syncthreads();
+    const int xe = __shfl_up_sync(0xffffffffu, x, 1), ye = __shfl_down_sync(0xffffffffu, y, 1);
+    int before = lane > 0 ? xe : -1, after = lane < 31 ? ye : INT_MAX;
+    if (warp > 0) before = max(before, warp_sums[warp - 1]);
+    if (warp < 31) after = min(after, warp_sums2[warp + 1]);
+    __syncthreads();
+    *max_before = before;
+    *min_after = after;
+}
+
 // Block 0: sort, segments, chunks, for NP = KPL * 1024 >= B*T key slots.
 // Thread t owns the KPL consecutive slots from t KPL. The keys start in
 // position order (padding, all ones, after the last position), so a stable
@@ -170,6 +245,7 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     enc_sort_wpe_kernel(const int32_t* __restrict__ inp, int BT, int V, int passes, int G, EncTables tb,
                         T* __restrict__ dwpe, const T* __restrict__ dout, int B, int T_, int C) {
     enc_grid_wait();
+    enc_launch_dependents();
     const int tid = static_cast<int>(threadIdx.x);
     if (blockIdx.x > 0) {
         enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(blockIdx.x - 1) * ENC_SORT_THREADS + tid,
@@ -180,8 +256,7 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     extern __shared__ __align__(16) unsigned enc_smem[];  // keys[NP], then counters[ENC_CNT_WORDS]
     unsigned* keys = enc_smem;
     int* cnt = reinterpret_cast<int*>(enc_smem + NP);
-    __shared__ int warp_sums[32];
-    const int lane = tid & 31, warp = tid >> 5;
+    __shared__ int warp_sums[32], warp_sums2[32];
     const int i0 = tid * KPL;
     unsigned k[KPL];
 #pragma unroll
@@ -258,187 +333,186 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     }
 
     // Each thread takes its KPL consecutive sorted slots, read once into
-    // registers with the token of the slot before; the scans below combine
-    // the threads' runs in thread order.
+    // registers with the tokens of the slots before and after.
     unsigned tk[KPL];  // token of each slot (the padding reads as all ones)
+    if constexpr (KPL >= 4) {
 #pragma unroll
-    for (int r = 0; r < KPL; ++r) tk[r] = keys[i0 + r] >> 15;
+        for (int q = 0; q < KPL / 4; ++q) {
+            const uint4 v = reinterpret_cast<const uint4*>(keys + i0)[q];
+            tk[4 * q] = v.x >> 15, tk[4 * q + 1] = v.y >> 15, tk[4 * q + 2] = v.z >> 15, tk[4 * q + 3] = v.w >> 15;
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < KPL; ++r) tk[r] = keys[i0 + r] >> 15;
+    }
     const unsigned tk_prev = i0 > 0 ? keys[i0 - 1] >> 15 : ENC_PAD;
     int nvalid_local = 0;
 #pragma unroll
     for (int r = 0; r < KPL; ++r) nvalid_local += tk[r] != (ENC_PAD >> 15);
     int nvalid = 0;
     block_exclusive_scan(nvalid_local, warp_sums, &nvalid);
-    // sorted positions, coalesced
-    for (int i = tid; i < nvalid; i += ENC_SORT_THREADS) tb.rows[i] = static_cast<int>(keys[i] & 0x7FFFu);
-    // segment starts (token changes)
-    bool starts[KPL];
-    int seg_local = 0;
-    int last_start_local = -1;  // last segment start inside this thread's slots
+    for (int i = tid; i < nvalid; i += ENC_SORT_THREADS) tb.skeys[i] = keys[i];  // coalesced
+    // run starts; the run holding a window's first slot starts at the largest
+    // start at or before it, the run holding its last slot ends before the
+    // smallest start after it
+    int first_start = INT_MAX, last_start = -1;
+    bool start0 = false;
 #pragma unroll
-    for (int r = 0; r < KPL; ++r) {
+    for (int r = KPL - 1; r >= 0; --r) {
         const int i = i0 + r;
-        starts[r] = i < nvalid && (i == 0 || tk[r] != (r > 0 ? tk[r - 1] : tk_prev));
-        if (starts[r]) {
-            ++seg_local;
-            last_start_local = i;
+        const bool st = i < nvalid && (i == 0 || tk[r] != (r > 0 ? tk[r - 1] : tk_prev));
+        if (st) {
+            first_start = i;
+            if (last_start < 0) last_start = i;
         }
+        if (r == 0) start0 = st;
     }
-    int nseg = 0;
-    const int seg_before = block_exclusive_scan(seg_local, warp_sums, &nseg);
-    // the start of the segment open at this thread's first slot: the largest
-    // segment start to the left (an exclusive max-scan over the threads)
-    int open_start = -1;
-    {
-        int x = last_start_local;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x = max(x, y);
-        }
-        if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int w = warp_sums[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, w, off);
-                if (lane >= off) w = max(w, y);
-            }
-            warp_sums[lane] = w;
-        }
-        __syncthreads();
-        const int excl_in_warp = __shfl_up_sync(0xffffffffu, x, 1);
-        open_start = lane > 0 ? excl_in_warp : -1;
-        if (warp > 0) open_start = max(open_start, warp_sums[warp - 1]);
-        __syncthreads();
-    }
-    // chunk starts: a segment start, or every ENC_CHUNK positions into a segment
-    bool cstarts[KPL];
-    int chunk_local = 0;
-    {
-        int os = open_start;
-#pragma unroll
-        for (int r = 0; r < KPL; ++r) {
-            const int i = i0 + r;
-            if (starts[r]) os = i;
-            cstarts[r] = i < nvalid && (starts[r] || (i - os) % ENC_CHUNK == 0);
-            chunk_local += cstarts[r];
-        }
-    }
-    int nchunk = 0;
-    const int chunk_before = block_exclusive_scan(chunk_local, warp_sums, &nchunk);
-    // tables; a segment's arrival counters are cleared when its second chunk starts
-    int sid = seg_before - 1, cid = chunk_before - 1;
-#pragma unroll
-    for (int r = 0; r < KPL; ++r) {
-        const int i = i0 + r;
-        if (cstarts[r]) {
-            ++cid;
-            if (starts[r]) {
-                open_start = i;
-                ++sid;
-                tb.seg[sid] = make_int2(static_cast<int>(tk[r]), cid);
-            }
-            tb.chunk[cid] = make_int2(i, sid);
-            if (i - open_start == ENC_CHUNK)
-                for (int g = 0; g < G; ++g) tb.arrivals[static_cast<int64_t>(sid) * G + g] = 0u;
-        }
-    }
-    if (tid == 0) {
-        tb.chunk[nchunk] = make_int2(nvalid, nseg);
-        tb.seg[nseg] = make_int2(0, nchunk);
-        tb.meta[0] = nvalid;
-        tb.meta[1] = nchunk;
-        tb.meta[2] = nseg;
-    }
+    int open_start = -1, next_start = INT_MAX;
+    block_exclusive_max_and_suffix_min(last_start, first_start, warp_sums, warp_sums2, &open_start, &next_start);
+    if ((i0 & (ENC_WIN - 1)) == 0 && i0 < nvalid) tb.win_head[i0 / ENC_WIN] = start0 ? i0 : open_start;
+    const int ilast = i0 + KPL - 1;
+    if (((ilast + 1) & (ENC_WIN - 1)) == 0 && ilast < nvalid)
+        tb.win_tail[ilast / ENC_WIN] = min(next_start, nvalid) - 1;
+    const int nwin_g = (nvalid + ENC_WIN - 1) / ENC_WIN * G;
+    for (int e = tid; e < nwin_g; e += ENC_SORT_THREADS) tb.arrivals[e] = 0u;
+    if (tid == 0) tb.meta[0] = nvalid;
 }
 
-// One warp per (chunk, channel group of 32 vectors), looping over the chunks:
-// the chunk's dout rows in sorted (position) order, sixteen loads in flight,
-// into an fp32 sum. A one-chunk segment goes straight to its dwte row;
-// otherwise the partial is stored and the last of the segment's chunks to
-// arrive adds all partials in chunk order (eight at a time in flight) to the
-// row. The table reads that do not depend on each other are issued together.
+// Finishes one run that crosses a window edge (see the file comment), the
+// token's windows being span.x..span.y: stores this window's partial (slot q:
+// 0 for the run entering at the window's first slot, 1 for the run leaving at
+// its last), counts the window on the token's counter, and if it is the last
+// of windows wa..wb adds their partials in window order (window wa's slot 1,
+// then slot 0 of the others) to the old dwte row. Warp-uniform.
+template <typename T>
+__device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, int c, bool active, int lane, int w,
+                              int q, int2 span, unsigned tok, const float (&acc)[4],
+                              typename EncVec4<T>::V old) {
+    using EV = EncVec4<T>;
+    constexpr int PB = 16;  // partials in flight
+    const int wa = span.x, wb = span.y, nw = wb - wa + 1;
+    if (active)
+        __stcg(reinterpret_cast<float4*>(tb.partials + (static_cast<int64_t>(w) * 2 + q) * C + c),
+               make_float4(acc[0], acc[1], acc[2], acc[3]));
+    __threadfence();
+    __syncwarp();
+    unsigned done = 0;
+    if (lane == 0) done = atomicAdd(&tb.arrivals[static_cast<int64_t>(wa) * gridDim.y + blockIdx.y], 1u);
+    done = __shfl_sync(0xffffffffu, done, 0);
+    if (done != static_cast<unsigned>(nw - 1) || !active) return;  // not the last window of the token
+    __threadfence();
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < nw; k += PB) {
+        float4 pv[PB];
+#pragma unroll
+        for (int u = 0; u < PB; ++u) {
+            const int64_t idx = (static_cast<int64_t>(wa + k + u) * 2 + (k + u == 0 ? 1 : 0)) * C + c;
+            pv[u] = k + u < nw ? __ldcg(reinterpret_cast<const float4*>(tb.partials + idx))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < PB; ++u)
+            if (k + u < nw) sum[0] += pv[u].x, sum[1] += pv[u].y, sum[2] += pv[u].z, sum[3] += pv[u].w;
+    }
+    EV::st(dwte + static_cast<int64_t>(tok) * C + c, EV::add_round(old, sum));
+}
+
+// One warp per (window of 32 sorted slots, group of 128 channels); lane l
+// holds slot 32 w + l and channels 4 l..4 l + 3 of the group. Runs of equal
+// tokens are cut with one ballot. The rows are summed in slot order, RB at a
+// time (16 for bf16, 8 for fp32: 4 KB per warp in flight, with every warp of
+// the grid resident at once), with the old dwte row of every run that ends in
+// the batch loaded alongside.
+// Loads that do not depend on each other are issued together (the keys are
+// read before the valid count is known, at indexes clamped to the table).
 // Lanes past C take part in the shuffles only.
 template <typename T>
-__global__ void __launch_bounds__(256) enc_chunk_kernel(T* __restrict__ dwte, const T* __restrict__ dout, int C,
-                                                       EncTables tb) {
-    using E = EncElem<T>;
-    constexpr int N = E::N;
-    constexpr int RB = 16;  // rows in flight
-    constexpr int PB = 8;   // partials in flight
+__global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte, const T* __restrict__ dout, int C,
+                                                           int BT, EncTables tb) {
+    using EV = EncVec4<T>;
+    using V = typename EV::V;
+    constexpr int RB = sizeof(T) == 2 ? 16 : 8;  // rows in flight
+    constexpr unsigned NONE = 0xFFFFFFFFu;
     enc_grid_wait();
+    enc_launch_dependents();
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-    const int c = (static_cast<int>(blockIdx.y) * 32 + lane) * N;
+    const int w = static_cast<int>(blockIdx.x) * 4 + warp;
+    const int base = w * ENC_WIN;
+    if (base >= BT) return;
+    const int c = (static_cast<int>(blockIdx.y) * 32 + lane) * 4;
     const bool active = c < C;
-    const int nchunk = tb.meta[1];
-    for (int cid = static_cast<int>(blockIdx.x) * 8 + warp; cid < nchunk; cid += static_cast<int>(gridDim.x) * 8) {
-        const int2 ch = tb.chunk[cid], ch1 = tb.chunk[cid + 1];
-        const int s0 = ch.x, sid = ch.y;
-        const int n = ch1.x - s0;  // 1..ENC_CHUNK
-        const int my_row = lane < n ? tb.rows[s0 + lane] : 0;
-        const int2 sg = tb.seg[sid], sg1 = tb.seg[sid + 1];
-        const int k0 = sg.y, nk = sg1.y - k0;
-        const int64_t tok = sg.x;
-        float acc[N];
+    const int nvalid = tb.meta[0];
+    const unsigned key = tb.skeys[min(base + lane, BT - 1)];
+    const unsigned pkey = base > 0 ? tb.skeys[base - 1] : NONE;
+    const unsigned nkey = base + ENC_WIN < BT ? tb.skeys[base + ENC_WIN] : NONE;
+    const int hstart = tb.win_head[w], tend = tb.win_tail[w];  // read only where defined (below)
+    if (base >= nvalid) return;
+    const int nv = min(ENC_WIN, nvalid - base);
+    const bool valid = lane < nv;
+    const unsigned tok = key >> 15;
+    unsigned ptok = __shfl_up_sync(0xffffffffu, tok, 1);
+    if (lane == 0) ptok = base > 0 ? pkey >> 15 : NONE;
+    const unsigned smask = __ballot_sync(0xffffffffu, valid && tok != ptok);  // run starts
+    const unsigned tok0 = __shfl_sync(0xffffffffu, tok, 0), tokl = __shfl_sync(0xffffffffu, tok, nv - 1);
+    const bool head_cross = (smask & 1u) == 0;  // the first run began in an earlier window
+    const bool tail_cross = nv == ENC_WIN && base + ENC_WIN < nvalid && (nkey >> 15) == tokl;
+    // windows wa..wb of the crossing runs: the head run's began at win_head; it
+    // ends here unless it fills the window and crosses the tail too, where its
+    // end and the tail run's end are win_tail
+    const int whead = head_cross ? hstart / ENC_WIN : w;
+    const int wtail = tail_cross ? tend / ENC_WIN : w;
+    const int2 hspan = make_int2(whead, (smask == 0u && tail_cross) ? wtail : w);
+    const int2 tspan = make_int2(w, wtail);
+    // run ends: slot j ends a run where slot j + 1 starts one or j is the last
+    const unsigned vmask = nv == ENC_WIN ? 0xffffffffu : (1u << nv) - 1u;
+    const unsigned emask = ((smask >> 1) | (1u << (nv - 1))) & vmask;
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, hacc[4] = {0.f, 0.f, 0.f, 0.f}, tacc[4] = {0.f, 0.f, 0.f, 0.f};
+    V hold = EV::zero(), told = EV::zero();
 #pragma unroll
-        for (int e = 0; e < N; ++e) acc[e] = 0.f;
-        for (int j0 = 0; j0 < n; j0 += RB) {
-            uint4 v[RB];
+    for (int j0 = 0; j0 < ENC_WIN; j0 += RB) {
+        if (j0 < nv) {  // warp-uniform
+            V v[RB], o[RB];
 #pragma unroll
             for (int u = 0; u < RB; ++u) {
-                const int64_t r = __shfl_sync(0xffffffffu, my_row, (j0 + u) & 31);
-                v[u] = (active && j0 + u < n) ? __ldg(reinterpret_cast<const uint4*>(dout + r * C + c))
-                                              : make_uint4(0u, 0u, 0u, 0u);
+                constexpr unsigned one = 1u;
+                const int j = j0 + u;  // compile-time slot
+                const unsigned kj = __shfl_sync(0xffffffffu, key, j);
+                const int64_t r = kj & 0x7FFFu, t = kj >> 15;
+                v[u] = (active && ((vmask >> j) & one)) ? EV::ld(dout + r * C + c) : EV::zero();
+                o[u] = (active && ((emask >> j) & one)) ? EV::ld_plain(dwte + t * C + c) : EV::zero();
             }
 #pragma unroll
-            for (int u = 0; u < RB; ++u)
-                if (j0 + u < n) E::add(v[u], acc);
-        }
-        if (nk > 1) {
-            float* part = tb.partials + static_cast<int64_t>(cid) * C + c;
-            if (active) {
+            for (int u = 0; u < RB; ++u) {
+                const int j = j0 + u;
+                if ((vmask >> j) & 1u) {  // warp-uniform
+                    EV::add(v[u], acc);
+                    if ((emask >> j) & 1u) {  // run ends at slot j (warp-uniform)
+                        const int64_t t = __shfl_sync(0xffffffffu, key, j) >> 15;
+                        const unsigned below = j == 31 ? 0xffffffffu : (2u << j) - 1u;
+                        const bool is_head = head_cross && (smask & below) == 0;
+                        const bool is_tail = tail_cross && j == nv - 1;
+                        if (is_head) {
 #pragma unroll
-                for (int e = 0; e < N; e += 4)
-                    __stcg(reinterpret_cast<float4*>(part + e), make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]));
-            }
-            __threadfence();
-            __syncwarp();
-            unsigned done = 0;
-            if (lane == 0) done = atomicAdd(&tb.arrivals[static_cast<int64_t>(sid) * gridDim.y + blockIdx.y], 1u);
-            done = __shfl_sync(0xffffffffu, done, 0);
-            if (done != static_cast<unsigned>(nk - 1)) continue;  // not the last chunk of the segment
-            __threadfence();
+                            for (int e = 0; e < 4; ++e) hacc[e] = acc[e];
+                            hold = o[u];
+                        } else if (is_tail) {
 #pragma unroll
-            for (int e = 0; e < N; ++e) acc[e] = 0.f;
-            if (active) {
-                const float* src = tb.partials + static_cast<int64_t>(k0) * C + c;
-                for (int k = 0; k < nk; k += PB) {
-                    float4 pv[PB][N / 4];
-#pragma unroll
-                    for (int u = 0; u < PB; ++u)
-#pragma unroll
-                        for (int e = 0; e < N / 4; ++e)
-                            pv[u][e] = k + u < nk ? __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(k + u) * C) + e)
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int u = 0; u < PB; ++u)
-                        if (k + u < nk) {
-#pragma unroll
-                            for (int e = 0; e < N / 4; ++e) {
-                                acc[4 * e] += pv[u][e].x, acc[4 * e + 1] += pv[u][e].y;
-                                acc[4 * e + 2] += pv[u][e].z, acc[4 * e + 3] += pv[u][e].w;
-                            }
+                            for (int e = 0; e < 4; ++e) tacc[e] = acc[e];
+                            told = o[u];
+                        } else if (active) {
+                            EV::st(dwte + t * C + c, EV::add_round(o[u], acc));
                         }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+                    }
                 }
             }
         }
-        if (active) {
-            uint4* dst = reinterpret_cast<uint4*>(dwte + tok * C + c);
-            *dst = E::add_round(*dst, acc);
-        }
     }
+    // A run that fills the window and crosses both edges is the head run.
+    if (head_cross) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, 0, hspan, tok0, hacc, hold);
+    if (tail_cross && smask != 0u) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, 1, tspan, tokl, tacc, told);
 }
 
 cudaError_t launch_pdl(const void* k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
@@ -476,18 +550,21 @@ const void* enc_sort_fn(int kpl) {
 
 }  // namespace
 
-// Sized for fp32 (4 elements per vector, the most channel groups).
-size_t enc_workspace_bytes(int64_t BT, int64_t C) {
-    const size_t n = static_cast<size_t>(BT);
-    return a256(4 * 4) + a256(n * 4) + a256((n + 1) * 8) + a256((n + 1) * 8) +
-           a256(n * static_cast<size_t>(enc_groups(C, 4)) * 4) + a256(n * static_cast<size_t>(C) * 4);
+// Workspace: meta, sorted keys, per-window tables, counters (four channels
+// per lane), partials.
+size_t enc_workspace_bytes(int64_t BT, int64_t C, int64_t V) {
+    const size_t n = static_cast<size_t>(BT), nwin = (n + ENC_WIN - 1) / ENC_WIN;
+    (void)V;
+    return a256(4 * 4) + a256(n * 4) + a256(nwin * 4) + a256(nwin * 4) +
+           a256(nwin * static_cast<size_t>(enc_groups(C, 4)) * 4) + a256(nwin * 2 * static_cast<size_t>(C) * 4);
 }
 
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                        int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream) {
     const int BT = static_cast<int>(B * T);
-    const int N = dtype == MMBWD_F32 ? 4 : 8;
-    int G = enc_groups(C, N);
+    const int nwin = (BT + ENC_WIN - 1) / ENC_WIN;
+    const int N = dtype == MMBWD_F32 ? 4 : 8;  // elements per 16-byte vector (dwpe)
+    int G = enc_groups(C, 4);                   // window kernel: four channels per lane
     uint8_t* w = static_cast<uint8_t*>(ws);
     EncTables tb{};
     auto take = [&](size_t bytes) {
@@ -496,11 +573,11 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
         return p;
     };
     tb.meta = reinterpret_cast<int*>(take(4 * 4));
-    tb.rows = reinterpret_cast<int*>(take(static_cast<size_t>(BT) * 4));
-    tb.chunk = reinterpret_cast<int2*>(take((static_cast<size_t>(BT) + 1) * 8));
-    tb.seg = reinterpret_cast<int2*>(take((static_cast<size_t>(BT) + 1) * 8));
-    tb.arrivals = reinterpret_cast<unsigned*>(take(static_cast<size_t>(BT) * enc_groups(C, 4) * 4));
-    tb.partials = reinterpret_cast<float*>(take(static_cast<size_t>(BT) * C * 4));
+    tb.skeys = reinterpret_cast<unsigned*>(take(static_cast<size_t>(BT) * 4));
+    tb.win_head = reinterpret_cast<int*>(take(static_cast<size_t>(nwin) * 4));
+    tb.win_tail = reinterpret_cast<int*>(take(static_cast<size_t>(nwin) * 4));
+    tb.arrivals = reinterpret_cast<unsigned*>(take(static_cast<size_t>(nwin) * enc_groups(C, 4) * 4));
+    tb.partials = reinterpret_cast<float*>(take(static_cast<size_t>(nwin) * 2 * C * 4));
     int kpl = 1;
     while (kpl * ENC_SORT_THREADS < BT) kpl <<= 1;
     // sort on the smallest b with 2^b > V: the padding's digits (all ones) then
@@ -514,25 +591,23 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
     cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sort_smem));
     if (e != cudaSuccess) return e;
     int Vi = static_cast<int>(V), Ci = static_cast<int>(C), Bi = static_cast<int>(B), Ti = static_cast<int>(T);
+    int BTi = BT;
     {
         // block 0 sorts; one wave of blocks (at most one per SM besides it) forms dwpe
         const int64_t wpe_threads = (T * C / N + ENC_SORT_THREADS - 1) / ENC_SORT_THREADS;
         const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, std::max(num_sms - 1, 1)));
-        void* args[] = {const_cast<int32_t**>(&inp), const_cast<int*>(&BT), &Vi, &passes, &G, &tb,
+        void* args[] = {const_cast<int32_t**>(&inp), &BTi, &Vi, &passes, &G, &tb,
                         &dwpe, const_cast<void**>(&dout), &Bi, &Ti, &Ci};
         e = launch_pdl(ks, dim3(static_cast<unsigned>(1 + wpe_blocks)), dim3(ENC_SORT_THREADS), sort_smem, stream,
                        args);
         if (e != cudaSuccess) return e;
     }
     {
-        // about four blocks of eight warps per SM in all (two waves at two
-        // resident blocks per SM); each warp loops over chunks
-        const int per_group = std::max(1, 4 * num_sms / G);
-        const int gx = std::min((BT + 7) / 8, per_group);
-        void* args[] = {&dwte, const_cast<void**>(&dout), &Ci, &tb};
-        const void* k = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&enc_chunk_kernel<float>)
-                                           : reinterpret_cast<const void*>(&enc_chunk_kernel<__nv_bfloat16>);
-        e = launch_pdl(k, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(G)), dim3(256), 0, stream, args);
+        const void* k = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&enc_window_kernel<float>)
+                                           : reinterpret_cast<const void*>(&enc_window_kernel<__nv_bfloat16>);
+        void* args[] = {&dwte, const_cast<void**>(&dout), &Ci, &BTi, &tb};
+        e = launch_pdl(k, dim3(static_cast<unsigned>((nwin + 3) / 4), static_cast<unsigned>(G)), dim3(128), 0, stream,
+                       args);
     }
     return e;
 }

@@ -303,12 +303,13 @@ class EncProblem:
     def BT(self) -> int:
         return self.B * self.T
 
-    def bytes(self) -> int:
-        """Algorithmic HBM bytes: dout read (for dwte and for dwpe), the touched
-        dwte rows read and written (bounded here by B*T rows), dwpe read and
-        written, token ids read."""
+    def bytes(self, distinct_tokens: int | None = None) -> int:
+        """Algorithmic HBM bytes: dout read once, the touched dwte rows read and
+        written (distinct_tokens rows; without it, the bound min(B*T, V)), dwpe
+        read and written, token ids read."""
         s = 4 if self.dtype == "f32" else 2
-        return 2 * self.BT * self.C * s + 2 * self.T * self.C * s + 4 * self.BT
+        u = min(self.BT, self.V) if distinct_tokens is None else distinct_tokens
+        return self.BT * self.C * s + 2 * u * self.C * s + 2 * self.T * self.C * s + 4 * self.BT
 
 
 ENC_WORKLOADS = {
