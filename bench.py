@@ -446,6 +446,10 @@ def run_gpu(args):
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32")
 ENC_CONFIGS = ("enc_gpt2_small", "enc_gpt2_small_f32")
+# each MLP layer alone, rounded to nearest (mmbwd_run) and stochastically
+# (mmbwd_run_sr, a new seed per call)
+LAYER_CONFIGS = (("mlp_fc", "mlp:0", False), ("mlp_fc_proj", "mlp:1", False),
+                 ("mlp_fc_sr", "mlp:0", True), ("mlp_fc_proj_sr", "mlp:1", True))
 FORWARD_CONFIGS = (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
                    ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32"))
 
@@ -515,22 +519,26 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         if plan is not None:
             out[name]["plan"] = plan
 
-    for name in OTHER_CONFIGS:
+    backward = [(n, n, False) for n in OTHER_CONFIGS] + list(LAYER_CONFIGS)
+    for name, spec, sr in backward:
         if only is not None and name not in only:
             continue
-        layer = synth.WORKLOADS[name].layers[0]
+        wl, _, i = spec.partition(":")
+        layer = synth.WORKLOADS[wl].layers[int(i or 0)]
         x = synth.make_inputs(layer, seed=0)
         set_bytes = sum(v.nbytes for v in x.values())
         n_sets = input_sets(set_bytes)
         sets = [{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for _ in range(n_sets)]
         dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
 
-        def make_call(t, layer=layer, dt=dt):
+        def make_call(t, layer=layer, dt=dt, sr=sr):
+            seeds = iter(range(1, 1 << 62))
+
             def call():
-                rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
-                                  t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
-                                  t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T,
-                                  layer.C, layer.OC, dt, sh)
+                args = (t["dinp"].data_ptr(), t["dweight"].data_ptr(), t["dbias"].data_ptr() if layer.bias else None,
+                        t["dout"].data_ptr(), t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T,
+                        layer.C, layer.OC, dt)
+                rc = mm.mmbwd_run_sr(*args, next(seeds), sh) if sr else mm.mmbwd_run(*args, sh)
                 if rc != mm.OK:
                     raise RuntimeError(mm.strerror(rc))
             return call
@@ -541,6 +549,8 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
         finish(name, layer, layer.flops(), sec, n_sets, set_bytes,
                {k: info[k] for k in ("path", "grid", "items", "splits", "launches")})
+        if sr:
+            out[name]["rounding"] = "stochastic (mmbwd_run_sr, new seed per call)"
         del sets, calls
         torch.cuda.empty_cache()
     # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
@@ -706,7 +716,8 @@ def run_case(args):
 
     import linear_layer_gemms_gb300 as mm
 
-    names = set(OTHER_CONFIGS) | set(LN_CONFIGS) | set(ENC_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
+    names = (set(OTHER_CONFIGS) | set(LN_CONFIGS) | set(ENC_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
+             | {n for n, _, _ in LAYER_CONFIGS})
     if args.case not in names:
         raise SystemExit(f"unknown case {args.case}; one of {sorted(names)}")
     dev = torch.device("cuda", 0)

@@ -109,6 +109,32 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias_or_null, const void* dout, 
               const void* weight, int64_t B, int64_t T, int64_t C, int64_t OC, int dtype,
               cudaStream_t stream);
 
+/*
+ * mmbwd_run_sr -- mmbwd_run with stochastic rounding of the bf16 outputs.
+ *
+ * The encoder page's kernels round their fp32 sums to bf16 stochastically,
+ * with a deterministic per-element seed (wte_backward_kernel and
+ * wpe_backward_kernel); this is that option for the linear layer's outputs.
+ * Arguments, layout, ownership, workspace, errors and degenerate sizes are
+ * those of mmbwd_run; dtype must be MMBWD_BF16 (anything else:
+ * MMBWD_ERR_DTYPE, nothing enqueued).
+ *
+ * Each output value v = old + sum (fp32; dbias: the sum) is rounded to bf16
+ * as follows. Element e (row-major index) of output tensor k (0 dinp,
+ * 1 dweight, 2 dbias) takes the 16-bit threshold r = bits 16*(e mod 4) ..
+ * 16*(e mod 4)+15 of output number n = (k << 58) | (e / 4) of the splitmix64
+ * generator seeded with `seed` (z = seed + (n+1)*0x9E3779B97F4A7C15;
+ * z = (z ^ z>>30)*0xBF58476D1CE4E5B9; z = (z ^ z>>27)*0x94D049BB133111EB;
+ * z ^ z>>31); the result is the high 16 bits of (bits(v) + r), so the
+ * magnitude rounds up with probability (low 16 bits of v) / 65536 and the
+ * rounding is unbiased. Infinities and NaNs are truncated (NaNs stay NaN).
+ * The same seed and inputs give bitwise identical results; a new seed per
+ * step gives fresh rounding noise.
+ */
+int mmbwd_run_sr(void* dinp, void* dweight, void* dbias_or_null, const void* dout, const void* inp,
+                 const void* weight, int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, uint64_t seed,
+                 cudaStream_t stream);
+
 /* Bytes of workspace mmbwd_run needs for this shape on the current device
  * (0 when it needs none, and for invalid arguments). The work split depends
  * on the device's SM count, which this queries (152, a full GB300, when no

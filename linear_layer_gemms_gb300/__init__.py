@@ -42,6 +42,7 @@ _vp, _i64, _ci, _u64, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctyp
                              ctypes.c_size_t)
 SIGNATURES = {
     "mmbwd_run": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
+    "mmbwd_run_sr": ([_vp] * 6 + [_i64] * 4 + [_ci, _u64, _vp], _ci),
     "mmbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
     "mmbwd_release": ([], _ci),
     "mmbwd_strerror": ([_ci], ctypes.c_char_p),
@@ -109,6 +110,15 @@ def mmbwd_run(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, O
     """Enqueue one backward pass; returns the C status code (0 = OK)."""
     return load().mmbwd_run(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp),
                             _ptr(weight), B, T, C, OC, dtype, _stream(stream))
+
+
+def mmbwd_run_sr(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, OC: int, dtype: int,
+                 seed: int, stream=None) -> int:
+    """mmbwd_run with the bf16 outputs rounded stochastically (unbiased; the
+    threshold of each element comes from the splitmix64 generator seeded with
+    ``seed``, so the same seed repeats the same bits). bf16 only."""
+    return load().mmbwd_run_sr(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dout), _ptr(inp),
+                               _ptr(weight), B, T, C, OC, dtype, seed, _stream(stream))
 
 
 def mmbwd_run_static_scratch(dinp, dweight, dbias, dout, inp, weight, B: int, T: int, C: int, OC: int,

@@ -289,8 +289,13 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     return m;
 }
 
-int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
-              int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream) {
+namespace {
+
+// mmbwd_run and mmbwd_run_sr: `sr` selects stochastic rounding of the bf16
+// outputs with `seed` (sr.cuh).
+int run_backward(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+                 int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, bool sr, uint64_t seed,
+                 cudaStream_t stream) {
     Shape s;
     int rc = check_shape(B, T, C, OC, dtype, &s);
     if (rc != MMBWD_OK) return rc;
@@ -332,7 +337,7 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     if (C == 0) {
-        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, stream);
+        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, sr, seed, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
 
@@ -354,8 +359,21 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
     const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads);
     rc = ensure_workspace(*d, plan.ws_bytes(), stream);
     if (rc != MMBWD_OK) return rc;
-    e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream);
+    e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream, sr, seed);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+}  // namespace
+
+int mmbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+              int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream) {
+    return run_backward(dinp, dweight, dbias, dout, inp, weight, B, T, C, OC, dtype, false, 0, stream);
+}
+
+int mmbwd_run_sr(void* dinp, void* dweight, void* dbias, const void* dout, const void* inp, const void* weight,
+                 int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, uint64_t seed, cudaStream_t stream) {
+    if (dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    return run_backward(dinp, dweight, dbias, dout, inp, weight, B, T, C, OC, dtype, true, seed, stream);
 }
 
 int mmbwd_release(void) {
@@ -675,7 +693,7 @@ extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, 
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     if (C == 0) {
-        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, stream);
+        if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, false, 0, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     if (dtype == MMBWD_F32) {  // the fp32 path uses no scratch at all

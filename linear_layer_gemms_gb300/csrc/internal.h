@@ -96,6 +96,8 @@ struct TcParams {
     float* partials;       // [dw half tile][split][BM][dw_bn]; half tile = 128-row tile x column tile
     float* bias_partials;  // [dw 128-row tile][split][BM]
     unsigned long long timeout_ns;
+    int sr;                         // stochastic rounding of the bf16 outputs (backward)
+    unsigned long long sr_seed;
 };
 
 // Plans (pure functions of the shape and the number of co-resident CTAs,
@@ -119,10 +121,11 @@ cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, co
 
 // Launch the tensor-core kernel (and, with split dweight, the fixed-order
 // split reduction after it on the same stream). `ws` must hold plan.ws_bytes()
-// bytes. Returns a cudaError_t.
+// bytes. `sr`: stochastic rounding of the outputs with `sr_seed` (sr.cuh).
+// Returns a cudaError_t.
 cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC,
-                      void* ws, cudaStream_t stream);
+                      void* ws, cudaStream_t stream, bool sr = false, uint64_t sr_seed = 0);
 
 size_t tc_smem_bytes();
 
@@ -153,7 +156,7 @@ cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t 
                              cudaStream_t stream);
 
 // dbias = column sums of dout (used when C == 0, where no GEMM tile exists).
-cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype,
+cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype, bool sr, uint64_t sr_seed,
                           cudaStream_t stream);
 
 // Driver entry point for tensor-map encoding (resolved through the runtime).

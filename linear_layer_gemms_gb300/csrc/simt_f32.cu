@@ -16,6 +16,7 @@
 // and overwrite dbias. No split of K, so each output has one writer.
 #include "../../include/mmbwd.h"
 #include "internal.h"
+#include "sr.cuh"
 
 #include <algorithm>
 
@@ -157,11 +158,18 @@ __global__ void __launch_bounds__(SIMT_THREADS, 2)
 
 // dbias[o] = sum over rows of dout[row, o], one thread per column, rows in order.
 template <typename T>
-__global__ void colsum_kernel(T* __restrict__ dbias, const T* __restrict__ dout, int64_t BT, int64_t OC) {
+__global__ void colsum_kernel(T* __restrict__ dbias, const T* __restrict__ dout, int64_t BT, int64_t OC, int sr,
+                              uint64_t sr_seed) {
     const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (o >= OC) return;
     float s = 0.f;
     for (int64_t r = 0; r < BT; ++r) s += static_cast<float>(dout[r * OC + o]);
+    if constexpr (sizeof(T) == 2) {
+        if (sr) {
+            dbias[o] = sr::round(s, sr_seed, sr::DBIAS, static_cast<uint64_t>(o));
+            return;
+        }
+    }
     dbias[o] = static_cast<T>(s);
 }
 
@@ -214,14 +222,17 @@ cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t 
     return cudaGetLastError();
 }
 
-cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype, cudaStream_t stream) {
+cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype, bool sr, uint64_t sr_seed,
+                          cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>((OC + 255) / 256);
     if (blocks == 0) return cudaSuccess;
     if (dtype == MMBWD_F32)
-        colsum_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<float*>(dbias), static_cast<const float*>(dout), BT, OC);
+        colsum_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<float*>(dbias), static_cast<const float*>(dout), BT, OC,
+                                                         0, 0);
     else
         colsum_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(dbias),
-                                                                 static_cast<const __nv_bfloat16*>(dout), BT, OC);
+                                                                 static_cast<const __nv_bfloat16*>(dout), BT, OC,
+                                                                 sr ? 1 : 0, sr_seed);
     return cudaGetLastError();
 }
 

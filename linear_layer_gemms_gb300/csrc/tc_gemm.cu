@@ -50,6 +50,7 @@
 #include "../../include/mmbwd.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "sr.cuh"
 
 #include <algorithm>
 #include <cstdio>
@@ -211,13 +212,34 @@ __device__ __forceinline__ uint4 add_round8(uint4 old, const float (&s)[8]) {
     return r;
 }
 
+// Two elements (old bf16 pair) + (a, b), stochastically rounded (sr.cuh) with
+// the 16-bit thresholds in the low and high halves of r2. Branch-free: an
+// infinity plus any threshold stays an infinity after the low half is
+// dropped, and a NaN takes threshold 0 (it is truncated, as sr.cuh states).
+__device__ __forceinline__ uint32_t add_sr_pair(uint32_t old2, float a, float b, uint32_t r2) {
+    const float x0 = bf_lo(old2) + a, x1 = bf_hi(old2) + b;
+    const uint32_t r0 = (x0 == x0) ? (r2 & 0xFFFFu) : 0u, r1 = (x1 == x1) ? (r2 >> 16) : 0u;
+    return __byte_perm(__float_as_uint(x0) + r0, __float_as_uint(x1) + r1, 0x7632);
+}
+
+// (old bf16 x 8) + s, stochastically rounded; w0 and w1 are the generator
+// words of elements e0..e0+3 and e0+4..e0+7 (e0 a multiple of 4).
+__device__ __forceinline__ uint4 add_sr8(uint4 old, const float (&s)[8], uint64_t w0, uint64_t w1) {
+    return make_uint4(add_sr_pair(old.x, s[0], s[1], static_cast<uint32_t>(w0)),
+                      add_sr_pair(old.y, s[2], s[3], static_cast<uint32_t>(w0 >> 32)),
+                      add_sr_pair(old.z, s[4], s[5], static_cast<uint32_t>(w1)),
+                      add_sr_pair(old.w, s[6], s[7], static_cast<uint32_t>(w1 >> 32)));
+}
+
 // MODE 0: the backward (dinp and dweight items). MODE 1: the forward
 // (dinp-type items with a K-major B and an overwrite epilogue). MODE 2: one
 // fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves, both
 // operands K-major: each operand arrives as a high part (its tf32 value) and
 // a low part (the exact remainder), and each K step issues three tf32 MMAs,
 // hi.hi + hi.lo + lo.hi, into one fp32 accumulator; fp32 read-modify-write
-// epilogue. Three instantiations, so that none pays for the others' branches.
+// epilogue. MODE 3: the backward with stochastic rounding of the bf16 outputs
+// (seeded; sr.cuh). Four instantiations, so that none pays for the
+// others' branches.
 template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_mmbwd_kernel(const __grid_constant__ CUtensorMap tm_dout_k,   // dout, A of dinp (K-major)
@@ -227,8 +249,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_dinp_out, // dinp, for L2 prefetch of old values
                     const __grid_constant__ CUtensorMap tm_dw_out,   // dweight, likewise
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
-    constexpr bool FWD = MODE != 0;  // dinp-type items only, K-major B
-    constexpr bool X3 = MODE == 2;   // fp32 from three tf32 products
+    constexpr bool FWD = MODE == 1 || MODE == 2;  // dinp-type items only, K-major B
+    constexpr bool X3 = MODE == 2;                // fp32 from three tf32 products
+    constexpr bool SR = MODE == 3;                // stochastic rounding of the outputs
     // MODE 2 stages hold A hi | A lo | B hi | B lo (twice the bytes, half the
     // stages: the same shared memory) and 32 fp32 of K per k-block (128 bytes).
     constexpr int STAGES = X3 ? TC_STAGES / 2 : TC_STAGES;
@@ -658,7 +681,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         uint4 base8 = oldw[c][i];  // zero for the forward: out = acc (+ bias)
                         if (FWD && p.fwd_bias)
                             base8 = *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg);
-                        *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(base8, s8);
+                        if constexpr (SR) {
+                            const uint64_t e0 = static_cast<uint64_t>(qrow0 + 8 * i + r8) * n_extent + col0 + c * 32 + cg;
+                            const uint64_t t = it.is_dw ? sr::DWEIGHT : sr::DINP;
+                            *reinterpret_cast<uint4*>(drow[i] + c * 32) =
+                                add_sr8(base8, s8, sr::word(p.sr_seed, t, e0), sr::word(p.sr_seed, t, e0 + 4));
+                        } else {
+                            *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(base8, s8);
+                        }
                     }
                 }
                 __syncwarp();
@@ -667,8 +697,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int64_t brow = static_cast<int64_t>(m_tile) * TC_BM + rit;
                 if (split_mode)
                     p.bias_partials[(static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + rit] = bias_val;
-                else if (brow < p.OC)
-                    p.dbias[brow] = __float2bfloat16_rn(bias_val);
+                else if (brow < p.OC) {
+                    if constexpr (SR)
+                        p.dbias[brow] = sr::round(bias_val, p.sr_seed, sr::DBIAS, brow);
+                    else
+                        p.dbias[brow] = __float2bfloat16_rn(bias_val);
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -699,7 +733,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // Split reduction: dweight = dweight + (partial_0 + partial_1 + ... + partial_{S-1})
-// with the partials summed in split order and one rounding to bf16, and
+// with the partials summed in split order and one rounding to bf16 (to nearest,
+// or stochastic as in the kernel's MODE 3), and
 // dbias = bias_partial_0 + ... + bias_partial_{S-1} in the same order. One
 // thread per 8-column vector of dweight; all loads are independent, so the
 // pass runs at memory speed with the partials still in L2.
@@ -726,7 +761,12 @@ __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) 
             for (int e = 0; e < 8; ++e) s8[e] = (sp == 0) ? f[e] : s8[e] + f[e];
         }
         uint4* dst = reinterpret_cast<uint4*>(p.dweight + row * p.C + col);
-        *dst = add_round8(*dst, s8);
+        if (p.sr) {
+            const uint64_t e0 = static_cast<uint64_t>(row * p.C + col);
+            *dst = add_sr8(*dst, s8, sr::word(p.sr_seed, sr::DWEIGHT, e0), sr::word(p.sr_seed, sr::DWEIGHT, e0 + 4));
+        } else {
+            *dst = add_round8(*dst, s8);
+        }
     }
     if (p.dbias) {
         for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < p.OC; o += stride) {
@@ -736,7 +776,7 @@ __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) 
                 const float f = __ldcg(p.bias_partials + (static_cast<size_t>(m_tile) * p.splits + sp) * TC_BM + rl);
                 b = (sp == 0) ? f : b + f;
             }
-            p.dbias[o] = __float2bfloat16_rn(b);
+            p.dbias[o] = p.sr ? sr::round(b, p.sr_seed, sr::DBIAS, o) : __float2bfloat16_rn(b);
         }
     }
 }
@@ -1046,6 +1086,8 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
                 e = cudaFuncSetAttribute(tc_mmbwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(tc_mmbwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(tc_mmbwd_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) g_attr_set[dev] = true;
         }
@@ -1104,6 +1146,9 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     else if (mode == 1)
         e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
+    else if (mode == 3)
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+                               plan.sched);
     else
         e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
                                plan.sched);
@@ -1121,7 +1166,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
 
 cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC, void* ws,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool sr, uint64_t sr_seed) {
     const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
     const MapSpec specs[6] = {
         {dout, oc, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},        // dout, K-major A of dinp
@@ -1142,7 +1187,9 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.partials = plan.splits > 1 ? reinterpret_cast<float*>(w) : nullptr;
     p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
-    return launch_common(plan, specs, p, 0, stream);
+    p.sr = sr ? 1 : 0;
+    p.sr_seed = sr_seed;
+    return launch_common(plan, specs, p, sr ? 3 : 0, stream);
 }
 
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight, const void* bias,

@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product library never imports it.
 ``mmbwd_oracle.c`` (the linear layer), ``layernorm_oracle.c`` (the LayerNorm
-backward) and ``encoder_oracle.c`` (the encoder backward) state what is
-computed and which readings of the pages they take.
+backward), ``encoder_oracle.c`` (the encoder backward) and ``sr_oracle.c``
+(the stochastic-rounding option of the bf16 outputs) state what is computed
+and which readings of the pages they take.
 
 Builds (gcc, -O2, -ffp-contract=off, no -ffast-math):
   * ``st``  - single-threaded
@@ -21,14 +22,16 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = tuple(os.path.join(_HERE, f) for f in ("mmbwd_oracle.c", "layernorm_oracle.c", "encoder_oracle.c"))
+_SRCS = tuple(os.path.join(_HERE, f)
+              for f in ("mmbwd_oracle.c", "layernorm_oracle.c", "encoder_oracle.c", "sr_oracle.c"))
 _BUILD = os.path.join(_HERE, "_build")
 _lock = threading.Lock()
 _libs: dict = {}
 
 F32, BF16, F64 = 0, 1, 2
 DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
-MUTANTS = tuple(range(1, 19))
+MUTANTS = tuple(range(1, 23))
+SR_DINP, SR_DWEIGHT, SR_DBIAS = 0, 1, 2
 
 
 def lib_path(variant: str) -> str:
@@ -69,6 +72,13 @@ class Oracle:
         lib.oracle_layernorm_dinp_rows.argtypes = [vp, vp, i64] + [vp] * 6 + [ci, i64, i64, ci]
         lib.oracle_layernorm_params.argtypes = [vp] * 8 + [ci, i64, i64, ci]
         lib.oracle_encoder_backward.argtypes = [vp] * 6 + [i64] * 4 + [ci]
+        u64 = ctypes.c_uint64
+        lib.oracle_splitmix64.argtypes = [u64, u64]
+        lib.oracle_splitmix64.restype = u64
+        lib.oracle_sr_draw.argtypes = [u64, ci, i64]
+        lib.oracle_sr_draw.restype = ctypes.c_uint32
+        lib.oracle_sr_round.argtypes = [vp, vp, i64, u64, ci, i64]
+        lib.oracle_sr_round.restype = None
         for f in (lib.oracle_dinp_rows, lib.oracle_dweight_rows, lib.oracle_matmul_backward,
                   lib.oracle_forward_rows, lib.oracle_threads, lib.oracle_mutant,
                   lib.oracle_layernorm_forward, lib.oracle_layernorm_dinp_rows,
@@ -232,6 +242,30 @@ class Oracle:
             raise ValueError("token id outside [0, V)")
         assert rc == 0
         return dwte, dwpe
+
+
+    # ------------------------------------------------------------------ stochastic rounding
+    def splitmix64(self, seed: int, n: int) -> int:
+        """The n-th output (from 0) of splitmix64 seeded with ``seed``."""
+        return int(self._lib.oracle_splitmix64(seed, n))
+
+    def sr_draw(self, seed: int, tensor: int, e: int) -> int:
+        return int(self._lib.oracle_sr_draw(seed, tensor, e))
+
+    def sr_round(self, values, seed: int, tensor: int, e0: int = 0):
+        """bf16 bit patterns (uint16, same shape) of float64 ``values`` rounded
+        stochastically; element i of the flattened array has index e0 + i."""
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, dtype=np.uint16)
+        self._lib.oracle_sr_round(v.ctypes.data, out.ctypes.data, v.size, seed, tensor, e0)
+        return out
+
+    def matmul_backward_sr(self, dout, inp, weight, seed: int, dinp_init=None, dweight_init=None, bias=True):
+        """mmbwd_run_sr's outputs (bf16 bit patterns): the exact results of
+        matmul_backward, each rounded stochastically as a float."""
+        dinp, dweight, dbias = self.matmul_backward(dout, inp, weight, "bf16", dinp_init, dweight_init, bias)
+        return (self.sr_round(dinp, seed, SR_DINP), self.sr_round(dweight, seed, SR_DWEIGHT),
+                None if dbias is None else self.sr_round(dbias, seed, SR_DBIAS))
 
 
 def get(variant: str = "st") -> Oracle:

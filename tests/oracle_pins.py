@@ -314,3 +314,6 @@ ALL_PINS = ALL_PINS + LN_PINS
 from oracle_pins_enc import ENC_PINS  # noqa: E402
 
 ALL_PINS = ALL_PINS + ENC_PINS
+from oracle_pins_sr import SR_PINS  # noqa: E402
+
+ALL_PINS = ALL_PINS + SR_PINS

@@ -204,6 +204,18 @@ def test_layernorm_rejects_bad_arguments():
     assert mm.LNBWD_MAX_C == {mm.F32: 2048, mm.BF16: 4096}
 
 
+def test_sr_rejects_fp32_and_bad_arguments():
+    f = lambda **kw: mm.mmbwd_run_sr(**{**dict(dinp=A, dweight=2 * A, dbias=3 * A, dout=4 * A, inp=5 * A,  # noqa: E731
+                                                weight=6 * A, B=2, T=8, C=64, OC=64, dtype=mm.BF16, seed=1,
+                                                stream=0), **kw})
+    assert f(dtype=mm.F32) == mm.ERR_DTYPE          # stochastic rounding is for bf16 outputs
+    assert f(dtype=7) == mm.ERR_DTYPE
+    assert f(T=-1) == mm.ERR_SHAPE
+    assert f(dout=None) == mm.ERR_NULL
+    assert f(dinp=A + 8) == mm.ERR_ALIGN
+    assert f(dweight=4 * A) == mm.ERR_ALIAS
+
+
 def test_encoder_rejects_bad_arguments():
     f = lambda **kw: mm.encbwd_run(**{**dict(dwte=A, dwpe=2 * A, dout=3 * A, inp=4 * A, B=2, T=8, C=64,  # noqa: E731
                                              V=100, dtype=mm.BF16, stream=0), **kw})
