@@ -13,7 +13,8 @@
  * of up to 32, and the chunks of a token added in order; dwpe is summed in
  * batch order. No atomics on the data: repeated calls give bitwise identical
  * results. Each output element is rounded
- * once (round-to-nearest-even for bf16) after its old value is added.
+ * once (round-to-nearest-even for bf16; stochastically with encbwd_run_sr)
+ * after its old value is added.
  *
  * Element types: MMBWD_F32 or MMBWD_BF16 (mmbwd.h) for dwte, dwpe and dout;
  * inp is int32.
@@ -61,6 +62,21 @@ extern "C" {
  */
 int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                int64_t V, int dtype, cudaStream_t stream);
+
+/*
+ * encbwd_run_sr -- encbwd_run with the bf16 outputs rounded stochastically, as
+ * the page's wte and wpe kernels round theirs (a deterministic seed per
+ * element). Everything else as encbwd_run; dtype must be MMBWD_BF16
+ * (otherwise MMBWD_ERR_DTYPE, nothing enqueued).
+ *
+ * The rule is mmbwd_run_sr's (mmbwd.h): element e (row-major index) of dwte
+ * (tensor 3) or dwpe (tensor 4) takes the 16-bit threshold r = bits
+ * 16*(e mod 4) .. 16*(e mod 4)+15 of splitmix64 output number
+ * (tensor << 58) | (e / 4) from `seed`, and the bf16 result is the high half
+ * of (bits(old + sum) + r). The same seed repeats the same bits.
+ */
+int encbwd_run_sr(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+                  int64_t V, int dtype, uint64_t seed, cudaStream_t stream);
 
 /* Workspace bytes encbwd_run needs for this problem (0 for invalid arguments). */
 size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype);

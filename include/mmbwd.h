@@ -121,7 +121,8 @@ int mmbwd_run(void* dinp, void* dweight, void* dbias_or_null, const void* dout, 
  *
  * Each output value v = old + sum (fp32; dbias: the sum) is rounded to bf16
  * as follows. Element e (row-major index) of output tensor k (0 dinp,
- * 1 dweight, 2 dbias) takes the 16-bit threshold r = bits 16*(e mod 4) ..
+ * 1 dweight, 2 dbias; the encoder's dwte and dwpe are 3 and 4) takes the
+ * 16-bit threshold r = bits 16*(e mod 4) ..
  * 16*(e mod 4)+15 of output number n = (k << 58) | (e / 4) of the splitmix64
  * generator seeded with `seed` (z = seed + (n+1)*0x9E3779B97F4A7C15;
  * z = (z ^ z>>30)*0xBF58476D1CE4E5B9; z = (z ^ z>>27)*0x94D049BB133111EB;

@@ -56,6 +56,7 @@ SIGNATURES = {
     "mmbwd_forward_path": ([_i64] * 4 + [_ci], _ci),
     "lnbwd_run": ([_vp] * 8 + [_i64] * 3 + [_ci, _vp], _ci),
     "encbwd_run": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
+    "encbwd_run_sr": ([_vp] * 4 + [_i64] * 4 + [_ci, _u64, _vp], _ci),
     "encbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
     "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
@@ -152,6 +153,14 @@ def encbwd_run(dwte, dwpe, dout, inp, B: int, T: int, C: int, V: int, dtype: int
     """Enqueue the encoder backward (dwte and dwpe +=); inp holds int32 token
     ids; returns the C status code."""
     return load().encbwd_run(_ptr(dwte), _ptr(dwpe), _ptr(dout), _ptr(inp), B, T, C, V, dtype, _stream(stream))
+
+
+def encbwd_run_sr(dwte, dwpe, dout, inp, B: int, T: int, C: int, V: int, dtype: int, seed: int,
+                  stream=None) -> int:
+    """encbwd_run with the bf16 outputs rounded stochastically (seeded, as
+    mmbwd_run_sr); bf16 only."""
+    return load().encbwd_run_sr(_ptr(dwte), _ptr(dwpe), _ptr(dout), _ptr(inp), B, T, C, V, dtype, seed,
+                                _stream(stream))
 
 
 def encbwd_workspace_bytes(B: int, T: int, C: int, V: int, dtype: int) -> int:

@@ -502,8 +502,10 @@ size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dt
     return enc_workspace_bytes(BT, C, V);
 }
 
-int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
-               int64_t V, int dtype, cudaStream_t stream) {
+namespace {
+
+int run_encoder(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+                int64_t V, int dtype, bool sr, uint64_t seed, cudaStream_t stream) {
     int64_t BT = 0;
     int rc = enc_check(B, T, C, V, dtype, &BT);
     if (rc != MMBWD_OK) return rc;
@@ -528,8 +530,21 @@ int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int
     if (BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
     rc = ensure_workspace(*d, enc_workspace_bytes(BT, C, V), stream);
     if (rc != MMBWD_OK) return rc;
-    const cudaError_t e = enc_launch(dwte, dwpe, dout, inp, B, T, C, V, dtype, d->ws, d->num_sms, stream);
+    const cudaError_t e = enc_launch(dwte, dwpe, dout, inp, B, T, C, V, dtype, d->ws, d->num_sms, stream, sr, seed);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+}  // namespace
+
+int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+               int64_t V, int dtype, cudaStream_t stream) {
+    return run_encoder(dwte, dwpe, dout, inp, B, T, C, V, dtype, false, 0, stream);
+}
+
+int encbwd_run_sr(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+                  int64_t V, int dtype, uint64_t seed, cudaStream_t stream) {
+    if (dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    return run_encoder(dwte, dwpe, dout, inp, B, T, C, V, dtype, true, seed, stream);
 }
 
 // ---------------------------------------------------------------------------

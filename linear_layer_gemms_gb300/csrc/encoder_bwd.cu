@@ -33,6 +33,7 @@
 #include "../../include/encoder_backward.h"
 #include "../../include/mmbwd.h"
 #include "internal.h"
+#include "sr.cuh"
 
 namespace mmbwd {
 
@@ -106,6 +107,7 @@ struct EncVec4<float> {
     __device__ static void st(float* p, V v) { *reinterpret_cast<uint4*>(p) = v; }
     __device__ static void add(const V& v, float (&a)[4]) { EncElem<float>::add(v, a); }
     __device__ static V add_round(const V& old, const float (&s)[4]) { return EncElem<float>::add_round(old, s); }
+    __device__ static V add_sr(const V& old, const float (&s)[4], uint64_t) { return add_round(old, s); }  // fp32: exact
 };
 template <>
 struct EncVec4<__nv_bfloat16> {
@@ -121,6 +123,15 @@ struct EncVec4<__nv_bfloat16> {
     __device__ static V add_round(const V& old, const float (&s)[4]) {
         return make_uint2(E::rp(old.x, s[0], s[1]), E::rp(old.y, s[2], s[3]));
     }
+    // Stochastic rounding (sr.cuh): w is the generator word of these four
+    // elements (their first index is a multiple of 4).
+    __device__ static V add_sr(const V& old, const float (&s)[4], uint64_t w) {
+        const float x[4] = {E::lo(old.x) + s[0], E::hi(old.x) + s[1], E::lo(old.y) + s[2], E::hi(old.y) + s[3]};
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = sr::round_bits(x[k], static_cast<uint32_t>(w >> (16 * k)) & 0xFFFFu);
+        return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    }
 };
 
 struct EncTables {
@@ -130,6 +141,8 @@ struct EncTables {
     int* win_tail;       // [windows] last slot of the run holding the window's last slot
     unsigned* arrivals;  // [windows][G] windows done for the token whose run starts in the window
     float* partials;     // [windows][2][C] fp32 sums of a window's first / last run
+    int sr;              // bf16 outputs rounded stochastically (sr.cuh) with `seed`
+    unsigned long long seed;
 };
 
 // Exclusive scan of one value per thread over the block (1024 threads, in
@@ -165,7 +178,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 // (four loads in flight), added to the old value, rounded once.
 template <typename T>
 __device__ void enc_wpe_part(T* __restrict__ dwpe, const T* __restrict__ dout, int B, int T_, int C, int64_t v0,
-                             int64_t nthreads) {
+                             int64_t nthreads, int sr, uint64_t seed) {
     using E = EncElem<T>;
     constexpr int N = E::N;
     const int64_t nv = static_cast<int64_t>(T_) * C / N;
@@ -185,6 +198,17 @@ __device__ void enc_wpe_part(T* __restrict__ dwpe, const T* __restrict__ dout, i
         }
         for (; b < B; ++b) E::add(__ldcs(reinterpret_cast<const uint4*>(dout + b * row + off)), acc);
         uint4* dst = reinterpret_cast<uint4*>(dwpe + off);
+        if constexpr (sizeof(T) == 2) {
+            if (sr) {  // stochastic rounding (sr.cuh): two generator words per 8 elements
+                const uint4 o = *dst;
+                const uint64_t w0 = sr::word(seed, sr::DWPE, off), w1 = sr::word(seed, sr::DWPE, off + 4);
+                const float lo4[4] = {acc[0], acc[1], acc[2], acc[3]}, hi4[4] = {acc[4], acc[5], acc[6], acc[7]};
+                const uint2 a = EncVec4<T>::add_sr(make_uint2(o.x, o.y), lo4, w0);
+                const uint2 b = EncVec4<T>::add_sr(make_uint2(o.z, o.w), hi4, w1);
+                *dst = make_uint4(a.x, a.y, b.x, b.y);
+                continue;
+            }
+        }
         *dst = E::add_round(*dst, acc);
     }
 }
@@ -249,7 +273,7 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     const int tid = static_cast<int>(threadIdx.x);
     if (blockIdx.x > 0) {
         enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(blockIdx.x - 1) * ENC_SORT_THREADS + tid,
-                        static_cast<int64_t>(gridDim.x - 1) * ENC_SORT_THREADS);
+                        static_cast<int64_t>(gridDim.x - 1) * ENC_SORT_THREADS, tb.sr, tb.seed);
         return;
     }
     constexpr int NP = KPL * ENC_SORT_THREADS;
@@ -414,7 +438,8 @@ __device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, 
         for (int u = 0; u < PB; ++u)
             if (k + u < nw) sum[0] += pv[u].x, sum[1] += pv[u].y, sum[2] += pv[u].z, sum[3] += pv[u].w;
     }
-    EV::st(dwte + static_cast<int64_t>(tok) * C + c, EV::add_round(old, sum));
+    const int64_t e = static_cast<int64_t>(tok) * C + c;
+    EV::st(dwte + e, tb.sr ? EV::add_sr(old, sum, sr::word(tb.seed, sr::DWTE, e)) : EV::add_round(old, sum));
 }
 
 // One warp per (window of 32 sorted slots, group of 128 channels); lane l
@@ -501,7 +526,8 @@ __global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte
                             for (int e = 0; e < 4; ++e) tacc[e] = acc[e];
                             told = o[u];
                         } else if (active) {
-                            EV::st(dwte + t * C + c, EV::add_round(o[u], acc));
+                            EV::st(dwte + t * C + c, tb.sr ? EV::add_sr(o[u], acc, sr::word(tb.seed, sr::DWTE, t * C + c))
+                                                           : EV::add_round(o[u], acc));
                         }
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[e] = 0.f;
@@ -560,7 +586,7 @@ size_t enc_workspace_bytes(int64_t BT, int64_t C, int64_t V) {
 }
 
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
-                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream) {
+                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr, uint64_t seed) {
     const int BT = static_cast<int>(B * T);
     const int nwin = (BT + ENC_WIN - 1) / ENC_WIN;
     const int N = dtype == MMBWD_F32 ? 4 : 8;  // elements per 16-byte vector (dwpe)
@@ -578,6 +604,8 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
     tb.win_tail = reinterpret_cast<int*>(take(static_cast<size_t>(nwin) * 4));
     tb.arrivals = reinterpret_cast<unsigned*>(take(static_cast<size_t>(nwin) * enc_groups(C, 4) * 4));
     tb.partials = reinterpret_cast<float*>(take(static_cast<size_t>(nwin) * 2 * C * 4));
+    tb.sr = sr ? 1 : 0;
+    tb.seed = seed;
     int kpl = 1;
     while (kpl * ENC_SORT_THREADS < BT) kpl <<= 1;
     // sort on the smallest b with 2^b > V: the padding's digits (all ones) then

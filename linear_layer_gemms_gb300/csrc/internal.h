@@ -183,7 +183,8 @@ cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight,
 
 size_t enc_workspace_bytes(int64_t BT, int64_t C, int64_t V);
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
-                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream);
+                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr = false,
+                       uint64_t seed = 0);
 cudaError_t enc_read_status(int* code, int* info3, bool reset);
 
 // ---------------------------------------------------------------- LayerNorm backward

@@ -31,7 +31,7 @@ _libs: dict = {}
 F32, BF16, F64 = 0, 1, 2
 DTYPES = {"f32": F32, "bf16": BF16, "f64": F64}
 MUTANTS = tuple(range(1, 23))
-SR_DINP, SR_DWEIGHT, SR_DBIAS = 0, 1, 2
+SR_DINP, SR_DWEIGHT, SR_DBIAS, SR_DWTE, SR_DWPE = 0, 1, 2, 3, 4
 
 
 def lib_path(variant: str) -> str:
@@ -266,6 +266,12 @@ class Oracle:
         dinp, dweight, dbias = self.matmul_backward(dout, inp, weight, "bf16", dinp_init, dweight_init, bias)
         return (self.sr_round(dinp, seed, SR_DINP), self.sr_round(dweight, seed, SR_DWEIGHT),
                 None if dbias is None else self.sr_round(dbias, seed, SR_DBIAS))
+
+    def encoder_backward_sr(self, dout, inp, B: int, T: int, V: int, seed: int, dwte_init=None, dwpe_init=None):
+        """encbwd_run_sr's outputs (bf16 bit patterns): the exact results of
+        encoder_backward, each rounded stochastically as a float."""
+        dwte, dwpe = self.encoder_backward(dout, inp, B, T, V, "bf16", dwte_init, dwpe_init)
+        return self.sr_round(dwte, seed, SR_DWTE), self.sr_round(dwpe, seed, SR_DWPE)
 
 
 def get(variant: str = "st") -> Oracle:

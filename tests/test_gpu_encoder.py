@@ -2,7 +2,9 @@
 element by element on every dwte and dwpe element: ragged position counts
 (not powers of two), a token repeated far beyond one chunk, the largest sort
 (B*T = 16384), the GPT-2 small workload with Zipf-distributed tokens,
-run-to-run bitwise determinism, a token id out of range, empty problems."""
+run-to-run bitwise determinism, a token id out of range, empty problems; with
+stochastic rounding (encbwd_run_sr), bit-exact against the oracle on integer
+problems (fp32 sums exact, results wider than bf16) and repeatable per seed."""
 import numpy as np
 import pytest
 
@@ -143,3 +145,37 @@ def test_encoder_bad_tokens_among_last_id():
     fixed["inp"] = x["inp"].copy()
     fixed["inp"][bad] = 0
     check(fixed, g, B, T, V, dtype)
+
+
+def test_encoder_sr_integer_exact_and_repeatable():
+    import torch
+
+    B, T, C, V = 4, 500, 64, 40
+    rng = np.random.default_rng(17)
+
+    def ints(shape, lim, scale=1):
+        v = (rng.integers(-lim, lim + 1, size=shape) * scale).astype(np.float32)  # exact in bf16: |v / scale| < 256
+        return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+    # initial values multiples of 8 up to 1600, so that old + sum needs more
+    # than bf16's eight significant bits; the last 5 ids are unused (rows kept)
+    x = {"dout": ints((B * T, C), 3), "dwte": ints((V, C), 200, 8), "dwpe": ints((T, C), 200, 8),
+         "inp": synth.zipf_tokens(B * T, V - 5, 1.1, 3, 0)}
+    want = oracle.get("st").encoder_backward_sr(x["dout"], x["inp"], B, T, V, 99, x["dwte"], x["dwpe"])
+    outs = []
+    for seed in (99, 99, 100):
+        g = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+        gi = torch.from_numpy(x["inp"]).to("cuda:0")
+        assert mm.encbwd_run_sr(g["dwte"], g["dwpe"], g["dout"], gi, B, T, C, V, mm.BF16, seed) == mm.OK
+        torch.cuda.synchronize()
+        outs.append([g[k].view(torch.int16).cpu().numpy().view(np.uint16) for k in ("dwte", "dwpe")])
+    assert np.array_equal(outs[0][0], want[0]) and np.array_equal(outs[0][1], want[1])
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    exact = synth.bf16_bits_to_f64(x["dwpe"]) + synth.bf16_bits_to_f64(x["dout"]).reshape(B, T, C).sum(axis=0)
+    trunc = ((exact.astype(np.float32).view(np.uint32) >> 16) << 16).view(np.float32).astype(np.float64)
+    rounded = trunc != exact  # sums that are not bf16 values
+    assert rounded.mean() > 0.5  # most sums are not bf16 values
+    assert np.mean(outs[0][1][rounded] != outs[2][1][rounded]) > 0.2  # another seed, other roundings
+    got = synth.bf16_bits_to_f64(outs[0][1])
+    assert np.any(got > exact) and np.any(got < exact)  # rounded both ways
+    assert mm.encbwd_run_sr(None, None, None, None, B, T, C, V, mm.F32, 1) == mm.ERR_DTYPE
