@@ -618,16 +618,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 drow[i] = D + (rok[i] ? row : 0) * n_extent + col0 + cg;
                 drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
-            // All old output values of this tile, loaded before waiting for the
-            // accumulator (the producer has prefetched them into L2).
+            // All old output values of this tile (the backward; the producer has
+            // prefetched them into L2), or the bias columns of the tile (the bf16
+            // forward, in oldw[c][0]), loaded before waiting for the accumulator.
             uint4 oldw[TC_BN / 32][4];
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    oldw[c][i] = (!X3 && !split_mode && !FWD && c < nchunks && rok[i] && c * 32 + cg < ncols)
-                                     ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (FWD && !X3)
+                        oldw[c][i] = (i == 0 && p.fwd_bias && c < nchunks && c * 32 + cg < ncols)
+                                         ? *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                    else
+                        oldw[c][i] = (!X3 && !split_mode && c < nchunks && rok[i] && c * 32 + cg < ncols)
+                                         ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                }
 
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
@@ -678,9 +685,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                     } else if (rok[i] && c * 32 + cg < ncols) {
                         float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-                        uint4 base8 = oldw[c][i];  // zero for the forward: out = acc (+ bias)
-                        if (FWD && p.fwd_bias)
-                            base8 = *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg);
+                        // backward: the old value; forward: the bias (zero without one)
+                        const uint4 base8 = FWD ? oldw[c][0] : oldw[c][i];
                         if constexpr (SR) {
                             const uint64_t e0 = static_cast<uint64_t>(qrow0 + 8 * i + r8) * n_extent + col0 + c * 32 + cg;
                             const uint64_t t = it.is_dw ? sr::DWEIGHT : sr::DINP;
