@@ -667,46 +667,73 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
 
 
 def run_e2e(torch, mm, wl, host, dev, stream, steps, barrier):
-    """Same steps through mmbwd_run with pinned host inputs: H2D of dout, inp,
-    weight and D2H of dinp, dweight, dbias every step, inside the timed region."""
+    """Same steps through mmbwd_run with pinned host inputs: every step copies
+    its dout, inp and weight in and its dinp, dweight and dbias out, inside the
+    timed region. Pipelined as a training loop would run it: a copy-in stream,
+    the compute stream and a copy-out stream, two device buffer sets used by
+    alternate steps, events ordering each buffer's copy-in, compute and
+    copy-out (step k's copy-in waits for step k-2's compute on the same set,
+    step k's compute for step k-2's copy-out)."""
     pin_in = [{k: torch.from_numpy(x[k]).pin_memory() for k in ("dout", "inp", "weight")} for x in host]
     pin_out = [{k: torch.from_numpy(x[k].copy()).pin_memory() for k in ("dinp", "dweight", "dbias")} for x in host]
-    d = [{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for x in host]
+    sets = [[{k: to_device_tensor(torch, v, dev) for k, v in x.items()} for x in host] for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for x in pin_in for v in x.values())
     d2h = sum(v.numel() * v.element_size() for x in pin_out for v in x.values())
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
+    ev = {(name, b): None for name in ("in", "comp", "out") for b in (0, 1)}
 
-    def step():
-        for layer, pi, po, t in zip(wl.layers, pin_in, pin_out, d):
-            for k in ("dout", "inp", "weight"):
-                t[k].view(torch.int16).copy_(pi[k].view(torch.int16), non_blocking=True)
+    def record(name, b, st):
+        e = torch.cuda.Event()
+        e.record(st)
+        ev[(name, b)] = e
+
+    def step(k):
+        b = k % 2
+        d = sets[b]
+        with torch.cuda.stream(s_in):
+            if ev[("comp", b)] is not None:
+                s_in.wait_event(ev[("comp", b)])
+            for pi, t in zip(pin_in, d):
+                for key in ("dout", "inp", "weight"):
+                    t[key].view(torch.int16).copy_(pi[key].view(torch.int16), non_blocking=True)
+            record("in", b, s_in)
+        stream.wait_event(ev[("in", b)])
+        if ev[("out", b)] is not None:
+            stream.wait_event(ev[("out", b)])
+        for layer, t in zip(wl.layers, d):
             rc = mm.mmbwd_run(t["dinp"].data_ptr(), t["dweight"].data_ptr(),
                               t["dbias"].data_ptr() if layer.bias else None, t["dout"].data_ptr(),
                               t["inp"].data_ptr(), t["weight"].data_ptr(), layer.B, layer.T, layer.C,
                               layer.OC, mm.BF16, sh)
             if rc != mm.OK:
                 raise RuntimeError(mm.strerror(rc))
-            for k in ("dinp", "dweight", "dbias"):
-                po[k].view(torch.int16).copy_(t[k].view(torch.int16), non_blocking=True)
+        record("comp", b, stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev[("comp", b)])
+            for po, t in zip(pin_out, d):
+                for key in ("dinp", "dweight", "dbias"):
+                    po[key].view(torch.int16).copy_(t[key].view(torch.int16), non_blocking=True)
+            record("out", b, s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+    for k in range(3):
+        step(k)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for _ in range(steps):
-            step()
-        b.record(stream)
+    a.record(s_in)  # before the first copy-in
+    for k in range(steps):
+        step(k)
+    s_in.wait_event(ev[("out", (steps - 1) % 2)])  # after the last copy-out
+    e_end.record(s_in)
     torch.cuda.synchronize()
     barrier()
-    s = a.elapsed_time(b) / 1e3
+    s = a.elapsed_time(e_end) / 1e3
     units, max_s = aggregate(wl.flops() * steps, s)
     return {"value": units / max_s / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": max_s / steps * 1e3}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": max_s / steps * 1e3,
+            "pipelined": "copy-in, compute and copy-out streams; two device buffer sets"}
 
 
 def run_case(args):
