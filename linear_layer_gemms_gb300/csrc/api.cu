@@ -499,7 +499,7 @@ int enc_check(int64_t B, int64_t T, int64_t C, int64_t V, int dtype, int64_t* BT
 size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype) {
     int64_t BT = 0;
     if (enc_check(B, T, C, V, dtype, &BT) != MMBWD_OK || BT == 0 || C == 0) return 0;
-    return enc_workspace_bytes(BT, C, V);
+    return enc_workspace_bytes(BT, C);
 }
 
 namespace {
@@ -528,7 +528,7 @@ int run_encoder(void* dwte, void* dwpe, const void* dout, const int32_t* inp, in
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
     if (BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
-    rc = ensure_workspace(*d, enc_workspace_bytes(BT, C, V), stream);
+    rc = ensure_workspace(*d, enc_workspace_bytes(BT, C), stream);
     if (rc != MMBWD_OK) return rc;
     const cudaError_t e = enc_launch(dwte, dwpe, dout, inp, B, T, C, V, dtype, d->ws, d->num_sms, stream, sr, seed);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;

@@ -578,9 +578,8 @@ const void* enc_sort_fn(int kpl) {
 
 // Workspace: meta, sorted keys, per-window tables, counters (four channels
 // per lane), partials.
-size_t enc_workspace_bytes(int64_t BT, int64_t C, int64_t V) {
+size_t enc_workspace_bytes(int64_t BT, int64_t C) {
     const size_t n = static_cast<size_t>(BT), nwin = (n + ENC_WIN - 1) / ENC_WIN;
-    (void)V;
     return a256(4 * 4) + a256(n * 4) + a256(nwin * 4) + a256(nwin * 4) +
            a256(nwin * static_cast<size_t>(enc_groups(C, 4)) * 4) + a256(nwin * 2 * static_cast<size_t>(C) * 4);
 }

@@ -181,7 +181,7 @@ cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight,
 
 // ---------------------------------------------------------------- encoder backward
 
-size_t enc_workspace_bytes(int64_t BT, int64_t C, int64_t V);
+size_t enc_workspace_bytes(int64_t BT, int64_t C);
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                        int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr = false,
                        uint64_t seed = 0);
