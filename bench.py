@@ -446,6 +446,9 @@ def run_gpu(args):
 OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32")
 ENC_CONFIGS = ("enc_gpt2_small", "enc_gpt2_small_f32")
+# the same workload in two calls: encbwd_prepare (timed on its own) ahead of
+# time, encbwd_run_planned (timed) on the backward's critical path
+ENC_PLANNED_CONFIGS = (("enc_gpt2_small_planned", "enc_gpt2_small"),)
 # each MLP layer alone, rounded to nearest (mmbwd_run) and stochastically
 # (mmbwd_run_sr, a new seed per call)
 LAYER_CONFIGS = (("mlp_fc", "mlp:0", False), ("mlp_fc_proj", "mlp:1", False),
@@ -660,6 +663,52 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
                      "l2": "rotating sets > L2" if n_sets * x["dout"].nbytes > L2_BYTES else "L2-resident"}
         del sets, calls
         torch.cuda.empty_cache()
+    for name, wname in ENC_PLANNED_CONFIGS:
+        if only is not None and name not in only:
+            continue
+        p = synth.ENC_WORKLOADS[wname]
+        x = synth.make_enc_inputs(p, seed=0)
+        distinct = int(np.unique(x["inp"]).size)
+        set_bytes = p.bytes(distinct)
+        n_sets = input_sets(x["dout"].nbytes)
+        dt = mm.BF16 if p.dtype == "bf16" else mm.F32
+        nplan = mm.encbwd_plan_bytes(p.B, p.T, p.C, p.V, dt)
+        sets = []
+        for _ in range(n_sets):
+            t = {k: to_device_tensor(torch, x[k], dev) for k in ("dout", "dwte", "dwpe")}
+            t["inp"] = torch.from_numpy(x["inp"]).to(dev)
+            t["plan"] = torch.empty(nplan, dtype=torch.uint8, device=dev)
+            sets.append(t)
+
+        def make_prep(t, p=p, dt=dt):
+            def prep():
+                rc = mm.encbwd_prepare(t["plan"].data_ptr(), nplan, t["inp"].data_ptr(), p.B, p.T, p.C, p.V, dt, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return prep
+
+        def make_run(t, p=p, dt=dt):
+            def run():
+                rc = mm.encbwd_run_planned(t["dwte"].data_ptr(), t["dwpe"].data_ptr(), t["dout"].data_ptr(),
+                                           t["plan"].data_ptr(), p.B, p.T, p.C, p.V, dt, None, sh)
+                if rc != mm.OK:
+                    raise RuntimeError(mm.strerror(rc))
+            return run
+
+        preps = [make_prep(t) for t in sets]
+        sec_prep = time_back_to_back(torch, stream, preps, max(len(preps), 40), batches)
+        runs = [make_run(t) for t in sets]
+        sec = time_back_to_back(torch, stream, runs, max(len(runs), 40), batches)
+        gbs = set_bytes / sec / 1e9
+        out[name] = {"B": p.B, "T": p.T, "C": p.C, "V": p.V, "dtype": p.dtype, "us": round(sec * 1e6, 2),
+                     "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
+                     "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": set_bytes,
+                     "prepare_us": round(sec_prep * 1e6, 2),
+                     "timed": "encbwd_run_planned; encbwd_prepare (the sort of the token ids) timed apart",
+                     "tokens": f"Zipf(s=1.1) over 50257 ids, {distinct} distinct", "input_sets": n_sets,
+                     "l2": "rotating sets > L2" if n_sets * x["dout"].nbytes > L2_BYTES else "L2-resident"}
+        del sets, preps, runs
+        torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
         raise RuntimeError(f"device status after other configs: {mm.strerror(status)} {info}")
@@ -744,7 +793,7 @@ def run_case(args):
     import linear_layer_gemms_gb300 as mm
 
     names = (set(OTHER_CONFIGS) | set(LN_CONFIGS) | set(ENC_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
-             | {n for n, _, _ in LAYER_CONFIGS})
+             | {n for n, _, _ in LAYER_CONFIGS} | {n for n, _ in ENC_PLANNED_CONFIGS})
     if args.case not in names:
         raise SystemExit(f"unknown case {args.case}; one of {sorted(names)}")
     dev = torch.device("cuda", 0)

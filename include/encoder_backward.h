@@ -78,6 +78,45 @@ int encbwd_run(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int
 int encbwd_run_sr(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                   int64_t V, int dtype, uint64_t seed, cudaStream_t stream);
 
+/*
+ * The same computation in two calls, so that the bucketing (which depends only
+ * on the token ids, known at the start of a training step) can run early --
+ * beside the forward pass, on another stream -- and leave the backward's
+ * critical path:
+ *
+ * encbwd_plan_bytes -- bytes of a plan for this problem (0 for invalid
+ *   arguments or an empty problem).
+ *
+ * encbwd_prepare -- enqueue the device sort of the token ids into `plan`.
+ *   plan       device, caller-owned, >= encbwd_plan_bytes bytes, 256-byte aligned;
+ *              written. A plan holds the sorted (token, position) keys, per-window
+ *              run tables and counters, and records B*T, V and C.
+ *   plan_bytes its size (MMBWD_ERR_SHAPE if too small)
+ *   inp        device, (B*T) int32 token ids, read only; ids outside [0, V) are
+ *              left out and reported by mmbwd_device_status()
+ *   B, T, C, V, dtype   as encbwd_run (C and dtype fix the plan's counters and
+ *              the alignment rule)
+ *   Errors as encbwd_run (ERR_NULL, ERR_ALIGN, ERR_ALIAS, ERR_SHAPE, ...).
+ *
+ * encbwd_run_planned -- enqueue dwte += ..., dwpe += ... from a plan.
+ *   dwte, dwpe, dout, B, T, C, V, dtype   as encbwd_run
+ *   plan       a plan from encbwd_prepare for the same B*T, V and C, ordered
+ *              before this call (same stream, or an event); read, and its
+ *              counters are returned to zero, so one plan serves any number of
+ *              runs (not at the same time). A plan of another problem is
+ *              detected on the device: nothing is written and
+ *              mmbwd_device_status() reports MMBWD_ERR_SHAPE (info[0] = -1).
+ *   sr_seed    NULL: round to nearest; else bf16 outputs rounded stochastically
+ *              with *sr_seed (as encbwd_run_sr; MMBWD_ERR_DTYPE for fp32)
+ *   Results are bitwise those of encbwd_run / encbwd_run_sr. Uses the shared
+ *   library workspace for its scratch (as encbwd_run). One launch.
+ */
+size_t encbwd_plan_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype);
+int encbwd_prepare(void* plan, size_t plan_bytes, const int32_t* inp, int64_t B, int64_t T, int64_t C, int64_t V,
+                   int dtype, cudaStream_t stream);
+int encbwd_run_planned(void* dwte, void* dwpe, const void* dout, void* plan, int64_t B, int64_t T, int64_t C,
+                       int64_t V, int dtype, const uint64_t* sr_seed, cudaStream_t stream);
+
 /* Workspace bytes encbwd_run needs for this problem (0 for invalid arguments). */
 size_t encbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype);
 

@@ -57,6 +57,9 @@ SIGNATURES = {
     "lnbwd_run": ([_vp] * 8 + [_i64] * 3 + [_ci, _vp], _ci),
     "encbwd_run": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
     "encbwd_run_sr": ([_vp] * 4 + [_i64] * 4 + [_ci, _u64, _vp], _ci),
+    "encbwd_plan_bytes": ([_i64] * 4 + [_ci], _sz),
+    "encbwd_prepare": ([_vp, _sz, _vp] + [_i64] * 4 + [_ci, _vp], _ci),
+    "encbwd_run_planned": ([_vp] * 4 + [_i64] * 4 + [_ci, ctypes.POINTER(_u64), _vp], _ci),
     "encbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
     "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
@@ -161,6 +164,26 @@ def encbwd_run_sr(dwte, dwpe, dout, inp, B: int, T: int, C: int, V: int, dtype: 
     mmbwd_run_sr); bf16 only."""
     return load().encbwd_run_sr(_ptr(dwte), _ptr(dwpe), _ptr(dout), _ptr(inp), B, T, C, V, dtype, seed,
                                 _stream(stream))
+
+
+def encbwd_plan_bytes(B: int, T: int, C: int, V: int, dtype: int) -> int:
+    """Bytes of the device buffer encbwd_prepare fills (0 for invalid arguments)."""
+    return int(load().encbwd_plan_bytes(B, T, C, V, dtype))
+
+
+def encbwd_prepare(plan, plan_bytes: int, inp, B: int, T: int, C: int, V: int, dtype: int, stream=None) -> int:
+    """Sort the token ids into ``plan`` (device, 256-byte aligned): the part of
+    the encoder backward that depends only on inp, to run ahead of time."""
+    return load().encbwd_prepare(_ptr(plan), plan_bytes, _ptr(inp), B, T, C, V, dtype, _stream(stream))
+
+
+def encbwd_run_planned(dwte, dwpe, dout, plan, B: int, T: int, C: int, V: int, dtype: int, seed=None,
+                       stream=None) -> int:
+    """dwte and dwpe += from a prepared plan (one launch); ``seed`` (an int)
+    selects stochastic rounding of bf16 outputs, None rounds to nearest."""
+    s = None if seed is None else ctypes.byref(_u64(seed))
+    return load().encbwd_run_planned(_ptr(dwte), _ptr(dwpe), _ptr(dout), _ptr(plan), B, T, C, V, dtype, s,
+                                     _stream(stream))
 
 
 def encbwd_workspace_bytes(B: int, T: int, C: int, V: int, dtype: int) -> int:

@@ -547,6 +547,66 @@ int encbwd_run_sr(void* dwte, void* dwpe, const void* dout, const int32_t* inp, 
     return run_encoder(dwte, dwpe, dout, inp, B, T, C, V, dtype, true, seed, stream);
 }
 
+size_t encbwd_plan_bytes(int64_t B, int64_t T, int64_t C, int64_t V, int dtype) {
+    int64_t BT = 0;
+    if (enc_check(B, T, C, V, dtype, &BT) != MMBWD_OK || BT == 0 || C == 0) return 0;
+    return enc_plan_bytes(BT, C);
+}
+
+int encbwd_prepare(void* plan, size_t plan_bytes, const int32_t* inp, int64_t B, int64_t T, int64_t C, int64_t V,
+                   int dtype, cudaStream_t stream) {
+    int64_t BT = 0;
+    int rc = enc_check(B, T, C, V, dtype, &BT);
+    if (rc != MMBWD_OK) return rc;
+    const size_t es = dtype == MMBWD_F32 ? 4 : 2;
+    if ((static_cast<size_t>(C) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+    if (BT == 0 || C == 0) return MMBWD_OK;  // nothing to bucket; a planned run of this size does nothing
+    if (!plan || !inp) return MMBWD_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(plan) & 255u) || (reinterpret_cast<uintptr_t>(inp) & 3u)) return MMBWD_ERR_ALIGN;
+    const size_t need = enc_plan_bytes(BT, C);
+    if (plan_bytes < need) return MMBWD_ERR_SHAPE;
+    if (overlaps(plan, need, inp, static_cast<size_t>(BT) * 4)) return MMBWD_ERR_ALIAS;
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    const cudaError_t e = enc_prepare_launch(plan, inp, B, T, C, V, stream);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
+int encbwd_run_planned(void* dwte, void* dwpe, const void* dout, void* plan, int64_t B, int64_t T, int64_t C,
+                       int64_t V, int dtype, const uint64_t* sr_seed, cudaStream_t stream) {
+    int64_t BT = 0;
+    int rc = enc_check(B, T, C, V, dtype, &BT);
+    if (rc != MMBWD_OK) return rc;
+    if (sr_seed && dtype != MMBWD_BF16) return MMBWD_ERR_DTYPE;
+    const size_t es = dtype == MMBWD_F32 ? 4 : 2;
+    const size_t b_out = static_cast<size_t>(BT) * C * es, b_wte = static_cast<size_t>(V) * C * es,
+                 b_wpe = static_cast<size_t>(T) * C * es;
+    if ((b_out && (!dout || !dwpe || !plan)) || (b_wte && !dwte)) return MMBWD_ERR_NULL;
+    const void* vecs[3] = {dwte, dwpe, dout};
+    for (const void* p : vecs)
+        if (p && !aligned16(p)) return MMBWD_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(plan) & 255u) return MMBWD_ERR_ALIGN;
+    if ((static_cast<size_t>(C) * es) % 16 != 0) return MMBWD_ERR_ALIGN;
+    const size_t b_plan = (BT && C) ? enc_plan_bytes(BT, C) : 0;
+    if (overlaps(dwte, b_wte, dwpe, b_wpe) || overlaps(dwte, b_wte, dout, b_out) || overlaps(dwpe, b_wpe, dout, b_out) ||
+        overlaps(plan, b_plan, dwte, b_wte) || overlaps(plan, b_plan, dwpe, b_wpe) || overlaps(plan, b_plan, dout, b_out))
+        return MMBWD_ERR_ALIAS;
+    std::lock_guard<std::mutex> g(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    if (BT == 0 || C == 0) return MMBWD_OK;
+    rc = ensure_workspace(*d, enc_run_workspace_bytes(BT, C), stream);
+    if (rc != MMBWD_OK) return rc;
+    const cudaError_t e = enc_run_planned_launch(dwte, dwpe, dout, plan, B, T, C, V, dtype, d->ws, d->num_sms, stream,
+                                                 sr_seed != nullptr, sr_seed ? *sr_seed : 0);
+    return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------
 // LayerNorm backward (layernorm_backward.h)
 

@@ -135,7 +135,7 @@ struct EncVec4<__nv_bfloat16> {
 };
 
 struct EncTables {
-    int* meta;           // [0] valid positions
+    int* meta;           // [0] valid positions; [1..3] B*T, V, C of the problem
     unsigned* skeys;     // [B*T] sorted keys (token << 15 | position)
     int* win_head;       // [windows] first slot of the run holding the window's first slot
     int* win_tail;       // [windows] last slot of the run holding the window's last slot
@@ -399,18 +399,24 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
         tb.win_tail[ilast / ENC_WIN] = min(next_start, nvalid) - 1;
     const int nwin_g = (nvalid + ENC_WIN - 1) / ENC_WIN * G;
     for (int e = tid; e < nwin_g; e += ENC_SORT_THREADS) tb.arrivals[e] = 0u;
-    if (tid == 0) tb.meta[0] = nvalid;
+    if (tid == 0) {
+        tb.meta[0] = nvalid;
+        tb.meta[1] = BT;  // the problem these tables describe
+        tb.meta[2] = V;
+        tb.meta[3] = C;
+    }
 }
 
 // Finishes one run that crosses a window edge (see the file comment), the
 // token's windows being span.x..span.y: stores this window's partial (slot q:
 // 0 for the run entering at the window's first slot, 1 for the run leaving at
 // its last), counts the window on the token's counter, and if it is the last
-// of windows wa..wb adds their partials in window order (window wa's slot 1,
-// then slot 0 of the others) to the old dwte row. Warp-uniform.
+// of windows wa..wb clears the counter and adds their partials in window order
+// (window wa's slot 1, then slot 0 of the others) to the old dwte row.
+// Warp-uniform.
 template <typename T>
 __device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, int c, bool active, int lane, int w,
-                              int q, int2 span, unsigned tok, const float (&acc)[4],
+                              int g, int G, int q, int2 span, unsigned tok, const float (&acc)[4],
                               typename EncVec4<T>::V old) {
     using EV = EncVec4<T>;
     constexpr int PB = 16;  // partials in flight
@@ -421,9 +427,12 @@ __device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, 
     __threadfence();
     __syncwarp();
     unsigned done = 0;
-    if (lane == 0) done = atomicAdd(&tb.arrivals[static_cast<int64_t>(wa) * gridDim.y + blockIdx.y], 1u);
+    const int64_t ci = static_cast<int64_t>(wa) * G + g;
+    if (lane == 0) done = atomicAdd(&tb.arrivals[ci], 1u);
     done = __shfl_sync(0xffffffffu, done, 0);
-    if (done != static_cast<unsigned>(nw - 1) || !active) return;  // not the last window of the token
+    if (done != static_cast<unsigned>(nw - 1)) return;  // not the last window of the token
+    if (lane == 0) tb.arrivals[ci] = 0u;  // every window has counted: cleared for the next call with this plan
+    if (!active) return;
     __threadfence();
     float sum[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < nw; k += PB) {
@@ -451,22 +460,42 @@ __device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, 
 // Loads that do not depend on each other are issued together (the keys are
 // read before the valid count is known, at indexes clamped to the table).
 // Lanes past C take part in the shuffles only.
+// One-dimensional grid: blocks [0, nwb G) are window blocks (block b: windows
+// 4 (b mod nwb) .. +3, channel group b / nwb); `wpe_blocks` more blocks form
+// dwpe (a planned run, whose sort launch had none). The tables must describe
+// this problem (the sort records B*T, V and C beside them); otherwise the
+// status word reports it and nothing is written.
 template <typename T>
-__global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte, const T* __restrict__ dout, int C,
-                                                           int BT, EncTables tb) {
+__global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte, T* __restrict__ dwpe,
+                                                           const T* __restrict__ dout, int C, int BT, int B, int T_,
+                                                           int V, int nwb, int G, int wpe_blocks, EncTables tb) {
     using EV = EncVec4<T>;
-    using V = typename EV::V;
+    using V4 = typename EV::V;
     constexpr int RB = sizeof(T) == 2 ? 16 : 8;  // rows in flight
     constexpr unsigned NONE = 0xFFFFFFFFu;
     enc_grid_wait();
     enc_launch_dependents();
+    const int bid = static_cast<int>(blockIdx.x);
+    if (tb.meta[1] != BT || tb.meta[2] != V || tb.meta[3] != C) {  // tables of another problem
+        if (threadIdx.x == 0 && atomicCAS(&g_enc_status[0], 0u, static_cast<unsigned>(-MMBWD_ERR_SHAPE)) == 0u) {
+            g_enc_status[1] = 0xFFFFFFFFu;
+            g_enc_status[2] = static_cast<unsigned>(tb.meta[1]);
+        }
+        return;
+    }
+    if (bid >= nwb * G) {
+        enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(bid - nwb * G) * blockDim.x + threadIdx.x,
+                        static_cast<int64_t>(wpe_blocks) * blockDim.x, tb.sr, tb.seed);
+        return;
+    }
+    const int nvalid = tb.meta[0];
+    const int g = bid / nwb;
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-    const int w = static_cast<int>(blockIdx.x) * 4 + warp;
+    const int w = (bid - g * nwb) * 4 + warp;
     const int base = w * ENC_WIN;
     if (base >= BT) return;
-    const int c = (static_cast<int>(blockIdx.y) * 32 + lane) * 4;
+    const int c = (g * 32 + lane) * 4;
     const bool active = c < C;
-    const int nvalid = tb.meta[0];
     const unsigned key = tb.skeys[min(base + lane, BT - 1)];
     const unsigned pkey = base > 0 ? tb.skeys[base - 1] : NONE;
     const unsigned nkey = base + ENC_WIN < BT ? tb.skeys[base + ENC_WIN] : NONE;
@@ -493,11 +522,11 @@ __global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte
     const unsigned emask = ((smask >> 1) | (1u << (nv - 1))) & vmask;
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, hacc[4] = {0.f, 0.f, 0.f, 0.f}, tacc[4] = {0.f, 0.f, 0.f, 0.f};
-    V hold = EV::zero(), told = EV::zero();
+    V4 hold = EV::zero(), told = EV::zero();
 #pragma unroll
     for (int j0 = 0; j0 < ENC_WIN; j0 += RB) {
         if (j0 < nv) {  // warp-uniform
-            V v[RB], o[RB];
+            V4 v[RB], o[RB];
 #pragma unroll
             for (int u = 0; u < RB; ++u) {
                 constexpr unsigned one = 1u;
@@ -537,8 +566,9 @@ __global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte
         }
     }
     // A run that fills the window and crosses both edges is the head run.
-    if (head_cross) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, 0, hspan, tok0, hacc, hold);
-    if (tail_cross && smask != 0u) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, 1, tspan, tokl, tacc, told);
+    if (head_cross) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, g, G, 0, hspan, tok0, hacc, hold);
+    if (tail_cross && smask != 0u)
+        enc_cross_run<T>(dwte, tb, C, c, active, lane, w, g, G, 1, tspan, tokl, tacc, told);
 }
 
 cudaError_t launch_pdl(const void* k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
@@ -576,35 +606,42 @@ const void* enc_sort_fn(int kpl) {
 
 }  // namespace
 
-// Workspace: meta, sorted keys, per-window tables, counters (four channels
-// per lane), partials.
-size_t enc_workspace_bytes(int64_t BT, int64_t C) {
-    const size_t n = static_cast<size_t>(BT), nwin = (n + ENC_WIN - 1) / ENC_WIN;
-    return a256(4 * 4) + a256(n * 4) + a256(nwin * 4) + a256(nwin * 4) +
-           a256(nwin * static_cast<size_t>(enc_groups(C, 4)) * 4) + a256(nwin * 2 * static_cast<size_t>(C) * 4);
-}
+namespace {
 
-cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
-                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr, uint64_t seed) {
-    const int BT = static_cast<int>(B * T);
-    const int nwin = (BT + ENC_WIN - 1) / ENC_WIN;
-    const int N = dtype == MMBWD_F32 ? 4 : 8;  // elements per 16-byte vector (dwpe)
-    int G = enc_groups(C, 4);                   // window kernel: four channels per lane
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    EncTables tb{};
+// The tables of one problem, laid out from `base`: meta, sorted keys, the two
+// per-window tables, the per-(window, channel group) counters. Returns the
+// bytes they take.
+size_t enc_tables_layout(uint8_t* base, int64_t BT, int64_t C, EncTables* tb) {
+    const size_t n = static_cast<size_t>(BT), nwin = (n + ENC_WIN - 1) / ENC_WIN;
+    size_t off = 0;
     auto take = [&](size_t bytes) {
-        uint8_t* p = w;
-        w += a256(bytes);
+        uint8_t* p = base ? base + off : nullptr;
+        off += a256(bytes);
         return p;
     };
-    tb.meta = reinterpret_cast<int*>(take(4 * 4));
-    tb.skeys = reinterpret_cast<unsigned*>(take(static_cast<size_t>(BT) * 4));
-    tb.win_head = reinterpret_cast<int*>(take(static_cast<size_t>(nwin) * 4));
-    tb.win_tail = reinterpret_cast<int*>(take(static_cast<size_t>(nwin) * 4));
-    tb.arrivals = reinterpret_cast<unsigned*>(take(static_cast<size_t>(nwin) * enc_groups(C, 4) * 4));
-    tb.partials = reinterpret_cast<float*>(take(static_cast<size_t>(nwin) * 2 * C * 4));
-    tb.sr = sr ? 1 : 0;
-    tb.seed = seed;
+    uint8_t* meta = take(4 * 4);
+    uint8_t* skeys = take(n * 4);
+    uint8_t* whead = take(nwin * 4);
+    uint8_t* wtail = take(nwin * 4);
+    uint8_t* arr = take(nwin * static_cast<size_t>(enc_groups(C, 4)) * 4);
+    if (tb) {
+        tb->meta = reinterpret_cast<int*>(meta);
+        tb->skeys = reinterpret_cast<unsigned*>(skeys);
+        tb->win_head = reinterpret_cast<int*>(whead);
+        tb->win_tail = reinterpret_cast<int*>(wtail);
+        tb->arrivals = reinterpret_cast<unsigned*>(arr);
+    }
+    return off;
+}
+
+size_t enc_partials_bytes(int64_t BT, int64_t C) {
+    const size_t nwin = (static_cast<size_t>(BT) + ENC_WIN - 1) / ENC_WIN;
+    return a256(nwin * 2 * static_cast<size_t>(C) * 4);
+}
+
+// The sort: block 0 builds the tables; `wpe_blocks` more blocks form dwpe.
+cudaError_t enc_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C, int64_t B, int64_t T, int dtype,
+                            const EncTables& tb, void* dwpe, const void* dout, int wpe_blocks, cudaStream_t stream) {
     int kpl = 1;
     while (kpl * ENC_SORT_THREADS < BT) kpl <<= 1;
     // sort on the smallest b with 2^b > V: the padding's digits (all ones) then
@@ -617,26 +654,76 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
     const void* ks = dtype == MMBWD_F32 ? enc_sort_fn<float>(kpl) : enc_sort_fn<__nv_bfloat16>(kpl);
     cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sort_smem));
     if (e != cudaSuccess) return e;
-    int Vi = static_cast<int>(V), Ci = static_cast<int>(C), Bi = static_cast<int>(B), Ti = static_cast<int>(T);
-    int BTi = BT;
-    {
-        // block 0 sorts; one wave of blocks (at most one per SM besides it) forms dwpe
-        const int64_t wpe_threads = (T * C / N + ENC_SORT_THREADS - 1) / ENC_SORT_THREADS;
-        const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, std::max(num_sms - 1, 1)));
-        void* args[] = {const_cast<int32_t**>(&inp), &BTi, &Vi, &passes, &G, &tb,
-                        &dwpe, const_cast<void**>(&dout), &Bi, &Ti, &Ci};
-        e = launch_pdl(ks, dim3(static_cast<unsigned>(1 + wpe_blocks)), dim3(ENC_SORT_THREADS), sort_smem, stream,
-                       args);
-        if (e != cudaSuccess) return e;
-    }
-    {
-        const void* k = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&enc_window_kernel<float>)
-                                           : reinterpret_cast<const void*>(&enc_window_kernel<__nv_bfloat16>);
-        void* args[] = {&dwte, const_cast<void**>(&dout), &Ci, &BTi, &tb};
-        e = launch_pdl(k, dim3(static_cast<unsigned>((nwin + 3) / 4), static_cast<unsigned>(G)), dim3(128), 0, stream,
-                       args);
-    }
-    return e;
+    int BTi = BT, Vi = static_cast<int>(V), Ci = static_cast<int>(C), Bi = static_cast<int>(B), Ti = static_cast<int>(T);
+    int G = enc_groups(C, 4);
+    EncTables t = tb;
+    void* args[] = {const_cast<int32_t**>(&inp), &BTi, &Vi, &passes, &G, &t,
+                    &dwpe, const_cast<void**>(&dout), &Bi, &Ti, &Ci};
+    return launch_pdl(ks, dim3(static_cast<unsigned>(1 + wpe_blocks)), dim3(ENC_SORT_THREADS), sort_smem, stream, args);
+}
+
+// The window sums (and, with wpe_blocks > 0, dwpe) over tables `tb`.
+cudaError_t enc_window_launch(void* dwte, void* dwpe, const void* dout, int64_t B, int64_t T, int64_t C, int64_t V,
+                              int dtype, const EncTables& tb, int wpe_blocks, cudaStream_t stream) {
+    int BTi = static_cast<int>(B * T), Ci = static_cast<int>(C), Bi = static_cast<int>(B), Ti = static_cast<int>(T),
+        Vi = static_cast<int>(V);
+    const int nwin = (BTi + ENC_WIN - 1) / ENC_WIN;
+    int nwb = (nwin + 3) / 4, G = enc_groups(C, 4), wb = wpe_blocks;
+    EncTables t = tb;
+    void* args[] = {&dwte, &dwpe, const_cast<void**>(&dout), &Ci, &BTi, &Bi, &Ti, &Vi, &nwb, &G, &wb, &t};
+    const void* k = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&enc_window_kernel<float>)
+                                       : reinterpret_cast<const void*>(&enc_window_kernel<__nv_bfloat16>);
+    return launch_pdl(k, dim3(static_cast<unsigned>(nwb * G + wpe_blocks)), dim3(128), 0, stream, args);
+}
+
+}  // namespace
+
+// Workspace of the one-call form: the tables, then the partials.
+size_t enc_workspace_bytes(int64_t BT, int64_t C) {
+    return enc_tables_layout(nullptr, BT, C, nullptr) + enc_partials_bytes(BT, C);
+}
+
+size_t enc_plan_bytes(int64_t BT, int64_t C) { return enc_tables_layout(nullptr, BT, C, nullptr); }
+size_t enc_run_workspace_bytes(int64_t BT, int64_t C) { return enc_partials_bytes(BT, C); }
+
+cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
+                       int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr, uint64_t seed) {
+    const int BT = static_cast<int>(B * T);
+    const int N = dtype == MMBWD_F32 ? 4 : 8;  // elements per 16-byte vector (dwpe)
+    EncTables tb{};
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const size_t tbytes = enc_tables_layout(w, BT, C, &tb);
+    tb.partials = reinterpret_cast<float*>(w + tbytes);
+    tb.sr = sr ? 1 : 0;
+    tb.seed = seed;
+    // block 0 sorts; one wave of blocks (at most one per SM besides it) forms dwpe
+    const int64_t wpe_threads = (T * C / N + ENC_SORT_THREADS - 1) / ENC_SORT_THREADS;
+    const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, std::max(num_sms - 1, 1)));
+    cudaError_t e = enc_sort_launch(inp, BT, V, C, B, T, dtype, tb, dwpe, dout, wpe_blocks, stream);
+    if (e != cudaSuccess) return e;
+    return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, 0, stream);
+}
+
+cudaError_t enc_prepare_launch(void* plan, const int32_t* inp, int64_t B, int64_t T, int64_t C, int64_t V,
+                               cudaStream_t stream) {
+    EncTables tb{};
+    enc_tables_layout(static_cast<uint8_t*>(plan), B * T, C, &tb);
+    return enc_sort_launch(inp, static_cast<int>(B * T), V, C, B, T, MMBWD_BF16, tb, nullptr, nullptr, 0, stream);
+}
+
+cudaError_t enc_run_planned_launch(void* dwte, void* dwpe, const void* dout, void* plan, int64_t B, int64_t T,
+                                   int64_t C, int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr,
+                                   uint64_t seed) {
+    const int N = dtype == MMBWD_F32 ? 4 : 8;
+    EncTables tb{};
+    enc_tables_layout(static_cast<uint8_t*>(plan), B * T, C, &tb);
+    tb.partials = static_cast<float*>(ws);
+    tb.sr = sr ? 1 : 0;
+    tb.seed = seed;
+    // dwpe blocks of 128 threads (one 16-byte vector each), at most two per SM
+    const int64_t vecs = T * C / N;
+    const int wpe_blocks = static_cast<int>(std::min<int64_t>((vecs + 127) / 128, 2 * std::max(num_sms, 1)));
+    return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, wpe_blocks, stream);
 }
 
 cudaError_t enc_read_status(int* code, int* info3, bool reset) {

@@ -182,6 +182,13 @@ cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight,
 // ---------------------------------------------------------------- encoder backward
 
 size_t enc_workspace_bytes(int64_t BT, int64_t C);
+size_t enc_plan_bytes(int64_t BT, int64_t C);           // the tables encbwd_prepare writes
+size_t enc_run_workspace_bytes(int64_t BT, int64_t C);  // scratch of a planned run
+cudaError_t enc_prepare_launch(void* plan, const int32_t* inp, int64_t B, int64_t T, int64_t C, int64_t V,
+                               cudaStream_t stream);
+cudaError_t enc_run_planned_launch(void* dwte, void* dwpe, const void* dout, void* plan, int64_t B, int64_t T,
+                                   int64_t C, int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream,
+                                   bool sr, uint64_t seed);
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                        int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr = false,
                        uint64_t seed = 0);

@@ -216,6 +216,25 @@ def test_sr_rejects_fp32_and_bad_arguments():
     assert f(dweight=4 * A) == mm.ERR_ALIAS
 
 
+def test_encoder_plan_rejects_bad_arguments():
+    need = mm.encbwd_plan_bytes(2, 8, 64, 100, mm.BF16)
+    assert need > 0 and mm.encbwd_plan_bytes(2, 8, 64, 131072, mm.BF16) == 0
+    p = lambda **kw: mm.encbwd_prepare(**{**dict(plan=8 * A, plan_bytes=need, inp=4 * A, B=2, T=8, C=64, V=100,  # noqa: E731
+                                                 dtype=mm.BF16, stream=0), **kw})
+    assert p(plan=None) == mm.ERR_NULL
+    assert p(plan=8 * A + 16) == mm.ERR_ALIGN           # plans are 256-byte aligned
+    assert p(plan_bytes=need - 1) == mm.ERR_SHAPE
+    assert p(inp=8 * A + 64) == mm.ERR_ALIAS             # ids inside the plan
+    assert p(C=12) == mm.ERR_ALIGN
+    r = lambda **kw: mm.encbwd_run_planned(**{**dict(dwte=A, dwpe=2 * A, dout=3 * A, plan=8 * A, B=2, T=8,  # noqa: E731
+                                                     C=64, V=100, dtype=mm.BF16, seed=None, stream=0), **kw})
+    assert r(plan=None) == mm.ERR_NULL
+    assert r(plan=8 * A + 32) == mm.ERR_ALIGN
+    assert r(dtype=mm.F32, seed=5) == mm.ERR_DTYPE       # stochastic rounding is for bf16 outputs
+    assert r(plan=A + 256) == mm.ERR_ALIAS               # plan inside dwte
+    assert r(dwpe=3 * A) == mm.ERR_ALIAS
+
+
 def test_encoder_rejects_bad_arguments():
     f = lambda **kw: mm.encbwd_run(**{**dict(dwte=A, dwpe=2 * A, dout=3 * A, inp=4 * A, B=2, T=8, C=64,  # noqa: E731
                                              V=100, dtype=mm.BF16, stream=0), **kw})

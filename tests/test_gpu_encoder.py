@@ -179,3 +179,45 @@ def test_encoder_sr_integer_exact_and_repeatable():
     got = synth.bf16_bits_to_f64(outs[0][1])
     assert np.any(got > exact) and np.any(got < exact)  # rounded both ways
     assert mm.encbwd_run_sr(None, None, None, None, B, T, C, V, mm.F32, 1) == mm.ERR_DTYPE
+
+
+def test_encoder_planned_matches_one_call_and_plan_reuse():
+    """encbwd_prepare + encbwd_run_planned gives the bits of encbwd_run (and of
+    encbwd_run_sr with a seed); one plan serves repeated runs; a plan of
+    another problem is reported and changes nothing."""
+    import torch
+
+    for name in ("enc_gpt2_small", "enc_tiny"):
+        p = synth.ENC_WORKLOADS[name]
+        x = synth.make_enc_inputs(p, seed=5)
+        dt = mm.BF16 if p.dtype == "bf16" else mm.F32
+        gi = torch.from_numpy(x["inp"]).to("cuda:0")
+        one = run_enc(x, p.B, p.T, p.C, p.V, p.dtype)
+        nbytes = mm.encbwd_plan_bytes(p.B, p.T, p.C, p.V, dt)
+        plan = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+        assert mm.encbwd_prepare(plan, nbytes, gi, p.B, p.T, p.C, p.V, dt) == mm.OK
+        for _ in range(2):  # the same plan twice, from fresh initial values
+            g = {k: to_dev(x[k], p.dtype) for k in ("dout", "dwte", "dwpe")}
+            assert mm.encbwd_run_planned(g["dwte"], g["dwpe"], g["dout"], plan, p.B, p.T, p.C, p.V, dt) == mm.OK
+            torch.cuda.synchronize()
+            for k in ("dwte", "dwpe"):
+                assert torch.equal(g[k].view(torch.uint8), one[k].view(torch.uint8)), (name, k)
+        assert mm.mmbwd_device_status(reset=True)[0] == mm.OK
+        if p.dtype == "bf16":
+            a = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+            b = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+            assert mm.encbwd_run_sr(a["dwte"], a["dwpe"], a["dout"], gi, p.B, p.T, p.C, p.V, dt, 77) == mm.OK
+            assert mm.encbwd_run_planned(b["dwte"], b["dwpe"], b["dout"], plan, p.B, p.T, p.C, p.V, dt, 77) == mm.OK
+            torch.cuda.synchronize()
+            for k in ("dwte", "dwpe"):
+                assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), ("sr", k)
+            # the plan of another problem (T halved): reported, nothing written
+            c = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+            before = {k: v.clone() for k, v in c.items()}
+            mm.mmbwd_device_status(reset=True)
+            assert mm.encbwd_run_planned(c["dwte"], c["dwpe"], c["dout"], plan, p.B, p.T // 2, p.C, p.V, dt) == mm.OK
+            torch.cuda.synchronize()
+            status, info = mm.mmbwd_device_status(reset=True)
+            assert status == mm.ERR_SHAPE and info[0] == -1
+            for k in c:
+                assert torch.equal(c[k], before[k]), k
