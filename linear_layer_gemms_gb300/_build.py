@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmmbwd.so")
 SOURCES = ["api.cu", "tc_gemm.cu", "simt_f32.cu", "layernorm_bwd.cu", "split_tf32.cu", "encoder_bwd.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+HEADERS = ["internal.h", "ops.h", "ptx.cuh", "sr.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

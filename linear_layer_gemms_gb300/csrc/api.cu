@@ -5,6 +5,7 @@
 #include "../../include/layernorm_backward.h"
 #include "../../include/encoder_backward.h"
 #include "internal.h"
+#include "ops.h"
 
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -32,7 +32,7 @@
 
 #include "../../include/encoder_backward.h"
 #include "../../include/mmbwd.h"
-#include "internal.h"
+#include "ops.h"
 #include "sr.cuh"
 
 namespace mmbwd {

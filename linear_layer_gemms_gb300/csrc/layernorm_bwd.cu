@@ -33,7 +33,7 @@
 // global memory only after `griddepcontrol.wait`.
 #include "../../include/layernorm_backward.h"
 #include "../../include/mmbwd.h"
-#include "internal.h"
+#include "ops.h"
 #include "ptx.cuh"
 
 #include <algorithm>

@@ -15,7 +15,7 @@
 // the dout tile they stage in shared memory over its K (= BT) rows, in K order,
 // and overwrite dbias. No split of K, so each output has one writer.
 #include "../../include/mmbwd.h"
-#include "internal.h"
+#include "ops.h"
 #include "sr.cuh"
 
 #include <algorithm>

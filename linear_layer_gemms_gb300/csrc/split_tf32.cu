@@ -17,6 +17,7 @@
 // a second small kernel adds those tile sums in tile order: dbias.
 #include "../../include/mmbwd.h"
 #include "internal.h"
+#include "ops.h"
 
 namespace mmbwd {
 namespace {
