@@ -211,7 +211,7 @@ int oracle_forward_rows(double* out, const int64_t* rows, int64_t nrows, const v
     return 0;
 }
 
-/* Number of threads a parallel region of this build uses (1 when built without OpenMP). */
+/* Number of threads a parallel region of this compiled variant uses (1 without OpenMP). */
 int oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
