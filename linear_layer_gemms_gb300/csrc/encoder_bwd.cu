@@ -460,15 +460,18 @@ __device__ void enc_cross_run(T* __restrict__ dwte, const EncTables& tb, int C, 
 // Loads that do not depend on each other are issued together (the keys are
 // read before the valid count is known, at indexes clamped to the table).
 // Lanes past C take part in the shuffles only.
-// One-dimensional grid: blocks [0, nwb G) are window blocks (block b: windows
-// 4 (b mod nwb) .. +3, channel group b / nwb); `wpe_blocks` more blocks form
-// dwpe (a planned run, whose sort launch had none). The tables must describe
-// this problem (the sort records B*T, V and C beside them); otherwise the
-// status word reports it and nothing is written.
+// One-dimensional grid of blocks of GPB = blockDim / 32 warps: blocks
+// [0, nwin ngb) are window blocks, ngb = ceil(G / GPB) per window, block b
+// serving window b / ngb with warp k taking channel group (b mod ngb) GPB + k,
+// so that the warps reading the slices of the same dout and dwte rows run side
+// by side; `wpe_blocks` more blocks form dwpe (a planned run, whose sort launch
+// had none). The tables must describe this problem (the sort records B*T, V
+// and C beside them); otherwise the status word reports it and nothing is
+// written.
 template <typename T>
-__global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte, T* __restrict__ dwpe,
+__global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte, T* __restrict__ dwpe,
                                                            const T* __restrict__ dout, int C, int BT, int B, int T_,
-                                                           int V, int nwb, int G, int wpe_blocks, EncTables tb) {
+                                                           int V, int nwin, int G, int wpe_blocks, EncTables tb) {
     using EV = EncVec4<T>;
     using V4 = typename EV::V;
     constexpr int RB = sizeof(T) == 2 ? 16 : 8;  // rows in flight
@@ -483,15 +486,17 @@ __global__ void __launch_bounds__(128, 4) enc_window_kernel(T* __restrict__ dwte
         }
         return;
     }
-    if (bid >= nwb * G) {
-        enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(bid - nwb * G) * blockDim.x + threadIdx.x,
+    const int gpb = static_cast<int>(blockDim.x >> 5), ngb = (G + gpb - 1) / gpb;
+    if (bid >= nwin * ngb) {
+        enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(bid - nwin * ngb) * blockDim.x + threadIdx.x,
                         static_cast<int64_t>(wpe_blocks) * blockDim.x, tb.sr, tb.seed);
         return;
     }
     const int nvalid = tb.meta[0];
-    const int g = bid / nwb;
     const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-    const int w = (bid - g * nwb) * 4 + warp;
+    const int w = bid / ngb;
+    const int g = (bid - w * ngb) * gpb + warp;
+    if (g >= G) return;  // the last group block of a window may be partly empty
     const int base = w * ENC_WIN;
     if (base >= BT) return;
     const int c = (g * 32 + lane) * 4;
@@ -668,12 +673,13 @@ cudaError_t enc_window_launch(void* dwte, void* dwpe, const void* dout, int64_t 
     int BTi = static_cast<int>(B * T), Ci = static_cast<int>(C), Bi = static_cast<int>(B), Ti = static_cast<int>(T),
         Vi = static_cast<int>(V);
     const int nwin = (BTi + ENC_WIN - 1) / ENC_WIN;
-    int nwb = (nwin + 3) / 4, G = enc_groups(C, 4), wb = wpe_blocks;
+    int nw = nwin, G = enc_groups(C, 4), wb = wpe_blocks;
+    const int gpb = std::min(G, 8), ngb = (G + gpb - 1) / gpb;  // warps (channel groups) per block
     EncTables t = tb;
-    void* args[] = {&dwte, &dwpe, const_cast<void**>(&dout), &Ci, &BTi, &Bi, &Ti, &Vi, &nwb, &G, &wb, &t};
+    void* args[] = {&dwte, &dwpe, const_cast<void**>(&dout), &Ci, &BTi, &Bi, &Ti, &Vi, &nw, &G, &wb, &t};
     const void* k = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&enc_window_kernel<float>)
                                        : reinterpret_cast<const void*>(&enc_window_kernel<__nv_bfloat16>);
-    return launch_pdl(k, dim3(static_cast<unsigned>(nwb * G + wpe_blocks)), dim3(128), 0, stream, args);
+    return launch_pdl(k, dim3(static_cast<unsigned>(nwin * ngb + wpe_blocks)), dim3(32 * gpb), 0, stream, args);
 }
 
 }  // namespace
@@ -720,9 +726,10 @@ cudaError_t enc_run_planned_launch(void* dwte, void* dwpe, const void* dout, voi
     tb.partials = static_cast<float*>(ws);
     tb.sr = sr ? 1 : 0;
     tb.seed = seed;
-    // dwpe blocks of 128 threads (one 16-byte vector each), at most two per SM
+    // dwpe blocks of the window blocks' width (one 16-byte vector per thread), at most two per SM
     const int64_t vecs = T * C / N;
-    const int wpe_blocks = static_cast<int>(std::min<int64_t>((vecs + 127) / 128, 2 * std::max(num_sms, 1)));
+    const int64_t width = 32 * std::min(enc_groups(C, 4), 8);
+    const int wpe_blocks = static_cast<int>(std::min<int64_t>((vecs + width - 1) / width, 2 * std::max(num_sms, 1)));
     return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, wpe_blocks, stream);
 }
 
