@@ -528,7 +528,7 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, hacc[4] = {0.f, 0.f, 0.f, 0.f}, tacc[4] = {0.f, 0.f, 0.f, 0.f};
     V4 hold = EV::zero(), told = EV::zero();
-#pragma unroll
+#pragma unroll 1
     for (int j0 = 0; j0 < ENC_WIN; j0 += RB) {
         if (j0 < nv) {  // warp-uniform
             V4 v[RB], o[RB];
