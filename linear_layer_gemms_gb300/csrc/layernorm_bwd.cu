@@ -200,6 +200,18 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
     for (int j = 0; j < VPT; ++j)
 #pragma unroll
         for (int e = 0; e < N; ++e) acc_w[j][e] = acc_b[j][e] = 0.f;
+    // this thread's weights are the same for every row: registers
+    float wr[VPT][N];
+#pragma unroll
+    for (int jj = 0; jj < VPT; ++jj) {
+        const int v = tt + 32 * P * jj;
+        if (v < p.nvec) {
+            weights(v, wr[jj]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < N; ++e) wr[jj][e] = 0.f;
+        }
+    }
 
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_block;
     const int64_t r1 = r0 + p.rows_per_block < p.BT ? r0 + p.rows_per_block : p.BT;
@@ -237,22 +249,27 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
         ln_wait(full0 + 8u * (j % LN_STAGES), static_cast<uint32_t>((j / LN_STAGES) & 1), abort, LN_SITE_FULL, r);
         const uint32_t sb = team_buf + static_cast<uint32_t>(j % LN_STAGES) * stage_bytes;
 
-        // first pass: the two row sums
+        // first pass: the two row sums; dout and the normalised input stay in
+        // registers for the second pass
         float sa = 0.f, sc = 0.f;
+        float d[VPT][N], nrm[VPT][N];
 #pragma unroll
         for (int jj = 0; jj < VPT; ++jj) {
             const int v = tt + 32 * P * jj;
             if (v < p.nvec) {
-                float d[N], x[N], w[N];
-                E::unpack(ptx::lds128(sb + 16u * v), d);
+                float x[N];
+                E::unpack(ptx::lds128(sb + 16u * v), d[jj]);
                 E::unpack(ptx::lds128(sb + row_bytes + 16u * v), x);
-                weights(v, w);
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
-                    const float g = w[e] * d[e];
+                    nrm[jj][e] = (x[e] - m) * sd;
+                    const float g = wr[jj][e] * d[jj][e];
                     sa += g;
-                    sc += g * ((x[e] - m) * sd);
+                    sc += g * nrm[jj][e];
                 }
+            } else {
+#pragma unroll
+                for (int e = 0; e < N; ++e) d[jj][e] = nrm[jj][e] = 0.f;
             }
         }
 #pragma unroll
@@ -284,18 +301,14 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
         for (int jj = 0; jj < VPT; ++jj) {
             const int v = tt + 32 * P * jj;
             if (v < p.nvec) {
-                float d[N], x[N], o[N], w[N];
-                E::unpack(ptx::lds128(sb + 16u * v), d);
-                E::unpack(ptx::lds128(sb + row_bytes + 16u * v), x);
+                float o[N];
                 E::unpack(ptx::lds128(sb + 2 * row_bytes + 16u * v), o);
-                weights(v, w);
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
-                    const float nrm = (x[e] - m) * sd;
                     // rstd * (g - a - n c), as sd*g - sd*a - (sd*c)*n
-                    o[e] += fmaf(sd, w[e] * d[e], -fmaf(sdc, nrm, sda));
-                    acc_w[jj][e] = fmaf(nrm, d[e], acc_w[jj][e]);
-                    acc_b[jj][e] += d[e];
+                    o[e] += fmaf(sd, wr[jj][e] * d[jj][e], -fmaf(sdc, nrm[jj][e], sda));
+                    acc_w[jj][e] = fmaf(nrm[jj][e], d[jj][e], acc_w[jj][e]);
+                    acc_b[jj][e] += d[jj][e];
                 }
                 __stcg(orow + v, E::pack(o));
             }
