@@ -48,13 +48,14 @@ constexpr int ENC_WIN = 32;  // sorted slots per window (one per lane)
 constexpr unsigned ENC_PAD = 0xFFFFFFFFu;
 constexpr int ENC_DIGIT_BITS = 4;  // radix digit width per pass
 constexpr int ENC_DIGITS = 1 << ENC_DIGIT_BITS;
-constexpr int ENC_CNT = ENC_DIGITS * ENC_SORT_THREADS;  // (digit, thread) counters
-constexpr int ENC_CNT_WORDS = ENC_CNT + ENC_CNT / 32;   // with one pad word per 32
+// (digit, thread) counters, two digits (2k, 2k + 1) packed in the 16-bit halves
+// of word k * 1024 + thread
+constexpr int ENC_CNT = ENC_DIGITS / 2 * ENC_SORT_THREADS;
+constexpr int ENC_CNT_WORDS = ENC_CNT + ENC_CNT / 32;  // with one pad word per 32
 
-// Counter e = digit * 1024 + thread, padded so that a warp's 32 threads (one
-// digit each) and a thread's 16 consecutive counters in the scan both fall in
-// 32 distinct banks.
-__device__ __forceinline__ int enc_cnt_at(int e) { return e + (e >> 5); }
+// Word w, padded so that a warp's 32 threads (one word row each) and a
+// thread's 8 consecutive words in the scan both fall in 32 distinct banks.
+__device__ __forceinline__ int enc_cnt_at(int w) { return w + (w >> 5); }
 
 __device__ __forceinline__ void enc_grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Lets the next kernel on the stream be scheduled now; it still waits (its
@@ -256,11 +257,12 @@ __device__ void block_exclusive_max_and_suffix_min(int mx, int mn, int* warp_sum
 // position order (padding, all ones, after the last position), so a stable
 // sort by token leaves each token's positions in increasing order and the
 // padding last. A pass over a 4-bit digit (no warp votes):
-//   - each thread ranks its keys among its own keys of equal digit
-//     (compares in registers) and stores its count per digit at counter
-//     (digit, thread);
-//   - one block scan over the counters in (digit, thread) order turns them into
-//     each thread's first slot per digit;
+//   - each thread counts its keys per digit in registers (its keys' ranks among
+//     its own keys of equal digit come with it) and stores the counts, two
+//     digits per word, at word (digit / 2, thread);
+//   - one block scan over the words, whose 16-bit halves add independently,
+//     and the prefix at the start of each word row turn them into each
+//     thread's first slot per digit in (digit, thread) order;
 //   - each key goes to first slot + rank, back into the same shared buffer.
 // Thread order is slot order, so the pass is stable.
 // Blocks 1.. form dwpe (enc_wpe_part).
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     unsigned* keys = enc_smem;
     int* cnt = reinterpret_cast<int*>(enc_smem + NP);
     __shared__ int warp_sums[32], warp_sums2[32];
+    __shared__ int row_start[ENC_DIGITS / 2 + 1];
     const int i0 = tid * KPL;
     unsigned k[KPL];
 #pragma unroll
@@ -312,42 +315,62 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
                 for (int r = 0; r < KPL; ++r) k[r] = keys[i0 + r];
             }
         }
-#pragma unroll
-        for (int q = 0; q < ENC_DIGITS; ++q) cnt[enc_cnt_at(tid * ENC_DIGITS + q)] = 0;
-        int rank[KPL];  // earlier keys of this thread with the same digit
+        // per-thread digit counts in 8-bit fields (digits 0-7 in c0, 8-15 in
+        // c1); a key's rank is its digit's count before it
+        uint64_t c0 = 0, c1 = 0;
+        int rank[KPL];
 #pragma unroll
         for (int r = 0; r < KPL; ++r) {
             const unsigned d = (k[r] >> sh) & (ENC_DIGITS - 1);
-            int n = 0;
-#pragma unroll
-            for (int q = 0; q < r; ++q) n += ((k[q] >> sh) & (ENC_DIGITS - 1)) == d;
-            rank[r] = n;
+            const int f = 8 * static_cast<int>(d & 7u);
+            rank[r] = static_cast<int>((((d & 8u) ? c1 : c0) >> f) & 0xFFu);
+            if (d & 8u) c1 += uint64_t(1) << f;
+            else c0 += uint64_t(1) << f;
         }
-        __syncthreads();  // counters zeroed; every thread has read its keys
+        // this thread's 8 packed words (every word written, so no clearing)
 #pragma unroll
-        for (int r = 0; r < KPL; ++r)  // in order: the last store per digit is the count
-            cnt[enc_cnt_at(static_cast<int>((k[r] >> sh) & (ENC_DIGITS - 1)) * ENC_SORT_THREADS + tid)] = rank[r] + 1;
+        for (int kk = 0; kk < ENC_DIGITS / 2; ++kk) {
+            const uint64_t c = kk < 4 ? c0 : c1;
+            const int f = 16 * (kk & 3);
+            cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)] =
+                static_cast<int>(((c >> f) & 0xFFu) | (((c >> (f + 8)) & 0xFFu) << 16));
+        }
         __syncthreads();
+        // exclusive scan of the packed words in (word row, thread) order: thread
+        // t scans words [8 t, 8 t + 8); the halves add without carries (each
+        // stays below 2^15); R(k) = the prefix at the start of word row k
         {
-            int loc[ENC_DIGITS];
+            int loc[ENC_DIGITS / 2];
             int sum = 0;
 #pragma unroll
-            for (int q = 0; q < ENC_DIGITS; ++q) {
-                loc[q] = cnt[enc_cnt_at(tid * ENC_DIGITS + q)];
+            for (int q = 0; q < ENC_DIGITS / 2; ++q) {
+                loc[q] = cnt[enc_cnt_at(tid * (ENC_DIGITS / 2) + q)];
                 sum += loc[q];
             }
-            int before = block_exclusive_scan(sum, warp_sums, nullptr);
+            int total = 0;
+            int before = block_exclusive_scan(sum, warp_sums, &total);
+            if ((tid & (ENC_SORT_THREADS / (ENC_DIGITS / 2) - 1)) == 0)
+                row_start[tid / (ENC_SORT_THREADS / (ENC_DIGITS / 2))] = before;
+            if (tid == 0) row_start[ENC_DIGITS / 2] = total;
 #pragma unroll
-            for (int q = 0; q < ENC_DIGITS; ++q) {
-                cnt[enc_cnt_at(tid * ENC_DIGITS + q)] = before;
+            for (int q = 0; q < ENC_DIGITS / 2; ++q) {
+                cnt[enc_cnt_at(tid * (ENC_DIGITS / 2) + q)] = before;
                 before += loc[q];
             }
         }
         __syncthreads();
+        // digit-major first slot: digit 2k at thread t: low half of P(k, t) plus
+        // the high half of R(k) (all odd digits below); digit 2k + 1: high half
+        // of P(k, t) plus the low half of R(k + 1) (all even digits up to 2k)
 #pragma unroll
-        for (int r = 0; r < KPL; ++r)
-            keys[cnt[enc_cnt_at(static_cast<int>((k[r] >> sh) & (ENC_DIGITS - 1)) * ENC_SORT_THREADS + tid)] + rank[r]] =
-                k[r];
+        for (int r = 0; r < KPL; ++r) {
+            const unsigned d = (k[r] >> sh) & (ENC_DIGITS - 1);
+            const int kk = static_cast<int>(d >> 1);
+            const unsigned pw = static_cast<unsigned>(cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)]);
+            const unsigned first = (d & 1u) ? (pw >> 16) + (static_cast<unsigned>(row_start[kk + 1]) & 0xFFFFu)
+                                            : (pw & 0xFFFFu) + (static_cast<unsigned>(row_start[kk]) >> 16);
+            keys[first + rank[r]] = k[r];
+        }
         __syncthreads();
     }
     if (passes == 0) {  // V == 0: every key is padding
