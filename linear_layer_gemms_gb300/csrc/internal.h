@@ -99,11 +99,19 @@ struct TcParams {
     unsigned long long timeout_ns;
     int sr;                         // stochastic rounding of the bf16 outputs (backward)
     unsigned long long sr_seed;
+    int wide_maps;                  // TC_WIDE_* bits: operands that also have a two-box map
 };
+
+// Operands whose two 64-column halves can arrive in one TMA request.
+constexpr int TC_WIDE_WEIGHT = 1;   // weight: B of dinp (backward), B of the forward
+constexpr int TC_WIDE_DOUT_MN = 2;  // dout: A of dweight
+constexpr int TC_WIDE_INP = 4;      // inp: B of dweight
 
 // Plans (pure functions of the shape and the number of co-resident CTAs,
 // twice the resident CTA pairs). Overrides for tuning and tests come from the
-// environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs).
+// environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs),
+// MMBWD_PPC (CTA pairs per cluster), MMBWD_TILE_N ("dinp,dweight" tile widths);
+// at launch, MMBWD_WIDE_MAPS=0 loads every 64-column box with its own request.
 TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
 
 // Plan of the forward out (BT x OC) = inp (BT x C) . weight^T (+ bias): only

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Three-dimensional box {x, y, z} of a tiled tensor map into shared memory
+// (the box's elements in x-fastest order), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // The same load delivered to the same shared-memory offset in every CTA of
 // `cta_mask` (this GPU's memory only), each receiving the transaction bytes on
 // its barrier at the same offset.

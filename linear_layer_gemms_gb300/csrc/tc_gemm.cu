@@ -248,6 +248,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_inp,      // inp, B of dweight (MN-major)
                     const __grid_constant__ CUtensorMap tm_dinp_out, // dinp, for L2 prefetch of old values
                     const __grid_constant__ CUtensorMap tm_dw_out,   // dweight, likewise
+                    // Both 64-column halves of a B (or dweight A) operand in one request:
+                    // backward, three-dimensional maps {64, rows, extent / 64} whose
+                    // boxes {64, 64, 2} land as two consecutive 64 x 64 boxes; forward,
+                    // weight rows in boxes of 128. Used where p.wide_maps has the bit.
+                    const __grid_constant__ CUtensorMap tm_weight_w,
+                    const __grid_constant__ CUtensorMap tm_dout_mn_w,
+                    const __grid_constant__ CUtensorMap tm_inp_w,
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
     constexpr bool FWD = MODE == 1 || MODE == 2;  // dinp-type items only, K-major B
     constexpr bool X3 = MODE == 2;                // fp32 from three tf32 products
@@ -317,6 +324,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ptx::prefetch_tmap(&tm_weight);
             ptx::prefetch_tmap(&tm_dout_mn);
             ptx::prefetch_tmap(&tm_inp);
+            if (p.wide_maps & TC_WIDE_WEIGHT) ptx::prefetch_tmap(&tm_weight_w);
+            if (p.wide_maps & TC_WIDE_DOUT_MN) ptx::prefetch_tmap(&tm_dout_mn_w);
+            if (p.wide_maps & TC_WIDE_INP) ptx::prefetch_tmap(&tm_inp_w);
             ptx::prefetch_tmap(&tm_dinp_out);
             ptx::prefetch_tmap(&tm_dw_out);
             uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
@@ -374,15 +384,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, &tm_inp, fb, kb * KBLK, col0 + j * 64);
                         }
                     } else if (it.is_dw) {
-                        for (int j = 0; j < na; ++j)
-                            ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * KBLK);
+                        if (na == 2 && (p.wide_maps & TC_WIDE_DOUT_MN))
+                            ptx::tma_load_3d(sA, &tm_dout_mn_w, fb, 0, kb * KBLK, row0 / 64);
+                        else
+                            for (int j = 0; j < na; ++j)
+                                ptx::tma_load_2d(sA + j * BOX_BYTES, &tm_dout_mn, fb, row0 + j * 64, kb * KBLK);
                     } else if (na) {
                         ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * KBLK, row0);
                     }
                     const void* tmB = it.is_dw ? static_cast<const void*>(&tm_inp) : static_cast<const void*>(&tm_weight);
+                    const void* tmBw =
+                        it.is_dw ? static_cast<const void*>(&tm_inp_w) : static_cast<const void*>(&tm_weight_w);
+                    const bool b_wide = nb == 2 && (p.wide_maps & (it.is_dw ? TC_WIDE_INP : TC_WIDE_WEIGHT));
                     // B boxes: 64 columns x 64 k, MN-major (backward) or K-major (forward)
                     if (X3) {
                         // loaded above (one pair per cluster)
+                    } else if (ppc == 1 && b_wide) {
+                        if (FWD) ptx::tma_load_2d(sB, tmBw, fb, kb * KBLK, col0);
+                        else ptx::tma_load_3d(sB, tmBw, fb, 0, kb * KBLK, col0 / 64);
                     } else if (ppc == 1) {
                         for (int j = 0; j < nb; ++j) {
                             if (FWD) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, kb * KBLK, col0 + j * 64);
@@ -818,11 +837,15 @@ long env_long(const char* name, long dflt) {
 // epilogue, whichever is longer, since the two overlap across the two
 // accumulators; the last item's epilogue is not overlapped. Split dweight adds
 // the fixup pass.
-// One k-block of a cluster item (ppc pairs, 256 * ppc rows): load-bound, and two
-// pairs that share B through multicast read a quarter less from L2 per pair.
+// One k-block of a pair (a 256 x bn tile, 64 deep): load-bound. With both
+// 64-column boxes of an operand in one TMA request, a pair alone feeds its
+// k-blocks as fast as two pairs sharing B through multicast (measured on the
+// LM head: 0.37 us per pair k-block either way); what sets the two cluster
+// modes apart is then the number of pairs resident (clusters of four CTAs
+// leave SMs idle) and the granularity of the items.
 double t_kb(int bn, int ppc) {
-    if (ppc == 2) return bn == 256 ? 0.31 : 0.29;
-    return bn == 256 ? 0.37 : 0.33;
+    (void)ppc;
+    return bn == 256 ? 0.31 : 0.29;
 }
 double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
 double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
@@ -961,7 +984,12 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
     const int max_splits = with_dw ? std::max(1, std::min(pl.dw_kb, 16)) : 1;
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
-    for (int ppc = 1; ppc <= 2; ++ppc) {
+    // On a modelled tie the cluster mode tried first keeps the plan: for the
+    // backward two pairs sharing B (measured on the GPT-2 MLP fc layer, 57.0 us
+    // against 58.0 with pairs alone), for the forward pairs alone, whose
+    // 128-row weight requests measured faster (34.1 us against 35.5).
+    for (int t = 0; t < 2; ++t) {
+    const int ppc = with_dw ? 2 - t : 1 + t;
     if (force_ppc && ppc != force_ppc) continue;
     const int max_clusters =
         std::max(1, std::min(ppc == 1 ? num_sms / 2 : num_quads, TC_MAX_PAIRS));
@@ -1100,7 +1128,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     }
     EncodeTiledFn encode = get_encode_tiled();
     if (!encode) return cudaErrorNotSupported;
-    CUtensorMap maps[6];
+    CUtensorMap maps[9];
     for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
         const uint64_t es = mode == 2 ? 4 : 2;
@@ -1112,6 +1140,39 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
                                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, specs[i].swz,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // Two-box maps of maps 1..3 (weight, dout MN-major, inp). Backward: the
+    // MN-major operands as {64 columns, rows, column blocks} with strides
+    // {row pitch, 128 bytes}, box {64, 64, 2}: the two 64-column boxes in the
+    // order the shared-memory stage holds them. Only where the extent is a
+    // multiple of 64, so that the last column block ends at the row's end.
+    // Forward: weight rows in boxes of 128 (two 64-row boxes).
+    p.wide_maps = 0;
+    for (int i = 1; i <= 3; ++i) {
+        maps[5 + i] = maps[i];  // placeholder where unused
+        const MapSpec& m = specs[i];
+        CUresult r = CUDA_SUCCESS;
+        if ((mode == 0 || mode == 3) && m.box_inner == 64 && m.inner >= 64 && m.inner % 64 == 0) {
+            const cuuint64_t dims[3] = {64, m.outer, m.inner / 64};
+            const cuuint64_t strides[2] = {m.pitch ? m.pitch : m.inner * 2, 128};
+            const cuuint32_t box[3] = {64, m.box_outer, 2};
+            const cuuint32_t estr[3] = {1, 1, 1};
+            r = encode(&maps[5 + i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(m.base), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, m.swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else if (mode == 1 && i == 1) {
+            const cuuint64_t dims[2] = {m.inner, m.outer};
+            const cuuint64_t strides[1] = {m.pitch ? m.pitch : m.inner * 2};
+            const cuuint32_t box[2] = {m.box_inner, 2 * m.box_outer};
+            const cuuint32_t estr[2] = {1, 1};
+            r = encode(&maps[5 + i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(m.base), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, m.swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            continue;
+        }
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (env_long("MMBWD_WIDE_MAPS", 1)) p.wide_maps |= 1 << (i - 1);
     }
     p.dinp_bn = plan.dinp_bn;
     p.dw_bn = plan.dw_bn;
@@ -1147,16 +1208,16 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (mode == 2)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
                                plan.sched);
     else if (mode == 1)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
                                plan.sched);
     else if (mode == 3)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
                                plan.sched);
     else
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
                                plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     cudaLaunchConfig_t fcfg{};

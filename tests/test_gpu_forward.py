@@ -71,6 +71,20 @@ def test_forward_cluster_modes(monkeypatch, ppc, tile_n):
     assert_close(to_host(out, "bf16"), ref, "bf16", "out")
 
 
+def test_forward_two_box_requests(monkeypatch):
+    """One cluster pair: the two 64-row weight boxes of a stage in one request
+    of 128 rows (ragged OC, so the last request reads past the rows); bitwise
+    equal to one request per box."""
+    BT, C, OC = 600, 520, 776
+    monkeypatch.setenv("MMBWD_PPC", "1")
+    monkeypatch.setenv("MMBWD_TILE_N", "256,256")
+    x = inputs(BT, C, OC, "bf16", seed=4)
+    wide = to_host(run_fwd(x, BT, C, OC, "bf16"), "bf16")
+    monkeypatch.setenv("MMBWD_WIDE_MAPS", "0")
+    narrow = to_host(run_fwd(x, BT, C, OC, "bf16"), "bf16")
+    assert np.array_equal(wide, narrow)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_forward_integer_case_exact(dtype):
     g = json.load(open(os.path.join(GOLDEN, "int_case.json")))

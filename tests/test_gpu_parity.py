@@ -240,3 +240,24 @@ def test_pairs_per_cluster(monkeypatch, ppc, tile_n, splits):
     g1, _ = check_full(x, B, T, C, OC, "bf16")
     for k in ("dinp", "dweight", "dbias"):
         assert np.array_equal(to_host(g0[k], "bf16"), to_host(g1[k], "bf16")), k
+
+
+@pytest.mark.parametrize("ppc", [1, 2])
+@pytest.mark.parametrize("tile_n", ["256,256", "128,128"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_two_box_requests(monkeypatch, ppc, tile_n, splits):
+    """Where an MN-major operand's extent is a multiple of 64, both 64-column
+    boxes of a stage may arrive in one three-dimensional TMA request; the last
+    column block of C and the last 128 rows of OC (extents 5 and 11 times 64)
+    still take the one-box loads. Within tolerance of the oracle, and bitwise
+    equal to the run with one request per box."""
+    B, T, C, OC = 2, 300, 320, 704
+    monkeypatch.setenv("MMBWD_PPC", str(ppc))
+    monkeypatch.setenv("MMBWD_TILE_N", tile_n)
+    monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+    _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
+    g1, _ = check_full(x, B, T, C, OC, "bf16")
+    monkeypatch.setenv("MMBWD_WIDE_MAPS", "0")
+    g0, _ = check_full(x, B, T, C, OC, "bf16")
+    for k in ("dinp", "dweight", "dbias"):
+        assert np.array_equal(to_host(g0[k], "bf16"), to_host(g1[k], "bf16")), k
