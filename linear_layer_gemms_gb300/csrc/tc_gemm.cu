@@ -311,9 +311,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     ptx::cluster_sync();  // every CTA's barriers exist before any remote arrive or multicast
     ptx::tc_fence_after();
-    // Everything above overlaps the previous launch on the stream; global memory
-    // is touched only after it has completed.
-    ptx::grid_dependency_wait();
+    // Everything above overlaps the previous launch on the stream. Threads that
+    // touch global memory wait for it to complete first: the epilogue warps
+    // here, the producer only just ahead of its first load, so that its first
+    // item's schedule entry, geometry and barrier steps (first-touch latencies
+    // of about 2 us in all) also overlap the previous launch. The MMA and bias
+    // warps read only shared and tensor memory.
+    const bool defer_wait = warp < WARP_EPI;
+    if (!defer_wait) ptx::grid_dependency_wait();
     const uint32_t tmem_base = misc[0];
     const Waiter wt{misc + 1, p.timeout_ns};
 
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ptx::prefetch_tmap(&tm_dinp_out);
             ptx::prefetch_tmap(&tm_dw_out);
             uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
-            bool ok = true;
+            bool ok = true, waited = false;
             for (int r = 0; ok; ++r) {
                 const int w = item_at(p, sch, r);
                 if (w >= p.n_items) break;
@@ -367,6 +372,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint32_t sB = sA + (X3 ? 2 : 1) * A_BYTES;
                     const uint32_t fb = bars + 8u * (BAR_FULL + stage);
                     ptx::mbar_arrive_expect_tx(fb, bytes);
+                    if (!waited) {  // the previous launch has completed before any load
+                        ptx::grid_dependency_wait();
+                        waited = true;
+                    }
                     if (direct && kb == pf_kb && row0 < out_rows) {
                         for (int j = 0; j < it.bn / 128; ++j)
                             if (it.n_tile * it.bn + j * 128 < n_extent)
