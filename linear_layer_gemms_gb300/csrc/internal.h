@@ -36,6 +36,7 @@ enum WaitSite : int {
     SITE_TEARDOWN = 8,
     SITE_SELFTEST = 9,
     SITE_FORWARD_FULL = 10,
+    SITE_EPI_OLD = 11,
 };
 
 // Schedule of a launch: which work items each cluster (one or two CTA pairs)

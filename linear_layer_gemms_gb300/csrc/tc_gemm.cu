@@ -87,13 +87,21 @@ constexpr int BAR_TEMPTY = 2 * TC_STAGES + 2;  // [2] accumulator drained by bot
 constexpr int BAR_EPIDONE = 2 * TC_STAGES + 4; // [2] this CTA's epilogue finished an item
 constexpr int BAR_BIAS = 2 * TC_STAGES + 6;    // [2] bias sums ready
 constexpr int BAR_TEARDOWN = 2 * TC_STAGES + 8;
-constexpr int N_BARS = 2 * TC_STAGES + 9;
+constexpr int OLD_SLOTS = 4;                   // old-value chunk buffers per epilogue warp
+constexpr int BAR_OLD = 2 * TC_STAGES + 9;     // [epilogue warp][slot] old chunk landed
+constexpr int N_BARS = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;
 constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag, [2] broadcast
 constexpr int OFF_BIAS = (OFF_MISC + 16 + 127) & ~127;
 constexpr int STG_STRIDE = 36;  // floats per staged row: 16-byte aligned, conflict-free
 constexpr int STG_WARP_BYTES = 32 * STG_STRIDE * 4;
-constexpr int OFF_STAGE = OFF_BIAS + 2 * TC_BM * 4;
-constexpr int SMEM_USED = OFF_STAGE + NUM_EPI_WARPS * STG_WARP_BYTES;
+// bf16 read-modify-write through TMA: a 32-row x 32-column chunk of the output
+// (2 KB, rows of 64 bytes, 64-byte swizzle), OLD_SLOTS of them per warp. The
+// fp32 staging of the other epilogues uses the same region.
+constexpr int OLD_CHUNK_BYTES = 32 * 32 * 2;
+constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
+constexpr int OFF_STAGE = (OFF_BIAS + 2 * TC_BM * 4 + 1023) & ~1023;
+constexpr int STAGE_REGION = NUM_EPI_WARPS * (STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES);
+constexpr int SMEM_USED = OFF_STAGE + STAGE_REGION;
 constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
 
@@ -255,6 +263,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_weight_w,
                     const __grid_constant__ CUtensorMap tm_dout_mn_w,
                     const __grid_constant__ CUtensorMap tm_inp_w,
+                    // dinp and dweight in 32 x 32 boxes, 64-byte swizzle: the bf16
+                    // read-modify-write of the backward (MODE 0 and 3)
+                    const __grid_constant__ CUtensorMap tm_dinp_rmw,
+                    const __grid_constant__ CUtensorMap tm_dw_rmw,
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
     constexpr bool FWD = MODE == 1 || MODE == 2;  // dinp-type items only, K-major B
     constexpr bool X3 = MODE == 2;                // fp32 from three tf32 products
@@ -300,6 +312,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ptx::mbar_init(bars + 8u * (BAR_BIAS + a), NUM_BIAS_WARPS);
         }
         ptx::mbar_init(bars + 8u * BAR_TEARDOWN, 1);
+        for (int b = 0; b < NUM_EPI_WARPS * OLD_SLOTS; ++b) ptx::mbar_init(bars + 8u * (BAR_OLD + b), 1);
         misc[1] = 0u;
         ptx::fence_mbar_init();
     }
@@ -618,6 +631,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int r8 = lane >> 2;       // coalesced phase: rows 8i + r8 of the quadrant,
         const int cg = (lane & 3) * 8;  //   columns cg..cg+7 of each 32-column chunk
         const uint32_t stg = base + OFF_STAGE + q * STG_WARP_BYTES;
+        // bf16 read-modify-write (MODE 0 and 3, unsplit items): this warp's
+        // ring of old-value chunks, their barriers, parities and pending loads
+        const uint32_t oldbuf = base + OFF_STAGE + q * OLD_WARP_BYTES;
+        const uint32_t oldbar0 = bars + 8u * (BAR_OLD + q * OLD_SLOTS);
+        uint32_t oldpar = 0, oldpend = 0;
         const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, pair_leader);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t bias_parity[2] = {0u, 0u};
@@ -646,23 +664,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 drow[i] = D + (rok[i] ? row : 0) * n_extent + col0 + cg;
                 drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
-            // All old output values of this tile (the backward; the producer has
-            // prefetched them into L2), or the bias columns of the tile (the bf16
-            // forward, in oldw[c][0]), loaded before waiting for the accumulator.
-            uint4 oldw[TC_BN / 32][4];
-#pragma unroll
-            for (int c = 0; c < TC_BN / 32; ++c)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if constexpr (FWD && !X3)
-                        oldw[c][i] = (i == 0 && p.fwd_bias && c < nchunks && c * 32 + cg < ncols)
-                                         ? *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-                    else
-                        oldw[c][i] = (!X3 && !split_mode && c < nchunks && rok[i] && c * 32 + cg < ncols)
-                                         ? *reinterpret_cast<const uint4*>(drow[i] + c * 32)
-                                         : make_uint4(0u, 0u, 0u, 0u);
+            // The backward's bf16 read-modify-write goes through TMA: the old
+            // values of this warp's 32 rows arrive in 32-column chunks (the first
+            // OLD_SLOTS requested before waiting for the accumulator; the
+            // producer has prefetched the tile into L2), each thread adds its own
+            // row in place, and the chunk goes back out with one bulk store. Rows
+            // and columns outside the tensor read as zero and are not stored.
+            const bool tma_rmw = !FWD && !X3 && !split_mode;
+            const void* tmo = it.is_dw ? static_cast<const void*>(&tm_dw_rmw) : static_cast<const void*>(&tm_dinp_rmw);
+            const int nvc = (ncols + 31) / 32;  // chunks holding columns of the tensor
+            const bool qvalid = qrow0 < rows_total;
+            if (tma_rmw && qvalid && lane == 0) {
+                for (int c = 0; c < OLD_SLOTS && c < nvc; ++c) {
+                    const uint32_t b = oldbar0 + 8u * c;
+                    ptx::mbar_arrive_expect_tx(b, OLD_CHUNK_BYTES);
+                    ptx::tma_load_2d(oldbuf + c * OLD_CHUNK_BYTES, tmo, b, col0 + c * 32, static_cast<int32_t>(qrow0));
+                    oldpend |= 1u << c;
                 }
+            }
+            // The forward: the bias columns of the tile, loaded before waiting for
+            // the accumulator.
+            uint4 bias8[TC_BN / 32];
+#pragma unroll
+            for (int c = 0; c < TC_BN / 32; ++c) {
+                if constexpr (FWD && !X3)
+                    bias8[c] = (p.fwd_bias && c < nchunks && c * 32 + cg < ncols)
+                                   ? *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                else
+                    bias8[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
 
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
@@ -679,9 +710,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.dw_tiles_n + it.n_tile) * p.splits +
                                                      it.split) * (TC_BM * p.dw_bn)
                                      : nullptr;
+            if (tma_rmw && qvalid) {
+                const uint64_t t_sr = it.is_dw ? sr::DWEIGHT : sr::DINP;
+                // 16-byte granule g of row `lane` sits at granule g ^ ((lane >> 1) & 3)
+                // (64-byte swizzle; conflict-free across each 8-thread phase)
+                const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll 1
+                for (int c = 0; c < nvc; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tbase + c * 32, v);
+                    const int slot = c & (OLD_SLOTS - 1);
+                    const uint32_t b = oldbar0 + 8u * slot;
+                    if (!wt.wait_warp(b, (oldpar >> slot) & 1u, SITE_EPI_OLD, w)) {
+                        ok = false;
+                        break;
+                    }
+                    oldpar ^= 1u << slot;
+                    oldpend &= ~(1u << slot);
+                    const uint32_t rowaddr = oldbuf + slot * OLD_CHUNK_BYTES + lane * 64;
+                    const uint64_t e_row = static_cast<uint64_t>(qrow0 + lane) * n_extent + col0 + c * 32;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const uint32_t a = rowaddr + ((static_cast<uint32_t>(g) ^ swz) << 4);
+                        const uint4 o = ptx::lds128(a);
+                        float s8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s8[e] = __uint_as_float(v[8 * g + e]);
+                        uint4 res;
+                        if constexpr (SR)
+                            res = add_sr8(o, s8, sr::word(p.sr_seed, t_sr, e_row + 8 * g),
+                                          sr::word(p.sr_seed, t_sr, e_row + 8 * g + 4));
+                        else
+                            res = add_round8(o, s8);
+                        ptx::sts128u(a, res);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(tmo, oldbuf + slot * OLD_CHUNK_BYTES, col0 + c * 32, static_cast<int32_t>(qrow0));
+                        ptx::bulk_commit_group();
+                        // Refill the previous chunk's slot with chunk c + OLD_SLOTS - 1
+                        // once that chunk's store (committed an iteration ago) has
+                        // read it; this chunk's store stays in flight.
+                        const int cn = c + OLD_SLOTS - 1;
+                        if (c >= 1 && cn < nvc) {
+                            const int sn = cn & (OLD_SLOTS - 1);
+                            const uint32_t bn_ = oldbar0 + 8u * sn;
+                            ptx::bulk_wait_read_but_last();
+                            ptx::mbar_arrive_expect_tx(bn_, OLD_CHUNK_BYTES);
+                            ptx::tma_load_2d(oldbuf + sn * OLD_CHUNK_BYTES, tmo, bn_, col0 + cn * 32,
+                                             static_cast<int32_t>(qrow0));
+                            oldpend |= 1u << sn;
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) ptx::bulk_wait_read_all();  // the chunks are free for the next item
+                __syncwarp();
+            }
+            if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c) {
-                if (c >= nchunks) break;
+                if (tma_rmw || c >= nchunks) break;
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
                 // Row `lane` of the quadrant into the staging buffer ...
@@ -711,17 +801,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             dp[0] = o0;
                             dp[1] = o1;
                         }
-                    } else if (rok[i] && c * 32 + cg < ncols) {
-                        float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-                        // backward: the old value; forward: the bias (zero without one)
-                        const uint4 base8 = FWD ? oldw[c][0] : oldw[c][i];
-                        if constexpr (SR) {
-                            const uint64_t e0 = static_cast<uint64_t>(qrow0 + 8 * i + r8) * n_extent + col0 + c * 32 + cg;
-                            const uint64_t t = it.is_dw ? sr::DWEIGHT : sr::DINP;
-                            *reinterpret_cast<uint4*>(drow[i] + c * 32) =
-                                add_sr8(base8, s8, sr::word(p.sr_seed, t, e0), sr::word(p.sr_seed, t, e0 + 4));
-                        } else {
-                            *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(base8, s8);
+                    } else if constexpr (FWD && !X3) {
+                        if (rok[i] && c * 32 + cg < ncols) {  // forward: the bias (zero without one)
+                            float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+                            *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(bias8[c], s8);
                         }
                     }
                 }
@@ -749,6 +832,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 acc_phase ^= 1u;
             }
         }
+        // Old-value loads still in flight (only after an abort) land, and every
+        // bulk store has completed, before shared memory goes away.
+        if (lane == 0) {
+            for (int sl = 0; sl < OLD_SLOTS; ++sl)
+                if ((oldpend >> sl) & 1u) wt.wait_teardown(oldbar0 + 8u * sl, (oldpar >> sl) & 1u);
+            ptx::bulk_wait_all();
+        }
+        __syncwarp();
     }
 
     // Each thread is done with its role: the next launch on the stream may start
@@ -1137,7 +1228,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     }
     EncodeTiledFn encode = get_encode_tiled();
     if (!encode) return cudaErrorNotSupported;
-    CUtensorMap maps[9];
+    CUtensorMap maps[11];
     for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
         const uint64_t es = mode == 2 ? 4 : 2;
@@ -1183,6 +1274,21 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         if (env_long("MMBWD_WIDE_MAPS", 1)) p.wide_maps |= 1 << (i - 1);
     }
+    // Output maps of the backward's bf16 read-modify-write (maps 4 and 5 give
+    // the tensors and their extents): boxes of 32 columns x 32 rows.
+    for (int i = 0; i < 2; ++i) {
+        maps[9 + i] = maps[4 + i];  // placeholder where unused
+        if (mode != 0 && mode != 3) continue;
+        const MapSpec& m = specs[4 + i];
+        const cuuint64_t dims[2] = {m.inner, m.outer};
+        const cuuint64_t strides[1] = {m.inner * 2};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult r = encode(&maps[9 + i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(m.base), dims,
+                                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     p.dinp_bn = plan.dinp_bn;
     p.dw_bn = plan.dw_bn;
     p.dinp_tiles_n = plan.dinp_tiles_n;
@@ -1217,16 +1323,16 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (mode == 2)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
                                plan.sched);
     else if (mode == 1)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
                                plan.sched);
     else if (mode == 3)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
                                plan.sched);
     else
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
                                plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     cudaLaunchConfig_t fcfg{};
