@@ -118,6 +118,13 @@ __device__ __forceinline__ void bulk_wait_read_but_last() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Every committed bulk store of this thread but the most recent N (a
+// compile-time constant) has finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_but_n() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -636,6 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t oldbuf = base + OFF_STAGE + q * OLD_WARP_BYTES;
         const uint32_t oldbar0 = bars + 8u * (BAR_OLD + q * OLD_SLOTS);
         uint32_t oldpar = 0, oldpend = 0;
+        uint32_t fwd_chunks = 0;  // forward: chunks this warp has stored (slot = count mod OLD_SLOTS)
         const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, pair_leader);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t bias_parity[2] = {0u, 0u};
@@ -671,9 +672,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // row in place, and the chunk goes back out with one bulk store. Rows
             // and columns outside the tensor read as zero and are not stored.
             const bool tma_rmw = !FWD && !X3 && !split_mode;
+            constexpr bool TMA_FWD = FWD && !X3;  // the forward's stores through TMA as well
             const void* tmo = it.is_dw ? static_cast<const void*>(&tm_dw_rmw) : static_cast<const void*>(&tm_dinp_rmw);
             const int nvc = (ncols + 31) / 32;  // chunks holding columns of the tensor
             const bool qvalid = qrow0 < rows_total;
+            if constexpr (!FWD && !X3) {
+                // the previous item's stores have read the chunk buffers (also the
+                // staging area of a split item)
+                if (lane == 0) ptx::bulk_wait_read_all();
+                __syncwarp();
+            }
             if (tma_rmw && qvalid && lane == 0) {
                 for (int c = 0; c < OLD_SLOTS && c < nvc; ++c) {
                     const uint32_t b = oldbar0 + 8u * c;
@@ -681,18 +689,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ptx::tma_load_2d(oldbuf + c * OLD_CHUNK_BYTES, tmo, b, col0 + c * 32, static_cast<int32_t>(qrow0));
                     oldpend |= 1u << c;
                 }
-            }
-            // The forward: the bias columns of the tile, loaded before waiting for
-            // the accumulator.
-            uint4 bias8[TC_BN / 32];
-#pragma unroll
-            for (int c = 0; c < TC_BN / 32; ++c) {
-                if constexpr (FWD && !X3)
-                    bias8[c] = (p.fwd_bias && c < nchunks && c * 32 + cg < ncols)
-                                   ? *reinterpret_cast<const uint4*>(p.fwd_bias + col0 + c * 32 + cg)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-                else
-                    bias8[c] = make_uint4(0u, 0u, 0u, 0u);
             }
 
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
@@ -765,13 +761,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     __syncwarp();
                 }
-                if (lane == 0) ptx::bulk_wait_read_all();  // the chunks are free for the next item
-                __syncwarp();
+            }
+            if (TMA_FWD && qvalid) {
+                // out = acc + bias, rounded once, row by row into a chunk buffer and
+                // out with one bulk store; a buffer is rewritten once the store that
+                // used it OLD_SLOTS chunks ago has read it.
+                const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll 1
+                for (int c = 0; c < nvc; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tbase + c * 32, v);
+                    const uint32_t slot = fwd_chunks & (OLD_SLOTS - 1);
+                    if (fwd_chunks >= OLD_SLOTS && lane == 0) ptx::bulk_wait_read_but_n<OLD_SLOTS - 1>();
+                    __syncwarp();
+                    const uint32_t rowaddr = oldbuf + slot * OLD_CHUNK_BYTES + lane * 64;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int cc = col0 + c * 32 + 8 * g;
+                        const uint4 b8 = (p.fwd_bias && cc < n_extent)
+                                             ? __ldg(reinterpret_cast<const uint4*>(p.fwd_bias + cc))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        float s8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) s8[e] = __uint_as_float(v[8 * g + e]);
+                        ptx::sts128u(rowaddr + ((static_cast<uint32_t>(g) ^ swz) << 4), add_round8(b8, s8));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(tmo, oldbuf + slot * OLD_CHUNK_BYTES, col0 + c * 32, static_cast<int32_t>(qrow0));
+                        ptx::bulk_commit_group();
+                    }
+                    ++fwd_chunks;
+                }
             }
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c) {
-                if (tma_rmw || c >= nchunks) break;
+                if (tma_rmw || TMA_FWD || c >= nchunks) break;
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
                 // Row `lane` of the quadrant into the staging buffer ...
@@ -800,11 +827,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
                             dp[0] = o0;
                             dp[1] = o1;
-                        }
-                    } else if constexpr (FWD && !X3) {
-                        if (rok[i] && c * 32 + cg < ncols) {  // forward: the bias (zero without one)
-                            float s8[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
-                            *reinterpret_cast<uint4*>(drow[i] + c * 32) = add_round8(bias8[c], s8);
                         }
                     }
                 }
@@ -1274,11 +1296,11 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
         if (env_long("MMBWD_WIDE_MAPS", 1)) p.wide_maps |= 1 << (i - 1);
     }
-    // Output maps of the backward's bf16 read-modify-write (maps 4 and 5 give
-    // the tensors and their extents): boxes of 32 columns x 32 rows.
+    // Output maps of the bf16 epilogues (maps 4 and 5 give the tensors and
+    // their extents): boxes of 32 columns x 32 rows.
     for (int i = 0; i < 2; ++i) {
         maps[9 + i] = maps[4 + i];  // placeholder where unused
-        if (mode != 0 && mode != 3) continue;
+        if (mode == 2 || (mode == 1 && i == 1)) continue;  // the forward writes through map 9
         const MapSpec& m = specs[4 + i];
         const cuuint64_t dims[2] = {m.inner, m.outer};
         const cuuint64_t strides[1] = {m.inner * 2};
