@@ -992,9 +992,11 @@ ItemCost item_cost(const TcPlan& pl, int w) {
 double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
     if (pl.splits == 1) return 0.0;
     // a launch gap plus S fp32 partials read and dweight read and written, and
-    // the partial stores; measured, the pass costs about twice the traffic time
+    // the partial stores (L2-resident: 4 MB/us; with this, the GPT-2 attention
+    // projection takes the plan that measured fastest, single pairs and 4 splits,
+    // 30.4 us against 31.4 with 3 splits and 32.2 with two pairs and 3 splits)
     const double bytes = static_cast<double>(OC) * C * (4.0 * pl.splits + 4.0);
-    return 6.0 + bytes / 2.5e6;
+    return 6.0 + bytes / 4e6;
 }
 
 // Longest-first greedy assignment of items to pairs; fills pl.sched and
