@@ -20,15 +20,27 @@ namespace sr {
 
 enum : uint32_t { DINP = 0, DWEIGHT = 1, DBIAS = 2, DWTE = 3, DWPE = 4 };
 
-__device__ __forceinline__ uint64_t sm64_out(uint64_t seed, uint64_t n) {
-    uint64_t z = seed + (n + 1) * 0x9E3779B97F4A7C15ull;
+constexpr uint64_t SM64_GAMMA = 0x9E3779B97F4A7C15ull;
+
+// The output function applied to the state seed + (n + 1) * gamma.
+__device__ __forceinline__ uint64_t sm64_mix(uint64_t z) {
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
 }
 
+__device__ __forceinline__ uint64_t sm64_out(uint64_t seed, uint64_t n) {
+    return sm64_mix(seed + (n + 1) * SM64_GAMMA);
+}
+
 __device__ __forceinline__ uint64_t word(uint64_t seed, uint64_t tensor, uint64_t e) {
     return sm64_out(seed, (tensor << 58) | (e >> 2));
+}
+
+// State of the word of element e (a multiple of 4): the words of elements
+// e + 4 j follow as sm64_mix(state + j * gamma).
+__device__ __forceinline__ uint64_t word_state(uint64_t seed, uint64_t tensor, uint64_t e) {
+    return seed + (((tensor << 58) | (e >> 2)) + 1) * SM64_GAMMA;
 }
 
 __device__ __forceinline__ uint32_t threshold(uint64_t seed, uint64_t tensor, uint64_t e) {

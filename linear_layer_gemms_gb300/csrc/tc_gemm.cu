@@ -724,7 +724,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     oldpar ^= 1u << slot;
                     oldpend &= ~(1u << slot);
                     const uint32_t rowaddr = oldbuf + slot * OLD_CHUNK_BYTES + lane * 64;
+                    // the row's 32 columns start at element e_row (a multiple of 8:
+                    // C is), so their eight words have consecutive counters
                     const uint64_t e_row = static_cast<uint64_t>(qrow0 + lane) * n_extent + col0 + c * 32;
+                    const uint64_t z0 = SR ? sr::word_state(p.sr_seed, t_sr, e_row) : 0;
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const uint32_t a = rowaddr + ((static_cast<uint32_t>(g) ^ swz) << 4);
@@ -734,8 +737,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int e = 0; e < 8; ++e) s8[e] = __uint_as_float(v[8 * g + e]);
                         uint4 res;
                         if constexpr (SR)
-                            res = add_sr8(o, s8, sr::word(p.sr_seed, t_sr, e_row + 8 * g),
-                                          sr::word(p.sr_seed, t_sr, e_row + 8 * g + 4));
+                            res = add_sr8(o, s8, sr::sm64_mix(z0 + (2 * g) * sr::SM64_GAMMA),
+                                          sr::sm64_mix(z0 + (2 * g + 1) * sr::SM64_GAMMA));
                         else
                             res = add_round8(o, s8);
                         ptx::sts128u(a, res);
