@@ -653,16 +653,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int64_t n_extent = FWD ? p.n_dinp : p.C;  // columns and row stride of D
             const int ncols = static_cast<int>(min(static_cast<int64_t>(it.bn), n_extent - col0));
             const int nchunks = it.bn / 32;
-            __nv_bfloat16* D = it.is_dw ? p.dweight : p.dinp;
-            float* Df = reinterpret_cast<float*>(D);  // MODE 2: fp32 output
+            float* Df = reinterpret_cast<float*>(it.is_dw ? p.dweight : p.dinp);  // MODE 2: fp32 output
+            // fp32 read-modify-write (MODE 2): this thread's rows of the coalesced phase
             bool rok[4];
-            __nv_bfloat16* drow[4];
             float* drowf[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int64_t row = qrow0 + 8 * i + r8;
                 rok[i] = row < rows_total;
-                drow[i] = D + (rok[i] ? row : 0) * n_extent + col0 + cg;
                 drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
             // The backward's bf16 read-modify-write goes through TMA: the old
