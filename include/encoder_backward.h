@@ -55,7 +55,8 @@ extern "C" {
  * Returns MMBWD_OK or a negative MMBWD_ERR_* code (nothing enqueued on an
  * error): ERR_NULL, ERR_DTYPE, ERR_SHAPE (a size out of range), ERR_ALIGN
  * (dwte, dwpe, dout not 16-byte aligned or C times the element size not a
- * multiple of 16 bytes; inp not 4-byte aligned), ERR_ALIAS, ERR_ALLOC /
+ * multiple of 16 bytes; inp not 4-byte aligned), ERR_ALIAS, ERR_MEMORY (a
+ * non-empty tensor not in device memory of the current device), ERR_ALLOC /
  * ERR_CAPTURE (the shared workspace). A token id outside [0, V) is skipped by
  * the kernels and reported as MMBWD_ERR_SHAPE by mmbwd_device_status().
  * B*T == 0, C == 0 enqueue nothing.
@@ -96,7 +97,7 @@ int encbwd_run_sr(void* dwte, void* dwpe, const void* dout, const int32_t* inp, 
  *              left out and reported by mmbwd_device_status()
  *   B, T, C, V, dtype   as encbwd_run (C and dtype fix the plan's counters and
  *              the alignment rule)
- *   Errors as encbwd_run (ERR_NULL, ERR_ALIGN, ERR_ALIAS, ERR_SHAPE, ...).
+ *   Errors as encbwd_run (ERR_NULL, ERR_ALIGN, ERR_ALIAS, ERR_SHAPE, ERR_MEMORY, ...).
  *
  * encbwd_run_planned -- enqueue dwte += ..., dwpe += ... from a plan.
  *   dwte, dwpe, dout, B, T, C, V, dtype   as encbwd_run

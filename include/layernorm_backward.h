@@ -71,7 +71,8 @@ extern "C" {
  * limit. MMBWD_ERR_ALIGN: a tensor pointer not 16-byte aligned, mean or rstd
  * not 4-byte aligned, or C times the element size not a multiple of 16 bytes.
  * MMBWD_ERR_ALIAS: an output overlaps an input or another output.
- * MMBWD_ERR_ALLOC / MMBWD_ERR_CAPTURE: the shared workspace (per-block fp32
+ * MMBWD_ERR_MEMORY: a non-empty tensor is not device memory of the current
+ * device. MMBWD_ERR_ALLOC / MMBWD_ERR_CAPTURE: the shared workspace (per-block fp32
  * partial sums, lnbwd_workspace_bytes) could not grow, or would have to grow
  * during stream capture. B*T == 0 or C == 0 enqueue nothing (empty sums).
  *

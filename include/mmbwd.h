@@ -59,6 +59,10 @@ extern "C" {
 #define MMBWD_ERR_ARCH (-9)           /* the current device is not sm_103 */
 #define MMBWD_ERR_CAPTURE (-10)       /* the workspace would have to grow while the
                                          stream is being captured into a CUDA graph */
+#define MMBWD_ERR_MEMORY (-12)        /* a non-empty tensor does not lie in device memory
+                                         of the current device (host memory, pinned or
+                                         mapped host memory, managed memory, or memory
+                                         of another GPU) */
 
 /*
  * mmbwd_run -- enqueue the whole backward pass of one linear layer on `stream`.
@@ -79,10 +83,13 @@ extern "C" {
  * needed. Layout: row-major, contiguous, no strides.
  *
  * Ownership: the caller owns every buffer; the library never frees them.
- * Outputs must not overlap inputs or each other (MMBWD_ERR_ALIAS); inputs may
- * overlap each other. Pointers must be 16-byte aligned, and C and OC times the
- * element size must be multiples of 16 bytes (MMBWD_ERR_ALIGN). A pointer may
- * be NULL only when its tensor has no elements.
+ * Every non-empty tensor must be device memory of the current device: its
+ * first and last bytes are checked with cudaPointerGetAttributes, and host,
+ * managed or another GPU's memory gives MMBWD_ERR_MEMORY with nothing
+ * enqueued. Outputs must not overlap inputs or each other (MMBWD_ERR_ALIAS);
+ * inputs may overlap each other. Pointers must be 16-byte aligned, and C and
+ * OC times the element size must be multiples of 16 bytes (MMBWD_ERR_ALIGN).
+ * A pointer may be NULL only when its tensor has no elements.
  *
  * Workspace: the bf16 path may need a library-owned fp32 workspace for its
  * split reduction, and the fp32 tensor-core path one for the split operands
@@ -161,12 +168,11 @@ int mmbwd_version(void);
  * and the number of co-resident CTAs; num_sms <= 0 takes the current device's
  * value, or 152 without a usable device). out[0..n) receives, in order: path (0 = fp32 SIMT,
  * 1 = bf16 tensor-core, 2 = fp32 from three tf32 products), grid size (CTAs), work items, dweight splits, k-blocks
- * per split, dinp tiles, dweight tiles, schedule kind (1 = per-cluster tables),
- * tile M (rows per cluster), tile N of dinp, tile N of dweight, tile K,
- * pipeline stages, kernel launches per call, CTA pairs per cluster. num_sms
- * stands for the resident CTAs; a quarter of it is taken as the resident
- * 4-CTA clusters. Returns the number of values written (at most 15), or a
- * negative status. */
+ * per split, dinp tiles, dweight tiles, schedule kind (1 = per-pair tables),
+ * tile M (rows per CTA pair), tile N of dinp, tile N of dweight, tile K,
+ * pipeline stages, kernel launches per call, CTA pairs per cluster (always 1:
+ * a cluster is one CTA pair). num_sms stands for the resident CTAs. Returns
+ * the number of values written (at most 15), or a negative status. */
 int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms,
                     int* out, int n);
 
@@ -215,8 +221,8 @@ void mmbwd_debug_fail_next_alloc(int n);
 #define MMBWD_ERR_SCRATCH (-11) /* the problem needs more scratch than that buffer holds */
 
 /*
- * mmbwd_run_static_scratch -- the same operation, arguments, layout, errors and
- * results as mmbwd_run, for callers that must not allocate device memory.
+ * mmbwd_run_static_scratch -- the operation of mmbwd_run, with its arguments,
+ * layout and errors, for callers that must not allocate device memory.
  * The paper has no counterpart: this entry point exists only for such callers.
  *
  * Who needs it: code that runs where device allocation is unavailable or not
@@ -227,13 +233,21 @@ void mmbwd_debug_fail_next_alloc(int n);
  * cudaMalloc; this entry point never calls cudaMalloc, cudaFree or any other
  * allocating routine.
  *
- * Instead, the split reduction of the bf16 path uses one fixed buffer of
- * MMBWD_STATIC_SCRATCH_BYTES compiled into the library (a file-scope device
- * array, so every GPU that loads the library holds it until the process
- * exits). A problem whose work split needs more than that returns
- * MMBWD_ERR_SCRATCH and enqueues nothing; mmbwd_workspace_bytes() tells the
- * need in advance. Nothing in the buffer has to start at zero: every value a
- * call reads there is written earlier by the same call.
+ * bf16: the plan, the kernels and so the results are those of mmbwd_run; the
+ * split reduction uses one fixed buffer of MMBWD_STATIC_SCRATCH_BYTES compiled
+ * into the library (a file-scope device array, so every GPU that loads the
+ * library holds it until the process exits) instead of the grown workspace.
+ * A problem whose work split needs more than that returns MMBWD_ERR_SCRATCH
+ * and enqueues nothing; for bf16, mmbwd_workspace_bytes() gives the need in
+ * advance. Nothing in the buffer has to start at zero: every value a call
+ * reads there is written earlier by the same call.
+ *
+ * fp32: always the fp32 fused-multiply-add kernel, which needs no scratch at
+ * all (the three-tf32-product path of mmbwd_run needs a workspace far larger
+ * than the fixed buffer). Where mmbwd_run takes that tensor-core path (large
+ * layers), results here differ from its results in the last bits (both are
+ * fp32-accurate) and the call is several times slower; mmbwd_workspace_bytes()
+ * reports that path's workspace, which this entry point does not use.
  *
  * All calls on a device share the one buffer, which keeps whatever the last
  * call left in it: calls that overlap on the GPU (for example on two streams

@@ -30,7 +30,7 @@ BF16 = 1
 OK = 0
 ERR_NULL, ERR_DTYPE, ERR_SHAPE, ERR_ALIGN, ERR_ALIAS = -1, -2, -3, -4, -5
 ERR_ALLOC, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_ARCH, ERR_CAPTURE = -6, -7, -8, -9, -10
-ERR_SCRATCH = -11
+ERR_SCRATCH, ERR_MEMORY = -11, -12
 STATIC_SCRATCH_BYTES = 32 << 20  # MMBWD_STATIC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

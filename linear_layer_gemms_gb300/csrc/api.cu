@@ -41,7 +41,6 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     int arch_checked = 0;  // 0 unknown, 1 ok, -1 not sm_103
     int num_sms = 0;
-    int num_quads = 0;  // resident 4-CTA clusters (two CTA pairs each)
     void* ws = nullptr;
     size_t ws_bytes = 0;
 };
@@ -54,11 +53,11 @@ std::atomic<int> g_fail_allocs{0};
 // schedule search is cached so that a call costs a table lookup.
 struct PlanKey {
     int64_t BT, C, OC;
-    int sms, quads, fwd;
-    long splitk, grid, tile_n, ppc;
+    int sms, fwd;
+    long splitk, grid, tile_n;
     bool operator==(const PlanKey& o) const {
-        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && quads == o.quads && fwd == o.fwd &&
-               splitk == o.splitk && grid == o.grid && tile_n == o.tile_n && ppc == o.ppc;
+        return BT == o.BT && C == o.C && OC == o.OC && sms == o.sms && fwd == o.fwd && splitk == o.splitk &&
+               grid == o.grid && tile_n == o.tile_n;
     }
 };
 constexpr int kPlanCache = 32;
@@ -79,16 +78,15 @@ long env_tile_n() {
 }
 
 // Caller holds g_mutex.
-const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int quads, int fwd = 0) {
-    const PlanKey k{BT, C, OC, sms, quads, fwd, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n(),
-                    env_long("MMBWD_PPC")};
+const TcPlan& cached_plan(int64_t BT, int64_t C, int64_t OC, int sms, int fwd = 0) {
+    const PlanKey k{BT, C, OC, sms, fwd, env_long("MMBWD_SPLITK"), env_long("MMBWD_GRID"), env_tile_n()};
     for (int i = 0; i < g_plan_count; ++i)
         if (g_plan_keys[i] == k) return g_plans[i];
     const int slot = g_plan_next;
     g_plan_next = (g_plan_next + 1) % kPlanCache;
     if (g_plan_count < kPlanCache) ++g_plan_count;
     g_plan_keys[slot] = k;
-    g_plans[slot] = fwd ? tc_make_plan_forward(BT, C, OC, sms, quads) : tc_make_plan(BT, C, OC, sms, quads);
+    g_plans[slot] = fwd ? tc_make_plan_forward(BT, C, OC, sms) : tc_make_plan(BT, C, OC, sms);
     return g_plans[slot];
 }
 
@@ -99,6 +97,32 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A tensor argument: its first byte and its size in bytes.
+struct Span {
+    const void* p;
+    size_t n;
+};
+
+// Every non-empty tensor must lie in device memory of the current device
+// `dev` (its first and its last byte): the kernels and their tensor maps
+// address it directly, and no call is meant to reach host memory or another
+// GPU's memory through a mapping. Checked before anything is enqueued.
+int check_local(const Span* t, int n, int dev) {
+    for (int i = 0; i < n; ++i) {
+        if (!t[i].p || t[i].n == 0) continue;
+        const void* ends[2] = {t[i].p, static_cast<const uint8_t*>(t[i].p) + (t[i].n - 1)};
+        for (const void* q : ends) {
+            cudaPointerAttributes a{};
+            if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+                cudaGetLastError();
+                return MMBWD_ERR_MEMORY;
+            }
+            if (a.type != cudaMemoryTypeDevice || a.device != dev) return MMBWD_ERR_MEMORY;
+        }
+    }
+    return MMBWD_OK;
+}
 
 // a * b without overflow beyond 2^62; returns false on overflow.
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
@@ -150,7 +174,6 @@ int device_state(DeviceState** out, int* dev_out) {
             // CTAs the persistent kernel can keep resident: whole pairs only.
             const int pairs = tc_max_active_clusters(2);
             if (pairs > 0 && 2 * pairs < sms) d.num_sms = 2 * pairs;
-            d.num_quads = tc_max_active_clusters(4);
         }
     }
     if (d.arch_checked != 1) return MMBWD_ERR_ARCH;
@@ -233,6 +256,7 @@ const char* mmbwd_strerror(int code) {
         case MMBWD_ERR_ARCH: return "the current device is not sm_103 (GB300)";
         case MMBWD_ERR_CAPTURE: return "the workspace must grow but the stream is being captured";
         case MMBWD_ERR_SCRATCH: return "the problem needs more scratch than the library's fixed buffer holds";
+        case MMBWD_ERR_MEMORY: return "a tensor is not in device memory of the current device";
         default: return "unknown status code";
     }
 }
@@ -242,15 +266,15 @@ size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dt
     if (check_shape(B, T, C, OC, dtype, &s) != MMBWD_OK) return 0;
     if (s.BT == 0 || C == 0 || OC == 0) return 0;
     if (dtype == MMBWD_F32) return use_x3(s.BT, C, OC) ? x3_workspace_bytes(s.BT, C, OC, true) : 0;
-    int sms = 0, quads = 0;
+    int sms = 0;
     {
         std::lock_guard<std::mutex> g(g_mutex);
         DeviceState* d = nullptr;
         int dev = 0;
-        if (device_state(&d, &dev) == MMBWD_OK) sms = d->num_sms, quads = d->num_quads;
+        if (device_state(&d, &dev) == MMBWD_OK) sms = d->num_sms;
     }
-    if (sms <= 0) sms = 152, quads = 38;  // no usable device: size for a full GB300
-    return tc_make_plan(s.BT, C, OC, sms, quads).ws_bytes();
+    if (sms <= 0) sms = 152;  // no usable device: size for a full GB300
+    return tc_make_plan(s.BT, C, OC, sms).ws_bytes();
 }
 
 int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int num_sms, int* out, int n) {
@@ -259,20 +283,17 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     if (rc != MMBWD_OK) return rc;
     if (!out || n < 0) return MMBWD_ERR_NULL;
     int v[15] = {0};
-    int num_quads = num_sms / 4;
     if (num_sms <= 0) {  // the current device's resident CTAs (a full GB300 without a device)
         std::lock_guard<std::mutex> g(g_mutex);
         DeviceState* d = nullptr;
         int dev = 0;
-        const bool have = device_state(&d, &dev) == MMBWD_OK;
-        num_sms = have ? d->num_sms : 152;
-        num_quads = have ? d->num_quads : 38;
+        num_sms = device_state(&d, &dev) == MMBWD_OK ? d->num_sms : 152;
     }
     if (dtype == MMBWD_BF16) {
-        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms, num_quads);
+        const TcPlan pl = tc_make_plan(s.BT, C, OC, num_sms);
         const int vals[15] = {1, pl.grid, pl.n_items, pl.splits, pl.kb_per_split, pl.n_dinp_items,
                               pl.n_dw_items / (pl.splits > 0 ? pl.splits : 1), pl.table,
-                              TC_PAIR_BM * pl.ppc, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), pl.ppc};
+                              TC_PAIR_BM, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), 1};
         for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else if (use_x3(s.BT, C, OC)) {
         const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
@@ -330,6 +351,9 @@ int run_backward(void* dinp, void* dweight, void* dbias, const void* dout, const
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    const Span spans[6] = {{dinp, b_dinp}, {dweight, b_dw}, {dbias, b_db}, {dout, b_dout}, {inp, b_inp}, {weight, b_w}};
+    rc = check_local(spans, 6, dev);
+    if (rc != MMBWD_OK) return rc;
 
     cudaError_t e = cudaSuccess;
     if (OC == 0) return MMBWD_OK;  // empty sums everywhere; dbias has no elements
@@ -357,7 +381,7 @@ int run_backward(void* dinp, void* dweight, void* dbias, const void* dout, const
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
 
-    const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads);
+    const TcPlan plan = cached_plan(s.BT, C, OC, d->num_sms);
     rc = ensure_workspace(*d, plan.ws_bytes(), stream);
     if (rc != MMBWD_OK) return rc;
     e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, d->ws, stream, sr, seed);
@@ -448,6 +472,9 @@ int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bi
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    const Span spans[4] = {{out, b_out}, {inp, b_inp}, {weight, b_w}, {bias, b_b}};
+    rc = check_local(spans, 4, dev);
+    if (rc != MMBWD_OK) return rc;
     cudaError_t e = cudaSuccess;
     if (s.BT == 0 || OC == 0) return MMBWD_OK;  // no output element
     if (C == 0) {                                // the empty product: out = bias (or 0)
@@ -468,7 +495,7 @@ int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bi
         }
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
-    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads, 1);
+    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, 1);
     e = tc_launch_forward(plan, out, inp, weight, bias, s.BT, C, OC, stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
 }
@@ -528,6 +555,9 @@ int run_encoder(void* dwte, void* dwpe, const void* dout, const int32_t* inp, in
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    const Span spans[4] = {{dwte, b_wte}, {dwpe, b_wpe}, {dout, b_out}, {inp, b_inp}};
+    rc = check_local(spans, 4, dev);
+    if (rc != MMBWD_OK) return rc;
     if (BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
     rc = ensure_workspace(*d, enc_workspace_bytes(BT, C), stream);
     if (rc != MMBWD_OK) return rc;
@@ -572,6 +602,9 @@ int encbwd_prepare(void* plan, size_t plan_bytes, const int32_t* inp, int64_t B,
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    const Span spans[2] = {{plan, need}, {inp, static_cast<size_t>(BT) * 4}};
+    rc = check_local(spans, 2, dev);
+    if (rc != MMBWD_OK) return rc;
     const cudaError_t e = enc_prepare_launch(plan, inp, B, T, C, V, stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
 }
@@ -599,6 +632,9 @@ int encbwd_run_planned(void* dwte, void* dwpe, const void* dout, void* plan, int
     DeviceState* d = nullptr;
     int dev = 0;
     rc = device_state(&d, &dev);
+    if (rc != MMBWD_OK) return rc;
+    const Span spans[4] = {{dwte, b_wte}, {dwpe, b_wpe}, {dout, b_out}, {plan, b_plan}};
+    rc = check_local(spans, 4, dev);
     if (rc != MMBWD_OK) return rc;
     if (BT == 0 || C == 0) return MMBWD_OK;
     rc = ensure_workspace(*d, enc_run_workspace_bytes(BT, C), stream);
@@ -684,6 +720,10 @@ int lnbwd_run(void* dinp, void* dweight, void* dbias, const void* dout, const vo
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    const Span spans[8] = {{dinp, b_rows}, {dweight, b_col}, {dbias, b_col},  {dout, b_rows},
+                           {inp, b_rows},  {weight, b_col},  {mean, b_stat}, {rstd, b_stat}};
+    rc = check_local(spans, 8, dev);
+    if (rc != MMBWD_OK) return rc;
     if (s.BT == 0 || C == 0) return MMBWD_OK;  // empty sums: nothing changes
     int sms = 0;
     rc = ln_num_sms(&sms);
@@ -753,6 +793,17 @@ extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, 
     int dev = 0;
     rc = device_state(&d, &dev);
     if (rc != MMBWD_OK) return rc;
+    {
+        const size_t es = s.es, b_x = static_cast<size_t>(s.n_dinp) * es, b_w = static_cast<size_t>(s.n_dw) * es;
+        const Span spans[6] = {{dinp, b_x},
+                               {dweight, b_w},
+                               {dbias, static_cast<size_t>(OC) * es},
+                               {dout, static_cast<size_t>(s.n_dout) * es},
+                               {inp, b_x},
+                               {weight, b_w}};
+        rc = check_local(spans, 6, dev);
+        if (rc != MMBWD_OK) return rc;
+    }
     if (!g_static_scratch_addr[dev]) {  // first call on this device: it is the current device
         void* addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) {
@@ -778,7 +829,7 @@ extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, 
                         static_cast<const float*>(weight), s.BT, C, OC, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
-    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms, d->num_quads);
+    const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms);
     if (plan.ws_bytes() > MMBWD_STATIC_SCRATCH_BYTES) return MMBWD_ERR_SCRATCH;
     e = tc_launch(plan, dinp, dweight, dbias, dout, inp, weight, s.BT, C, OC, g_static_scratch_addr[dev], stream);
     return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;

@@ -39,9 +39,9 @@ enum WaitSite : int {
     SITE_EPI_OLD = 11,
 };
 
-// Schedule of a launch: which work items each cluster (one or two CTA pairs)
-// processes, in order (items of cluster c: items[start[c] .. start[c+1])). It travels in the kernel
-// parameters, so a launch needs no device memory for it.
+// Schedule of a launch: which work items each CTA pair (a cluster of two CTAs)
+// processes, in order (items of pair c: items[start[c] .. start[c+1])). It
+// travels in the kernel parameters, so a launch needs no device memory for it.
 constexpr int TC_MAX_PAIRS = 128;
 constexpr int TC_MAX_SCHED_ITEMS = 3072;
 struct TcSchedule {
@@ -68,8 +68,7 @@ struct TcPlan {
     int n_dw_items;    // dw_tiles_m * dw_tiles_n * splits
     int n_dinp_items;  // dinp_tiles_m * dinp_tiles_n
     int n_items;
-    int table;         // 1: per-cluster item lists in `sched`; 0: round-robin
-    int ppc;           // CTA pairs per cluster: 1, or 2 sharing the B tile through multicast
+    int table;         // 1: per-pair item lists in `sched`; 0: round-robin
     int grid;          // CTAs (twice the number of CTA pairs)
     double est_us;     // the planner's time estimate
     int fixup_grid;    // CTAs of the split-reduction pass (0 when splits == 1)
@@ -94,7 +93,7 @@ struct TcParams {
     __nv_bfloat16* dbias;  // may be null
     int dinp_bn, dw_bn, dinp_tiles_n, dw_tiles_n;
     int dinp_tiles_m, dw_tiles_m, dinp_kb, dw_kb, splits, kb_per_split;
-    int n_dw_items, n_dinp_items, n_items, table, ppc;
+    int n_dw_items, n_dinp_items, n_items, table;
     float* partials;       // [dw half tile][split][BM][dw_bn]; half tile = 128-row tile x column tile
     float* bias_partials;  // [dw 128-row tile][split][BM]
     unsigned long long timeout_ns;
@@ -111,13 +110,13 @@ constexpr int TC_WIDE_INP = 4;      // inp: B of dweight
 // Plans (pure functions of the shape and the number of co-resident CTAs,
 // twice the resident CTA pairs). Overrides for tuning and tests come from the
 // environment: MMBWD_SPLITK (splits), MMBWD_GRID (CTAs, rounded to pairs),
-// MMBWD_PPC (CTA pairs per cluster), MMBWD_TILE_N ("dinp,dweight" tile widths);
-// at launch, MMBWD_WIDE_MAPS=0 loads every 64-column box with its own request.
-TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
+// MMBWD_TILE_N ("dinp,dweight" tile widths); at launch, MMBWD_WIDE_MAPS=0
+// loads every 64-column box with its own request.
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms);
 
 // Plan of the forward out (BT x OC) = inp (BT x C) . weight^T (+ bias): only
 // dinp-type items, K = C, N = OC.
-TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads);
+TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms);
 
 // One fp32 product D (M x N, row-major, leading dimension N) += A (M x K) .
 // B (N x K)^T from tf32 halves (hi: the tf32 value, lo: the exact remainder),

@@ -85,18 +85,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// The same load delivered to the same shared-memory offset in every CTA of
-// `cta_mask` (this GPU's memory only), each receiving the transaction bytes on
-// its barrier at the same offset.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
-                                                      int32_t y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // Store one box of a tiled tensor map from this CTA's shared memory (the
 // box's elements in the map's shared-memory layout); parts of the box outside
 // the tensor are not written. Completion is tracked by bulk groups.

@@ -25,8 +25,8 @@
 //               the CTA's own "full" barrier.
 //   warp 1      even CTA: MMA issuer (one thread) into one of two 128 x 256 fp32
 //               accumulators per CTA (512 tensor-memory columns), so the epilogue
-//               of one item overlaps the main loop of the next; commits are
-//               multicast to both CTAs' barriers.
+//               of one item overlaps the main loop of the next; each commit
+//               arrives on both CTAs' barriers.
 //               odd CTA: forwards each stage's "full" to the even CTA's barrier.
 //   warps 2-3   bias: on dweight items of the first column tile, sum the CTA's
 //               dout tile of every stage over its BT rows (the A operand already
@@ -193,13 +193,12 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
 
 // Item processed by this CTA pair in round `round` (>= n_items: none).
 __device__ __forceinline__ int item_at(const TcParams& p, const TcSchedule& sch, int round) {
-    const int csize = 2 * p.ppc;
-    const int c = static_cast<int>(blockIdx.x) / csize;
+    const int c = static_cast<int>(blockIdx.x) / 2;
     if (p.table) {
         const int idx = sch.start[c] + round;
         return idx < sch.start[c + 1] ? static_cast<int>(sch.items[idx]) : p.n_items;
     }
-    return round * (static_cast<int>(gridDim.x) / csize) + c;
+    return round * (static_cast<int>(gridDim.x) / 2) + c;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -286,24 +285,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
-    const uint32_t crank = ptx::cluster_ctarank();  // 0 .. 2*ppc-1
-    const uint32_t rank = crank & 1u;               // within the CTA pair: 0 issues the pair MMAs
-    const uint32_t pp = crank >> 1;                 // which pair of the cluster
-    const uint32_t pair_leader = crank & ~1u;       // cluster rank of this pair's MMA issuer
-    const uint32_t twin = crank ^ 2u;               // same position in the other pair (ppc == 2)
+    const uint32_t rank = ptx::cluster_ctarank();  // within the CTA pair: 0 issues the pair MMAs
     const bool leader = rank == 0;
     const bool bias_on = p.dbias != nullptr;
-    const int ppc = p.ppc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
-            // refilled once every pair MMA reading it has completed (one commit
-            // per pair of the cluster) and every bias warp reading it is done
-            // (this CTA's and, with two pairs, the twin CTA's: the twin's loads
-            // multicast into this stage)
-            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s),
-                           static_cast<uint32_t>(ppc) * (1u + (bias_on ? NUM_BIAS_WARPS : 0)));
+            // refilled once the pair MMAs reading it have completed (one commit)
+            // and this CTA's bias warps are done with it
+            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on ? NUM_BIAS_WARPS : 0));
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
@@ -322,7 +313,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    ptx::cluster_sync();  // every CTA's barriers exist before any remote arrive or multicast
+    ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive or commit
     ptx::tc_fence_after();
     // Everything above overlaps the previous launch on the stream. Threads that
     // touch global memory wait for it to complete first: the epilogue warps
@@ -356,16 +347,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // This CTA's rows of A and columns of B. Boxes wholly outside the
                 // tensor are skipped: they would only feed accumulator rows or
                 // columns that are never stored.
-                const int prow = it.pm * ppc + static_cast<int>(pp);  // this pair's 256-row tile
-                const int row0 = prow * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
+                const int row0 = it.pm * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
                 const int half = it.bn / 2;  // columns of B staged by this CTA
                 const int col0 = it.n_tile * it.bn + static_cast<int>(rank) * half;
                 const int64_t n_extent = FWD ? p.n_dinp : p.C;  // N of this item's product
                 int nb = 0;
                 for (int j = 0; j < half / 64; ++j) nb += (col0 + j * 64 < n_extent) ? 1 : 0;
-                // With two pairs, the twin CTA needs the same B boxes: box j is loaded
-                // by the CTA of pair j and multicast to both.
-                const uint16_t bmask = static_cast<uint16_t>((1u << crank) | (1u << twin));
                 // Output tile of this CTA, prefetched into L2 a few k-blocks before the
                 // main loop ends so that the epilogue's read of the old values hits L2.
                 const bool direct = X3 || (!(it.is_dw && p.splits > 1) && !FWD);  // forward: nothing to read back
@@ -420,19 +407,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const bool b_wide = nb == 2 && (p.wide_maps & (it.is_dw ? TC_WIDE_INP : TC_WIDE_WEIGHT));
                     // B boxes: 64 columns x 64 k, MN-major (backward) or K-major (forward)
                     if (X3) {
-                        // loaded above (one pair per cluster)
-                    } else if (ppc == 1 && b_wide) {
+                        // loaded above
+                    } else if (b_wide) {
                         if (FWD) ptx::tma_load_2d(sB, tmBw, fb, kb * KBLK, col0);
                         else ptx::tma_load_3d(sB, tmBw, fb, 0, kb * KBLK, col0 / 64);
-                    } else if (ppc == 1) {
+                    } else {
                         for (int j = 0; j < nb; ++j) {
                             if (FWD) ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, kb * KBLK, col0 + j * 64);
                             else ptx::tma_load_2d(sB + j * BOX_BYTES, tmB, fb, col0 + j * 64, kb * KBLK);
                         }
-                    } else if (static_cast<int>(pp) < nb) {
-                        const int cj = col0 + static_cast<int>(pp) * 64;
-                        if (FWD) ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, kb * KBLK, cj, bmask);
-                        else ptx::tma_load_2d_multicast(sB + pp * BOX_BYTES, tmB, fb, cj, kb * KBLK, bmask);
                     }
                     issued |= 1u << stage;
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -453,8 +436,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (leader) {
             // -------------------------------------------------------- MMA issuer
             if (lane == 0) {
-                const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2u * pp));
-                const uint16_t empty_mask = static_cast<uint16_t>(ppc == 2 ? 0xFu : pair_mask);
+                const uint16_t pair_mask = 0x3u;  // both CTAs of the pair
                 uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
                 bool ok = true;
                 for (int r = 0; ok; ++r) {
@@ -507,7 +489,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
                         }
                         }
-                        ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), empty_mask);
+                        ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), pair_mask);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -528,7 +510,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         } else {
             // ---------------------------------------------- forwarder (odd CTA)
             if (lane == 0) {
-                const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, pair_leader);
+                const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, 0);
                 uint32_t stage = 0, phase = 0;
                 bool ok = true;
                 for (int r = 0; ok; ++r) {
@@ -554,7 +536,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ------------------------------------------------------------ bias warps
         if (bias_on) {
             const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
-            const uint32_t twin_empty = ptx::mapa(bars + 8u * BAR_EMPTY, twin);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             for (int r = 0;; ++r) {
                 const int w = item_at(p, sch, r);
@@ -595,10 +576,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                     }
                     __syncwarp();
-                    if (lane == 0) {
-                        ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
-                        if (ppc == 2) ptx::mbar_arrive_cluster_relaxed(twin_empty + 8u * stage);
-                    }
+                    if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -637,14 +615,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t oldbar0 = bars + 8u * (BAR_OLD + q * OLD_SLOTS);
         uint32_t oldpar = 0, oldpend = 0;
         uint32_t fwd_chunks = 0;  // forward: chunks this warp has stored (slot = count mod OLD_SLOTS)
-        const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, pair_leader);
+        const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, 0);
         uint32_t acc = 0, acc_phase = 0;
         uint32_t bias_parity[2] = {0u, 0u};
         for (int r = 0;; ++r) {
             const int w = item_at(p, sch, r);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
-            const int m_tile = (it.pm * ppc + static_cast<int>(pp)) * 2 + static_cast<int>(rank);  // 128-row tile
+            const int m_tile = it.pm * 2 + static_cast<int>(rank);  // 128-row tile
             const bool has_bias = bias_on && it.is_dw && it.n_tile == 0;
             const bool split_mode = it.is_dw && p.splits > 1;
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
@@ -960,16 +938,10 @@ long env_long(const char* name, long dflt) {
 // epilogue, whichever is longer, since the two overlap across the two
 // accumulators; the last item's epilogue is not overlapped. Split dweight adds
 // the fixup pass.
-// One k-block of a pair (a 256 x bn tile, 64 deep): load-bound. With both
-// 64-column boxes of an operand in one TMA request, a pair alone feeds its
-// k-blocks as fast as two pairs sharing B through multicast (measured on the
-// LM head: 0.37 us per pair k-block either way); what sets the two cluster
-// modes apart is then the number of pairs resident (clusters of four CTAs
-// leave SMs idle) and the granularity of the items.
-double t_kb(int bn, int ppc) {
-    (void)ppc;
-    return bn == 256 ? 0.31 : 0.29;
-}
+// One k-block of a pair (a 256 x bn tile, 64 deep): load-bound (both 64-column
+// boxes of an operand in one TMA request; measured on the LM head, about
+// 0.37 us per pair k-block under load).
+double t_kb(int bn) { return bn == 256 ? 0.31 : 0.29; }
 double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
 double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
 constexpr double T_ITEM = 0.3;                                 // per-item handoff
@@ -984,10 +956,10 @@ ItemCost item_cost(const TcPlan& pl, int w) {
         const int kb0 = split * pl.kb_per_split;
         const int kb = std::min(kb0 + pl.kb_per_split, pl.dw_kb) - kb0;
         const double epi = pl.splits > 1 ? t_partial(pl.dw_bn) : t_rmw(pl.dw_bn);
-        return {std::max(kb * t_kb(pl.dw_bn, pl.ppc), epi) + T_ITEM, epi};
+        return {std::max(kb * t_kb(pl.dw_bn), epi) + T_ITEM, epi};
     }
     const double epi = t_rmw(pl.dinp_bn);
-    return {std::max(pl.dinp_kb * t_kb(pl.dinp_bn, pl.ppc), epi) + T_ITEM, epi};
+    return {std::max(pl.dinp_kb * t_kb(pl.dinp_bn), epi) + T_ITEM, epi};
 }
 
 double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
@@ -1087,7 +1059,7 @@ int tc_max_active_clusters(int cluster_size) {
 
 // The planner for a launch whose dinp-type product is (BT x N) += (BT x K) . (K x N)
 // with N = C and K = OC, plus, when `with_dw`, the dweight product.
-static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads, bool with_dw) {
+static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, bool with_dw) {
     TcPlan pl{};
     pl.dinp_kb = ceil_div_i(OC, TC_BK);
     pl.dw_kb = ceil_div_i(BT, TC_BK);
@@ -1097,7 +1069,6 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
     // is rounded down to whole pairs; MMBWD_TILE_N = "<dinp>,<dweight>" widths.
     const long force_splits = env_long("MMBWD_SPLITK", 0);
     const long force_grid = env_long("MMBWD_GRID", 0);
-    const long force_ppc = env_long("MMBWD_PPC", 0);
     int force_dinp_bn = 0, force_dw_bn = 0;
     if (const char* t = std::getenv("MMBWD_TILE_N")) {
         int a = 0, b = 0;
@@ -1109,16 +1080,7 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
     const int max_splits = with_dw ? std::max(1, std::min(pl.dw_kb, 16)) : 1;
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
-    // On a modelled tie the cluster mode tried first keeps the plan: for the
-    // backward two pairs sharing B (measured on the GPT-2 MLP fc layer, 57.0 us
-    // against 58.0 with pairs alone), for the forward pairs alone, whose
-    // 128-row weight requests measured faster (34.1 us against 35.5).
-    for (int t = 0; t < 2; ++t) {
-    const int ppc = with_dw ? 2 - t : 1 + t;
-    if (force_ppc && ppc != force_ppc) continue;
-    const int max_clusters =
-        std::max(1, std::min(ppc == 1 ? num_sms / 2 : num_quads, TC_MAX_PAIRS));
-    if (ppc == 2 && num_quads <= 0) continue;
+    const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
     for (int dinp_bn = 256; dinp_bn >= 128; dinp_bn -= 128) {
         if (force_dinp_bn && dinp_bn != force_dinp_bn) continue;
         for (int dw_bn = 256; dw_bn >= 128; dw_bn -= 128) {
@@ -1134,9 +1096,8 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
                                     ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
                     continue;
                 c = pl;
-                c.ppc = ppc;
-                c.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM * ppc);
-                c.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM * ppc);
+                c.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
+                c.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
                 c.dinp_bn = dinp_bn;
                 c.dw_bn = dw_bn;
                 c.dinp_tiles_n = ceil_div_i(C, dinp_bn);
@@ -1146,9 +1107,9 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
                 c.kb_per_split = kps;
                 c.n_dw_items = with_dw ? c.dw_tiles_m * c.dw_tiles_n * S : 0;
                 c.n_items = c.n_dw_items + c.n_dinp_items;
-                int pairs = std::max(1, std::min(c.n_items, max_clusters));  // clusters
-                if (force_grid > 0) pairs = static_cast<int>(std::max<long>(1, std::min<long>(force_grid / (2 * ppc), pairs)));
-                c.grid = 2 * ppc * pairs;
+                int pairs = std::max(1, std::min(c.n_items, max_pairs));
+                if (force_grid > 0) pairs = static_cast<int>(std::max<long>(1, std::min<long>(force_grid / 2, pairs)));
+                c.grid = 2 * pairs;
                 c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
                 const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
                 c.est_us = cost;
@@ -1159,13 +1120,12 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
             }
         }
     }
-    }
     pl = best_pl;
     pl.fixup_grid = 0;
     if (pl.splits > 1) {
         const int64_t nvec = OC * (C / 8);
         pl.fixup_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((nvec + 255) / 256, 8 * std::max(2, num_sms))));
-        const size_t row_tiles = static_cast<size_t>(2 * pl.ppc * pl.dw_tiles_m);  // 128-row tiles
+        const size_t row_tiles = static_cast<size_t>(2 * pl.dw_tiles_m);  // 128-row tiles
         const size_t half_tiles = row_tiles * pl.dw_tiles_n;
         pl.ws_partials_bytes = align256(half_tiles * pl.splits * TC_BM * pl.dw_bn * 4);
         pl.ws_bias_bytes = align256(row_tiles * pl.splits * TC_BM * 4);
@@ -1173,13 +1133,13 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, int
     return pl;
 }
 
-TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
-    return make_plan_impl(BT, C, OC, num_sms, num_quads, true);
+TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms) {
+    return make_plan_impl(BT, C, OC, num_sms, true);
 }
 
-TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int num_quads) {
+TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     // forward: N = OC, K = C, no dweight product
-    return make_plan_impl(BT, OC, C, num_sms, num_quads, false);
+    return make_plan_impl(BT, OC, C, num_sms, false);
 }
 
 // One fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves: one
@@ -1188,7 +1148,6 @@ TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms, int 
 // in cost, so a round-robin assignment is balanced.
 TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
     TcPlan pl{};
-    pl.ppc = 1;
     pl.dinp_kb = ceil_div_i(K, TC_BK / 2);
     pl.dw_kb = 0;
     pl.dinp_tiles_m = ceil_div_i(M, TC_PAIR_BM);
@@ -1328,7 +1287,6 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     p.n_dinp_items = plan.n_dinp_items;
     p.n_items = plan.n_items;
     p.table = plan.table;
-    p.ppc = plan.ppc;
     p.timeout_ns = static_cast<unsigned long long>(env_long("MMBWD_WAIT_TIMEOUT_NS", static_cast<long>(DEFAULT_TIMEOUT_NS)));
 
     cudaLaunchConfig_t cfg{};
@@ -1338,7 +1296,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(2 * plan.ppc);
+    attr[0].val.clusterDim.x = 2;  // one CTA pair
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     // Programmatic dependent launch: the prologue may start while the previous

@@ -134,11 +134,12 @@ def test_split_override_from_environment(monkeypatch):
     monkeypatch.delenv("MMBWD_GRID")
 
 
-def test_pairs_per_cluster_override(monkeypatch):
-    for ppc in (1, 2):
-        monkeypatch.setenv("MMBWD_PPC", str(ppc))
-        a = mm.mmbwd_plan_info(8, 1024, 768, 3072, mm.BF16, 152)
-        assert a["pairs_per_cluster"] == ppc and a["tile_m"] == 256 * ppc
+def test_one_cta_pair_per_cluster():
+    """Every plan runs clusters of one CTA pair (no operand shared across
+    pairs), forward and backward, whatever the shape."""
+    for shape in ((8, 1024, 768, 3072), (8, 1024, 3072, 768), (8, 1024, 768, 768), (4, 1024, 1600, 6400)):
+        a = mm.mmbwd_plan_info(*shape, mm.BF16, 152)
+        assert a["pairs_per_cluster"] == 1 and a["tile_m"] == 256 and a["grid"] % 2 == 0
 
 
 def test_tile_width_override(monkeypatch):
@@ -157,11 +158,10 @@ def test_workspace_size_formula():
         B, T, C, OC = 1, 1000, 264, 392
         info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
         ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
-        ppc = info["pairs_per_cluster"]
-        half_tiles = 2 * ppc * info["dweight_tiles"]  # per-CTA 128-row parts of the cluster tiles
+        half_tiles = 2 * info["dweight_tiles"]  # per-CTA 128-row parts of the pair tiles
         align = lambda x: (x + 255) // 256 * 256  # noqa: E731
         want = (align(half_tiles * 2 * 128 * info["tile_n_dweight"] * 4) +
-                align(2 * ppc * -(-OC // info["tile_m"]) * 2 * 128 * 4))
+                align(2 * -(-OC // info["tile_m"]) * 2 * 128 * 4))
         assert info["launches"] == 2  # the split reduction is a second kernel
         assert ws == want
     finally:

@@ -104,7 +104,6 @@ def test_split_reduction_and_schedule(monkeypatch, splits):
     B, T, C, OC = 1, 1000, 264, 392
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-2)
     monkeypatch.setenv("MMBWD_SPLITK", str(splits))
-    monkeypatch.setenv("MMBWD_PPC", "1")  # one CTA pair per cluster: grids of any even size
     kb = -(-B * T // 64)
     want_splits = -(-kb // -(-kb // splits))  # lowered so that no split is empty
     outs = []
@@ -221,38 +220,33 @@ def test_tile_widths(monkeypatch, tile_n, splits):
     check_full(x, B, T, C, OC, "bf16")
 
 
-@pytest.mark.parametrize("ppc", [1, 2])
 @pytest.mark.parametrize("tile_n", ["256,256", "128,128"])
 @pytest.mark.parametrize("splits", [1, 3])
-def test_pairs_per_cluster(monkeypatch, ppc, tile_n, splits):
-    """One CTA pair per cluster, or two pairs sharing the B tile through TMA
-    multicast, with both tile widths and with or without a split dweight
-    reduction, on a ragged shape; and the 4-CTA mode on a grid of one cluster."""
+def test_tile_widths_on_one_pair(monkeypatch, tile_n, splits):
+    """Both tile widths, with or without a split dweight reduction, on a ragged
+    shape; and the same plan on a grid of one CTA pair, bitwise equal."""
     B, T, C, OC = 3, 300, 392, 1032
-    monkeypatch.setenv("MMBWD_PPC", str(ppc))
     monkeypatch.setenv("MMBWD_TILE_N", tile_n)
     monkeypatch.setenv("MMBWD_SPLITK", str(splits))
     info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
-    assert info["pairs_per_cluster"] == ppc
+    assert info["pairs_per_cluster"] == 1
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
     g0, _ = check_full(x, B, T, C, OC, "bf16")
-    monkeypatch.setenv("MMBWD_GRID", str(2 * ppc))  # every item on one cluster
+    monkeypatch.setenv("MMBWD_GRID", "2")  # every item on one CTA pair
     g1, _ = check_full(x, B, T, C, OC, "bf16")
     for k in ("dinp", "dweight", "dbias"):
         assert np.array_equal(to_host(g0[k], "bf16"), to_host(g1[k], "bf16")), k
 
 
-@pytest.mark.parametrize("ppc", [1, 2])
 @pytest.mark.parametrize("tile_n", ["256,256", "128,128"])
 @pytest.mark.parametrize("splits", [1, 3])
-def test_two_box_requests(monkeypatch, ppc, tile_n, splits):
+def test_two_box_requests(monkeypatch, tile_n, splits):
     """Where an MN-major operand's extent is a multiple of 64, both 64-column
     boxes of a stage may arrive in one three-dimensional TMA request; the last
     column block of C and the last 128 rows of OC (extents 5 and 11 times 64)
     still take the one-box loads. Within tolerance of the oracle, and bitwise
     equal to the run with one request per box."""
     B, T, C, OC = 2, 300, 320, 704
-    monkeypatch.setenv("MMBWD_PPC", str(ppc))
     monkeypatch.setenv("MMBWD_TILE_N", tile_n)
     monkeypatch.setenv("MMBWD_SPLITK", str(splits))
     _, x = make(B, T, C, OC, "bf16", dout_std=1e-1)
