@@ -17,10 +17,18 @@ FLOPs = 4*B*T*C*OC + B*T*OC (the bias sum) per layer.
 * e2e: the same steps through the same C-ABI call, with pinned HOST inputs:
   every step copies dout, inp, weight host->device and reads dinp, dweight,
   dbias back, copies inside the timed region.
-* roofline: the tensor-core kernel's FLOPs per launch / its mean launch time
-  (events around each launch), against the measured bf16 peak.
+* roofline: the step launches only the tensor-core kernel (one launch per
+  layer), so its mean launch time is the timed region over its launches;
+  FLOPs per launch over that time, against the measured bf16 peak. Each
+  layer alone (back-to-back calls) is reported beside it.
+* windows: the K steps cut into up to five windows (events between steps
+  only), min / median / max TFLOP/s over them.
 * cpu_baseline / --impl reference: the C oracle (OpenMP build, all host
-  cores) on a bounded row sample of the same workload.
+  cores) on a bounded row sample of the same workload; the single-threaded
+  build on a smaller sample beside it.
+* other_configs: every other configuration timed alone, each with its
+  largest scaled error against the oracle on sampled rows and whether a
+  second call from identical buffers repeats every bit.
 """
 from __future__ import annotations
 
@@ -46,7 +54,7 @@ WORKLOAD = "mlp"
 METRIC = "matmul_backward TFLOP/s at GPT-2 shapes; % of GB300 dense bf16 peak"
 UNIT = "TFLOP/s"
 N_SETS = 3
-EVENT_EVERY = 4  # steps between the ones timed launch by launch (for the roofline)
+N_WINDOWS = 5  # the timed steps are cut into this many windows (events between steps only)
 
 
 def parse_args(argv=None):
@@ -60,6 +68,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-other", action="store_true", help="skip the other configurations")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="skip the oracle check and repeat check of the other configurations")
     ap.add_argument("--case", default=None,
                     help="time only this one configuration of the other-configs list (for example "
                          "ln_xl or attn_proj) with --steps batches, print its line and exit")
@@ -82,8 +92,16 @@ def config_dict():
 
 
 def layer_bytes(l):
+    """Bytes of one layer's six tensors (the footprint of an input set)."""
     es = l.elem_bytes()
     return es * (l.BT * l.OC + 2 * l.BT * l.C + 2 * l.OC * l.C + l.OC)
+
+
+def layer_alg_bytes(l):
+    """Algorithmic bytes of one call: dout, inp and weight read once, dinp and
+    dweight read and written, dbias written."""
+    es = l.elem_bytes()
+    return es * (l.BT * l.OC + 3 * l.BT * l.C + 3 * l.OC * l.C + (l.OC if l.bias else 0))
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -218,13 +236,14 @@ def profiled_traffic():
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(seconds: float, inputs=None, seed=0):
-    """Time the C oracle (OpenMP build, all host cores) on a bounded row sample
-    of the workload: first dinp rows and dweight rows (with the bias) of each
-    layer, as many as fill about `seconds`. Returns (TFLOP/s, seconds, desc, threads)."""
+def oracle_sample(seconds: float, inputs=None, seed=0, variant="omp"):
+    """Time the C oracle (`variant` "omp": the OpenMP build on all host cores;
+    "st": the single-threaded build) on a bounded row sample of the workload:
+    first dinp rows and dweight rows (with the bias) of each layer, as many as
+    fill about `seconds`. Returns (TFLOP/s, seconds, desc, threads, flops)."""
     import oracle
 
-    orc = oracle.get("omp")
+    orc = oracle.get(variant)
     wl = synth.WORKLOADS[WORKLOAD]
     if inputs is None:
         inputs = [synth.make_inputs(l, seed) for l in wl.layers]
@@ -352,50 +371,57 @@ def run_gpu(args):
         raise RuntimeError(f"device status after warm-up: {mm.strerror(status)} {info}")
 
     K = args.steps
-    L = len(wl.layers)
-    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(L)] for k in range(0, K, EVENT_EVERY)}
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_win = max(1, min(N_WINDOWS, K))
+    bounds = [round(w * K / n_win) for w in range(n_win + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_win + 1)]
     sampler = ClockSampler(gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
     if sampler:
         sampler.start()
     barrier()
     torch.cuda.synchronize()
-    # Per-launch events on every EVENT_EVERY-th step only (they sit between
-    # launches and would otherwise keep the next launch's prologue from
-    # overlapping the previous kernel on every step).
+    # Events only between steps (at window edges): an event between two
+    # launches would keep the second launch's prologue from overlapping the
+    # first kernel.
     with torch.cuda.stream(stream):
-        e_start.record(stream)
-        for k in range(K):
-            tset = sets[k % N_SETS]
-            timed = k % EVENT_EVERY == 0
-            for li, layer in enumerate(wl.layers):
-                if timed:
-                    ev[k][li][0].record(stream)
-                call(layer, tset[li])
-                if timed:
-                    ev[k][li][1].record(stream)
-        e_end.record(stream)
+        ev[0].record(stream)
+        for w in range(n_win):
+            for k in range(bounds[w], bounds[w + 1]):
+                tset = sets[k % N_SETS]
+                for li, layer in enumerate(wl.layers):
+                    call(layer, tset[li])
+            ev[w + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_s = e_start.elapsed_time(e_end) / 1e3
+    elapsed_s = ev[0].elapsed_time(ev[-1]) / 1e3
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
         raise RuntimeError(f"device status after timed region: {mm.strerror(status)} {info}")
 
-    launch_ms = [[ev[k][li][0].elapsed_time(ev[k][li][1]) for k in range(0, K, EVENT_EVERY)] for li in range(L)]
     flops_step = wl.flops()
     units, max_s = aggregate(flops_step * K, elapsed_s)
     value = units / max_s / 1e12
+    win_tf = sorted(flops_step * (bounds[w + 1] - bounds[w]) / (ev[w].elapsed_time(ev[w + 1]) / 1e3) / 1e12
+                    for w in range(n_win) if bounds[w + 1] > bounds[w])
+    windows = {"n": len(win_tf), "steps_each": [bounds[w + 1] - bounds[w] for w in range(n_win)],
+               "tflops_min": win_tf[0], "tflops_median": statistics.median(win_tf), "tflops_max": win_tf[-1]}
 
-    # roofline of the tensor-core kernel (the only kernel these launches run)
+    # roofline of the tensor-core kernel: the timed step launches only this
+    # kernel, one launch per layer, so its mean launch time is this rank's
+    # timed region over its launches (gaps between launches included)
     peaks, peak_src = measured_peaks()
-    kernel_flops = sum(l.flops() for l in wl.layers) * len(launch_ms[0])
-    kernel_s = sum(sum(x) for x in launch_ms) / 1e3
-    achieved = kernel_flops / kernel_s / 1e12
+    n_launch = K * sum(mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0)["launches"] for l in wl.layers)
+    kernel_flops = flops_step * K
+    achieved = kernel_flops / elapsed_s / 1e12
     peak = float(peaks["bf16_tflops"])
     traffic = profiled_traffic()
+    # each layer alone: back-to-back calls over the rotating sets
+    per_layer = {}
+    for li, layer in enumerate(wl.layers):
+        calls = [lambda t=sets[k][li], layer=layer: call(layer, t) for k in range(N_SETS)]
+        sec = time_back_to_back(torch, stream, calls, 30, 5)
+        per_layer[layer.name] = {"us": round(sec * 1e6, 2), "tflops": round(layer.flops() / sec / 1e12, 1),
+                                 "timed": "back-to-back calls of this layer alone"}
 
     # end to end through host buffers
     e2e = None
@@ -404,7 +430,7 @@ def run_gpu(args):
 
     other = None
     if not args.no_other and rank == 0:
-        other = measure_other_configs(torch, mm, dev, stream)
+        other = measure_other_configs(torch, mm, dev, stream, verify=not args.no_verify)
 
     if rank != 0:
         return 0
@@ -412,23 +438,27 @@ def run_gpu(args):
     if not args.no_cpu_baseline and ws >= 1:
         v, dt, desc, cores, _ = oracle_sample(args.cpu_seconds, inputs=host)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2), "build": "OpenMP, -O2, all host cores"}
+        v1, dt1, desc1, _, _ = oracle_sample(args.cpu_seconds / 3, inputs=host, variant="st")
+        cpu["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc1,
+                                "seconds": round(dt1, 2), "build": "single-threaded, -O2"}
 
-    per_layer = {l.name: {"mean_us": 1e3 * statistics.mean(launch_ms[i]),
-                          "tflops": l.flops() / (statistics.mean(launch_ms[i]) / 1e3) / 1e12}
-                 for i, l in enumerate(wl.layers)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": max_s / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal inputs, GPT-2 small MLP shapes)",
         "config": config_dict(),
         "frac_of_bf16_peak": value / peak,
+        "windows": windows,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "tc_mmbwd_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "launches": n_launch, "flops_per_launch": kernel_flops / n_launch,
+                     "mean_launch_us": elapsed_s / n_launch * 1e6,
+                     "timing": "CUDA events around the timed region on the launching stream; every "
+                               "launch in it is this kernel's",
                      "per_layer": per_layer},
-        "gpu_launches": K * sum(mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0)["launches"]
-                                for l in wl.layers),
+        "gpu_launches": n_launch,
         "plans": {l.name: mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0) for l in wl.layers},
         "clocks": clocks,
         "e2e": e2e,
@@ -481,6 +511,98 @@ def time_back_to_back(torch, stream, calls, per_batch, batches=5):
     return statistics.median(times)
 
 
+VERIFY_ROWS = 48  # seeded random rows checked per product, beside the tile-edge rows
+TOL = {"bf16": 2e-2, "f32": 1e-4}  # |gpu - ref| <= tau * (|ref| + rms(ref)), per output tensor
+
+
+def _check_rows(n, seed):
+    """Rows at tile edges and seeded random rows of an n-row output."""
+    edges = [0, 1, 127, 128, 255, 256, n // 2, n - 129, n - 128, n - 1]
+    rng = np.random.default_rng(seed)
+    rows = {r for r in edges if 0 <= r < n} | {int(r) for r in rng.integers(0, n, VERIFY_ROWS)}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _scaled_error(got, ref):
+    """max |got - ref| / (|ref| + rms(ref)); rms over the checked elements."""
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    den = np.abs(ref) + rms
+    return float(np.max(np.abs(got - ref) / np.where(den == 0, 1.0, den)))
+
+
+def _to_f64(torch, t, dtype):
+    if dtype == "bf16":
+        return synth.bf16_bits_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return t.cpu().numpy().astype(np.float64)
+
+
+def _same_bits(torch, a, b):
+    return bool(torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                            b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)))
+
+
+def verify_backward(torch, mm, layer, x, dev, sr=False):
+    """Two calls of mmbwd_run (or mmbwd_run_sr with one seed) from identical
+    buffers: whether every output bit repeats, and the largest scaled error of
+    the first call against the oracle on sampled rows of dinp and dweight and
+    on every dbias element."""
+    import oracle
+
+    dt = mm.BF16 if layer.dtype == "bf16" else mm.F32
+    outs = []
+    for _ in range(2):
+        t = {k: to_device_tensor(torch, v, dev) for k, v in x.items()}
+        args = (t["dinp"], t["dweight"], t["dbias"] if layer.bias else None, t["dout"], t["inp"], t["weight"],
+                layer.B, layer.T, layer.C, layer.OC, dt)
+        rc = mm.mmbwd_run_sr(*args, 12345) if sr else mm.mmbwd_run(*args)
+        if rc != mm.OK:
+            raise RuntimeError(mm.strerror(rc))
+        torch.cuda.synchronize()
+        outs.append(t)
+    repeat = all(_same_bits(torch, outs[0][k], outs[1][k]) for k in ("dinp", "dweight", "dbias"))
+    orc = oracle.get("omp")
+    rb, ro = _check_rows(layer.BT, 1), _check_rows(layer.OC, 2)
+    g = outs[0]
+    errs = {"dinp": _scaled_error(_to_f64(torch, g["dinp"][torch.from_numpy(rb).to(dev)], layer.dtype),
+                                  orc.dinp_rows(x["dout"], x["weight"], layer.dtype, rb, x["dinp"])),
+            "dweight": _scaled_error(_to_f64(torch, g["dweight"][torch.from_numpy(ro).to(dev)], layer.dtype),
+                                     orc.dweight_rows(x["dout"], x["inp"], layer.dtype, ro, x["dweight"],
+                                                      bias=False)[0])}
+    if layer.bias:
+        empty = np.zeros((layer.BT, 0), dtype=x["inp"].dtype)
+        errs["dbias"] = _scaled_error(_to_f64(torch, g["dbias"], layer.dtype),
+                                      orc.dweight_rows(x["dout"], empty, layer.dtype, None, None, bias=True)[1])
+    del outs
+    return {"max_scaled_error": max(errs.values()), "tolerance": TOL[layer.dtype], "bitwise_repeat": repeat,
+            "checked": f"{len(rb)} dinp rows, {len(ro)} dweight rows" + (", every dbias element" if layer.bias else "")
+                       + " against the OpenMP oracle; a second call from identical buffers for the repeat"}
+
+
+def verify_encoder(torch, p, x, dev, run, like):
+    """Two runs of the encoder backward (`run(t)` on buffers shaped like
+    `like`) from identical buffers: whether every bit repeats, and the largest
+    scaled error of the first against the oracle (every element)."""
+    import oracle
+
+    outs = []
+    for _ in range(2):
+        t = {k: to_device_tensor(torch, x[k], dev) for k in ("dout", "dwte", "dwpe")}
+        t["inp"] = torch.from_numpy(x["inp"]).to(dev)
+        run(t)
+        torch.cuda.synchronize()
+        outs.append(t)
+    rte, rpe = oracle.get("omp").encoder_backward(x["dout"], x["inp"], p.B, p.T, p.V, p.dtype, x["dwte"], x["dwpe"])
+    g = outs[0]
+    err = max(_scaled_error(_to_f64(torch, g["dwte"], p.dtype), rte),
+              _scaled_error(_to_f64(torch, g["dwpe"], p.dtype), rpe))
+    rep = all(_same_bits(torch, outs[0][k], outs[1][k]) for k in ("dwte", "dwpe"))
+    return {"max_scaled_error": err, "tolerance": TOL[p.dtype], "bitwise_repeat": rep,
+            "checked": "every dwte and dwpe element against the OpenMP oracle; a second run from identical "
+                       "buffers for the repeat"}
+
+
 def input_sets(nbytes_one, cap=8):
     """How many copies of a configuration's tensors to rotate through so that
     they span more than the L2 (capped; tiny problems stay L2-resident)."""
@@ -497,7 +619,7 @@ def enc_input_sets(torch, x, set_bytes, dev):
     return n, [first] + [{k: v.clone() for k, v in first.items()} for _ in range(n - 1)]
 
 
-def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
+def measure_other_configs(torch, mm, dev, stream, only=None, batches=5, verify=True):
     """The remaining configurations of the workload set and the forward of the
     GPT-2 layers: back-to-back calls on device-resident inputs rotated over
     enough copies to exceed the L2 (see `input_sets`), timed with CUDA events,
@@ -513,10 +635,16 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
     sh = stream.cuda_stream
     out = {}
 
-    def finish(name, layer, flops, sec, n_sets, set_bytes, plan=None):
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+
+    def finish(name, layer, flops, sec, n_sets, set_bytes, plan=None, alg_bytes=None):
         tf = flops / sec / 1e12
         rec = {"B": layer.B, "T": layer.T, "C": layer.C, "OC": layer.OC, "dtype": layer.dtype,
                "bias": layer.bias, "us": round(sec * 1e6, 2), "tflops": round(tf, 2)}
+        if alg_bytes:  # the same time against HBM: algorithmic bytes (inputs once, outputs read and written)
+            gbs = alg_bytes / sec / 1e9
+            rec.update(alg_bytes=alg_bytes, gb_per_s=round(gbs, 1), frac_of_hbm=round(gbs / hbm, 4),
+                       hbm_peak=f"HBM copy (measured) {hbm:.0f} GB/s")
         if layer.dtype == "bf16":
             rec.update(frac_of_peak=round(tf / float(peaks["bf16_tflops"]), 4), peak="bf16 tensor (measured)")
         elif plan is not None and plan.get("path") == 2:
@@ -561,11 +689,14 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         sec = time_back_to_back(torch, stream, calls, per_batch, batches)
         info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
         finish(name, layer, layer.flops(), sec, n_sets, set_bytes,
-               {k: info[k] for k in ("path", "grid", "items", "splits", "launches")})
+               {k: info[k] for k in ("path", "grid", "items", "splits", "launches")}, alg_bytes=layer_alg_bytes(layer))
         if sr:
             out[name]["rounding"] = "stochastic (mmbwd_run_sr, new seed per call)"
         del sets, calls
         torch.cuda.empty_cache()
+        if verify:
+            out[name].update(verify_backward(torch, mm, layer, x, dev, sr))
+            torch.cuda.empty_cache()
     # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
     for name, lname in FORWARD_CONFIGS:
         if only is not None and name not in only:
@@ -595,13 +726,30 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         flops = 2 * layer.BT * layer.C * layer.OC + (layer.BT * layer.OC if layer.bias else 0)
         per_batch = max(len(calls), 20 if flops < 2.5e11 else 8)
         sec = time_back_to_back(torch, stream, calls, per_batch, batches)
+        es = layer.elem_bytes()
         finish(name, layer, flops, sec, n_sets, set_bytes,
-               {"path": mm.mmbwd_forward_path(layer.B, layer.T, layer.C, layer.OC, dt)})
+               {"path": mm.mmbwd_forward_path(layer.B, layer.T, layer.C, layer.OC, dt)},
+               alg_bytes=es * (layer.BT * layer.C + layer.OC * layer.C + layer.BT * layer.OC
+                               + (layer.OC if layer.bias else 0)))
+        if verify:
+            t = sets[0]
+            first = t["out"].clone()
+            make_fcall(t)()
+            torch.cuda.synchronize()
+            import oracle
+
+            rows = _check_rows(layer.BT, 3)
+            ref = oracle.get("omp").forward_rows(x["inp"], x["weight"], layer.dtype, rows,
+                                                 bias=x["dbias"] if layer.bias else None)
+            err = _scaled_error(_to_f64(torch, t["out"][torch.from_numpy(rows).to(dev)], layer.dtype), ref)
+            out[name].update(max_scaled_error=err, tolerance=TOL[layer.dtype],
+                             bitwise_repeat=_same_bits(torch, first, t["out"]),
+                             checked=f"{len(rows)} rows of out against the OpenMP oracle; the previous "
+                                     "call's output for the repeat")
         del sets, calls
         torch.cuda.empty_cache()
     # the LayerNorm backward (lnbwd_run): bound by HBM, reported in GB/s of
     # algorithmic bytes against the measured copy bandwidth
-    hbm = float(peaks.get("hbm_gbs", 6800.0))
     for name in LN_CONFIGS:
         if only is not None and name not in only:
             continue
@@ -639,6 +787,32 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
                      "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
         del sets, calls
         torch.cuda.empty_cache()
+        if verify:
+            import oracle
+
+            orc = oracle.get("omp")
+            outs = []
+            for _ in range(2):
+                t = {k: to_device_tensor(torch, v, dev) for k, v in x.items()}
+                t["mean"], t["rstd"] = torch.from_numpy(mean).to(dev), torch.from_numpy(rstd).to(dev)
+                make_lcall(t)()
+                torch.cuda.synchronize()
+                outs.append(t)
+            rows = _check_rows(p.BT, 4)
+            g = outs[0]
+            e = [_scaled_error(_to_f64(torch, g["dinp"][torch.from_numpy(rows).to(dev)], p.dtype),
+                               orc.layernorm_dinp_rows(x["dout"], x["inp"], x["weight"], mean, rstd, p.dtype, rows,
+                                                       x["dinp"]))]
+            rdw, rdb = orc.layernorm_params(x["dout"], x["inp"], mean, rstd, p.dtype, x["dweight"], x["dbias"])
+            e += [_scaled_error(_to_f64(torch, g["dweight"], p.dtype), rdw),
+                  _scaled_error(_to_f64(torch, g["dbias"], p.dtype), rdb)]
+            out[name].update(max_scaled_error=max(e), tolerance=TOL[p.dtype],
+                             bitwise_repeat=all(_same_bits(torch, outs[0][k], outs[1][k])
+                                                for k in ("dinp", "dweight", "dbias")),
+                             checked=f"{len(rows)} dinp rows, every dweight and dbias element against the "
+                                     "OpenMP oracle; a second call from identical buffers for the repeat")
+            del outs
+            torch.cuda.empty_cache()
     # the encoder backward (encbwd_run): bound by HBM, GB/s of algorithmic bytes
     for name in ENC_CONFIGS:
         if only is not None and name not in only:
@@ -661,11 +835,12 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         calls = [make_ecall(t) for t in sets]
         sec = time_back_to_back(torch, stream, calls, max(len(calls), 40), batches)
         gbs = set_bytes / sec / 1e9
+        check = verify_encoder(torch, p, x, dev, lambda t: make_ecall(t)(), sets[0]) if verify else {}
         out[name] = {"B": p.B, "T": p.T, "C": p.C, "V": p.V, "dtype": p.dtype, "us": round(sec * 1e6, 2),
                      "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
                      "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": set_bytes,
                      "tokens": f"Zipf(s=1.1) over 50257 ids, {distinct} distinct", "input_sets": n_sets,
-                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
+                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident", **check}
         del sets, calls
         torch.cuda.empty_cache()
     for name, wname in ENC_PLANNED_CONFIGS:
@@ -701,13 +876,20 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5):
         runs = [make_run(t) for t in sets]
         sec = time_back_to_back(torch, stream, runs, max(len(runs), 40), batches)
         gbs = set_bytes / sec / 1e9
+
+        def planned(t, p=p, dt=dt):
+            t["plan"] = torch.empty(nplan, dtype=torch.uint8, device=dev)
+            make_prep(t)()
+            make_run(t)()
+
+        check = verify_encoder(torch, p, x, dev, planned, sets[0]) if verify else {}
         out[name] = {"B": p.B, "T": p.T, "C": p.C, "V": p.V, "dtype": p.dtype, "us": round(sec * 1e6, 2),
                      "gb_per_s": round(gbs, 1), "frac_of_peak": round(gbs / hbm, 4),
                      "peak": f"HBM copy (measured) {hbm:.0f} GB/s", "bytes": set_bytes,
                      "prepare_us": round(sec_prep * 1e6, 2),
                      "timed": "encbwd_run_planned; encbwd_prepare (the sort of the token ids) timed apart",
                      "tokens": f"Zipf(s=1.1) over 50257 ids, {distinct} distinct", "input_sets": n_sets,
-                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident"}
+                     "l2": "rotating sets > L2" if n_sets * set_bytes > L2_BYTES else "L2-resident", **check}
         del sets, preps, runs
         torch.cuda.empty_cache()
     status, info = mm.mmbwd_device_status(reset=True)
@@ -801,7 +983,8 @@ def run_case(args):
     torch.cuda.set_device(dev)
     mm.load()
     stream = torch.cuda.Stream(device=dev)
-    out = measure_other_configs(torch, mm, dev, stream, only={args.case}, batches=max(1, args.steps))
+    out = measure_other_configs(torch, mm, dev, stream, only={args.case}, batches=max(1, args.steps),
+                                verify=not args.no_verify)
     print(json.dumps({"case": args.case, **out[args.case]}))
     return 0
 

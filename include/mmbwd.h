@@ -19,11 +19,14 @@
  *               rounded once to bf16 (round-to-nearest-even) after the old value
  *               (converted to fp32) and the fp32 sum are added.
  *   MMBWD_F32:  fp32 storage and fp32-accurate products. Problems large enough
- *               to fill the GPU (B*T, C, OC >= 256, C a multiple of 8) run on the
- *               tensor cores: each operand is split into its tf32 value and the
- *               exact fp32 remainder, and each product is formed from three tf32
- *               products (hi.hi + hi.lo + lo.hi) accumulated in fp32 (relative
- *               error near 2^-20 per product). Smaller or other shapes use fp32
+ *               to fill the GPU (B*T, C, OC >= 256, C a multiple of 8), with both
+ *               reduction lengths (OC and B*T) at most 8192, run on the tensor
+ *               cores: each operand is split into its tf32 value and the exact
+ *               fp32 remainder, and each product is formed from three tf32
+ *               products, hi.hi in one fp32 accumulator and hi.lo + lo.hi in a
+ *               second, added once at the end. The tensor core rounds each
+ *               accumulation toward zero, so this path's error grows with the
+ *               reduction length (hence the 8192 limit). Other shapes use fp32
  *               fused multiply-adds on the CUDA cores. MMBWD_F32_PATH = "ffma" or
  *               "x3" in the environment forces one where the shape allows it.
  *
@@ -199,8 +202,8 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
  *
  * bf16: fp32 accumulation on the tensor cores, out rounded once (RNE) after
  * adding the bias in fp32. fp32: as for mmbwd_run, three tf32 products on the
- * tensor cores for large layers (OC a multiple of 8; out is set to the bias,
- * then the product is added), FFMA otherwise. Same alignment, aliasing (out
+ * tensor cores for large layers (OC a multiple of 8, C at most 8192; out is set
+ * to the bias, then the product is added), FFMA otherwise. Same alignment, aliasing (out
  * must not overlap an input), status codes, asynchrony and determinism as
  * mmbwd_run; the fp32 tensor-core path uses the library workspace. C == 0
  * gives out = bias (or 0).
@@ -215,6 +218,11 @@ int mmbwd_forward_path(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype);
 
 /* Test hook: make the next `n` workspace allocations fail (MMBWD_ERR_ALLOC). */
 void mmbwd_debug_fail_next_alloc(int n);
+
+/* Test hook: the next `n` launch steps of any entry point fail as the CUDA
+ * runtime does when it refuses a launch, before anything is enqueued; the
+ * entry point returns MMBWD_ERR_CUDA and the outputs are untouched. */
+void mmbwd_debug_fail_next_launch(int n);
 
 /* Size of the library's fixed scratch buffer used by mmbwd_run_static_scratch. */
 #define MMBWD_STATIC_SCRATCH_BYTES (32u << 20)

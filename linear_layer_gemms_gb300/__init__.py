@@ -51,6 +51,7 @@ SIGNATURES = {
     "mmbwd_plan_info": ([_i64] * 4 + [_ci, _ci, ctypes.POINTER(_ci), _ci], _ci),
     "mmbwd_selftest_wait_timeout": ([_u64], _ci),
     "mmbwd_debug_fail_next_alloc": ([_ci], None),
+    "mmbwd_debug_fail_next_launch": ([_ci], None),
     "mmbwd_run_static_scratch": ([_vp] * 6 + [_i64] * 4 + [_ci, _vp], _ci),
     "mmbwd_forward": ([_vp] * 4 + [_i64] * 4 + [_ci, _vp], _ci),
     "mmbwd_forward_path": ([_i64] * 4 + [_ci], _ci),
@@ -245,6 +246,10 @@ def mmbwd_selftest_wait_timeout(timeout_ns: int) -> int:
 
 def mmbwd_debug_fail_next_alloc(n: int) -> None:
     load().mmbwd_debug_fail_next_alloc(n)
+
+
+def mmbwd_debug_fail_next_launch(n: int) -> None:
+    load().mmbwd_debug_fail_next_launch(n)
 
 
 def matmul_backward(dinp, dweight, dbias, dout, inp, weight, stream=None) -> None:

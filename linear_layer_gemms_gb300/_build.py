@@ -71,7 +71,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results], "-ldl",
            "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

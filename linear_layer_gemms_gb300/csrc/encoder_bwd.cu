@@ -717,6 +717,7 @@ size_t enc_run_workspace_bytes(int64_t BT, int64_t C) { return enc_partials_byte
 
 cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* inp, int64_t B, int64_t T, int64_t C,
                        int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr, uint64_t seed) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const int BT = static_cast<int>(B * T);
     const int N = dtype == MMBWD_F32 ? 4 : 8;  // elements per 16-byte vector (dwpe)
     EncTables tb{};
@@ -735,6 +736,7 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
 
 cudaError_t enc_prepare_launch(void* plan, const int32_t* inp, int64_t B, int64_t T, int64_t C, int64_t V,
                                cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     EncTables tb{};
     enc_tables_layout(static_cast<uint8_t*>(plan), B * T, C, &tb);
     return enc_sort_launch(inp, static_cast<int>(B * T), V, C, B, T, MMBWD_BF16, tb, nullptr, nullptr, 0, stream);
@@ -743,6 +745,7 @@ cudaError_t enc_prepare_launch(void* plan, const int32_t* inp, int64_t B, int64_
 cudaError_t enc_run_planned_launch(void* dwte, void* dwpe, const void* dout, void* plan, int64_t B, int64_t T,
                                    int64_t C, int64_t V, int dtype, void* ws, int num_sms, cudaStream_t stream, bool sr,
                                    uint64_t seed) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const int N = dtype == MMBWD_F32 ? 4 : 8;
     EncTables tb{};
     enc_tables_layout(static_cast<uint8_t*>(plan), B * T, C, &tb);

@@ -142,6 +142,9 @@ size_t tc_smem_bytes();
 // resident at once on the current device (0 if the query fails).
 int tc_max_active_clusters(int cluster_size);
 
+// Test hook of the launch functions (defined with the C ABI; see ops.h).
+bool take_injected_launch_failure();
+
 // Device status word of the tensor-core translation unit.
 cudaError_t tc_read_status(int* code, int* info3, bool reset);
 cudaError_t tc_selftest_wait(unsigned long long timeout_ns);

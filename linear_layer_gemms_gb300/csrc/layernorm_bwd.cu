@@ -453,6 +453,7 @@ cudaError_t ln_make_plan(int64_t BT, int C, int dtype, int num_sms, LnPlan* plan
 cudaError_t ln_launch(const LnPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, const float* mean, const float* rstd, int64_t BT,
                       int C, int dtype, void* ws, cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     LnParams p{};
     p.dinp = dinp;
     p.dout = dout;

@@ -11,6 +11,12 @@
 
 namespace mmbwd {
 
+// Test hook (mmbwd_debug_fail_next_launch): true for the next n calls, set by
+// the test; every launch function checks it before it enqueues anything and
+// then fails as the runtime does when it refuses a launch, so the error path
+// of each entry point can be exercised without a GPU fault.
+bool take_injected_launch_failure();
+
 // ------------------------------------------------------------ fp32 SIMT path
 constexpr int SIMT_BM = 128;
 constexpr int SIMT_BN = 128;

@@ -177,6 +177,7 @@ __global__ void colsum_kernel(T* __restrict__ dbias, const T* __restrict__ dout,
 
 cudaError_t simt_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
                         const float* weight, int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     // dinp: M = BT, N = C, K = OC
     {
         dim3 grid(static_cast<unsigned>((BT + BM - 1) / BM), static_cast<unsigned>((C + BN - 1) / BN));
@@ -192,6 +193,7 @@ cudaError_t simt_launch(float* dinp, float* dweight, float* dbias, const float* 
 
 cudaError_t simt_forward_launch(float* out, const float* inp, const float* weight, const float* bias,
                                 int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     // out: M = BT, N = OC, K = C; A = inp (BT x C), B = weight stored (OC x C)
     dim3 grid(static_cast<unsigned>((BT + BM - 1) / BM), static_cast<unsigned>((OC + BN - 1) / BN));
     if (grid.x && grid.y)
@@ -210,6 +212,7 @@ __global__ void fill_rows_kernel(T* __restrict__ out, const T* __restrict__ bias
 
 cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t cols, int dtype,
                              cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const int64_t n = rows * cols;
     if (n == 0) return cudaSuccess;
     const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4096));
@@ -224,6 +227,7 @@ cudaError_t fill_rows_launch(void* out, const void* bias, int64_t rows, int64_t 
 
 cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC, int dtype, bool sr, uint64_t sr_seed,
                           cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const unsigned blocks = static_cast<unsigned>((OC + 255) / 256);
     if (blocks == 0) return cudaSuccess;
     if (dtype == MMBWD_F32)

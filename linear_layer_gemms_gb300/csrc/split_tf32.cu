@@ -122,6 +122,7 @@ bool x3_shape_ok(int64_t BT, int64_t C, int64_t OC) {
 cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
                       const float* weight, int64_t BT, int64_t C, int64_t OC, void* ws, int num_sms,
                       cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     const int64_t ldbt = x3_ld(BT);
     uint8_t* w = static_cast<uint8_t*>(ws);
@@ -179,6 +180,7 @@ size_t x3_forward_workspace_bytes(int64_t BT, int64_t C, int64_t OC) {
 
 cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight, const float* bias, int64_t BT,
                               int64_t C, int64_t OC, void* ws, int num_sms, cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* inp_hi = reinterpret_cast<float*>(w);

@@ -288,6 +288,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t rank = ptx::cluster_ctarank();  // within the CTA pair: 0 issues the pair MMAs
     const bool leader = rank == 0;
     const bool bias_on = p.dbias != nullptr;
+    // Accumulator sets in tensor memory. MODE 2 keeps two accumulators per
+    // item side by side -- the hi.hi product, and the two small correction
+    // products -- so a set is 2 x bn columns: two sets when bn <= 128, else
+    // one (the epilogue then does not overlap the next item's main loop).
+    const uint32_t acc_cols = X3 ? 2u * static_cast<uint32_t>(p.dinp_bn) : static_cast<uint32_t>(TC_BN);
+    const int acc_sets = (X3 && p.dinp_bn > 128) ? 1 : 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const Item it = decode_item(p, w);
                     if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + acc * TC_BN;
+                    const uint32_t d_tmem = tmem_base + acc * acc_cols;
                     const uint32_t idesc = X3 ? ptx::idesc_tf32_f32(TC_PAIR_BM, it.bn, 0, 0)
                                               : ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw,
                                                                     /*B MN*/ FWD ? 0 : 1);
@@ -468,9 +474,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 const uint64_t al = ptx::smem_desc_sw128(sA + A_BYTES + k * 32, 16, 1024);
                                 const uint64_t bh = ptx::smem_desc_sw128(sB + k * 32, 16, 1024);
                                 const uint64_t bl = ptx::smem_desc_sw128(sB + B_BYTES + k * 32, 16, 1024);
-                                ptx::mma_tf32_pair(d_tmem, ah, bh, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
-                                ptx::mma_tf32_pair(d_tmem, ah, bl, idesc, 1u);
-                                ptx::mma_tf32_pair(d_tmem, al, bh, idesc, 1u);
+                                // The tensor core rounds each accumulation toward zero, so
+                                // the error of an accumulator grows with the number of
+                                // accumulations into it times its own magnitude: hi.hi
+                                // alone in the main accumulator, hi.lo + lo.hi (about
+                                // 2^-11 of it) in the correction accumulator beside it.
+                                const uint32_t acc0 = (kb > it.kb0 || k > 0) ? 1u : 0u;
+                                ptx::mma_tf32_pair(d_tmem, ah, bh, idesc, acc0);
+                                ptx::mma_tf32_pair(d_tmem + it.bn, ah, bl, idesc, acc0);
+                                ptx::mma_tf32_pair(d_tmem + it.bn, al, bh, idesc, 1u);
                             }
                         } else {
 #pragma unroll
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (!ok) break;
                     ptx::mma_commit_pair_multicast(bars + 8u * (BAR_TFULL + acc), pair_mask);
-                    if (++acc == 2) {
+                    if (++acc == acc_sets) {
                         acc = 0;
                         acc_phase ^= 1u;
                     }
@@ -596,7 +608,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_BIAS + acc));
                 }
-                if (++acc == 2) {
+                if (++acc == acc_sets) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -677,7 +689,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
                 bias_val = bias_smem[acc * TC_BM + rit];
             }
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * TC_BN;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
             // Partial tile of this split: [128 rows][dw_bn columns] fp32, row-major.
             float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.dw_tiles_n + it.n_tile) * p.splits +
                                                      it.split) * (TC_BM * p.dw_bn)
@@ -780,6 +792,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (tma_rmw || TMA_FWD || c >= nchunks) break;
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
+                if constexpr (X3) {  // main + correction, one IEEE fp32 addition
+                    uint32_t w[32];
+                    ptx::tmem_ld32(tbase + it.bn + c * 32, w);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w[e]));
+                }
                 // Row `lane` of the quadrant into the staging buffer ...
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
@@ -828,7 +846,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 ptx::mbar_arrive(bars + 8u * (BAR_EPIDONE + acc));
                 ptx::mbar_arrive_cluster_relaxed(leader_tempty + 8u * acc);
             }
-            if (++acc == 2) {
+            if (++acc == acc_sets) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -1332,6 +1350,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
 cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias, const void* dout,
                       const void* inp, const void* weight, int64_t BT, int64_t C, int64_t OC, void* ws,
                       cudaStream_t stream, bool sr, uint64_t sr_seed) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
     const MapSpec specs[6] = {
         {dout, oc, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},        // dout, K-major A of dinp
@@ -1359,6 +1378,7 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
 
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight, const void* bias,
                               int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
     const MapSpec specs[6] = {
         {inp, c, bt, TC_BK, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B},      // inp, K-major A

@@ -252,3 +252,19 @@ def test_encoder_rejects_bad_arguments():
     assert f(dwte=3 * A - 64) == mm.ERR_ALIAS         # dwte runs into dout
     assert mm.encbwd_workspace_bytes(2, 8, 64, 100, mm.BF16) > 0
     assert mm.encbwd_workspace_bytes(-1, 8, 64, 100, mm.BF16) == 0
+
+
+def test_fp32_tensor_core_path_reduction_limit(monkeypatch):
+    """The three-tf32 path's error grows with the reduction length (the tensor
+    core rounds each accumulation toward zero), so it is taken only while both
+    reduction lengths (OC for dinp, B*T for dweight) are at most 8192, even
+    when forced; the forward's is C."""
+    monkeypatch.delenv("MMBWD_F32_PATH", raising=False)
+    assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32, 152)["path"] == 2
+    assert mm.mmbwd_plan_info(8, 1024, 768, 8192, mm.F32, 152)["path"] == 2
+    assert mm.mmbwd_plan_info(8, 1024, 768, 8200, mm.F32, 152)["path"] == 0
+    assert mm.mmbwd_plan_info(16, 1024, 768, 768, mm.F32, 152)["path"] == 0
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    assert mm.mmbwd_plan_info(1, 1024, 512, 16384, mm.F32, 152)["path"] == 0
+    assert mm.mmbwd_forward_path(1, 1024, 16384, 512, mm.F32) == 0
+    assert mm.mmbwd_forward_path(1, 1024, 8192, 512, mm.F32) == 2
