@@ -325,7 +325,7 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
     } else if (use_x3(s.BT, C, OC)) {
         const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
         const int vals[15] = {2, std::max(p1.grid, p2.grid), p1.n_items + p2.n_items, 1, 0, p1.n_items, p2.n_items,
-                              0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES / 2, 6, 1};
+                              0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES_X3, 6, 1};
         for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);

@@ -21,7 +21,8 @@ constexpr int TC_BM = 128;       // rows per CTA
 constexpr int TC_PAIR_BM = 256;  // rows per CTA pair
 constexpr int TC_BN = 256;       // widest tile (N of one MMA); each CTA stages half of the columns
 constexpr int TC_BK = 64;
-constexpr int TC_STAGES = 6;
+constexpr int TC_STAGES = 5;     // bf16 pipeline stages (32 KB each)
+constexpr int TC_STAGES_X3 = 3;  // fp32 three-product stages (64 KB each)
 constexpr int TC_THREADS = 256;
 
 // Wait sites reported in the device status word.
@@ -30,8 +31,8 @@ enum WaitSite : int {
     SITE_MMA_TMEM_EMPTY = 2,
     SITE_MMA_FULL = 3,
     SITE_EPI_TMEM_FULL = 4,
-    SITE_EPI_BIAS_FULL = 5,
-    SITE_BIAS_TMEM_EMPTY = 6,
+    SITE_EPI_BIAS_FULL = 5,    // (retired: the bias warps store their sums themselves)
+    SITE_BIAS_TMEM_EMPTY = 6,  // (retired)
     SITE_BIAS_FULL = 7,
     SITE_TEARDOWN = 8,
     SITE_SELFTEST = 9,

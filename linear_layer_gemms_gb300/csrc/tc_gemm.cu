@@ -53,6 +53,7 @@
 #include "sr.cuh"
 
 #include <algorithm>
+#include <climits>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -78,33 +79,47 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_EPI_THREADS = 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * TC_BN;
 
-// Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int OFF_BARS = TC_STAGES * STAGE_BYTES;
-constexpr int BAR_FULL = 0;                    // [stages] TMA landed (even CTA: and the peer's too)
-constexpr int BAR_EMPTY = TC_STAGES;           // [stages] stage may be refilled
-constexpr int BAR_TFULL = 2 * TC_STAGES;       // [2] accumulator ready
-constexpr int BAR_TEMPTY = 2 * TC_STAGES + 2;  // [2] accumulator drained by both CTAs (even CTA)
-constexpr int BAR_EPIDONE = 2 * TC_STAGES + 4; // [2] this CTA's epilogue finished an item
-constexpr int BAR_BIAS = 2 * TC_STAGES + 6;    // [2] bias sums ready
-constexpr int BAR_TEARDOWN = 2 * TC_STAGES + 8;
-constexpr int OLD_SLOTS = 4;                   // old-value chunk buffers per epilogue warp
-constexpr int BAR_OLD = 2 * TC_STAGES + 9;     // [epilogue warp][slot] old chunk landed
-constexpr int N_BARS = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;
-constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag, [2] broadcast
-constexpr int OFF_BIAS = (OFF_MISC + 16 + 127) & ~127;
 constexpr int STG_STRIDE = 36;  // floats per staged row: 16-byte aligned, conflict-free
 constexpr int STG_WARP_BYTES = 32 * STG_STRIDE * 4;
-// bf16 read-modify-write through TMA: a 32-row x 32-column chunk of the output
-// (2 KB, rows of 64 bytes, 64-byte swizzle), OLD_SLOTS of them per warp. The
-// fp32 staging of the other epilogues uses the same region.
+// Epilogue chunks: 32 rows x 32 columns of the output, one row per thread.
+// bf16: 2 KB, rows of 64 bytes, 64-byte swizzle (read-modify-write and forward
+// stores). fp32 split partials: 4 KB, rows of 128 bytes, 128-byte swizzle.
 constexpr int OLD_CHUNK_BYTES = 32 * 32 * 2;
-constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
-constexpr int OFF_STAGE = (OFF_BIAS + 2 * TC_BM * 4 + 1023) & ~1023;
-constexpr int STAGE_REGION = NUM_EPI_WARPS * (STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES);
-constexpr int SMEM_USED = OFF_STAGE + STAGE_REGION;
-constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // slack for aligning the base
-static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
+constexpr int PART_CHUNK_BYTES = 32 * 32 * 4;
 
+// Shared memory map (offsets from a 1024-byte aligned base), per kernel mode:
+// the TMA stage ring, the barriers, then one region per epilogue warp. The
+// bf16 modes keep five 32 KB stages and give each epilogue warp eight chunk
+// buffers (16 KB), so that a whole 128 x 256 output tile of old values is
+// requested at the start of an item and lands while its main loop runs (four
+// buffers a warp, requested just ahead of use, left the epilogue waiting on
+// L2 latency: about 4 us for a 128 x 256 tile). MODE 2 keeps three 64 KB
+// stages and the fp32 staging rows.
+template <int MODE>
+struct Smem {
+    static constexpr bool X3 = MODE == 2;
+    static constexpr int STAGES = X3 ? TC_STAGES_X3 : TC_STAGES;
+    static constexpr int STG_BYTES = X3 ? 2 * STAGE_BYTES : STAGE_BYTES;
+    static constexpr int OLD_SLOTS = X3 ? 4 : 8;  // bf16 chunk buffers per epilogue warp
+    static constexpr int PART_SLOTS = X3 ? 1 : 4;  // fp32 partial chunk buffers (same memory)
+    static constexpr int OFF_BARS = STAGES * STG_BYTES;
+    static constexpr int BAR_FULL = 0;                   // [stages] TMA landed (even CTA: and the peer's too)
+    static constexpr int BAR_EMPTY = STAGES;             // [stages] stage may be refilled
+    static constexpr int BAR_TFULL = 2 * STAGES;         // [2] accumulator ready
+    static constexpr int BAR_TEMPTY = 2 * STAGES + 2;    // [2] accumulator drained by both CTAs (even CTA)
+    static constexpr int BAR_TEARDOWN = 2 * STAGES + 4;
+    static constexpr int BAR_OLD = 2 * STAGES + 5;       // [epilogue warp][slot] old chunk landed
+    static constexpr int N_BARS = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;
+    static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag
+    static constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) & ~1023;
+    static constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
+    static constexpr int WARP_REGION = STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES;
+    static constexpr int SMEM_TOTAL = OFF_STAGE + NUM_EPI_WARPS * WARP_REGION + 1024;  // + slack for aligning the base
+    static_assert(X3 || PART_SLOTS * PART_CHUNK_BYTES <= WARP_REGION, "partial chunks fit the warp region");
+    static_assert(WARP_REGION % 1024 == 0, "chunk buffers stay 1024-byte aligned (128-byte swizzle)");
+    static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
+};
+constexpr int SMEM_TOTAL = Smem<0>::SMEM_TOTAL > Smem<2>::SMEM_TOTAL ? Smem<0>::SMEM_TOTAL : Smem<2>::SMEM_TOTAL;
 
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s per wait
 
@@ -266,22 +281,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     // read-modify-write of the backward (MODE 0 and 3)
                     const __grid_constant__ CUtensorMap tm_dinp_rmw,
                     const __grid_constant__ CUtensorMap tm_dw_rmw,
+                    // fp32 partial tiles of a split dweight reduction, 32 x 32
+                    // boxes, 128-byte swizzle (MODE 0 and 3 with splits > 1)
+                    const __grid_constant__ CUtensorMap tm_part,
                     const TcParams p, const __grid_constant__ TcSchedule sch) {
     constexpr bool FWD = MODE == 1 || MODE == 2;  // dinp-type items only, K-major B
     constexpr bool X3 = MODE == 2;                // fp32 from three tf32 products
     constexpr bool SR = MODE == 3;                // stochastic rounding of the outputs
     // MODE 2 stages hold A hi | A lo | B hi | B lo (twice the bytes, half the
     // stages: the same shared memory) and 32 fp32 of K per k-block (128 bytes).
-    constexpr int STAGES = X3 ? TC_STAGES / 2 : TC_STAGES;
-    constexpr int STG_BYTES = X3 ? 2 * STAGE_BYTES : STAGE_BYTES;
+    using L = Smem<MODE>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int STG_BYTES = L::STG_BYTES;
+    constexpr int OLD_SLOTS = L::OLD_SLOTS;
+    constexpr int BAR_FULL = L::BAR_FULL, BAR_EMPTY = L::BAR_EMPTY, BAR_TFULL = L::BAR_TFULL;
+    constexpr int BAR_TEMPTY = L::BAR_TEMPTY, BAR_TEARDOWN = L::BAR_TEARDOWN, BAR_OLD = L::BAR_OLD;
     constexpr int KBLK = X3 ? TC_BK / 2 : TC_BK;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
-    const uint32_t bars = base + OFF_BARS;
-    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC);
-    float* bias_smem = reinterpret_cast<float*>(smem + OFF_BIAS);
+    const uint32_t bars = base + L::OFF_BARS;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_MISC);
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int acc_sets = (X3 && p.dinp_bn > 128) ? 1 : 2;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < TC_STAGES; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
             // refilled once the pair MMAs reading it have completed (one commit)
             // and this CTA's bias warps are done with it
@@ -305,8 +326,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
             ptx::mbar_init(bars + 8u * (BAR_TEMPTY + a), 2 * NUM_EPI_WARPS);
-            ptx::mbar_init(bars + 8u * (BAR_EPIDONE + a), NUM_EPI_WARPS);
-            ptx::mbar_init(bars + 8u * (BAR_BIAS + a), NUM_BIAS_WARPS);
         }
         ptx::mbar_init(bars + 8u * BAR_TEARDOWN, 1);
         for (int b = 0; b < NUM_EPI_WARPS * OLD_SLOTS; ++b) ptx::mbar_init(bars + 8u * (BAR_OLD + b), 1);
@@ -314,7 +333,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         ptx::fence_mbar_init();
     }
     if (warp == WARP_MMA) {
-        ptx::tmem_alloc_pair(base + OFF_MISC, TMEM_COLS);
+        ptx::tmem_alloc_pair(base + L::OFF_MISC, TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // This CTA's copies still in flight land before shared memory goes
             // away (its own full barrier counts its own bytes; in a normal run
             // every phase has already been consumed and these return at once).
-            for (int s = 0; s < TC_STAGES; ++s)
+            for (int s = 0; s < STAGES; ++s)
                 if ((issued >> s) & 1u) wt.wait_teardown(bars + 8u * (BAR_FULL + s), (last_parity >> s) & 1u);
         }
         __syncwarp();
@@ -546,18 +565,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
     } else if (warp < WARP_EPI) {
         // ------------------------------------------------------------ bias warps
+        // They read every stage (releasing it), sum the dout tiles of dweight
+        // items of the first column tile, and store their 64 column sums
+        // themselves: to dbias, rounded once, or as this split's fp32 partial
+        // (the split reduction adds them in split order). They share no
+        // buffer with the epilogue, so they never wait for it.
         if (bias_on) {
             const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            uint32_t stage = 0, phase = 0;
             for (int r = 0;; ++r) {
                 const int w = item_at(p, sch, r);
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
                 const bool has_bias = it.is_dw && it.n_tile == 0;
-                // The epilogue of this CTA has finished with this accumulator
-                // slot (and its bias slot) from two items ago.
-                if (!wt.wait_warp(bars + 8u * (BAR_EPIDONE + acc), acc_phase ^ 1u, SITE_BIAS_TMEM_EMPTY, w))
-                    break;
                 float s[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) s[e] = 0.f;
@@ -602,40 +622,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
                     }
                     if (lane < 8) {
+                        const int m_tile = it.pm * 2 + static_cast<int>(rank);  // 128-row tile of dweight
+                        const int row0 = bw * 64 + lane * 8;                    // first of this lane's 8 rows
+                        if (p.splits > 1) {
+                            float* bp = p.bias_partials + (static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + row0;
+                            *reinterpret_cast<float4*>(bp) = make_float4(s[0], s[1], s[2], s[3]);
+                            *reinterpret_cast<float4*>(bp + 4) = make_float4(s[4], s[5], s[6], s[7]);
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) bias_smem[acc * TC_BM + bw * 64 + lane * 8 + e] = s[e];
+                            for (int e = 0; e < 8; ++e) {
+                                const int64_t o = static_cast<int64_t>(m_tile) * TC_BM + row0 + e;
+                                if (o < p.OC) {
+                                    if constexpr (SR)
+                                        p.dbias[o] = sr::round(s[e], p.sr_seed, sr::DBIAS, o);
+                                    else
+                                        p.dbias[o] = __float2bfloat16_rn(s[e]);
+                                }
+                            }
+                        }
                     }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_BIAS + acc));
-                }
-                if (++acc == acc_sets) {
-                    acc = 0;
-                    acc_phase ^= 1u;
                 }
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;         // tensor-memory lane quadrant: tile rows 32q..32q+31
-        const int rit = q * 32 + lane;  // tile row this thread reads from tensor memory
         const int r8 = lane >> 2;       // coalesced phase: rows 8i + r8 of the quadrant,
         const int cg = (lane & 3) * 8;  //   columns cg..cg+7 of each 32-column chunk
-        const uint32_t stg = base + OFF_STAGE + q * STG_WARP_BYTES;
+        const uint32_t stg = base + L::OFF_STAGE + q * L::WARP_REGION;
         // bf16 read-modify-write (MODE 0 and 3, unsplit items): this warp's
         // ring of old-value chunks, their barriers, parities and pending loads
-        const uint32_t oldbuf = base + OFF_STAGE + q * OLD_WARP_BYTES;
+        const uint32_t oldbuf = base + L::OFF_STAGE + q * L::WARP_REGION;
         const uint32_t oldbar0 = bars + 8u * (BAR_OLD + q * OLD_SLOTS);
         uint32_t oldpar = 0, oldpend = 0;
         uint32_t fwd_chunks = 0;  // forward: chunks this warp has stored (slot = count mod OLD_SLOTS)
         const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, 0);
         uint32_t acc = 0, acc_phase = 0;
-        uint32_t bias_parity[2] = {0u, 0u};
         for (int r = 0;; ++r) {
             const int w = item_at(p, sch, r);
             if (w >= p.n_items) break;
             const Item it = decode_item(p, w);
             const int m_tile = it.pm * 2 + static_cast<int>(rank);  // 128-row tile
-            const bool has_bias = bias_on && it.is_dw && it.n_tile == 0;
             const bool split_mode = it.is_dw && p.splits > 1;
             const int64_t rows_total = it.is_dw ? p.OC : p.BT;
             const int64_t qrow0 = static_cast<int64_t>(m_tile) * TC_BM + q * 32;  // first row of the quadrant
@@ -654,11 +681,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
             // The backward's bf16 read-modify-write goes through TMA: the old
-            // values of this warp's 32 rows arrive in 32-column chunks (the first
-            // OLD_SLOTS requested before waiting for the accumulator; the
-            // producer has prefetched the tile into L2), each thread adds its own
-            // row in place, and the chunk goes back out with one bulk store. Rows
-            // and columns outside the tensor read as zero and are not stored.
+            // values of this warp's 32 rows arrive in 32-column chunks (all of a
+            // 256-wide tile requested at the start of the item, before waiting
+            // for the accumulator), each thread adds its own row in place, and
+            // the chunk goes back out with one bulk store. Rows and columns
+            // outside the tensor read as zero and are not stored.
             const bool tma_rmw = !FWD && !X3 && !split_mode;
             constexpr bool TMA_FWD = FWD && !X3;  // the forward's stores through TMA as well
             const void* tmo = it.is_dw ? static_cast<const void*>(&tm_dw_rmw) : static_cast<const void*>(&tm_dinp_rmw);
@@ -682,18 +709,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
             ptx::tc_fence_after();
-            float bias_val = 0.f;
-            if (has_bias) {
-                ok = wt.wait_warp(bars + 8u * (BAR_BIAS + acc), bias_parity[acc], SITE_EPI_BIAS_FULL, w);
-                bias_parity[acc] ^= 1u;
-                if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
-                bias_val = bias_smem[acc * TC_BM + rit];
-            }
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
-            // Partial tile of this split: [128 rows][dw_bn columns] fp32, row-major.
-            float* part = split_mode ? p.partials + (static_cast<size_t>(m_tile * p.dw_tiles_n + it.n_tile) * p.splits +
-                                                     it.split) * (TC_BM * p.dw_bn)
-                                     : nullptr;
+            if constexpr (!FWD && !X3) {
+                if (split_mode && qvalid) {
+                    // This split's fp32 partial through TMA: row `lane` of each 32 x 32
+                    // chunk into a 4 KB buffer (128-byte rows; 16-byte granule g at
+                    // g ^ (lane & 7), the 128-byte swizzle, conflict-free), one bulk
+                    // store per chunk into [128-row tile x column tile][split][128][bn];
+                    // a buffer is rewritten once the store that used it PART_SLOTS
+                    // chunks ago has read it.
+                    const int32_t prow = static_cast<int32_t>(
+                        ((static_cast<int64_t>(m_tile) * p.dw_tiles_n + it.n_tile) * p.splits + it.split) * TC_BM + q * 32);
+                    const uint32_t swz = static_cast<uint32_t>(lane & 7);
+#pragma unroll 1
+                    for (int c = 0; c < nchunks; ++c) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tbase + c * 32, v);
+                        const int slot = c & (L::PART_SLOTS - 1);
+                        if (c >= L::PART_SLOTS && lane == 0) ptx::bulk_wait_read_but_n<L::PART_SLOTS - 1>();
+                        __syncwarp();
+                        const uint32_t rowaddr = oldbuf + slot * PART_CHUNK_BYTES + lane * 128;
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            ptx::sts128u(rowaddr + ((static_cast<uint32_t>(g) ^ swz) << 4),
+                                         make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&tm_part, oldbuf + slot * PART_CHUNK_BYTES, c * 32, prow);
+                            ptx::bulk_commit_group();
+                        }
+                    }
+                }
+            }
             if (tma_rmw && qvalid) {
                 const uint64_t t_sr = it.is_dw ? sr::DWEIGHT : sr::DINP;
                 // 16-byte granule g of row `lane` sits at granule g ^ ((lane >> 1) & 3)
@@ -789,10 +837,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
 #pragma unroll
             for (int c = 0; c < TC_BN / 32; ++c) {
-                if (tma_rmw || TMA_FWD || c >= nchunks) break;
+                if (!X3 || c >= nchunks) break;  // MODE 2: fp32 read-modify-write through staging rows
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
-                if constexpr (X3) {  // main + correction, one IEEE fp32 addition
+                {  // main + correction, one IEEE fp32 addition
                     uint32_t w[32];
                     ptx::tmem_ld32(tbase + it.bn + c * 32, w);
 #pragma unroll
@@ -811,41 +859,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int lr = 8 * i + r8;
                     const float4 a4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg) * 4);
                     const float4 b4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg + 4) * 4);
-                    if (split_mode) {
-                        float* pp = part + static_cast<size_t>(q * 32 + lr) * p.dw_bn + c * 32 + cg;
-                        __stcg(reinterpret_cast<float4*>(pp), a4);
-                        __stcg(reinterpret_cast<float4*>(pp + 4), b4);
-                    } else if (X3) {
-                        // fp32 read-modify-write (the old values were prefetched into L2)
-                        if (rok[i] && c * 32 + cg < ncols) {
-                            float4* dp = reinterpret_cast<float4*>(drowf[i] + c * 32);
-                            float4 o0 = dp[0], o1 = dp[1];
-                            o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
-                            o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
-                            dp[0] = o0;
-                            dp[1] = o1;
-                        }
+                    // fp32 read-modify-write (the old values were prefetched into L2)
+                    if (rok[i] && c * 32 + cg < ncols) {
+                        float4* dp = reinterpret_cast<float4*>(drowf[i] + c * 32);
+                        float4 o0 = dp[0], o1 = dp[1];
+                        o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
+                        o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
+                        dp[0] = o0;
+                        dp[1] = o1;
                     }
                 }
                 __syncwarp();
             }
-            if (has_bias) {
-                const int64_t brow = static_cast<int64_t>(m_tile) * TC_BM + rit;
-                if (split_mode)
-                    p.bias_partials[(static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + rit] = bias_val;
-                else if (brow < p.OC) {
-                    if constexpr (SR)
-                        p.dbias[brow] = sr::round(bias_val, p.sr_seed, sr::DBIAS, brow);
-                    else
-                        p.dbias[brow] = __float2bfloat16_rn(bias_val);
-                }
-            }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bars + 8u * (BAR_EPIDONE + acc));
-                ptx::mbar_arrive_cluster_relaxed(leader_tempty + 8u * acc);
-            }
+            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(leader_tempty + 8u * acc);
             if (++acc == acc_sets) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -1109,6 +1137,10 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, boo
                 const int S = ceil_div_i(pl.dw_kb, kps);  // every split non-empty
                 if (S == prev_S) continue;
                 prev_S = S;
+                // the partial tiles' rows are addressed by a 32-bit TMA coordinate
+                if (S > 1 && static_cast<int64_t>(2 * ceil_div_i(OC, TC_PAIR_BM)) * ceil_div_i(C, dw_bn) * S * TC_BM >
+                                 INT32_MAX)
+                    continue;
                 if (force_splits > 0 &&
                     S != ceil_div_i(pl.dw_kb,
                                     ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
@@ -1161,9 +1193,12 @@ TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms) {
 }
 
 // One fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves: one
-// pair per cluster, k-blocks of 32, the tile width (128 or 256) that gives the
-// fewer column-weighted waves of 256-row tiles over the pairs; items are equal
-// in cost, so a round-robin assignment is balanced.
+// pair per cluster, k-blocks of 32, the tile width (128 or 256) with the lower
+// modelled time; items are equal in cost, so a round-robin assignment is
+// balanced. Model (us, measured on the GPT-2 XL layers): a k-block of three
+// pair MMAs takes about 0.75 us at width 256 and 0.42 at 128; a 256-wide tile
+// keeps its main and correction accumulators in all 512 tensor-memory
+// columns, so its fp32 epilogue (about 4 us) is not overlapped.
 TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
     TcPlan pl{};
     pl.dinp_kb = ceil_div_i(K, TC_BK / 2);
@@ -1176,7 +1211,8 @@ TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
         if (force && bn != force) continue;
         const int tiles = pl.dinp_tiles_m * ceil_div_i(N, bn);
         const int pairs = std::max(1, std::min(tiles, max_pairs));
-        const double cost = std::ceil(static_cast<double>(tiles) / pairs) * (bn + 32);
+        const double item = pl.dinp_kb * (bn == 256 ? 0.75 : 0.42) + (bn == 256 ? 4.0 : 0.0);
+        const double cost = std::ceil(static_cast<double>(tiles) / pairs) * item;
         if (cost < best) {
             best = cost;
             pl.dinp_bn = bn;
@@ -1230,7 +1266,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     }
     EncodeTiledFn encode = get_encode_tiled();
     if (!encode) return cudaErrorNotSupported;
-    CUtensorMap maps[11];
+    CUtensorMap maps[12];
     for (int i = 0; i < 6; ++i) {
         const cuuint64_t dims[2] = {specs[i].inner, specs[i].outer};
         const uint64_t es = mode == 2 ? 4 : 2;
@@ -1291,6 +1327,20 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
+    // fp32 partial tiles of a split reduction: [half tile][split][128][dw_bn]
+    // as rows of dw_bn floats, stored in 32 x 32 boxes (128-byte swizzle).
+    maps[11] = maps[0];  // placeholder where unused
+    if ((mode == 0 || mode == 3) && plan.splits > 1 && p.partials) {
+        const uint64_t rows = static_cast<uint64_t>(2 * plan.dw_tiles_m) * plan.dw_tiles_n * plan.splits * TC_BM;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(plan.dw_bn), rows};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(plan.dw_bn) * 4};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t estr[2] = {1, 1};
+        const CUresult r = encode(&maps[11], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.partials, dims, strides, box, estr,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     p.dinp_bn = plan.dinp_bn;
     p.dw_bn = plan.dw_bn;
     p.dinp_tiles_n = plan.dinp_tiles_n;
@@ -1324,16 +1374,16 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (mode == 2)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<2>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], p,
                                plan.sched);
     else if (mode == 1)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<1>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], p,
                                plan.sched);
     else if (mode == 3)
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<3>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], p,
                                plan.sched);
     else
-        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], p,
+        e = cudaLaunchKernelEx(&cfg, tc_mmbwd_kernel<0>, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], p,
                                plan.sched);
     if (e != cudaSuccess || plan.splits == 1) return e;
     cudaLaunchConfig_t fcfg{};
