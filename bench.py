@@ -483,6 +483,10 @@ ENC_PLANNED_CONFIGS = (("enc_gpt2_small_planned", "enc_gpt2_small"),)
 # (mmbwd_run_sr, a new seed per call)
 LAYER_CONFIGS = (("mlp_fc", "mlp:0", False), ("mlp_fc_proj", "mlp:1", False),
                  ("mlp_fc_sr", "mlp:0", True), ("mlp_fc_proj_sr", "mlp:1", True))
+# the same layers with dbias formed by an extra MMA against a ones tile
+# (MMBWD_DBIAS=ones) instead of the bias warps
+DBIAS_MMA_CONFIGS = (("mlp_fc_dbias_mma", "mlp:0"), ("mlp_fc_proj_dbias_mma", "mlp:1"),
+                     ("attn_proj_dbias_mma", "attn_proj"))
 FORWARD_CONFIGS = (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1"),
                    ("forward_lm_head", "lm_head"), ("forward_xl_fc_f32", "xl_fc_f32"))
 
@@ -660,10 +664,16 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5, verify=T
         if plan is not None:
             out[name]["plan"] = plan
 
-    backward = [(n, n, False) for n in OTHER_CONFIGS] + list(LAYER_CONFIGS)
+    backward = ([(n, n, False) for n in OTHER_CONFIGS] + list(LAYER_CONFIGS) +
+                [(n, spec, False) for n, spec in DBIAS_MMA_CONFIGS])
+    dbias_mma = {n for n, _ in DBIAS_MMA_CONFIGS}
     for name, spec, sr in backward:
         if only is not None and name not in only:
             continue
+        if name in dbias_mma:
+            os.environ["MMBWD_DBIAS"] = "ones"
+        else:
+            os.environ.pop("MMBWD_DBIAS", None)
         wl, _, i = spec.partition(":")
         layer = synth.WORKLOADS[wl].layers[int(i or 0)]
         x = synth.make_inputs(layer, seed=0)
@@ -697,6 +707,9 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5, verify=T
         if verify:
             out[name].update(verify_backward(torch, mm, layer, x, dev, sr))
             torch.cuda.empty_cache()
+        if name in dbias_mma:
+            out[name]["dbias"] = "extra pair MMA against a ones tile (MMBWD_DBIAS=ones)"
+        os.environ.pop("MMBWD_DBIAS", None)
     # the forward of the same layers (mmbwd_forward): 2*B*T*C*OC FLOPs (+ B*T*OC with the bias)
     for name, lname in FORWARD_CONFIGS:
         if only is not None and name not in only:
@@ -976,6 +989,7 @@ def run_case(args):
     import linear_layer_gemms_gb300 as mm
 
     names = (set(OTHER_CONFIGS) | set(LN_CONFIGS) | set(ENC_CONFIGS) | {n for n, _ in FORWARD_CONFIGS}
+             | {n for n, _ in DBIAS_MMA_CONFIGS}
              | {n for n, _, _ in LAYER_CONFIGS} | {n for n, _ in ENC_PLANNED_CONFIGS})
     if args.case not in names:
         raise SystemExit(f"unknown case {args.case}; one of {sorted(names)}")

@@ -101,7 +101,14 @@ struct TcParams {
     int sr;                         // stochastic rounding of the bf16 outputs (backward)
     unsigned long long sr_seed;
     int wide_maps;                  // TC_WIDE_* bits: operands that also have a two-box map
+    int bias_mma;                   // dbias from an extra pair MMA against a ones tile (MMBWD_DBIAS=ones)
+    int x3_corr;                    // MODE 2: hi.lo + lo.hi in their own accumulator (long K)
 };
+
+// MODE 2 reductions longer than this keep the two correction products in an
+// accumulator of their own (the tensor core rounds each accumulation toward
+// zero; see the fp32 path's selection in the C-ABI layer).
+constexpr int64_t TC_X3_CORR_K = 2048;
 
 // Operands whose two 64-column halves can arrive in one TMA request.
 constexpr int TC_WIDE_WEIGHT = 1;   // weight: B of dinp (backward), B of the forward

@@ -191,6 +191,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// One 32-bit column of 32 lanes: thread i receives lane (taddr.lane + i).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r)
+        : "r"(taddr)
+        : "memory");
+    return r;
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading-
 // and stride-dimension byte offsets (all >> 4), descriptor version 1 at bit
 // 46, swizzle mode at bits 61..63 (2 = 128-byte swizzle).

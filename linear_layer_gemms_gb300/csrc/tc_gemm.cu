@@ -56,6 +56,7 @@
 #include <climits>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace mmbwd {
@@ -114,7 +115,10 @@ struct Smem {
     static constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) & ~1023;
     static constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
     static constexpr int WARP_REGION = STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES;
-    static constexpr int SMEM_TOTAL = OFF_STAGE + NUM_EPI_WARPS * WARP_REGION + 1024;  // + slack for aligning the base
+    // ones tile of the dbias-by-MMA variant: 8 rows (this CTA's half of N = 16)
+    // of 64 bf16 ones, one 128-byte-swizzled 1 KB atom
+    static constexpr int OFF_ONES = OFF_STAGE + NUM_EPI_WARPS * WARP_REGION;
+    static constexpr int SMEM_TOTAL = OFF_ONES + 1024 + 1024;  // + slack for aligning the base
     static_assert(X3 || PART_SLOTS * PART_CHUNK_BYTES <= WARP_REGION, "partial chunks fit the warp region");
     static_assert(WARP_REGION % 1024 == 0, "chunk buffers stay 1024-byte aligned (128-byte swizzle)");
     static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
@@ -309,19 +313,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t rank = ptx::cluster_ctarank();  // within the CTA pair: 0 issues the pair MMAs
     const bool leader = rank == 0;
     const bool bias_on = p.dbias != nullptr;
-    // Accumulator sets in tensor memory. MODE 2 keeps two accumulators per
-    // item side by side -- the hi.hi product, and the two small correction
-    // products -- so a set is 2 x bn columns: two sets when bn <= 128, else
-    // one (the epilogue then does not overlap the next item's main loop).
-    const uint32_t acc_cols = X3 ? 2u * static_cast<uint32_t>(p.dinp_bn) : static_cast<uint32_t>(TC_BN);
-    const int acc_sets = (X3 && p.dinp_bn > 128) ? 1 : 2;
+    // Accumulator sets in tensor memory. For long reductions MODE 2 keeps two
+    // accumulators per item side by side -- the hi.hi product, and the two
+    // small correction products -- so a set is 2 x bn columns: two sets when
+    // bn <= 128, else one (the epilogue then does not overlap the next item's
+    // main loop).
+    const bool corr = X3 && p.x3_corr;
+    const uint32_t acc_cols = corr ? 2u * static_cast<uint32_t>(p.dinp_bn) : static_cast<uint32_t>(TC_BN);
+    const int acc_sets = (corr && p.dinp_bn > 128) ? 1 : 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
             // refilled once the pair MMAs reading it have completed (one commit)
             // and this CTA's bias warps are done with it
-            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on ? NUM_BIAS_WARPS : 0));
+            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on && !p.bias_mma ? NUM_BIAS_WARPS : 0));
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
@@ -335,6 +341,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == WARP_MMA) {
         ptx::tmem_alloc_pair(base + L::OFF_MISC, TMEM_COLS);
         ptx::tmem_relinquish_pair();
+    }
+    if constexpr (!FWD && !X3) {
+        if (p.bias_mma) {  // the ones tile (bf16 1.0 in every element, so any layout reads ones)
+            reinterpret_cast<uint32_t*>(smem + L::OFF_ONES)[threadIdx.x] = 0x3F803F80u;
+            ptx::fence_proxy_async_smem();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -464,13 +476,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint16_t pair_mask = 0x3u;  // both CTAs of the pair
                 uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
                 bool ok = true;
+                bool prev_bias = false;  // the previous item put its column sums in this set
                 for (int r = 0; ok; ++r) {
                     const int w = item_at(p, sch, r);
                     if (w >= p.n_items) break;
                     const Item it = decode_item(p, w);
                     if (!wt.wait(bars + 8u * (BAR_TEMPTY + acc), acc_phase ^ 1u, SITE_MMA_TMEM_EMPTY, w)) break;
+                    // dbias by MMA: a dweight item of the first column tile also
+                    // accumulates doutT . ones (N = 16) into the first 16 columns of
+                    // the other accumulator set, so the last item issued into that set
+                    // must have been drained, and the item after this one must wait
+                    // until this item's epilogue has read the sums.
+                    const bool bias_item = !FWD && !X3 && p.bias_mma && it.is_dw && it.n_tile == 0;
+                    if (bias_item || prev_bias) {
+                        const uint32_t o = acc ^ 1u, ph_o = acc == 0 ? acc_phase ^ 1u : acc_phase;
+                        if (!wt.wait(bars + 8u * (BAR_TEMPTY + o), ph_o, SITE_MMA_TMEM_EMPTY, w)) break;
+                    }
+                    prev_bias = bias_item;
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * acc_cols;
+                    const uint32_t d_bias = tmem_base + (acc ^ 1u) * TC_BN;
+                    const uint32_t ones = base + L::OFF_ONES;
                     const uint32_t idesc = X3 ? ptx::idesc_tf32_f32(TC_PAIR_BM, it.bn, 0, 0)
                                               : ptx::idesc_bf16_f32(TC_PAIR_BM, it.bn, /*A MN*/ it.is_dw,
                                                                     /*B MN*/ FWD ? 0 : 1);
@@ -495,13 +521,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 const uint64_t bl = ptx::smem_desc_sw128(sB + B_BYTES + k * 32, 16, 1024);
                                 // The tensor core rounds each accumulation toward zero, so
                                 // the error of an accumulator grows with the number of
-                                // accumulations into it times its own magnitude: hi.hi
-                                // alone in the main accumulator, hi.lo + lo.hi (about
-                                // 2^-11 of it) in the correction accumulator beside it.
+                                // accumulations into it times its own magnitude. Long
+                                // reductions: hi.hi alone in the main accumulator, hi.lo +
+                                // lo.hi (about 2^-11 of it) in the correction accumulator
+                                // beside it; short ones: all three in one.
                                 const uint32_t acc0 = (kb > it.kb0 || k > 0) ? 1u : 0u;
+                                const uint32_t d_corr = corr ? d_tmem + it.bn : d_tmem;
                                 ptx::mma_tf32_pair(d_tmem, ah, bh, idesc, acc0);
-                                ptx::mma_tf32_pair(d_tmem + it.bn, ah, bl, idesc, acc0);
-                                ptx::mma_tf32_pair(d_tmem + it.bn, al, bh, idesc, 1u);
+                                ptx::mma_tf32_pair(d_corr, ah, bl, idesc, corr ? acc0 : 1u);
+                                ptx::mma_tf32_pair(d_corr, al, bh, idesc, 1u);
                             }
                         } else {
 #pragma unroll
@@ -518,6 +546,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             const uint64_t bdesc = FWD ? ptx::smem_desc_sw128(sB + k * 32, 16, 1024)
                                                          : ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
                             ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
+                            if (bias_item)  // D_bias (256 x 16) += doutT (256 x 16 of K) . ones (16 x 16)
+                                ptx::mma_bf16_pair(d_bias, adesc, ptx::smem_desc_sw128(ones + k * 32, 16, 1024),
+                                                   ptx::idesc_bf16_f32(TC_PAIR_BM, 16, 1, 0),
+                                                   (kb > it.kb0 || k > 0) ? 1u : 0u);
                         }
                         }
                         ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), pair_mask);
@@ -570,7 +602,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // themselves: to dbias, rounded once, or as this split's fp32 partial
         // (the split reduction adds them in split order). They share no
         // buffer with the epilogue, so they never wait for it.
-        if (bias_on) {
+        if (bias_on && !p.bias_mma) {
             const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
             uint32_t stage = 0, phase = 0;
             for (int r = 0;; ++r) {
@@ -711,6 +743,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
             if constexpr (!FWD && !X3) {
+                if (p.bias_mma && it.is_dw && it.n_tile == 0 && qvalid) {
+                    // dbias by MMA: every column of the sums block holds the row's sum
+                    const float bsum = __uint_as_float(
+                        ptx::tmem_ld1(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (acc ^ 1u) * TC_BN));
+                    const int64_t o = qrow0 + lane;
+                    if (split_mode)
+                        p.bias_partials[(static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + q * 32 + lane] = bsum;
+                    else if (o < p.OC) {
+                        if constexpr (SR)
+                            p.dbias[o] = sr::round(bsum, p.sr_seed, sr::DBIAS, o);
+                        else
+                            p.dbias[o] = __float2bfloat16_rn(bsum);
+                    }
+                }
+            }
+            if constexpr (!FWD && !X3) {
                 if (split_mode && qvalid) {
                     // This split's fp32 partial through TMA: row `lane` of each 32 x 32
                     // chunk into a 4 KB buffer (128-byte rows; 16-byte granule g at
@@ -840,7 +888,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (!X3 || c >= nchunks) break;  // MODE 2: fp32 read-modify-write through staging rows
                 uint32_t v[32];
                 ptx::tmem_ld32(tbase + c * 32, v);
-                {  // main + correction, one IEEE fp32 addition
+                if (corr) {  // main + correction, one IEEE fp32 addition
                     uint32_t w[32];
                     ptx::tmem_ld32(tbase + it.bn + c * 32, w);
 #pragma unroll
@@ -1196,9 +1244,9 @@ TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms) {
 // pair per cluster, k-blocks of 32, the tile width (128 or 256) with the lower
 // modelled time; items are equal in cost, so a round-robin assignment is
 // balanced. Model (us, measured on the GPT-2 XL layers): a k-block of three
-// pair MMAs takes about 0.75 us at width 256 and 0.42 at 128; a 256-wide tile
-// keeps its main and correction accumulators in all 512 tensor-memory
-// columns, so its fp32 epilogue (about 4 us) is not overlapped.
+// pair MMAs takes about 0.75 us at width 256 and 0.42 at 128; with a separate
+// correction accumulator (K > TC_X3_CORR_K) a 256-wide tile fills all 512
+// tensor-memory columns, so its fp32 epilogue (about 4 us) is not overlapped.
 TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
     TcPlan pl{};
     pl.dinp_kb = ceil_div_i(K, TC_BK / 2);
@@ -1211,7 +1259,7 @@ TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
         if (force && bn != force) continue;
         const int tiles = pl.dinp_tiles_m * ceil_div_i(N, bn);
         const int pairs = std::max(1, std::min(tiles, max_pairs));
-        const double item = pl.dinp_kb * (bn == 256 ? 0.75 : 0.42) + (bn == 256 ? 4.0 : 0.0);
+        const double item = pl.dinp_kb * (bn == 256 ? 0.75 : 0.42) + (bn == 256 && K > TC_X3_CORR_K ? 4.0 : 0.0);
         const double cost = std::ceil(static_cast<double>(tiles) / pairs) * item;
         if (cost < best) {
             best = cost;
@@ -1423,6 +1471,10 @@ cudaError_t tc_launch(const TcPlan& plan, void* dinp, void* dweight, void* dbias
     p.bias_partials = plan.splits > 1 ? reinterpret_cast<float*>(w + plan.ws_partials_bytes) : nullptr;
     p.sr = sr ? 1 : 0;
     p.sr_seed = sr_seed;
+    // MMBWD_DBIAS=ones: dbias from an extra MMA against a ones tile instead of
+    // the bias warps (the variant the page's commented-out Sgemv suggests)
+    const char* db = std::getenv("MMBWD_DBIAS");
+    p.bias_mma = (dbias && db && std::strcmp(db, "ones") == 0) ? 1 : 0;
     return launch_common(plan, specs, p, sr ? 3 : 0, stream);
 }
 
@@ -1466,6 +1518,7 @@ cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const 
     p.C = K;
     p.OC = K;
     p.n_dinp = N;
+    p.x3_corr = K > TC_X3_CORR_K ? 1 : 0;
     p.dinp = reinterpret_cast<__nv_bfloat16*>(D);
     return launch_common(plan, specs, p, 2, stream);
 }
