@@ -513,12 +513,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         if constexpr (X3) {
                             // K-major tf32 slices of 8 elements: 32 bytes further into
                             // each swizzled 128-byte row, as for the bf16 K-major case.
+                            const uint64_t ah0 = ptx::smem_desc_sw128(sA, 16, 1024);
+                            const uint64_t al0 = ptx::smem_desc_sw128(sA + A_BYTES, 16, 1024);
+                            const uint64_t bh0 = ptx::smem_desc_sw128(sB, 16, 1024);
+                            const uint64_t bl0 = ptx::smem_desc_sw128(sB + B_BYTES, 16, 1024);
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const uint64_t ah = ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
-                                const uint64_t al = ptx::smem_desc_sw128(sA + A_BYTES + k * 32, 16, 1024);
-                                const uint64_t bh = ptx::smem_desc_sw128(sB + k * 32, 16, 1024);
-                                const uint64_t bl = ptx::smem_desc_sw128(sB + B_BYTES + k * 32, 16, 1024);
+                                const uint64_t ah = ah0 + 2u * k, al = al0 + 2u * k;  // +32 bytes per slice
+                                const uint64_t bh = bh0 + 2u * k, bl = bl0 + 2u * k;
                                 // The tensor core rounds each accumulation toward zero, so
                                 // the error of an accumulator grows with the number of
                                 // accumulations into it times its own magnitude. Long
@@ -532,25 +534,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 ptx::mma_tf32_pair(d_corr, al, bh, idesc, 1u);
                             }
                         } else {
-#pragma unroll
-                        for (int k = 0; k < TC_BK / 16; ++k) {
                             // K-major A: the 16-element K slice starts 32 bytes further
-                            // into each swizzled 128-byte row; rows in 8-row groups of
-                            // 1024 bytes. MN-major operands: 16 K rows of 128 bytes per
-                            // slice (2048 bytes); 64-wide MN boxes 8 KB apart (leading
-                            // offset), 8-row K groups 1024 bytes apart (stride offset).
-                            const uint64_t adesc =
-                                it.is_dw ? ptx::smem_desc_sw128(sA + k * 2048, BOX_BYTES, 1024)
-                                         : ptx::smem_desc_sw128(sA + k * 32, 16, 1024);
+                            // into each swizzled 128-byte row (descriptor address +2);
+                            // rows in 8-row groups of 1024 bytes. MN-major operands: 16 K
+                            // rows of 128 bytes per slice (2048 bytes: address +128);
+                            // 64-wide MN boxes 8 KB apart (leading offset), 8-row K groups
+                            // 1024 bytes apart (stride offset). The descriptors of a
+                            // k-block are formed once and stepped by addition (the address
+                            // field stays below 2^14), which keeps this single thread's
+                            // issue loop short: the tensor pipe waits on it.
+                            const uint64_t a0 = it.is_dw ? ptx::smem_desc_sw128(sA, BOX_BYTES, 1024)
+                                                         : ptx::smem_desc_sw128(sA, 16, 1024);
+                            const uint64_t a_step = it.is_dw ? 128u : 2u;
                             // Forward: B is K-major like A (weight rows of 128 bytes of K).
-                            const uint64_t bdesc = FWD ? ptx::smem_desc_sw128(sB + k * 32, 16, 1024)
-                                                         : ptx::smem_desc_sw128(sB + k * 2048, BOX_BYTES, 1024);
-                            ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
-                            if (bias_item)  // D_bias (256 x 16) += doutT (256 x 16 of K) . ones (16 x 16)
-                                ptx::mma_bf16_pair(d_bias, adesc, ptx::smem_desc_sw128(ones + k * 32, 16, 1024),
-                                                   ptx::idesc_bf16_f32(TC_PAIR_BM, 16, 1, 0),
-                                                   (kb > it.kb0 || k > 0) ? 1u : 0u);
-                        }
+                            const uint64_t b0 = FWD ? ptx::smem_desc_sw128(sB, 16, 1024)
+                                                    : ptx::smem_desc_sw128(sB, BOX_BYTES, 1024);
+                            constexpr uint64_t b_step = FWD ? 2u : 128u;
+                            const uint32_t first = kb > it.kb0 ? 1u : 0u;
+                            if (!bias_item) {
+#pragma unroll
+                                for (int k = 0; k < TC_BK / 16; ++k)
+                                    ptx::mma_bf16_pair(d_tmem, a0 + k * a_step, b0 + k * b_step, idesc,
+                                                       k > 0 ? 1u : first);
+                            } else {
+                                // dbias by MMA: D_bias (256 x 16) += doutT (256 x 16 of K) .
+                                // ones (16 x 16) beside each main MMA
+                                const uint64_t o0 = ptx::smem_desc_sw128(ones, 16, 1024);
+                                constexpr uint32_t idesc_b = ptx::idesc_bf16_f32(TC_PAIR_BM, 16, 1, 0);
+#pragma unroll
+                                for (int k = 0; k < TC_BK / 16; ++k) {
+                                    ptx::mma_bf16_pair(d_tmem, a0 + k * a_step, b0 + k * b_step, idesc,
+                                                       k > 0 ? 1u : first);
+                                    ptx::mma_bf16_pair(d_bias, a0 + k * a_step, o0 + k * 2u, idesc_b,
+                                                       k > 0 ? 1u : first);
+                                }
+                            }
                         }
                         ptx::mma_commit_pair_multicast(bars + 8u * (BAR_EMPTY + stage), pair_mask);
                         if (++stage == STAGES) {
