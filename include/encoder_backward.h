@@ -32,9 +32,10 @@
 extern "C" {
 #endif
 
-/* Limits of the single-block device sort (B*T positions, V token ids) and of
- * the channel count C. */
-#define ENCBWD_MAX_POSITIONS 16384
+/* Limits of the device sort (B*T positions, V token ids) and of the channel
+ * count C. Up to 16384 positions are sorted by one block; more by a
+ * multi-block radix sort (a few more launches). */
+#define ENCBWD_MAX_POSITIONS (1 << 24)
 #define ENCBWD_MAX_VOCAB 131071
 #define ENCBWD_MAX_CHANNELS 65536
 

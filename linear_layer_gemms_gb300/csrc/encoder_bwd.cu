@@ -137,7 +137,9 @@ struct EncVec4<__nv_bfloat16> {
 
 struct EncTables {
     int* meta;           // [0] valid positions; [1..3] B*T, V, C of the problem
-    unsigned* skeys;     // [B*T] sorted keys (token << 15 | position)
+    unsigned long long* mb_alt;  // the multi-block sort's second key buffer (B*T > ENC_FAST_MAX)
+    int* mb_hist;                // its per-(digit, tile) counts and offsets
+    unsigned long long* skeys;  // [B*T] sorted keys (token << 32 | position); invalid slots all ones
     int* win_head;       // [windows] first slot of the run holding the window's first slot
     int* win_tail;       // [windows] last slot of the run holding the window's last slot
     unsigned* arrivals;  // [windows][G] windows done for the token whose run starts in the window
@@ -398,7 +400,8 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     for (int r = 0; r < KPL; ++r) nvalid_local += tk[r] != (ENC_PAD >> 15);
     int nvalid = 0;
     block_exclusive_scan(nvalid_local, warp_sums, &nvalid);
-    for (int i = tid; i < nvalid; i += ENC_SORT_THREADS) tb.skeys[i] = keys[i];  // coalesced
+    for (int i = tid; i < nvalid; i += ENC_SORT_THREADS)  // coalesced; (token, position) widened to 32 + 32 bits
+        tb.skeys[i] = (static_cast<unsigned long long>(keys[i] >> 15) << 32) | (keys[i] & 0x7FFFu);
     // run starts; the run holding a window's first slot starts at the largest
     // start at or before it, the run holding its last slot ends before the
     // smallest start after it
@@ -499,6 +502,7 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
     using V4 = typename EV::V;
     constexpr int RB = sizeof(T) == 2 ? 16 : 8;  // rows in flight
     constexpr unsigned NONE = 0xFFFFFFFFu;
+    constexpr unsigned long long NONE64 = ~0ull;
     enc_grid_wait();
     enc_launch_dependents();
     const int bid = static_cast<int>(blockIdx.x);
@@ -524,20 +528,20 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
     if (base >= BT) return;
     const int c = (g * 32 + lane) * 4;
     const bool active = c < C;
-    const unsigned key = tb.skeys[min(base + lane, BT - 1)];
-    const unsigned pkey = base > 0 ? tb.skeys[base - 1] : NONE;
-    const unsigned nkey = base + ENC_WIN < BT ? tb.skeys[base + ENC_WIN] : NONE;
+    const unsigned long long key = tb.skeys[min(base + lane, BT - 1)];
+    const unsigned long long pkey = base > 0 ? tb.skeys[base - 1] : NONE64;
+    const unsigned long long nkey = base + ENC_WIN < BT ? tb.skeys[base + ENC_WIN] : NONE64;
     const int hstart = tb.win_head[w], tend = tb.win_tail[w];  // read only where defined (below)
     if (base >= nvalid) return;
     const int nv = min(ENC_WIN, nvalid - base);
     const bool valid = lane < nv;
-    const unsigned tok = key >> 15;
+    const unsigned tok = static_cast<unsigned>(key >> 32);
     unsigned ptok = __shfl_up_sync(0xffffffffu, tok, 1);
-    if (lane == 0) ptok = base > 0 ? pkey >> 15 : NONE;
+    if (lane == 0) ptok = base > 0 ? static_cast<unsigned>(pkey >> 32) : NONE;
     const unsigned smask = __ballot_sync(0xffffffffu, valid && tok != ptok);  // run starts
     const unsigned tok0 = __shfl_sync(0xffffffffu, tok, 0), tokl = __shfl_sync(0xffffffffu, tok, nv - 1);
     const bool head_cross = (smask & 1u) == 0;  // the first run began in an earlier window
-    const bool tail_cross = nv == ENC_WIN && base + ENC_WIN < nvalid && (nkey >> 15) == tokl;
+    const bool tail_cross = nv == ENC_WIN && base + ENC_WIN < nvalid && static_cast<unsigned>(nkey >> 32) == tokl;
     // windows wa..wb of the crossing runs: the head run's began at win_head; it
     // ends here unless it fills the window and crosses the tail too, where its
     // end and the tail run's end are win_tail
@@ -559,8 +563,8 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
             for (int u = 0; u < RB; ++u) {
                 constexpr unsigned one = 1u;
                 const int j = j0 + u;  // compile-time slot
-                const unsigned kj = __shfl_sync(0xffffffffu, key, j);
-                const int64_t r = kj & 0x7FFFu, t = kj >> 15;
+                const unsigned long long kj = __shfl_sync(0xffffffffu, key, j);
+                const int64_t r = static_cast<int64_t>(kj & 0xFFFFFFFFull), t = static_cast<int64_t>(kj >> 32);
                 v[u] = (active && ((vmask >> j) & one)) ? EV::ld(dout + r * C + c) : EV::zero();
                 o[u] = (active && ((emask >> j) & one)) ? EV::ld_plain(dwte + t * C + c) : EV::zero();
             }
@@ -570,7 +574,7 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
                 if ((vmask >> j) & 1u) {  // warp-uniform
                     EV::add(v[u], acc);
                     if ((emask >> j) & 1u) {  // run ends at slot j (warp-uniform)
-                        const int64_t t = __shfl_sync(0xffffffffu, key, j) >> 15;
+                        const int64_t t = static_cast<int64_t>(__shfl_sync(0xffffffffu, key, j) >> 32);
                         const unsigned below = j == 31 ? 0xffffffffu : (2u << j) - 1u;
                         const bool is_head = head_cross && (smask & below) == 0;
                         const bool is_tail = tail_cross && j == nv - 1;
@@ -597,6 +601,201 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
     if (head_cross) enc_cross_run<T>(dwte, tb, C, c, active, lane, w, g, G, 0, hspan, tok0, hacc, hold);
     if (tail_cross && smask != 0u)
         enc_cross_run<T>(dwte, tb, C, c, active, lane, w, g, G, 1, tspan, tokl, tacc, told);
+}
+
+// ---------------------------------------------------------------------------
+// The sort for more than ENC_FAST_MAX positions: a stable LSD radix sort of the
+// 64-bit keys (token << 32 | position) on 4-bit digits of the token, spread
+// over tiles of MB_TILE keys, three launches a pass and no wait between blocks:
+//   hist     every tile counts its keys per digit (H[digit][tile]);
+//   scan     one block turns H into exclusive prefixes in (digit, tile) order:
+//            where each tile's keys of each digit start in the output;
+//   scatter  every tile ranks its keys stably by digit (the packed per-thread
+//            counters of the one-block sort) and writes them there.
+// The initial keys are in position order, so the positions of a token end up
+// in increasing order. A last launch derives the window tables from the
+// sorted keys by binary search (a run is the range of one token).
+constexpr int ENC_FAST_MAX = 16384;  // positions the one-block sort takes
+constexpr int MB_KPT = 8;            // keys per thread of a tile
+constexpr int MB_TILE = MB_KPT * ENC_SORT_THREADS;
+
+__device__ __forceinline__ unsigned mb_digit(unsigned long long k, int sh) {
+    return static_cast<unsigned>(k >> (32 + sh)) & (ENC_DIGITS - 1);
+}
+
+// Keys in position order; ids outside [0, V) become padding (all ones, sorted
+// last) and are reported in the status word.
+__global__ void __launch_bounds__(256) enc_mb_keys_kernel(const int32_t* __restrict__ inp, int BT, int V,
+                                                          unsigned long long* __restrict__ dst) {
+    enc_grid_wait();
+    enc_launch_dependents();
+    for (int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i < BT;
+         i += static_cast<int>(gridDim.x * blockDim.x)) {
+        const int tok = inp[i];
+        unsigned long long key = ~0ull;
+        if (tok >= 0 && tok < V) {
+            key = (static_cast<unsigned long long>(tok) << 32) | static_cast<unsigned>(i);
+        } else if (atomicCAS(&g_enc_status[0], 0u, static_cast<unsigned>(-MMBWD_ERR_SHAPE)) == 0u) {
+            g_enc_status[1] = static_cast<unsigned>(i);
+            g_enc_status[2] = static_cast<unsigned>(tok);
+        }
+        dst[i] = key;
+    }
+}
+
+// H[d * ntiles + tile] = keys of the tile with digit d (integer counts).
+__global__ void __launch_bounds__(ENC_SORT_THREADS) enc_mb_hist_kernel(const unsigned long long* __restrict__ src,
+                                                                      int BT, int sh, int ntiles, int* __restrict__ H) {
+    enc_grid_wait();
+    enc_launch_dependents();
+    __shared__ int cnt[ENC_DIGITS];
+    const int tid = static_cast<int>(threadIdx.x), lane = tid & 31;
+    if (tid < ENC_DIGITS) cnt[tid] = 0;
+    __syncthreads();
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * MB_TILE;
+    int mine[ENC_DIGITS];
+#pragma unroll
+    for (int d = 0; d < ENC_DIGITS; ++d) mine[d] = 0;
+#pragma unroll
+    for (int r = 0; r < MB_KPT; ++r) {
+        const int64_t i = i0 + static_cast<int64_t>(r) * ENC_SORT_THREADS + tid;  // coalesced
+        const bool in = i < BT;
+        const unsigned d = in ? mb_digit(src[i], sh) : 0u;
+#pragma unroll
+        for (int dd = 0; dd < ENC_DIGITS; ++dd) mine[dd] += __popc(__ballot_sync(0xffffffffu, in && d == dd));
+    }
+    if (lane < ENC_DIGITS) {
+        int v = 0;
+#pragma unroll
+        for (int dd = 0; dd < ENC_DIGITS; ++dd) v = dd == lane ? mine[dd] : v;
+        atomicAdd(&cnt[lane], v);
+    }
+    __syncthreads();
+    if (tid < ENC_DIGITS) H[tid * ntiles + blockIdx.x] = cnt[tid];
+}
+
+// In place: H becomes its exclusive prefix sums (one block, in index order).
+__global__ void __launch_bounds__(ENC_SORT_THREADS) enc_mb_scan_kernel(int* __restrict__ H, int n) {
+    enc_grid_wait();
+    enc_launch_dependents();
+    __shared__ int warp_sums[32];
+    int carry = 0;
+    for (int b0 = 0; b0 < n; b0 += ENC_SORT_THREADS) {
+        const int i = b0 + static_cast<int>(threadIdx.x);
+        const int v = i < n ? H[i] : 0;
+        int total = 0;
+        const int before = block_exclusive_scan(v, warp_sums, &total);
+        if (i < n) H[i] = carry + before;
+        carry += total;
+    }
+}
+
+// Stable scatter of one tile by the digit at `sh`: thread t owns keys
+// i0 + t*MB_KPT .. +MB_KPT-1 (keys past BT take no part); their slots in the
+// tile sorted by digit come from the packed counters as in the one-block
+// sort, and O (the scanned H) gives where the tile's keys of each digit go.
+__global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
+    enc_mb_scatter_kernel(const unsigned long long* __restrict__ src, unsigned long long* __restrict__ dst, int BT,
+                          int sh, int ntiles, const int* __restrict__ O) {
+    enc_grid_wait();
+    enc_launch_dependents();
+    __shared__ int cnt[ENC_CNT_WORDS];
+    __shared__ int warp_sums[32];
+    __shared__ int row_start[ENC_DIGITS / 2 + 1];
+    __shared__ int gofs[ENC_DIGITS];
+    const int tid = static_cast<int>(threadIdx.x);
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * MB_TILE + static_cast<int64_t>(tid) * MB_KPT;
+    if (tid < ENC_DIGITS) gofs[tid] = O[tid * ntiles + blockIdx.x];
+    unsigned long long k[MB_KPT];
+    unsigned dg[MB_KPT];
+    int rank[MB_KPT];
+    uint64_t c0 = 0, c1 = 0;
+#pragma unroll
+    for (int r = 0; r < MB_KPT; ++r) {
+        const bool in = i0 + r < BT;
+        k[r] = in ? src[i0 + r] : ~0ull;
+        dg[r] = mb_digit(k[r], sh);
+        const int f = 8 * static_cast<int>(dg[r] & 7u);
+        rank[r] = static_cast<int>((((dg[r] & 8u) ? c1 : c0) >> f) & 0xFFu);
+        if (in) {
+            if (dg[r] & 8u) c1 += uint64_t(1) << f;
+            else c0 += uint64_t(1) << f;
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < ENC_DIGITS / 2; ++kk) {
+        const uint64_t c = kk < 4 ? c0 : c1;
+        const int f = 16 * (kk & 3);
+        cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)] = static_cast<int>(((c >> f) & 0xFFu) | (((c >> (f + 8)) & 0xFFu) << 16));
+    }
+    __syncthreads();
+    {
+        int loc[ENC_DIGITS / 2];
+        int sum = 0;
+#pragma unroll
+        for (int q = 0; q < ENC_DIGITS / 2; ++q) {
+            loc[q] = cnt[enc_cnt_at(tid * (ENC_DIGITS / 2) + q)];
+            sum += loc[q];
+        }
+        int total = 0;
+        int before = block_exclusive_scan(sum, warp_sums, &total);
+        if ((tid & (ENC_SORT_THREADS / (ENC_DIGITS / 2) - 1)) == 0)
+            row_start[tid / (ENC_SORT_THREADS / (ENC_DIGITS / 2))] = before;
+        if (tid == 0) row_start[ENC_DIGITS / 2] = total;
+#pragma unroll
+        for (int q = 0; q < ENC_DIGITS / 2; ++q) {
+            cnt[enc_cnt_at(tid * (ENC_DIGITS / 2) + q)] = before;
+            before += loc[q];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < MB_KPT; ++r) {
+        if (i0 + r >= BT) continue;
+        const unsigned d = dg[r];
+        const int kk = static_cast<int>(d >> 1);
+        const unsigned pw = static_cast<unsigned>(cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)]);
+        const unsigned rs = static_cast<unsigned>(row_start[kk]), rs1 = static_cast<unsigned>(row_start[kk + 1]);
+        // the tile's first slot of digit d and this key's slot in the sorted tile
+        const unsigned dstart = (d & 1u) ? (rs >> 16) + (rs1 & 0xFFFFu) : (rs & 0xFFFFu) + (rs >> 16);
+        const unsigned first = (d & 1u) ? (pw >> 16) + (rs1 & 0xFFFFu) : (pw & 0xFFFFu) + (rs >> 16);
+        dst[gofs[d] + static_cast<int64_t>(first + rank[r] - dstart)] = k[r];
+    }
+}
+
+__device__ __forceinline__ int mb_lower_bound(const unsigned long long* keys, int n, unsigned tok) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<unsigned>(keys[mid] >> 32) < tok) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Window tables from the sorted keys: valid count (the first padding key),
+// per window of 32 slots where the run (token) of its first slot begins and
+// where the run of its last slot ends, the problem's sizes, cleared counters.
+__global__ void __launch_bounds__(256) enc_mb_tables_kernel(int BT, int V, int C, int G, EncTables tb) {
+    enc_grid_wait();
+    enc_launch_dependents();
+    const int nvalid = mb_lower_bound(tb.skeys, BT, 0xFFFFFFFFu);
+    const int nwin = (nvalid + ENC_WIN - 1) / ENC_WIN;
+    const int stride = static_cast<int>(gridDim.x * blockDim.x);
+    const int g0 = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+    for (int w = g0; w < nwin; w += stride) {
+        const int base = w * ENC_WIN, last = min(base + ENC_WIN, nvalid) - 1;
+        tb.win_head[w] = mb_lower_bound(tb.skeys, nvalid, static_cast<unsigned>(tb.skeys[base] >> 32));
+        const unsigned tl = static_cast<unsigned>(tb.skeys[last] >> 32);
+        tb.win_tail[w] = (tl == 0xFFFFFFFEu ? nvalid : mb_lower_bound(tb.skeys, nvalid, tl + 1u)) - 1;
+    }
+    for (int e = g0; e < nwin * G; e += stride) tb.arrivals[e] = 0u;
+    if (g0 == 0) {
+        tb.meta[0] = nvalid;
+        tb.meta[1] = BT;
+        tb.meta[2] = V;
+        tb.meta[3] = C;
+    }
 }
 
 cudaError_t launch_pdl(const void* k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void** args) {
@@ -648,13 +847,18 @@ size_t enc_tables_layout(uint8_t* base, int64_t BT, int64_t C, EncTables* tb) {
         return p;
     };
     uint8_t* meta = take(4 * 4);
-    uint8_t* skeys = take(n * 4);
+    uint8_t* skeys = take(n * 8);
     uint8_t* whead = take(nwin * 4);
     uint8_t* wtail = take(nwin * 4);
     uint8_t* arr = take(nwin * static_cast<size_t>(enc_groups(C, 4)) * 4);
+    const bool mb = BT > ENC_FAST_MAX;
+    uint8_t* alt = mb ? take(n * 8) : nullptr;
+    uint8_t* hist = mb ? take(static_cast<size_t>(ENC_DIGITS) * ((n + MB_TILE - 1) / MB_TILE) * 4) : nullptr;
     if (tb) {
+        tb->mb_alt = reinterpret_cast<unsigned long long*>(alt);
+        tb->mb_hist = reinterpret_cast<int*>(hist);
         tb->meta = reinterpret_cast<int*>(meta);
-        tb->skeys = reinterpret_cast<unsigned*>(skeys);
+        tb->skeys = reinterpret_cast<unsigned long long*>(skeys);
         tb->win_head = reinterpret_cast<int*>(whead);
         tb->win_tail = reinterpret_cast<int*>(wtail);
         tb->arrivals = reinterpret_cast<unsigned*>(arr);
@@ -667,9 +871,57 @@ size_t enc_partials_bytes(int64_t BT, int64_t C) {
     return a256(nwin * 2 * static_cast<size_t>(C) * 4);
 }
 
+// The multi-block sort (B*T > ENC_FAST_MAX) and the window tables: keys,
+// then per pass hist, scan and scatter (the buffers alternate so that the last
+// pass writes tb.skeys), then the tables.
+cudaError_t enc_mb_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C, const EncTables& tb,
+                               cudaStream_t stream) {
+    int token_bits = 0;
+    while ((int64_t(1) << token_bits) <= V) ++token_bits;
+    const int passes = (token_bits + ENC_DIGIT_BITS - 1) / ENC_DIGIT_BITS;
+    int ntiles = (BT + MB_TILE - 1) / MB_TILE, BTi = BT, Vi = static_cast<int>(V), Ci = static_cast<int>(C);
+    int G = enc_groups(C, 4);
+    unsigned long long* src = (passes % 2 == 0) ? tb.skeys : tb.mb_alt;
+    const int kblocks = std::max(1, std::min((BT + 255) / 256, 4096));
+    {
+        void* args[] = {const_cast<int32_t**>(&inp), &BTi, &Vi, &src};
+        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&enc_mb_keys_kernel), dim3(kblocks), dim3(256), 0,
+                                   stream, args);
+        if (e != cudaSuccess) return e;
+    }
+    int* H = tb.mb_hist;
+    int nh = ENC_DIGITS * ntiles;
+    for (int pass = 0; pass < passes; ++pass) {
+        int sh = pass * ENC_DIGIT_BITS;
+        unsigned long long* dst = src == tb.skeys ? tb.mb_alt : tb.skeys;
+        void* hargs[] = {&src, &BTi, &sh, &ntiles, &H};
+        cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&enc_mb_hist_kernel), dim3(ntiles),
+                                   dim3(ENC_SORT_THREADS), 0, stream, hargs);
+        if (e != cudaSuccess) return e;
+        void* sargs[] = {&H, &nh};
+        e = launch_pdl(reinterpret_cast<const void*>(&enc_mb_scan_kernel), dim3(1), dim3(ENC_SORT_THREADS), 0, stream,
+                       sargs);
+        if (e != cudaSuccess) return e;
+        void* xargs[] = {&src, &dst, &BTi, &sh, &ntiles, &H};
+        e = launch_pdl(reinterpret_cast<const void*>(&enc_mb_scatter_kernel), dim3(ntiles), dim3(ENC_SORT_THREADS), 0,
+                       stream, xargs);
+        if (e != cudaSuccess) return e;
+        src = dst;
+    }
+    EncTables t = tb;
+    void* targs[] = {&BTi, &Vi, &Ci, &G, &t};
+    const int nwin = (BT + ENC_WIN - 1) / ENC_WIN;
+    return launch_pdl(reinterpret_cast<const void*>(&enc_mb_tables_kernel),
+                      dim3(static_cast<unsigned>(std::max(1, std::min((nwin * G + 255) / 256, 4096)))), dim3(256), 0,
+                      stream, targs);
+}
+
 // The sort: block 0 builds the tables; `wpe_blocks` more blocks form dwpe.
+// Above ENC_FAST_MAX positions the multi-block sort runs instead and forms no
+// dwpe (the caller adds dwpe blocks to the window launch).
 cudaError_t enc_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C, int64_t B, int64_t T, int dtype,
                             const EncTables& tb, void* dwpe, const void* dout, int wpe_blocks, cudaStream_t stream) {
+    if (BT > ENC_FAST_MAX) return enc_mb_sort_launch(inp, BT, V, C, tb, stream);
     int kpl = 1;
     while (kpl * ENC_SORT_THREADS < BT) kpl <<= 1;
     // sort on the smallest b with 2^b > V: the padding's digits (all ones) then
@@ -726,6 +978,13 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
     tb.partials = reinterpret_cast<float*>(w + tbytes);
     tb.sr = sr ? 1 : 0;
     tb.seed = seed;
+    if (BT > ENC_FAST_MAX) {  // multi-block sort; dwpe beside the window sums, as in a planned run
+        cudaError_t e = enc_sort_launch(inp, BT, V, C, B, T, dtype, tb, nullptr, nullptr, 0, stream);
+        if (e != cudaSuccess) return e;
+        const int64_t width = 32 * std::min(enc_groups(C, 4), 8);
+        const int wb = static_cast<int>(std::min<int64_t>((T * C / N + width - 1) / width, 2 * std::max(num_sms, 1)));
+        return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, wb, stream);
+    }
     // block 0 sorts; one wave of blocks (at most one per SM besides it) forms dwpe
     const int64_t wpe_threads = (T * C / N + ENC_SORT_THREADS - 1) / ENC_SORT_THREADS;
     const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, std::max(num_sms - 1, 1)));

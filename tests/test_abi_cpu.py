@@ -240,7 +240,7 @@ def test_encoder_rejects_bad_arguments():
                                              V=100, dtype=mm.BF16, stream=0), **kw})
     assert f(dtype=5) == mm.ERR_DTYPE
     assert f(T=-1) == mm.ERR_SHAPE
-    assert f(B=2, T=8193) == mm.ERR_SHAPE             # above ENCBWD_MAX_POSITIONS
+    assert f(B=2, T=(1 << 23) + 1) == mm.ERR_SHAPE    # above ENCBWD_MAX_POSITIONS
     assert f(V=131072) == mm.ERR_SHAPE                # above ENCBWD_MAX_VOCAB
     assert f(C=65536 + 8) == mm.ERR_SHAPE             # above ENCBWD_MAX_CHANNELS
     assert f(dout=None) == mm.ERR_NULL

@@ -221,3 +221,70 @@ def test_encoder_planned_matches_one_call_and_plan_reuse():
             assert status == mm.ERR_SHAPE and info[0] == -1
             for k in c:
                 assert torch.equal(c[k], before[k]), k
+
+
+# Above 16384 positions the sort runs over many blocks (a radix sort of
+# 64-bit keys, three launches a pass): ragged counts just past the one-block
+# limit, GPT-2 sized batches of 65536 positions, a one-token run spanning
+# every tile, invalid ids, fp32 and stochastic rounding, the planned form.
+LARGE = [(1, 16385, 64, 50304, "bf16"), (2, 10007, 96, 1000, "f32"), (64, 1024, 768, 50304, "bf16"),
+         (16, 4096, 128, 131071, "bf16")]
+
+
+@pytest.mark.parametrize("case", LARGE, ids=lambda c: "x".join(map(str, c)))
+def test_encoder_multiblock_sort_parity(case):
+    B, T, C, V, dtype = case
+    x = problem(B, T, C, V, dtype, v_used=min(V, 50257))
+    g = run_enc(x, B, T, C, V, dtype)
+    check(x, g, B, T, V, dtype)
+    assert mm.mmbwd_device_status()[0] == mm.OK
+    again = run_enc(x, B, T, C, V, dtype)
+    for k in ("dwte", "dwpe"):
+        assert np.array_equal(to_host(g[k], dtype), to_host(again[k], dtype)), k
+
+
+def test_encoder_multiblock_one_token_and_invalid_ids():
+    B, T, C, V, dtype = 4, 9000, 64, 300, "bf16"
+    x = problem(B, T, C, V, dtype)
+    x["inp"][:] = 7
+    g = run_enc(x, B, T, C, V, dtype)
+    check(x, g, B, T, V, dtype)
+    # invalid ids are skipped (and reported), the rest is summed
+    x = problem(B, T, C, V, dtype, seed=2)
+    bad = np.array([5, 17000, 35999])
+    x["inp"][bad] = V + 3
+    g = run_enc(x, B, T, C, V, dtype)
+    status, info = mm.mmbwd_device_status(reset=True)
+    assert status == mm.ERR_SHAPE and info[1] == V + 3
+    keep = x["inp"] < V
+    ref_x = dict(x, inp=np.where(keep, x["inp"], 0).astype(np.int32),
+                 dout=np.where(keep[:, None], x["dout"], 0).astype(x["dout"].dtype))
+    ref_wte, _ = oracle.get("omp").encoder_backward(ref_x["dout"], ref_x["inp"], B, T, V, dtype, x["dwte"], x["dwpe"])
+    assert_close(to_host(g["dwte"], dtype), ref_wte, dtype, "dwte")
+
+
+def test_encoder_multiblock_planned_and_sr():
+    import torch
+
+    B, T, C, V = 8, 4096, 256, 50304
+    x = problem(B, T, C, V, "bf16", v_used=50257, seed=3)
+    one = run_enc(x, B, T, C, V, "bf16")
+    g = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+    gi = torch.from_numpy(x["inp"]).to("cuda:0")
+    n = mm.encbwd_plan_bytes(B, T, C, V, mm.BF16)
+    plan = torch.empty(n, dtype=torch.uint8, device="cuda:0")
+    assert mm.encbwd_prepare(plan, n, gi, B, T, C, V, mm.BF16) == mm.OK
+    assert mm.encbwd_run_planned(g["dwte"], g["dwpe"], g["dout"], plan, B, T, C, V, mm.BF16) == mm.OK
+    torch.cuda.synchronize()
+    for k in ("dwte", "dwpe"):
+        assert torch.equal(g[k], one[k]), k
+    # stochastic rounding, repeatable per seed
+    outs = []
+    for _ in range(2):
+        h = {k: to_dev(x[k], "bf16") for k in ("dout", "dwte", "dwpe")}
+        assert mm.encbwd_run_sr(h["dwte"], h["dwpe"], h["dout"], gi, B, T, C, V, mm.BF16, 99) == mm.OK
+        torch.cuda.synchronize()
+        outs.append(h)
+    for k in ("dwte", "dwpe"):
+        assert torch.equal(outs[0][k], outs[1][k]), k
+    check(x, outs[0], B, T, V, "bf16")
