@@ -43,9 +43,12 @@
 extern "C" {
 #endif
 
-/* Largest C accepted (16-byte vectors, at most 16 per lane of a warp). */
-#define LNBWD_MAX_C_BF16 4096
-#define LNBWD_MAX_C_F32 2048
+/* Largest C accepted. Rows up to 4096 (bf16) / 2048 (fp32) wide are staged
+ * whole in shared memory by one fused kernel; wider rows take two passes over
+ * global memory (the row sums, then column tiles), with the same result
+ * contract. */
+#define LNBWD_MAX_C_BF16 (1 << 20)
+#define LNBWD_MAX_C_F32 (1 << 20)
 
 /*
  * lnbwd_run -- enqueue the LayerNorm backward of B*T rows of width C on `stream`.

@@ -64,7 +64,7 @@ SIGNATURES = {
     "encbwd_workspace_bytes": ([_i64] * 4 + [_ci], _sz),
     "lnbwd_workspace_bytes": ([_i64] * 3 + [_ci], _sz),
 }
-LNBWD_MAX_C = {F32: 2048, BF16: 4096}  # LNBWD_MAX_C_F32, LNBWD_MAX_C_BF16
+LNBWD_MAX_C = {F32: 1 << 20, BF16: 1 << 20}  # LNBWD_MAX_C_F32, LNBWD_MAX_C_BF16
 ENCBWD_MAX_POSITIONS, ENCBWD_MAX_VOCAB, ENCBWD_MAX_CHANNELS = 1 << 24, 131071, 65536
 
 _lock = threading.Lock()

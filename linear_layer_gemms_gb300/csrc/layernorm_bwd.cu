@@ -52,6 +52,10 @@ constexpr int LN_MAX_VPT = 2;  // 16-byte vectors per thread and row
 constexpr int LN_PARAM_WARPS = 32;
 constexpr int LN_STAGES = 4;  // row buffers per team (three rows in flight)
 constexpr unsigned long long LN_TIMEOUT_NS = 2000000000ull;
+// Widest rows of the fused rows kernel (row ring and weights in shared memory,
+// at most two 16-byte vectors per thread); wider rows take the two-pass path.
+constexpr int LN_FUSED_MAX_C_BF16 = 4096;
+constexpr int LN_FUSED_MAX_C_F32 = 2048;
 
 enum LnSite { LN_SITE_FULL = 2, LN_SITE_TEARDOWN = 4 };
 
@@ -379,6 +383,116 @@ __global__ void __launch_bounds__(LN_PARAM_WARPS * 32)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Rows too wide for the fused kernel (its row buffers and weights in shared
+// memory): two passes over global memory, any C.
+//   ln_wide_sums_kernel: one warp per row (grid-stride) forms the row's two
+//     sums, sum of g = w*dout and of g*n, lanes over 16-byte vectors in order
+//     and an xor butterfly, and stores them as a float pair;
+//   ln_wide_cols_kernel: block (column tile of 256 vectors, range of rows);
+//     each thread owns one vector of the tile, walks the block's rows in order
+//     (four rows' loads in flight) applying dinp += rstd (g - a - n c), and
+//     keeps its columns' n*dout and dout sums in registers; one fp32 partial
+//     row pair per block, which the params kernel adds in block order.
+constexpr int LN_WIDE_TILE = 256;  // vectors per column tile (one per thread)
+
+template <typename T>
+__global__ void __launch_bounds__(256) ln_wide_sums_kernel(const T* __restrict__ dout, const T* __restrict__ inp,
+                                                           const T* __restrict__ weight, const float* __restrict__ mean,
+                                                           const float* __restrict__ rstd, float2* __restrict__ sums,
+                                                           int64_t BT, int C) {
+    using E = LnElem<T>;
+    constexpr int N = E::N;
+    ln_grid_wait();
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int nvec = C / N;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < BT; r += warps) {
+        const float m = mean[r], sd = rstd[r];
+        const uint4* dr = reinterpret_cast<const uint4*>(dout + r * C);
+        const uint4* xr = reinterpret_cast<const uint4*>(inp + r * C);
+        float sa = 0.f, sc = 0.f;
+        for (int v = lane; v < nvec; v += 32) {
+            float d[N], x[N], w[N];
+            E::unpack(__ldg(dr + v), d);
+            E::unpack(__ldg(xr + v), x);
+            E::unpack(__ldg(reinterpret_cast<const uint4*>(weight) + v), w);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const float g = w[e] * d[e];
+                sa += g;
+                sc += g * ((x[e] - m) * sd);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sa += __shfl_xor_sync(0xffffffffu, sa, off);
+            sc += __shfl_xor_sync(0xffffffffu, sc, off);
+        }
+        if (lane == 0) sums[r] = make_float2(sa, sc);
+    }
+    ln_launch_dependents();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(LN_WIDE_TILE) ln_wide_cols_kernel(const LnParams p, const float2* __restrict__ sums) {
+    using E = LnElem<T>;
+    constexpr int N = E::N;
+    ln_grid_wait();
+    const int v = static_cast<int>(blockIdx.x) * LN_WIDE_TILE + static_cast<int>(threadIdx.x);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * p.rows_per_block;
+    const int64_t r1 = r0 + p.rows_per_block < p.BT ? r0 + p.rows_per_block : p.BT;
+    const int C = p.C;
+    float acc_w[N], acc_b[N], w[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) acc_w[e] = acc_b[e] = w[e] = 0.f;
+    const bool on = v < p.nvec;
+    if (on) E::unpack(__ldg(reinterpret_cast<const uint4*>(p.weight) + v), w);
+    const float inv_c = 1.f / static_cast<float>(C);
+    constexpr int RU = 4;  // rows in flight
+    for (int64_t rb = r0; rb < r1 && on; rb += RU) {
+        uint4 dv[RU], xv[RU], ov[RU];
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const int64_t r = rb + u < r1 ? rb + u : r1 - 1;
+            dv[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + r * C) + v);
+            xv[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.inp) + r * C) + v);
+            ov[u] = *(reinterpret_cast<const uint4*>(static_cast<const T*>(p.dinp) + r * C) + v);
+        }
+#pragma unroll
+        for (int u = 0; u < RU; ++u) {
+            const int64_t r = rb + u;
+            if (r >= r1) break;
+            const float m = __ldg(p.mean + r), sd = __ldg(p.rstd + r);
+            const float2 sm = sums[r];
+            const float a = sm.x * inv_c, c = sm.y * inv_c;
+            const float sda = sd * a, sdc = sd * c;
+            float d[N], x[N], o[N];
+            E::unpack(dv[u], d);
+            E::unpack(xv[u], x);
+            E::unpack(ov[u], o);
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+                const float n = (x[e] - m) * sd;
+                o[e] += fmaf(sd, w[e] * d[e], -fmaf(sdc, n, sda));
+                acc_w[e] = fmaf(n, d[e], acc_w[e]);
+                acc_b[e] += d[e];
+            }
+            __stcg(reinterpret_cast<uint4*>(static_cast<T*>(p.dinp) + r * C) + v, E::pack(o));
+        }
+    }
+    ln_launch_dependents();
+    if (on) {
+        float* dst = p.partials + static_cast<size_t>(blockIdx.y) * 2 * C + static_cast<size_t>(v) * N;
+#pragma unroll
+        for (int e = 0; e < N; e += 4) {
+            __stcg(reinterpret_cast<float4*>(dst + e), make_float4(acc_w[e], acc_w[e + 1], acc_w[e + 2], acc_w[e + 3]));
+            __stcg(reinterpret_cast<float4*>(dst + C + e),
+                   make_float4(acc_b[e], acc_b[e + 1], acc_b[e + 2], acc_b[e + 3]));
+        }
+    }
+}
+
 template <typename T, int VPT>
 const void* rows_kernel_p(int P) {
     switch (P) {
@@ -419,6 +533,19 @@ cudaError_t ln_make_plan(int64_t BT, int C, int dtype, int num_sms, LnPlan* plan
     *plan = LnPlan{};
     const int N = ln_vec_elems(dtype);
     const int nvec = C / N;
+    if (C > (dtype == MMBWD_F32 ? LN_FUSED_MAX_C_F32 : LN_FUSED_MAX_C_BF16)) {
+        // wide rows: column tiles x row blocks, about four blocks per SM
+        plan->wide = 1;
+        plan->col_tiles = (nvec + LN_WIDE_TILE - 1) / LN_WIDE_TILE;
+        int64_t row_blocks = std::max<int64_t>(1, (4 * static_cast<int64_t>(std::max(num_sms, 1)) + plan->col_tiles - 1) /
+                                                      plan->col_tiles);
+        row_blocks = std::min<int64_t>(row_blocks, std::min<int64_t>(BT, 65535));
+        const int64_t rows = (BT + row_blocks - 1) / row_blocks;
+        plan->rows_per_block = rows;
+        plan->grid = static_cast<int>((BT + rows - 1) / rows);  // row blocks, none empty
+        plan->ws_bytes = static_cast<size_t>(plan->grid) * 2 * static_cast<size_t>(C) * 4 + static_cast<size_t>(BT) * 8;
+        return cudaSuccess;
+    }
     // team width: the fewest warps (a power of two) that cover a row with at
     // most two vectors per thread
     int P = 1;
@@ -468,10 +595,30 @@ cudaError_t ln_launch(const LnPlan& plan, void* dinp, void* dweight, void* dbias
     p.nvec = C / ln_vec_elems(dtype);
     p.team_warps = plan.team_warps;
     p.off_ring = static_cast<uint32_t>(plan.off_ring);
-    const void* k = dtype == MMBWD_F32 ? rows_kernel_for<float>(plan.vpl, plan.team_warps)
-                                       : rows_kernel_for<__nv_bfloat16>(plan.vpl, plan.team_warps);
-    void* args[] = {&p};
-    cudaError_t e = launch_pdl(k, dim3(plan.grid), dim3(LN_THREADS), plan.smem, stream, args);
+    cudaError_t e = cudaSuccess;
+    if (plan.wide) {
+        // row sums after the partials (the workspace holds [grid][2][C] fp32, then the pairs)
+        float2* sums = reinterpret_cast<float2*>(p.partials + static_cast<size_t>(plan.grid) * 2 * C);
+        const void* sk = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&ln_wide_sums_kernel<float>)
+                                            : reinterpret_cast<const void*>(&ln_wide_sums_kernel<__nv_bfloat16>);
+        int64_t bt = BT;
+        int c = C;
+        void* sargs[] = {const_cast<void**>(&dout), const_cast<void**>(&inp), const_cast<void**>(&weight),
+                         const_cast<float**>(&mean), const_cast<float**>(&rstd), &sums, &bt, &c};
+        const unsigned sblocks = static_cast<unsigned>(std::min<int64_t>((BT + 7) / 8, 65535));
+        e = launch_pdl(sk, dim3(sblocks), dim3(256), 0, stream, sargs);
+        if (e != cudaSuccess) return e;
+        const void* ck = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&ln_wide_cols_kernel<float>)
+                                            : reinterpret_cast<const void*>(&ln_wide_cols_kernel<__nv_bfloat16>);
+        void* cargs[] = {&p, &sums};
+        e = launch_pdl(ck, dim3(static_cast<unsigned>(plan.col_tiles), static_cast<unsigned>(plan.grid)),
+                       dim3(LN_WIDE_TILE), 0, stream, cargs);
+    } else {
+        const void* k = dtype == MMBWD_F32 ? rows_kernel_for<float>(plan.vpl, plan.team_warps)
+                                           : rows_kernel_for<__nv_bfloat16>(plan.vpl, plan.team_warps);
+        void* args[] = {&p};
+        e = launch_pdl(k, dim3(plan.grid), dim3(LN_THREADS), plan.smem, stream, args);
+    }
     if (e != cudaSuccess) return e;
     const unsigned pblocks = static_cast<unsigned>((2 * C + 31) / 32);
     const void* pk = dtype == MMBWD_F32 ? reinterpret_cast<const void*>(&ln_bwd_params_kernel<float>)

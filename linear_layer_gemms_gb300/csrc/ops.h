@@ -70,6 +70,7 @@ cudaError_t enc_read_status(int* code, int* info3, bool reset);
 // ---------------------------------------------------------------- LayerNorm backward
 
 struct LnPlan {
+    int wide = 0;            // 1: rows too wide for the fused kernel (row sums, then column tiles)
     int vpl = 0;             // 16-byte column vectors per thread and row
     int team_warps = 0;      // warps that share one row
     int warps = 0;           // warps per block
@@ -77,7 +78,8 @@ struct LnPlan {
     int64_t rows_per_block = 0;
     size_t off_ring = 0;     // start of the teams' row buffers in shared memory
     size_t smem = 0;         // weight (fp32) + row-sum exchange + barriers + row buffers
-    size_t ws_bytes = 0;     // per-block partial sums, fp32 [grid][2][C]
+    size_t ws_bytes = 0;     // per-block partial sums, fp32 [grid][2][C] (+ the row sums when wide)
+    int col_tiles = 0;       // wide: column tiles of 256 vectors
 };
 
 int ln_vec_elems(int dtype);

@@ -242,6 +242,9 @@ LN_WORKLOADS = {
     "ln_gpt2_small": LNProblem("ln_gpt2_small", 8, 1024, 768, "bf16"),
     "ln_xl": LNProblem("ln_xl", 8, 1024, 1600, "bf16"),
     "ln_xl_f32": LNProblem("ln_xl_f32", 8, 1024, 1600, "f32"),
+    # rows wider than the fused kernel stages in shared memory (a 12800-wide
+    # hidden state, eight times GPT-2 XL's)
+    "ln_wide": LNProblem("ln_wide", 4, 1024, 12800, "bf16"),
 }
 
 

@@ -188,8 +188,8 @@ def test_layernorm_rejects_bad_arguments():
                                              dtype=mm.BF16, stream=0), **kw})
     assert f(dtype=2) == mm.ERR_DTYPE
     assert f(T=-1) == mm.ERR_SHAPE
-    assert f(C=4104) == mm.ERR_SHAPE                  # above LNBWD_MAX_C_BF16
-    assert f(C=2052, dtype=mm.F32) == mm.ERR_SHAPE    # above LNBWD_MAX_C_F32
+    assert f(C=(1 << 20) + 8) == mm.ERR_SHAPE            # above LNBWD_MAX_C_BF16
+    assert f(C=(1 << 20) + 4, dtype=mm.F32) == mm.ERR_SHAPE  # above LNBWD_MAX_C_F32
     assert f(B=1 << 40, T=1 << 40) == mm.ERR_SHAPE
     assert f(mean=None) == mm.ERR_NULL
     assert f(weight=None) == mm.ERR_NULL
@@ -201,7 +201,7 @@ def test_layernorm_rejects_bad_arguments():
     assert f(dbias=2 * A + 16) == mm.ERR_ALIAS        # dbias overlaps dweight
     assert f(dweight=7 * A) == mm.ERR_ALIAS           # dweight on top of mean
     assert mm.lnbwd_workspace_bytes(-1, 8, 64, mm.BF16) == 0
-    assert mm.LNBWD_MAX_C == {mm.F32: 2048, mm.BF16: 4096}
+    assert mm.LNBWD_MAX_C == {mm.F32: 1 << 20, mm.BF16: 1 << 20}
 
 
 def test_sr_rejects_fp32_and_bad_arguments():

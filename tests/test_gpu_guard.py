@@ -144,7 +144,7 @@ def test_forward_guard_bands(monkeypatch, dtype, path, shape):
     assert scaled_error(to_host(out.t, dtype), ref) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("dtype,C", [("bf16", 264), ("bf16", 1600), ("f32", 392)])
+@pytest.mark.parametrize("dtype,C", [("bf16", 264), ("bf16", 1600), ("f32", 392), ("bf16", 6408), ("f32", 2060)])
 def test_layernorm_guard_bands(dtype, C):
     import torch
 
