@@ -1056,7 +1056,7 @@ long env_long(const char* name, long dflt) {
 double t_kb(int bn) { return bn == 256 ? 0.31 : 0.29; }
 double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
 double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
-constexpr double T_ITEM = 0.3;                                 // per-item handoff
+constexpr double T_ITEM = 1.0;                                 // per-item handoff (first data of the next item, measured)
 
 struct ItemCost {
     double run, epi;
