@@ -1056,7 +1056,7 @@ long env_long(const char* name, long dflt) {
 double t_kb(int bn) { return bn == 256 ? 0.31 : 0.29; }
 double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
 double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
-constexpr double T_ITEM = 1.0;                                 // per-item handoff (first data of the next item, measured)
+constexpr double T_ITEM = 0.3;                                 // per-item handoff
 
 struct ItemCost {
     double run, epi;
@@ -1076,12 +1076,13 @@ ItemCost item_cost(const TcPlan& pl, int w) {
 
 double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
     if (pl.splits == 1) return 0.0;
-    // a launch gap plus S fp32 partials read and dweight read and written, and
-    // the partial stores (L2-resident: 4 MB/us; with this, the GPT-2 attention
-    // projection takes the plan that measured fastest, single pairs and 4 splits,
-    // 30.4 us against 31.4 with 3 splits and 32.2 with two pairs and 3 splits)
+    // a launch gap, about 1 us per split (each adds a wave of partial-store
+    // epilogues), and the S fp32 partials read and dweight read and written
+    // (L2-resident: 4 MB/us). Fitted to the GPT-2 attention projection, timed
+    // back to back with 2, 3, 4 and 5 splits: 31.8, 27.7, 30.0, 29.3 us
+    // against 31.8, 26.9, 27.7, 29.5 modelled.
     const double bytes = static_cast<double>(OC) * C * (4.0 * pl.splits + 4.0);
-    return 6.0 + bytes / 4e6;
+    return 6.0 + 1.0 * pl.splits + bytes / 4e6;
 }
 
 // Longest-first greedy assignment of items to pairs; fills pl.sched and
