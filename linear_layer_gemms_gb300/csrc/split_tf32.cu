@@ -12,9 +12,14 @@
 // Layouts (every product becomes D += A . B^T with both operands K-major):
 //   dinp    (BT x C) += dout (BT x OC) . (weight^T) (C x OC)^T   A = dout,    B = weight^T
 //   dweight (OC x C) += (dout^T) (OC x BT) . (inp^T) (C x BT)^T  A = dout^T,  B = inp^T
-// so dout is split in place and transposed, weight and inp transposed. The
-// transposing pass over dout also sums each 32-row tile of every column, and
-// a second small kernel adds those tile sums in tile order: dbias.
+// so dout's low parts are written with its own layout and both parts
+// transposed, weight and inp transposed. The tensor core reads an fp32
+// operand of a tf32 product as its tf32 truncation (the low 13 mantissa bits
+// ignored: measured bit for bit on GB300, the raw dout in place of its cleared
+// copy gave identical results), so a tensor in its own layout serves as its
+// own high part and only its low part is copied. The transposing pass over
+// dout also sums each 32-row tile of every column, and a second small kernel
+// adds those tile sums in tile order: dbias.
 #include "../../include/mmbwd.h"
 #include "internal.h"
 #include "ops.h"
@@ -30,7 +35,7 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 }
 
 // src (R x Cc, row-major) in 32 x 32 tiles, 256 threads (32 x 8):
-//   COPY:   hi / lo with the layout of src
+//   COPY:   lo with the layout of src (src itself is the high part)
 //   TRANS:  thi / tlo = the transpose (Cc x R), row pitch ldT
 //   COLSUM: part[tile row][c] = sum of the tile's rows of column c, in row order
 template <bool COPY, bool TRANS, bool COLSUM>
@@ -50,7 +55,6 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ sr
             if (COPY) {
                 float h, l;
                 split_tf32(x, h, l);
-                hi[r * Cc + c] = h;
                 lo[r * Cc + c] = l;
             }
         }
@@ -77,14 +81,30 @@ __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ sr
     }
 }
 
-// dbias[c] = sum over tile rows of part[.][c], in tile order (overwrite).
-__global__ void __launch_bounds__(256) tile_sum_kernel(float* __restrict__ dbias, const float* __restrict__ part,
-                                                       int64_t tiles, int64_t Cc) {
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= Cc) return;
+// dbias[c] = sum over tile rows of part[.][c] (overwrite), in a fixed order:
+// 32 columns per block, 8 slices of the tile rows; slice j sums its rows in
+// order (eight loads in flight), then the slices are added in slice order.
+constexpr int TS_SLICES = 8;
+__global__ void __launch_bounds__(32 * TS_SLICES) tile_sum_kernel(float* __restrict__ dbias,
+                                                                  const float* __restrict__ part, int64_t tiles,
+                                                                  int64_t Cc) {
+    __shared__ float red[TS_SLICES][32];
+    const int lane = static_cast<int>(threadIdx.x & 31), j = static_cast<int>(threadIdx.x >> 5);
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
+    const int64_t per = (tiles + TS_SLICES - 1) / TS_SLICES;
+    const int64_t k0 = j * per, k1 = k0 + per < tiles ? k0 + per : tiles;
     float s = 0.f;
-    for (int64_t k = 0; k < tiles; ++k) s += part[k * Cc + c];
-    dbias[c] = s;
+    if (c < Cc) {
+#pragma unroll 8
+        for (int64_t k = k0; k < k1; ++k) s += part[k * Cc + c];
+    }
+    red[j][lane] = s;
+    __syncthreads();
+    if (j == 0 && c < Cc) {
+        float t = red[0][lane];
+        for (int q = 1; q < TS_SLICES; ++q) t += red[q][lane];
+        dbias[c] = t;
+    }
 }
 
 template <bool COPY, bool TRANS, bool COLSUM>
@@ -104,7 +124,7 @@ size_t x3_workspace_bytes(int64_t BT, int64_t C, int64_t OC, bool bias) {
     const size_t f = 4;
     const size_t ldbt = static_cast<size_t>(x3_ld(BT));
     size_t n = 0;
-    n += 2 * a(static_cast<size_t>(BT) * OC * f);  // dout hi, lo
+    n += a(static_cast<size_t>(BT) * OC * f);      // dout lo (dout itself is the high part)
     n += 2 * a(static_cast<size_t>(OC) * ldbt * f);  // dout^T hi, lo
     n += 2 * a(static_cast<size_t>(C) * OC * f);     // weight^T hi, lo
     n += 2 * a(static_cast<size_t>(C) * ldbt * f);   // inp^T hi, lo
@@ -131,7 +151,6 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
         w += a(bytes);
         return p;
     };
-    float* dout_hi = take(static_cast<size_t>(BT) * OC * 4);
     float* dout_lo = take(static_cast<size_t>(BT) * OC * 4);
     float* doutT_hi = take(static_cast<size_t>(OC) * ldbt * 4);
     float* doutT_lo = take(static_cast<size_t>(OC) * ldbt * 4);
@@ -141,9 +160,9 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
     float* inpT_lo = take(static_cast<size_t>(C) * ldbt * 4);
     float* part = dbias ? take(static_cast<size_t>((BT + TILE - 1) / TILE) * OC * 4) : nullptr;
 
-    cudaError_t e = dbias ? launch_split<true, true, true>(dout, BT, OC, dout_hi, dout_lo, doutT_hi, doutT_lo, ldbt,
+    cudaError_t e = dbias ? launch_split<true, true, true>(dout, BT, OC, nullptr, dout_lo, doutT_hi, doutT_lo, ldbt,
                                                            part, stream)
-                          : launch_split<true, true, false>(dout, BT, OC, dout_hi, dout_lo, doutT_hi, doutT_lo, ldbt,
+                          : launch_split<true, true, false>(dout, BT, OC, nullptr, dout_lo, doutT_hi, doutT_lo, ldbt,
                                                             nullptr, stream);
     if (e != cudaSuccess) return e;
     e = launch_split<false, true, false>(weight, OC, C, nullptr, nullptr, wT_hi, wT_lo, OC, nullptr, stream);
@@ -151,14 +170,14 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
     e = launch_split<false, true, false>(inp, BT, C, nullptr, nullptr, inpT_hi, inpT_lo, ldbt, nullptr, stream);
     if (e != cudaSuccess) return e;
     if (dbias) {
-        tile_sum_kernel<<<static_cast<unsigned>((OC + 255) / 256), 256, 0, stream>>>(dbias, part,
-                                                                                       (BT + TILE - 1) / TILE, OC);
+        tile_sum_kernel<<<static_cast<unsigned>((OC + 31) / 32), 32 * TS_SLICES, 0, stream>>>(
+            dbias, part, (BT + TILE - 1) / TILE, OC);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // dinp (BT x C) += dout . (weight^T)^T, K = OC
     const TcPlan p1 = tc_make_plan_x3(BT, C, OC, num_sms);
-    e = tc_launch_x3(p1, dinp, dout_hi, dout_lo, OC, wT_hi, wT_lo, OC, BT, C, OC, stream);
+    e = tc_launch_x3(p1, dinp, dout, dout_lo, OC, wT_hi, wT_lo, OC, BT, C, OC, stream);
     if (e != cudaSuccess) return e;
     // dweight (OC x C) += (dout^T) . (inp^T)^T, K = BT
     const TcPlan p2 = tc_make_plan_x3(OC, C, BT, num_sms);
@@ -175,7 +194,7 @@ bool x3_forward_shape_ok(int64_t BT, int64_t C, int64_t OC) {
 
 size_t x3_forward_workspace_bytes(int64_t BT, int64_t C, int64_t OC) {
     auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    return 2 * a(static_cast<size_t>(BT) * C * 4) + 2 * a(static_cast<size_t>(OC) * C * 4);
+    return a(static_cast<size_t>(BT) * C * 4) + a(static_cast<size_t>(OC) * C * 4);  // the low parts
 }
 
 cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight, const float* bias, int64_t BT,
@@ -183,18 +202,17 @@ cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight,
     if (take_injected_launch_failure()) return cudaErrorLaunchFailure;
     auto a = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     uint8_t* w = static_cast<uint8_t*>(ws);
-    float* inp_hi = reinterpret_cast<float*>(w);
-    float* inp_lo = reinterpret_cast<float*>(w + a(static_cast<size_t>(BT) * C * 4));
-    float* w_hi = reinterpret_cast<float*>(w + 2 * a(static_cast<size_t>(BT) * C * 4));
-    float* w_lo = reinterpret_cast<float*>(w + 2 * a(static_cast<size_t>(BT) * C * 4) + a(static_cast<size_t>(OC) * C * 4));
+    // inp and weight are already K-major and serve as their own high parts
+    float* inp_lo = reinterpret_cast<float*>(w);
+    float* w_lo = reinterpret_cast<float*>(w + a(static_cast<size_t>(BT) * C * 4));
     cudaError_t e = fill_rows_launch(out, bias, BT, OC, MMBWD_F32, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<true, false, false>(inp, BT, C, inp_hi, inp_lo, nullptr, nullptr, 0, nullptr, stream);
+    e = launch_split<true, false, false>(inp, BT, C, nullptr, inp_lo, nullptr, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<true, false, false>(weight, OC, C, w_hi, w_lo, nullptr, nullptr, 0, nullptr, stream);
+    e = launch_split<true, false, false>(weight, OC, C, nullptr, w_lo, nullptr, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
     const TcPlan p = tc_make_plan_x3(BT, OC, C, num_sms);
-    return tc_launch_x3(p, out, inp_hi, inp_lo, C, w_hi, w_lo, C, BT, OC, C, stream);
+    return tc_launch_x3(p, out, inp, inp_lo, C, weight, w_lo, C, BT, OC, C, stream);
 }
 
 }  // namespace mmbwd
