@@ -21,7 +21,7 @@ constexpr int TC_BM = 128;       // rows per CTA
 constexpr int TC_PAIR_BM = 256;  // rows per CTA pair
 constexpr int TC_BN = 256;       // widest tile (N of one MMA); each CTA stages half of the columns
 constexpr int TC_BK = 64;
-constexpr int TC_STAGES = 5;     // bf16 pipeline stages (32 KB each)
+constexpr int TC_STAGES = 6;     // bf16 pipeline stages (32 KB each)
 constexpr int TC_STAGES_X3 = 3;  // fp32 three-product stages (64 KB each)
 constexpr int TC_THREADS = 256;
 

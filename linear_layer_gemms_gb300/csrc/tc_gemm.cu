@@ -32,12 +32,12 @@
 //               dout tile of every stage over its BT rows (the A operand already
 //               in shared memory) and reduce across lanes with shuffles.
 //   warps 4-7   epilogue (both CTAs): tcgen05.ld the accumulator (warp w reads
-//               tensor-memory lanes 32*(w%4)..+31, i.e. tile rows), transpose each
-//               32-column chunk through shared memory so that global accesses are
-//               row-contiguous, then either
+//               tensor-memory lanes 32*(w%4)..+31, i.e. tile rows) in 32 x 32
+//               chunks that travel between global and shared memory by TMA, then
+//               either
 //                 - read-modify-write the bf16 output: old + acc, one rounding
 //                   (dinp, and dweight when it is not split), old values
-//                   prefetched four chunks ahead, or
+//                   loaded up to four chunks ahead, or
 //                 - store the fp32 partial tile of this split (dweight split
 //                   along BT); a second kernel then sums the partials of every
 //                   tile in split order 0..S-1 and does the read-modify-write, so
@@ -90,19 +90,20 @@ constexpr int PART_CHUNK_BYTES = 32 * 32 * 4;
 
 // Shared memory map (offsets from a 1024-byte aligned base), per kernel mode:
 // the TMA stage ring, the barriers, then one region per epilogue warp. The
-// bf16 modes keep five 32 KB stages and give each epilogue warp eight chunk
-// buffers (16 KB), so that a whole 128 x 256 output tile of old values is
-// requested at the start of an item and lands while its main loop runs (four
-// buffers a warp, requested just ahead of use, left the epilogue waiting on
-// L2 latency: about 4 us for a 128 x 256 tile). MODE 2 keeps three 64 KB
-// stages and the fp32 staging rows.
+// bf16 modes keep six 32 KB stages and give each epilogue warp four chunk
+// buffers (8 KB): the first four chunks of old values are requested at the
+// start of an item, the rest just ahead of use. A sixth stage (a stage's round
+// trip is about 2 us, five covered it only just) is worth more than a whole
+// tile of old values in flight: with five stages and eight buffers a warp
+// every bf16 backward plan ran 1-4 % slower. MODE 2 keeps three 64 KB stages
+// and the fp32 staging rows.
 template <int MODE>
 struct Smem {
     static constexpr bool X3 = MODE == 2;
     static constexpr int STAGES = X3 ? TC_STAGES_X3 : TC_STAGES;
     static constexpr int STG_BYTES = X3 ? 2 * STAGE_BYTES : STAGE_BYTES;
-    static constexpr int OLD_SLOTS = X3 ? 4 : 8;  // bf16 chunk buffers per epilogue warp
-    static constexpr int PART_SLOTS = X3 ? 1 : 4;  // fp32 partial chunk buffers (same memory)
+    static constexpr int OLD_SLOTS = 4;  // bf16 chunk buffers per epilogue warp
+    static constexpr int PART_SLOTS = X3 ? 1 : 2;  // fp32 partial chunk buffers (same memory)
     static constexpr int OFF_BARS = STAGES * STG_BYTES;
     static constexpr int BAR_FULL = 0;                   // [stages] TMA landed (even CTA: and the peer's too)
     static constexpr int BAR_EMPTY = STAGES;             // [stages] stage may be refilled
