@@ -1,6 +1,7 @@
 """ncu harness: per-kernel counters of the benchmarked configurations.
 
-    python ncu_harness.py [CASE ...] [--raw-dir DIR] [--list]
+    python ncu_harness.py [CASE ...] [--raw-dir DIR] [--out-dir DIR] [--list]
+    python ncu_harness.py [CASE ...] --from-raw     # summaries from saved CSVs
 
 For each case (default: all of CASES) on one GPU:
 
@@ -19,7 +20,9 @@ For each case (default: all of CASES) on one GPU:
 and writes `profiles/<kernel>_<case>.md`: the commands, the hash of the
 kernel's source files, `dram_bytes_per_launch` (the mean DRAM traffic of the
 captured launches of the top kernel, which bench.py reports as the roofline
-traffic while the hash matches), and the tables. Raw CSV goes to --raw-dir.
+traffic while the hash matches), and the tables. Raw CSV goes to --raw-dir,
+with the capture times; `--from-raw` writes the summaries from those files
+alone (on a machine without the GPU, from the same sources).
 Every ncu command runs with --clock-control none.
 """
 from __future__ import annotations
@@ -28,6 +31,7 @@ import argparse
 import csv
 import hashlib
 import io
+import json
 import os
 import subprocess
 import sys
@@ -197,13 +201,6 @@ def profile(name: str, raw_dir: str, out_dir: str, max_launches: int) -> str | N
     if rc != 0:
         print(f"[{name}] launch list: ncu exited {rc}", flush=True)
         return None
-    launches = parse_csv(open(lfile).read())
-    per_kernel = {}
-    for _, k, m in launches:
-        s = per_kernel.setdefault(short_name(k), [0, 0.0])
-        s[0] += 1
-        s[1] += (m.get("gpu__time_duration.sum") or 0.0)
-    total = sum(v[1] for v in per_kernel.values()) or 1.0
     # 2. counters of the case's kernels
     mfile = os.path.join(raw_dir, f"{name}_metrics.csv")
     mcmd = ncu_cmd(["--metrics", ",".join(METRICS), "-k", f"regex:{spec['kernel']}", "-s", str(spec["skip"]),
@@ -212,9 +209,45 @@ def profile(name: str, raw_dir: str, out_dir: str, max_launches: int) -> str | N
     if rc != 0:
         print(f"[{name}] counters: ncu exited {rc}", flush=True)
         return None
+    with open(os.path.join(raw_dir, f"{name}_times.json"), "w") as f:
+        json.dump({"launch_list_s": dt_l, "counters_s": dt_m}, f)
+    return summarize(name, raw_dir, out_dir, lcmd, mcmd)
+
+
+def summarize(name: str, raw_dir: str, out_dir: str, lcmd=None, mcmd=None, max_launches: int = 400) -> str | None:
+    """Summary of case `name` from the CSV files in raw_dir (written by profile)."""
+    spec = CASES[name]
+    cmd = spec["cmd"]
+    lfile = os.path.join(raw_dir, f"{name}_launches.csv")
+    mfile = os.path.join(raw_dir, f"{name}_metrics.csv")
+    if not (os.path.exists(lfile) and os.path.exists(mfile)):
+        print(f"[{name}] no raw files in {raw_dir}", flush=True)
+        return None
+    if lcmd is None:
+        lcmd = ncu_cmd(["--metrics", "gpu__time_duration.sum", "-c", str(max_launches)], lfile, cmd)
+    if mcmd is None:
+        mcmd = ncu_cmd(["--metrics", ",".join(METRICS), "-k", f"regex:{spec['kernel']}", "-s", str(spec["skip"]),
+                        "-c", str(spec["count"])], mfile, cmd)
+    times = {}
+    tpath = os.path.join(raw_dir, f"{name}_times.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            times = json.load(f)
+    launches = parse_csv(open(lfile).read())
+    per_kernel = {}
+    for _, k, m in launches:
+        s = per_kernel.setdefault(short_name(k), [0, 0.0])
+        s[0] += 1
+        s[1] += (m.get("gpu__time_duration.sum") or 0.0)
+    total = sum(v[1] for v in per_kernel.values()) or 1.0
     caps = parse_csv(open(mfile).read())
     sha = source_sha(spec["sources"])
-    return write_summary(name, spec, sha, lcmd, mcmd, per_kernel, total, caps, dt_l, dt_m, out_dir)
+    return write_summary(name, spec, sha, lcmd, mcmd, per_kernel, total, caps, times.get("launch_list_s"),
+                         times.get("counters_s"), out_dir)
+
+
+def _took(dt) -> str:
+    return "(capture time not recorded)" if dt is None else f"({dt:.0f} s)"
 
 
 def _fmt(v, scale=1.0, nd=1, unit=""):
@@ -234,11 +267,11 @@ def write_summary(name, spec, sha, lcmd, mcmd, per_kernel, total, caps, dt_l, dt
     if dram:
         lines.append(f"- dram_bytes_per_launch: `{sum(dram) / len(dram):.0f}`")
     lines += ["", "## Launch list (`gpu__time_duration.sum` alone: one pass, cold-cache and serialised)", "",
-              f"    {rel(lcmd)}", "", f"({dt_l:.0f} s)", "",
+              f"    {rel(lcmd)}", "", _took(dt_l), "",
               "| kernel | launches | total | share | mean |", "|---|---|---|---|---|"]
     for k, (n, t) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
         lines.append(f"| `{k}` | {n} | {t / 1e3:.1f} us | {100 * t / total:.1f} % | {t / n / 1e3:.2f} us |")
-    lines += ["", "## Counters of the captured launches", "", f"    {rel(mcmd)}", "", f"({dt_m:.0f} s)", ""]
+    lines += ["", "## Counters of the captured launches", "", f"    {rel(mcmd)}", "", _took(dt_m), ""]
     head = ["metric"]
     for i, (_, k, _) in enumerate(caps):
         lab = spec["labels"][i] if spec.get("labels") and i < len(spec["labels"]) else short_name(k)
@@ -287,6 +320,8 @@ def main(argv=None):
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "profiles"))
     ap.add_argument("--max-launches", type=int, default=400)
     ap.add_argument("--list", action="store_true")
+    ap.add_argument("--from-raw", action="store_true",
+                    help="write the summaries from the CSV files already in --raw-dir (no GPU, no ncu)")
     a = ap.parse_args(argv)
     if a.list:
         for k, v in CASES.items():
@@ -299,7 +334,11 @@ def main(argv=None):
         raise SystemExit(f"unknown case(s) {bad}; one of {list(CASES)}")
     failed = 0
     for n in names:
-        if profile(n, a.raw_dir, a.out_dir, a.max_launches) is None:
+        if a.from_raw:
+            r = summarize(n, a.raw_dir, a.out_dir, max_launches=a.max_launches)
+        else:
+            r = profile(n, a.raw_dir, a.out_dir, a.max_launches)
+        if r is None:
             failed += 1
     return 1 if failed else 0
 
