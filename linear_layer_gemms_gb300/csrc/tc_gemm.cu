@@ -978,6 +978,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // thread per 8-column vector of dweight; all loads are independent, so the
 // pass runs at memory speed with the partials still in L2.
 __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) {
+    // The next launch on the stream (the tensor-core kernel, as a rule) may
+    // start its prologue beside this small pass; it still waits for this grid
+    // to complete before touching global memory.
+    ptx::grid_launch_dependents();
     ptx::grid_dependency_wait();  // the partials of the GEMM launch before this one
     const int64_t vec_per_row = p.C / 8;
     const int64_t nvec = p.OC * vec_per_row;

@@ -122,6 +122,34 @@ def test_split_reduction_and_schedule(monkeypatch, splits):
             assert np.array_equal(o[k], outs[0][k]), k
 
 
+def test_split_counts_across_launches(monkeypatch):
+    """Split launches of different shapes and split counts, with unsplit
+    launches between them, sharing the workspace's partial tiles: each gives
+    the same bits every time it runs from the same buffers, within tolerance
+    of the oracle."""
+    shapes = [((1, 1000, 264, 392), 3), ((2, 640, 520, 776), 2), ((1, 1000, 264, 392), 5), ((1, 512, 128, 128), 0)]
+    inputs = {s: make(*s[0], "bf16", dout_std=1e-2)[1] for s in shapes}
+    first = {}
+    for rep in range(3):
+        for shape, splits in shapes:
+            if splits:
+                monkeypatch.setenv("MMBWD_SPLITK", str(splits))
+            else:
+                monkeypatch.delenv("MMBWD_SPLITK", raising=False)
+            B, T, C, OC = shape
+            if rep == 0:
+                g, _ = check_full(inputs[(shape, splits)], B, T, C, OC, "bf16")
+            else:
+                g = run_gpu(inputs[(shape, splits)], B, T, C, OC, "bf16")
+            out = {k: to_host(g[k], "bf16") for k in ("dinp", "dweight", "dbias")}
+            if rep == 0:
+                first[(shape, splits)] = out
+            else:
+                for k in out:
+                    assert np.array_equal(out[k], first[(shape, splits)][k]), (shape, splits, k)
+    assert mm.mmbwd_device_status()[0] == mm.OK
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_bitwise_deterministic(dtype):
     B, T, C, OC = 4, 256, 768, 1024
