@@ -5,9 +5,10 @@
 // The page buckets the positions of each token on the host every step (a hash
 // map and a sort over host token ids, then two host-to-device copies). Here
 // the bucketing stays on the device, in two launches:
-//   1. enc_sort_wpe_kernel. Block 0 (1024 threads) sorts the keys
-//      (token << 15) | position stably by token in shared memory (LSD radix
-//      passes of 4 bits over the token bits), so each token's positions end
+//   1. enc_sort_wpe_kernel. A cluster of eight CTAs sorts the keys
+//      (token << 15) | position stably by token in their shared memory (LSD
+//      radix passes of 4 bits over the token bits, keys moved between the CTAs
+//      through the cluster's shared memory), so each token's positions end
 //      up contiguous and in increasing order, and writes the sorted keys and,
 //      per window of 32 sorted slots, where the run of the window's first slot
 //      begins and where the run of its last slot ends.
@@ -33,6 +34,7 @@
 #include "../../include/encoder_backward.h"
 #include "../../include/mmbwd.h"
 #include "ops.h"
+#include "ptx.cuh"
 #include "sr.cuh"
 
 namespace mmbwd {
@@ -44,6 +46,10 @@ __device__ unsigned int g_enc_status[4];
 namespace {
 
 constexpr int ENC_SORT_THREADS = 1024;
+// The sort of up to ENC_FAST_MAX positions: one cluster of ENC_CS_CTAS CTAs of
+// ENC_CS_THREADS threads.
+constexpr int ENC_CS_CTAS = 8;
+constexpr int ENC_CS_THREADS = 256;
 constexpr int ENC_WIN = 32;  // sorted slots per window (one per lane)
 constexpr unsigned ENC_PAD = 0xFFFFFFFFu;
 constexpr int ENC_DIGIT_BITS = 4;  // radix digit width per pass
@@ -52,6 +58,8 @@ constexpr int ENC_DIGITS = 1 << ENC_DIGIT_BITS;
 // of word k * 1024 + thread
 constexpr int ENC_CNT = ENC_DIGITS / 2 * ENC_SORT_THREADS;
 constexpr int ENC_CNT_WORDS = ENC_CNT + ENC_CNT / 32;  // with one pad word per 32
+constexpr int ENC_CS_CNT = ENC_DIGITS / 2 * ENC_CS_THREADS;  // the same for one CTA of the sorting cluster
+constexpr int ENC_CS_CNT_WORDS = ENC_CS_CNT + ENC_CS_CNT / 32;
 
 // Word w, padded so that a warp's 32 threads (one word row each) and a
 // thread's 8 consecutive words in the scan both fall in 32 distinct banks.
@@ -148,10 +156,11 @@ struct EncTables {
     unsigned long long seed;
 };
 
-// Exclusive scan of one value per thread over the block (1024 threads, in
-// thread order); returns the thread's prefix and writes the total.
+// Exclusive scan of one value per thread over the block (up to 1024 threads,
+// in thread order); returns the thread's prefix and writes the total.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     const int lane = static_cast<int>(threadIdx.x & 31), warp = static_cast<int>(threadIdx.x >> 5);
+    const int nw = static_cast<int>(blockDim.x >> 5);
     int x = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -161,7 +170,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = warp_sums[lane];
+        int w = lane < nw ? warp_sums[lane] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, w, off);
@@ -221,6 +230,7 @@ __device__ void enc_wpe_part(T* __restrict__ dwpe, const T* __restrict__ dout, i
 __device__ void block_exclusive_max_and_suffix_min(int mx, int mn, int* warp_sums, int* warp_sums2, int* max_before,
                                                    int* min_after) {
     const int lane = static_cast<int>(threadIdx.x & 31), warp = static_cast<int>(threadIdx.x >> 5);
+    const int nw = static_cast<int>(blockDim.x >> 5);
     int x = mx, y = mn;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -233,7 +243,7 @@ __device__ void block_exclusive_max_and_suffix_min(int mx, int mn, int* warp_sum
     if (lane == 0) warp_sums2[warp] = y;
     __syncthreads();
     if (warp == 0) {
-        int a = warp_sums[lane], b = warp_sums2[lane];
+        int a = lane < nw ? warp_sums[lane] : -1, b = lane < nw ? warp_sums2[lane] : INT_MAX;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, a, off);
@@ -248,49 +258,67 @@ __device__ void block_exclusive_max_and_suffix_min(int mx, int mn, int* warp_sum
     const int xe = __shfl_up_sync(0xffffffffu, x, 1), ye = __shfl_down_sync(0xffffffffu, y, 1);
     int before = lane > 0 ? xe : -1, after = lane < 31 ? ye : INT_MAX;
     if (warp > 0) before = max(before, warp_sums[warp - 1]);
-    if (warp < 31) after = min(after, warp_sums2[warp + 1]);
+    if (warp + 1 < nw) after = min(after, warp_sums2[warp + 1]);
     __syncthreads();
     *max_before = before;
     *min_after = after;
 }
 
-// Block 0: sort, segments, chunks, for NP = KPL * 1024 >= B*T key slots.
-// Thread t owns the KPL consecutive slots from t KPL. The keys start in
-// position order (padding, all ones, after the last position), so a stable
-// sort by token leaves each token's positions in increasing order and the
-// padding last. A pass over a 4-bit digit (no warp votes):
-//   - each thread counts its keys per digit in registers (its keys' ranks among
-//     its own keys of equal digit come with it) and stores the counts, two
-//     digits per word, at word (digit / 2, thread);
-//   - one block scan over the words, whose 16-bit halves add independently,
-//     and the prefix at the start of each word row turn them into each
-//     thread's first slot per digit in (digit, thread) order;
-//   - each key goes to first slot + rank, back into the same shared buffer.
-// Thread order is slot order, so the pass is stable.
-// Blocks 1.. form dwpe (enc_wpe_part).
+// The sort, by one cluster of ENC_CS_CTAS CTAs (blocks 0 .. ENC_CS_CTAS - 1 of
+// the launch), for NPC = KPL * ENC_CS_THREADS key slots per CTA (the cluster's
+// ENC_CS_CTAS * NPC >= B*T). CTA c holds slots c NPC .. c NPC + NPC - 1 in its
+// shared memory, thread t the KPL consecutive ones from c NPC + t KPL. The keys
+// start in position order (padding, all ones, after the last position), so a
+// stable sort by token leaves each token's positions in increasing order and
+// the padding last. A pass over a 4-bit digit:
+//   - each CTA ranks its keys among its own keys of equal digit: each thread
+//     counts its keys per digit in registers (its keys' ranks among its own
+//     keys of equal digit come with it) and stores the counts, two digits per
+//     word, at word (digit / 2, thread); one block scan over the words (whose
+//     16-bit halves add independently) gives each thread its first slot per
+//     digit in the CTA's (digit, thread) order, and the CTA's count per digit;
+//   - behind a cluster barrier every CTA reads the eight CTAs' counts (shared
+//     memory across the cluster) and finds where its keys of each digit start
+//     in the whole sorted order: after every key of a lower digit, and after
+//     the keys of the same digit held by lower CTAs;
+//   - each key is stored straight into the other buffer of the CTA that holds
+//     its new slot, and a second cluster barrier makes the stores visible.
+// Slot order is (CTA, thread, key) order throughout, so the pass is stable.
+// The window tables follow, their cross-CTA parts (the slot before a CTA's
+// first, the valid count, the run starts before and after a CTA) read
+// through the cluster's shared memory.
+// Blocks ENC_CS_CTAS.. form dwpe (enc_wpe_part).
 template <typename T, int KPL>
-__global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
+__global__ void __cluster_dims__(ENC_CS_CTAS, 1, 1) __launch_bounds__(ENC_CS_THREADS, 1)
     enc_sort_wpe_kernel(const int32_t* __restrict__ inp, int BT, int V, int passes, int G, EncTables tb,
                         T* __restrict__ dwpe, const T* __restrict__ dout, int B, int T_, int C) {
     enc_grid_wait();
     enc_launch_dependents();
     const int tid = static_cast<int>(threadIdx.x);
-    if (blockIdx.x > 0) {
-        enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(blockIdx.x - 1) * ENC_SORT_THREADS + tid,
-                        static_cast<int64_t>(gridDim.x - 1) * ENC_SORT_THREADS, tb.sr, tb.seed);
+    if (blockIdx.x >= ENC_CS_CTAS) {
+        enc_wpe_part<T>(dwpe, dout, B, T_, C, static_cast<int64_t>(blockIdx.x - ENC_CS_CTAS) * ENC_CS_THREADS + tid,
+                        static_cast<int64_t>(gridDim.x - ENC_CS_CTAS) * ENC_CS_THREADS, tb.sr, tb.seed);
         return;
     }
-    constexpr int NP = KPL * ENC_SORT_THREADS;
-    extern __shared__ __align__(16) unsigned enc_smem[];  // keys[NP], then counters[ENC_CNT_WORDS]
-    unsigned* keys = enc_smem;
-    int* cnt = reinterpret_cast<int*>(enc_smem + NP);
+    constexpr int NPC = KPL * ENC_CS_THREADS;
+    constexpr unsigned PADT = ENC_PAD >> 15;  // the padding's token field
+    const int c = static_cast<int>(ptx::cluster_ctarank());
+    // two key buffers of NPC (the passes alternate), then the packed counters
+    extern __shared__ __align__(16) unsigned enc_smem[];
+    auto kbuf = [&](int b) { return enc_smem + (b ? NPC : 0); };
+    int* cnt = reinterpret_cast<int*>(enc_smem + 2 * NPC);
     __shared__ int warp_sums[32], warp_sums2[32];
     __shared__ int row_start[ENC_DIGITS / 2 + 1];
-    const int i0 = tid * KPL;
+    __shared__ int dstart[ENC_DIGITS + 1];                // this CTA's first slot of each digit (its own order)
+    __shared__ int hist[ENC_DIGITS];                      // this CTA's keys of each digit (read by the cluster)
+    __shared__ int allh[ENC_CS_CTAS][ENC_DIGITS];
+    __shared__ int gbase[ENC_DIGITS];                     // where this CTA's keys of each digit start
+    __shared__ int xinfo[3];  // valid slots of this CTA, its last run start, its first run start (read by the cluster)
+    const int i0l = tid * KPL, g0 = c * NPC + i0l;  // this thread's first slot: local, global
     unsigned k[KPL];
 #pragma unroll
     for (int r = 0; r < KPL; ++r) {
-        const int i = i0 + r;
+        const int i = g0 + r;
         unsigned key = ENC_PAD;
         if (i < BT) {
             const int tok = inp[i];
@@ -303,19 +331,12 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
         }
         k[r] = key;
     }
+    int cur = 0;
     for (int pass = 0; pass < passes; ++pass) {
         const int sh = 15 + pass * ENC_DIGIT_BITS;
         if (pass > 0) {
-            if constexpr (KPL >= 4) {
 #pragma unroll
-                for (int q = 0; q < KPL / 4; ++q) {
-                    const uint4 v = reinterpret_cast<const uint4*>(keys + i0)[q];
-                    k[4 * q] = v.x, k[4 * q + 1] = v.y, k[4 * q + 2] = v.z, k[4 * q + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < KPL; ++r) k[r] = keys[i0 + r];
-            }
+            for (int r = 0; r < KPL; ++r) k[r] = kbuf(cur)[i0l + r];
         }
         // per-thread digit counts in 8-bit fields (digits 0-7 in c0, 8-15 in
         // c1); a key's rank is its digit's count before it
@@ -329,18 +350,14 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
             if (d & 8u) c1 += uint64_t(1) << f;
             else c0 += uint64_t(1) << f;
         }
-        // this thread's 8 packed words (every word written, so no clearing)
 #pragma unroll
         for (int kk = 0; kk < ENC_DIGITS / 2; ++kk) {
-            const uint64_t c = kk < 4 ? c0 : c1;
+            const uint64_t cw = kk < 4 ? c0 : c1;
             const int f = 16 * (kk & 3);
-            cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)] =
-                static_cast<int>(((c >> f) & 0xFFu) | (((c >> (f + 8)) & 0xFFu) << 16));
+            cnt[enc_cnt_at(kk * ENC_CS_THREADS + tid)] =
+                static_cast<int>(((cw >> f) & 0xFFu) | (((cw >> (f + 8)) & 0xFFu) << 16));
         }
         __syncthreads();
-        // exclusive scan of the packed words in (word row, thread) order: thread
-        // t scans words [8 t, 8 t + 8); the halves add without carries (each
-        // stays below 2^15); R(k) = the prefix at the start of word row k
         {
             int loc[ENC_DIGITS / 2];
             int sum = 0;
@@ -351,8 +368,8 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
             }
             int total = 0;
             int before = block_exclusive_scan(sum, warp_sums, &total);
-            if ((tid & (ENC_SORT_THREADS / (ENC_DIGITS / 2) - 1)) == 0)
-                row_start[tid / (ENC_SORT_THREADS / (ENC_DIGITS / 2))] = before;
+            if ((tid & (ENC_CS_THREADS / (ENC_DIGITS / 2) - 1)) == 0)
+                row_start[tid / (ENC_CS_THREADS / (ENC_DIGITS / 2))] = before;
             if (tid == 0) row_start[ENC_DIGITS / 2] = total;
 #pragma unroll
             for (int q = 0; q < ENC_DIGITS / 2; ++q) {
@@ -361,76 +378,121 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
             }
         }
         __syncthreads();
-        // digit-major first slot: digit 2k at thread t: low half of P(k, t) plus
-        // the high half of R(k) (all odd digits below); digit 2k + 1: high half
-        // of P(k, t) plus the low half of R(k + 1) (all even digits up to 2k)
+        // this CTA's first slot of digit d: every key of a lower digit (the two
+        // halves of the word-row prefixes hold the even and the odd digits)
+        if (tid <= ENC_DIGITS) {
+            const int d = tid;
+            int st = NPC;
+            if (d < ENC_DIGITS) {
+                const unsigned rs = static_cast<unsigned>(row_start[d >> 1]), rs1 = static_cast<unsigned>(row_start[(d >> 1) + 1]);
+                st = static_cast<int>((d & 1) ? (rs >> 16) + (rs1 & 0xFFFFu) : (rs & 0xFFFFu) + (rs >> 16));
+            }
+            dstart[d] = st;
+        }
+        __syncthreads();
+        if (tid < ENC_DIGITS) hist[tid] = dstart[tid + 1] - dstart[tid];
+        ptx::cluster_sync();  // every CTA's counts are visible
+        if (tid < ENC_CS_CTAS * ENC_DIGITS) {
+            const int cc = tid / ENC_DIGITS, d = tid % ENC_DIGITS;
+            allh[cc][d] = static_cast<int>(ptx::ld_dsmem_u32(ptx::mapa(ptx::smem_u32(&hist[d]), static_cast<uint32_t>(cc))));
+        }
+        __syncthreads();
+        if (tid < ENC_DIGITS) {
+            const int d = tid;
+            int b = 0;
+            for (int dd = 0; dd < d; ++dd)
+                for (int cc = 0; cc < ENC_CS_CTAS; ++cc) b += allh[cc][dd];
+            for (int cc = 0; cc < c; ++cc) b += allh[cc][d];
+            gbase[d] = b;
+        }
+        __syncthreads();
+        const uint32_t nb = ptx::smem_u32(kbuf(cur ^ 1));
 #pragma unroll
         for (int r = 0; r < KPL; ++r) {
             const unsigned d = (k[r] >> sh) & (ENC_DIGITS - 1);
             const int kk = static_cast<int>(d >> 1);
-            const unsigned pw = static_cast<unsigned>(cnt[enc_cnt_at(kk * ENC_SORT_THREADS + tid)]);
-            const unsigned first = (d & 1u) ? (pw >> 16) + (static_cast<unsigned>(row_start[kk + 1]) & 0xFFFFu)
-                                            : (pw & 0xFFFFu) + (static_cast<unsigned>(row_start[kk]) >> 16);
-            keys[first + rank[r]] = k[r];
+            const unsigned pw = static_cast<unsigned>(cnt[enc_cnt_at(kk * ENC_CS_THREADS + tid)]);
+            const unsigned rs = static_cast<unsigned>(row_start[kk]), rs1 = static_cast<unsigned>(row_start[kk + 1]);
+            const unsigned first = (d & 1u) ? (pw >> 16) + (rs1 & 0xFFFFu) : (pw & 0xFFFFu) + (rs >> 16);
+            const int g = gbase[d] + static_cast<int>(first) + rank[r] - dstart[d];  // the key's new slot
+            ptx::st_dsmem_u32(ptx::mapa(nb + 4u * static_cast<uint32_t>(g % NPC), static_cast<uint32_t>(g / NPC)), k[r]);
         }
-        __syncthreads();
+        ptx::cluster_sync();  // the stored keys are visible; this CTA's buffers are free again
+        cur ^= 1;
     }
-    if (passes == 0) {  // V == 0: every key is padding
+    unsigned* keys = kbuf(cur);
+    if (passes == 0) {  // V == 0: every key is padding and stays where it is
 #pragma unroll
-        for (int r = 0; r < KPL; ++r) keys[i0 + r] = k[r];
-        __syncthreads();
+        for (int r = 0; r < KPL; ++r) keys[i0l + r] = k[r];
+        ptx::cluster_sync();  // (the CTA after reads this CTA's last slot)
     }
 
-    // Each thread takes its KPL consecutive sorted slots, read once into
-    // registers with the tokens of the slots before and after.
-    unsigned tk[KPL];  // token of each slot (the padding reads as all ones)
-    if constexpr (KPL >= 4) {
+    // Each thread takes its KPL consecutive sorted slots with the token of the
+    // slot before (in the CTA before for a CTA's first slot).
+    unsigned tk[KPL];
 #pragma unroll
-        for (int q = 0; q < KPL / 4; ++q) {
-            const uint4 v = reinterpret_cast<const uint4*>(keys + i0)[q];
-            tk[4 * q] = v.x >> 15, tk[4 * q + 1] = v.y >> 15, tk[4 * q + 2] = v.z >> 15, tk[4 * q + 3] = v.w >> 15;
-        }
-    } else {
-#pragma unroll
-        for (int r = 0; r < KPL; ++r) tk[r] = keys[i0 + r] >> 15;
-    }
-    const unsigned tk_prev = i0 > 0 ? keys[i0 - 1] >> 15 : ENC_PAD;
+    for (int r = 0; r < KPL; ++r) tk[r] = keys[i0l + r] >> 15;
+    unsigned tk_prev = PADT;
+    if (tid > 0)
+        tk_prev = keys[i0l - 1] >> 15;
+    else if (c > 0)
+        tk_prev = ptx::ld_dsmem_u32(ptx::mapa(ptx::smem_u32(&keys[NPC - 1]), static_cast<uint32_t>(c - 1))) >> 15;
     int nvalid_local = 0;
 #pragma unroll
-    for (int r = 0; r < KPL; ++r) nvalid_local += tk[r] != (ENC_PAD >> 15);
-    int nvalid = 0;
-    block_exclusive_scan(nvalid_local, warp_sums, &nvalid);
-    for (int i = tid; i < nvalid; i += ENC_SORT_THREADS)  // coalesced; (token, position) widened to 32 + 32 bits
-        tb.skeys[i] = (static_cast<unsigned long long>(keys[i] >> 15) << 32) | (keys[i] & 0x7FFFu);
-    // run starts; the run holding a window's first slot starts at the largest
-    // start at or before it, the run holding its last slot ends before the
-    // smallest start after it
+    for (int r = 0; r < KPL; ++r) nvalid_local += tk[r] != PADT;
+    // run starts (a valid slot whose token differs from the slot before's)
     int first_start = INT_MAX, last_start = -1;
     bool start0 = false;
 #pragma unroll
     for (int r = KPL - 1; r >= 0; --r) {
-        const int i = i0 + r;
-        const bool st = i < nvalid && (i == 0 || tk[r] != (r > 0 ? tk[r - 1] : tk_prev));
+        const int i = g0 + r;
+        const bool st = tk[r] != PADT && (i == 0 || tk[r] != (r > 0 ? tk[r - 1] : tk_prev));
         if (st) {
             first_start = i;
             if (last_start < 0) last_start = i;
         }
         if (r == 0) start0 = st;
     }
+    if (tid == 0) {
+        xinfo[1] = -1;
+        xinfo[2] = INT_MAX;
+    }
+    int cta_valid = 0;
+    block_exclusive_scan(nvalid_local, warp_sums, &cta_valid);  // (its barriers order the stores above)
+    if (last_start >= 0) atomicMax(&xinfo[1], last_start);
+    if (first_start < INT_MAX) atomicMin(&xinfo[2], first_start);
+    if (tid == 0) xinfo[0] = cta_valid;
     int open_start = -1, next_start = INT_MAX;
     block_exclusive_max_and_suffix_min(last_start, first_start, warp_sums, warp_sums2, &open_start, &next_start);
-    if ((i0 & (ENC_WIN - 1)) == 0 && i0 < nvalid) tb.win_head[i0 / ENC_WIN] = start0 ? i0 : open_start;
-    const int ilast = i0 + KPL - 1;
-    if (((ilast + 1) & (ENC_WIN - 1)) == 0 && ilast < nvalid)
-        tb.win_tail[ilast / ENC_WIN] = min(next_start, nvalid) - 1;
+    ptx::cluster_sync();  // every CTA's valid count and run starts are visible
+    int nvalid = 0;
+    for (int cc = 0; cc < ENC_CS_CTAS; ++cc) {
+        const uint32_t a = ptx::smem_u32(xinfo);
+        nvalid += static_cast<int>(ptx::ld_dsmem_u32(ptx::mapa(a, static_cast<uint32_t>(cc))));
+        if (cc < c)
+            open_start = max(open_start, static_cast<int>(ptx::ld_dsmem_u32(ptx::mapa(a + 4u, static_cast<uint32_t>(cc)))));
+        if (cc > c)
+            next_start = min(next_start, static_cast<int>(ptx::ld_dsmem_u32(ptx::mapa(a + 8u, static_cast<uint32_t>(cc)))));
+    }
+    for (int i = tid; i < NPC; i += ENC_CS_THREADS) {  // coalesced; (token, position) widened to 32 + 32 bits
+        const int gi = c * NPC + i;
+        if (gi < nvalid) tb.skeys[gi] = (static_cast<unsigned long long>(keys[i] >> 15) << 32) | (keys[i] & 0x7FFFu);
+    }
+    // the run holding a window's first slot starts at the largest start at or
+    // before it, the run holding its last slot ends before the smallest start
+    // after it
+    if ((g0 & (ENC_WIN - 1)) == 0 && g0 < nvalid) tb.win_head[g0 / ENC_WIN] = start0 ? g0 : open_start;
+    const int ilast = g0 + KPL - 1;
+    if (((ilast + 1) & (ENC_WIN - 1)) == 0 && ilast < nvalid) tb.win_tail[ilast / ENC_WIN] = min(next_start, nvalid) - 1;
     const int nwin_g = (nvalid + ENC_WIN - 1) / ENC_WIN * G;
-    for (int e = tid; e < nwin_g; e += ENC_SORT_THREADS) tb.arrivals[e] = 0u;
-    if (tid == 0) {
+    for (int e = c * ENC_CS_THREADS + tid; e < nwin_g; e += ENC_CS_CTAS * ENC_CS_THREADS) tb.arrivals[e] = 0u;
+    if (c == 0 && tid == 0) {
         tb.meta[0] = nvalid;
         tb.meta[1] = BT;  // the problem these tables describe
         tb.meta[2] = V;
         tb.meta[3] = C;
     }
+    ptx::cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // Finishes one run that crosses a window edge (see the file comment), the
@@ -826,8 +888,7 @@ const void* enc_sort_fn(int kpl) {
         case 1: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 1>);
         case 2: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 2>);
         case 4: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 4>);
-        case 8: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 8>);
-        default: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 16>);
+        default: return reinterpret_cast<const void*>(&enc_sort_wpe_kernel<T, 8>);
     }
 }
 
@@ -922,15 +983,15 @@ cudaError_t enc_mb_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C,
 cudaError_t enc_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C, int64_t B, int64_t T, int dtype,
                             const EncTables& tb, void* dwpe, const void* dout, int wpe_blocks, cudaStream_t stream) {
     if (BT > ENC_FAST_MAX) return enc_mb_sort_launch(inp, BT, V, C, tb, stream);
-    int kpl = 1;
-    while (kpl * ENC_SORT_THREADS < BT) kpl <<= 1;
+    int kpl = 1;  // keys per thread of the sorting cluster (at most 8: ENC_FAST_MAX positions)
+    while (kpl * ENC_CS_THREADS * ENC_CS_CTAS < BT) kpl <<= 1;
     // sort on the smallest b with 2^b > V: the padding's digits (all ones) then
     // exceed those of every valid token, so the padding sorts last even where
     // invalid ids sit between valid ones
     int token_bits = 0;
     while ((int64_t(1) << token_bits) <= V) ++token_bits;
     int passes = (token_bits + ENC_DIGIT_BITS - 1) / ENC_DIGIT_BITS;
-    const size_t sort_smem = (static_cast<size_t>(kpl) * ENC_SORT_THREADS + ENC_CNT_WORDS) * 4;
+    const size_t sort_smem = (2 * static_cast<size_t>(kpl) * ENC_CS_THREADS + ENC_CS_CNT_WORDS) * 4;
     const void* ks = dtype == MMBWD_F32 ? enc_sort_fn<float>(kpl) : enc_sort_fn<__nv_bfloat16>(kpl);
     cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sort_smem));
     if (e != cudaSuccess) return e;
@@ -939,7 +1000,9 @@ cudaError_t enc_sort_launch(const int32_t* inp, int BT, int64_t V, int64_t C, in
     EncTables t = tb;
     void* args[] = {const_cast<int32_t**>(&inp), &BTi, &Vi, &passes, &G, &t,
                     &dwpe, const_cast<void**>(&dout), &Bi, &Ti, &Ci};
-    return launch_pdl(ks, dim3(static_cast<unsigned>(1 + wpe_blocks)), dim3(ENC_SORT_THREADS), sort_smem, stream, args);
+    // the sorting cluster, then whole clusters of dwpe blocks
+    const int grid = ENC_CS_CTAS + (wpe_blocks + ENC_CS_CTAS - 1) / ENC_CS_CTAS * ENC_CS_CTAS;
+    return launch_pdl(ks, dim3(static_cast<unsigned>(grid)), dim3(ENC_CS_THREADS), sort_smem, stream, args);
 }
 
 // The window sums (and, with wpe_blocks > 0, dwpe) over tables `tb`.
@@ -985,9 +1048,9 @@ cudaError_t enc_launch(void* dwte, void* dwpe, const void* dout, const int32_t* 
         const int wb = static_cast<int>(std::min<int64_t>((T * C / N + width - 1) / width, 2 * std::max(num_sms, 1)));
         return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, wb, stream);
     }
-    // block 0 sorts; one wave of blocks (at most one per SM besides it) forms dwpe
-    const int64_t wpe_threads = (T * C / N + ENC_SORT_THREADS - 1) / ENC_SORT_THREADS;
-    const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, std::max(num_sms - 1, 1)));
+    // the sorting cluster, and blocks of one 16-byte dwpe vector per thread
+    const int64_t wpe_threads = (T * C / N + ENC_CS_THREADS - 1) / ENC_CS_THREADS;
+    const int wpe_blocks = static_cast<int>(std::min<int64_t>(wpe_threads, 4 * std::max(num_sms, 1)));
     cudaError_t e = enc_sort_launch(inp, BT, V, C, B, T, dtype, tb, dwpe, dout, wpe_blocks, stream);
     if (e != cudaSuccess) return e;
     return enc_window_launch(dwte, dwpe, dout, B, T, C, V, dtype, tb, 0, stream);

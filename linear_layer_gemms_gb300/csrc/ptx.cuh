@@ -252,6 +252,17 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// 32-bit load and store of shared memory anywhere in the cluster (address
+// from mapa); ordered for other CTAs by a cluster barrier.
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Arrive on an mbarrier in any CTA of the cluster (address from mapa), without
 // release semantics. Used only where the arrival orders work of the async
 // proxy (a TMA copy that has completed, tensor-memory reads that have been
