@@ -323,10 +323,20 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
                               TC_PAIR_BM, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), 1};
         for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else if (use_x3(s.BT, C, OC)) {
-        const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
-        const int vals[15] = {2, std::max(p1.grid, p2.grid), p1.n_items + p2.n_items, 1, 0, p1.n_items, p2.n_items,
-                              0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES_X3, 6, 1};
-        for (int i = 0; i < 15; ++i) v[i] = vals[i];
+        // the pre-pass (three split launches and the dbias tile sum), then both
+        // products in one launch, or one launch each where they cannot share one
+        static thread_local TcPlan pp;
+        pp = tc_make_plan_x3_pair(s.BT, C, OC, num_sms);
+        if (pp.n_items > 0) {
+            const int vals[15] = {2, pp.grid, pp.n_items, 1, 0, pp.n_dinp_items, pp.n_dw_items, pp.table,
+                                  TC_PAIR_BM, pp.dinp_bn, pp.dw_bn, TC_BK / 2, TC_STAGES_X3, 5, 1};
+            for (int i = 0; i < 15; ++i) v[i] = vals[i];
+        } else {
+            const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
+            const int vals[15] = {2, std::max(p1.grid, p2.grid), p1.n_items + p2.n_items, 1, 0, p1.n_items,
+                                  p2.n_items, 0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES_X3, 6, 1};
+            for (int i = 0; i < 15; ++i) v[i] = vals[i];
+        }
     } else {
         const int gm = static_cast<int>((s.BT + SIMT_BM - 1) / SIMT_BM), gn = static_cast<int>((C + SIMT_BN - 1) / SIMT_BN);
         const int go = static_cast<int>((OC + SIMT_BM - 1) / SIMT_BM);

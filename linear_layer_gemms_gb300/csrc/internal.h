@@ -70,6 +70,8 @@ struct TcPlan {
     int n_dinp_items;  // dinp_tiles_m * dinp_tiles_n
     int n_items;
     int table;         // 1: per-pair item lists in `sched`; 0: round-robin
+    int x3;            // fp32 (three tf32 products): both products K-major, tf32 item costs
+    int x3_corr;       // fp32: the correction products in their own accumulator
     int grid;          // CTAs (twice the number of CTA pairs)
     double est_us;     // the planner's time estimate
     int fixup_grid;    // CTAs of the split-reduction pass (0 when splits == 1)
@@ -133,6 +135,18 @@ TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
                          const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
                          cudaStream_t stream);
+// Both fp32 products of the backward in one launch, their items (tiles of
+// either product) assigned to CTA pairs longest first:
+//   dinp (BT x C) += A1 (BT x OC) . B1 (C x OC)^T     (A1 = dout, B1 = weight^T)
+//   dweight (OC x C) += A2 (OC x BT) . B2 (C x BT)^T  (A2 = dout^T, B2 = inp^T)
+// every operand as a tf32 high and low part, K-major (leading dimensions in
+// elements, multiples of 4). The plan has n_items == 0 where one launch does
+// not fit (then the products go to tc_launch_x3 one at a time).
+TcPlan tc_make_plan_x3_pair(int64_t BT, int64_t C, int64_t OC, int num_sms);
+cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, const float* a1_hi, const float* a1_lo,
+                              int64_t lda1, const float* b1_hi, const float* b1_lo, int64_t ldb1, const float* a2_hi,
+                              const float* a2_lo, int64_t lda2, const float* b2_hi, const float* b2_lo, int64_t ldb2,
+                              int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight,
                               const void* bias, int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
 

@@ -175,6 +175,15 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    // Both products in one launch where it fits (their tiles share the CTA
+    // pairs, longest first, instead of each launch ending on a partial wave):
+    // dinp (BT x C) += dout . (weight^T)^T, K = OC, and
+    // dweight (OC x C) += (dout^T) . (inp^T)^T, K = BT
+    static thread_local TcPlan pp;
+    pp = tc_make_plan_x3_pair(BT, C, OC, num_sms);
+    if (pp.n_items > 0)
+        return tc_launch_x3_pair(pp, dinp, dweight, dout, dout_lo, OC, wT_hi, wT_lo, OC, doutT_hi, doutT_lo, ldbt,
+                                 inpT_hi, inpT_lo, ldbt, BT, C, OC, stream);
     // dinp (BT x C) += dout . (weight^T)^T, K = OC
     const TcPlan p1 = tc_make_plan_x3(BT, C, OC, num_sms);
     e = tc_launch_x3(p1, dinp, dout, dout_lo, OC, wT_hi, wT_lo, OC, BT, C, OC, stream);

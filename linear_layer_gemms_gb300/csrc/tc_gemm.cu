@@ -374,6 +374,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (p.wide_maps & TC_WIDE_WEIGHT) ptx::prefetch_tmap(&tm_weight_w);
             if (p.wide_maps & TC_WIDE_DOUT_MN) ptx::prefetch_tmap(&tm_dout_mn_w);
             if (p.wide_maps & TC_WIDE_INP) ptx::prefetch_tmap(&tm_inp_w);
+            if (X3 && p.n_dw_items > 0) {  // the dweight product's maps of a paired fp32 launch
+                ptx::prefetch_tmap(&tm_weight_w);
+                ptx::prefetch_tmap(&tm_dout_mn_w);
+                ptx::prefetch_tmap(&tm_inp_w);
+                ptx::prefetch_tmap(&tm_dinp_rmw);
+            }
             ptx::prefetch_tmap(&tm_dinp_out);
             ptx::prefetch_tmap(&tm_dw_out);
             uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
@@ -396,11 +402,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const bool direct = X3 || (!(it.is_dw && p.splits > 1) && !FWD);  // forward: nothing to read back
                 const int64_t out_rows = it.is_dw ? p.OC : p.BT;
                 const int pf_kb = max(it.kb0, it.kb1 - 8);
+                // A of a bf16 dweight item: MN-major 64-row boxes; every other A
+                // (fp32 items of either product too): one K-major 128-row tile
                 int na;
-                if (it.is_dw) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
-                else na = row0 < p.BT ? 1 : 0;
+                if (it.is_dw && !X3) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
+                else na = row0 < out_rows ? 1 : 0;
                 const uint32_t bytes = static_cast<uint32_t>(
-                    ((it.is_dw ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES) * (X3 ? 2 : 1));
+                    ((it.is_dw && !X3 ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES) * (X3 ? 2 : 1));
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wt.wait(bars + 8u * (BAR_EMPTY + stage), phase ^ 1u, SITE_PRODUCER_EMPTY, w)) {
                         ok = false;
@@ -421,14 +429,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                         it.n_tile * it.bn + j * 128, row0);
                     }
                     if (X3) {
-                        // A hi, A lo (maps 0 and 2), then B hi, B lo (maps 1 and 3)
+                        // A hi, A lo (maps 0 and 2), then B hi, B lo (maps 1 and 3);
+                        // the dweight product of a paired launch: maps 6, 8, 7, 9
+                        const void* ah = it.is_dw ? static_cast<const void*>(&tm_weight_w) : &tm_dout_k;
+                        const void* al = it.is_dw ? static_cast<const void*>(&tm_inp_w) : &tm_dout_mn;
+                        const void* bh = it.is_dw ? static_cast<const void*>(&tm_dout_mn_w) : &tm_weight;
+                        const void* bl = it.is_dw ? static_cast<const void*>(&tm_dinp_rmw) : &tm_inp;
                         if (na) {
-                            ptx::tma_load_2d(sA, &tm_dout_k, fb, kb * KBLK, row0);
-                            ptx::tma_load_2d(sA + A_BYTES, &tm_dout_mn, fb, kb * KBLK, row0);
+                            ptx::tma_load_2d(sA, ah, fb, kb * KBLK, row0);
+                            ptx::tma_load_2d(sA + A_BYTES, al, fb, kb * KBLK, row0);
                         }
                         for (int j = 0; j < nb; ++j) {
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, &tm_weight, fb, kb * KBLK, col0 + j * 64);
-                            ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, &tm_inp, fb, kb * KBLK, col0 + j * 64);
+                            ptx::tma_load_2d(sB + j * BOX_BYTES, bh, fb, kb * KBLK, col0 + j * 64);
+                            ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, bl, fb, kb * KBLK, col0 + j * 64);
                         }
                     } else if (it.is_dw) {
                         if (na == 2 && (p.wide_maps & TC_WIDE_DOUT_MN))
@@ -1067,7 +1080,20 @@ struct ItemCost {
     double run, epi;
 };
 
+// fp32 from three tf32 products, both products in one launch: a k-block of
+// 32 fp32 of K with three pair MMAs takes about 0.86 us at width 256 and 0.55
+// at 128, and with a correction accumulator a 256-wide tile fills all 512
+// tensor-memory columns, so its fp32 epilogue (about 12 us) is not
+// overlapped. Fitted, through this planner's own longest-first schedule, to
+// the paired launches of the GPT-2 XL fc and qkv layers at both widths
+// (612, 650, 508, 457 us measured; 612, 642, 507, 459 modelled).
+double x3_item_us(int kb, int bn, bool corr) { return kb * (bn == 256 ? 0.86 : 0.55) + (bn == 256 && corr ? 12.0 : 0.0); }
+
 ItemCost item_cost(const TcPlan& pl, int w) {
+    if (pl.x3) {
+        const bool dw = w < pl.n_dw_items;
+        return {x3_item_us(dw ? pl.dw_kb : pl.dinp_kb, dw ? pl.dw_bn : pl.dinp_bn, pl.x3_corr != 0), 0.0};
+    }
     if (w < pl.n_dw_items) {
         const int split = w / pl.dw_tiles_n / pl.dw_tiles_m;
         const int kb0 = split * pl.kb_per_split;
@@ -1301,6 +1327,8 @@ TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int pairs = std::max(1, std::min(pl.n_items, max_pairs));
     pl.grid = 2 * pairs;
     pl.table = 0;  // round robin
+    pl.x3 = 1;
+    pl.x3_corr = K > TC_X3_CORR_K ? 1 : 0;
     pl.est_us = best;
     pl.fixup_grid = 0;
     return pl;
@@ -1318,7 +1346,8 @@ struct MapSpec {
 
 // Encodes the six tensor maps, completes the parameters from the plan, and
 // launches the kernel (and the split fixup when the plan splits dweight).
-cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParams& p, int mode, cudaStream_t stream) {
+cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParams& p, int mode, cudaStream_t stream,
+                          const MapSpec* pair_specs = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1401,6 +1430,21 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     }
     // fp32 partial tiles of a split reduction: [half tile][split][128][dw_bn]
     // as rows of dw_bn floats, stored in 32 x 32 boxes (128-byte swizzle).
+    // fp32 launches with the dweight product too: its A hi, B hi, A lo, B lo
+    // in maps 6 to 9 (the slots the bf16 modes use for other maps)
+    if (mode == 2 && pair_specs) {
+        for (int i = 0; i < 4; ++i) {
+            const MapSpec& m = pair_specs[i];
+            const cuuint64_t dims[2] = {m.inner, m.outer};
+            const cuuint64_t strides[1] = {m.pitch ? m.pitch : m.inner * 4};
+            const cuuint32_t box[2] = {m.box_inner, m.box_outer};
+            const cuuint32_t estr[2] = {1, 1};
+            const CUresult r = encode(&maps[6 + i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(m.base), dims,
+                                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, m.swz,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        }
+    }
     maps[11] = maps[0];  // placeholder where unused
     if ((mode == 0 || mode == 3) && plan.splits > 1 && p.partials) {
         const uint64_t rows = static_cast<uint64_t>(2 * plan.dw_tiles_m) * plan.dw_tiles_n * plan.splits * TC_BM;
@@ -1524,6 +1568,42 @@ cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, co
     return launch_common(plan, specs, p, 1, stream);
 }
 
+TcPlan tc_make_plan_x3_pair(int64_t BT, int64_t C, int64_t OC, int num_sms) {
+    TcPlan best_pl{};
+    // one correction setting for the launch: only where both reductions agree
+    if ((OC > TC_X3_CORR_K) != (BT > TC_X3_CORR_K)) return best_pl;
+    const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
+    const long force = env_long("MMBWD_TILE_N_X3", 0);
+    double best = 1e300;
+    for (int bn = 256; bn >= 128; bn -= 128) {
+        if (force && bn != force) continue;
+        TcPlan c{};
+        c.x3 = 1;
+        c.x3_corr = OC > TC_X3_CORR_K ? 1 : 0;
+        c.dinp_kb = ceil_div_i(OC, TC_BK / 2);
+        c.dw_kb = ceil_div_i(BT, TC_BK / 2);
+        c.dinp_bn = c.dw_bn = bn;
+        c.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
+        c.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
+        c.dinp_tiles_n = c.dw_tiles_n = ceil_div_i(C, bn);
+        c.n_dinp_items = c.dinp_tiles_m * c.dinp_tiles_n;
+        c.n_dw_items = c.dw_tiles_m * c.dw_tiles_n;
+        c.n_items = c.n_dinp_items + c.n_dw_items;
+        c.splits = 1;
+        c.kb_per_split = c.dw_kb;
+        if (c.n_items > TC_MAX_SCHED_ITEMS) continue;
+        const int pairs = std::max(1, std::min(c.n_items, max_pairs));
+        c.grid = 2 * pairs;
+        c.table = 1;
+        c.est_us = assign_lpt(c, pairs);
+        if (c.est_us < best - 1e-9) {
+            best = c.est_us;
+            best_pl = c;
+        }
+    }
+    return best_pl;
+}
+
 cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
                          const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
                          cudaStream_t stream) {
@@ -1545,6 +1625,40 @@ cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const 
     p.x3_corr = K > TC_X3_CORR_K ? 1 : 0;
     p.dinp = reinterpret_cast<__nv_bfloat16*>(D);
     return launch_common(plan, specs, p, 2, stream);
+}
+
+cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, const float* a1_hi, const float* a1_lo,
+                              int64_t lda1, const float* b1_hi, const float* b1_lo, int64_t ldb1, const float* a2_hi,
+                              const float* a2_lo, int64_t lda2, const float* b2_hi, const float* b2_lo, int64_t ldb2,
+                              int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+    const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
+    const uint64_t pa1 = static_cast<uint64_t>(lda1) * 4, pb1 = static_cast<uint64_t>(ldb1) * 4;
+    const uint64_t pa2 = static_cast<uint64_t>(lda2) * 4, pb2 = static_cast<uint64_t>(ldb2) * 4;
+    // dinp product (K = OC): maps 0 to 3; the outputs (L2 prefetch of old values): maps 4 and 5
+    const MapSpec specs[6] = {
+        {a1_hi, oc, bt, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa1},
+        {b1_hi, oc, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb1},
+        {a1_lo, oc, bt, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa1},
+        {b1_lo, oc, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb1},
+        {dinp, c, bt, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},
+        {dweight, c, oc, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},
+    };
+    // dweight product (K = BT): A hi, B hi, A lo, B lo
+    const MapSpec pair[4] = {
+        {a2_hi, bt, oc, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa2},
+        {b2_hi, bt, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb2},
+        {a2_lo, bt, oc, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa2},
+        {b2_lo, bt, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb2},
+    };
+    TcParams p{};
+    p.BT = BT;
+    p.C = C;
+    p.OC = OC;
+    p.n_dinp = C;
+    p.x3_corr = plan.x3_corr;
+    p.dinp = reinterpret_cast<__nv_bfloat16*>(dinp);
+    p.dweight = reinterpret_cast<__nv_bfloat16*>(dweight);
+    return launch_common(plan, specs, p, 2, stream, pair);
 }
 
 cudaError_t tc_read_status(int* code, int* info3, bool reset) {
