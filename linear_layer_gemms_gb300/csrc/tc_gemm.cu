@@ -770,6 +770,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
 
+            // MODE 2: this thread's old values of the first chunk (4 rows x 8
+            // columns), requested before the accumulator is ready; each later
+            // chunk's are requested while the chunk before is added and stored
+            float4 olda[4], oldb[4];
+            auto x3_load_old = [&](int cc, float4 (&A)[4], float4 (&Bv)[4]) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    A[i] = Bv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (rok[i] && cc * 32 + cg < ncols) {
+                        const float4* dp = reinterpret_cast<const float4*>(drowf[i] + cc * 32);
+                        A[i] = dp[0];
+                        Bv[i] = dp[1];
+                    }
+                }
+            };
+            if constexpr (X3) x3_load_old(0, olda, oldb);
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
             ptx::tc_fence_after();
@@ -915,41 +931,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
             if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
+            if constexpr (X3) {  // MODE 2: fp32 read-modify-write through staging rows
+#pragma unroll 1
+                for (int c = 0; c < nchunks; ++c) {
+                    float4 nxa[4], nxb[4];
+                    if (c + 1 < nchunks) x3_load_old(c + 1, nxa, nxb);
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tbase + c * 32, v);
+                    if (corr) {  // main + correction, one IEEE fp32 addition
+                        uint32_t w2[32];
+                        ptx::tmem_ld32(tbase + it.bn + c * 32, w2);
 #pragma unroll
-            for (int c = 0; c < TC_BN / 32; ++c) {
-                if (!X3 || c >= nchunks) break;  // MODE 2: fp32 read-modify-write through staging rows
-                uint32_t v[32];
-                ptx::tmem_ld32(tbase + c * 32, v);
-                if (corr) {  // main + correction, one IEEE fp32 addition
-                    uint32_t w[32];
-                    ptx::tmem_ld32(tbase + it.bn + c * 32, w);
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w2[e]));
+                    }
+                    // Row `lane` of the quadrant into the staging buffer ...
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w[e]));
-                }
-                // Row `lane` of the quadrant into the staging buffer ...
+                    for (int k = 0; k < 8; ++k)
+                        ptx::sts128(stg + (lane * STG_STRIDE + 4 * k) * 4, __uint_as_float(v[4 * k]),
+                                    __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
+                                    __uint_as_float(v[4 * k + 3]));
+                    __syncwarp();
+                    // ... and back out as 8 rows x 32 columns per instruction.
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    ptx::sts128(stg + (lane * STG_STRIDE + 4 * k) * 4, __uint_as_float(v[4 * k]),
-                                __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
-                                __uint_as_float(v[4 * k + 3]));
-                __syncwarp();
-                // ... and back out as 8 rows x 32 columns per instruction.
+                    for (int i = 0; i < 4; ++i) {
+                        const int lr = 8 * i + r8;
+                        const float4 a4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg) * 4);
+                        const float4 b4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg + 4) * 4);
+                        if (rok[i] && c * 32 + cg < ncols) {
+                            float4* dp = reinterpret_cast<float4*>(drowf[i] + c * 32);
+                            float4 o0 = olda[i], o1 = oldb[i];
+                            o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
+                            o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
+                            dp[0] = o0;
+                            dp[1] = o1;
+                        }
+                    }
+                    __syncwarp();
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int lr = 8 * i + r8;
-                    const float4 a4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg) * 4);
-                    const float4 b4 = ptx::lds128f(stg + (lr * STG_STRIDE + cg + 4) * 4);
-                    // fp32 read-modify-write (the old values were prefetched into L2)
-                    if (rok[i] && c * 32 + cg < ncols) {
-                        float4* dp = reinterpret_cast<float4*>(drowf[i] + c * 32);
-                        float4 o0 = dp[0], o1 = dp[1];
-                        o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
-                        o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
-                        dp[0] = o0;
-                        dp[1] = o1;
+                    for (int i = 0; i < 4; ++i) {
+                        olda[i] = nxa[i];
+                        oldb[i] = nxb[i];
                     }
                 }
-                __syncwarp();
             }
             ptx::tc_fence_before();
             __syncwarp();
