@@ -1105,13 +1105,14 @@ struct ItemCost {
 };
 
 // fp32 from three tf32 products, both products in one launch: a k-block of
-// 32 fp32 of K with three pair MMAs takes about 0.86 us at width 256 and 0.55
-// at 128, and with a correction accumulator a 256-wide tile fills all 512
-// tensor-memory columns, so its fp32 epilogue (about 12 us) is not
-// overlapped. Fitted, through this planner's own longest-first schedule, to
-// the paired launches of the GPT-2 XL fc and qkv layers at both widths
-// (612, 650, 508, 457 us measured; 612, 642, 507, 459 modelled).
-double x3_item_us(int kb, int bn, bool corr) { return kb * (bn == 256 ? 0.86 : 0.55) + (bn == 256 && corr ? 12.0 : 0.0); }
+// 32 fp32 of K with three pair MMAs takes about 0.88 us at width 256 and 0.55
+// at 128; with a correction accumulator a 256-wide tile fills all 512
+// tensor-memory columns, so its fp32 epilogue is not overlapped (about 1 us
+// left exposed once its loads are pipelined). Fitted, through this planner's
+// own longest-first schedule, to the paired launches of the GPT-2 XL fc and
+// qkv layers at both widths (GEMM part 581, 648, 473, 452 us measured; 581,
+// 642, 474, 459 modelled).
+double x3_item_us(int kb, int bn, bool corr) { return kb * (bn == 256 ? 0.88 : 0.55) + (bn == 256 && corr ? 1.0 : 0.0); }
 
 ItemCost item_cost(const TcPlan& pl, int w) {
     if (pl.x3) {
