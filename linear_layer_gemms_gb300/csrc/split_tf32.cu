@@ -34,50 +34,72 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
     lo = x - hi;
 }
 
-// src (R x Cc, row-major) in 32 x 32 tiles, 256 threads (32 x 8):
+// src (R x Cc, row-major, Cc a multiple of 4) in 64 x 64 tiles, 256 threads,
+// 16-byte accesses throughout:
 //   COPY:   lo with the layout of src (src itself is the high part)
-//   TRANS:  thi / tlo = the transpose (Cc x R), row pitch ldT
-//   COLSUM: part[tile row][c] = sum of the tile's rows of column c, in row order
+//   TRANS:  thi / tlo = the transpose (Cc x R), row pitch ldT (a multiple of 4,
+//           >= R; the pitch's padding columns may be written)
+//   COLSUM: part[32-row tile][c] = the sum of the tile's rows of column c, in
+//           row order (two 32-row tiles per block)
+constexpr int ST = 64;        // tile side
+constexpr int ST_PAD = ST + 1;  // shared row pitch: the transposed reads fall in distinct banks
 template <bool COPY, bool TRANS, bool COLSUM>
 __global__ void __launch_bounds__(256) split_kernel(const float* __restrict__ src, int64_t R, int64_t Cc,
-                                                    float* __restrict__ hi, float* __restrict__ lo,
-                                                    float* __restrict__ thi, float* __restrict__ tlo, int64_t ldT,
-                                                    float* __restrict__ part) {
-    __shared__ float t[TILE][TILE + 1];
-    const int tx = static_cast<int>(threadIdx.x & 31), ty = static_cast<int>(threadIdx.x >> 5);
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * TILE, c0 = static_cast<int64_t>(blockIdx.x) * TILE;
+                                                    float* __restrict__ lo, float* __restrict__ thi,
+                                                    float* __restrict__ tlo, int64_t ldT, float* __restrict__ part) {
+    __shared__ float t[ST][ST_PAD];
+    const int tid = static_cast<int>(threadIdx.x);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * ST, c0 = static_cast<int64_t>(blockIdx.x) * ST;
+    // load: 64 rows x 16 float4; thread tid takes float4 q = tid % 16 of rows tid / 16 + 16 i
+    const int q = tid & 15;
 #pragma unroll
-    for (int i = 0; i < TILE / 8; ++i) {
-        const int64_t r = r0 + ty + 8 * i, c = c0 + tx;
-        float x = 0.f;
+    for (int i = 0; i < 4; ++i) {
+        const int lr = (tid >> 4) + 16 * i;
+        const int64_t r = r0 + lr, c = c0 + 4 * q;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < R && c < Cc) {
-            x = __ldcs(src + r * Cc + c);
+            x = __ldcs(reinterpret_cast<const float4*>(src + r * Cc + c));
             if (COPY) {
-                float h, l;
-                split_tf32(x, h, l);
-                lo[r * Cc + c] = l;
+                float h, l0, l1, l2, l3;
+                split_tf32(x.x, h, l0);
+                split_tf32(x.y, h, l1);
+                split_tf32(x.z, h, l2);
+                split_tf32(x.w, h, l3);
+                *reinterpret_cast<float4*>(lo + r * Cc + c) = make_float4(l0, l1, l2, l3);
             }
         }
-        t[ty + 8 * i][tx] = x;
+        t[lr][4 * q] = x.x;
+        t[lr][4 * q + 1] = x.y;
+        t[lr][4 * q + 2] = x.z;
+        t[lr][4 * q + 3] = x.w;
     }
     if (!TRANS && !COLSUM) return;
     __syncthreads();
     if (TRANS) {
+        // transposed row c0 + oc holds source rows r0 .. r0 + 63: thread tid
+        // writes float4 q (source rows 4q .. 4q + 3) of rows oc = tid / 16 + 16 i
 #pragma unroll
-        for (int i = 0; i < TILE / 8; ++i) {
-            const int64_t c = c0 + ty + 8 * i, r = r0 + tx;  // row c, column r of the transpose
+        for (int i = 0; i < 4; ++i) {
+            const int oc = (tid >> 4) + 16 * i;
+            const int64_t c = c0 + oc, r = r0 + 4 * q;
             if (c < Cc && r < R) {
-                float h, l;
-                split_tf32(t[tx][ty + 8 * i], h, l);
-                thi[c * ldT + r] = h;
-                tlo[c * ldT + r] = l;
+                float h[4], l[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split_tf32(t[4 * q + e][oc], h[e], l[e]);
+                *reinterpret_cast<float4*>(thi + c * ldT + r) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4*>(tlo + c * ldT + r) = make_float4(l[0], l[1], l[2], l[3]);
             }
         }
     }
-    if (COLSUM && ty == 0 && c0 + tx < Cc) {
-        float s = 0.f;
-        for (int i = 0; i < TILE; ++i) s += t[i][tx];  // rows past R hold 0
-        part[static_cast<int64_t>(blockIdx.y) * Cc + c0 + tx] = s;
+    if (COLSUM && tid < 2 * ST) {
+        // column tid % 64 of 32-row half tid / 64 (rows past R hold 0)
+        const int col = tid & (ST - 1), half = tid >> 6;
+        const int64_t tile = static_cast<int64_t>(blockIdx.y) * 2 + half;
+        if (c0 + col < Cc && r0 + 32 * half < R) {
+            float s = 0.f;
+            for (int i = 0; i < 32; ++i) s += t[32 * half + i][col];
+            part[tile * Cc + c0 + col] = s;
+        }
     }
 }
 
@@ -108,10 +130,10 @@ __global__ void __launch_bounds__(32 * TS_SLICES) tile_sum_kernel(float* __restr
 }
 
 template <bool COPY, bool TRANS, bool COLSUM>
-cudaError_t launch_split(const float* src, int64_t R, int64_t Cc, float* hi, float* lo, float* thi, float* tlo,
-                         int64_t ldT, float* part, cudaStream_t stream) {
-    const dim3 grid(static_cast<unsigned>((Cc + TILE - 1) / TILE), static_cast<unsigned>((R + TILE - 1) / TILE));
-    split_kernel<COPY, TRANS, COLSUM><<<grid, 256, 0, stream>>>(src, R, Cc, hi, lo, thi, tlo, ldT, part);
+cudaError_t launch_split(const float* src, int64_t R, int64_t Cc, float* lo, float* thi, float* tlo, int64_t ldT,
+                         float* part, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((Cc + ST - 1) / ST), static_cast<unsigned>((R + ST - 1) / ST));
+    split_kernel<COPY, TRANS, COLSUM><<<grid, 256, 0, stream>>>(src, R, Cc, lo, thi, tlo, ldT, part);
     return cudaGetLastError();
 }
 
@@ -160,14 +182,14 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
     float* inpT_lo = take(static_cast<size_t>(C) * ldbt * 4);
     float* part = dbias ? take(static_cast<size_t>((BT + TILE - 1) / TILE) * OC * 4) : nullptr;
 
-    cudaError_t e = dbias ? launch_split<true, true, true>(dout, BT, OC, nullptr, dout_lo, doutT_hi, doutT_lo, ldbt,
+    cudaError_t e = dbias ? launch_split<true, true, true>(dout, BT, OC, dout_lo, doutT_hi, doutT_lo, ldbt,
                                                            part, stream)
-                          : launch_split<true, true, false>(dout, BT, OC, nullptr, dout_lo, doutT_hi, doutT_lo, ldbt,
+                          : launch_split<true, true, false>(dout, BT, OC, dout_lo, doutT_hi, doutT_lo, ldbt,
                                                             nullptr, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<false, true, false>(weight, OC, C, nullptr, nullptr, wT_hi, wT_lo, OC, nullptr, stream);
+    e = launch_split<false, true, false>(weight, OC, C, nullptr, wT_hi, wT_lo, OC, nullptr, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<false, true, false>(inp, BT, C, nullptr, nullptr, inpT_hi, inpT_lo, ldbt, nullptr, stream);
+    e = launch_split<false, true, false>(inp, BT, C, nullptr, inpT_hi, inpT_lo, ldbt, nullptr, stream);
     if (e != cudaSuccess) return e;
     if (dbias) {
         tile_sum_kernel<<<static_cast<unsigned>((OC + 31) / 32), 32 * TS_SLICES, 0, stream>>>(
@@ -216,9 +238,9 @@ cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight,
     float* w_lo = reinterpret_cast<float*>(w + a(static_cast<size_t>(BT) * C * 4));
     cudaError_t e = fill_rows_launch(out, bias, BT, OC, MMBWD_F32, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<true, false, false>(inp, BT, C, nullptr, inp_lo, nullptr, nullptr, 0, nullptr, stream);
+    e = launch_split<true, false, false>(inp, BT, C, inp_lo, nullptr, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
-    e = launch_split<true, false, false>(weight, OC, C, nullptr, w_lo, nullptr, nullptr, 0, nullptr, stream);
+    e = launch_split<true, false, false>(weight, OC, C, w_lo, nullptr, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
     const TcPlan p = tc_make_plan_x3(BT, OC, C, num_sms);
     return tc_launch_x3(p, out, inp, inp_lo, C, weight, w_lo, C, BT, OC, C, stream);
