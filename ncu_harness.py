@@ -115,7 +115,8 @@ CASES = {
         "title": "GPT-2 XL fc backward in fp32 (three tf32 products), B=4 T=1024 C=1600 OC=6400",
         "cmd": _case_bench("xl_fc_f32"),
         "kernel": "tc_mmbwd_kernel", "skip": 4, "count": 2,
-        "labels": ["dinp product", "dweight product"], "units": None, "file": "tc_mmbwd_kernel_x3_xl_fc_f32",
+        "labels": ["both products", "next call"], "units": [_bw_units(4096, 1600, 6400, False, 4)] * 2,
+        "file": "tc_mmbwd_kernel_x3_xl_fc_f32",
         "sources": TC_SOURCES + ("split_tf32.cu",),
     },
     "ln_xl": {
@@ -328,6 +329,7 @@ def main(argv=None):
             print(f"{k}: {v['title']}")
         return 0
     os.makedirs(a.raw_dir, exist_ok=True)
+    os.makedirs(a.out_dir, exist_ok=True)
     names = a.cases or list(CASES)
     bad = [n for n in names if n not in CASES]
     if bad:
