@@ -33,7 +33,7 @@ extern "C" {
 #endif
 
 /* Limits of the device sort (B*T positions, V token ids) and of the channel
- * count C. Up to 16384 positions are sorted by one block; more by a
+ * count C. Up to 16384 positions are sorted by one cluster of eight CTAs; more by a
  * multi-block radix sort (a few more launches). */
 #define ENCBWD_MAX_POSITIONS (1 << 24)
 #define ENCBWD_MAX_VOCAB 131071

@@ -673,11 +673,11 @@ __global__ void __launch_bounds__(256, 2) enc_window_kernel(T* __restrict__ dwte
 //   scan     one block turns H into exclusive prefixes in (digit, tile) order:
 //            where each tile's keys of each digit start in the output;
 //   scatter  every tile ranks its keys stably by digit (the packed per-thread
-//            counters of the one-block sort) and writes them there.
+//            counters of the cluster sort) and writes them there.
 // The initial keys are in position order, so the positions of a token end up
 // in increasing order. A last launch derives the window tables from the
 // sorted keys by binary search (a run is the range of one token).
-constexpr int ENC_FAST_MAX = 16384;  // positions the one-block sort takes
+constexpr int ENC_FAST_MAX = 16384;  // positions the cluster sort takes
 constexpr int MB_KPT = 8;            // keys per thread of a tile
 constexpr int MB_TILE = MB_KPT * ENC_SORT_THREADS;
 
@@ -754,7 +754,7 @@ __global__ void __launch_bounds__(ENC_SORT_THREADS) enc_mb_scan_kernel(int* __re
 
 // Stable scatter of one tile by the digit at `sh`: thread t owns keys
 // i0 + t*MB_KPT .. +MB_KPT-1 (keys past BT take no part); their slots in the
-// tile sorted by digit come from the packed counters as in the one-block
+// tile sorted by digit come from the packed counters as in the cluster
 // sort, and O (the scanned H) gives where the tile's keys of each digit go.
 __global__ void __launch_bounds__(ENC_SORT_THREADS, 1)
     enc_mb_scatter_kernel(const unsigned long long* __restrict__ src, unsigned long long* __restrict__ dst, int BT,
