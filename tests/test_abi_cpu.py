@@ -151,6 +151,18 @@ def test_tile_width_override(monkeypatch):
     assert (a["tile_n_dinp"], a["tile_n_dweight"]) == (256, 128)
 
 
+def test_fp32_tensor_core_plans_pair_the_products(monkeypatch):
+    """The fp32 tensor-core backward runs both products in one launch (after the
+    pre-pass: three split launches and the dbias tile sum) where their
+    reductions agree on the correction accumulator, else one launch each."""
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    paired = mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32, 152)
+    assert paired["path"] == 2 and paired["launches"] == 5 and paired["table"] == 1
+    assert paired["items"] == paired["dinp_tiles"] + paired["dweight_tiles"]
+    split = mm.mmbwd_plan_info(1, 2560, 264, 512, mm.F32, 152)  # only B*T above the threshold
+    assert split["path"] == 2 and split["launches"] == 6
+
+
 def test_workspace_size_formula():
     import os as _os
     _os.environ["MMBWD_SPLITK"] = "2"

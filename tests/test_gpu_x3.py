@@ -33,8 +33,12 @@ def inputs(BT, C, OC, seed=0):
 
 
 # (BT, C, OC): K = OC or BT ragged against 32; BT not a multiple of 4 (the
-# transposed operands' rows are padded); one 256 x 128 tile; several tiles.
-SHAPES = [(64, 8, 4), (301, 264, 136), (513, 520, 1028), (256, 128, 256), (2048, 768, 768)]
+# transposed operands' rows are padded); one 256 x 128 tile; several tiles;
+# both reductions above 2048 (both products in one launch, each with its
+# correction accumulator); only the dweight reduction above 2048 (the
+# products in two launches).
+SHAPES = [(64, 8, 4), (301, 264, 136), (513, 520, 1028), (256, 128, 256), (2048, 768, 768), (2304, 264, 2304),
+          (2560, 264, 512)]
 
 
 @pytest.mark.parametrize("bias", [True, False])
@@ -53,6 +57,23 @@ def test_x3_parity(shape, bias, monkeypatch):
         assert_close(to_host(g["dbias"], "f32"), ref[2], "f32", "dbias")
     else:
         assert np.array_equal(to_host(g["dbias"], "f32"), x["dbias"].astype(np.float64))
+
+
+@pytest.mark.parametrize("tile_n", ["256", "128"])
+def test_x3_paired_launch_tile_widths(tile_n, monkeypatch):
+    """Both products in one launch at either tile width: the dinp and dweight
+    tiles share the CTA pairs (ragged in every dimension)."""
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    monkeypatch.setenv("MMBWD_TILE_N_X3", tile_n)
+    BT, C, OC = 777, 392, 520
+    info = mm.mmbwd_plan_info(1, BT, C, OC, mm.F32)
+    assert info["launches"] == 5 and info["tile_n_dinp"] == int(tile_n) == info["tile_n_dweight"]
+    x = inputs(BT, C, OC, seed=7)
+    g = run_gpu(x, 1, BT, C, OC, "f32")
+    ref = oracle.get("omp").matmul_backward(x["dout"], x["inp"], x["weight"], "f32", x["dinp"], x["dweight"])
+    assert_close(to_host(g["dinp"], "f32"), ref[0], "f32", "dinp")
+    assert_close(to_host(g["dweight"], "f32"), ref[1], "f32", "dweight")
+    assert_close(to_host(g["dbias"], "f32"), ref[2], "f32", "dbias")
 
 
 def test_x3_deterministic(monkeypatch):
