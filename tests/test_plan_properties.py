@@ -1,0 +1,73 @@
+"""Planner invariants over many shapes (host only, no GPU): every plan the
+C ABI reports for seeded random GPT-style shapes is internally consistent --
+tile counts, items and splits add up, the grid is an even number of CTAs no
+larger than the work, every split is non-empty -- and the fp32 tensor-core
+backward runs its two products in one launch exactly when their reduction
+lengths agree on the correction accumulator."""
+import numpy as np
+
+import linear_layer_gemms_gb300 as mm
+
+CORR_K = 2048  # reductions longer than this keep the fp32 correction products apart
+
+
+def _shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(n):
+        B = int(rng.integers(1, 9))
+        T = int(rng.integers(1, 2049))
+        C = 8 * int(rng.integers(1, 1025))
+        OC = 8 * int(rng.integers(1, 4097))
+        yield B, T, C, OC
+
+
+def test_bf16_plans_are_consistent():
+    for B, T, C, OC in _shapes(300, 11):
+        a = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        BT = B * T
+        assert a["path"] == 1 and a["launches"] in (1, 2)
+        assert 2 <= a["grid"] <= 152 and a["grid"] % 2 == 0
+        assert a["tile_n_dinp"] in (128, 256) and a["tile_n_dweight"] in (128, 256)
+        assert a["dinp_tiles"] == -(-BT // 256) * -(-C // a["tile_n_dinp"])
+        assert a["dweight_tiles"] == -(-OC // 256) * -(-C // a["tile_n_dweight"])
+        assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"] * a["splits"]
+        assert a["grid"] // 2 <= a["items"]
+        kb = -(-BT // 64)
+        assert 1 <= a["splits"] <= 16
+        assert (a["splits"] - 1) * a["kb_per_split"] < kb <= a["splits"] * a["kb_per_split"]
+        assert (a["launches"] == 2) == (a["splits"] > 1)
+        ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
+        assert (ws > 0) == (a["splits"] > 1)
+
+
+def test_fp32_tensor_core_plans_are_consistent(monkeypatch):
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    seen = set()
+    for B, T, C, OC in _shapes(300, 12):
+        a = mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 152)
+        BT = B * T
+        if a["path"] != 2:  # shapes the split layout cannot take run on the FMA kernel
+            assert a["path"] == 0
+            continue
+        assert a["tile_m"] == 256 and a["tile_k"] == 32 and a["grid"] % 2 == 0 and a["grid"] <= 152
+        assert a["dinp_tiles"] == -(-BT // 256) * -(-C // a["tile_n_dinp"])
+        assert a["dweight_tiles"] == -(-OC // 256) * -(-C // a["tile_n_dweight"])
+        assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"]
+        paired = (OC > CORR_K) == (BT > CORR_K) and a["items"] <= 3072
+        assert a["launches"] == (5 if paired else 6)
+        if paired:
+            assert a["tile_n_dinp"] == a["tile_n_dweight"] and a["table"] == 1
+        seen.add(a["launches"])
+    assert seen == {5, 6}  # both kinds of plan occur among the shapes
+
+
+def test_fp32_workspace_holds_the_split_operands():
+    # dout's low part, dout^T / weight^T / inp^T high and low parts (rows of
+    # B*T padded to a multiple of 4), the per-32-row column sums of dout
+    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for B, T, C, OC in [(4, 1024, 1600, 6400), (1, 301, 264, 136), (2, 777, 392, 520)]:
+        BT = B * T
+        ld = (BT + 3) // 4 * 4
+        want = a(BT * OC * 4) + 2 * a(OC * ld * 4) + 2 * a(C * OC * 4) + 2 * a(C * ld * 4) + a(-(-BT // 32) * OC * 4)
+        if mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 152)["path"] == 2:
+            assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.F32) == want
