@@ -473,7 +473,7 @@ def run_gpu(args):
     return 0
 
 
-OTHER_CONFIGS = ("tiny", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
+OTHER_CONFIGS = ("tiny", "qkv", "attn_proj", "lm_head", "xl_fc_bf16", "xl_qkv_bf16", "xl_fc_f32", "xl_qkv_f32")
 LN_CONFIGS = ("ln_gpt2_small", "ln_xl", "ln_xl_f32", "ln_wide")
 ENC_CONFIGS = ("enc_gpt2_small", "enc_gpt2_small_f32")
 # the same workload in two calls: encbwd_prepare (timed on its own) ahead of

@@ -1087,18 +1087,19 @@ long env_long(const char* name, long dflt) {
     return (end && *end == '\0') ? v : dflt;
 }
 
-// Planner cost model (µs), from per-item timelines on GB300 under load. An item
-// costs its main loop (a 64-deep k-block of a 256 x bn pair tile) or its
-// epilogue, whichever is longer, since the two overlap across the two
-// accumulators; the last item's epilogue is not overlapped. Split dweight adds
-// the fixup pass.
-// One k-block of a pair (a 256 x bn tile, 64 deep): load-bound (both 64-column
-// boxes of an operand in one TMA request; measured on the LM head, about
-// 0.37 us per pair k-block under load).
-double t_kb(int bn) { return bn == 256 ? 0.31 : 0.29; }
-double t_rmw(int bn) { return 0.3 + 2.4 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
-double t_partial(int bn) { return 0.3 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
-constexpr double T_ITEM = 0.3;                                 // per-item handoff
+// Planner cost model (µs). An item costs its main loop (a 64-deep k-block of
+// a 256 x bn pair tile) or its epilogue, whichever is longer, since the two
+// overlap across the two accumulators, plus a per-item handoff; the last
+// item's epilogue is not overlapped. Split dweight adds the fixup pass. The
+// constants are fitted, through this planner's own schedule, to 60 plans
+// forced on GB300 (six GPT-2 layer shapes, split counts 1 to 5, both tile
+// widths; squared relative error 0.07, and the measured-best plan picked for
+// every shape). A k-block costs the same at either width: the stage ring's
+// round trip, not the MMA, sets a 128-wide k-block's time.
+double t_kb(int /*bn*/) { return 0.32; }
+double t_rmw(int bn) { return 0.9 + 3.5 * bn / 256.0; }      // bf16 read-modify-write of 128 x bn
+double t_partial(int bn) { return 1.5 + 1.6 * bn / 256.0; }  // fp32 partial store of 128 x bn
+constexpr double T_ITEM = 1.0;                                 // per-item handoff
 
 struct ItemCost {
     double run, epi;
@@ -1134,11 +1135,9 @@ double fixup_cost(const TcPlan& pl, int64_t C, int64_t OC) {
     if (pl.splits == 1) return 0.0;
     // a launch gap, about 1 us per split (each adds a wave of partial-store
     // epilogues), and the S fp32 partials read and dweight read and written
-    // (L2-resident: 4 MB/us). Fitted to the GPT-2 attention projection, timed
-    // back to back with 2, 3, 4 and 5 splits: 31.8, 27.7, 30.0, 29.3 us
-    // against 31.8, 26.9, 27.7, 29.5 modelled.
+    // (L2-resident: 8 MB/us)
     const double bytes = static_cast<double>(OC) * C * (4.0 * pl.splits + 4.0);
-    return 6.0 + 1.0 * pl.splits + bytes / 4e6;
+    return 3.0 + 1.0 * pl.splits + bytes / 8e6;
 }
 
 // Longest-first greedy assignment of items to pairs; fills pl.sched and

@@ -160,6 +160,7 @@ WORKLOADS = {
     # fp32 check with += pre-fill
     "tiny": Workload("tiny", [_gpt2("tiny", 2, 64, 64, 192, "f32", dout_std=1.0, init_std=0.01)]),
     "attn_proj": Workload("attn_proj", [_gpt2("attn_proj", 8, 1024, 768, 768, "bf16")]),
+    "qkv": Workload("qkv", [_gpt2("qkv", 8, 1024, 768, 2304, "bf16")]),
     # the headline: the two MLP linears of one GPT-2 small block
     "mlp": Workload("mlp", [_gpt2("mlp_fc", 8, 1024, 768, 3072, "bf16", layer=0),
                             _gpt2("mlp_fc_proj", 8, 1024, 3072, 768, "bf16", layer=1)]),

@@ -12,7 +12,7 @@ from gpu_helpers import TOL, scaled_error, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["tiny", "attn_proj", "mlp:0", "mlp:1", "lm_head", "xl_fc_bf16", "xl_qkv_bf16",
+CONFIGS = ["tiny", "qkv", "attn_proj", "mlp:0", "mlp:1", "lm_head", "xl_fc_bf16", "xl_qkv_bf16",
            "xl_fc_f32", "xl_qkv_f32", "xl_fc_f32@ffma"]  # @ffma: the fp32 FMA kernel forced
 REPEATS = 10
 
