@@ -21,8 +21,9 @@
  *   MMBWD_F32:  fp32 storage and fp32-accurate products. Problems large enough
  *               to fill the GPU (B*T, C, OC >= 256, C a multiple of 8), with both
  *               reduction lengths (OC and B*T) at most 8192, run on the tensor
- *               cores: each operand is split into its tf32 value and the exact
- *               fp32 remainder, and each product is formed from three tf32
+ *               cores: the kernel splits each staged operand, in shared memory,
+ *               into its tf32 value and the exact fp32 remainder (no copy in
+ *               device memory, no workspace), and each product is formed from three tf32
  *               products, hi.hi in one fp32 accumulator and hi.lo + lo.hi in a
  *               second, added once at the end. The tensor core rounds each
  *               accumulation toward zero, so this path's error grows with the
@@ -95,8 +96,7 @@ extern "C" {
  * A pointer may be NULL only when its tensor has no elements.
  *
  * Workspace: the bf16 path may need a library-owned fp32 workspace for its
- * split reduction, and the fp32 tensor-core path one for the split operands
- * (mmbwd_workspace_bytes). It is allocated per device on
+ * split reduction (mmbwd_workspace_bytes); fp32 needs none. It is allocated per device on
  * first need and reused; growing it synchronises the device, so the first
  * call of a new, larger shape should not be made during stream capture
  * (MMBWD_ERR_CAPTURE). Calls that share a device share this workspace:
@@ -205,8 +205,7 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
  * tensor cores for large layers (OC a multiple of 8, C at most 8192; out is set
  * to the bias, then the product is added), FFMA otherwise. Same alignment, aliasing (out
  * must not overlap an input), status codes, asynchrony and determinism as
- * mmbwd_run; the fp32 tensor-core path uses the library workspace. C == 0
- * gives out = bias (or 0).
+ * mmbwd_run; no workspace. C == 0 gives out = bias (or 0).
  */
 int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bias_or_null, int64_t B,
                   int64_t T, int64_t C, int64_t OC, int dtype, cudaStream_t stream);
@@ -250,12 +249,9 @@ void mmbwd_debug_fail_next_launch(int n);
  * advance. Nothing in the buffer has to start at zero: every value a call
  * reads there is written earlier by the same call.
  *
- * fp32: always the fp32 fused-multiply-add kernel, which needs no scratch at
- * all (the three-tf32-product path of mmbwd_run needs a workspace far larger
- * than the fixed buffer). Where mmbwd_run takes that tensor-core path (large
- * layers), results here differ from its results in the last bits (both are
- * fp32-accurate) and the call is several times slower; mmbwd_workspace_bytes()
- * reports that path's workspace, which this entry point does not use.
+ * fp32: the path mmbwd_run takes (three tf32 products on the tensor cores for
+ * large layers, the fused-multiply-add kernel otherwise), so the results are
+ * those of mmbwd_run; neither path uses any scratch.
  *
  * All calls on a device share the one buffer, which keeps whatever the last
  * call left in it: calls that overlap on the GPU (for example on two streams

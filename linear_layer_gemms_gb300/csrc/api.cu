@@ -292,7 +292,7 @@ size_t mmbwd_workspace_bytes(int64_t B, int64_t T, int64_t C, int64_t OC, int dt
     Shape s;
     if (check_shape(B, T, C, OC, dtype, &s) != MMBWD_OK) return 0;
     if (s.BT == 0 || C == 0 || OC == 0) return 0;
-    if (dtype == MMBWD_F32) return use_x3(s.BT, C, OC) ? x3_workspace_bytes(s.BT, C, OC, true) : 0;
+    if (dtype == MMBWD_F32) return 0;  // both fp32 paths work in place
     int sms = 0;
     {
         std::lock_guard<std::mutex> g(g_mutex);
@@ -323,18 +323,18 @@ int mmbwd_plan_info(int64_t B, int64_t T, int64_t C, int64_t OC, int dtype, int 
                               TC_PAIR_BM, pl.dinp_bn, pl.dw_bn, TC_BK, TC_STAGES, pl.launches(), 1};
         for (int i = 0; i < 15; ++i) v[i] = vals[i];
     } else if (use_x3(s.BT, C, OC)) {
-        // the pre-pass (three split launches and the dbias tile sum), then both
-        // products in one launch, or one launch each where they cannot share one
+        // both products (and dbias) in one launch, or one launch each where
+        // they cannot share one
         static thread_local TcPlan pp;
         pp = tc_make_plan_x3_pair(s.BT, C, OC, num_sms);
         if (pp.n_items > 0) {
             const int vals[15] = {2, pp.grid, pp.n_items, 1, 0, pp.n_dinp_items, pp.n_dw_items, pp.table,
-                                  TC_PAIR_BM, pp.dinp_bn, pp.dw_bn, TC_BK / 2, TC_STAGES_X3, 5, 1};
+                                  TC_PAIR_BM, pp.dinp_bn, pp.dw_bn, TC_BK / 2, TC_STAGES_X3, 1, 1};
             for (int i = 0; i < 15; ++i) v[i] = vals[i];
         } else {
             const TcPlan p1 = tc_make_plan_x3(s.BT, C, OC, num_sms), p2 = tc_make_plan_x3(OC, C, s.BT, num_sms);
             const int vals[15] = {2, std::max(p1.grid, p2.grid), p1.n_items + p2.n_items, 1, 0, p1.n_items,
-                                  p2.n_items, 0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES_X3, 6, 1};
+                                  p2.n_items, 0, TC_PAIR_BM, p1.dinp_bn, p2.dinp_bn, TC_BK / 2, TC_STAGES_X3, 2, 1};
             for (int i = 0; i < 15; ++i) v[i] = vals[i];
         }
     } else {
@@ -405,11 +405,9 @@ int run_backward(void* dinp, void* dweight, void* dbias, const void* dout, const
 
     if (dtype == MMBWD_F32) {
         if (use_x3(s.BT, C, OC)) {
-            rc = ensure_workspace(*d, x3_workspace_bytes(s.BT, C, OC, dbias != nullptr), stream);
-            if (rc != MMBWD_OK) return rc;
             e = x3_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
                           static_cast<const float*>(dout), static_cast<const float*>(inp),
-                          static_cast<const float*>(weight), s.BT, C, OC, d->ws, d->num_sms, stream);
+                          static_cast<const float*>(weight), s.BT, C, OC, d->num_sms, stream);
         } else {
             e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
                             static_cast<const float*>(dout), static_cast<const float*>(inp),
@@ -525,11 +523,9 @@ int mmbwd_forward(void* out, const void* inp, const void* weight, const void* bi
     }
     if (dtype == MMBWD_F32) {
         if (use_x3_forward(s.BT, C, OC)) {
-            rc = ensure_workspace(*d, x3_forward_workspace_bytes(s.BT, C, OC), stream);
-            if (rc != MMBWD_OK) return rc;
             e = x3_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
                                   static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC,
-                                  d->ws, d->num_sms, stream);
+                                  d->num_sms, stream);
         } else {
             e = simt_forward_launch(static_cast<float*>(out), static_cast<const float*>(inp),
                                     static_cast<const float*>(weight), static_cast<const float*>(bias), s.BT, C, OC,
@@ -871,10 +867,15 @@ extern "C" int mmbwd_run_static_scratch(void* dinp, void* dweight, void* dbias, 
         if (dbias) e = colsum_launch(dbias, dout, s.BT, OC, dtype, false, 0, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
-    if (dtype == MMBWD_F32) {  // the fp32 path uses no scratch at all
-        e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
-                        static_cast<const float*>(dout), static_cast<const float*>(inp),
-                        static_cast<const float*>(weight), s.BT, C, OC, stream);
+    if (dtype == MMBWD_F32) {  // neither fp32 path uses scratch: mmbwd_run's choice
+        if (use_x3(s.BT, C, OC))
+            e = x3_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                          static_cast<const float*>(dout), static_cast<const float*>(inp),
+                          static_cast<const float*>(weight), s.BT, C, OC, d->num_sms, stream);
+        else
+            e = simt_launch(static_cast<float*>(dinp), static_cast<float*>(dweight), static_cast<float*>(dbias),
+                            static_cast<const float*>(dout), static_cast<const float*>(inp),
+                            static_cast<const float*>(weight), s.BT, C, OC, stream);
         return e == cudaSuccess ? MMBWD_OK : MMBWD_ERR_CUDA;
     }
     const TcPlan& plan = cached_plan(s.BT, C, OC, d->num_sms);

@@ -38,6 +38,8 @@ enum WaitSite : int {
     SITE_SELFTEST = 9,
     SITE_FORWARD_FULL = 10,
     SITE_EPI_OLD = 11,
+    SITE_CONV_RAW = 12,  // MODE 2: operand split warps waiting for a raw fp32 stage
+    SITE_MMA_CONV = 13,  // MODE 2: MMA issuer waiting for both CTAs' split stages
 };
 
 // Schedule of a launch: which work items each CTA pair (a cluster of two CTAs)
@@ -70,7 +72,7 @@ struct TcPlan {
     int n_dinp_items;  // dinp_tiles_m * dinp_tiles_n
     int n_items;
     int table;         // 1: per-pair item lists in `sched`; 0: round-robin
-    int x3;            // fp32 (three tf32 products): both products K-major, tf32 item costs
+    int x3;            // fp32 (three tf32 products, operands split in the kernel): tf32 item costs
     int x3_corr;       // fp32: the correction products in their own accumulator
     int grid;          // CTAs (twice the number of CTA pairs)
     double est_us;     // the planner's time estimate
@@ -105,6 +107,13 @@ struct TcParams {
     int wide_maps;                  // TC_WIDE_* bits: operands that also have a two-box map
     int bias_mma;                   // dbias from an extra pair MMA against a ones tile (MMBWD_DBIAS=ones)
     int x3_corr;                    // MODE 2: hi.lo + lo.hi in their own accumulator (long K)
+    // MODE 2: which raw fp32 operands arrive MN-major (and are transposed in
+    // shared memory); the others arrive K-major. Bits: 1 A and 2 B of the
+    // dinp-type items, 4 A and 8 B of the dweight items.
+    int x3_mn;
+    // MODE 2: fp32 dbias (overwritten) = the sums over K of A's rows, formed
+    // on the items of column tile 0 whose A arrives MN-major; null: none
+    float* x3_dbias;
 };
 
 // MODE 2 reductions longer than this keep the two correction products in an
@@ -129,24 +138,28 @@ TcPlan tc_make_plan(int64_t BT, int64_t C, int64_t OC, int num_sms);
 TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms);
 
 // One fp32 product D (M x N, row-major, leading dimension N) += A (M x K) .
-// B (N x K)^T from tf32 halves (hi: the tf32 value, lo: the exact remainder),
-// both K-major with leading dimensions lda, ldb (elements, multiples of 4).
+// B (N x K)^T from the raw fp32 operands: the kernel splits every staged
+// operand into its tf32 value (hi) and exact remainder (lo) in shared memory.
+// An operand is K-major (row r of A, or of B, holds K contiguous values,
+// leading dimension ld) or MN-major (row k holds the M, or N, contiguous
+// values of K index k, leading dimension ld); leading dimensions in elements,
+// multiples of 4. dbias_or_null: where A is MN-major, receives the sums of A's
+// rows over K (overwritten).
 TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms);
-cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
-                         const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
+cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* A, bool a_mn, int64_t lda, const float* B,
+                         bool b_mn, int64_t ldb, int64_t M, int64_t N, int64_t K, float* dbias_or_null,
                          cudaStream_t stream);
 // Both fp32 products of the backward in one launch, their items (tiles of
 // either product) assigned to CTA pairs longest first:
-//   dinp (BT x C) += A1 (BT x OC) . B1 (C x OC)^T     (A1 = dout, B1 = weight^T)
-//   dweight (OC x C) += A2 (OC x BT) . B2 (C x BT)^T  (A2 = dout^T, B2 = inp^T)
-// every operand as a tf32 high and low part, K-major (leading dimensions in
-// elements, multiples of 4). The plan has n_items == 0 where one launch does
-// not fit (then the products go to tc_launch_x3 one at a time).
+//   dinp (BT x C) += dout (BT x OC) . weight (OC x C)     A K-major, B MN-major
+//   dweight (OC x C) += dout^T (OC x BT) . inp (BT x C)   A and B MN-major
+// and dbias (fp32, overwritten, may be null) = the column sums of dout. The
+// plan has n_items == 0 where one launch does not fit (then the products go
+// to tc_launch_x3 one at a time).
 TcPlan tc_make_plan_x3_pair(int64_t BT, int64_t C, int64_t OC, int num_sms);
-cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, const float* a1_hi, const float* a1_lo,
-                              int64_t lda1, const float* b1_hi, const float* b1_lo, int64_t ldb1, const float* a2_hi,
-                              const float* a2_lo, int64_t lda2, const float* b2_hi, const float* b2_lo, int64_t ldb2,
-                              int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
+cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, float* dbias, const float* dout,
+                              const float* inp, const float* weight, int64_t BT, int64_t C, int64_t OC,
+                              cudaStream_t stream);
 cudaError_t tc_launch_forward(const TcPlan& plan, void* out, const void* inp, const void* weight,
                               const void* bias, int64_t BT, int64_t C, int64_t OC, cudaStream_t stream);
 

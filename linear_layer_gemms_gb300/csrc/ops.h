@@ -41,16 +41,13 @@ cudaError_t colsum_launch(void* dbias, const void* dout, int64_t BT, int64_t OC,
 
 // ---------------------------------------------------------------- fp32 on the tensor cores (3xTF32)
 
-int64_t x3_ld(int64_t n);
+// (no workspace: the kernel splits the raw fp32 operands in shared memory)
 bool x3_shape_ok(int64_t BT, int64_t C, int64_t OC);
-size_t x3_workspace_bytes(int64_t BT, int64_t C, int64_t OC, bool bias);
 cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
-                      const float* weight, int64_t BT, int64_t C, int64_t OC, void* ws, int num_sms,
-                      cudaStream_t stream);
+                      const float* weight, int64_t BT, int64_t C, int64_t OC, int num_sms, cudaStream_t stream);
 bool x3_forward_shape_ok(int64_t BT, int64_t C, int64_t OC);
-size_t x3_forward_workspace_bytes(int64_t BT, int64_t C, int64_t OC);
 cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight, const float* bias, int64_t BT,
-                              int64_t C, int64_t OC, void* ws, int num_sms, cudaStream_t stream);
+                              int64_t C, int64_t OC, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- encoder backward
 

@@ -96,7 +96,9 @@ constexpr int PART_CHUNK_BYTES = 32 * 32 * 4;
 // trip is about 2 us, five covered it only just) is worth more than a whole
 // tile of old values in flight: with five stages and eight buffers a warp
 // every bf16 backward plan ran 1-4 % slower. MODE 2 keeps three 64 KB stages
-// and the fp32 staging rows.
+// and the fp32 staging rows, and a second barrier per stage: the raw fp32
+// operands land on the first (TMA), the split planes are signalled on the
+// second (the split warps of both CTAs, on the even CTA's copy).
 template <int MODE>
 struct Smem {
     static constexpr bool X3 = MODE == 2;
@@ -111,7 +113,8 @@ struct Smem {
     static constexpr int BAR_TEMPTY = 2 * STAGES + 2;    // [2] accumulator drained by both CTAs (even CTA)
     static constexpr int BAR_TEARDOWN = 2 * STAGES + 4;
     static constexpr int BAR_OLD = 2 * STAGES + 5;       // [epilogue warp][slot] old chunk landed
-    static constexpr int N_BARS = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;
+    static constexpr int BAR_CONV = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;  // MODE 2: [stages] split planes ready
+    static constexpr int N_BARS = BAR_CONV + (X3 ? STAGES : 0);
     static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag
     static constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) & ~1023;
     static constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
@@ -143,11 +146,15 @@ struct Waiter {
 
     // Bounded wait for the phase of `bar` with parity `parity`. Returns false
     // on timeout (recorded) or when another warp of the CTA has aborted.
+    // CLUSTER: acquire at cluster scope (a barrier the other CTA of the pair
+    // arrives on).
+    template <bool CLUSTER = false>
     __device__ bool wait(uint32_t bar, uint32_t parity, int site, int item) const {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        auto probe = [&]() { return CLUSTER ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity); };
+        if (probe()) return true;
         const uint64_t t0 = ptx::globaltimer();
         for (uint32_t i = 1;; ++i) {
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (probe()) return true;
             if ((i & 31u) == 0) {
                 if (*abort) return false;
                 if (ptx::globaltimer() - t0 > timeout_ns) {
@@ -258,13 +265,82 @@ __device__ __forceinline__ uint4 add_sr8(uint4 old, const float (&s)[8], uint64_
                       add_sr_pair(old.w, s[6], s[7], static_cast<uint32_t>(w1 >> 32)));
 }
 
+// fp32 x = hi + lo with hi its tf32 truncation (13 low mantissa bits cleared)
+// and lo the exact remainder; the tensor core reads an fp32 operand as hi.
+__device__ __forceinline__ float tf32_lo(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+// Split warp, K-major raw operand: the tile in `hi` (n16 granules of 16
+// bytes, 128-byte swizzled rows; n16 a multiple of 256) is its own high
+// plane; its low plane goes to the same offsets in `lo`. Eight granules a
+// lane in flight (a warp reads 512 contiguous bytes per instruction).
+__device__ __forceinline__ void x3_split_k(uint32_t hi, uint32_t lo, int n16, int lane) {
+#pragma unroll 1
+    for (int i0 = 0; i0 < n16; i0 += 256) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = ptx::lds128f(hi + 16u * static_cast<uint32_t>(i0 + 32 * u + lane));
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            ptx::sts128(lo + 16u * static_cast<uint32_t>(i0 + 32 * u + lane), tf32_lo(x[u].x), tf32_lo(x[u].y),
+                        tf32_lo(x[u].z), tf32_lo(x[u].w));
+    }
+}
+
+// Split warp, MN-major raw operand: nbox (1 or 2) boxes of 32 K rows x 64
+// fp32 (256-byte rows, box j at j * 8 KB) in `lo`, transposed into both
+// K-major planes: row j * 64 + m holds the 32 K values of column m of box j in
+// 128 bytes, 16-byte granule g at g ^ (row & 7). Box j's raw bytes are exactly
+// where its 64 rows of the low plane go, so a box is read whole (lane l takes
+// columns l and l + 32: a warp reads 128 contiguous bytes per K row), the
+// warp synchronises, and its rows are written (a quarter warp's eight rows
+// hit eight distinct granule positions). With `sums`, sum[2 j + h] += the sum
+// of row j * 64 + 32 h + lane's 32 K values (pairwise, in a fixed order).
+__device__ __forceinline__ void x3_split_mn(uint32_t hi, uint32_t lo, int nbox, int lane, bool sums,
+                                            float (&sum)[4]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (j >= nbox) break;
+        float v[2][32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                v[h][k] = ptx::lds32f(lo + static_cast<uint32_t>(j * BOX_BYTES + k * 256 + (32 * h + lane) * 4));
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t row = static_cast<uint32_t>(j * 64 + 32 * h + lane);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const uint32_t off = row * 128u + ((static_cast<uint32_t>(g) ^ (row & 7u)) << 4);
+                const float* x = &v[h][4 * g];
+                ptx::sts128(hi + off, x[0], x[1], x[2], x[3]);
+                ptx::sts128(lo + off, tf32_lo(x[0]), tf32_lo(x[1]), tf32_lo(x[2]), tf32_lo(x[3]));
+            }
+            if (sums) {
+                float t[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) t[i] = v[h][2 * i] + v[h][2 * i + 1];
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+                sum[2 * j + h] += t[0];
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // MODE 0: the backward (dinp and dweight items). MODE 1: the forward
-// (dinp-type items with a K-major B and an overwrite epilogue). MODE 2: one
-// fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves, both
-// operands K-major: each operand arrives as a high part (its tf32 value) and
-// a low part (the exact remainder), and each K step issues three tf32 MMAs,
-// hi.hi + hi.lo + lo.hi, into one fp32 accumulator; fp32 read-modify-write
-// epilogue. MODE 3: the backward with stochastic rounding of the bf16 outputs
+// (dinp-type items with a K-major B and an overwrite epilogue). MODE 2: fp32
+// products D (M x N) += A (M x K) . B (N x K)^T from tf32 halves: the raw
+// fp32 operands arrive by TMA (K-major into the high plane, or MN-major into
+// the low plane as scratch), the two split warps of each CTA write both planes
+// K-major -- the high part (the value itself: the tensor core reads an fp32
+// operand as its tf32 truncation) and the low part (the exact remainder) --
+// and each K step issues three tf32 MMAs, hi.hi + hi.lo + lo.hi; fp32
+// read-modify-write epilogue. MODE 3: the backward with stochastic rounding of the bf16 outputs
 // (seeded; sr.cuh). Four instantiations, so that none pays for the
 // others' branches.
 template <int MODE>
@@ -325,10 +401,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader ? 2u : 1u);
+            // MODE 2: this CTA's raw copies only (the split warps signal the MMA)
+            ptx::mbar_init(bars + 8u * (BAR_FULL + s), leader && !X3 ? 2u : 1u);
             // refilled once the pair MMAs reading it have completed (one commit)
             // and this CTA's bias warps are done with it
-            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (bias_on && !p.bias_mma ? NUM_BIAS_WARPS : 0));
+            ptx::mbar_init(bars + 8u * (BAR_EMPTY + s), 1u + (!X3 && bias_on && !p.bias_mma ? NUM_BIAS_WARPS : 0));
+            // MODE 2, even CTA: both split warps of both CTAs
+            if constexpr (X3) ptx::mbar_init(bars + 8u * (L::BAR_CONV + s), 2u * NUM_BIAS_WARPS);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
@@ -377,8 +456,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (X3 && p.n_dw_items > 0) {  // the dweight product's maps of a paired fp32 launch
                 ptx::prefetch_tmap(&tm_weight_w);
                 ptx::prefetch_tmap(&tm_dout_mn_w);
-                ptx::prefetch_tmap(&tm_inp_w);
-                ptx::prefetch_tmap(&tm_dinp_rmw);
             }
             ptx::prefetch_tmap(&tm_dinp_out);
             ptx::prefetch_tmap(&tm_dw_out);
@@ -402,13 +479,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const bool direct = X3 || (!(it.is_dw && p.splits > 1) && !FWD);  // forward: nothing to read back
                 const int64_t out_rows = it.is_dw ? p.OC : p.BT;
                 const int pf_kb = max(it.kb0, it.kb1 - 8);
-                // A of a bf16 dweight item: MN-major 64-row boxes; every other A
-                // (fp32 items of either product too): one K-major 128-row tile
-                int na;
-                if (it.is_dw && !X3) na = (row0 < p.OC ? 1 : 0) + (row0 + 64 < p.OC ? 1 : 0);
-                else na = row0 < out_rows ? 1 : 0;
-                const uint32_t bytes = static_cast<uint32_t>(
-                    ((it.is_dw && !X3 ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES) * (X3 ? 2 : 1));
+                // A of a bf16 dweight item, or an MN-major fp32 A: 64-row boxes
+                // (8 KB either way); every other A: one K-major 128-row tile
+                const int sh = it.is_dw ? 2 : 0;
+                const bool a_mn = X3 ? ((p.x3_mn >> sh) & 1) != 0 : it.is_dw != 0;
+                const bool b_mn = X3 && ((p.x3_mn >> (sh + 1)) & 1) != 0;
+                const int na = a_mn ? (row0 < out_rows ? 1 : 0) + (row0 + 64 < out_rows ? 1 : 0)
+                                    : (row0 < out_rows ? 1 : 0);
+                const uint32_t bytes = static_cast<uint32_t>((a_mn ? na * BOX_BYTES : na * A_BYTES) + nb * BOX_BYTES);
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!wt.wait(bars + 8u * (BAR_EMPTY + stage), phase ^ 1u, SITE_PRODUCER_EMPTY, w)) {
                         ok = false;
@@ -429,19 +507,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                         it.n_tile * it.bn + j * 128, row0);
                     }
                     if (X3) {
-                        // A hi, A lo (maps 0 and 2), then B hi, B lo (maps 1 and 3);
-                        // the dweight product of a paired launch: maps 6, 8, 7, 9
-                        const void* ah = it.is_dw ? static_cast<const void*>(&tm_weight_w) : &tm_dout_k;
-                        const void* al = it.is_dw ? static_cast<const void*>(&tm_inp_w) : &tm_dout_mn;
-                        const void* bh = it.is_dw ? static_cast<const void*>(&tm_dout_mn_w) : &tm_weight;
-                        const void* bl = it.is_dw ? static_cast<const void*>(&tm_dinp_rmw) : &tm_inp;
-                        if (na) {
-                            ptx::tma_load_2d(sA, ah, fb, kb * KBLK, row0);
-                            ptx::tma_load_2d(sA + A_BYTES, al, fb, kb * KBLK, row0);
+                        // Raw fp32: a K-major operand into its high plane, an
+                        // MN-major one (64-wide boxes of 32 K rows) into its low
+                        // plane, which the split warps read before writing it.
+                        // Maps: A and B of dinp-type items 0 and 1, of the
+                        // dweight items of a paired launch 6 and 7.
+                        const void* ta = it.is_dw ? static_cast<const void*>(&tm_weight_w) : &tm_dout_k;
+                        const void* tb = it.is_dw ? static_cast<const void*>(&tm_dout_mn_w) : &tm_weight;
+                        if (a_mn) {
+                            for (int j = 0; j < na; ++j)
+                                ptx::tma_load_2d(sA + A_BYTES + j * BOX_BYTES, ta, fb, row0 + j * 64, kb * KBLK);
+                        } else if (na) {
+                            ptx::tma_load_2d(sA, ta, fb, kb * KBLK, row0);
                         }
                         for (int j = 0; j < nb; ++j) {
-                            ptx::tma_load_2d(sB + j * BOX_BYTES, bh, fb, kb * KBLK, col0 + j * 64);
-                            ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, bl, fb, kb * KBLK, col0 + j * 64);
+                            if (b_mn)
+                                ptx::tma_load_2d(sB + B_BYTES + j * BOX_BYTES, tb, fb, col0 + j * 64, kb * KBLK);
+                            else
+                                ptx::tma_load_2d(sB + j * BOX_BYTES, tb, fb, kb * KBLK, col0 + j * 64);
                         }
                     } else if (it.is_dw) {
                         if (na == 2 && (p.wide_maps & TC_WIDE_DOUT_MN))
@@ -516,8 +599,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                                     /*B MN*/ FWD ? 0 : 1);
                     for (int kb = it.kb0; kb < it.kb1; ++kb) {
                         // Both CTAs' copies of this stage have landed (own bytes +
-                        // the odd CTA's forwarded arrival).
-                        if (!wt.wait(bars + 8u * (BAR_FULL + stage), phase, SITE_MMA_FULL, w)) {
+                        // the odd CTA's forwarded arrival); MODE 2: both CTAs'
+                        // split warps have written the planes.
+                        const bool ready =
+                            X3 ? wt.wait<true>(bars + 8u * (L::BAR_CONV + stage), phase, SITE_MMA_CONV, w)
+                               : wt.wait(bars + 8u * (BAR_FULL + stage), phase, SITE_MMA_FULL, w);
+                        if (!ready) {
                             ok = false;
                             break;
                         }
@@ -604,7 +691,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         } else {
             // ---------------------------------------------- forwarder (odd CTA)
-            if (lane == 0) {
+            // (MODE 2: the split warps signal the even CTA themselves)
+            if (lane == 0 && !X3) {
                 const uint32_t leader_full = ptx::mapa(bars + 8u * BAR_FULL, 0);
                 uint32_t stage = 0, phase = 0;
                 bool ok = true;
@@ -628,79 +716,145 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         __syncwarp();
     } else if (warp < WARP_EPI) {
-        // ------------------------------------------------------------ bias warps
-        // They read every stage (releasing it), sum the dout tiles of dweight
-        // items of the first column tile, and store their 64 column sums
-        // themselves: to dbias, rounded once, or as this split's fp32 partial
-        // (the split reduction adds them in split order). They share no
-        // buffer with the epilogue, so they never wait for it.
-        if (bias_on && !p.bias_mma) {
-            const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
+        if constexpr (X3) {
+            // ------------------------------------------------------ split warps
+            // Warp 2 splits operand A of every stage, warp 3 operand B, each
+            // into its K-major high and low planes (x3_split_k / x3_split_mn),
+            // each on its own, then a proxy fence (the planes are read by the
+            // tensor cores of both CTAs) and one arrival on the even CTA's
+            // barrier of the stage. The fence completes only once the warp's
+            // shared-memory writes are visible to the async proxy, and the
+            // arrival is issued after it, so it is relaxed, as the forwarder's
+            // is for TMA data: a releasing arrival at cluster scope also waits
+            // for the SM's unrelated memory traffic in flight and cost this
+            // path a third of its time (XL fc 662 -> 980 us). On the items of
+            // column tile 0 whose A arrives MN-major (the dweight product: A =
+            // dout^T), warp 2 also sums A's rows over all of K: dbias.
+            const bool is_a = warp == WARP_BIAS;
+            const uint32_t conv0 = ptx::mapa(bars + 8u * L::BAR_CONV, 0);
             uint32_t stage = 0, phase = 0;
             for (int r = 0;; ++r) {
                 const int w = item_at(p, sch, r);
                 if (w >= p.n_items) break;
                 const Item it = decode_item(p, w);
-                const bool has_bias = it.is_dw && it.n_tile == 0;
-                float s[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] = 0.f;
+                const int sh = (it.is_dw ? 2 : 0) + (is_a ? 0 : 1);
+                const bool mn = ((p.x3_mn >> sh) & 1) != 0;
+                const int64_t a_rows = it.is_dw ? p.OC : p.BT;
+                const int row0 = it.pm * TC_PAIR_BM + static_cast<int>(rank) * TC_BM;
+                const int half = it.bn / 2;
+                const int col0 = it.n_tile * it.bn + static_cast<int>(rank) * half;
+                // this CTA's boxes of the operand holding any row of the tensor
+                int nbox = 0;
+                if (is_a) {
+                    nbox = mn ? (row0 < a_rows ? 1 : 0) + (row0 + 64 < a_rows ? 1 : 0) : (row0 < a_rows ? 1 : 0);
+                } else {
+                    for (int j = 0; j < half / 64; ++j) nbox += (col0 + j * 64 < p.n_dinp) ? 1 : 0;
+                }
+                const bool sums = is_a && mn && p.x3_dbias != nullptr && it.n_tile == 0;
+                float bsum[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t plane = base + (is_a ? 0u : 2u * A_BYTES);  // high plane; the low one follows
+                const uint32_t plane_bytes = is_a ? A_BYTES : B_BYTES;
                 bool ok = true;
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
-                    if (!wt.wait_warp(bars + 8u * (BAR_FULL + stage), phase, SITE_BIAS_FULL, w)) {
+                    if (!wt.wait_warp(bars + 8u * (BAR_FULL + stage), phase, SITE_CONV_RAW, w)) {
                         ok = false;
                         break;
                     }
-                    if (has_bias) {
-                        // A tile of dweight: 64 BT rows x 64 OC columns per box, each
-                        // row 128 bytes with its 16-byte chunks swizzled by (row & 7).
-                        const uint8_t* box = smem + stage * STG_BYTES + bw * BOX_BYTES;
-                        const int chunk = lane & 7;
-#pragma unroll
-                        for (int j = 0; j < TC_BK / 4; ++j) {
-                            const int row = (lane >> 3) + 4 * j;
-                            const uint4 v = *reinterpret_cast<const uint4*>(
-                                box + row * ROW_BYTES + ((chunk ^ (row & 7)) << 4));
-                            s[0] += bf_lo(v.x);
-                            s[1] += bf_hi(v.x);
-                            s[2] += bf_lo(v.y);
-                            s[3] += bf_hi(v.y);
-                            s[4] += bf_lo(v.z);
-                            s[5] += bf_hi(v.z);
-                            s[6] += bf_lo(v.w);
-                            s[7] += bf_hi(v.w);
-                        }
-                    }
+                    const uint32_t hi = plane + stage * STG_BYTES, lo = hi + plane_bytes;
+                    if (mn) x3_split_mn(hi, lo, nbox, lane, sums, bsum);
+                    else if (nbox) x3_split_k(hi, lo, is_a ? A_BYTES / 16 : nbox * (BOX_BYTES / 16), lane);
+                    ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
+                    if (lane == 0) ptx::mbar_arrive_cluster_relaxed(conv0 + 8u * stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (has_bias) {
+                if (sums) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
-                        s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
+                    for (int q = 0; q < 4; ++q) {
+                        const int64_t o = static_cast<int64_t>(row0) + 32 * q + lane;
+                        if (q / 2 < nbox && o < a_rows) p.x3_dbias[o] = bsum[q];
                     }
-                    if (lane < 8) {
-                        const int m_tile = it.pm * 2 + static_cast<int>(rank);  // 128-row tile of dweight
-                        const int row0 = bw * 64 + lane * 8;                    // first of this lane's 8 rows
-                        if (p.splits > 1) {
-                            float* bp = p.bias_partials + (static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + row0;
-                            *reinterpret_cast<float4*>(bp) = make_float4(s[0], s[1], s[2], s[3]);
-                            *reinterpret_cast<float4*>(bp + 4) = make_float4(s[4], s[5], s[6], s[7]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int64_t o = static_cast<int64_t>(m_tile) * TC_BM + row0 + e;
-                                if (o < p.OC) {
-                                    if constexpr (SR)
-                                        p.dbias[o] = sr::round(s[e], p.sr_seed, sr::DBIAS, o);
-                                    else
-                                        p.dbias[o] = __float2bfloat16_rn(s[e]);
+                }
+            }
+        } else {
+            // ------------------------------------------------------- bias warps
+            // They read every stage (releasing it), sum the dout tiles of dweight
+            // items of the first column tile, and store their 64 column sums
+            // themselves: to dbias, rounded once, or as this split's fp32 partial
+            // (the split reduction adds them in split order). They share no
+            // buffer with the epilogue, so they never wait for it.
+            if (bias_on && !p.bias_mma) {
+                const int bw = warp - WARP_BIAS;  // which 64-wide box of the A tile
+                uint32_t stage = 0, phase = 0;
+                for (int r = 0;; ++r) {
+                    const int w = item_at(p, sch, r);
+                    if (w >= p.n_items) break;
+                    const Item it = decode_item(p, w);
+                    const bool has_bias = it.is_dw && it.n_tile == 0;
+                    float s[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) s[e] = 0.f;
+                    bool ok = true;
+                    for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                        if (!wt.wait_warp(bars + 8u * (BAR_FULL + stage), phase, SITE_BIAS_FULL, w)) {
+                            ok = false;
+                            break;
+                        }
+                        if (has_bias) {
+                            // A tile of dweight: 64 BT rows x 64 OC columns per box, each
+                            // row 128 bytes with its 16-byte chunks swizzled by (row & 7).
+                            const uint8_t* box = smem + stage * STG_BYTES + bw * BOX_BYTES;
+                            const int chunk = lane & 7;
+    #pragma unroll
+                            for (int j = 0; j < TC_BK / 4; ++j) {
+                                const int row = (lane >> 3) + 4 * j;
+                                const uint4 v = *reinterpret_cast<const uint4*>(
+                                    box + row * ROW_BYTES + ((chunk ^ (row & 7)) << 4));
+                                s[0] += bf_lo(v.x);
+                                s[1] += bf_hi(v.x);
+                                s[2] += bf_lo(v.y);
+                                s[3] += bf_hi(v.y);
+                                s[4] += bf_lo(v.z);
+                                s[5] += bf_hi(v.z);
+                                s[6] += bf_lo(v.w);
+                                s[7] += bf_hi(v.w);
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bars + 8u * (BAR_EMPTY + stage));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (has_bias) {
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
+                            s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
+                        }
+                        if (lane < 8) {
+                            const int m_tile = it.pm * 2 + static_cast<int>(rank);  // 128-row tile of dweight
+                            const int row0 = bw * 64 + lane * 8;                    // first of this lane's 8 rows
+                            if (p.splits > 1) {
+                                float* bp = p.bias_partials + (static_cast<size_t>(m_tile) * p.splits + it.split) * TC_BM + row0;
+                                *reinterpret_cast<float4*>(bp) = make_float4(s[0], s[1], s[2], s[3]);
+                                *reinterpret_cast<float4*>(bp + 4) = make_float4(s[4], s[5], s[6], s[7]);
+                            } else {
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int64_t o = static_cast<int64_t>(m_tile) * TC_BM + row0 + e;
+                                    if (o < p.OC) {
+                                        if constexpr (SR)
+                                            p.dbias[o] = sr::round(s[e], p.sr_seed, sr::DBIAS, o);
+                                        else
+                                            p.dbias[o] = __float2bfloat16_rn(s[e]);
+                                    }
                                 }
                             }
                         }
@@ -1106,14 +1260,16 @@ struct ItemCost {
 };
 
 // fp32 from three tf32 products, both products in one launch: a k-block of
-// 32 fp32 of K with three pair MMAs takes about 0.88 us at width 256 and 0.55
-// at 128; with a correction accumulator a 256-wide tile fills all 512
-// tensor-memory columns, so its fp32 epilogue is not overlapped (about 1 us
-// left exposed once its loads are pipelined). Fitted, through this planner's
-// own longest-first schedule, to the paired launches of the GPT-2 XL fc and
-// qkv layers at both widths (GEMM part 581, 648, 473, 452 us measured; 581,
-// 642, 474, 459 modelled).
-double x3_item_us(int kb, int bn, bool corr) { return kb * (bn == 256 ? 0.88 : 0.55) + (bn == 256 && corr ? 1.0 : 0.0); }
+// 32 fp32 of K with three pair MMAs, its operands split in shared memory by
+// the kernel, takes about 0.99 us at width 256 and 0.87 at 128 (the split of
+// the A operand, the same at either width, and the stage ring's round trip
+// keep a 128-wide k-block from halving); with a correction accumulator a
+// 256-wide tile fills all 512 tensor-memory columns, so its fp32 epilogue is
+// not overlapped (about 2 us exposed). Fitted, through this planner's own
+// longest-first schedule, to the paired launches of the GPT-2 XL fc and qkv
+// layers at both widths (658, 1031, 540, 722 us measured; 660, 1019, 540, 729
+// modelled with 3 us per launch).
+double x3_item_us(int kb, int bn, bool corr) { return kb * (bn == 256 ? 0.99 : 0.87) + (bn == 256 && corr ? 2.0 : 0.0); }
 
 ItemCost item_cost(const TcPlan& pl, int w) {
     if (pl.x3) {
@@ -1317,10 +1473,11 @@ TcPlan tc_make_plan_forward(int64_t BT, int64_t C, int64_t OC, int num_sms) {
 // One fp32 product D (M x N) += A (M x K) . B (N x K)^T from tf32 halves: one
 // pair per cluster, k-blocks of 32, the tile width (128 or 256) with the lower
 // modelled time; items are equal in cost, so a round-robin assignment is
-// balanced. Model (us, measured on the GPT-2 XL layers): a k-block of three
-// pair MMAs takes about 0.75 us at width 256 and 0.42 at 128; with a separate
+// balanced. Model (us, measured on the GPT-2 XL forward: 311 us at width 256,
+// 429 at 128): a k-block of three pair MMAs with its operands split in shared
+// memory takes about 1.0 us at width 256 and 0.8 at 128; with a separate
 // correction accumulator (K > TC_X3_CORR_K) a 256-wide tile fills all 512
-// tensor-memory columns, so its fp32 epilogue (about 4 us) is not overlapped.
+// tensor-memory columns, so its fp32 epilogue (about 2 us) is not overlapped.
 TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
     TcPlan pl{};
     pl.dinp_kb = ceil_div_i(K, TC_BK / 2);
@@ -1333,7 +1490,7 @@ TcPlan tc_make_plan_x3(int64_t M, int64_t N, int64_t K, int num_sms) {
         if (force && bn != force) continue;
         const int tiles = pl.dinp_tiles_m * ceil_div_i(N, bn);
         const int pairs = std::max(1, std::min(tiles, max_pairs));
-        const double item = pl.dinp_kb * (bn == 256 ? 0.75 : 0.42) + (bn == 256 && K > TC_X3_CORR_K ? 4.0 : 0.0);
+        const double item = pl.dinp_kb * (bn == 256 ? 1.0 : 0.8) + (bn == 256 && K > TC_X3_CORR_K ? 2.0 : 0.0);
         const double cost = std::ceil(static_cast<double>(tiles) / pairs) * item;
         if (cost < best) {
             best = cost;
@@ -1454,10 +1611,10 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
     }
     // fp32 partial tiles of a split reduction: [half tile][split][128][dw_bn]
     // as rows of dw_bn floats, stored in 32 x 32 boxes (128-byte swizzle).
-    // fp32 launches with the dweight product too: its A hi, B hi, A lo, B lo
-    // in maps 6 to 9 (the slots the bf16 modes use for other maps)
+    // fp32 launches with the dweight product too: its raw A and B in maps 6
+    // and 7 (slots the bf16 modes use for other maps)
     if (mode == 2 && pair_specs) {
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const MapSpec& m = pair_specs[i];
             const cuuint64_t dims[2] = {m.inner, m.outer};
             const cuuint64_t strides[1] = {m.pitch ? m.pitch : m.inner * 4};
@@ -1628,16 +1785,25 @@ TcPlan tc_make_plan_x3_pair(int64_t BT, int64_t C, int64_t OC, int num_sms) {
     return best_pl;
 }
 
-cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const float* a_lo, int64_t lda,
-                         const float* b_hi, const float* b_lo, int64_t ldb, int64_t M, int64_t N, int64_t K,
+namespace {
+// Raw fp32 operand of an M x K (or N x K) product side: K-major, 32 K values
+// by `rows` rows per box (128-byte swizzle, the high plane's layout), or
+// MN-major, 64 M (N) values by 32 K rows per box (plain rows, split in the
+// kernel). ld: elements between rows of the tensor.
+MapSpec x3_operand(const float* t, bool mn, uint64_t mn_extent, uint64_t k_extent, int64_t ld, uint32_t rows) {
+    const uint64_t pitch = static_cast<uint64_t>(ld) * 4;
+    if (mn) return MapSpec{t, mn_extent, k_extent, 64, TC_BK / 2, CU_TENSOR_MAP_SWIZZLE_NONE, pitch};
+    return MapSpec{t, k_extent, mn_extent, TC_BK / 2, rows, CU_TENSOR_MAP_SWIZZLE_128B, pitch};
+}
+}  // namespace
+
+cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* A, bool a_mn, int64_t lda, const float* B,
+                         bool b_mn, int64_t ldb, int64_t M, int64_t N, int64_t K, float* dbias_or_null,
                          cudaStream_t stream) {
     const uint64_t m = static_cast<uint64_t>(M), n = static_cast<uint64_t>(N), k = static_cast<uint64_t>(K);
-    const uint64_t pa = static_cast<uint64_t>(lda) * 4, pb = static_cast<uint64_t>(ldb) * 4;
+    const MapSpec a = x3_operand(A, a_mn, m, k, lda, TC_BM), b = x3_operand(B, b_mn, n, k, ldb, 64);
     const MapSpec specs[6] = {
-        {a_hi, k, m, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa},  // A hi, K-major (128 rows per box)
-        {b_hi, k, n, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb},     // B hi, K-major (64 rows per box)
-        {a_lo, k, m, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa},  // A lo
-        {b_lo, k, n, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb},     // B lo
+        a, b, a, b,                                                      // (maps 2 and 3 unused)
         {D, n, m, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},            // D, L2 prefetch of old values
         {D, n, m, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},            // (dweight slot, unused)
     };
@@ -1647,39 +1813,34 @@ cudaError_t tc_launch_x3(const TcPlan& plan, float* D, const float* a_hi, const 
     p.OC = K;
     p.n_dinp = N;
     p.x3_corr = K > TC_X3_CORR_K ? 1 : 0;
+    p.x3_mn = (a_mn ? 1 : 0) | (b_mn ? 2 : 0);
+    p.x3_dbias = a_mn ? dbias_or_null : nullptr;
     p.dinp = reinterpret_cast<__nv_bfloat16*>(D);
     return launch_common(plan, specs, p, 2, stream);
 }
 
-cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, const float* a1_hi, const float* a1_lo,
-                              int64_t lda1, const float* b1_hi, const float* b1_lo, int64_t ldb1, const float* a2_hi,
-                              const float* a2_lo, int64_t lda2, const float* b2_hi, const float* b2_lo, int64_t ldb2,
-                              int64_t BT, int64_t C, int64_t OC, cudaStream_t stream) {
+cudaError_t tc_launch_x3_pair(const TcPlan& plan, float* dinp, float* dweight, float* dbias, const float* dout,
+                              const float* inp, const float* weight, int64_t BT, int64_t C, int64_t OC,
+                              cudaStream_t stream) {
     const uint64_t bt = static_cast<uint64_t>(BT), c = static_cast<uint64_t>(C), oc = static_cast<uint64_t>(OC);
-    const uint64_t pa1 = static_cast<uint64_t>(lda1) * 4, pb1 = static_cast<uint64_t>(ldb1) * 4;
-    const uint64_t pa2 = static_cast<uint64_t>(lda2) * 4, pb2 = static_cast<uint64_t>(ldb2) * 4;
-    // dinp product (K = OC): maps 0 to 3; the outputs (L2 prefetch of old values): maps 4 and 5
+    // dinp product (K = OC): A = dout K-major, B = weight MN-major (maps 0 and
+    // 1); the outputs (L2 prefetch of old values): maps 4 and 5
+    const MapSpec a1 = x3_operand(dout, false, bt, oc, OC, TC_BM), b1 = x3_operand(weight, true, c, oc, C, 64);
     const MapSpec specs[6] = {
-        {a1_hi, oc, bt, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa1},
-        {b1_hi, oc, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb1},
-        {a1_lo, oc, bt, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa1},
-        {b1_lo, oc, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb1},
+        a1, b1, a1, b1,
         {dinp, c, bt, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},
         {dweight, c, oc, 128, TC_BM, CU_TENSOR_MAP_SWIZZLE_NONE, 0},
     };
-    // dweight product (K = BT): A hi, B hi, A lo, B lo
-    const MapSpec pair[4] = {
-        {a2_hi, bt, oc, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa2},
-        {b2_hi, bt, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb2},
-        {a2_lo, bt, oc, TC_BK / 2, TC_BM, CU_TENSOR_MAP_SWIZZLE_128B, pa2},
-        {b2_lo, bt, c, TC_BK / 2, 64, CU_TENSOR_MAP_SWIZZLE_128B, pb2},
-    };
+    // dweight product (K = BT): A = dout^T and B = inp, both MN-major
+    const MapSpec pair[2] = {x3_operand(dout, true, oc, bt, OC, TC_BM), x3_operand(inp, true, c, bt, C, 64)};
     TcParams p{};
     p.BT = BT;
     p.C = C;
     p.OC = OC;
     p.n_dinp = C;
     p.x3_corr = plan.x3_corr;
+    p.x3_mn = 2 | 4 | 8;
+    p.x3_dbias = dbias;
     p.dinp = reinterpret_cast<__nv_bfloat16*>(dinp);
     p.dweight = reinterpret_cast<__nv_bfloat16*>(dweight);
     return launch_common(plan, specs, p, 2, stream, pair);

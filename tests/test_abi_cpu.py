@@ -152,15 +152,16 @@ def test_tile_width_override(monkeypatch):
 
 
 def test_fp32_tensor_core_plans_pair_the_products(monkeypatch):
-    """The fp32 tensor-core backward runs both products in one launch (after the
-    pre-pass: three split launches and the dbias tile sum) where their
-    reductions agree on the correction accumulator, else one launch each."""
+    """The fp32 tensor-core backward runs both products (and dbias) in one
+    launch where their reductions agree on the correction accumulator, else one
+    launch each; the operands are split in the kernel, so nothing runs before."""
     monkeypatch.setenv("MMBWD_F32_PATH", "x3")
     paired = mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32, 152)
-    assert paired["path"] == 2 and paired["launches"] == 5 and paired["table"] == 1
+    assert paired["path"] == 2 and paired["launches"] == 1 and paired["table"] == 1
     assert paired["items"] == paired["dinp_tiles"] + paired["dweight_tiles"]
     split = mm.mmbwd_plan_info(1, 2560, 264, 512, mm.F32, 152)  # only B*T above the threshold
-    assert split["path"] == 2 and split["launches"] == 6
+    assert split["path"] == 2 and split["launches"] == 2
+    assert mm.mmbwd_workspace_bytes(4, 1024, 1600, 6400, mm.F32) == 0
 
 
 def test_workspace_size_formula():

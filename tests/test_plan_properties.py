@@ -54,20 +54,17 @@ def test_fp32_tensor_core_plans_are_consistent(monkeypatch):
         assert a["dweight_tiles"] == -(-OC // 256) * -(-C // a["tile_n_dweight"])
         assert a["items"] == a["dinp_tiles"] + a["dweight_tiles"]
         paired = (OC > CORR_K) == (BT > CORR_K) and a["items"] <= 3072
-        assert a["launches"] == (5 if paired else 6)
+        assert a["launches"] == (1 if paired else 2)
         if paired:
             assert a["tile_n_dinp"] == a["tile_n_dweight"] and a["table"] == 1
         seen.add(a["launches"])
-    assert seen == {5, 6}  # both kinds of plan occur among the shapes
+    assert seen == {1, 2}  # both kinds of plan occur among the shapes
 
 
-def test_fp32_workspace_holds_the_split_operands():
-    # dout's low part, dout^T / weight^T / inp^T high and low parts (rows of
-    # B*T padded to a multiple of 4), the per-32-row column sums of dout
-    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    for B, T, C, OC in [(4, 1024, 1600, 6400), (1, 301, 264, 136), (2, 777, 392, 520)]:
-        BT = B * T
-        ld = (BT + 3) // 4 * 4
-        want = a(BT * OC * 4) + 2 * a(OC * ld * 4) + 2 * a(C * OC * 4) + 2 * a(C * ld * 4) + a(-(-BT // 32) * OC * 4)
-        if mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 152)["path"] == 2:
-            assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.F32) == want
+def test_fp32_needs_no_workspace(monkeypatch):
+    # the tensor-core path splits the raw operands in shared memory and forms
+    # dbias in the same launch; the FMA kernel works in place
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    for B, T, C, OC in [(4, 1024, 1600, 6400), (1, 301, 264, 136), (2, 777, 392, 520), (8, 1024, 768, 3072)]:
+        assert mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 152)["path"] == 2
+        assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.F32) == 0

@@ -116,9 +116,9 @@ def test_without_bias_matches_mmbwd_run_and_leaves_dbias_alone(monkeypatch):
         assert torch.equal(got["dbias"], dbias0)
 
 
-# fp32 always takes the FMA kernel here. (2,300,264,392): mmbwd_run takes it
-# too, so the bits agree; (1,1024,512,256): mmbwd_run takes the three-tf32
-# path, so both are compared with the oracle (fp32 tolerance) instead.
+# fp32 takes mmbwd_run's path here (neither fp32 path uses scratch), so the
+# bits agree with mmbwd_run: (2,300,264,392) on the FMA kernel,
+# (1,1024,512,256) on the three-tf32 path; both against the oracle too.
 @pytest.mark.parametrize("shape", [(2, 300, 264, 392), (1, 1024, 512, 256)], ids=lambda s: "x".join(map(str, s)))
 def test_fp32_matches_the_oracle_on_two_calls_in_a_row(shape):
     import torch
@@ -126,7 +126,6 @@ def test_fp32_matches_the_oracle_on_two_calls_in_a_row(shape):
     B, T, C, OC = shape
     layer = synth.Layer("no_alloc_f32", B, T, C, OC, "f32", True, init_std=0.01, dout_std=1.0, layer=5)
     x = synth.make_inputs(layer, seed=13)
-    same_path = mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 0)["path"] == 0
     ref = {k: to_dev(v, "f32") for k, v in x.items()}
     got = {k: to_dev(v, "f32") for k, v in x.items()}
     orc = oracle.get("omp")
@@ -141,8 +140,7 @@ def test_fp32_matches_the_oracle_on_two_calls_in_a_row(shape):
             g = to_host(got[name], "f32")
             assert scaled_error(g, w) <= TOL["f32"], (call, name)
             assert scaled_error(to_host(ref[name], "f32"), w) <= TOL["f32"], (call, name)
-            if same_path:
-                assert np.array_equal(g, to_host(ref[name], "f32")), (call, name)
+            assert np.array_equal(g, to_host(ref[name], "f32")), (call, name)
         # the next call starts from this call's outputs (as the device buffers do)
         dinp_o = to_host(got["dinp"], "f32").astype(np.float32)
         dw_o = to_host(got["dweight"], "f32").astype(np.float32)
