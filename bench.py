@@ -453,6 +453,9 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "tc_mmbwd_kernel", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     # context: the timed region runs thousands of launches back to back
+                     # under the power cap, the regime of the sustained measurement
+                     "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
                      "launches": n_launch, "flops_per_launch": kernel_flops / n_launch,
                      "mean_launch_us": elapsed_s / n_launch * 1e6,
                      "timing": "CUDA events around the timed region on the launching stream; every "
