@@ -244,10 +244,14 @@ __global__ void __launch_bounds__(LN_THREADS, 1) ln_bwd_rows_kernel(const LnPara
     if (issuer)
         for (int j = 0; j < LN_STAGES - 1 && j < nj; ++j) issue(j);
 
+    // the row statistics one row ahead: the next row's load overlaps this row
+    float m_next = 0.f, sd_next = 0.f;
+    if (nj > 0) m_next = __ldg(p.mean + first), sd_next = __ldg(p.rstd + first);
     int par = 0;
     for (int j = 0; j < nj; ++j, par ^= 1) {
         const int64_t r = first + static_cast<int64_t>(j) * teams;
-        const float m = __ldg(p.mean + r), sd = __ldg(p.rstd + r);
+        const float m = m_next, sd = sd_next;
+        if (j + 1 < nj) m_next = __ldg(p.mean + r + teams), sd_next = __ldg(p.rstd + r + teams);
         // A wait that gives up is recorded (device status) and the row is
         // processed anyway, so that every warp still reaches every barrier.
         ln_wait(full0 + 8u * (j % LN_STAGES), static_cast<uint32_t>((j / LN_STAGES) & 1), abort, LN_SITE_FULL, r);
