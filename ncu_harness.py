@@ -122,13 +122,13 @@ CASES = {
     "ln_xl": {
         "title": "LayerNorm backward, GPT-2 XL width, bf16, B=8 T=1024 C=1600",
         "cmd": _case_bench("ln_xl"),
-        "kernel": "layernorm_bwd", "skip": 4, "count": 2, "labels": None, "units": None,
+        "kernel": "ln_bwd_rows|ln_bwd_params", "skip": 4, "count": 2, "labels": None, "units": None,
         "file": "layernorm_bwd_rows_kernel_ln_xl", "sources": ("layernorm_bwd.cu",),
     },
     "enc": {
         "title": "Encoder backward, GPT-2 small, bf16, B=8 T=1024 C=768, Zipf token ids",
         "cmd": _case_bench("enc_gpt2_small"),
-        "kernel": "enc_", "skip": 24, "count": 2, "labels": None, "units": None,
+        "kernel": "enc_window|enc_sort", "skip": 24, "count": 2, "labels": None, "units": None,
         "file": "enc_window_kernel_enc_gpt2_small", "sources": ("encoder_bwd.cu",),
     },
 }
