@@ -94,3 +94,52 @@ def test_graph_replay_equals_eager(monkeypatch):
         for k in OUTPUTS:
             assert torch.equal(t[k].view(torch.uint8), eager[k].view(torch.uint8)), k
     assert mm.mmbwd_device_status(reset=True)[0] == mm.OK
+
+
+def test_fp32_tensor_core_path_captures_without_a_workspace(monkeypatch):
+    """The fp32 tensor-core path splits its operands in shared memory, so it
+    needs no workspace: with the library's workspace released, the first call
+    of a shape may already be captured (a call that had to allocate would
+    return MMBWD_ERR_CAPTURE). The replays equal the same call run eagerly,
+    bit for bit; the forward likewise."""
+    import torch
+
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    B, T, C, OC = 1, 777, 392, 520
+    assert mm.mmbwd_plan_info(B, T, C, OC, mm.F32)["path"] == 2
+    assert mm.mmbwd_forward_path(B, T, C, OC, mm.F32) == 2
+    layer = synth.Layer("graph_f32", B, T, C, OC, "f32", True, init_std=0.01, dout_std=1.0, layer=3)
+    x = synth.make_inputs(layer, seed=21)
+    t = {k: to_dev(v, "f32") for k, v in x.items()}
+    t["out"] = torch.zeros(B * T * OC, dtype=torch.float32, device="cuda")
+    outs = ("dinp", "dweight", "dbias", "out")
+    init = {k: t[k].clone() for k in outs}
+
+    def calls(stream):
+        s = stream.cuda_stream
+        return [mm.mmbwd_run(t["dinp"], t["dweight"], t["dbias"], t["dout"], t["inp"], t["weight"], B, T, C, OC,
+                             mm.F32, s),
+                mm.mmbwd_forward(t["out"], t["inp"], t["weight"], t["dbias"], B, T, C, OC, mm.F32, s)]
+
+    assert mm.mmbwd_release() == mm.OK
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rcs = calls(s)
+    assert rcs == [mm.OK, mm.OK], [mm.strerror(rc) for rc in rcs]
+    torch.cuda.synchronize()
+    for k in outs:
+        t[k].copy_(init[k])
+    with torch.cuda.stream(s):
+        assert calls(s) == [mm.OK, mm.OK]
+    torch.cuda.synchronize()
+    eager = {k: t[k].clone() for k in outs}
+    for _ in range(2):
+        for k in outs:
+            t[k].copy_(init[k])
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in outs:
+            assert torch.equal(t[k].view(torch.uint8), eager[k].view(torch.uint8)), k
+    assert mm.mmbwd_device_status(reset=True)[0] == mm.OK
