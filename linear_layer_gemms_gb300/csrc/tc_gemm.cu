@@ -1304,16 +1304,17 @@ double assign_lpt(TcPlan& pl, int pairs) {
     static thread_local int cnt[TC_MAX_PAIRS];
     static thread_local uint16_t owner[TC_MAX_SCHED_ITEMS];
     static thread_local int order[TC_MAX_SCHED_ITEMS];
+    static thread_local ItemCost cost[TC_MAX_SCHED_ITEMS];
     const int n = pl.n_items;
-    for (int w = 0; w < n; ++w) order[w] = w;
-    std::stable_sort(order, order + n, [&](int a, int b) { return item_cost(pl, a).run > item_cost(pl, b).run; });
+    for (int w = 0; w < n; ++w) order[w] = w, cost[w] = item_cost(pl, w);
+    std::stable_sort(order, order + n, [&](int a, int b) { return cost[a].run > cost[b].run; });
     for (int c = 0; c < pairs; ++c) load[c] = last_epi[c] = 0.0, cnt[c] = 0;
     for (int k = 0; k < n; ++k) {
         const int w = order[k];
         int best = 0;
         for (int c = 1; c < pairs; ++c)
             if (load[c] < load[best] - 1e-9) best = c;
-        const ItemCost ic = item_cost(pl, w);
+        const ItemCost ic = cost[w];
         load[best] += ic.run;
         last_epi[best] = ic.epi;
         owner[k] = static_cast<uint16_t>(best);
@@ -1390,8 +1391,10 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, boo
 
     // Overrides (tuning, tests): a forced split count that would leave an
     // empty split is lowered to the nearest count that does not; a forced grid
-    // is rounded down to whole pairs; MMBWD_TILE_N = "<dinp>,<dweight>" widths.
+    // is rounded down to whole pairs; MMBWD_TILE_N = "<dinp>,<dweight>" widths;
+    // MMBWD_SPLIT_KB = k-blocks per split (the last split takes the rest).
     const long force_splits = env_long("MMBWD_SPLITK", 0);
+    const long force_split_kb = env_long("MMBWD_SPLIT_KB", 0);
     const long force_grid = env_long("MMBWD_GRID", 0);
     int force_dinp_bn = 0, force_dw_bn = 0;
     if (const char* t = std::getenv("MMBWD_TILE_N")) {
@@ -1402,6 +1405,27 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, boo
         }
     }
     const int max_splits = with_dw ? std::max(1, std::min(pl.dw_kb, 16)) : 1;
+    // Split lengths tried: dw_kb / x k-blocks (rounded up), the last split
+    // taking what is left, for x = 1 .. max_splits (equal splits) and, up to
+    // eight splits, x in quarter steps: longer splits with a short last one,
+    // which shorten the longest items and leave the short ones to fill pairs
+    // that hold dinp items (GPT-2 small qkv: 103 + 25 k-blocks, 46.3 -> 44.8 us
+    // against two equal splits; every uneven split of the attention
+    // projection measured slower than its three equal ones).
+    static thread_local int kps_list[64];
+    int n_kps = 0;
+    auto add_kps = [&](int kps) {
+        kps = std::max(1, kps);
+        for (int i = 0; i < n_kps; ++i)
+            if (kps_list[i] == kps) return;
+        if (n_kps < 64) kps_list[n_kps++] = kps;
+    };
+    if (force_split_kb > 0) {
+        add_kps(static_cast<int>(std::min<long>(force_split_kb, pl.dw_kb)));
+    } else {
+        for (int x = 1; x <= max_splits; ++x) add_kps(ceil_div_i(pl.dw_kb, x));
+        for (int q = 5; q <= 4 * std::min(max_splits, 8); ++q) add_kps((4 * pl.dw_kb + q - 1) / q);
+    }
     double best = 1e300;
     static thread_local TcPlan best_pl, c;
     const int max_pairs = std::max(1, std::min(num_sms / 2, TC_MAX_PAIRS));
@@ -1409,20 +1433,17 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, boo
         if (force_dinp_bn && dinp_bn != force_dinp_bn) continue;
         for (int dw_bn = 256; dw_bn >= 128; dw_bn -= 128) {
             if (force_dw_bn && dw_bn != force_dw_bn) continue;
-            int prev_S = 0;
-            for (int s_try = 1; s_try <= max_splits; ++s_try) {
-                const int kps = ceil_div_i(pl.dw_kb, s_try);
+            for (int ki = 0; ki < n_kps; ++ki) {
+                const int kps = kps_list[ki];
                 const int S = ceil_div_i(pl.dw_kb, kps);  // every split non-empty
-                if (S == prev_S) continue;
-                prev_S = S;
                 // the partial tiles' rows are addressed by a 32-bit TMA coordinate
                 if (S > 1 && static_cast<int64_t>(2 * ceil_div_i(OC, TC_PAIR_BM)) * ceil_div_i(C, dw_bn) * S * TC_BM >
                                  INT32_MAX)
                     continue;
-                if (force_splits > 0 &&
-                    S != ceil_div_i(pl.dw_kb,
-                                    ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)))))
-                    continue;
+                if (force_splits > 0) {  // equal splits of the forced count
+                    const int fk = ceil_div_i(pl.dw_kb, static_cast<int>(std::min<long>(force_splits, max_splits)));
+                    if (kps != fk) continue;
+                }
                 c = pl;
                 c.dinp_tiles_m = ceil_div_i(BT, TC_PAIR_BM);
                 c.dw_tiles_m = ceil_div_i(OC, TC_PAIR_BM);
@@ -1439,6 +1460,23 @@ static TcPlan make_plan_impl(int64_t BT, int64_t C, int64_t OC, int num_sms, boo
                 if (force_grid > 0) pairs = static_cast<int>(std::max<long>(1, std::min<long>(force_grid / 2, pairs)));
                 c.grid = 2 * pairs;
                 c.table = (pairs <= TC_MAX_PAIRS && c.n_items <= TC_MAX_SCHED_ITEMS) ? 1 : 0;
+                // No schedule beats the work per pair or the longest item: skip
+                // the candidate when that bound is no better than the best so far.
+                {
+                    double work = 0.0, longest = 0.0;
+                    if (c.n_dinp_items > 0) {
+                        const ItemCost d = item_cost(c, c.n_dw_items);
+                        work += d.run * c.n_dinp_items;
+                        longest = d.run;
+                    }
+                    const int tiles = c.n_dw_items / std::max(1, S);
+                    for (int sp = 0; sp < S && tiles > 0; ++sp) {
+                        const ItemCost d = item_cost(c, sp * tiles);
+                        work += d.run * tiles;
+                        longest = std::max(longest, d.run);
+                    }
+                    if (std::max(work / pairs, longest) + fixup_cost(c, C, OC) >= best - 1e-9) continue;
+                }
                 const double cost = (c.table ? assign_lpt(c, pairs) : roundrobin_cost(c, pairs)) + fixup_cost(c, C, OC);
                 c.est_us = cost;
                 if (cost < best - 1e-9) {
