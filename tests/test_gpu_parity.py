@@ -122,6 +122,29 @@ def test_split_reduction_and_schedule(monkeypatch, splits):
             assert np.array_equal(o[k], outs[0][k]), k
 
 
+@pytest.mark.parametrize("split_kb", [7, 12])
+def test_uneven_split_lengths(monkeypatch, split_kb):
+    """Splits of a forced length with a shorter last one (16 k-blocks of B*T:
+    7 + 7 + 2, or 12 + 4): within tolerance of the oracle, dbias included, and
+    bitwise independent of the grid."""
+    B, T, C, OC = 1, 1000, 264, 392
+    _, x = make(B, T, C, OC, "bf16", dout_std=1e-2)
+    monkeypatch.setenv("MMBWD_SPLIT_KB", str(split_kb))
+    kb = -(-B * T // 64)
+    outs = []
+    for grid in (0, 6):
+        if grid:
+            monkeypatch.setenv("MMBWD_GRID", str(grid))
+        else:
+            monkeypatch.delenv("MMBWD_GRID", raising=False)
+        info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        assert info["kb_per_split"] == split_kb and info["splits"] == -(-kb // split_kb)
+        g, _ = check_full(x, B, T, C, OC, "bf16")
+        outs.append({k: to_host(g[k], "bf16") for k in ("dinp", "dweight", "dbias")})
+    for k in outs[0]:
+        assert np.array_equal(outs[1][k], outs[0][k]), k
+
+
 def test_split_counts_across_launches(monkeypatch):
     """Split launches of different shapes and split counts, with unsplit
     launches between them, sharing the workspace's partial tiles: each gives
