@@ -317,7 +317,7 @@ def write_summary(name, spec, sha, lcmd, mcmd, per_kernel, total, caps, dt_l, dt
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("cases", nargs="*")
-    ap.add_argument("--raw-dir", default=os.path.join(ROOT, "gpurun_out", "ncu"))
+    ap.add_argument("--raw-dir", default=os.path.join(ROOT, "ncu_raw"))
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "profiles"))
     ap.add_argument("--max-launches", type=int, default=400)
     ap.add_argument("--list", action="store_true")
