@@ -370,6 +370,9 @@ __global__ void __launch_bounds__(LN_PARAM_WARPS * 32)
     const int per = (grid + LN_PARAM_WARPS - 1) / LN_PARAM_WARPS;
     const int g0 = warp * per, g1 = g0 + per < grid ? g0 + per : grid;
     ln_grid_wait();  // the partials of the rows kernel
+    // the old value, requested beside the partials rather than after their sum
+    float old = 0.f;
+    if (warp == 0 && i < 2 * C) old = i < C ? E::load1(dweight, i) : E::load1(dbias, i - C);
     float acc = 0.f;
     if (i < 2 * C) {
 #pragma unroll 8
@@ -381,9 +384,9 @@ __global__ void __launch_bounds__(LN_PARAM_WARPS * 32)
         float sum = red[0][lane];
         for (int w = 1; w < LN_PARAM_WARPS; ++w) sum += red[w][lane];
         if (i < C)
-            E::store1(dweight, i, E::load1(dweight, i) + sum);
+            E::store1(dweight, i, old + sum);
         else
-            E::store1(dbias, i - C, E::load1(dbias, i - C) + sum);
+            E::store1(dbias, i - C, old + sum);
     }
 }
 
