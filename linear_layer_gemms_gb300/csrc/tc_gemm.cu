@@ -1185,6 +1185,8 @@ __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) 
         const int n_tile = static_cast<int>(col / p.dw_bn), cl = static_cast<int>(col % p.dw_bn);
         const float* pp = p.partials + static_cast<size_t>(m_tile * p.dw_tiles_n + n_tile) * p.splits * tile_elems +
                           static_cast<size_t>(rl) * p.dw_bn + cl;
+        uint4* dst = reinterpret_cast<uint4*>(p.dweight + row * p.C + col);
+        const uint4 old = *dst;  // requested beside the partials, not after their sum
         float s8[8];
 #pragma unroll 4
         for (int sp = 0; sp < p.splits; ++sp) {
@@ -1194,12 +1196,11 @@ __global__ void __launch_bounds__(256) tc_splitk_fixup_kernel(const TcParams p) 
 #pragma unroll
             for (int e = 0; e < 8; ++e) s8[e] = (sp == 0) ? f[e] : s8[e] + f[e];
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.dweight + row * p.C + col);
         if (p.sr) {
             const uint64_t e0 = static_cast<uint64_t>(row * p.C + col);
-            *dst = add_sr8(*dst, s8, sr::word(p.sr_seed, sr::DWEIGHT, e0), sr::word(p.sr_seed, sr::DWEIGHT, e0 + 4));
+            *dst = add_sr8(old, s8, sr::word(p.sr_seed, sr::DWEIGHT, e0), sr::word(p.sr_seed, sr::DWEIGHT, e0 + 4));
         } else {
-            *dst = add_round8(*dst, s8);
+            *dst = add_round8(old, s8);
         }
     }
     if (p.dbias) {
