@@ -68,3 +68,17 @@ def test_fp32_needs_no_workspace(monkeypatch):
     for B, T, C, OC in [(4, 1024, 1600, 6400), (1, 301, 264, 136), (2, 777, 392, 520), (8, 1024, 768, 3072)]:
         assert mm.mmbwd_plan_info(B, T, C, OC, mm.F32, 152)["path"] == 2
         assert mm.mmbwd_workspace_bytes(B, T, C, OC, mm.F32) == 0
+
+
+def test_forced_split_length(monkeypatch):
+    # MMBWD_SPLIT_KB fixes the k-blocks per split; the last split takes the rest
+    B, T, C, OC = 8, 1024, 768, 768  # 128 k-blocks of B*T
+    for kps in (20, 43, 64, 100, 128):
+        monkeypatch.setenv("MMBWD_SPLIT_KB", str(kps))
+        a = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 152)
+        assert a["kb_per_split"] == kps and a["splits"] == -(-128 // kps)
+        assert (a["launches"] == 2) == (a["splits"] > 1)
+    monkeypatch.delenv("MMBWD_SPLIT_KB")
+    # the planner's own choice for GPT-2 small qkv: a long split and a short one
+    a = mm.mmbwd_plan_info(8, 1024, 768, 2304, mm.BF16, 152)
+    assert a["splits"] == 2 and a["kb_per_split"] > 64
