@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const Item it = decode_item(p, w);
                     const bool has_bias = it.is_dw && it.n_tile == 0;
                     float s[8];
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 8; ++e) s[e] = 0.f;
                     bool ok = true;
                     for (int kb = it.kb0; kb < it.kb1; ++kb) {
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             // row 128 bytes with its 16-byte chunks swizzled by (row & 7).
                             const uint8_t* box = smem + stage * STG_BYTES + bw * BOX_BYTES;
                             const int chunk = lane & 7;
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < TC_BK / 4; ++j) {
                                 const int row = (lane >> 3) + 4 * j;
                                 const uint4 v = *reinterpret_cast<const uint4*>(
@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (!ok) break;
                     if (has_bias) {
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             s[e] += __shfl_xor_sync(0xffffffffu, s[e], 8);
                             s[e] += __shfl_xor_sync(0xffffffffu, s[e], 16);
@@ -846,7 +846,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 *reinterpret_cast<float4*>(bp) = make_float4(s[0], s[1], s[2], s[3]);
                                 *reinterpret_cast<float4*>(bp + 4) = make_float4(s[4], s[5], s[6], s[7]);
                             } else {
-    #pragma unroll
+#pragma unroll
                                 for (int e = 0; e < 8; ++e) {
                                     const int64_t o = static_cast<int64_t>(m_tile) * TC_BM + row0 + e;
                                     if (o < p.OC) {

@@ -1,9 +1,11 @@
-"""The fp32 path on the tensor cores (three tf32 products per K step from
-split operands) through the C ABI against the oracle, element by element:
-ragged sizes (K not a multiple of the 32-deep k-block, rows not a multiple of
-the 256-row tile or of 4, one tile, many tiles), with and without dbias,
-run-to-run bitwise determinism, and the choice between it and the fp32 FMA
-kernel."""
+"""The fp32 path on the tensor cores (three tf32 products per K step, the
+operands split in shared memory by the kernel) through the C ABI against the
+oracle, element by element: ragged sizes (K not a multiple of the 32-deep
+k-block, rows not a multiple of the 256-row tile or of 4, one tile, many
+tiles, 64-wide boxes partly outside the tensor), with and without dbias, a
+seeded sweep of ragged shapes through both the paired and the two-launch
+forms and the forward, run-to-run bitwise determinism, and the choice between
+it and the fp32 FMA kernel."""
 import numpy as np
 import pytest
 
@@ -97,3 +99,41 @@ def test_path_choice(monkeypatch):
     assert mm.mmbwd_plan_info(1, 512, 260, 512, mm.F32)["path"] == 0
     monkeypatch.setenv("MMBWD_F32_PATH", "ffma")
     assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 0
+
+
+def _sweep(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        BT = int(rng.integers(1, 3200))
+        C = 8 * int(rng.integers(1, 140))
+        OC = 4 * int(rng.integers(1, 700))
+        out.append((BT, C, OC))
+    return out
+
+
+@pytest.mark.parametrize("shape", _sweep(16, 7), ids=lambda s: "x".join(map(str, s)))
+def test_x3_ragged_sweep(shape, monkeypatch):
+    """Seeded ragged shapes (either reduction above or below the correction
+    threshold, so both launch forms occur), forced onto the tensor-core path:
+    dinp, dweight and dbias against the oracle, then the forward of the same
+    layer against the oracle's forward."""
+    monkeypatch.setenv("MMBWD_F32_PATH", "x3")
+    BT, C, OC = shape
+    assert mm.mmbwd_plan_info(1, BT, C, OC, mm.F32)["path"] == 2
+    x = inputs(BT, C, OC, seed=BT + C + OC)
+    g = run_gpu(x, 1, BT, C, OC, "f32")
+    orc = oracle.get("omp")
+    ref = orc.matmul_backward(x["dout"], x["inp"], x["weight"], "f32", x["dinp"], x["dweight"])
+    assert_close(to_host(g["dinp"], "f32"), ref[0], "f32", "dinp")
+    assert_close(to_host(g["dweight"], "f32"), ref[1], "f32", "dweight")
+    assert_close(to_host(g["dbias"], "f32"), ref[2], "f32", "dbias")
+    if mm.mmbwd_forward_path(1, BT, C, OC, mm.F32) == 2:
+        import torch
+
+        out = torch.empty(BT * OC, dtype=torch.float32, device="cuda")
+        bias = torch.from_numpy(x["dbias"].astype(np.float32)).cuda()
+        assert mm.mmbwd_forward(out, g["inp"], g["weight"], bias, 1, BT, C, OC, mm.F32) == mm.OK
+        torch.cuda.synchronize()
+        want = orc.forward_rows(x["inp"], x["weight"], "f32", bias=x["dbias"])
+        assert_close(out.cpu().numpy().astype(np.float64).reshape(BT, OC), want, "f32", "forward")
