@@ -423,6 +423,10 @@ def run_gpu(args):
         per_layer[layer.name] = {"us": round(sec * 1e6, 2), "tflops": round(layer.flops() / sec / 1e12, 1),
                                  "timed": "back-to-back calls of this layer alone"}
 
+    # context only: the same step through PyTorch's cuBLAS calls (dinp and
+    # dweight by addmm with beta = 1, dbias by a column sum), on the same sets
+    library = library_context(torch, wl, sets, stream, flops_step, value)
+
     # end to end through host buffers
     e2e = None
     if not args.no_e2e:
@@ -465,6 +469,7 @@ def run_gpu(args):
         "plans": {l.name: mm.mmbwd_plan_info(l.B, l.T, l.C, l.OC, mm.BF16, 0) for l in wl.layers},
         "clocks": clocks,
         "e2e": e2e,
+        "library_context": library,
         "cpu_baseline": cpu,
         "other_configs": other,
     }
@@ -495,6 +500,27 @@ FORWARD_CONFIGS = (("forward_mlp_fc", "mlp:0"), ("forward_mlp_fc_proj", "mlp:1")
 
 
 L2_BYTES = 129 * 1024 * 1024
+
+
+def library_context(torch, wl, sets, stream, flops_step, value):
+    """The benchmark's step through PyTorch (cuBLAS GEMMs, a reduction kernel
+    for dbias) on the same device-resident sets: context beside the library's
+    number, not part of it."""
+    def step(ts):
+        for layer, t in zip(wl.layers, ts):
+            dout = t["dout"].view(layer.BT, layer.OC)
+            inp = t["inp"].view(layer.BT, layer.C)
+            t["dinp"].view(layer.BT, layer.C).addmm_(dout, t["weight"].view(layer.OC, layer.C))
+            t["dweight"].view(layer.OC, layer.C).addmm_(dout.t(), inp)
+            if layer.bias:
+                torch.sum(dout, 0, out=t["dbias"].view(layer.OC))
+    try:
+        sec = time_back_to_back(torch, stream, [lambda ts=ts: step(ts) for ts in sets], 30, 5)
+    except RuntimeError as e:  # a PyTorch without these kernels for the type
+        return {"unavailable": str(e).splitlines()[0]}
+    tf = flops_step / sec / 1e12
+    return {"impl": "torch addmm (cuBLAS) + torch.sum", "tflops": round(tf, 1), "ms_per_step": round(sec * 1e3, 4),
+            "library_over_torch": round(value / tf, 3), "timed": "back-to-back steps over the rotating sets"}
 
 
 def time_back_to_back(torch, stream, calls, per_batch, batches=5):
