@@ -729,6 +729,16 @@ def measure_other_configs(torch, mm, dev, stream, only=None, batches=5, verify=T
         info = mm.mmbwd_plan_info(layer.B, layer.T, layer.C, layer.OC, dt, 0)
         finish(name, layer, layer.flops(), sec, n_sets, set_bytes,
                {k: info[k] for k in ("path", "grid", "items", "splits", "launches")}, alg_bytes=layer_alg_bytes(layer))
+        if layer.dtype == "bf16" and not sr and name not in dbias_mma:
+            # context only: the same backward through PyTorch's cuBLAS calls
+            def torch_step(t, layer=layer):
+                dout = t["dout"].view(layer.BT, layer.OC)
+                t["dinp"].view(layer.BT, layer.C).addmm_(dout, t["weight"].view(layer.OC, layer.C))
+                t["dweight"].view(layer.OC, layer.C).addmm_(dout.t(), t["inp"].view(layer.BT, layer.C))
+                if layer.bias:
+                    torch.sum(dout, 0, out=t["dbias"].view(layer.OC))
+            tsec = time_back_to_back(torch, stream, [lambda t=t: torch_step(t) for t in sets], per_batch, batches)
+            out[name]["torch_cublas_us"] = round(tsec * 1e6, 2)
         if sr:
             out[name]["rounding"] = "stochastic (mmbwd_run_sr, new seed per call)"
         del sets, calls
