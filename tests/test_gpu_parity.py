@@ -145,6 +145,20 @@ def test_uneven_split_lengths(monkeypatch, split_kb):
         assert np.array_equal(outs[1][k], outs[0][k]), k
 
 
+def test_round_robin_schedule_of_many_items():
+    """More items than the per-pair table holds (here 3516 dinp tiles and 16
+    splits of 3 dweight tiles, 293 k-blocks each): the round-robin schedule,
+    every element against the oracle and bitwise repeatable."""
+    B, T, C, OC = 1, 300000, 520, 136
+    info = mm.mmbwd_plan_info(B, T, C, OC, mm.BF16, 0)
+    assert info["table"] == 0 and info["items"] > 3072 and info["splits"] > 1
+    _, x = make(B, T, C, OC, "bf16", dout_std=1e-2)
+    g, _ = check_full(x, B, T, C, OC, "bf16")
+    again = run_gpu(x, B, T, C, OC, "bf16")
+    for k in ("dinp", "dweight", "dbias"):
+        assert np.array_equal(to_host(g[k], "bf16"), to_host(again[k], "bf16")), k
+
+
 def test_split_counts_across_launches(monkeypatch):
     """Split launches of different shapes and split counts, with unsplit
     launches between them, sharing the workspace's partial tiles: each gives
