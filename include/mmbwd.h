@@ -18,9 +18,9 @@
  *   MMBWD_BF16: bf16 storage, products accumulated in fp32, each output element
  *               rounded once to bf16 (round-to-nearest-even) after the old value
  *               (converted to fp32) and the fp32 sum are added.
- *   MMBWD_F32:  fp32 storage and fp32-accurate products. Problems large enough
- *               to fill the GPU (B*T, C, OC >= 256, C a multiple of 8), with both
- *               reduction lengths (OC and B*T) at most 8192, run on the tensor
+ *   MMBWD_F32:  fp32 storage and fp32-accurate products. Shapes with C a
+ *               multiple of 8 and both reduction lengths (OC and B*T) at most
+ *               8192 run on the tensor
  *               cores: the kernel splits each staged operand, in shared memory,
  *               into its tf32 value and the exact fp32 remainder (no copy in
  *               device memory, no workspace), and each product is formed from three tf32
@@ -202,8 +202,8 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
  *
  * bf16: fp32 accumulation on the tensor cores, out rounded once (RNE) after
  * adding the bias in fp32. fp32: as for mmbwd_run, three tf32 products on the
- * tensor cores for large layers (OC a multiple of 8, C at most 8192; out is set
- * to the bias, then the product is added), FFMA otherwise. Same alignment, aliasing (out
+ * tensor cores where OC is a multiple of 8 and C at most 8192 (out is set to the
+ * bias, then the product is added), FFMA otherwise. Same alignment, aliasing (out
  * must not overlap an input), status codes, asynchrony and determinism as
  * mmbwd_run; no workspace. C == 0 gives out = bias (or 0).
  */
@@ -249,8 +249,8 @@ void mmbwd_debug_fail_next_launch(int n);
  * advance. Nothing in the buffer has to start at zero: every value a call
  * reads there is written earlier by the same call.
  *
- * fp32: the path mmbwd_run takes (three tf32 products on the tensor cores for
- * large layers, the fused-multiply-add kernel otherwise), so the results are
+ * fp32: the path mmbwd_run takes (three tf32 products on the tensor cores
+ * where the shape allows, the fused-multiply-add kernel otherwise), so the results are
  * those of mmbwd_run; neither path uses any scratch.
  *
  * All calls on a device share the one buffer, which keeps whatever the last

@@ -91,8 +91,9 @@ def test_x3_deterministic(monkeypatch):
 
 def test_path_choice(monkeypatch):
     monkeypatch.delenv("MMBWD_F32_PATH", raising=False)
-    # the tiny check stays on the FMA kernel; the XL fp32 layers use the tensor cores
-    assert mm.mmbwd_plan_info(2, 64, 64, 192, mm.F32)["path"] == 0
+    # every shape the tensor-core path takes uses it, from the tiny check to the
+    # XL fp32 layers
+    assert mm.mmbwd_plan_info(2, 64, 64, 192, mm.F32)["path"] == 2
     assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 2
     # shapes the split layout cannot take fall back: C not a multiple of 8
     monkeypatch.setenv("MMBWD_F32_PATH", "x3")
