@@ -18,9 +18,9 @@
  *   MMBWD_BF16: bf16 storage, products accumulated in fp32, each output element
  *               rounded once to bf16 (round-to-nearest-even) after the old value
  *               (converted to fp32) and the fp32 sum are added.
- *   MMBWD_F32:  fp32 storage and fp32-accurate products. Shapes with C a
- *               multiple of 8 and both reduction lengths (OC and B*T) at most
- *               8192 run on the tensor
+ *   MMBWD_F32:  fp32 storage and fp32-accurate products. Shapes whose two
+ *               reduction lengths (OC and B*T) are at most 8192 run on the
+ *               tensor
  *               cores: the kernel splits each staged operand, in shared memory,
  *               into its tf32 value and the exact fp32 remainder (no copy in
  *               device memory, no workspace), and each product is formed from three tf32
@@ -202,7 +202,7 @@ int mmbwd_selftest_wait_timeout(uint64_t timeout_ns);
  *
  * bf16: fp32 accumulation on the tensor cores, out rounded once (RNE) after
  * adding the bias in fp32. fp32: as for mmbwd_run, three tf32 products on the
- * tensor cores where OC is a multiple of 8 and C at most 8192 (out is set to the
+ * tensor cores where C is at most 8192 (out is set to the
  * bias, then the product is added), FFMA otherwise. Same alignment, aliasing (out
  * must not overlap an input), status codes, asynchrony and determinism as
  * mmbwd_run; no workspace. C == 0 gives out = bias (or 0).

@@ -25,8 +25,8 @@
 namespace mmbwd {
 
 bool x3_shape_ok(int64_t BT, int64_t C, int64_t OC) {
-    // rows of 16-byte multiples for the tensor maps, 8-column epilogue groups
-    return BT > 0 && C > 0 && OC > 0 && C % 8 == 0 && OC % 4 == 0;
+    // rows of 16-byte multiples for the tensor maps and the epilogue's 4-column vectors
+    return BT > 0 && C > 0 && OC > 0 && C % 4 == 0 && OC % 4 == 0;
 }
 
 cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* dout, const float* inp,
@@ -49,7 +49,7 @@ cudaError_t x3_launch(float* dinp, float* dweight, float* dbias, const float* do
 // The forward out = inp . weight^T + bias on the same path: out is first set
 // to the bias (or zero) and the product is then added to it.
 bool x3_forward_shape_ok(int64_t BT, int64_t C, int64_t OC) {
-    return BT > 0 && C > 0 && OC > 0 && OC % 8 == 0 && C % 4 == 0;
+    return BT > 0 && C > 0 && OC > 0 && OC % 4 == 0 && C % 4 == 0;
 }
 
 cudaError_t x3_forward_launch(float* out, const float* inp, const float* weight, const float* bias, int64_t BT,

@@ -932,10 +932,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     A[i] = Bv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (rok[i] && cc * 32 + cg < ncols) {
+                    if (rok[i] && cc * 32 + cg < ncols) {  // (the row width is a multiple of 4)
                         const float4* dp = reinterpret_cast<const float4*>(drowf[i] + cc * 32);
                         A[i] = dp[0];
-                        Bv[i] = dp[1];
+                        if (cc * 32 + cg + 4 < ncols) Bv[i] = dp[1];
                     }
                 }
             };
@@ -1118,7 +1118,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                             o0.x += a4.x, o0.y += a4.y, o0.z += a4.z, o0.w += a4.w;
                             o1.x += b4.x, o1.y += b4.y, o1.z += b4.z, o1.w += b4.w;
                             dp[0] = o0;
-                            dp[1] = o1;
+                            if (c * 32 + cg + 4 < ncols) dp[1] = o1;
                         }
                     }
                     __syncwarp();

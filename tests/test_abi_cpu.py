@@ -111,15 +111,16 @@ def test_plan_is_a_pure_function_of_shape():
         ws = mm.mmbwd_workspace_bytes(B, T, C, OC, mm.BF16)
         assert (ws > 0) == (a["splits"] > 1)
     # fp32: three tf32 products on the tensor cores (two products, 256-row
-    # tiles, k-blocks of 32) for every shape they take, the tiny check included;
-    # the FMA kernel for C not a multiple of 8
+    # tiles, k-blocks of 32) for every shape they take, the tiny check and rows
+    # of 4 (mod 8) floats included; the FMA kernel for longer reductions
     f = mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32, 152)
     assert f["path"] == 2 and f["tile_m"] == 256 and f["tile_k"] == 32 and f["grid"] % 2 == 0
     assert f["dinp_tiles"] == -(-4096 // 256) * -(-1600 // f["tile_n_dinp"])
     assert f["dweight_tiles"] == -(-6400 // 256) * -(-1600 // f["tile_n_dweight"])
     assert f["items"] == f["dinp_tiles"] + f["dweight_tiles"]
     assert mm.mmbwd_plan_info(2, 64, 64, 192, mm.F32, 152)["path"] == 2
-    assert mm.mmbwd_plan_info(2, 64, 68, 192, mm.F32, 152)["path"] == 0
+    assert mm.mmbwd_plan_info(2, 64, 68, 196, mm.F32, 152)["path"] == 2
+    assert mm.mmbwd_plan_info(1, 64, 68, 8196, mm.F32, 152)["path"] == 0
 
 
 def test_split_override_from_environment(monkeypatch):

@@ -40,7 +40,7 @@ def inputs(BT, C, OC, seed=0):
 # correction accumulator); only the dweight reduction above 2048 (the
 # products in two launches).
 SHAPES = [(64, 8, 4), (301, 264, 136), (513, 520, 1028), (256, 128, 256), (2048, 768, 768), (2304, 264, 2304),
-          (2560, 264, 512)]
+          (2560, 264, 512), (301, 260, 132), (777, 132, 516)]
 
 
 @pytest.mark.parametrize("bias", [True, False])
@@ -95,9 +95,11 @@ def test_path_choice(monkeypatch):
     # XL fp32 layers
     assert mm.mmbwd_plan_info(2, 64, 64, 192, mm.F32)["path"] == 2
     assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 2
-    # shapes the split layout cannot take fall back: C not a multiple of 8
+    # rows of 4 (mod 8) floats stay on the tensor cores; a reduction longer
+    # than 8192 falls back to the FMA kernel, even when forced
+    assert mm.mmbwd_plan_info(1, 512, 260, 516, mm.F32)["path"] == 2
     monkeypatch.setenv("MMBWD_F32_PATH", "x3")
-    assert mm.mmbwd_plan_info(1, 512, 260, 512, mm.F32)["path"] == 0
+    assert mm.mmbwd_plan_info(1, 512, 260, 8196, mm.F32)["path"] == 0
     monkeypatch.setenv("MMBWD_F32_PATH", "ffma")
     assert mm.mmbwd_plan_info(4, 1024, 1600, 6400, mm.F32)["path"] == 0
 
@@ -107,7 +109,7 @@ def _sweep(n, seed):
     out = []
     for _ in range(n):
         BT = int(rng.integers(1, 3200))
-        C = 8 * int(rng.integers(1, 140))
+        C = 4 * int(rng.integers(1, 280))
         OC = 4 * int(rng.integers(1, 700))
         out.append((BT, C, OC))
     return out
