@@ -23,6 +23,11 @@ FLOPs = 4*B*T*C*OC + B*T*OC (the bias sum) per layer.
   layer alone (back-to-back calls) is reported beside it.
 * windows: the K steps cut into up to five windows (events between steps
   only), min / median / max TFLOP/s over them.
+* queued start: after the synchronize that opens a timed region, a device
+  spin (torch's `_sleep` kernel) holds the stream while the host enqueues the
+  timed launches, so the first window measures the device running queued
+  work and not the host's latency to its first launch; whether the spin was
+  still running when the last launch was queued is reported.
 * cpu_baseline / --impl reference: the C oracle (OpenMP build, all host
   cores) on a bounded row sample of the same workload; the single-threaded
   build on a smaller sample beside it.
@@ -55,6 +60,7 @@ METRIC = "matmul_backward TFLOP/s at GPT-2 shapes; % of GB300 dense bf16 peak"
 UNIT = "TFLOP/s"
 N_SETS = 3
 N_WINDOWS = 5  # the timed steps are cut into this many windows (events between steps only)
+SPIN_CYCLES_PER_US = 2070  # the GB300's maximum SM clock in MHz: a spin of us * this cycles lasts >= us
 
 
 def parse_args(argv=None):
@@ -362,9 +368,11 @@ def run_gpu(args):
 
     # warm-up (also grows the workspace outside the timed region)
     with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
         for k in range(args.warmup):
             for layer, t in zip(wl.layers, sets[k % N_SETS]):
                 call(layer, t)
+        host_us_step = (time.perf_counter() - t0) * 1e6 / max(1, args.warmup)
     torch.cuda.synchronize()
     status, info = mm.mmbwd_device_status(reset=True)
     if status != mm.OK:
@@ -379,9 +387,11 @@ def run_gpu(args):
         sampler.start()
     barrier()
     torch.cuda.synchronize()
-    # Events only between steps (at window edges): an event between two
-    # launches would keep the second launch's prologue from overlapping the
-    # first kernel.
+    # The spin holds the stream while the host queues the K steps (twice the
+    # warm-up's host time per step); events only between steps (at window
+    # edges): an event between two launches would keep the second launch's
+    # prologue from overlapping the first kernel.
+    held = hold_stream(torch, stream, min(2e5, 50.0 + 2.0 * host_us_step * K))
     with torch.cuda.stream(stream):
         ev[0].record(stream)
         for w in range(n_win):
@@ -390,6 +400,7 @@ def run_gpu(args):
                 for li, layer in enumerate(wl.layers):
                     call(layer, tset[li])
             ev[w + 1].record(stream)
+    queued = not held.query()
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop() if sampler else None
@@ -404,7 +415,8 @@ def run_gpu(args):
     win_tf = sorted(flops_step * (bounds[w + 1] - bounds[w]) / (ev[w].elapsed_time(ev[w + 1]) / 1e3) / 1e12
                     for w in range(n_win) if bounds[w + 1] > bounds[w])
     windows = {"n": len(win_tf), "steps_each": [bounds[w + 1] - bounds[w] for w in range(n_win)],
-               "tflops_min": win_tf[0], "tflops_median": statistics.median(win_tf), "tflops_max": win_tf[-1]}
+               "tflops_min": win_tf[0], "tflops_median": statistics.median(win_tf), "tflops_max": win_tf[-1],
+               "queued_before_start": queued, "host_us_per_step": round(host_us_step, 1)}
 
     # roofline of the tensor-core kernel: the timed step launches only this
     # kernel, one launch per layer, so its mean launch time is this rank's
@@ -523,23 +535,46 @@ def library_context(torch, wl, sets, stream, flops_step, value):
             "library_over_torch": round(value / tf, 3), "timed": "back-to-back steps over the rotating sets"}
 
 
+def hold_stream(torch, stream, us):
+    """Queue on `stream` a device spin of at least `us` microseconds and return
+    an event recorded behind it. Launches enqueued next wait behind the spin,
+    so a timed window that starts after it starts with its work queued; the
+    event not yet complete once the last launch is queued shows that held."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * SPIN_CYCLES_PER_US))
+        e = torch.cuda.Event()
+        e.record(stream)
+    return e
+
+
 def time_back_to_back(torch, stream, calls, per_batch, batches=5):
     """Median over `batches` of (time of `per_batch` back-to-back calls) /
     per_batch, CUDA events on `stream`; the calls cycle through `calls` (one
-    per resident input set) so that consecutive calls touch different memory."""
+    per resident input set) so that consecutive calls touch different memory.
+    Each batch is queued behind a device spin (`hold_stream`), lengthened and
+    the batch taken again if the spin ended before the batch was queued."""
     with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
         for c in calls * 2:
             c()
+        host_us = (time.perf_counter() - t0) * 1e6 / (2 * len(calls))
     torch.cuda.synchronize()
+    hold_us = 50.0 + 2.0 * host_us * per_batch
     times = []
     for _ in range(batches):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for k in range(per_batch):
-                calls[k % len(calls)]()
-            b.record(stream)
-        b.synchronize()
+        while True:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            held = hold_stream(torch, stream, hold_us)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for k in range(per_batch):
+                    calls[k % len(calls)]()
+                b.record(stream)
+            queued = not held.query()
+            b.synchronize()
+            if queued or hold_us > 1e5:
+                break
+            hold_us *= 2
         times.append(a.elapsed_time(b) / 1e3 / per_batch)
     return statistics.median(times)
 

@@ -63,3 +63,63 @@ def test_traffic_is_null_for_a_changed_kernel(tmp_path, monkeypatch):
     if os.path.exists(prof):
         t = bench.profiled_traffic()
         assert t is None or t > 0
+
+
+class _FakeEvent:
+    """Stands in for torch.cuda.Event: elapsed time is fixed; `query` says
+    whether the spin in front of it has ended, by a script of answers."""
+
+    def __init__(self, log, answers=None, **kw):
+        self.log, self.answers = log, answers
+
+    def record(self, stream=None):
+        self.log.append("record")
+
+    def query(self):
+        return self.answers.pop(0)
+
+    def synchronize(self):
+        pass
+
+    def elapsed_time(self, other):
+        return 2.0  # ms
+
+
+class _FakeCuda:
+    def __init__(self, answers):
+        self.log, self.answers, self.spins = [], answers, []
+
+    def Event(self, **kw):
+        return _FakeEvent(self.log, self.answers)
+
+    def _sleep(self, cycles):
+        self.spins.append(cycles)
+        self.log.append("spin")
+
+    def stream(self, s):
+        import contextlib
+
+        return contextlib.nullcontext()
+
+    def synchronize(self):
+        pass
+
+
+class _FakeTorch:
+    def __init__(self, answers):
+        self.cuda = _FakeCuda(answers)
+
+
+def test_time_back_to_back_queues_each_batch_behind_a_spin():
+    # first batch: the spin ended before the batch was queued (query True), so
+    # the batch is taken again behind a spin twice as long; then it held
+    ft = _FakeTorch([True, False, False])
+    calls = []
+    sec = bench.time_back_to_back(ft, None, [lambda: calls.append(1)], per_batch=4, batches=2)
+    assert sec == 2.0e-3 / 4
+    assert len(ft.cuda.spins) == 3
+    assert abs(ft.cuda.spins[1] - 2 * ft.cuda.spins[0]) <= 2 and ft.cuda.spins[2] == ft.cuda.spins[1]
+    assert ft.cuda.spins[0] >= 50 * bench.SPIN_CYCLES_PER_US
+    assert len(calls) == 2 + 3 * 4  # warm-up (each call twice) and three queued batches
+    # every batch's first event comes after its spin's event
+    assert ft.cuda.log[-4:] == ["spin", "record", "record", "record"]
