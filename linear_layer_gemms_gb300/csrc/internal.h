@@ -23,7 +23,6 @@ constexpr int TC_BN = 256;       // widest tile (N of one MMA); each CTA stages 
 constexpr int TC_BK = 64;
 constexpr int TC_STAGES = 6;     // bf16 pipeline stages (32 KB each)
 constexpr int TC_STAGES_X3 = 3;  // fp32 three-product stages (64 KB each)
-constexpr int TC_THREADS = 256;
 
 // Wait sites reported in the device status word.
 enum WaitSite : int {

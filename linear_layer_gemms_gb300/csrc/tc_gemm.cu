@@ -76,8 +76,6 @@ constexpr int WARP_TMA = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_BIAS = 2;
 constexpr int WARP_EPI = 4;
-constexpr int NUM_EPI_WARPS = 4;
-constexpr int NUM_EPI_THREADS = 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * TC_BN;
 
 constexpr int STG_STRIDE = 36;  // floats per staged row: 16-byte aligned, conflict-free
@@ -104,8 +102,15 @@ struct Smem {
     static constexpr bool X3 = MODE == 2;
     static constexpr int STAGES = X3 ? TC_STAGES_X3 : TC_STAGES;
     static constexpr int STG_BYTES = X3 ? 2 * STAGE_BYTES : STAGE_BYTES;
-    static constexpr int OLD_SLOTS = 4;  // bf16 chunk buffers per epilogue warp
-    static constexpr int PART_SLOTS = X3 ? 1 : 2;  // fp32 partial chunk buffers (same memory)
+    // Epilogue warps: in the bf16 modes two per tensor-memory lane quadrant, each
+    // taking every other 32-column chunk of the quadrant's rows with two chunk
+    // buffers of its own; MODE 2 keeps one per quadrant (its staging rows fill
+    // the region of one warp of four).
+    static constexpr int EPI_WARPS = X3 ? 4 : 8;
+    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+    static constexpr int THREADS = 32 * WARP_EPI + EPI_THREADS;
+    static constexpr int OLD_SLOTS = X3 ? 4 : 2;  // bf16 chunk buffers per epilogue warp
+    static constexpr int PART_SLOTS = 1;  // fp32 partial chunk buffers (same memory)
     static constexpr int OFF_BARS = STAGES * STG_BYTES;
     static constexpr int BAR_FULL = 0;                   // [stages] TMA landed (even CTA: and the peer's too)
     static constexpr int BAR_EMPTY = STAGES;             // [stages] stage may be refilled
@@ -113,17 +118,19 @@ struct Smem {
     static constexpr int BAR_TEMPTY = 2 * STAGES + 2;    // [2] accumulator drained by both CTAs (even CTA)
     static constexpr int BAR_TEARDOWN = 2 * STAGES + 4;
     static constexpr int BAR_OLD = 2 * STAGES + 5;       // [epilogue warp][slot] old chunk landed
-    static constexpr int BAR_CONV = BAR_OLD + NUM_EPI_WARPS * OLD_SLOTS;  // MODE 2: [stages] split planes ready
+    static constexpr int BAR_CONV = BAR_OLD + EPI_WARPS * OLD_SLOTS;  // MODE 2: [stages] split planes ready
     static constexpr int N_BARS = BAR_CONV + (X3 ? STAGES : 0);
     static constexpr int OFF_MISC = OFF_BARS + N_BARS * 8;  // [0] tmem base, [1] abort flag
     static constexpr int OFF_STAGE = (OFF_MISC + 16 + 1023) & ~1023;
     static constexpr int OLD_WARP_BYTES = OLD_SLOTS * OLD_CHUNK_BYTES;
-    static constexpr int WARP_REGION = STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES;
+    static constexpr int WARP_REGION =
+        X3 ? (STG_WARP_BYTES > OLD_WARP_BYTES ? STG_WARP_BYTES : OLD_WARP_BYTES) : OLD_WARP_BYTES;
     // ones tile of the dbias-by-MMA variant: 8 rows (this CTA's half of N = 16)
     // of 64 bf16 ones, one 128-byte-swizzled 1 KB atom
-    static constexpr int OFF_ONES = OFF_STAGE + NUM_EPI_WARPS * WARP_REGION;
+    static constexpr int OFF_ONES = OFF_STAGE + EPI_WARPS * WARP_REGION;
     static constexpr int SMEM_TOTAL = OFF_ONES + 1024 + 1024;  // + slack for aligning the base
     static_assert(X3 || PART_SLOTS * PART_CHUNK_BYTES <= WARP_REGION, "partial chunks fit the warp region");
+    static_assert(EPI_WARPS % 4 == 0 && (!X3 || EPI_WARPS == 4), "whole quadrants; MODE 2 one warp each");
     static_assert(WARP_REGION % 1024 == 0, "chunk buffers stay 1024-byte aligned (128-byte swizzle)");
     static_assert(SMEM_TOTAL <= 227 * 1024, "shared memory budget");
 };
@@ -344,7 +351,7 @@ __device__ __forceinline__ void x3_split_mn(uint32_t hi, uint32_t lo, int nbox, 
 // (seeded; sr.cuh). Four instantiations, so that none pays for the
 // others' branches.
 template <int MODE>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(Smem<MODE>::THREADS, 1)
     tc_mmbwd_kernel(const __grid_constant__ CUtensorMap tm_dout_k,   // dout, A of dinp (K-major)
                     const __grid_constant__ CUtensorMap tm_weight,   // weight, B of dinp (MN-major)
                     const __grid_constant__ CUtensorMap tm_dout_mn,  // dout, A of dweight (MN-major)
@@ -411,10 +418,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bars + 8u * (BAR_TFULL + a), 1);
-            ptx::mbar_init(bars + 8u * (BAR_TEMPTY + a), 2 * NUM_EPI_WARPS);
+            ptx::mbar_init(bars + 8u * (BAR_TEMPTY + a), 2 * L::EPI_WARPS);
         }
         ptx::mbar_init(bars + 8u * BAR_TEARDOWN, 1);
-        for (int b = 0; b < NUM_EPI_WARPS * OLD_SLOTS; ++b) ptx::mbar_init(bars + 8u * (BAR_OLD + b), 1);
+        for (int b = 0; b < L::EPI_WARPS * OLD_SLOTS; ++b) ptx::mbar_init(bars + 8u * (BAR_OLD + b), 1);
         misc[1] = 0u;
         ptx::fence_mbar_init();
     }
@@ -865,13 +872,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;         // tensor-memory lane quadrant: tile rows 32q..32q+31
+        const int ew = warp - WARP_EPI;  // this warp's buffers and barriers
+        constexpr int NH = L::EPI_WARPS / 4;  // warps per quadrant: chunks h, h + NH, h + 2 NH, ...
+        const int h = ew / 4;
         const int r8 = lane >> 2;       // coalesced phase: rows 8i + r8 of the quadrant,
         const int cg = (lane & 3) * 8;  //   columns cg..cg+7 of each 32-column chunk
-        const uint32_t stg = base + L::OFF_STAGE + q * L::WARP_REGION;
+        const uint32_t stg = base + L::OFF_STAGE + ew * L::WARP_REGION;
         // bf16 read-modify-write (MODE 0 and 3, unsplit items): this warp's
         // ring of old-value chunks, their barriers, parities and pending loads
-        const uint32_t oldbuf = base + L::OFF_STAGE + q * L::WARP_REGION;
-        const uint32_t oldbar0 = bars + 8u * (BAR_OLD + q * OLD_SLOTS);
+        const uint32_t oldbuf = base + L::OFF_STAGE + ew * L::WARP_REGION;
+        const uint32_t oldbar0 = bars + 8u * (BAR_OLD + ew * OLD_SLOTS);
         uint32_t oldpar = 0, oldpend = 0;
         uint32_t fwd_chunks = 0;  // forward: chunks this warp has stored (slot = count mod OLD_SLOTS)
         const uint32_t leader_tempty = ptx::mapa(bars + 8u * BAR_TEMPTY, 0);
@@ -908,6 +918,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             constexpr bool TMA_FWD = FWD && !X3;  // the forward's stores through TMA as well
             const void* tmo = it.is_dw ? static_cast<const void*>(&tm_dw_rmw) : static_cast<const void*>(&tm_dinp_rmw);
             const int nvc = (ncols + 31) / 32;  // chunks holding columns of the tensor
+            const int nloc = nvc > h ? (nvc - h + NH - 1) / NH : 0;  // of them this warp's
+            const int nloc_all = (nchunks - h + NH - 1) / NH;       // this warp's of the tile
             const bool qvalid = qrow0 < rows_total;
             if constexpr (!FWD && !X3) {
                 // the previous item's stores have read the chunk buffers (also the
@@ -916,11 +928,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
             }
             if (tma_rmw && qvalid && lane == 0) {
-                for (int c = 0; c < OLD_SLOTS && c < nvc; ++c) {
-                    const uint32_t b = oldbar0 + 8u * c;
+                for (int k = 0; k < OLD_SLOTS && k < nloc; ++k) {
+                    const uint32_t b = oldbar0 + 8u * k;
                     ptx::mbar_arrive_expect_tx(b, OLD_CHUNK_BYTES);
-                    ptx::tma_load_2d(oldbuf + c * OLD_CHUNK_BYTES, tmo, b, col0 + c * 32, static_cast<int32_t>(qrow0));
-                    oldpend |= 1u << c;
+                    ptx::tma_load_2d(oldbuf + k * OLD_CHUNK_BYTES, tmo, b, col0 + (h + NH * k) * 32,
+                                     static_cast<int32_t>(qrow0));
+                    oldpend |= 1u << k;
                 }
             }
 
@@ -941,11 +954,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             };
             if constexpr (X3) x3_load_old(0, olda, oldb);
             bool ok = wt.wait_warp(bars + 8u * (BAR_TFULL + acc), acc_phase, SITE_EPI_TMEM_FULL, w);
-            if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
+            if (!ptx::named_bar_and(1, L::EPI_THREADS, ok)) break;
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * acc_cols;
             if constexpr (!FWD && !X3) {
-                if (p.bias_mma && it.is_dw && it.n_tile == 0 && qvalid) {
+                if (p.bias_mma && it.is_dw && it.n_tile == 0 && qvalid && h == 0) {
                     // dbias by MMA: every column of the sums block holds the row's sum
                     const float bsum = __uint_as_float(
                         ptx::tmem_ld1(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (acc ^ 1u) * TC_BN));
@@ -972,11 +985,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         ((static_cast<int64_t>(m_tile) * p.dw_tiles_n + it.n_tile) * p.splits + it.split) * TC_BM + q * 32);
                     const uint32_t swz = static_cast<uint32_t>(lane & 7);
 #pragma unroll 1
-                    for (int c = 0; c < nchunks; ++c) {
+                    for (int k = 0; k < nloc_all; ++k) {
+                        const int c = h + NH * k;
                         uint32_t v[32];
                         ptx::tmem_ld32(tbase + c * 32, v);
-                        const int slot = c & (L::PART_SLOTS - 1);
-                        if (c >= L::PART_SLOTS && lane == 0) ptx::bulk_wait_read_but_n<L::PART_SLOTS - 1>();
+                        const int slot = k & (L::PART_SLOTS - 1);
+                        if (k >= L::PART_SLOTS && lane == 0) ptx::bulk_wait_read_but_n<L::PART_SLOTS - 1>();
                         __syncwarp();
                         const uint32_t rowaddr = oldbuf + slot * PART_CHUNK_BYTES + lane * 128;
 #pragma unroll
@@ -998,10 +1012,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // (64-byte swizzle; conflict-free across each 8-thread phase)
                 const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
-                for (int c = 0; c < nvc; ++c) {
+                for (int k = 0; k < nloc; ++k) {
+                    const int c = h + NH * k;
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c * 32, v);
-                    const int slot = c & (OLD_SLOTS - 1);
+                    const int slot = k & (OLD_SLOTS - 1);
                     const uint32_t b = oldbar0 + 8u * slot;
                     if (!wt.wait_warp(b, (oldpar >> slot) & 1u, SITE_EPI_OLD, w)) {
                         ok = false;
@@ -1034,18 +1049,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (lane == 0) {
                         ptx::tma_store_2d(tmo, oldbuf + slot * OLD_CHUNK_BYTES, col0 + c * 32, static_cast<int32_t>(qrow0));
                         ptx::bulk_commit_group();
-                        // Refill the previous chunk's slot with chunk c + OLD_SLOTS - 1
-                        // once that chunk's store (committed an iteration ago) has
-                        // read it; this chunk's store stays in flight.
-                        const int cn = c + OLD_SLOTS - 1;
-                        if (c >= 1 && cn < nvc) {
-                            const int sn = cn & (OLD_SLOTS - 1);
-                            const uint32_t bn_ = oldbar0 + 8u * sn;
-                            ptx::bulk_wait_read_but_last();
-                            ptx::mbar_arrive_expect_tx(bn_, OLD_CHUNK_BYTES);
-                            ptx::tma_load_2d(oldbuf + sn * OLD_CHUNK_BYTES, tmo, bn_, col0 + cn * 32,
+                        // Refill this chunk's buffer with the warp's chunk OLD_SLOTS
+                        // ahead once this chunk's store has read it.
+                        const int kn = k + OLD_SLOTS;
+                        if (kn < nloc) {
+                            ptx::bulk_wait_read_all();
+                            ptx::mbar_arrive_expect_tx(b, OLD_CHUNK_BYTES);
+                            ptx::tma_load_2d(oldbuf + slot * OLD_CHUNK_BYTES, tmo, b, col0 + (h + NH * kn) * 32,
                                              static_cast<int32_t>(qrow0));
-                            oldpend |= 1u << sn;
+                            oldpend |= 1u << slot;
                         }
                     }
                     __syncwarp();
@@ -1057,7 +1069,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // used it OLD_SLOTS chunks ago has read it.
                 const uint32_t swz = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
-                for (int c = 0; c < nvc; ++c) {
+                for (int k = 0; k < nloc; ++k) {
+                    const int c = h + NH * k;
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c * 32, v);
                     const uint32_t slot = fwd_chunks & (OLD_SLOTS - 1);
@@ -1084,7 +1097,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     ++fwd_chunks;
                 }
             }
-            if (!ptx::named_bar_and(1, NUM_EPI_THREADS, ok)) break;
+            if (!ptx::named_bar_and(1, L::EPI_THREADS, ok)) break;
             if constexpr (X3) {  // MODE 2: fp32 read-modify-write through staging rows
 #pragma unroll 1
                 for (int c = 0; c < nchunks; ++c) {
@@ -1366,7 +1379,7 @@ int tc_max_active_clusters(int cluster_size) {
         return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster_size), 1, 1);
-    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.blockDim = dim3(Smem<0>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_TOTAL;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1695,7 +1708,7 @@ cudaError_t launch_common(const TcPlan& plan, const MapSpec (&specs)[6], TcParam
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
-    cfg.blockDim = dim3(TC_THREADS, 1, 1);
+    cfg.blockDim = dim3(mode == 2 ? Smem<2>::THREADS : Smem<0>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_TOTAL;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
