@@ -38,7 +38,6 @@ FLOPs = 4*B*T*C*OC + B*T*OC (the bias sum) per layer.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import statistics
@@ -214,11 +213,12 @@ def measured_peaks():
 
 
 def kernel_source_sha() -> str:
-    h = hashlib.sha1()
-    for f in ("tc_gemm.cu", "ptx.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "linear_layer_gemms_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:12]
+    """Hash of the tensor-core kernel's code (comments and white space ignored),
+    as the ncu harness writes it into its summaries."""
+    from ncu_harness import code_sha
+
+    return code_sha([os.path.join(ROOT, "linear_layer_gemms_gb300", "csrc", f)
+                     for f in ("tc_gemm.cu", "ptx.cuh", "internal.h")])
 
 
 def profiled_traffic():

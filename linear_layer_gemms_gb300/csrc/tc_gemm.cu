@@ -19,7 +19,7 @@
 // dweight is cut into `splits` items along its long BT reduction. Each pair
 // walks a static, shape-determined sequence of items.
 //
-// Warp roles (256 threads per CTA):
+// Warp roles (384 threads per CTA; 256 in MODE 2):
 //   warp 0      TMA producer (both CTAs): a 6-stage ring of (A 16 KB, B 16 KB)
 //               tiles in 128-byte-swizzled shared memory; completion lands on
 //               the CTA's own "full" barrier.
@@ -31,13 +31,14 @@
 //   warps 2-3   bias: on dweight items of the first column tile, sum the CTA's
 //               dout tile of every stage over its BT rows (the A operand already
 //               in shared memory) and reduce across lanes with shuffles.
-//   warps 4-7   epilogue (both CTAs): tcgen05.ld the accumulator (warp w reads
-//               tensor-memory lanes 32*(w%4)..+31, i.e. tile rows) in 32 x 32
-//               chunks that travel between global and shared memory by TMA, then
-//               either
+//   warps 4-11  epilogue (both CTAs; warps 4-7 in MODE 2): tcgen05.ld the
+//               accumulator (warp w reads tensor-memory lanes 32*(w%4)..+31, i.e.
+//               tile rows; the two warps of a lane quadrant take every other
+//               32-column chunk) in 32 x 32 chunks that travel between global and
+//               shared memory by TMA, then either
 //                 - read-modify-write the bf16 output: old + acc, one rounding
-//                   (dinp, and dweight when it is not split), old values
-//                   loaded up to four chunks ahead, or
+//                   (dinp, and dweight when it is not split), each warp's old
+//                   values loaded two of its chunks ahead, or
 //                 - store the fp32 partial tile of this split (dweight split
 //                   along BT); a second kernel then sums the partials of every
 //                   tile in split order 0..S-1 and does the read-modify-write, so
@@ -88,12 +89,13 @@ constexpr int PART_CHUNK_BYTES = 32 * 32 * 4;
 
 // Shared memory map (offsets from a 1024-byte aligned base), per kernel mode:
 // the TMA stage ring, the barriers, then one region per epilogue warp. The
-// bf16 modes keep six 32 KB stages and give each epilogue warp four chunk
-// buffers (8 KB): the first four chunks of old values are requested at the
-// start of an item, the rest just ahead of use. A sixth stage (a stage's round
-// trip is about 2 us, five covered it only just) is worth more than a whole
-// tile of old values in flight: with five stages and eight buffers a warp
-// every bf16 backward plan ran 1-4 % slower. MODE 2 keeps three 64 KB stages
+// bf16 modes keep six 32 KB stages and give each of their eight epilogue warps
+// two chunk buffers (4 KB): its first two chunks of old values are requested at
+// the start of an item, each later one as soon as the store of the chunk two
+// before has read its buffer. A sixth stage (a stage's round trip is about
+// 2 us, five covered it only just) is worth more than a whole tile of old values
+// in flight: with five stages and eight buffers a quadrant every bf16 backward
+// plan ran 1-4 % slower. MODE 2 keeps three 64 KB stages
 // and the fp32 staging rows, and a second barrier per stage: the raw fp32
 // operands land on the first (TMA), the split planes are signalled on the
 // second (the split warps of both CTAs, on the even CTA's copy).
@@ -909,11 +911,11 @@ __global__ void __launch_bounds__(Smem<MODE>::THREADS, 1)
                 drowf[i] = Df + (rok[i] ? row : 0) * n_extent + col0 + cg;
             }
             // The backward's bf16 read-modify-write goes through TMA: the old
-            // values of this warp's 32 rows arrive in 32-column chunks (all of a
-            // 256-wide tile requested at the start of the item, before waiting
-            // for the accumulator), each thread adds its own row in place, and
-            // the chunk goes back out with one bulk store. Rows and columns
-            // outside the tensor read as zero and are not stored.
+            // values of this warp's 32 rows arrive in 32-column chunks (its first
+            // two requested at the start of the item, before waiting for the
+            // accumulator), each thread adds its own row in place, and the chunk
+            // goes back out with one bulk store. Rows and columns outside the
+            // tensor read as zero and are not stored.
             const bool tma_rmw = !FWD && !X3 && !split_mode;
             constexpr bool TMA_FWD = FWD && !X3;  // the forward's stores through TMA as well
             const void* tmo = it.is_dw ? static_cast<const void*>(&tm_dw_rmw) : static_cast<const void*>(&tm_dinp_rmw);

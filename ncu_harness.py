@@ -134,12 +134,46 @@ CASES = {
 }
 
 
-def source_sha(files) -> str:
+def strip_comments(text: str) -> str:
+    """C/C++/CUDA source without its comments and with every run of white space
+    as one space: what the compiler reads, so that a summary stays matched to
+    its kernel across edits of comments or layout. String and character
+    literals are copied as they are."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_sha(paths) -> str:
+    """First 12 hex digits of the SHA-1 of the files' code (strip_comments), in order."""
     h = hashlib.sha1()
-    for f in files:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+    for path in paths:
+        with open(path) as fh:
+            h.update(strip_comments(fh.read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:12]
+
+
+def source_sha(files) -> str:
+    return code_sha([os.path.join(CSRC, f) for f in files])
 
 
 def _num(v: str) -> float | None:
@@ -264,7 +298,7 @@ def write_summary(name, spec, sha, lcmd, mcmd, per_kernel, total, caps, dt_l, dt
              "Written by `ncu_harness.py` (the case's command ran once without ncu and exited 0 first).", "",
              f"- case: `{name}`",
              f"- kernel_source_sha: `{sha}`",
-             f"- hashed sources: {', '.join(spec['sources'])}"]
+             f"- hashed sources (code only: comments and white space are not hashed): {', '.join(spec['sources'])}"]
     if dram:
         lines.append(f"- dram_bytes_per_launch: `{sum(dram) / len(dram):.0f}`")
     lines += ["", "## Launch list (`gpu__time_duration.sum` alone: one pass, cold-cache and serialised)", "",

@@ -123,3 +123,23 @@ def test_time_back_to_back_queues_each_batch_behind_a_spin():
     assert len(calls) == 2 + 3 * 4  # warm-up (each call twice) and three queued batches
     # every batch's first event comes after its spin's event
     assert ft.cuda.log[-4:] == ["spin", "record", "record", "record"]
+
+
+def test_code_hash_ignores_comments_and_layout_only(tmp_path):
+    # the profiles' kernel_source_sha: edits of comments or white space keep it,
+    # any change of code (a string literal included) does not
+    import ncu_harness as H
+
+    def sha(name, text):
+        p = tmp_path / name
+        p.write_text(text)
+        return H.code_sha([p])
+
+    base = sha("a.cu", 'int f(int x) { return x + 1; }  // one\n/* two */\nconst char* s = "a // b";\n')
+    relaid = sha("b.cu", '// header\nint f(int x) {\n    return x + 1;   // other words\n}\n'
+                         '/* several\n   lines */ const char* s = "a // b";\n')
+    code = sha("c.cu", 'int f(int x) { return x + 2; }\nconst char* s = "a // b";\n')
+    literal = sha("d.cu", 'int f(int x) { return x + 1; }\nconst char* s = "a ";\n')
+    assert base == relaid
+    assert len({base, code, literal}) == 3
+    assert bench.kernel_source_sha() == H.source_sha(("tc_gemm.cu", "ptx.cuh", "internal.h"))
