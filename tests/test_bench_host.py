@@ -3,7 +3,6 @@ world size 2, CPU) and the workload accounting."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 import bench

@@ -13,7 +13,7 @@ import pytest
 import linear_layer_gemms_gb300 as mm
 import oracle
 import synth
-from gpu_helpers import TOL, scaled_error, to_dev, to_host
+from gpu_helpers import TOL, scaled_error, to_dev
 
 pytestmark = pytest.mark.gpu
 

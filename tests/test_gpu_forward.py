@@ -9,7 +9,7 @@ import pytest
 import linear_layer_gemms_gb300 as mm
 import oracle
 import synth
-from gpu_helpers import TOL, assert_close, to_dev, to_host
+from gpu_helpers import assert_close, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
